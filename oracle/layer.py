@@ -1,0 +1,269 @@
+"""CPU oracle for one pre-norm decoder-layer step over a mixed, paged batch.
+
+TEST INFRASTRUCTURE.  Only the test suite, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this module.  The library never
+does, and it shares no code with the CUDA path.
+
+What it computes is the plain definition of the layer.  The method this
+repository accelerates (nano-batching with overlapped execution) reaches exactly
+that result, because nano-batches share no data dependencies ("NanoFlow:
+Towards Optimal LLM Serving Throughput", "The Intra-Device Parallelism
+Mechanism").  So the oracle never splits the batch: it walks tokens in order.
+
+Arithmetic: float64 throughout.  bf16 inputs are converted exactly; nothing is
+rounded back to bf16 (not even the K/V it appends).
+
+Readings taken where the pages leave a step open (each is listed with its
+reason in the design notes):
+
+* layer structure: Llama pre-norm, no biases — x -> RMSNorm -> QKV -> RoPE ->
+  paged GQA attention -> O-proj + residual -> RMSNorm -> SwiGLU FFN + residual.
+  The pages give only the operation list (KQV, attention, O, Up/Gate/Down;
+  "NanoFlow: Towards Optimal LLM Serving Throughput", "The Intra-Device
+  Parallelism Mechanism"; "CSE 451 Lecture 25", slide 81 names RoPE).
+* RoPE: rotate-half pairing (i, i + d/2), angle pos * theta^(-2i/d).
+* ``seq_lens`` is the KV length after this step's tokens are appended.
+* GQA: query head h reads KV head h // (n_q / n_kv) (contiguous groups).
+* softmax scale 1/sqrt(d); masked positions are excluded, not -inf-added.
+
+Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
+(closed forms, invariants, brute force and printed values); none is unpinned.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+
+# --------------------------------------------------------------------------
+# conversions
+
+def f64(t) -> np.ndarray:
+    """Exact conversion of a bf16/fp32 tensor or array to float64."""
+    if isinstance(t, torch.Tensor):
+        return t.detach().to("cpu", torch.float64).numpy()
+    return np.asarray(t, dtype=np.float64)
+
+
+def weights_f64(w: dict) -> dict:
+    """Convert a weight dict (bf16 tensors) to float64 arrays once."""
+    return {k: f64(v) for k, v in w.items()}
+
+
+# --------------------------------------------------------------------------
+# elementary steps
+
+def rmsnorm(x: np.ndarray, g: np.ndarray, eps: float) -> np.ndarray:
+    """RMSNorm of each row: x * g / sqrt(mean(x^2) + eps).
+
+    Pre-norm placement as in a Llama decoder layer ("CSE 451 Lecture 25",
+    slide 25, decoder-only transformer layer diagram).
+    """
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return x * g / np.sqrt(ms + eps)
+
+
+def rope(u: np.ndarray, pos: np.ndarray, theta: float) -> np.ndarray:
+    """Rotary position embedding, rotate-half form.
+
+    u: [N, heads, d]; pos: [N].  For i < d/2 the pair (u_i, u_{i+d/2}) is
+    rotated by the angle pos * theta^(-2i/d).  ("CSE 451 Lecture 25",
+    slide 81 lists RoPE among the layer's operations; the pairing convention
+    is this library's reading.)
+    """
+    d = u.shape[-1]
+    half = d // 2
+    i = np.arange(half, dtype=np.float64)
+    inv_freq = theta ** (-2.0 * i / d)
+    ang = pos.astype(np.float64)[:, None] * inv_freq[None, :]          # [N, half]
+    c = np.cos(ang)[:, None, :]
+    s = np.sin(ang)[:, None, :]
+    a, b = u[..., :half], u[..., half:]
+    return np.concatenate([a * c - b * s, b * c + a * s], axis=-1)
+
+
+def silu(z: np.ndarray) -> np.ndarray:
+    return z / (1.0 + np.exp(-z))
+
+
+def attention_one(q: np.ndarray, K: np.ndarray, V: np.ndarray, n_q: int, n_kv: int) -> np.ndarray:
+    """Softmax attention of one token's query heads over its KV positions.
+
+    q: [n_q, d]; K, V: [L, n_kv, d] (every position the token may see).
+    Query head h uses KV head h // (n_q / n_kv): grouped-query attention, where
+    several query heads share one K/V head ("LLM Inference Performance", KV
+    cache sizing; "NanoFlow: Towards Optimal LLM Serving Throughput",
+    "Factor 1").  Returns o: [n_q, d].
+    """
+    d = q.shape[-1]
+    grp = n_q // n_kv
+    o = np.empty_like(q)
+    for h in range(n_q):
+        g = h // grp
+        s = K[:, g, :] @ q[h] / np.sqrt(d)
+        p = np.exp(s - s.max())
+        o[h] = (p @ V[:, g, :]) / p.sum()
+    return o
+
+
+# --------------------------------------------------------------------------
+# step metadata (integer)
+
+def token_map(q_lens: np.ndarray, seq_lens: np.ndarray):
+    """Sequence id and position of each token of the step.
+
+    Sequence s owns q_lens[s] consecutive tokens, at positions
+    seq_lens[s] - q_lens[s] ... seq_lens[s] - 1 (a decode request has one token
+    at seq_lens[s] - 1; a prefill chunk continues its prompt after the cached
+    prefix).  Returns (seq [T], pos [T]) as int64.
+    """
+    seq, pos = [], []
+    for s, (q, L) in enumerate(zip(q_lens.tolist(), seq_lens.tolist())):
+        for i in range(q):
+            seq.append(s)
+            pos.append(L - q + i)
+    return np.asarray(seq, np.int64), np.asarray(pos, np.int64)
+
+
+def slot_of(seq: np.ndarray, pos: np.ndarray, block_table: np.ndarray, page: int) -> np.ndarray:
+    """Physical pool slot of (sequence, position): block_table[s][pos // P] * P
+    + pos % P.  The block table maps logical blocks to physical blocks
+    ("LLM Inference Performance", "PagedAttention: virtual memory for the KV
+    cache"; "Inside nano-vLLM", 4.2 Paged KV, slot mapping of new KV writes).
+    """
+    return block_table[seq, pos // page].astype(np.int64) * page + pos % page
+
+
+def split_kv_items(ctx_len: np.ndarray, chunk: int, row_begin: int = 0, row_end: int | None = None):
+    """Work items of split-KV attention for rows [row_begin, row_end).
+
+    Row t sees ctx_len[t] positions; they are cut into pieces of ``chunk``
+    positions, the last one ragged.  Returns a sorted list of
+    (row, first_position, n_positions).  The set is unique; the order in which
+    a kernel visits the items is not part of the result.
+    """
+    if row_end is None:
+        row_end = len(ctx_len)
+    out = []
+    for t in range(row_begin, row_end):
+        L = int(ctx_len[t])
+        for b in range(0, L, chunk):
+            out.append((t, b, min(chunk, L - b)))
+    return sorted(out)
+
+
+# --------------------------------------------------------------------------
+# the layer step
+
+def _needed_rows(seq, rows):
+    """rows plus every earlier token of the same sequence in this step: a
+    prefill row attends to the K/V this step appends for earlier rows of its
+    chunk (the dependency rule of the pages: a nano-operation depends on
+    another when their parent operations depend and their token ranges
+    intersect)."""
+    need = set(int(r) for r in rows)
+    for r in list(need):
+        s = seq[r]
+        t = r - 1
+        while t >= 0 and seq[t] == s:
+            need.add(t)
+            t -= 1
+    return np.asarray(sorted(need), np.int64)
+
+
+def layer_step(shape, w64: dict, x, k_pool, v_pool, block_table, seq_lens, q_lens,
+               rows=None, keep=False) -> dict:
+    """One decoder-layer step over a mixed prefill+decode batch.
+
+    shape: a Shape (hidden, n_q, n_kv, head_dim, ffn, rms_eps, rope_theta,
+    page_size).  w64: float64 weights (see ``weights_f64``).  x: [T, H] layer
+    input.  k_pool, v_pool: [num_pages, n_kv, P, d] caches holding the
+    positions cached before the step (bf16 tensors; only the pages a computed
+    row reads are converted).  block_table [n_seq, max_pages], seq_lens and
+    q_lens [n_seq] as in the workload module.
+
+    rows: the token rows whose outputs are wanted (default: all).  Returns a
+    dict with ``rows``, ``y`` [len(rows), H], the appended ``k_new`` / ``v_new``
+    [len(rows), n_kv, d] and their ``slots``, plus the integer ``seq``/``pos``
+    maps.  With keep=True the intermediates n1, q, o, h, n2, a are returned
+    for the same rows.
+
+    Steps, in the order of a pre-norm layer:
+      n1 = RMSNorm(x; g1); [q|k|v] = n1 W_qkv^T; q, k <- RoPE(pos);
+      K/V of the step appended at slot(seq, pos);
+      o = GQA softmax attention over positions 0..pos of the token's sequence;
+      h = x + o W_o^T; n2 = RMSNorm(h; g2); a = silu(n2 W_g^T) * (n2 W_u^T);
+      y = h + a W_d^T.
+    """
+    H, nq, nkv, d, F = shape.hidden, shape.n_q, shape.n_kv, shape.head_dim, shape.ffn
+    P = shape.page_size
+    q_lens = np.asarray(q_lens, np.int64)
+    seq_lens = np.asarray(seq_lens, np.int64)
+    block_table = np.asarray(block_table)
+    seq, pos = token_map(q_lens, seq_lens)
+    T = len(seq)
+    rows = np.arange(T, dtype=np.int64) if rows is None else np.asarray(rows, np.int64)
+    need = _needed_rows(seq, rows)
+
+    # projections for every needed row
+    xn = f64(x[torch.as_tensor(need)]) if isinstance(x, torch.Tensor) else f64(x)[need]
+    n1 = rmsnorm(xn, w64["norm1"], shape.rms_eps)
+    qkv = n1 @ w64["w_qkv"].T
+    q = qkv[:, : nq * d].reshape(-1, nq, d)
+    k = qkv[:, nq * d: (nq + nkv) * d].reshape(-1, nkv, d)
+    v = qkv[:, (nq + nkv) * d:].reshape(-1, nkv, d)
+    q = rope(q, pos[need], shape.rope_theta)
+    k = rope(k, pos[need], shape.rope_theta)
+    new_k = {int(t): k[i] for i, t in enumerate(need)}
+    new_v = {int(t): v[i] for i, t in enumerate(need)}
+    qrow = {int(t): q[i] for i, t in enumerate(need)}
+    xrow = {int(t): xn[i] for i, t in enumerate(need)}
+    n1row = {int(t): n1[i] for i, t in enumerate(need)}
+
+    # first token index of each sequence (tokens of one sequence are contiguous)
+    first_tok = {}
+    for t in range(T):
+        first_tok.setdefault(int(seq[t]), t)
+
+    o = np.empty((len(rows), nq, d))
+    for i, t in enumerate(rows.tolist()):
+        s, p = int(seq[t]), int(pos[t])
+        cached = int(seq_lens[s] - q_lens[s])      # positions already in the pool
+        L = p + 1                                    # causal: positions 0..p
+        K = np.empty((L, nkv, d))
+        V = np.empty((L, nkv, d))
+        n_old = min(cached, L)
+        if n_old > 0:
+            j = np.arange(n_old)
+            pages = torch.as_tensor(block_table[s, j // P].astype(np.int64))
+            offs = torch.as_tensor(j % P)
+            K[:n_old] = f64(k_pool[pages, :, offs, :])
+            V[:n_old] = f64(v_pool[pages, :, offs, :])
+        for pp in range(n_old, L):                   # positions appended this step
+            tt = first_tok[s] + (pp - cached)
+            K[pp] = new_k[tt]
+            V[pp] = new_v[tt]
+        o[i] = attention_one(qrow[t], K, V, nq, nkv)
+
+    xr = np.stack([xrow[t] for t in rows.tolist()])
+    h = xr + o.reshape(len(rows), nq * d) @ w64["w_o"].T
+    n2 = rmsnorm(h, w64["norm2"], shape.rms_eps)
+    gate = n2 @ w64["w_gate_up"][:F].T
+    up = n2 @ w64["w_gate_up"][F:].T
+    a = silu(gate) * up
+    y = h + a @ w64["w_down"].T
+
+    out = {
+        "rows": rows,
+        "y": y,
+        "k_new": np.stack([new_k[t] for t in rows.tolist()]),
+        "v_new": np.stack([new_v[t] for t in rows.tolist()]),
+        "slots": slot_of(seq[rows], pos[rows], block_table, P),
+        "seq": seq,
+        "pos": pos,
+    }
+    if keep:
+        out.update(n1=np.stack([n1row[t] for t in rows.tolist()]),
+                   q=np.stack([qrow[t] for t in rows.tolist()]),
+                   o=o, h=h, n2=n2, a=a)
+    return out

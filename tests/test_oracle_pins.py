@@ -1,0 +1,358 @@
+"""Pins for the CPU oracle: closed forms, invariants, brute force, special cases.
+
+Each test checks the oracle against something other than itself, chosen so
+that a plausible slip (a dropped term, a wrong sign or index, a transposed
+operand, a wrong GQA grouping, a wrong page/slot mapping) fails at least one.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from nano_intra_device_gb300 import workload as wl
+from oracle import layer as orc
+
+
+# ----------------------------------------------------------------- RMSNorm
+
+def test_rmsnorm_constant_row_closed_form():
+    H, c, eps = 64, 1.7, 1e-5
+    g = np.linspace(0.5, 1.5, H)
+    x = np.full((1, H), c)
+    y = orc.rmsnorm(x, g, eps)
+    np.testing.assert_allclose(y[0], g * c / math.sqrt(c * c + eps), rtol=1e-15)
+
+
+def test_rmsnorm_zero_row_and_scale_invariance():
+    rng = np.random.default_rng(0)
+    g = rng.uniform(0.5, 2, 32)
+    assert np.all(orc.rmsnorm(np.zeros((1, 32)), g, 1e-5) == 0)
+    x = rng.standard_normal((3, 32))
+    a = orc.rmsnorm(x, g, 0.0)
+    b = orc.rmsnorm(7.5 * x, g, 0.0)
+    np.testing.assert_allclose(a, b, rtol=1e-13)
+    # unit mean square after dividing out the gains
+    np.testing.assert_allclose(np.mean((a / g) ** 2, axis=-1), 1.0, rtol=1e-13)
+
+
+# -------------------------------------------------------------------- RoPE
+
+def test_rope_position_zero_is_identity():
+    u = np.random.default_rng(1).standard_normal((4, 3, 64))
+    np.testing.assert_array_equal(orc.rope(u, np.zeros(4, np.int64), 1e4), u)
+
+
+def test_rope_rotate_half_closed_form():
+    d, theta = 8, 1e4
+    for i in range(d // 2):
+        for p in (1, 5, 123):
+            u = np.zeros((1, 1, d))
+            u[0, 0, i] = 1.0
+            r = orc.rope(u, np.array([p]), theta)[0, 0]
+            ang = p * theta ** (-2.0 * i / d)
+            expect = np.zeros(d)
+            expect[i] = math.cos(ang)
+            expect[i + d // 2] = math.sin(ang)
+            np.testing.assert_allclose(r, expect, atol=1e-15)
+
+
+def test_rope_keeps_pair_norms_and_is_relative():
+    rng = np.random.default_rng(2)
+    d = 64
+    q = rng.standard_normal((1, 1, d))
+    k = rng.standard_normal((1, 1, d))
+    rq = orc.rope(q, np.array([37]), 1e4)
+    half = d // 2
+    np.testing.assert_allclose(rq[..., :half] ** 2 + rq[..., half:] ** 2,
+                               q[..., :half] ** 2 + q[..., half:] ** 2, rtol=1e-12)
+    dots = []
+    for m, n in ((37, 11), (137, 111), (1037, 1011)):
+        dots.append(float(np.sum(orc.rope(q, np.array([m]), 1e4) * orc.rope(k, np.array([n]), 1e4))))
+    np.testing.assert_allclose(dots, dots[0], rtol=1e-10)
+
+
+# --------------------------------------------------------------- attention
+
+def _brute_attention(q, K, V, n_q, n_kv):
+    """Pure-Python softmax attention with explicit loops (tiny inputs)."""
+    L, d = K.shape[0], q.shape[1]
+    out = []
+    for h in range(n_q):
+        g = h * n_kv // n_q
+        s = [sum(q[h, c] * K[j, g, c] for c in range(d)) / math.sqrt(d) for j in range(L)]
+        mx = max(s)
+        e = [math.exp(v - mx) for v in s]
+        z = sum(e)
+        out.append([sum(e[j] * V[j, g, c] for j in range(L)) / z for c in range(d)])
+    return np.asarray(out)
+
+
+def test_attention_matches_brute_force():
+    rng = np.random.default_rng(3)
+    for n_q, n_kv, L in ((4, 2, 7), (8, 8, 3), (4, 1, 11)):
+        q = rng.standard_normal((n_q, 8))
+        K = rng.standard_normal((L, n_kv, 8))
+        V = rng.standard_normal((L, n_kv, 8))
+        np.testing.assert_allclose(orc.attention_one(q, K, V, n_q, n_kv),
+                                   _brute_attention(q, K, V, n_q, n_kv), rtol=1e-12, atol=1e-13)
+
+
+def test_attention_matches_torch_sdpa_with_expanded_gqa():
+    rng = np.random.default_rng(4)
+    n_q, n_kv, L, d = 8, 2, 40, 16
+    q = rng.standard_normal((n_q, d))
+    K = rng.standard_normal((L, n_kv, d))
+    V = rng.standard_normal((L, n_kv, d))
+    grp = n_q // n_kv
+    Kt = torch.from_numpy(K).permute(1, 0, 2).repeat_interleave(grp, 0)   # [n_q, L, d]
+    Vt = torch.from_numpy(V).permute(1, 0, 2).repeat_interleave(grp, 0)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q)[:, None, :], Kt, Vt)[:, 0, :].numpy()
+    np.testing.assert_allclose(orc.attention_one(q, K, V, n_q, n_kv), ref, rtol=1e-11, atol=1e-12)
+
+
+def test_attention_special_cases():
+    rng = np.random.default_rng(5)
+    d = 16
+    # one key: output is that key's value
+    V = rng.standard_normal((1, 2, d))
+    o = orc.attention_one(rng.standard_normal((4, d)), rng.standard_normal((1, 2, d)), V, 4, 2)
+    np.testing.assert_allclose(o[:2], np.repeat(V[:, 0], 2, 0), rtol=1e-14)
+    np.testing.assert_allclose(o[2:], np.repeat(V[:, 1], 2, 0), rtol=1e-14)
+    # identical keys: mean of the values
+    K = np.repeat(rng.standard_normal((1, 1, d)), 9, axis=0)
+    V = rng.standard_normal((9, 1, d))
+    o = orc.attention_one(rng.standard_normal((2, d)), K, V, 2, 1)
+    np.testing.assert_allclose(o, np.repeat(V[:, 0].mean(0, keepdims=True), 2, 0), rtol=1e-12)
+    # a large one-hot query picks the key with the largest matching coordinate
+    K = rng.standard_normal((12, 1, d))
+    q = np.zeros((1, d)); q[0, 3] = 1e4
+    V = rng.standard_normal((12, 1, d))
+    o = orc.attention_one(q, K, V, 1, 1)
+    np.testing.assert_allclose(o[0], V[np.argmax(K[:, 0, 3]), 0], rtol=1e-9)
+
+
+def test_attention_gqa_groups_are_contiguous():
+    d, L = 8, 5
+    K = np.zeros((L, 2, d))
+    V = np.zeros((L, 2, d)); V[:, 1, :] = 1.0
+    o = orc.attention_one(np.ones((4, d)), K, V, 4, 2)
+    np.testing.assert_array_equal(o[:2], 0.0)   # heads 0,1 -> KV head 0
+    np.testing.assert_array_equal(o[2:], 1.0)   # heads 2,3 -> KV head 1
+
+
+# ---------------------------------------------------------- metadata, paging
+
+def test_token_map_and_slots_roundtrip_contiguous():
+    shape = wl.tiny_shape()
+    b = wl.tiny_batch()
+    P = shape.page_size
+    # every (sequence, position) maps to a distinct slot inside its own pages,
+    # and reading them back through the block table returns the logical order
+    seen = set()
+    for s in range(b.n_seq):
+        L = int(b.seq_lens[s])
+        pos = np.arange(L)
+        sl = orc.slot_of(np.full(L, s), pos, b.block_table, P)
+        own = set()
+        for j in range((L + P - 1) // P):
+            own.update(range(b.block_table[s, j] * P, b.block_table[s, j] * P + P))
+        assert set(sl.tolist()) <= own
+        assert len(set(sl.tolist())) == L
+        assert not (seen & set(sl.tolist()))
+        seen |= set(sl.tolist())
+        # brute-force page walk
+        for p in (0, L - 1, L // 2):
+            page_list = [int(x) for x in b.block_table[s] if x >= 0]
+            assert sl[p] == page_list[p // P] * P + (p % P)
+
+
+def test_token_map_decode_and_prefill_positions():
+    q_lens = np.array([1, 1, 5, 1, 3])
+    seq_lens = np.array([10, 1, 12, 7, 3])
+    seq, pos = orc.token_map(q_lens, seq_lens)
+    assert seq.tolist() == [0, 1, 2, 2, 2, 2, 2, 3, 4, 4, 4]
+    assert pos.tolist() == [9, 0, 7, 8, 9, 10, 11, 6, 0, 1, 2]
+
+
+def test_split_kv_items_cover_each_row_once():
+    ctx = np.array([1, 15, 16, 17, 512, 513, 1030])
+    for chunk in (16, 64, 512):
+        items = orc.split_kv_items(ctx, chunk)
+        for t, L in enumerate(ctx.tolist()):
+            mine = [(b, n) for (r, b, n) in items if r == t]
+            assert len(mine) == math.ceil(L / chunk)
+            cover = np.zeros(L, int)
+            for b0, n in mine:
+                assert 1 <= n <= chunk and b0 % chunk == 0
+                cover[b0:b0 + n] += 1
+            assert np.all(cover == 1)
+
+
+# ------------------------------------------------------------ whole layer
+
+def _tiny_inputs(gain_std=0.1, seed=0):
+    shape = wl.tiny_shape()
+    b = wl.tiny_batch()
+    w = wl.make_weights(shape, seed=seed, gain_std=gain_std)
+    x = wl.make_x(shape, b.n_tokens, seed=seed)
+    k, v = wl.make_pools(shape, b, "cpu")
+    return shape, b, w, x, k, v
+
+
+def _brute_layer(shape, w, x, k_pool, v_pool, b):
+    """Independent float64 restatement of the layer on tiny inputs: complex
+    rotation for RoPE, each sequence's full contiguous K/V rebuilt position by
+    position, one dense masked softmax per sequence and head."""
+    H, nq, nkv, d, F, P = (shape.hidden, shape.n_q, shape.n_kv, shape.head_dim,
+                           shape.ffn, shape.page_size)
+    X = x.double()
+    W = {kk: vv.double() for kk, vv in w.items()}
+    n1 = X * torch.rsqrt((X * X).mean(-1, keepdim=True) + shape.rms_eps) * W["norm1"]
+    proj = torch.einsum("th,rh->tr", n1, W["w_qkv"])
+    q = proj[:, :nq * d].reshape(-1, nq, d)
+    k = proj[:, nq * d:(nq + nkv) * d].reshape(-1, nkv, d)
+    v = proj[:, (nq + nkv) * d:].reshape(-1, nkv, d)
+    # positions
+    pos, sid = [], []
+    for s in range(b.n_seq):
+        for i in range(int(b.q_lens[s])):
+            pos.append(int(b.seq_lens[s]) - int(b.q_lens[s]) + i)
+            sid.append(s)
+    pos_t = torch.tensor(pos, dtype=torch.float64)
+    half = d // 2
+    freq = shape.rope_theta ** (-torch.arange(half, dtype=torch.float64) * 2 / d)
+    rot = torch.polar(torch.ones(len(pos), half, dtype=torch.float64), pos_t[:, None] * freq)
+
+    def cplx(u):
+        z = torch.complex(u[..., :half], u[..., half:]) * rot[:, None, :]
+        return torch.cat([z.real, z.imag], -1)
+    q, k = cplx(q), cplx(k)
+    o = torch.zeros(len(pos), nq, d, dtype=torch.float64)
+    for s in range(b.n_seq):
+        L = int(b.seq_lens[s])
+        cached = L - int(b.q_lens[s])
+        toks = [t for t in range(len(pos)) if sid[t] == s]
+        Kc = torch.zeros(L, nkv, d, dtype=torch.float64)
+        Vc = torch.zeros(L, nkv, d, dtype=torch.float64)
+        for p in range(L):
+            if p < cached:
+                pg = int(b.block_table[s, p // P])
+                Kc[p] = k_pool[pg, :, p % P, :].double()
+                Vc[p] = v_pool[pg, :, p % P, :].double()
+            else:
+                Kc[p] = k[toks[p - cached]]
+                Vc[p] = v[toks[p - cached]]
+        for h in range(nq):
+            g = h // (nq // nkv)
+            S = torch.stack([q[t, h] for t in toks]) @ Kc[:, g, :].T / math.sqrt(d)
+            mask = torch.tensor([[j <= pos[t] for j in range(L)] for t in toks])
+            S = S.masked_fill(~mask, -math.inf)
+            o[toks, h] = torch.softmax(S, -1) @ Vc[:, g, :]
+    hres = X + o.reshape(len(pos), nq * d) @ W["w_o"].T
+    n2 = hres * torch.rsqrt((hres * hres).mean(-1, keepdim=True) + shape.rms_eps) * W["norm2"]
+    gu = n2 @ W["w_gate_up"].T
+    a = torch.nn.functional.silu(gu[:, :F]) * gu[:, F:]
+    y = hres + a @ W["w_down"].T
+    return y.numpy(), k.numpy(), v.numpy()
+
+
+def test_layer_matches_independent_brute_force():
+    shape, b, w, x, kp, vp = _tiny_inputs()
+    out = orc.layer_step(shape, orc.weights_f64(w), x, kp, vp, b.block_table, b.seq_lens, b.q_lens)
+    y, k, v = _brute_layer(shape, w, x, kp, vp, b)
+    np.testing.assert_allclose(out["y"], y, rtol=1e-11, atol=1e-11)
+    np.testing.assert_allclose(out["k_new"], k, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(out["v_new"], v, rtol=1e-11, atol=1e-12)
+    assert np.all(np.isfinite(out["y"]))
+
+
+def test_layer_zero_weights_is_identity_and_zero_gate_gives_h():
+    shape, b, w, x, kp, vp = _tiny_inputs()
+    w0 = {k: (torch.zeros_like(v) if k.startswith("w_") else v) for k, v in w.items()}
+    out = orc.layer_step(shape, orc.weights_f64(w0), x, kp, vp, b.block_table, b.seq_lens, b.q_lens)
+    np.testing.assert_array_equal(out["y"], orc.f64(x))
+    wg = dict(w)
+    gu = w["w_gate_up"].clone()
+    gu[: shape.ffn] = 0
+    wg["w_gate_up"] = gu
+    out = orc.layer_step(shape, orc.weights_f64(wg), x, kp, vp, b.block_table, b.seq_lens,
+                         b.q_lens, keep=True)
+    np.testing.assert_array_equal(out["a"], 0.0)
+    np.testing.assert_array_equal(out["y"], out["h"])
+
+
+def test_layer_projection_orientation_one_hot():
+    # x = e_j with unit gains and eps=0 gives n1 = sqrt(H) e_j, so the fused
+    # projection returns sqrt(H) * column j of W_qkv split into q | k | v
+    shape = wl.Shape(hidden=64, n_q=2, n_kv=1, head_dim=16, ffn=32, rms_eps=0.0)
+    b = wl.make_batch(shape, [1], [], seed_bt=0)
+    w = wl.make_weights(shape, seed=3)
+    j = 5
+    x = torch.zeros(1, 64, dtype=torch.bfloat16); x[0, j] = 1
+    kp, vp = wl.make_pools(shape, b)
+    out = orc.layer_step(shape, orc.weights_f64(w), x, kp, vp, b.block_table, b.seq_lens,
+                         b.q_lens, keep=True)
+    col = orc.f64(w["w_qkv"])[:, j] * 8.0      # sqrt(64); position 0 -> RoPE identity
+    np.testing.assert_allclose(out["q"].reshape(-1), col[:32], rtol=1e-14)
+    np.testing.assert_allclose(out["k_new"].reshape(-1), col[32:48], rtol=1e-14)
+    np.testing.assert_allclose(out["v_new"].reshape(-1), col[48:], rtol=1e-14)
+    # a single position: attention returns v, so o == v_new for both q heads
+    np.testing.assert_allclose(out["o"][0, 0], out["v_new"][0, 0], rtol=1e-14)
+    np.testing.assert_allclose(out["o"][0, 1], out["v_new"][0, 0], rtol=1e-14)
+
+
+def test_layer_shuffled_block_table_invariance():
+    shape, b, w, x, kp, vp = _tiny_inputs()
+    w64 = orc.weights_f64(w)
+    base = orc.layer_step(shape, w64, x, kp, vp, b.block_table, b.seq_lens, b.q_lens)
+    perm = np.random.default_rng(9).permutation(b.num_pages)
+    bt2 = np.where(b.block_table >= 0, perm[np.maximum(b.block_table, 0)], -1).astype(np.int32)
+    kp2 = torch.empty_like(kp); vp2 = torch.empty_like(vp)
+    kp2[torch.as_tensor(perm)] = kp
+    vp2[torch.as_tensor(perm)] = vp
+    out = orc.layer_step(shape, w64, x, kp2, vp2, bt2, b.seq_lens, b.q_lens)
+    np.testing.assert_array_equal(out["y"], base["y"])
+    np.testing.assert_array_equal(out["k_new"], base["k_new"])
+
+
+def test_layer_rows_subset_equals_full():
+    shape, b, w, x, kp, vp = _tiny_inputs()
+    w64 = orc.weights_f64(w)
+    full = orc.layer_step(shape, w64, x, kp, vp, b.block_table, b.seq_lens, b.q_lens)
+    rows = [2, 9, 20, 35]
+    sub = orc.layer_step(shape, w64, x, kp, vp, b.block_table, b.seq_lens, b.q_lens, rows=rows)
+    np.testing.assert_allclose(sub["y"], full["y"][rows], rtol=1e-13, atol=1e-13)
+    np.testing.assert_array_equal(sub["slots"], full["slots"][rows])
+
+
+def test_prefill_chunk_in_two_steps_equals_one_step():
+    """Splitting a prefill chunk across two steps (the first appends its K/V to
+    the cache, the second continues after that prefix) gives the same rows as
+    one step: the nano-batch dependency rule the pipeline relies on."""
+    shape = wl.tiny_shape()
+    P = shape.page_size
+    w = wl.make_weights(shape, seed=1, gain_std=0.1)
+    w64 = orc.weights_f64(w)
+    b_one = wl.make_batch(shape, [], [32], [0], seed_bt=4)
+    x = wl.make_x(shape, 32, seed=5)
+    kp, vp = wl.make_pools(shape, b_one)
+    kp = kp.double(); vp = vp.double()
+    one = orc.layer_step(shape, w64, x, kp, vp, b_one.block_table, b_one.seq_lens, b_one.q_lens)
+    first = orc.layer_step(shape, w64, x[:12], kp, vp, b_one.block_table, np.array([12]),
+                           np.array([12]))
+    kp2, vp2 = kp.clone(), vp.clone()
+    for i, sl in enumerate(first["slots"].tolist()):
+        kp2[sl // P, :, sl % P, :] = torch.from_numpy(first["k_new"][i])
+        vp2[sl // P, :, sl % P, :] = torch.from_numpy(first["v_new"][i])
+    second = orc.layer_step(shape, w64, x[12:], kp2, vp2, b_one.block_table, np.array([32]),
+                            np.array([20]))
+    np.testing.assert_allclose(first["y"], one["y"][:12], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(second["y"], one["y"][12:], rtol=1e-12, atol=1e-12)
+
+
+def test_silu_values():
+    z = np.array([0.0, 1.0, -1.0, 20.0])
+    np.testing.assert_allclose(orc.silu(z), [0.0, 1 / (1 + math.exp(-1)), -1 / (1 + math.e), 20 / (1 + math.exp(-20))],
+                               rtol=1e-15)
