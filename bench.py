@@ -1,0 +1,439 @@
+#!/usr/bin/env python
+"""Benchmark of the nano-batched decoder-layer step on one GB300 (or N replicas).
+
+Workload: one Llama-3-8B-shaped decoder layer (hidden 4096, 32 q / 8 KV heads,
+head_dim 128, FFN 14336, bf16) over a mixed step of T = 2048 tokens: 1792
+decode requests with lognormal KV lengths (median 600, sigma 1, clipped to
+[1, 8192]) plus one 256-token prefill chunk, KV in 16-token pages under a
+random block table.  Synthetic, seeded inputs; random N(0, 0.02) weights.
+
+Metric: tokens/s of the layer step (T / step time, summed over replicas) and
+the fraction of the layer roofline, max(FLOPs / bf16 peak, bytes / HBM peak)
+divided by the step time.
+
+The JSON line also carries: e2e (the same step through the host-buffer entry
+point, copies included), the roofline of the dominant kernel (paged decode
+attention, HBM-bound) measured inside the timed steps, clocks sampled during
+the timed region, the CPU oracle timed on a bounded sample (cpu_baseline),
+and the sequential / nanobatch-only / overlapped comparison.
+
+`--impl reference` times the CPU oracle itself on the same workload (bounded
+sample per step) and prints the same line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from nano_intra_device_gb300 import costmodel as cm  # noqa: E402
+from nano_intra_device_gb300 import workload as wl  # noqa: E402
+
+METRIC = "tokens/s per GB300 for mixed prefill+decode layer step; % of layer roofline"
+WORKLOAD = ("llama3-8b-shaped decoder layer, mixed step of 2048 tokens: 1792 decode "
+            "(lognormal KV median 600, sigma 1, clip [1,8192]) + one 256-token prefill chunk, "
+            "16-token pages, random block table")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="nanoflow", choices=["nanoflow", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-ablation", action="store_true")
+    ap.add_argument("--plan", default="auto", help="auto | search | n=<k>,sms=<s>")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks
+class Clocks:
+    """nvidia-smi samples (every 200 ms) during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self):
+        self.proc = None
+        self.path = tempfile.mktemp(suffix=".csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        want = vis.split(",")[0] if vis and vis.split(",")[0].isdigit() else None
+        if want is not None and any(r[0] == want for r in rows):
+            rows = [r for r in rows if r[0] == want]
+        elif rows:
+            rows = [r for r in rows if r[0] == rows[0][0]]
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- workload
+class Workload:
+    def __init__(self, dev):
+        self.shape = wl.llama8b_shape()
+        self.batch = wl.llama8b_batch()
+        self.T = self.batch.n_tokens
+        self.w_cpu = wl.make_weights(self.shape, seed=0)
+        self.x_cpu = wl.make_x(self.shape, self.T, seed=0)
+        self.dev = dev
+        self.w = {k: v.to(dev) for k, v in self.w_cpu.items()}
+        self.x = self.x_cpu.to(dev)
+        self.kp, self.vp = wl.make_pools(self.shape, self.batch, dev, seed=3)
+        self.bt = torch.from_numpy(self.batch.block_table).to(dev)
+        self.sl = torch.from_numpy(self.batch.seq_lens).to(dev)
+        self.y = torch.empty_like(self.x)
+        self.work = cm.step_work(self.shape, self.batch.seq_lens, self.batch.q_lens)
+        self.attn_bytes = self._attn_bytes()
+
+    def _attn_bytes(self):
+        """Bytes attention must move per step: every token's visible K/V once
+        (decode history; prefill rows share their chunk's K/V), q in, o out."""
+        s, b = self.shape, self.batch
+        kv_tok = 2 * s.n_kv * s.head_dim * 2
+        qo = 2 * self.T * s.n_q * s.head_dim * 2
+        return int(b.seq_lens.sum()) * kv_tok + qo
+
+
+def oracle_sample(wk: Workload, n_decode: int, n_prefill: int, seed: int = 0):
+    """A bounded piece of the workload the CPU oracle can run: n_decode random
+    decode requests plus the first n_prefill rows of the prefill chunk, with
+    only their pages copied to host memory."""
+    b, s = wk.batch, wk.shape
+    rng = np.random.default_rng(seed)
+    dec = sorted(rng.choice(b.n_decode, n_decode, replace=False).tolist())
+    seqs = dec + ([b.n_decode] if n_prefill > 0 else [])
+    P = s.page_size
+    pages, bt_rows = [], []
+    for sq in seqs:
+        n = (int(b.seq_lens[sq]) + P - 1) // P
+        ids = b.block_table[sq, :n]
+        bt_rows.append(list(range(len(pages), len(pages) + n)))
+        pages.extend(ids.tolist())
+    width = max(len(r) for r in bt_rows)
+    bt = np.full((len(seqs), width), -1, np.int32)
+    for i, r in enumerate(bt_rows):
+        bt[i, :len(r)] = r
+    idx = torch.as_tensor(pages, device=wk.kp.device)
+    kp = wk.kp[idx].cpu()
+    vp = wk.vp[idx].cpu()
+    sl = b.seq_lens[seqs].astype(np.int32)
+    ql = b.q_lens[seqs].astype(np.int32)
+    tok = dec + (list(range(b.n_decode, b.n_decode + int(b.q_lens[b.n_decode]))) if n_prefill else [])
+    x = wk.x_cpu[torch.as_tensor(tok)]
+    rows = list(range(len(dec))) + list(range(len(dec), len(dec) + n_prefill))
+    return dict(shape=s, w=wk.w_cpu, x=x, kp=kp, vp=vp, bt=bt, sl=sl, ql=ql, rows=rows,
+                desc=f"{n_decode} random decode rows + first {n_prefill} prefill rows of the "
+                     f"8B-shaped step, one oracle call (float64 weights converted per call)")
+
+
+def time_oracle(sample):
+    from oracle import layer as orc   # CPU baseline leg only
+    t0 = time.perf_counter()
+    orc.layer_step(sample["shape"], orc.weights_f64(sample["w"]), sample["x"], sample["kp"],
+                   sample["vp"], sample["bt"], sample["sl"], sample["ql"], rows=sample["rows"])
+    return time.perf_counter() - t0
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+# ---------------------------------------------------------------- distributed
+def dist_setup(n):
+    rank, world, local = 0, 1, 0
+    if "WORLD_SIZE" in os.environ and int(os.environ["WORLD_SIZE"]) > 1:
+        import torch.distributed as dist
+        local = int(os.environ.get("LOCAL_RANK", 0))
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+        rank, world = dist.get_rank(), dist.get_world_size()
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------- reference
+def run_reference(args):
+    rank, world, _ = dist_setup(args.gpus)
+    if rank != 0:
+        return
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    wk = Workload(dev)
+    sample = oracle_sample(wk, 24, 8, seed=1)
+    n_tok = len(sample["rows"])
+    for _ in range(args.warmup):
+        time_oracle(sample)
+    ts = [time_oracle(sample) for _ in range(args.steps)]
+    t = sum(ts) / len(ts)
+    v = n_tok / t
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "tokens_per_step_sample": n_tok},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cpu_cores(),
+                             "kind": "oracle", "sample": sample["desc"]},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# -------------------------------------------------------------------- main
+def time_steps(fn, steps, warmup, world, stream):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    return e0.elapsed_time(e1) / steps
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    from nano_intra_device_gb300 import _lib
+
+    rank, world, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    _lib.lib()
+    wk = Workload(dev)
+    T = wk.T
+    stream = torch.cuda.current_stream()
+    pk = peaks()
+    sms = _lib.device_sm_count()
+
+    def make_plan(opts):
+        return _lib.Plan(wk.shape, wk.batch, opts)
+
+    def stepper(plan):
+        return lambda: _lib.layer_step(plan, wk.w, wk.x, wk.kp, wk.vp, wk.bt, wk.sl, wk.y)
+
+    # candidates: the library's search, then measured neighbours (real timing of
+    # the best predicted plans, the last step of the plan search)
+    searched = make_plan(None)
+    so, _ = searched.info()
+    cands = [("search", searched)]
+    if args.plan == "auto":
+        for n in (2, 3):
+            ab = [0] + [int(round(T * i / n / 128)) * 128 for i in range(1, n)] + [T]
+            for a_sms in (sms * 9 // 16, sms * 10 // 16, sms * 11 // 16, sms * 12 // 16):
+                o = _lib.make_opts(T, ab, ab, executor=_lib.NF_EXEC_STREAMS, attn_sms=a_sms)
+                cands.append((f"n={n},attn_sms={a_sms}", make_plan(o)))
+    elif args.plan.startswith("n="):
+        kv = dict(p.split("=") for p in args.plan.split(","))
+        n, a_sms = int(kv["n"]), int(kv.get("sms", sms * 5 // 8))
+        ab = [0] + [int(round(T * i / n / 128)) * 128 for i in range(1, n)] + [T]
+        cands = [(args.plan, make_plan(_lib.make_opts(T, ab, ab, executor=_lib.NF_EXEC_STREAMS,
+                                                      attn_sms=a_sms)))]
+    tried = {}
+    for name, p in cands:
+        tried[name] = time_steps(stepper(p), 5, 2, 1, stream)
+        p.poll()
+    best_name = min(tried, key=tried.get)
+    plan = dict(cands)[best_name]
+    for name, p in cands:
+        if p is not plan:
+            p.close()
+    po, _ = plan.info()
+
+    # timed region
+    clocks = Clocks()
+    plan.trace_enable(args.steps)
+    for _ in range(args.warmup):
+        stepper(plan)()
+    torch.cuda.synchronize()
+    plan.trace_enable(args.steps)      # record exactly the timed steps
+    clocks.start()
+    ms = time_steps(stepper(plan), args.steps, 0, world, stream)
+    clk = clocks.stop()
+    plan.poll()
+    trace = plan.trace_read()
+    plan.trace_enable(0)
+    ms = max_over_ranks(ms, world)
+    value = T * world / (ms * 1e-3)
+
+    # roofline of the dominant kernel (attention) from the timed steps
+    attn = [e["ms"] for e in trace if e["op"] == "attn"]
+    n_attn = po.n_attn
+    attn_bytes_per_launch = wk.attn_bytes / n_attn
+    attn_ms = sum(attn) / max(1, len(attn))
+    achieved = attn_bytes_per_launch / (attn_ms * 1e-3) / 1e9
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "attn_traffic.json")
+    if os.path.exists(tpath):
+        tj = json.load(open(tpath))
+        src = open(os.path.join(ROOT, "nano_intra_device_gb300", "csrc", "attn.cu"), "rb").read()
+        if tj.get("source_sha256") == hashlib.sha256(src).hexdigest():
+            traffic = tj.get("bytes_per_launch", {}).get(str(n_attn))
+    roof = {"bound": "hbm", "kernel": "attn_kernel (paged GQA decode attention)",
+            "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
+            "peak_source": pk["source"] + " hbm_gbs (copy)",
+            "algorithmic_bytes_per_launch": attn_bytes_per_launch, "launches_per_step": n_attn,
+            "avg_launch_ms": attn_ms}
+
+    # layer roofline
+    rf = cm.roofline_time(wk.work, pk["bf16_tflops_sustained"] * 1e12, pk["hbm_gbs"] * 1e9)
+    layer_frac = rf["t_roof"] / (ms * 1e-3)
+
+    # timeline summary of the last traced step: overlap of attention with GEMMs
+    last = max((e["step"] for e in trace), default=0)
+    ev = [e for e in trace if e["step"] == last]
+    a_iv = [(e["start_ms"], e["start_ms"] + e["ms"]) for e in ev if e["op"] == "attn"]
+    g_iv = [(e["start_ms"], e["start_ms"] + e["ms"]) for e in ev if e["op"] in ("qkv", "oproj", "ffn")]
+    overlap = sum(max(0.0, min(a1, g1) - max(a0, g0)) for a0, a1 in a_iv for g0, g1 in g_iv)
+    timeline = [{k: (round(v, 4) if isinstance(v, float) else v) for k, v in e.items() if k != "step"}
+                for e in sorted(ev, key=lambda e: e["start_ms"])]
+
+    # e2e through the host-buffer entry point
+    xh = wk.x_cpu.pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    bth = torch.from_numpy(wk.batch.block_table).pin_memory()
+    slh = torch.from_numpy(wk.batch.seq_lens).pin_memory()
+    for _ in range(max(1, args.warmup)):
+        _lib.layer_step_host(plan, wk.w, xh, wk.kp, wk.vp, bth, slh, yh)
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _lib.layer_step_host(plan, wk.w, xh, wk.kp, wk.vp, bth, slh, yh)
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / args.steps, world)
+    h2d = xh.numel() * 2 + bth.numel() * 4 + slh.numel() * 4
+    d2h = yh.numel() * 2
+
+    # ablation: sequential, nanobatch-only, overlapped (same kernels)
+    ablation = None
+    if not args.no_ablation:
+        ablation = {}
+        seq = make_plan(_lib.make_opts(T))
+        ablation["sequential_n1"] = T / (time_steps(stepper(seq), 10, 3, world, stream) * 1e-3)
+        seq.close()
+        ab = list(po.attn_bounds[: po.n_attn + 1])
+        fb = list(po.ffn_bounds[: po.n_ffn + 1])
+        nb = make_plan(_lib.make_opts(T, ab, fb, executor=_lib.NF_EXEC_SEQUENTIAL))
+        ablation["nanobatch_only"] = T / (time_steps(stepper(nb), 10, 3, world, stream) * 1e-3)
+        nb.close()
+        ablation["overlap"] = value / world
+
+    launches_per_step = 1 + 4 * po.n_attn + 3 * po.n_ffn
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "tokens": T, "decode": wk.batch.n_decode,
+                       "prefill": wk.batch.prefill_q_lens,
+                       "kv_read_gb_per_step": wk.work["kv_read_bytes"] / 1e9,
+                       "l2": "inputs larger than L2 (KV read per step > 7 GB, weights 0.44 GB)",
+                       "plan": dict(_lib.opts_dict(po), chosen=best_name),
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "layer_roofline": {"frac": layer_frac, "t_roof_ms": rf["t_roof"] * 1e3,
+                               "t_flop_ms": rf["t_flop"] * 1e3, "t_byte_ms": rf["t_byte"] * 1e3,
+                               "bound": rf["bound"], "flops": wk.work["flops"],
+                               "bytes": wk.work["bytes"],
+                               "peaks": f"{pk['source']}: {pk['bf16_tflops_sustained']} TF/s bf16 sustained, {pk['hbm_gbs']} GB/s"},
+            "clocks": clk,
+            "e2e": {"value": T * world / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_step * args.steps,
+            "roofline": roof,
+            "overlap": {"attn_gemm_concurrent_ms": overlap, "timeline_last_step": timeline},
+            "ablation_tokens_per_s": ablation,
+            "plan_candidates_ms": tried}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sample = oracle_sample(wk, 128, 16, seed=1)
+        t = time_oracle(sample)
+        line["cpu_baseline"] = {"value": len(sample["rows"]) / t, "unit": "tokens/s",
+                                "cores": cpu_cores(), "kind": "oracle", "sample": sample["desc"]}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    plan.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,291 @@
+/*
+ * nanoflow.h — C ABI of the GB300 (sm_103a) nano-batched decoder-layer step.
+ *
+ * One call, nf_layer_step, runs one pre-norm decoder layer over a mixed batch
+ * of decode requests and prefill chunks whose K/V live in a paged cache:
+ *
+ *   n1 = RMSNorm(x; g1)                 [T, H]
+ *   q|k|v = n1 W_qkv^T, RoPE on q and k, k and v appended to the paged cache
+ *   o = GQA softmax attention of each token over positions 0..pos of its
+ *       sequence (decode: the whole history; prefill: causal)
+ *   h = x + o W_o^T
+ *   y = h + (silu(n2 W_g^T) * (n2 W_u^T)) W_d^T,  n2 = RMSNorm(h; g2)
+ *
+ * The batch is cut into nano-batches of tokens so that the tensor-core GEMMs of
+ * one nano-batch run on the GPU while the HBM-bound decode attention of another
+ * runs beside them ("NanoFlow: Towards Optimal LLM Serving Throughput",
+ * "The Intra-Device Parallelism Mechanism").  A plan fixes the split, the order
+ * and the SM share of each nano-operation ("Auto-Search Stage I" and
+ * "Auto-Search Stage II" of the same page); the result never depends on it.
+ *
+ * Conventions for every entry point:
+ *  - Pointers marked "device" are CUDA device pointers on the current device;
+ *    "host" pointers are ordinary host memory.  The caller owns all buffers it
+ *    passes; the library never frees or reallocates them.
+ *  - Tensors are dense, row-major, bf16 (stored as 16-bit words) unless stated.
+ *  - Calls that take a `stream` (a cudaStream_t, NULL = legacy default stream)
+ *    only enqueue work and return; results are ready when the stream completes.
+ *  - Argument errors are detected on the host before anything is launched and
+ *    return NF_ERR_INVALID_ARG with a message in nf_last_error().  Device-side
+ *    problems (a page id outside the pool, a bounded wait that gave up) set a
+ *    status word in the plan; nf_plan_poll reports it.  Nothing traps.
+ *  - No entry point throws across the ABI.  Functions are thread-safe except
+ *    that one plan must not be used by two threads at once.
+ */
+#ifndef NANOFLOW_H
+#define NANOFLOW_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define NF_MAX_NANO 8
+
+typedef enum {
+  NF_OK = 0,
+  NF_ERR_INVALID_ARG = 1, /* a size, pointer or layout the library does not accept */
+  NF_ERR_UNSUPPORTED = 2, /* valid request this build does not implement */
+  NF_ERR_OOM = 3,         /* device or host allocation failed */
+  NF_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed */
+  NF_ERR_TIMEOUT = 5,     /* a bounded device wait gave up (from nf_plan_poll) */
+  NF_ERR_DEVICE = 6,      /* device-side check failed, e.g. page id out of range */
+  NF_ERR_INTERNAL = 7
+} nf_status;
+
+typedef enum {
+  NF_EXEC_SEQUENTIAL = 0, /* every nano-operation in order on the caller's stream */
+  NF_EXEC_STREAMS = 1     /* GEMMs and attention on two streams ordered by events,
+                             each kernel capped to its SM share */
+} nf_executor;
+
+/* Shape of one Llama-style decoder layer.  head_dim in {64, 128};
+ * n_q_heads a multiple of n_kv_heads with n_q/n_kv in {1, 2, 4, 8};
+ * hidden and ffn multiples of 64; page_size = 16. */
+typedef struct {
+  int32_t hidden;
+  int32_t n_q_heads;
+  int32_t n_kv_heads;
+  int32_t head_dim;
+  int32_t ffn;
+  int32_t page_size;
+  float rms_eps;
+  float rope_theta;
+} nf_model_shape;
+
+/* Structure of the mixed batch a plan serves ("NanoFlow: Towards Optimal LLM
+ * Serving Throughput", "The NanoFlow Runtime System", batch formation: decode
+ * requests first, prefill chunks fill the rest of a constant dense batch).
+ * Tokens [0, n_decode) are decode requests, one token each (sequence i = token
+ * i); then n_prefill chunks, chunk j holding prefill_q_lens[j] consecutive
+ * tokens of sequence n_decode + j.  T = n_decode + sum(prefill_q_lens). */
+typedef struct {
+  int32_t n_decode;
+  int32_t n_prefill;
+  const int32_t* prefill_q_lens; /* host [n_prefill]; copied by nf_plan_create */
+  const int32_t* seq_lens_hint;  /* host [n_decode + n_prefill] or NULL: typical KV
+                                    lengths, used only by the plan search */
+  int32_t max_pages_per_seq;     /* row stride of the block table */
+  int32_t num_pages;             /* pages in each of the K and V pools */
+} nf_batch_desc;
+
+/* A plan: the nano-batch split and the resources of each nano-operation
+ * (the output of the pages' two-stage auto-search).  Passed to nf_plan_create
+ * to force a plan, or read back with nf_plan_info.
+ * attn_bounds: token boundaries of the attention group (QKV projection,
+ *   attention, O projection): nano-batch i is [attn_bounds[i], attn_bounds[i+1]),
+ *   attn_bounds[0] = 0, attn_bounds[n_attn] = T, strictly increasing.
+ * ffn_bounds: the same for the FFN group (RMSNorm-2, gate/up, down). */
+typedef struct {
+  int32_t n_attn;
+  int32_t attn_bounds[NF_MAX_NANO + 1];
+  int32_t n_ffn;
+  int32_t ffn_bounds[NF_MAX_NANO + 1];
+  int32_t executor;   /* nf_executor */
+  int32_t attn_sms;   /* SMs for attention while it overlaps GEMMs (0 = automatic) */
+  int32_t gemm_sms;   /* SMs for a GEMM while it overlaps attention (0 = the rest) */
+  int32_t kv_chunk;   /* split-KV piece in tokens, multiple of page_size (0 = 512) */
+  int32_t validate;   /* 1 = check page ids and lengths on the device */
+  int64_t timeout_ns; /* limit of every device-side wait (0 = 2e9) */
+} nf_plan_opts;
+
+typedef struct nf_plan_s* nf_plan;
+
+/* Layer weights, all device, bf16.
+ * norm1, norm2: [H].  w_qkv: [(n_q + 2 n_kv) * head_dim, H], rows are the q
+ * heads, then the k heads, then the v heads.  w_o: [H, n_q * head_dim].
+ * w_gate_up: [2 F, H], gate rows then up rows.  w_down: [H, F]. */
+typedef struct {
+  const void* norm1;
+  const void* w_qkv;
+  const void* w_o;
+  const void* norm2;
+  const void* w_gate_up;
+  const void* w_down;
+} nf_layer_weights;
+
+/* Create a plan for one model shape and batch structure
+ * ("Auto-Search Stage I" / "Stage II": split, order, resource share).
+ * opts NULL: search the split and the SM shares with the library's cost
+ * model (uses seq_lens_hint when given).  opts non-NULL: use it as given
+ * (validated).  Allocates the plan's device workspace on the current device.
+ * Errors: NF_ERR_INVALID_ARG (shape/batch/opts), NF_ERR_OOM, NF_ERR_CUDA. */
+nf_status nf_plan_create(const nf_model_shape* shape, const nf_batch_desc* batch,
+                         const nf_plan_opts* opts, nf_plan* out);
+
+/* The plan's split and resources, and the batch's token count. */
+nf_status nf_plan_info(nf_plan plan, nf_plan_opts* out, int32_t* n_tokens);
+
+/* Write / read a plan (shape, batch structure and opts) as a text file. */
+nf_status nf_plan_save(nf_plan plan, const char* path);
+nf_status nf_plan_load(const char* path, nf_plan* out);
+
+/* Free a plan and its device workspace.  The caller must make sure no step
+ * that uses the plan is still running.  NULL is ignored. */
+void nf_plan_destroy(nf_plan plan);
+
+/* One decoder-layer step (see the top of this file).
+ * x, y: device [T, H]; x != y (no aliasing).
+ * k_pool, v_pool: device [num_pages, n_kv, page_size, head_dim]; the step
+ *   writes this step's k (after RoPE) and v at slot(seq, pos) =
+ *   block_table[seq][pos / page_size] * page_size + pos % page_size, and reads
+ *   positions 0..pos of each token's sequence.
+ * block_table: device int32 [n_seq, max_pages_per_seq]; must cover every
+ *   position < seq_lens[s].
+ * seq_lens: device int32 [n_seq], KV length of each sequence AFTER this step:
+ *   decode token i sits at position seq_lens[i] - 1; prefill chunk j continues
+ *   its prompt at position seq_lens[s] - prefill_q_lens[j].
+ * Returns after enqueueing on `stream`. */
+nf_status nf_layer_step(nf_plan plan, const nf_layer_weights* w, const void* x, void* k_pool,
+                        void* v_pool, const int32_t* block_table, const int32_t* seq_lens, void* y,
+                        void* stream);
+
+/* The same step with the per-step inputs and the output in HOST memory:
+ * x_host [T, H] bf16, block_table_host and seq_lens_host as above, y_host
+ * [T, H].  Copies them through plan-owned device staging buffers on `stream`
+ * and synchronizes the stream before returning (y_host is then valid).
+ * Pinned host memory gives full copy bandwidth; pageable memory works. */
+nf_status nf_layer_step_host(nf_plan plan, const nf_layer_weights* w, const void* x_host,
+                             void* k_pool, void* v_pool, const int32_t* block_table_host,
+                             const int32_t* seq_lens_host, void* y_host, void* stream);
+
+/* Report device-side errors of earlier steps.  wait != 0 synchronizes the
+ * device first.  Returns NF_OK, NF_ERR_TIMEOUT or NF_ERR_DEVICE (and clears
+ * the status word), or NF_ERR_CUDA for an asynchronous CUDA error. */
+nf_status nf_plan_poll(nf_plan plan, int wait);
+
+/* Text of the last error on the calling thread ("" if none). */
+const char* nf_last_error(void);
+
+/* Number of SMs the plan's device has (the unit of SM shares). */
+int32_t nf_device_sm_count(void);
+
+/* ---------------------------------------------------------------------------
+ * Single steps of the path, for tests and for the profiler.  Each runs exactly
+ * the kernel nf_layer_step runs for that step.
+ */
+
+/* Step metadata (integer, bit-exact): per token its sequence, position and
+ * cache slot, and the split-KV attention work list of each attention
+ * nano-batch.  ("NanoFlow: Towards Optimal LLM Serving Throughput",
+ * "Auto-Search Stage I", constraints on dependencies: a nano-operation's token
+ * range; "Inside nano-vLLM", 4.2 Paged KV: slot mapping.)  Reads block_table and
+ * seq_lens (device, as in nf_layer_step); results stay in the plan, read them
+ * with nf_plan_copy_buffer. */
+nf_status nf_step_metadata(nf_plan plan, const int32_t* block_table, const int32_t* seq_lens,
+                           void* stream);
+
+/* Paged GQA attention of every token of the batch, from q already computed:
+ * q: device [T, n_q, head_dim] (RoPE applied); o: device [T, n_q, head_dim].
+ * The cache must already hold this step's K/V.  Runs nf_step_metadata first.
+ * ("NanoFlow: Towards Optimal LLM Serving Throughput", "The Intra-Device
+ * Parallelism Mechanism": decode attention is the memory-bound operation;
+ * "LLM Inference Performance", "PagedAttention".) */
+nf_status nf_attention(nf_plan plan, const void* q, const void* k_pool, const void* v_pool,
+                       const int32_t* block_table, const int32_t* seq_lens, void* o, void* stream);
+
+/* RMSNorm of rows [0, rows): out = x * g / sqrt(mean(x^2) + eps), fp32
+ * arithmetic, bf16 out.  x, out: device [rows, hidden]; g: device [hidden]. */
+nf_status nf_rmsnorm(const void* x, const void* g, void* out, int32_t rows, int32_t hidden,
+                     float eps, void* stream);
+
+/* Tensor-core GEMM, C = A * B^T with fp32 accumulation.
+ * A: device [M, K], B: device [N, K], both bf16 row-major, K a multiple of 8,
+ * 16-byte aligned rows.  epilogue:
+ *   NF_EPI_STORE   C[M, N] = acc
+ *   NF_EPI_RESID   C[M, N] = R[M, N] + acc          (R device [M, N])
+ *   NF_EPI_SWIGLU  B holds 2F rows (gate rows then up rows), N = F:
+ *                  C[M, F] = silu(A Bg^T) * (A Bu^T)
+ * max_sms caps the persistent grid (0 = all SMs). */
+typedef enum { NF_EPI_STORE = 0, NF_EPI_RESID = 1, NF_EPI_SWIGLU = 2 } nf_epilogue;
+nf_status nf_gemm(const void* A, const void* B, void* C, const void* R, int32_t M, int32_t N,
+                  int32_t K, int32_t epilogue, int32_t max_sms, void* stream);
+
+/* Copy one of the plan's device buffers (written by the last step or
+ * metadata call on the plan's device) to dst (host or device), synchronously.
+ * bytes must not exceed the buffer size (nf_plan_buffer_size). */
+typedef enum {
+  NF_BUF_TOK_SEQ = 0,   /* int32 [T] */
+  NF_BUF_TOK_POS = 1,   /* int32 [T] */
+  NF_BUF_TOK_SLOT = 2,  /* int32 [T], -1 where the page id was invalid */
+  NF_BUF_ITEMS = 3,     /* int32 [2 * capacity]: (row, chunk) pairs of the work
+                           list, nano-batch segments back to back */
+  NF_BUF_ITEM_SEG = 4,  /* int32 [n_attn + 1]: start of each segment in ITEMS;
+                           the last entry is the total */
+  NF_BUF_N1 = 5,        /* bf16 [T, H] */
+  NF_BUF_Q = 6,         /* bf16 [T, n_q * head_dim] */
+  NF_BUF_O = 7,         /* bf16 [T, n_q * head_dim] */
+  NF_BUF_H = 8,         /* bf16 [T, H] */
+  NF_BUF_N2 = 9,        /* bf16 [T, H] */
+  NF_BUF_A = 10         /* bf16 [T, F] */
+} nf_buffer;
+nf_status nf_plan_buffer_size(nf_plan plan, int32_t which, size_t* bytes);
+nf_status nf_plan_copy_buffer(nf_plan plan, int32_t which, void* dst, size_t bytes);
+
+/* Tracing: CUDA-event timestamps of every nano-operation of a step, taken on
+ * the stream each one is launched on (the pages' per-microsecond utilisation
+ * timelines, "NanoFlow: Towards Optimal LLM Serving Throughput", evaluation of
+ * resource usage).  nf_plan_trace_enable(plan, max_steps) starts recording the
+ * next max_steps steps (0 stops and drops the record).  nf_plan_trace_read
+ * synchronizes the plan's streams and returns one entry per nano-operation
+ * per recorded step: op (NF_OP_*), nano-batch index, step index, start time
+ * relative to that step's start and duration, both in milliseconds. */
+typedef enum { NF_OP_META = 0, NF_OP_QKV = 1, NF_OP_ATTN = 2, NF_OP_OPROJ = 3, NF_OP_FFN = 4 } nf_op;
+typedef struct {
+  int32_t op;
+  int32_t nano;
+  int32_t step;
+  float start_ms;
+  float ms;
+} nf_trace_entry;
+nf_status nf_plan_trace_enable(nf_plan plan, int32_t max_steps);
+nf_status nf_plan_trace_read(nf_plan plan, nf_trace_entry* out, int32_t cap, int32_t* n_out);
+
+/* ---------------------------------------------------------------------------
+ * Profiler and plan search ("NanoFlow: Towards Optimal LLM Serving
+ * Throughput", "Kernel Profiling and Interference Modeling", "Auto-Search
+ * Stage I/II").
+ */
+
+/* Measure, on the current device, the interference-free time of each
+ * operation of the layer at token counts that are multiples of 128 (up to
+ * max_tokens) and SM counts, and the time of attention when it shares the GPU
+ * with a GEMM at several SM splits; write them to out_json.  Allocates and
+ * frees its own buffers; takes seconds to minutes. */
+nf_status nf_profile(const nf_model_shape* shape, int32_t max_tokens, int32_t mean_ctx,
+                     const char* out_json);
+
+/* Plan search on the host only (no device work): given a profile table
+ * (JSON written by nf_profile, or NULL for the built-in roofline model), pick
+ * the split and SM shares that minimise the predicted step time.  Fills `out`
+ * and the predicted time in microseconds. */
+nf_status nf_plan_search(const nf_model_shape* shape, const nf_batch_desc* batch,
+                         const char* profile_json, int32_t num_sms, nf_plan_opts* out,
+                         double* predicted_us);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NANOFLOW_H */

@@ -1,0 +1,269 @@
+"""ctypes binding of libnanoflow.so: the C ABI declared in include/nanoflow.h.
+
+Argument marshalling only.  Every step of the layer runs in the library's CUDA
+kernels; if the library is missing this module raises instead of falling back
+to anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from ctypes import POINTER, Structure, c_char_p, c_double, c_float, c_int, c_int32, c_int64, c_size_t, c_void_p
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_build", "libnanoflow.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "nanoflow.h")
+NF_MAX_NANO = 8
+
+NF_OK, NF_ERR_INVALID_ARG, NF_ERR_UNSUPPORTED, NF_ERR_OOM, NF_ERR_CUDA, NF_ERR_TIMEOUT, \
+    NF_ERR_DEVICE, NF_ERR_INTERNAL = range(8)
+NF_EXEC_SEQUENTIAL, NF_EXEC_STREAMS = 0, 1
+NF_EPI_STORE, NF_EPI_RESID, NF_EPI_SWIGLU = 0, 1, 2
+(NF_BUF_TOK_SEQ, NF_BUF_TOK_POS, NF_BUF_TOK_SLOT, NF_BUF_ITEMS, NF_BUF_ITEM_SEG, NF_BUF_N1,
+ NF_BUF_Q, NF_BUF_O, NF_BUF_H, NF_BUF_N2, NF_BUF_A) = range(11)
+
+
+class nf_model_shape(Structure):
+    _fields_ = [("hidden", c_int32), ("n_q_heads", c_int32), ("n_kv_heads", c_int32),
+                ("head_dim", c_int32), ("ffn", c_int32), ("page_size", c_int32),
+                ("rms_eps", c_float), ("rope_theta", c_float)]
+
+
+class nf_batch_desc(Structure):
+    _fields_ = [("n_decode", c_int32), ("n_prefill", c_int32),
+                ("prefill_q_lens", POINTER(c_int32)), ("seq_lens_hint", POINTER(c_int32)),
+                ("max_pages_per_seq", c_int32), ("num_pages", c_int32)]
+
+
+class nf_plan_opts(Structure):
+    _fields_ = [("n_attn", c_int32), ("attn_bounds", c_int32 * (NF_MAX_NANO + 1)),
+                ("n_ffn", c_int32), ("ffn_bounds", c_int32 * (NF_MAX_NANO + 1)),
+                ("executor", c_int32), ("attn_sms", c_int32), ("gemm_sms", c_int32),
+                ("kv_chunk", c_int32), ("validate", c_int32), ("timeout_ns", c_int64)]
+
+
+class nf_trace_entry(Structure):
+    _fields_ = [("op", c_int32), ("nano", c_int32), ("step", c_int32), ("start_ms", c_float),
+                ("ms", c_float)]
+
+
+NF_OP_NAMES = {0: "meta", 1: "qkv", 2: "attn", 3: "oproj", 4: "ffn"}
+
+
+class nf_layer_weights(Structure):
+    _fields_ = [(n, c_void_p) for n in ("norm1", "w_qkv", "w_o", "norm2", "w_gate_up", "w_down")]
+
+
+_SIGS = {
+    "nf_plan_create": (c_int, [POINTER(nf_model_shape), POINTER(nf_batch_desc), POINTER(nf_plan_opts), POINTER(c_void_p)]),
+    "nf_plan_info": (c_int, [c_void_p, POINTER(nf_plan_opts), POINTER(c_int32)]),
+    "nf_plan_save": (c_int, [c_void_p, c_char_p]),
+    "nf_plan_load": (c_int, [c_char_p, POINTER(c_void_p)]),
+    "nf_plan_destroy": (None, [c_void_p]),
+    "nf_layer_step": (c_int, [c_void_p, POINTER(nf_layer_weights), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "nf_layer_step_host": (c_int, [c_void_p, POINTER(nf_layer_weights), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "nf_plan_poll": (c_int, [c_void_p, c_int]),
+    "nf_last_error": (c_char_p, []),
+    "nf_device_sm_count": (c_int32, []),
+    "nf_step_metadata": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p]),
+    "nf_attention": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "nf_rmsnorm": (c_int, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_float, c_void_p]),
+    "nf_gemm": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32, c_int32, c_void_p]),
+    "nf_plan_buffer_size": (c_int, [c_void_p, c_int32, POINTER(c_size_t)]),
+    "nf_plan_copy_buffer": (c_int, [c_void_p, c_int32, c_void_p, c_size_t]),
+    "nf_plan_trace_enable": (c_int, [c_void_p, c_int32]),
+    "nf_plan_trace_read": (c_int, [c_void_p, POINTER(nf_trace_entry), c_int32, POINTER(c_int32)]),
+    "nf_profile": (c_int, [POINTER(nf_model_shape), c_int32, c_int32, c_char_p]),
+    "nf_plan_search": (c_int, [POINTER(nf_model_shape), POINTER(nf_batch_desc), c_char_p, c_int32, POINTER(nf_plan_opts), POINTER(c_double)]),
+}
+
+_lib = None
+
+
+class NanoflowError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"nanoflow error {code}: {msg}")
+        self.code = code
+
+
+def header_functions() -> list:
+    """Names of the functions include/nanoflow.h declares."""
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w]+\**\s+\**\s*(nf_\w+)\s*\(", text, re.M)))
+
+
+def lib():
+    """Load the library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it first "
+                               "(python -c 'import __graft_entry__ as g; g.build()')")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def check(code):
+    if code != NF_OK:
+        raise NanoflowError(code, lib().nf_last_error().decode())
+
+
+def ptr(t):
+    """Device/host address of a torch tensor (None -> NULL)."""
+    return None if t is None else c_void_p(t.data_ptr())
+
+
+def stream_handle(stream=None):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return c_void_p(s.cuda_stream)
+
+
+def make_shape(shape) -> nf_model_shape:
+    return nf_model_shape(shape.hidden, shape.n_q, shape.n_kv, shape.head_dim, shape.ffn,
+                          shape.page_size, shape.rms_eps, shape.rope_theta)
+
+
+def make_batch_desc(batch, hint=True):
+    pq = (c_int32 * max(1, len(batch.prefill_q_lens)))(*batch.prefill_q_lens)
+    sl = (c_int32 * batch.n_seq)(*[int(v) for v in batch.seq_lens]) if hint else None
+    d = nf_batch_desc(batch.n_decode, len(batch.prefill_q_lens), pq, sl,
+                      batch.max_pages, batch.num_pages)
+    d._keep = (pq, sl)
+    return d
+
+
+def make_opts(T, attn_bounds=None, ffn_bounds=None, executor=NF_EXEC_SEQUENTIAL, attn_sms=0,
+              gemm_sms=0, kv_chunk=512, validate=0, timeout_ns=2_000_000_000) -> nf_plan_opts:
+    ab = list(attn_bounds) if attn_bounds is not None else [0, T]
+    fb = list(ffn_bounds) if ffn_bounds is not None else list(ab)
+    o = nf_plan_opts()
+    o.n_attn = len(ab) - 1
+    for i, v in enumerate(ab):
+        o.attn_bounds[i] = v
+    o.n_ffn = len(fb) - 1
+    for i, v in enumerate(fb):
+        o.ffn_bounds[i] = v
+    o.executor, o.attn_sms, o.gemm_sms = executor, attn_sms, gemm_sms
+    o.kv_chunk, o.validate, o.timeout_ns = kv_chunk, validate, timeout_ns
+    return o
+
+
+def opts_dict(o: nf_plan_opts) -> dict:
+    return {"attn_bounds": list(o.attn_bounds[: o.n_attn + 1]),
+            "ffn_bounds": list(o.ffn_bounds[: o.n_ffn + 1]),
+            "executor": "streams" if o.executor == NF_EXEC_STREAMS else "sequential",
+            "attn_sms": o.attn_sms, "gemm_sms": o.gemm_sms, "kv_chunk": o.kv_chunk}
+
+
+def make_weights_struct(w: dict) -> nf_layer_weights:
+    return nf_layer_weights(*[w[k].data_ptr() for k in
+                              ("norm1", "w_qkv", "w_o", "norm2", "w_gate_up", "w_down")])
+
+
+class Plan:
+    """Owns an nf_plan."""
+
+    def __init__(self, shape, batch, opts: nf_plan_opts | None = None, hint=True):
+        self.h = c_void_p()
+        self._shape = make_shape(shape)
+        self._batch = make_batch_desc(batch, hint)
+        check(lib().nf_plan_create(ctypes.byref(self._shape), ctypes.byref(self._batch),
+                                   ctypes.byref(opts) if opts is not None else None,
+                                   ctypes.byref(self.h)))
+
+    @classmethod
+    def from_handle(cls, handle):
+        p = cls.__new__(cls)
+        p.h = handle
+        return p
+
+    def info(self):
+        o = nf_plan_opts()
+        n = c_int32()
+        check(lib().nf_plan_info(self.h, ctypes.byref(o), ctypes.byref(n)))
+        return o, n.value
+
+    def close(self):
+        if self.h:
+            lib().nf_plan_destroy(self.h)
+            self.h = c_void_p()
+
+    def __del__(self):  # pragma: no cover
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def buffer(self, which, dtype, shape):
+        import torch
+        out = torch.empty(shape, dtype=dtype)
+        check(lib().nf_plan_copy_buffer(self.h, which, ptr(out), out.numel() * out.element_size()))
+        return out
+
+    def trace_enable(self, max_steps):
+        check(lib().nf_plan_trace_enable(self.h, max_steps))
+
+    def trace_read(self):
+        n = c_int32()
+        check(lib().nf_plan_trace_read(self.h, None, 0, ctypes.byref(n)))
+        buf = (nf_trace_entry * max(1, n.value))()
+        check(lib().nf_plan_trace_read(self.h, buf, n.value, ctypes.byref(n)))
+        return [{"op": NF_OP_NAMES.get(e.op, str(e.op)), "nano": e.nano, "step": e.step,
+                 "start_ms": e.start_ms, "ms": e.ms} for e in buf[: n.value]]
+
+    def poll(self, wait=True):
+        check(lib().nf_plan_poll(self.h, 1 if wait else 0))
+
+
+def layer_step(plan: Plan, w: dict, x, k_pool, v_pool, block_table, seq_lens, y, stream=None):
+    ws = make_weights_struct(w)
+    check(lib().nf_layer_step(plan.h, ctypes.byref(ws), ptr(x), ptr(k_pool), ptr(v_pool),
+                              ptr(block_table), ptr(seq_lens), ptr(y), stream_handle(stream)))
+
+
+def layer_step_host(plan: Plan, w: dict, x_host, k_pool, v_pool, bt_host, sl_host, y_host, stream=None):
+    ws = make_weights_struct(w)
+    check(lib().nf_layer_step_host(plan.h, ctypes.byref(ws), ptr(x_host), ptr(k_pool), ptr(v_pool),
+                                   ptr(bt_host), ptr(sl_host), ptr(y_host), stream_handle(stream)))
+
+
+def step_metadata(plan: Plan, block_table, seq_lens, stream=None):
+    check(lib().nf_step_metadata(plan.h, ptr(block_table), ptr(seq_lens), stream_handle(stream)))
+
+
+def attention(plan: Plan, q, k_pool, v_pool, block_table, seq_lens, o, stream=None):
+    check(lib().nf_attention(plan.h, ptr(q), ptr(k_pool), ptr(v_pool), ptr(block_table),
+                             ptr(seq_lens), ptr(o), stream_handle(stream)))
+
+
+def rmsnorm(x, g, out, eps, stream=None):
+    check(lib().nf_rmsnorm(ptr(x), ptr(g), ptr(out), x.shape[0], x.shape[1], eps, stream_handle(stream)))
+
+
+def gemm(A, B, C, R=None, epilogue=NF_EPI_STORE, max_sms=0, stream=None):
+    M, K = A.shape
+    N = C.shape[1]
+    check(lib().nf_gemm(ptr(A), ptr(B), ptr(C), ptr(R), M, N, K, epilogue, max_sms,
+                        stream_handle(stream)))
+
+
+def plan_search(shape, batch, profile_json=None, num_sms=152):
+    o = nf_plan_opts()
+    t = c_double()
+    s = make_shape(shape)
+    b = make_batch_desc(batch, True)
+    check(lib().nf_plan_search(ctypes.byref(s), ctypes.byref(b),
+                               profile_json.encode() if profile_json else None, num_sms,
+                               ctypes.byref(o), ctypes.byref(t)))
+    return o, t.value
+
+
+def device_sm_count():
+    return lib().nf_device_sm_count()

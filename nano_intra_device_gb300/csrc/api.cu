@@ -1,0 +1,875 @@
+// C ABI of the nano-batched decoder-layer step: plans, executors, single-step
+// entry points.  Host code; every arithmetic step runs in the kernels.
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/nanoflow.h"
+#include "common.cuh"
+#include "kernels.h"
+
+using nf::GemmArgs;
+
+namespace {
+
+thread_local std::string g_err;
+
+nf_status fail(nf_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return s;
+}
+
+#define NF_CUDA(call)                                                                   \
+  do {                                                                                  \
+    cudaError_t e_ = (call);                                                            \
+    if (e_ != cudaSuccess)                                                              \
+      return fail(NF_ERR_CUDA, "%s failed: %s", #call, cudaGetErrorString(e_));         \
+  } while (0)
+
+int device_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+// Status word for entry points that run without a plan (nf_gemm, nf_rmsnorm).
+uint32_t* global_status() {
+  static uint32_t* p = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    if (cudaMalloc(&p, sizeof(uint32_t)) == cudaSuccess) cudaMemset(p, 0, sizeof(uint32_t));
+  });
+  return p;
+}
+
+constexpr int64_t kDefaultTimeoutNs = 2000000000LL;
+
+}  // namespace
+
+struct nf_plan_s {
+  nf_model_shape shape{};
+  int n_decode = 0, n_prefill = 0;
+  std::vector<int> prefill_q, seq_hint;
+  int max_pages = 0, num_pages = 0;
+  int n_seq = 0, T = 0;
+  std::vector<int> q_lens, tok_begin;
+  nf_plan_opts opts{};
+  int num_sms = 0;
+  int max_chunks = 0, item_capacity = 0;
+  // device workspace
+  int *d_q_lens = nullptr, *d_tok_begin = nullptr, *d_seg_bounds = nullptr;
+  int *tok_seq = nullptr, *tok_pos = nullptr, *tok_slot = nullptr, *tok_nchunks = nullptr;
+  int *items = nullptr, *seg_items = nullptr, *fetch = nullptr, *row_done = nullptr;
+  float* partials = nullptr;
+  uint32_t* status = nullptr;
+  __nv_bfloat16 *n1 = nullptr, *q = nullptr, *o = nullptr, *h = nullptr, *n2 = nullptr,
+                *a = nullptr;
+  // host-API staging
+  __nv_bfloat16 *x_stage = nullptr, *y_stage = nullptr;
+  int *bt_stage = nullptr, *sl_stage = nullptr;
+  // executor
+  cudaStream_t s_gemm = nullptr, s_attn = nullptr;
+  std::vector<cudaEvent_t> ev;
+  // tensor maps over plan buffers (A operands)
+  CUtensorMap tm_n1{}, tm_o{}, tm_n2{}, tm_a{};
+  // tensor maps over the weights, rebuilt when the pointers change
+  const void* wkey[4] = {nullptr, nullptr, nullptr, nullptr};
+  CUtensorMap tm_wqkv{}, tm_wo{}, tm_wg{}, tm_wu{}, tm_wd{};
+  // tracing
+  struct TraceRec {
+    int op, nano, step;
+    cudaEvent_t b, e, s0;
+  };
+  int trace_left = 0, trace_step = 0;
+  cudaEvent_t trace_s0 = nullptr;
+  std::vector<TraceRec> trace;
+  std::vector<cudaEvent_t> ev_pool;
+};
+
+namespace {
+
+size_t buf_bytes(nf_plan p, int which) {
+  const size_t T = p->T, H = p->shape.hidden, QD = (size_t)p->shape.n_q_heads * p->shape.head_dim;
+  switch (which) {
+    case NF_BUF_TOK_SEQ:
+    case NF_BUF_TOK_POS:
+    case NF_BUF_TOK_SLOT: return T * 4;
+    case NF_BUF_ITEMS: return (size_t)p->item_capacity * 2 * 4;
+    case NF_BUF_ITEM_SEG: return (size_t)(p->opts.n_attn + 1) * 4;
+    case NF_BUF_N1:
+    case NF_BUF_H:
+    case NF_BUF_N2: return T * H * 2;
+    case NF_BUF_Q:
+    case NF_BUF_O: return T * QD * 2;
+    case NF_BUF_A: return T * (size_t)p->shape.ffn * 2;
+    default: return 0;
+  }
+}
+
+const void* buf_ptr(nf_plan p, int which) {
+  switch (which) {
+    case NF_BUF_TOK_SEQ: return p->tok_seq;
+    case NF_BUF_TOK_POS: return p->tok_pos;
+    case NF_BUF_TOK_SLOT: return p->tok_slot;
+    case NF_BUF_ITEMS: return p->items;
+    case NF_BUF_ITEM_SEG: return p->seg_items;
+    case NF_BUF_N1: return p->n1;
+    case NF_BUF_Q: return p->q;
+    case NF_BUF_O: return p->o;
+    case NF_BUF_H: return p->h;
+    case NF_BUF_N2: return p->n2;
+    case NF_BUF_A: return p->a;
+    default: return nullptr;
+  }
+}
+
+nf_status check_shape(const nf_model_shape* s) {
+  if (!s) return fail(NF_ERR_INVALID_ARG, "shape is NULL");
+  if (s->hidden <= 0 || s->hidden % 64)
+    return fail(NF_ERR_INVALID_ARG, "hidden must be a positive multiple of 64 (got %d)", s->hidden);
+  if (s->ffn <= 0 || s->ffn % 64)
+    return fail(NF_ERR_INVALID_ARG, "ffn must be a positive multiple of 64 (got %d)", s->ffn);
+  if (s->head_dim != 64 && s->head_dim != 128)
+    return fail(NF_ERR_INVALID_ARG, "head_dim must be 64 or 128 (got %d)", s->head_dim);
+  if (s->n_kv_heads <= 0 || s->n_q_heads <= 0 || s->n_q_heads % s->n_kv_heads)
+    return fail(NF_ERR_INVALID_ARG, "n_q_heads must be a positive multiple of n_kv_heads");
+  const int grp = s->n_q_heads / s->n_kv_heads;
+  if (grp != 1 && grp != 2 && grp != 4 && grp != 8)
+    return fail(NF_ERR_INVALID_ARG, "n_q_heads / n_kv_heads must be 1, 2, 4 or 8 (got %d)", grp);
+  if (s->page_size != 16) return fail(NF_ERR_INVALID_ARG, "page_size must be 16 (got %d)", s->page_size);
+  if (!(s->rms_eps >= 0.f) || !(s->rope_theta > 0.f))
+    return fail(NF_ERR_INVALID_ARG, "rms_eps must be >= 0 and rope_theta > 0");
+  return NF_OK;
+}
+
+nf_status check_opts(const nf_plan_opts* o, int T, int num_sms) {
+  for (int grp = 0; grp < 2; ++grp) {
+    const int n = grp ? o->n_ffn : o->n_attn;
+    const int32_t* b = grp ? o->ffn_bounds : o->attn_bounds;
+    if (n < 1 || n > NF_MAX_NANO)
+      return fail(NF_ERR_INVALID_ARG, "nano-batch count must be 1..%d (got %d)", NF_MAX_NANO, n);
+    if (b[0] != 0 || b[n] != T)
+      return fail(NF_ERR_INVALID_ARG, "nano-batch bounds must run from 0 to T=%d", T);
+    for (int i = 0; i < n; ++i)
+      if (b[i + 1] <= b[i]) return fail(NF_ERR_INVALID_ARG, "nano-batch bounds must increase");
+  }
+  if (o->executor != NF_EXEC_SEQUENTIAL && o->executor != NF_EXEC_STREAMS)
+    return fail(NF_ERR_INVALID_ARG, "unknown executor %d", o->executor);
+  if (o->kv_chunk < 16 || o->kv_chunk > 2048 || o->kv_chunk % 16)
+    return fail(NF_ERR_INVALID_ARG, "kv_chunk must be a multiple of 16 in [16, 2048]");
+  if (o->attn_sms < 0 || o->attn_sms > num_sms || o->gemm_sms < 0 || o->gemm_sms > num_sms)
+    return fail(NF_ERR_INVALID_ARG, "SM shares must lie in [0, %d]", num_sms);
+  if (o->timeout_ns <= 0) return fail(NF_ERR_INVALID_ARG, "timeout_ns must be positive");
+  return NF_OK;
+}
+
+void free_plan(nf_plan p) {
+  if (!p) return;
+  void* bufs[] = {p->d_q_lens, p->d_tok_begin, p->d_seg_bounds, p->tok_seq, p->tok_pos,
+                  p->tok_slot, p->tok_nchunks, p->items, p->seg_items, p->fetch, p->row_done,
+                  p->partials, p->status, p->n1, p->q, p->o, p->h, p->n2, p->a, p->x_stage,
+                  p->y_stage, p->bt_stage, p->sl_stage};
+  for (void* b : bufs)
+    if (b) cudaFree(b);
+  for (cudaEvent_t e : p->ev) cudaEventDestroy(e);
+  for (auto& r : p->trace) {
+    cudaEventDestroy(r.b);
+    cudaEventDestroy(r.e);
+  }
+  std::vector<cudaEvent_t> s0s;
+  for (auto& r : p->trace)
+    if (std::find(s0s.begin(), s0s.end(), r.s0) == s0s.end()) s0s.push_back(r.s0);
+  for (cudaEvent_t e : s0s) cudaEventDestroy(e);
+  for (cudaEvent_t e : p->ev_pool) cudaEventDestroy(e);
+  if (p->s_gemm) cudaStreamDestroy(p->s_gemm);
+  if (p->s_attn) cudaStreamDestroy(p->s_attn);
+  delete p;
+}
+
+template <typename T>
+nf_status dalloc(T** ptr, size_t bytes) {
+  if (bytes == 0) bytes = 16;
+  if (cudaMalloc(reinterpret_cast<void**>(ptr), bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(NF_ERR_OOM, "cudaMalloc of %zu bytes failed", bytes);
+  }
+  return NF_OK;
+}
+
+#define NF_TRY(expr)                \
+  do {                              \
+    nf_status s_ = (expr);          \
+    if (s_ != NF_OK) return s_;     \
+  } while (0)
+
+nf_status alloc_plan(nf_plan p) {
+  const size_t T = p->T, H = p->shape.hidden, F = p->shape.ffn;
+  const size_t QD = (size_t)p->shape.n_q_heads * p->shape.head_dim;
+  p->max_chunks = (p->max_pages * p->shape.page_size + p->opts.kv_chunk - 1) / p->opts.kv_chunk;
+  p->item_capacity = p->T * p->max_chunks;
+  const size_t rec = nf::attn_partial_floats(p->shape.n_q_heads, p->shape.n_kv_heads,
+                                             p->shape.head_dim);
+  NF_TRY(dalloc(&p->d_q_lens, p->n_seq * 4));
+  NF_TRY(dalloc(&p->d_tok_begin, (p->n_seq + 1) * 4));
+  NF_TRY(dalloc(&p->d_seg_bounds, (NF_MAX_NANO + 1) * 4));
+  NF_TRY(dalloc(&p->tok_seq, T * 4));
+  NF_TRY(dalloc(&p->tok_pos, T * 4));
+  NF_TRY(dalloc(&p->tok_slot, T * 4));
+  NF_TRY(dalloc(&p->tok_nchunks, T * 4));
+  NF_TRY(dalloc(&p->items, (size_t)p->item_capacity * 8));
+  NF_TRY(dalloc(&p->seg_items, (NF_MAX_NANO + 1) * 4));
+  NF_TRY(dalloc(&p->fetch, NF_MAX_NANO * 4));
+  NF_TRY(dalloc(&p->row_done, T * p->shape.n_kv_heads * 4));
+  NF_TRY(dalloc(&p->partials, T * p->max_chunks * p->shape.n_kv_heads * rec * 4));
+  NF_TRY(dalloc(&p->status, 4));
+  NF_TRY(dalloc(&p->n1, T * H * 2));
+  NF_TRY(dalloc(&p->q, T * QD * 2));
+  NF_TRY(dalloc(&p->o, T * QD * 2));
+  NF_TRY(dalloc(&p->h, T * H * 2));
+  NF_TRY(dalloc(&p->n2, T * H * 2));
+  NF_TRY(dalloc(&p->a, T * F * 2));
+  NF_CUDA(cudaMemset(p->status, 0, 4));
+  NF_CUDA(cudaMemcpy(p->d_q_lens, p->q_lens.data(), p->n_seq * 4, cudaMemcpyHostToDevice));
+  NF_CUDA(cudaMemcpy(p->d_tok_begin, p->tok_begin.data(), (p->n_seq + 1) * 4,
+                     cudaMemcpyHostToDevice));
+  NF_CUDA(cudaMemcpy(p->d_seg_bounds, p->opts.attn_bounds, (p->opts.n_attn + 1) * 4,
+                     cudaMemcpyHostToDevice));
+  NF_CUDA(cudaStreamCreateWithFlags(&p->s_gemm, cudaStreamNonBlocking));
+  NF_CUDA(cudaStreamCreateWithFlags(&p->s_attn, cudaStreamNonBlocking));
+  p->ev.resize(2 + 2 * NF_MAX_NANO);
+  for (auto& e : p->ev) NF_CUDA(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+  const int BMr = 128;
+  if (!nf::make_tmap_bf16(&p->tm_n1, p->n1, T, H, BMr) ||
+      !nf::make_tmap_bf16(&p->tm_o, p->o, T, QD, BMr) ||
+      !nf::make_tmap_bf16(&p->tm_n2, p->n2, T, H, BMr) ||
+      !nf::make_tmap_bf16(&p->tm_a, p->a, T, F, BMr))
+    return fail(NF_ERR_CUDA, "tensor map creation failed (driver entry point missing?)");
+  return NF_OK;
+}
+
+nf_status build_plan(const nf_model_shape* shape, const nf_batch_desc* batch,
+                     const nf_plan_opts* opts, nf_plan* out) {
+  if (!out) return fail(NF_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  NF_TRY(check_shape(shape));
+  if (!batch) return fail(NF_ERR_INVALID_ARG, "batch is NULL");
+  if (batch->n_decode < 0 || batch->n_prefill < 0 || batch->n_decode + batch->n_prefill < 1)
+    return fail(NF_ERR_INVALID_ARG, "batch needs at least one sequence");
+  if (batch->n_prefill > 0 && !batch->prefill_q_lens)
+    return fail(NF_ERR_INVALID_ARG, "prefill_q_lens is NULL");
+  if (batch->max_pages_per_seq < 1 || batch->num_pages < 1)
+    return fail(NF_ERR_INVALID_ARG, "max_pages_per_seq and num_pages must be >= 1");
+  const int num_sms = device_sms();
+  if (num_sms <= 0) return fail(NF_ERR_CUDA, "no CUDA device");
+
+  nf_plan p = new nf_plan_s();
+  p->shape = *shape;
+  p->n_decode = batch->n_decode;
+  p->n_prefill = batch->n_prefill;
+  p->max_pages = batch->max_pages_per_seq;
+  p->num_pages = batch->num_pages;
+  p->n_seq = batch->n_decode + batch->n_prefill;
+  p->num_sms = num_sms;
+  p->tok_begin.push_back(0);
+  for (int i = 0; i < p->n_seq; ++i) {
+    int q = 1;
+    if (i >= batch->n_decode) {
+      q = batch->prefill_q_lens[i - batch->n_decode];
+      if (q < 1) {
+        delete p;
+        return fail(NF_ERR_INVALID_ARG, "prefill_q_lens[%d] must be >= 1", i - batch->n_decode);
+      }
+      p->prefill_q.push_back(q);
+    }
+    p->q_lens.push_back(q);
+    p->tok_begin.push_back(p->tok_begin.back() + q);
+  }
+  p->T = p->tok_begin.back();
+  if (batch->seq_lens_hint) p->seq_hint.assign(batch->seq_lens_hint, batch->seq_lens_hint + p->n_seq);
+
+  if (opts) {
+    p->opts = *opts;
+  } else {
+    double pred = 0;
+    nf_status s = nf_plan_search(shape, batch, nullptr, num_sms, &p->opts, &pred);
+    if (s != NF_OK) {
+      delete p;
+      return s;
+    }
+  }
+  if (p->opts.kv_chunk == 0) p->opts.kv_chunk = 512;
+  if (p->opts.timeout_ns == 0) p->opts.timeout_ns = kDefaultTimeoutNs;
+  nf_status s = check_opts(&p->opts, p->T, num_sms);
+  if (s != NF_OK) {
+    delete p;
+    return s;
+  }
+  s = alloc_plan(p);
+  if (s != NF_OK) {
+    std::string keep = g_err;
+    free_plan(p);
+    g_err = keep;
+    return s;
+  }
+  *out = p;
+  return NF_OK;
+}
+
+nf_status refresh_weight_maps(nf_plan p, const nf_layer_weights* w) {
+  const void* key[4] = {w->w_qkv, w->w_o, w->w_gate_up, w->w_down};
+  if (std::memcmp(key, p->wkey, sizeof(key)) == 0) return NF_OK;
+  const nf_model_shape& s = p->shape;
+  const uint64_t H = s.hidden, F = s.ffn, QD = (uint64_t)s.n_q_heads * s.head_dim;
+  const uint64_t NQKV = (uint64_t)(s.n_q_heads + 2 * s.n_kv_heads) * s.head_dim;
+  const char* up = static_cast<const char*>(w->w_gate_up) + F * H * 2;
+  if (!nf::make_tmap_bf16(&p->tm_wqkv, w->w_qkv, NQKV, H, 256) ||
+      !nf::make_tmap_bf16(&p->tm_wo, w->w_o, H, QD, 256) ||
+      !nf::make_tmap_bf16(&p->tm_wg, w->w_gate_up, F, H, 128) ||
+      !nf::make_tmap_bf16(&p->tm_wu, up, F, H, 128) ||
+      !nf::make_tmap_bf16(&p->tm_wd, w->w_down, H, F, 256))
+    return fail(NF_ERR_INVALID_ARG, "weight tensor maps: pointers must be 16-byte aligned");
+  std::memcpy(p->wkey, key, sizeof(key));
+  return NF_OK;
+}
+
+GemmArgs base_args(nf_plan p) {
+  GemmArgs g{};
+  g.status = p->status;
+  g.timeout_ns = (unsigned long long)p->opts.timeout_ns;
+  g.n_q = p->shape.n_q_heads;
+  g.n_kv = p->shape.n_kv_heads;
+  g.head_dim = p->shape.head_dim;
+  g.page_size = p->shape.page_size;
+  g.log2_theta = std::log2(p->shape.rope_theta);
+  return g;
+}
+
+int cap_grid(int tiles, int cap) { return tiles < cap ? tiles : cap; }
+
+
+cudaEvent_t pooled_event(nf_plan p) {
+  cudaEvent_t e = nullptr;
+  if (!p->ev_pool.empty()) {
+    e = p->ev_pool.back();
+    p->ev_pool.pop_back();
+  } else if (cudaEventCreate(&e) != cudaSuccess) {
+    return nullptr;
+  }
+  return e;
+}
+
+// Begin/end markers around one nano-operation (no-ops unless tracing).
+struct TraceScope {
+  nf_plan p;
+  cudaStream_t st;
+  int op, nano;
+  cudaEvent_t b = nullptr;
+  TraceScope(nf_plan p_, cudaStream_t st_, int op_, int nano_) : p(p_), st(st_), op(op_), nano(nano_) {
+    if (p->trace_left > 0 && p->trace_s0) {
+      b = pooled_event(p);
+      if (b) cudaEventRecord(b, st);
+    }
+  }
+  ~TraceScope() {
+    if (!b) return;
+    cudaEvent_t e = pooled_event(p);
+    if (!e) return;
+    cudaEventRecord(e, st);
+    p->trace.push_back({op, nano, p->trace_step, b, e, p->trace_s0});
+  }
+};
+
+nf_status run_meta(nf_plan p, const int32_t* bt, const int32_t* sl, cudaStream_t st) {
+  TraceScope ts_(p, st, NF_OP_META, 0);
+  nf::MetaArgs m{};
+  m.seq_lens = sl;
+  m.block_table = bt;
+  m.q_lens = p->d_q_lens;
+  m.tok_begin = p->d_tok_begin;
+  m.seg_bounds = p->d_seg_bounds;
+  m.n_seq = p->n_seq;
+  m.n_tok = p->T;
+  m.n_seg = p->opts.n_attn;
+  m.max_pages = p->max_pages;
+  m.num_pages = p->num_pages;
+  m.page_size = p->shape.page_size;
+  m.kv_chunk = p->opts.kv_chunk;
+  m.n_kv = p->shape.n_kv_heads;
+  m.max_chunks = p->max_chunks;
+  m.item_capacity = p->item_capacity;
+  m.tok_seq = p->tok_seq;
+  m.tok_pos = p->tok_pos;
+  m.tok_slot = p->tok_slot;
+  m.tok_nchunks = p->tok_nchunks;
+  m.items = p->items;
+  m.seg_items = p->seg_items;
+  m.fetch = p->fetch;
+  m.row_done = p->row_done;
+  m.status = p->status;
+  m.validate = p->opts.validate;
+  NF_CUDA(nf::launch_meta(m, st));
+  return NF_OK;
+}
+
+nf_status run_attention(nf_plan p, int seg, const void* q, const void* kp, const void* vp,
+                        const int32_t* bt, void* o, int grid, cudaStream_t st) {
+  TraceScope ts_(p, st, NF_OP_ATTN, seg);
+  nf::AttnArgs a{};
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.k_pool = static_cast<const __nv_bfloat16*>(kp);
+  a.v_pool = static_cast<const __nv_bfloat16*>(vp);
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.block_table = bt;
+  a.tok_seq = p->tok_seq;
+  a.tok_pos = p->tok_pos;
+  a.tok_nchunks = p->tok_nchunks;
+  a.items = p->items;
+  a.seg_items = p->seg_items;
+  a.fetch = p->fetch;
+  a.row_done = p->row_done;
+  a.partials = p->partials;
+  a.seg = seg;
+  a.n_q = p->shape.n_q_heads;
+  a.n_kv = p->shape.n_kv_heads;
+  a.head_dim = p->shape.head_dim;
+  a.page_size = p->shape.page_size;
+  a.max_pages = p->max_pages;
+  a.num_pages = p->num_pages;
+  a.kv_chunk = p->opts.kv_chunk;
+  a.max_chunks = p->max_chunks;
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p->shape.head_dim));
+  a.status = p->status;
+  a.timeout_ns = (unsigned long long)p->opts.timeout_ns;
+  NF_CUDA(nf::launch_attention(a, grid, st));
+  return NF_OK;
+}
+
+// One nano-operation of the layer; which = 0 QKV, 1 O, 2 RMSNorm-2 + gate/up + down.
+nf_status run_qkv(nf_plan p, const nf_layer_weights* w, const void* x, void* kp, void* vp, int r0,
+                  int r1, int grid, cudaStream_t st, int nano = 0) {
+  TraceScope ts_(p, st, NF_OP_QKV, nano);
+  const nf_model_shape& s = p->shape;
+  NF_CUDA(nf::launch_rmsnorm(static_cast<const __nv_bfloat16*>(x),
+                             static_cast<const __nv_bfloat16*>(w->norm1), p->n1, r0, r1, s.hidden,
+                             s.rms_eps, st));
+  GemmArgs g = base_args(p);
+  g.m_begin = r0;
+  g.m_end = r1;
+  g.N = (s.n_q_heads + 2 * s.n_kv_heads) * s.head_dim;
+  g.K = s.hidden;
+  g.m_tiles = (r1 - r0 + 127) / 128;
+  g.n_tiles = (g.N + 255) / 256;
+  g.tok_pos = p->tok_pos;
+  g.tok_slot = p->tok_slot;
+  g.q_out = p->q;
+  g.k_pool = static_cast<__nv_bfloat16*>(kp);
+  g.v_pool = static_cast<__nv_bfloat16*>(vp);
+  NF_CUDA(nf::launch_gemm(nf::EPI_QKV, p->tm_n1, p->tm_wqkv, p->tm_wqkv, g,
+                          cap_grid(g.m_tiles * g.n_tiles, grid), st));
+  return NF_OK;
+}
+
+nf_status run_oproj(nf_plan p, const void* x, int r0, int r1, int grid, cudaStream_t st,
+                    int nano = 0) {
+  TraceScope ts_(p, st, NF_OP_OPROJ, nano);
+  const nf_model_shape& s = p->shape;
+  GemmArgs g = base_args(p);
+  g.m_begin = r0;
+  g.m_end = r1;
+  g.N = s.hidden;
+  g.K = s.n_q_heads * s.head_dim;
+  g.m_tiles = (r1 - r0 + 127) / 128;
+  g.n_tiles = (g.N + 255) / 256;
+  g.C = p->h;
+  g.ldc = s.hidden;
+  g.R = static_cast<const __nv_bfloat16*>(x);
+  g.ldr = s.hidden;
+  NF_CUDA(nf::launch_gemm(nf::EPI_RESID, p->tm_o, p->tm_wo, p->tm_wo, g,
+                          cap_grid(g.m_tiles * g.n_tiles, grid), st));
+  return NF_OK;
+}
+
+nf_status run_ffn(nf_plan p, const nf_layer_weights* w, void* y, int r0, int r1, int grid,
+                  cudaStream_t st, int nano = 0) {
+  TraceScope ts_(p, st, NF_OP_FFN, nano);
+  const nf_model_shape& s = p->shape;
+  NF_CUDA(nf::launch_rmsnorm(p->h, static_cast<const __nv_bfloat16*>(w->norm2), p->n2, r0, r1,
+                             s.hidden, s.rms_eps, st));
+  GemmArgs g = base_args(p);
+  g.m_begin = r0;
+  g.m_end = r1;
+  g.N = s.ffn;
+  g.K = s.hidden;
+  g.m_tiles = (r1 - r0 + 127) / 128;
+  g.n_tiles = (g.N + 127) / 128;
+  g.C = p->a;
+  g.ldc = s.ffn;
+  NF_CUDA(nf::launch_gemm(nf::EPI_SWIGLU, p->tm_n2, p->tm_wg, p->tm_wu, g,
+                          cap_grid(g.m_tiles * g.n_tiles, grid), st));
+  GemmArgs d = base_args(p);
+  d.m_begin = r0;
+  d.m_end = r1;
+  d.N = s.hidden;
+  d.K = s.ffn;
+  d.m_tiles = (r1 - r0 + 127) / 128;
+  d.n_tiles = (d.N + 255) / 256;
+  d.C = static_cast<__nv_bfloat16*>(y);
+  d.ldc = s.hidden;
+  d.R = p->h;
+  d.ldr = s.hidden;
+  NF_CUDA(nf::launch_gemm(nf::EPI_RESID, p->tm_a, p->tm_wd, p->tm_wd, d,
+                          cap_grid(d.m_tiles * d.n_tiles, grid), st));
+  return NF_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+nf_status check_step_args(nf_plan p, const nf_layer_weights* w, const void* x, void* kp, void* vp,
+                          const int32_t* bt, const int32_t* sl, void* y) {
+  if (!p) return fail(NF_ERR_INVALID_ARG, "plan is NULL");
+  if (!w || !w->norm1 || !w->norm2 || !w->w_qkv || !w->w_o || !w->w_gate_up || !w->w_down)
+    return fail(NF_ERR_INVALID_ARG, "a weight pointer is NULL");
+  if (!x || !y || !kp || !vp || !bt || !sl) return fail(NF_ERR_INVALID_ARG, "a pointer is NULL");
+  if (x == y) return fail(NF_ERR_INVALID_ARG, "x and y must not alias");
+  const void* ptrs[] = {x, y, kp, vp, w->norm1, w->norm2, w->w_qkv, w->w_o, w->w_gate_up, w->w_down};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return fail(NF_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  return NF_OK;
+}
+
+nf_status layer_step(nf_plan p, const nf_layer_weights* w, const void* x, void* kp, void* vp,
+                     const int32_t* bt, const int32_t* sl, void* y, cudaStream_t st) {
+  NF_TRY(refresh_weight_maps(p, w));
+  if (p->trace_left > 0) {
+    p->trace_s0 = pooled_event(p);
+    if (p->trace_s0) cudaEventRecord(p->trace_s0, st);
+  }
+  struct StepEnd {
+    nf_plan p;
+    ~StepEnd() {
+      if (p->trace_left > 0 && p->trace_s0) {
+        --p->trace_left;
+        ++p->trace_step;
+      }
+      p->trace_s0 = nullptr;
+    }
+  } step_end_{p};
+  const nf_plan_opts& o = p->opts;
+  const int all = p->num_sms;
+  if (o.executor == NF_EXEC_SEQUENTIAL) {
+    NF_TRY(run_meta(p, bt, sl, st));
+    for (int i = 0; i < o.n_attn; ++i) {
+      const int r0 = o.attn_bounds[i], r1 = o.attn_bounds[i + 1];
+      NF_TRY(run_qkv(p, w, x, kp, vp, r0, r1, all, st, i));
+      NF_TRY(run_attention(p, i, p->q, kp, vp, bt, p->o, all, st));
+      NF_TRY(run_oproj(p, x, r0, r1, all, st, i));
+    }
+    for (int j = 0; j < o.n_ffn; ++j)
+      NF_TRY(run_ffn(p, w, y, o.ffn_bounds[j], o.ffn_bounds[j + 1], all, st, j));
+    return NF_OK;
+  }
+  // Two streams: GEMM-class nano-operations on s_gemm, attention on s_attn,
+  // ordered by events on the token-range dependencies.
+  const int n = o.n_attn;
+  const int attn_grid = (n == 1) ? all : (o.attn_sms > 0 ? o.attn_sms : (all * 5) / 8);
+  const int gemm_overlap = o.gemm_sms > 0 ? o.gemm_sms : (all - attn_grid > 0 ? all - attn_grid : all);
+  cudaEvent_t ev_start = p->ev[0], ev_done = p->ev[1];
+  cudaEvent_t* ev_q = &p->ev[2];
+  cudaEvent_t* ev_a = &p->ev[2 + NF_MAX_NANO];
+  NF_CUDA(cudaEventRecord(ev_start, st));
+  NF_CUDA(cudaStreamWaitEvent(p->s_gemm, ev_start, 0));
+  NF_CUDA(cudaStreamWaitEvent(p->s_attn, ev_start, 0));
+  NF_TRY(run_meta(p, bt, sl, p->s_gemm));
+  for (int i = 0; i < n; ++i) {
+    NF_TRY(run_qkv(p, w, x, kp, vp, o.attn_bounds[i], o.attn_bounds[i + 1],
+                   i == 0 ? all : gemm_overlap, p->s_gemm, i));
+    NF_CUDA(cudaEventRecord(ev_q[i], p->s_gemm));
+  }
+  for (int i = 0; i < n; ++i) {
+    NF_CUDA(cudaStreamWaitEvent(p->s_attn, ev_q[i], 0));
+    NF_TRY(run_attention(p, i, p->q, kp, vp, bt, p->o, attn_grid, p->s_attn));
+    NF_CUDA(cudaEventRecord(ev_a[i], p->s_attn));
+  }
+  int next_ffn = 0;
+  for (int i = 0; i < n; ++i) {
+    NF_CUDA(cudaStreamWaitEvent(p->s_gemm, ev_a[i], 0));
+    const int grid = (i == n - 1) ? all : gemm_overlap;
+    NF_TRY(run_oproj(p, x, o.attn_bounds[i], o.attn_bounds[i + 1], grid, p->s_gemm, i));
+    while (next_ffn < o.n_ffn && o.ffn_bounds[next_ffn + 1] <= o.attn_bounds[i + 1]) {
+      NF_TRY(run_ffn(p, w, y, o.ffn_bounds[next_ffn], o.ffn_bounds[next_ffn + 1], grid,
+                     p->s_gemm, next_ffn));
+      ++next_ffn;
+    }
+  }
+  NF_CUDA(cudaEventRecord(ev_done, p->s_gemm));
+  NF_CUDA(cudaStreamWaitEvent(st, ev_done, 0));
+  return NF_OK;
+}
+
+}  // namespace
+
+// ============================================================== C ABI
+extern "C" {
+
+const char* nf_last_error(void) { return g_err.c_str(); }
+
+int32_t nf_device_sm_count(void) { return device_sms(); }
+
+nf_status nf_plan_create(const nf_model_shape* shape, const nf_batch_desc* batch,
+                         const nf_plan_opts* opts, nf_plan* out) {
+  g_err.clear();
+  return build_plan(shape, batch, opts, out);
+}
+
+nf_status nf_plan_info(nf_plan plan, nf_plan_opts* out, int32_t* n_tokens) {
+  if (!plan) return fail(NF_ERR_INVALID_ARG, "plan is NULL");
+  if (out) *out = plan->opts;
+  if (n_tokens) *n_tokens = plan->T;
+  return NF_OK;
+}
+
+void nf_plan_destroy(nf_plan plan) { free_plan(plan); }
+
+nf_status nf_plan_save(nf_plan p, const char* path) {
+  if (!p || !path) return fail(NF_ERR_INVALID_ARG, "plan or path is NULL");
+  FILE* f = std::fopen(path, "w");
+  if (!f) return fail(NF_ERR_INVALID_ARG, "cannot open %s", path);
+  const nf_model_shape& s = p->shape;
+  std::fprintf(f, "nanoflow-plan 1\n");
+  std::fprintf(f, "shape %d %d %d %d %d %d %.9g %.9g\n", s.hidden, s.n_q_heads, s.n_kv_heads,
+               s.head_dim, s.ffn, s.page_size, s.rms_eps, s.rope_theta);
+  std::fprintf(f, "batch %d %d %d %d\n", p->n_decode, p->n_prefill, p->max_pages, p->num_pages);
+  std::fprintf(f, "prefill");
+  for (int q : p->prefill_q) std::fprintf(f, " %d", q);
+  std::fprintf(f, "\n");
+  const nf_plan_opts& o = p->opts;
+  std::fprintf(f, "attn %d", o.n_attn);
+  for (int i = 0; i <= o.n_attn; ++i) std::fprintf(f, " %d", o.attn_bounds[i]);
+  std::fprintf(f, "\nffn %d", o.n_ffn);
+  for (int i = 0; i <= o.n_ffn; ++i) std::fprintf(f, " %d", o.ffn_bounds[i]);
+  std::fprintf(f, "\nexec %d %d %d %d %d %lld\n", o.executor, o.attn_sms, o.gemm_sms, o.kv_chunk,
+               o.validate, (long long)o.timeout_ns);
+  std::fclose(f);
+  return NF_OK;
+}
+
+nf_status nf_plan_load(const char* path, nf_plan* out) {
+  if (!path || !out) return fail(NF_ERR_INVALID_ARG, "path or out is NULL");
+  FILE* f = std::fopen(path, "r");
+  if (!f) return fail(NF_ERR_INVALID_ARG, "cannot open %s", path);
+  nf_model_shape s{};
+  nf_plan_opts o{};
+  int nd = 0, np = 0, mp = 0, npg = 0, ver = 0;
+  long long tmo = 0;
+  std::vector<int> pq;
+  bool ok = std::fscanf(f, " nanoflow-plan %d", &ver) == 1 && ver == 1;
+  ok = ok && std::fscanf(f, " shape %d %d %d %d %d %d %f %f", &s.hidden, &s.n_q_heads,
+                         &s.n_kv_heads, &s.head_dim, &s.ffn, &s.page_size, &s.rms_eps,
+                         &s.rope_theta) == 8;
+  ok = ok && std::fscanf(f, " batch %d %d %d %d", &nd, &np, &mp, &npg) == 4;
+  ok = ok && std::fscanf(f, " prefill") == 0;
+  for (int i = 0; ok && i < np; ++i) {
+    int q = 0;
+    ok = std::fscanf(f, " %d", &q) == 1;
+    pq.push_back(q);
+  }
+  ok = ok && std::fscanf(f, " attn %d", &o.n_attn) == 1 && o.n_attn >= 1 && o.n_attn <= NF_MAX_NANO;
+  for (int i = 0; ok && i <= o.n_attn; ++i) ok = std::fscanf(f, " %d", &o.attn_bounds[i]) == 1;
+  ok = ok && std::fscanf(f, " ffn %d", &o.n_ffn) == 1 && o.n_ffn >= 1 && o.n_ffn <= NF_MAX_NANO;
+  for (int i = 0; ok && i <= o.n_ffn; ++i) ok = std::fscanf(f, " %d", &o.ffn_bounds[i]) == 1;
+  ok = ok && std::fscanf(f, " exec %d %d %d %d %d %lld", &o.executor, &o.attn_sms, &o.gemm_sms,
+                         &o.kv_chunk, &o.validate, &tmo) == 6;
+  std::fclose(f);
+  if (!ok) return fail(NF_ERR_INVALID_ARG, "%s is not a plan file", path);
+  o.timeout_ns = tmo;
+  nf_batch_desc b{};
+  b.n_decode = nd;
+  b.n_prefill = np;
+  b.prefill_q_lens = pq.data();
+  b.max_pages_per_seq = mp;
+  b.num_pages = npg;
+  return nf_plan_create(&s, &b, &o, out);
+}
+
+nf_status nf_layer_step(nf_plan plan, const nf_layer_weights* w, const void* x, void* k_pool,
+                        void* v_pool, const int32_t* block_table, const int32_t* seq_lens, void* y,
+                        void* stream) {
+  NF_TRY(check_step_args(plan, w, x, k_pool, v_pool, block_table, seq_lens, y));
+  return layer_step(plan, w, x, k_pool, v_pool, block_table, seq_lens, y,
+                    static_cast<cudaStream_t>(stream));
+}
+
+nf_status nf_layer_step_host(nf_plan p, const nf_layer_weights* w, const void* x_host,
+                             void* k_pool, void* v_pool, const int32_t* bt_host,
+                             const int32_t* sl_host, void* y_host, void* stream) {
+  if (!p) return fail(NF_ERR_INVALID_ARG, "plan is NULL");
+  if (!x_host || !y_host || !bt_host || !sl_host)
+    return fail(NF_ERR_INVALID_ARG, "a host pointer is NULL");
+  const size_t xb = (size_t)p->T * p->shape.hidden * 2;
+  const size_t btb = (size_t)p->n_seq * p->max_pages * 4, slb = (size_t)p->n_seq * 4;
+  if (!p->x_stage) {
+    NF_TRY(dalloc(&p->x_stage, xb));
+    NF_TRY(dalloc(&p->y_stage, xb));
+    NF_TRY(dalloc(&p->bt_stage, btb));
+    NF_TRY(dalloc(&p->sl_stage, slb));
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  NF_CUDA(cudaMemcpyAsync(p->x_stage, x_host, xb, cudaMemcpyHostToDevice, st));
+  NF_CUDA(cudaMemcpyAsync(p->bt_stage, bt_host, btb, cudaMemcpyHostToDevice, st));
+  NF_CUDA(cudaMemcpyAsync(p->sl_stage, sl_host, slb, cudaMemcpyHostToDevice, st));
+  NF_TRY(check_step_args(p, w, p->x_stage, k_pool, v_pool, p->bt_stage, p->sl_stage, p->y_stage));
+  NF_TRY(layer_step(p, w, p->x_stage, k_pool, v_pool, p->bt_stage, p->sl_stage, p->y_stage, st));
+  NF_CUDA(cudaMemcpyAsync(y_host, p->y_stage, xb, cudaMemcpyDeviceToHost, st));
+  NF_CUDA(cudaStreamSynchronize(st));
+  return NF_OK;
+}
+
+nf_status nf_plan_poll(nf_plan p, int wait) {
+  if (!p) return fail(NF_ERR_INVALID_ARG, "plan is NULL");
+  if (wait) NF_CUDA(cudaDeviceSynchronize());
+  NF_CUDA(cudaGetLastError());
+  uint32_t st = 0;
+  NF_CUDA(cudaMemcpy(&st, p->status, 4, cudaMemcpyDeviceToHost));
+  if (st) NF_CUDA(cudaMemset(p->status, 0, 4));
+  if (st & nf::ST_TIMEOUT) return fail(NF_ERR_TIMEOUT, "a device wait timed out (status 0x%x)", st);
+  if (st) return fail(NF_ERR_DEVICE, "device-side check failed (status 0x%x: %s%s%s)", st,
+                      (st & nf::ST_BAD_PAGE) ? "page id out of range " : "",
+                      (st & nf::ST_BAD_LEN) ? "bad sequence length " : "",
+                      (st & nf::ST_OVERFLOW) ? "work list overflow" : "");
+  return NF_OK;
+}
+
+nf_status nf_step_metadata(nf_plan p, const int32_t* bt, const int32_t* sl, void* stream) {
+  if (!p || !bt || !sl) return fail(NF_ERR_INVALID_ARG, "NULL argument");
+  return run_meta(p, bt, sl, static_cast<cudaStream_t>(stream));
+}
+
+nf_status nf_attention(nf_plan p, const void* q, const void* kp, const void* vp,
+                       const int32_t* bt, const int32_t* sl, void* o, void* stream) {
+  if (!p || !q || !kp || !vp || !bt || !sl || !o) return fail(NF_ERR_INVALID_ARG, "NULL argument");
+  if (!aligned16(q) || !aligned16(kp) || !aligned16(vp) || !aligned16(o))
+    return fail(NF_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  NF_TRY(run_meta(p, bt, sl, st));
+  for (int i = 0; i < p->opts.n_attn; ++i)
+    NF_TRY(run_attention(p, i, q, kp, vp, bt, o, p->num_sms, st));
+  return NF_OK;
+}
+
+nf_status nf_rmsnorm(const void* x, const void* g, void* out, int32_t rows, int32_t hidden,
+                     float eps, void* stream) {
+  if (!x || !g || !out) return fail(NF_ERR_INVALID_ARG, "NULL argument");
+  if (rows < 0 || hidden <= 0 || hidden % 8)
+    return fail(NF_ERR_INVALID_ARG, "hidden must be a positive multiple of 8");
+  if (!aligned16(x) || !aligned16(g) || !aligned16(out))
+    return fail(NF_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  NF_CUDA(nf::launch_rmsnorm(static_cast<const __nv_bfloat16*>(x),
+                             static_cast<const __nv_bfloat16*>(g),
+                             static_cast<__nv_bfloat16*>(out), 0, rows, hidden, eps,
+                             static_cast<cudaStream_t>(stream)));
+  return NF_OK;
+}
+
+nf_status nf_gemm(const void* A, const void* B, void* C, const void* R, int32_t M, int32_t N,
+                  int32_t K, int32_t epilogue, int32_t max_sms, void* stream) {
+  if (!A || !B || !C) return fail(NF_ERR_INVALID_ARG, "NULL argument");
+  if (M < 1 || N < 8 || K < 8 || N % 8 || K % 8)
+    return fail(NF_ERR_INVALID_ARG, "need M >= 1 and N, K positive multiples of 8");
+  if (epilogue < NF_EPI_STORE || epilogue > NF_EPI_SWIGLU)
+    return fail(NF_ERR_INVALID_ARG, "unknown epilogue %d", epilogue);
+  if (epilogue == NF_EPI_RESID && !R) return fail(NF_ERR_INVALID_ARG, "residual R is NULL");
+  if (!aligned16(A) || !aligned16(B) || !aligned16(C) || (R && !aligned16(R)))
+    return fail(NF_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  const int sms = device_sms();
+  if (sms <= 0) return fail(NF_ERR_CUDA, "no CUDA device");
+  CUtensorMap ta, tb, tb2;
+  bool ok = nf::make_tmap_bf16(&ta, A, M, K, 128);
+  if (epilogue == NF_EPI_SWIGLU) {
+    ok = ok && nf::make_tmap_bf16(&tb, B, N, K, 128) &&
+         nf::make_tmap_bf16(&tb2, static_cast<const char*>(B) + (size_t)N * K * 2, N, K, 128);
+  } else {
+    ok = ok && nf::make_tmap_bf16(&tb, B, N, K, 256);
+    tb2 = tb;
+  }
+  if (!ok) return fail(NF_ERR_CUDA, "tensor map creation failed");
+  GemmArgs g{};
+  g.m_begin = 0;
+  g.m_end = M;
+  g.N = N;
+  g.K = K;
+  g.m_tiles = (M + 127) / 128;
+  g.n_tiles = (N + nf::gemm_block_n(epilogue) - 1) / nf::gemm_block_n(epilogue);
+  g.C = static_cast<__nv_bfloat16*>(C);
+  g.ldc = N;
+  g.R = static_cast<const __nv_bfloat16*>(R);
+  g.ldr = N;
+  g.status = global_status();
+  g.timeout_ns = kDefaultTimeoutNs;
+  const int cap = (max_sms > 0 && max_sms < sms) ? max_sms : sms;
+  NF_CUDA(nf::launch_gemm(epilogue, ta, tb, tb2, g, cap_grid(g.m_tiles * g.n_tiles, cap),
+                          static_cast<cudaStream_t>(stream)));
+  return NF_OK;
+}
+
+nf_status nf_plan_trace_enable(nf_plan p, int32_t max_steps) {
+  if (!p || max_steps < 0) return fail(NF_ERR_INVALID_ARG, "bad argument");
+  NF_CUDA(cudaDeviceSynchronize());
+  std::vector<cudaEvent_t> s0s;
+  for (auto& r : p->trace) {
+    p->ev_pool.push_back(r.b);
+    p->ev_pool.push_back(r.e);
+    if (std::find(s0s.begin(), s0s.end(), r.s0) == s0s.end()) s0s.push_back(r.s0);
+  }
+  for (cudaEvent_t e : s0s) p->ev_pool.push_back(e);
+  p->trace.clear();
+  p->trace_left = max_steps;
+  p->trace_step = 0;
+  return NF_OK;
+}
+
+nf_status nf_plan_trace_read(nf_plan p, nf_trace_entry* out, int32_t cap, int32_t* n_out) {
+  if (!p || !n_out || (cap > 0 && !out)) return fail(NF_ERR_INVALID_ARG, "bad argument");
+  NF_CUDA(cudaDeviceSynchronize());
+  int n = 0;
+  for (auto& r : p->trace) {
+    if (n < cap) {
+      float st = 0.f, ms = 0.f;
+      NF_CUDA(cudaEventElapsedTime(&st, r.s0, r.b));
+      NF_CUDA(cudaEventElapsedTime(&ms, r.b, r.e));
+      out[n] = {r.op, r.nano, r.step, st, ms};
+    }
+    ++n;
+  }
+  *n_out = n;
+  return NF_OK;
+}
+
+nf_status nf_plan_buffer_size(nf_plan p, int32_t which, size_t* bytes) {
+  if (!p || !bytes) return fail(NF_ERR_INVALID_ARG, "NULL argument");
+  *bytes = buf_bytes(p, which);
+  if (*bytes == 0) return fail(NF_ERR_INVALID_ARG, "unknown buffer %d", which);
+  return NF_OK;
+}
+
+nf_status nf_plan_copy_buffer(nf_plan p, int32_t which, void* dst, size_t bytes) {
+  if (!p || !dst) return fail(NF_ERR_INVALID_ARG, "NULL argument");
+  const size_t have = buf_bytes(p, which);
+  if (have == 0) return fail(NF_ERR_INVALID_ARG, "unknown buffer %d", which);
+  if (bytes > have) return fail(NF_ERR_INVALID_ARG, "asked %zu bytes, buffer has %zu", bytes, have);
+  NF_CUDA(cudaDeviceSynchronize());
+  NF_CUDA(cudaMemcpy(dst, buf_ptr(p, which), bytes, cudaMemcpyDefault));
+  return NF_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,349 @@
+// Paged GQA attention over the KV cache, split-KV, one warp per work piece.
+//
+// Decode attention is the step's memory-bound operation: each request streams
+// its own K/V history, which no other token shares ("NanoFlow: Towards Optimal
+// LLM Serving Throughput", "The Intra-Device Parallelism Mechanism"; "LLM
+// Inference Performance", "PagedAttention: virtual memory for the KV cache").
+// Every token of the batch (decode or prefill) is a query row: row t of
+// sequence s at position p attends to positions 0..p of s, read through the
+// block table.
+//
+// Work: a piece = (row, chunk of kv_chunk positions, KV head).  The kernel is
+// persistent; each warp fetches pieces from a per-nano-batch counter, so a
+// grid of S CTAs (one per SM) is the SM share of the nano-operation.
+// Per piece the warp:
+//   * stages each (page, KV head) block of K and of V (P x d bf16, contiguous)
+//     into shared memory with 1-D bulk copies (TMA engine), ATT_STAGES pages in
+//     flight per warp, completion on an mbarrier;
+//   * lane (ts = lane/8, dg = lane%8) owns tokens ts, ts+4, ts+8, ts+12 of a
+//     page and the 8*NCH dims {ch*64 + dg*8 ...}: 16-byte, conflict-free loads;
+//     all GRP query heads of the KV group share every K/V read;
+//   * scores are reduced over dg with three xor-shuffles, then an online
+//     softmax (running max and sum, base 2) per page;
+//   * a piece that is a row's only chunk writes o directly; otherwise it
+//     writes (acc, m, l) and the warp that finishes the row's last piece merges
+//     them by log-sum-exp.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace nf {
+
+constexpr int ATT_WARPS = 8;
+constexpr int ATT_STAGES = 3;
+constexpr int ATT_P = 16;              // page size the kernel is built for
+constexpr int ATT_MIN_SMEM = 120 * 1024;  // > half an SM: one CTA per SM
+
+int attn_partial_floats(int n_q, int n_kv, int head_dim) {
+  const int grp = n_q / n_kv;
+  return grp * head_dim + 2 * grp;
+}
+
+int attn_smem_bytes(int head_dim, int page_size) {
+  const int blk = page_size * head_dim * 2;
+  const int need = ATT_WARPS * (ATT_STAGES * 2 * blk + ATT_STAGES * 8) + 128;
+  return need < ATT_MIN_SMEM ? ATT_MIN_SMEM : need;
+}
+
+template <int NCH>
+__device__ __forceinline__ void load_row8(const uint8_t* base, int dg, float (&out)[NCH * 8]) {
+#pragma unroll
+  for (int ch = 0; ch < NCH; ++ch) {
+    const uint4 u = *reinterpret_cast<const uint4*>(base + (ch * 64 + dg * 8) * 2);
+    out[ch * 8 + 0] = bf16lo(u.x); out[ch * 8 + 1] = bf16hi(u.x);
+    out[ch * 8 + 2] = bf16lo(u.y); out[ch * 8 + 3] = bf16hi(u.y);
+    out[ch * 8 + 4] = bf16lo(u.z); out[ch * 8 + 5] = bf16hi(u.z);
+    out[ch * 8 + 6] = bf16lo(u.w); out[ch * 8 + 7] = bf16hi(u.w);
+  }
+}
+
+template <int GRP, int NCH>
+__global__ void __launch_bounds__(ATT_WARPS * 32, 1) attn_kernel(const AttnArgs a) {
+  constexpr int D = NCH * 64;
+  constexpr int P = ATT_P;
+  constexpr int BLK = P * D * 2;  // bytes of one (page, KV head) block
+  constexpr int E = NCH * 8;      // dims per lane
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ts = lane >> 3, dg = lane & 7;
+  uint8_t* ring = smem + warp * (ATT_STAGES * 2 * BLK);
+  uint64_t* bar =
+      reinterpret_cast<uint64_t*>(smem + ATT_WARPS * ATT_STAGES * 2 * BLK) + warp * ATT_STAGES;
+  if (lane == 0) {
+    for (int s = 0; s < ATT_STAGES; ++s) mbar_init(&bar[s], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  const int seg = a.seg;
+  const int begin = a.seg_items[seg];
+  const int total = (a.seg_items[seg + 1] - begin) * a.n_kv;
+  const int n_kv = a.n_kv, n_q = a.n_q, C = a.kv_chunk;
+  const size_t page_stride = static_cast<size_t>(n_kv) * P * D;  // elements per page
+  const uint64_t policy = l2_policy_evict_first();
+  uint32_t gk = 0;  // pages this warp has consumed (ring position)
+  bool failed = false;
+
+  for (;;) {
+    int idx = 0;
+    if (lane == 0) idx = atomicAdd(&a.fetch[seg], 1);
+    idx = __shfl_sync(0xffffffffu, idx, 0);
+    if (idx >= total) break;
+    const int pair = begin + idx / n_kv, g = idx % n_kv;
+    const int t = a.items[2 * pair], c = a.items[2 * pair + 1];
+    const int s = a.tok_seq[t];
+    const int ctx = a.tok_pos[t] + 1;
+    const int b0 = c * C;
+    const int n = min(C, ctx - b0);
+    const int npg = (n + P - 1) / P;
+    const int* bt = a.block_table + static_cast<size_t>(s) * a.max_pages + b0 / P;
+
+    auto issue = [&](int k) {
+      const uint32_t st = (gk + k) % ATT_STAGES;
+      int page = bt[k];
+      if (page < 0 || page >= a.num_pages) {  // never read outside the pool
+        raise_status(a.status, ST_BAD_PAGE);
+        page = 0;
+      }
+      const size_t off = static_cast<size_t>(page) * page_stride + static_cast<size_t>(g) * P * D;
+      uint8_t* kb = ring + st * 2 * BLK;
+      mbar_arrive_expect_tx(&bar[st], 2 * BLK);
+      bulk_g2s_evict_first(kb, a.k_pool + off, BLK, &bar[st], policy);
+      bulk_g2s_evict_first(kb + BLK, a.v_pool + off, BLK, &bar[st], policy);
+    };
+    int issued = 0;  // pages of this piece whose copies were started (lane 0)
+    if (lane == 0) {
+      const int pre = npg < ATT_STAGES ? npg : ATT_STAGES;
+      for (int k = 0; k < pre; ++k) issue(k);
+      issued = pre;
+    }
+
+    // q of the GRP heads of this KV group, scaled to base-2 logits
+    float qv[GRP][E];
+#pragma unroll
+    for (int h = 0; h < GRP; ++h) {
+      const uint8_t* qrow = reinterpret_cast<const uint8_t*>(
+          a.q + (static_cast<size_t>(t) * n_q + g * GRP + h) * D);
+      load_row8<NCH>(qrow, dg, qv[h]);
+#pragma unroll
+      for (int e = 0; e < E; ++e) qv[h][e] *= a.scale_log2;
+    }
+    float m[GRP], l[GRP], acc[GRP][E];
+#pragma unroll
+    for (int h = 0; h < GRP; ++h) {
+      m[h] = -INFINITY;
+      l[h] = 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[h][e] = 0.f;
+    }
+
+    for (int k = 0; k < npg; ++k) {
+      const uint32_t st = (gk + k) % ATT_STAGES;
+      const uint32_t par = ((gk + k) / ATT_STAGES) & 1;
+      const bool got = __all_sync(0xffffffffu, mbar_wait(&bar[st], par, a.timeout_ns));
+      if (!got) {
+        // drain: every copy this warp started must land before the CTA exits
+        if (lane == 0)
+          for (int kk = k; kk < issued; ++kk)
+            mbar_wait(&bar[(gk + kk) % ATT_STAGES], ((gk + kk) / ATT_STAGES) & 1, a.timeout_ns);
+        failed = true;
+        break;
+      }
+      const uint8_t* kb = ring + st * 2 * BLK;
+      const uint8_t* vb = kb + BLK;
+      float sc[4][GRP];
+      bool valid[4];
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const int j = ts + 4 * jj;
+        valid[jj] = k * P + j < n;
+        float kv[E];
+        load_row8<NCH>(kb + j * D * 2, dg, kv);
+#pragma unroll
+        for (int h = 0; h < GRP; ++h) {
+          float dot = 0.f;
+#pragma unroll
+          for (int e = 0; e < E; ++e) dot = fmaf(qv[h][e], kv[e], dot);
+          sc[jj][h] = dot;
+        }
+      }
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+        for (int h = 0; h < GRP; ++h) {
+          float v = sc[jj][h];
+          v += __shfl_xor_sync(0xffffffffu, v, 1);
+          v += __shfl_xor_sync(0xffffffffu, v, 2);
+          v += __shfl_xor_sync(0xffffffffu, v, 4);
+          sc[jj][h] = valid[jj] ? v : -INFINITY;
+        }
+#pragma unroll
+      for (int h = 0; h < GRP; ++h) {
+        float mx = fmaxf(fmaxf(sc[0][h], sc[1][h]), fmaxf(sc[2][h], sc[3][h]));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        const float mn = fmaxf(m[h], mx);
+        if (mn > m[h]) {  // warp-uniform
+          const float corr = exp2f(m[h] - mn);
+          l[h] *= corr;
+#pragma unroll
+          for (int e = 0; e < E; ++e) acc[h][e] *= corr;
+          m[h] = mn;
+        }
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const float p = valid[jj] ? exp2f(sc[jj][h] - m[h]) : 0.f;
+          sc[jj][h] = p;
+          l[h] += p;
+        }
+      }
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        if (valid[jj]) {  // positions past the piece may hold anything (even NaN)
+          float vv[E];
+          load_row8<NCH>(vb + (ts + 4 * jj) * D * 2, dg, vv);
+#pragma unroll
+          for (int h = 0; h < GRP; ++h)
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[h][e] = fmaf(sc[jj][h], vv[e], acc[h][e]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0 && k + ATT_STAGES < npg) {
+        fence_proxy_async_smem();
+        issue(k + ATT_STAGES);
+        ++issued;
+      }
+    }
+    if (failed) break;
+    gk += npg;
+
+    // merge the four token slots
+#pragma unroll
+    for (int h = 0; h < GRP; ++h) {
+      l[h] += __shfl_xor_sync(0xffffffffu, l[h], 8);
+      l[h] += __shfl_xor_sync(0xffffffffu, l[h], 16);
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        acc[h][e] += __shfl_xor_sync(0xffffffffu, acc[h][e], 8);
+        acc[h][e] += __shfl_xor_sync(0xffffffffu, acc[h][e], 16);
+      }
+    }
+    const int nch = a.tok_nchunks[t];
+    if (nch == 1) {
+#pragma unroll
+      for (int h = 0; h < GRP; ++h) {
+        if ((h & 3) != ts) continue;
+        const float inv = 1.f / l[h];
+        __nv_bfloat16* orow = a.o + (static_cast<size_t>(t) * n_q + g * GRP + h) * D;
+#pragma unroll
+        for (int ch = 0; ch < NCH; ++ch) {
+          uint4 u;
+          const float* v = &acc[h][ch * 8];
+          u.x = pack_bf16(v[0] * inv, v[1] * inv);
+          u.y = pack_bf16(v[2] * inv, v[3] * inv);
+          u.z = pack_bf16(v[4] * inv, v[5] * inv);
+          u.w = pack_bf16(v[6] * inv, v[7] * inv);
+          *reinterpret_cast<uint4*>(orow + ch * 64 + dg * 8) = u;
+        }
+      }
+      continue;
+    }
+    // several pieces: publish this one, the last finisher merges
+    constexpr int REC = GRP * D + 2 * GRP;
+    const size_t row_rec = static_cast<size_t>(t) * a.max_chunks;
+    float* rec = a.partials + ((row_rec + c) * n_kv + g) * REC;
+#pragma unroll
+    for (int h = 0; h < GRP; ++h) {
+      if ((h & 3) != ts) continue;
+#pragma unroll
+      for (int ch = 0; ch < NCH; ++ch) {
+        float4* dst = reinterpret_cast<float4*>(rec + h * D + ch * 64 + dg * 8);
+        dst[0] = make_float4(acc[h][ch * 8 + 0], acc[h][ch * 8 + 1], acc[h][ch * 8 + 2],
+                             acc[h][ch * 8 + 3]);
+        dst[1] = make_float4(acc[h][ch * 8 + 4], acc[h][ch * 8 + 5], acc[h][ch * 8 + 6],
+                             acc[h][ch * 8 + 7]);
+      }
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int h = 0; h < GRP; ++h) {
+        rec[GRP * D + h] = m[h];
+        rec[GRP * D + GRP + h] = l[h];
+      }
+    }
+    __threadfence();
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) last = atomicAdd(&a.row_done[t * n_kv + g], 1) == nch - 1;
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (!last) continue;
+    __threadfence();
+#pragma unroll
+    for (int h = 0; h < GRP; ++h) {
+      if ((h & 3) != ts) continue;
+      float M = -INFINITY;
+      for (int cc = 0; cc < nch; ++cc) {
+        const float* r = a.partials + ((row_rec + cc) * n_kv + g) * REC;
+        M = fmaxf(M, __ldcg(r + GRP * D + h));
+      }
+      float L = 0.f, O[E];
+#pragma unroll
+      for (int e = 0; e < E; ++e) O[e] = 0.f;
+      for (int cc = 0; cc < nch; ++cc) {
+        const float* r = a.partials + ((row_rec + cc) * n_kv + g) * REC;
+        const float w = exp2f(__ldcg(r + GRP * D + h) - M);
+        L += w * __ldcg(r + GRP * D + GRP + h);
+#pragma unroll
+        for (int ch = 0; ch < NCH; ++ch) {
+          const float4* src = reinterpret_cast<const float4*>(r + h * D + ch * 64 + dg * 8);
+          const float4 x0 = __ldcg(src), x1 = __ldcg(src + 1);
+          O[ch * 8 + 0] += w * x0.x; O[ch * 8 + 1] += w * x0.y;
+          O[ch * 8 + 2] += w * x0.z; O[ch * 8 + 3] += w * x0.w;
+          O[ch * 8 + 4] += w * x1.x; O[ch * 8 + 5] += w * x1.y;
+          O[ch * 8 + 6] += w * x1.z; O[ch * 8 + 7] += w * x1.w;
+        }
+      }
+      const float inv = 1.f / L;
+      __nv_bfloat16* orow = a.o + (static_cast<size_t>(t) * n_q + g * GRP + h) * D;
+#pragma unroll
+      for (int ch = 0; ch < NCH; ++ch) {
+        uint4 u;
+        u.x = pack_bf16(O[ch * 8 + 0] * inv, O[ch * 8 + 1] * inv);
+        u.y = pack_bf16(O[ch * 8 + 2] * inv, O[ch * 8 + 3] * inv);
+        u.z = pack_bf16(O[ch * 8 + 4] * inv, O[ch * 8 + 5] * inv);
+        u.w = pack_bf16(O[ch * 8 + 6] * inv, O[ch * 8 + 7] * inv);
+        *reinterpret_cast<uint4*>(orow + ch * 64 + dg * 8) = u;
+      }
+    }
+  }
+
+  if (failed) raise_status(a.status, ST_TIMEOUT);
+}
+
+template <int GRP, int NCH>
+static cudaError_t launch_t(const AttnArgs& a, int grid, cudaStream_t stream) {
+  const int smem = attn_smem_bytes(NCH * 64, ATT_P);
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(attn_kernel<GRP, NCH>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  attn_kernel<GRP, NCH><<<grid, ATT_WARPS * 32, smem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attention(const AttnArgs& a, int grid, cudaStream_t stream) {
+  if (a.page_size != ATT_P || grid <= 0) return cudaErrorInvalidValue;
+  const int grp = a.n_q / a.n_kv;
+  const int nch = a.head_dim / 64;
+#define NF_ATT_CASE(G, N) \
+  if (grp == G && nch == N) return launch_t<G, N>(a, grid, stream);
+  NF_ATT_CASE(1, 1) NF_ATT_CASE(2, 1) NF_ATT_CASE(4, 1) NF_ATT_CASE(8, 1)
+  NF_ATT_CASE(1, 2) NF_ATT_CASE(2, 2) NF_ATT_CASE(4, 2) NF_ATT_CASE(8, 2)
+#undef NF_ATT_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace nf

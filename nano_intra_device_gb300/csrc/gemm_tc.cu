@@ -1,0 +1,416 @@
+// Tensor-core GEMM for sm_103a: C = A * B^T, bf16 in, fp32 accumulate in TMEM.
+//
+// The projections and the FFN of the decoder layer are the step's dense
+// contractions ("NanoFlow: Towards Optimal LLM Serving Throughput", "The
+// Intra-Device Parallelism Mechanism": KQV, O, Up/Gate/Down are the
+// compute-bound operations).  Design:
+//  * persistent CTAs, one per SM (the shared-memory ring fills the SM), so a
+//    grid of S CTAs occupies exactly S SMs: the SM share of a nano-operation;
+//  * warp 0: one thread issues TMA tile loads (128-byte swizzle) into a
+//    4-stage ring; warp 1: one thread issues tcgen05.mma (M=128, N=256, K=16)
+//    into a double-buffered TMEM accumulator; warps 2-5: epilogue, tcgen05.ld
+//    of the accumulator rows, fused RoPE + KV append, residual or SwiGLU;
+//  * every wait is bounded; on expiry the kernel flags the status word, drains
+//    what it has in flight (bounded) and frees TMEM before returning.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace nf {
+
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int TMEM_COLS = 2 * BN;
+constexpr int GEMM_THREADS = 192;
+constexpr int GEMM_SMEM = STAGES * STAGE_BYTES + 1024 + 256;
+constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+
+struct GemmSmemTail {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ void store32_bf16(__nv_bfloat16* dst, const float* v) {
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint4 u;
+    u.x = pack_bf16(v[8 * i + 0], v[8 * i + 1]);
+    u.y = pack_bf16(v[8 * i + 2], v[8 * i + 3]);
+    u.z = pack_bf16(v[8 * i + 4], v[8 * i + 5]);
+    u.w = pack_bf16(v[8 * i + 6], v[8 * i + 7]);
+    d4[i] = u;
+  }
+}
+
+// Store 32 consecutive columns starting at column n of row `row`, keeping
+// only columns < ncols (ncols is a multiple of 8).
+__device__ __forceinline__ void store_row_chunk(__nv_bfloat16* row, int n, int ncols,
+                                                const float* v) {
+  if (n + 32 <= ncols) {
+    store32_bf16(row + n, v);
+  } else {
+    uint4* d4 = reinterpret_cast<uint4*>(row + n);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (n + 8 * i + 8 <= ncols) {
+        uint4 u;
+        u.x = pack_bf16(v[8 * i + 0], v[8 * i + 1]);
+        u.y = pack_bf16(v[8 * i + 2], v[8 * i + 3]);
+        u.z = pack_bf16(v[8 * i + 4], v[8 * i + 5]);
+        u.w = pack_bf16(v[8 * i + 6], v[8 * i + 7]);
+        d4[i] = u;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tmem_load32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  tc_ld_32x32b_x32(taddr, r);
+  tc_wait_ld();
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmB2, const GemmArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  GemmSmemTail* tail = reinterpret_cast<GemmSmemTail*>(smem + STAGES * STAGE_BYTES);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int total_tiles = args.m_tiles * args.n_tiles;
+  const int nk = (args.K + BK - 1) / BK;
+  const uint64_t tmo = args.timeout_ns;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&tail->full[s], 1);
+      mbar_init(&tail->empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tail->tfull[a], 1);
+      mbar_init(&tail->tempty[a], 128);
+    }
+    mbar_init(&tail->drain, 1);
+    tail->abort = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB);
+    if (EPI == EPI_SWIGLU) prefetch_tensormap(&tmB2);
+  }
+  if (warp == 1) {
+    tmem_alloc(&tail->tmem_base, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = tail->tmem_base;
+  volatile int* abort_flag = &tail->abort;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t st = 0, ph = 0;
+      uint32_t issued_mask = 0, last_ph[STAGES] = {0, 0, 0, 0};
+      bool ok = true;
+      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+        const int tm = t % args.m_tiles, tn = t / args.m_tiles;
+        const int m0 = args.m_begin + tm * BM;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&tail->empty[st], ph ^ 1, tmo, abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + st * STAGE_BYTES;
+          uint8_t* sb = sa + A_BYTES;
+          mbar_arrive_expect_tx(&tail->full[st], STAGE_BYTES);
+          tma_load_2d(sa, &tmA, &tail->full[st], kb * BK, m0);
+          if (EPI == EPI_SWIGLU) {
+            tma_load_2d(sb, &tmB, &tail->full[st], kb * BK, tn * (BN / 2));
+            tma_load_2d(sb + B_BYTES / 2, &tmB2, &tail->full[st], kb * BK, tn * (BN / 2));
+          } else {
+            tma_load_2d(sb, &tmB, &tail->full[st], kb * BK, tn * BN);
+          }
+          issued_mask |= 1u << st;
+          last_ph[st] = ph;
+          if (++st == STAGES) {
+            st = 0;
+            ph ^= 1;
+          }
+        }
+      }
+      if (!ok) {
+        raise_status(args.status, ST_TIMEOUT);
+        *abort_flag = 1;
+        // drain: every stage we filled must have landed before smem is released
+        for (int s = 0; s < STAGES; ++s)
+          if (issued_mask & (1u << s)) mbar_wait(&tail->full[s], last_ph[s], tmo);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      uint32_t st = 0, ph = 0, acc = 0, aph = 0;
+      bool ok = true, any = false;
+      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+        if (!mbar_wait(&tail->tempty[acc], aph ^ 1, tmo, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&tail->full[st], ph, tmo, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + st * STAGE_BYTES);
+          const uint64_t adesc = desc_sw128_kmajor(sa);
+          const uint64_t bdesc = desc_sw128_kmajor(sa + A_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            // advance 16 bf16 = 32 bytes along K inside the swizzled row
+            tc_mma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, IDESC, (kb | k) != 0);
+          }
+          any = true;
+          tc_commit(&tail->empty[st]);
+          if (++st == STAGES) {
+            st = 0;
+            ph ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&tail->tfull[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          aph ^= 1;
+        }
+      }
+      if (!ok) {
+        raise_status(args.status, ST_TIMEOUT);
+        *abort_flag = 1;
+        if (any) {  // wait for the MMAs already issued before TMEM goes away
+          tc_commit(&tail->drain);
+          mbar_wait(&tail->drain, 0, tmo);
+        }
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue
+    const int quarter = warp & 3;  // TMEM lanes this warp may access
+    const int row_in_tile = quarter * 32 + lane;
+    uint32_t acc = 0, aph = 0;
+    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+      // the wait result must be warp-uniform: tcgen05.ld below is .sync.aligned
+      const bool got = __all_sync(0xffffffffu, mbar_wait(&tail->tfull[acc], aph, tmo, abort_flag));
+      if (!got) {
+        raise_status(args.status, ST_TIMEOUT);
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const int tm = t % args.m_tiles, tn = t / args.m_tiles;
+      const int m = args.m_begin + tm * BM + row_in_tile;
+      const bool row_ok = m < args.m_end;
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
+      float v[32];
+
+      if (EPI == EPI_STORE || EPI == EPI_RESID) {
+        __nv_bfloat16* crow = args.C + static_cast<size_t>(m) * args.ldc;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          tmem_load32(tbase + c * 32, v);
+          const int n = tn * BN + c * 32;
+          if (row_ok && n < args.N) {
+            if (EPI == EPI_RESID) {
+              const __nv_bfloat16* rrow = args.R + static_cast<size_t>(m) * args.ldr + n;
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                if (n + 8 * i + 8 <= args.N) {
+                  uint4 u = *reinterpret_cast<const uint4*>(rrow + 8 * i);
+                  v[8 * i + 0] += bf16lo(u.x); v[8 * i + 1] += bf16hi(u.x);
+                  v[8 * i + 2] += bf16lo(u.y); v[8 * i + 3] += bf16hi(u.y);
+                  v[8 * i + 4] += bf16lo(u.z); v[8 * i + 5] += bf16hi(u.z);
+                  v[8 * i + 6] += bf16lo(u.w); v[8 * i + 7] += bf16hi(u.w);
+                }
+              }
+            }
+            store_row_chunk(crow, n, args.N, v);
+          }
+        }
+      } else if (EPI == EPI_SWIGLU) {
+        __nv_bfloat16* crow = args.C + static_cast<size_t>(m) * args.ldc;
+        float u[32];
+#pragma unroll 1
+        for (int c = 0; c < BN / 64; ++c) {
+          tmem_load32(tbase + c * 32, v);            // gate columns
+          tmem_load32(tbase + BN / 2 + c * 32, u);   // matching up columns
+          const int n = tn * (BN / 2) + c * 32;
+          if (row_ok && n < args.N) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = v[i] / (1.0f + __expf(-v[i])) * u[i];
+            store_row_chunk(crow, n, args.N, v);
+          }
+        }
+      } else {  // EPI_QKV
+        const int d = args.head_dim;
+        const int nq = args.n_q, nkv = args.n_kv;
+        const int pos = row_ok ? args.tok_pos[m] : 0;
+        const int slot = row_ok ? args.tok_slot[m] : -1;
+        const int P = args.page_size;
+        const size_t page_stride = static_cast<size_t>(nkv) * P * d;
+#pragma unroll 1
+        for (int hh = 0; hh < BN / d; ++hh) {
+          const int col0 = tn * BN + hh * d;
+          const int head = col0 / d;
+          const bool is_q = head < nq;
+          const bool is_k = !is_q && head < nq + nkv;
+          const bool in_range = col0 < args.N;
+          __nv_bfloat16* dst = nullptr;
+          if (row_ok && in_range) {
+            if (is_q) {
+              dst = args.q_out + static_cast<size_t>(m) * nq * d + static_cast<size_t>(head) * d;
+            } else if (slot >= 0) {
+              const int g = is_k ? head - nq : head - nq - nkv;
+              __nv_bfloat16* pool = is_k ? args.k_pool : args.v_pool;
+              dst = pool + static_cast<size_t>(slot / P) * page_stride +
+                    static_cast<size_t>(g) * P * d + static_cast<size_t>(slot % P) * d;
+            }
+          }
+          const uint32_t hb = tbase + hh * d;
+          if (is_q || is_k) {
+            float w[32];
+#pragma unroll 1
+            for (int j0 = 0; j0 < d / 2; j0 += 32) {
+              tmem_load32(hb + j0, v);
+              tmem_load32(hb + d / 2 + j0, w);
+              if (dst != nullptr) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                  // angle = pos * theta^(-2 i / d)
+                  const float inv_freq = exp2f(-(2.0f * (j0 + i) / d) * args.log2_theta);
+                  float s, c;
+                  sincosf(static_cast<float>(pos) * inv_freq, &s, &c);
+                  const float a = v[i], b = w[i];
+                  v[i] = a * c - b * s;
+                  w[i] = b * c + a * s;
+                }
+                store32_bf16(dst + j0, v);
+                store32_bf16(dst + d / 2 + j0, w);
+              }
+            }
+          } else {
+#pragma unroll 1
+            for (int j0 = 0; j0 < d; j0 += 32) {
+              tmem_load32(hb + j0, v);
+              if (dst != nullptr) store32_bf16(dst + j0, v);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tail->tempty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        aph ^= 1;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+int gemm_block_n(int epi) { return epi == EPI_SWIGLU ? BN / 2 : BN; }
+
+int gemm_tiles(int epi, int m_rows, int N) {
+  const int bn = gemm_block_n(epi);
+  return ((m_rows + BM - 1) / BM) * ((N + bn - 1) / bn);
+}
+
+template <int EPI>
+static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB,
+                              const CUtensorMap& tmB2, const GemmArgs& args, int grid,
+                              cudaStream_t stream) {
+  static bool attr_set = false;  // per process; the attribute is per function
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  gemm_tc_kernel<EPI><<<grid, GEMM_THREADS, GEMM_SMEM, stream>>>(tmA, tmB, tmB2, args);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                        const CUtensorMap& tmB2, const GemmArgs& args, int grid,
+                        cudaStream_t stream) {
+  if (grid <= 0) return cudaSuccess;
+  switch (epi) {
+    case EPI_STORE: return launch_one<EPI_STORE>(tmA, tmB, tmB2, args, grid, stream);
+    case EPI_RESID: return launch_one<EPI_RESID>(tmA, tmB, tmB2, args, grid, stream);
+    case EPI_SWIGLU: return launch_one<EPI_SWIGLU>(tmA, tmB, tmB2, args, grid, stream);
+    case EPI_QKV: return launch_one<EPI_QKV>(tmA, tmB, tmB2, args, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+// ------------------------------------------------------------ tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                    uint32_t box_rows) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return false;
+  if ((reinterpret_cast<uintptr_t>(base) & 15) || (cols * 2) % 16 || rows == 0 || cols == 0)
+    return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace nf

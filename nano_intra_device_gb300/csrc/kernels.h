@@ -1,0 +1,99 @@
+// Internal launch interface between the C ABI (api.cu) and the kernels.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace nf {
+
+// ------------------------------------------------------------------ GEMM
+enum GemmEpi : int { EPI_STORE = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_QKV = 3 };
+
+struct GemmArgs {
+  int m_begin, m_end;   // output rows [m_begin, m_end)
+  int N;                // output columns (F for SwiGLU)
+  int K;
+  int m_tiles, n_tiles; // tiles over the row range / the output columns
+  __nv_bfloat16* C;     // STORE/RESID/SWIGLU output, row stride ldc
+  int ldc;
+  const __nv_bfloat16* R;  // RESID residual, row stride ldr
+  int ldr;
+  // QKV epilogue: RoPE on q and k, q to q_out, k and v appended to the pools
+  const int* tok_pos;
+  const int* tok_slot;
+  __nv_bfloat16* q_out;
+  __nv_bfloat16* k_pool;
+  __nv_bfloat16* v_pool;
+  int n_q, n_kv, head_dim, page_size;
+  float log2_theta;
+  uint32_t* status;
+  unsigned long long timeout_ns;
+};
+
+// Build a 2-D bf16 tensor map over a row-major [rows, cols] matrix with a
+// box of box_rows x 64 columns and 128-byte swizzle.  Returns false on error.
+bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                    uint32_t box_rows);
+
+// C = A * B^T (+ epilogue).  tmA over A [*, K], tmB over B; for SwiGLU tmB is
+// the gate rows and tmB2 the up rows.  grid = persistent CTA count.
+cudaError_t launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                        const CUtensorMap& tmB2, const GemmArgs& args, int grid,
+                        cudaStream_t stream);
+int gemm_block_n(int epi);
+int gemm_tiles(int epi, int m_rows, int N);
+
+// --------------------------------------------------------------- RMSNorm
+cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* g, __nv_bfloat16* out,
+                           int row_begin, int row_end, int hidden, float eps, cudaStream_t stream);
+
+// ---------------------------------------------------------- step metadata
+struct MetaArgs {
+  const int* seq_lens;      // device [n_seq]
+  const int* block_table;   // device [n_seq, max_pages]
+  const int* q_lens;        // device [n_seq]
+  const int* tok_begin;     // device [n_seq + 1]
+  const int* seg_bounds;    // device [n_seg + 1], attention nano-batch token bounds
+  int n_seq, n_tok, n_seg, max_pages, num_pages, page_size, kv_chunk, n_kv;
+  int max_chunks;           // per-row chunk capacity = ceil(max_pages*page/kv_chunk)
+  int item_capacity;        // pairs the item buffer holds
+  int* tok_seq;             // out [n_tok]
+  int* tok_pos;             // out [n_tok]
+  int* tok_slot;            // out [n_tok]
+  int* tok_nchunks;         // out [n_tok]
+  int* items;               // out [2 * item_capacity] (row, chunk)
+  int* seg_items;           // out [n_seg + 1] segment starts in items
+  int* fetch;               // out [n_seg] dynamic fetch counters, zeroed
+  int* row_done;            // out [n_tok * n_kv] split-combine counters, zeroed
+  uint32_t* status;
+  int validate;
+};
+cudaError_t launch_meta(const MetaArgs& a, cudaStream_t stream);
+
+// -------------------------------------------------------------- attention
+struct AttnArgs {
+  const __nv_bfloat16* q;    // [T, n_q, d]
+  const __nv_bfloat16* k_pool;
+  const __nv_bfloat16* v_pool;
+  __nv_bfloat16* o;          // [T, n_q, d]
+  const int* block_table;
+  const int* tok_seq;
+  const int* tok_pos;
+  const int* tok_nchunks;
+  const int* items;          // (row, chunk) pairs
+  const int* seg_items;      // segment starts
+  int* fetch;                // per-segment fetch counter
+  int* row_done;             // [T, n_kv]
+  float* partials;           // [T, max_chunks, n_kv, rec]
+  int seg;                   // which attention nano-batch
+  int n_q, n_kv, head_dim, page_size, max_pages, num_pages, kv_chunk, max_chunks;
+  float scale_log2;          // log2(e) / sqrt(d)
+  uint32_t* status;
+  unsigned long long timeout_ns;
+};
+int attn_partial_floats(int n_q, int n_kv, int head_dim);  // floats per (row, chunk, kv head)
+cudaError_t launch_attention(const AttnArgs& a, int grid, cudaStream_t stream);
+int attn_smem_bytes(int head_dim, int page_size);
+
+}  // namespace nf

@@ -1,0 +1,56 @@
+// RMSNorm rows of a [rows, hidden] bf16 matrix: out = x * g / sqrt(mean(x^2) + eps).
+// Pre-norm of the decoder layer ("CSE 451 Lecture 25", slide 25, decoder-only
+// transformer layer).  HBM-bound: one CTA per row, 16-byte loads, fp32 sums.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace nf {
+
+constexpr int RMS_THREADS = 128;
+
+__global__ void __launch_bounds__(RMS_THREADS)
+    rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ g,
+                   __nv_bfloat16* __restrict__ out, int row_begin, int hidden, float eps) {
+  const int row = row_begin + blockIdx.x;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(row) * hidden);
+  const uint4* gr = reinterpret_cast<const uint4*>(g);
+  uint4* orow = reinterpret_cast<uint4*>(out + static_cast<size_t>(row) * hidden);
+  const int nvec = hidden / 8;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < nvec; i += RMS_THREADS) {
+    uint4 u = xr[i];
+    uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float a = bf16lo(w[j]), b = bf16hi(w[j]);
+      ss += a * a + b * b;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  __shared__ float red[RMS_THREADS / 32];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int i = 0; i < RMS_THREADS / 32; ++i) tot += red[i];
+  const float r = rsqrtf(tot / hidden + eps);
+  for (int i = threadIdx.x; i < nvec; i += RMS_THREADS) {
+    uint4 u = xr[i], gv = gr[i];
+    uint32_t w[4] = {u.x, u.y, u.z, u.w}, gg[4] = {gv.x, gv.y, gv.z, gv.w}, o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      o[j] = pack_bf16(bf16lo(w[j]) * r * bf16lo(gg[j]), bf16hi(w[j]) * r * bf16hi(gg[j]));
+    orow[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* g, __nv_bfloat16* out,
+                           int row_begin, int row_end, int hidden, float eps, cudaStream_t stream) {
+  if (row_end <= row_begin) return cudaSuccess;
+  rmsnorm_kernel<<<row_end - row_begin, RMS_THREADS, 0, stream>>>(x, g, out, row_begin, hidden,
+                                                                   eps);
+  return cudaGetLastError();
+}
+
+}  // namespace nf

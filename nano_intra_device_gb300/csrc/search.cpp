@@ -1,0 +1,221 @@
+// Plan search: nano-batch count, token boundaries and SM shares that minimise
+// the predicted step time of the two-stream pipeline.
+//
+// The pages' auto-search ("NanoFlow: Towards Optimal LLM Serving Throughput",
+// "Auto-Search Stage I" and "Auto-Search Stage II") solves two MILPs: first the
+// nano-batch structure (count, sizes in multiples of 128 summing to B_dense,
+// order) with interference-free kernel times, then the resource share of each
+// nano-operation from a measured R -> P table.  On one GPU with two resource
+// classes (tensor-core GEMMs, HBM-bound attention) and a fixed operation order
+// the space is small: n <= 4 nano-batches on a 128-token grid, an SM split on a
+// 1/16 grid.  This file enumerates it and scores each candidate with a list-
+// scheduling simulation of the two streams, which is exact under the same
+// time model the MILP would use, and needs no solver.
+//
+// Time model (per nano-operation, on S SMs):
+//   GEMM M x N x K: waves = ceil(tiles / S) with 128 x 256 tiles, each tile
+//     2*128*256*K / (per-SM tensor rate); plus a launch cost;
+//   attention: KV bytes / min(HBM bandwidth, S * per-SM attention bandwidth);
+//     an SM share is an SM count because every kernel runs one CTA per SM.
+// The rates come from a profile written by nf_profile, else from defaults.
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/nanoflow.h"
+
+namespace {
+
+struct Rates {
+  double gemm_flops_per_sm = 1.9e15 / 152 * 0.75;  // sustained per-SM tensor rate
+  double hbm_bps = 6.8e12 * 0.9;                   // achievable HBM bandwidth
+  double attn_bps_per_sm = 60e9;                   // attention bytes/s one SM sustains
+  double gemm_launch_s = 4e-6;
+  double attn_launch_s = 4e-6;
+  double overlap_bw_factor = 0.92;                 // HBM share attention keeps next to GEMMs
+};
+
+double json_number(const std::string& s, const char* key, double dflt) {
+  const std::string k = std::string("\"") + key + "\"";
+  size_t p = s.find(k);
+  if (p == std::string::npos) return dflt;
+  p = s.find(':', p);
+  if (p == std::string::npos) return dflt;
+  return std::strtod(s.c_str() + p + 1, nullptr);
+}
+
+bool load_rates(const char* path, Rates* r) {
+  if (!path) return true;
+  FILE* f = std::fopen(path, "r");
+  if (!f) return false;
+  std::string s;
+  char buf[4096];
+  size_t n;
+  while ((n = std::fread(buf, 1, sizeof(buf), f)) > 0) s.append(buf, n);
+  std::fclose(f);
+  r->gemm_flops_per_sm = json_number(s, "gemm_flops_per_sm", r->gemm_flops_per_sm);
+  r->hbm_bps = json_number(s, "hbm_bps", r->hbm_bps);
+  r->attn_bps_per_sm = json_number(s, "attn_bps_per_sm", r->attn_bps_per_sm);
+  r->gemm_launch_s = json_number(s, "gemm_launch_s", r->gemm_launch_s);
+  r->attn_launch_s = json_number(s, "attn_launch_s", r->attn_launch_s);
+  r->overlap_bw_factor = json_number(s, "overlap_bw_factor", r->overlap_bw_factor);
+  return true;
+}
+
+struct Model {
+  nf_model_shape s;
+  Rates r;
+  int sms;
+  std::vector<double> row_kv_bytes;  // KV bytes each token's attention reads
+  std::vector<double> prefix;        // prefix sums of row_kv_bytes
+
+  double gemm_time(int rows, int N, int K, int S, int bn) const {
+    if (rows <= 0) return 0;
+    const double tiles = std::ceil(rows / 128.0) * std::ceil(N / double(bn));
+    const double waves = std::ceil(tiles / S);
+    const double per_tile = 2.0 * 128 * bn * K / r.gemm_flops_per_sm;
+    return waves * per_tile + r.gemm_launch_s;
+  }
+  // QKV + O for rows, or RMSNorm-2 + gate/up + down for rows
+  double qkv_time(int rows, int S) const {
+    return gemm_time(rows, (s.n_q_heads + 2 * s.n_kv_heads) * s.head_dim, s.hidden, S, 256);
+  }
+  double o_time(int rows, int S) const {
+    return gemm_time(rows, s.hidden, s.n_q_heads * s.head_dim, S, 256);
+  }
+  double ffn_time(int rows, int S) const {
+    return gemm_time(rows, s.ffn, s.hidden, S, 128) + gemm_time(rows, s.hidden, s.ffn, S, 256);
+  }
+  double attn_time(int r0, int r1, int S, bool overlapped) const {
+    const double bytes = prefix[r1] - prefix[r0];
+    double bw = std::min(r.hbm_bps, S * r.attn_bps_per_sm);
+    if (overlapped) bw *= r.overlap_bw_factor;
+    return bytes / bw + r.attn_launch_s;
+  }
+};
+
+// Simulate the two-stream pipeline of api.cu's stream executor.
+double simulate(const Model& m, const nf_plan_opts& o) {
+  const int all = m.sms;
+  const int n = o.n_attn;
+  if (o.executor == NF_EXEC_SEQUENTIAL) {
+    double t = 0;
+    for (int i = 0; i < n; ++i) {
+      const int r0 = o.attn_bounds[i], r1 = o.attn_bounds[i + 1];
+      t += m.qkv_time(r1 - r0, all) + m.attn_time(r0, r1, all, false) + m.o_time(r1 - r0, all);
+    }
+    for (int j = 0; j < o.n_ffn; ++j) t += m.ffn_time(o.ffn_bounds[j + 1] - o.ffn_bounds[j], all);
+    return t;
+  }
+  const int attn_sms = n == 1 ? all : o.attn_sms;
+  const int gsm = o.gemm_sms > 0 ? o.gemm_sms : std::max(1, all - attn_sms);
+  double tg = 0, ta = 0;
+  std::vector<double> q_done(n), a_done(n);
+  for (int i = 0; i < n; ++i) {
+    tg += m.qkv_time(o.attn_bounds[i + 1] - o.attn_bounds[i], i == 0 ? all : gsm);
+    q_done[i] = tg;
+  }
+  for (int i = 0; i < n; ++i) {
+    ta = std::max(ta, q_done[i]);
+    ta += m.attn_time(o.attn_bounds[i], o.attn_bounds[i + 1], attn_sms, n > 1);
+    a_done[i] = ta;
+  }
+  int next_ffn = 0;
+  for (int i = 0; i < n; ++i) {
+    tg = std::max(tg, a_done[i]);
+    const int S = (i == n - 1) ? all : gsm;
+    tg += m.o_time(o.attn_bounds[i + 1] - o.attn_bounds[i], S);
+    while (next_ffn < o.n_ffn && o.ffn_bounds[next_ffn + 1] <= o.attn_bounds[i + 1]) {
+      tg += m.ffn_time(o.ffn_bounds[next_ffn + 1] - o.ffn_bounds[next_ffn], S);
+      ++next_ffn;
+    }
+  }
+  return tg;
+}
+
+// Boundaries that split the attention bytes of the batch evenly, on a grid.
+void balanced_bounds(const Model& m, int T, int n, int grid, int32_t* b) {
+  b[0] = 0;
+  b[n] = T;
+  const double total = m.prefix[T];
+  for (int i = 1; i < n; ++i) {
+    const double target = total * i / n;
+    int t = int(std::lower_bound(m.prefix.begin(), m.prefix.end(), target) - m.prefix.begin());
+    t = std::max(1, std::min(T - 1, (t + grid / 2) / grid * grid));
+    b[i] = std::max(t, b[i - 1] + 1);
+  }
+  for (int i = n - 1; i >= 1; --i) b[i] = std::min(b[i], b[i + 1] - 1);
+}
+
+}  // namespace
+
+extern "C" nf_status nf_plan_search(const nf_model_shape* shape, const nf_batch_desc* batch,
+                                    const char* profile_json, int32_t num_sms, nf_plan_opts* out,
+                                    double* predicted_us) {
+  if (!shape || !batch || !out || num_sms <= 0) return NF_ERR_INVALID_ARG;
+  Model m;
+  m.s = *shape;
+  m.sms = num_sms;
+  if (!load_rates(profile_json, &m.r)) return NF_ERR_INVALID_ARG;
+  const int n_seq = batch->n_decode + batch->n_prefill;
+  const double kv_tok = 2.0 * shape->n_kv_heads * shape->head_dim * 2;
+  const int default_ctx = batch->max_pages_per_seq * shape->page_size / 2;
+  for (int s = 0; s < n_seq; ++s) {
+    const int q = s < batch->n_decode ? 1 : batch->prefill_q_lens[s - batch->n_decode];
+    if (q < 1) return NF_ERR_INVALID_ARG;
+    const int L = batch->seq_lens_hint ? batch->seq_lens_hint[s]
+                                       : (s < batch->n_decode ? default_ctx : q);
+    for (int i = 0; i < q; ++i) m.row_kv_bytes.push_back(double(L - q + i + 1) * kv_tok);
+  }
+  const int T = int(m.row_kv_bytes.size());
+  if (T < 1) return NF_ERR_INVALID_ARG;
+  m.prefix.assign(T + 1, 0.0);
+  for (int t = 0; t < T; ++t) m.prefix[t + 1] = m.prefix[t] + m.row_kv_bytes[t];
+
+  nf_plan_opts best;
+  std::memset(&best, 0, sizeof(best));
+  best.n_attn = 1;
+  best.attn_bounds[1] = T;
+  best.n_ffn = 1;
+  best.ffn_bounds[1] = T;
+  best.executor = NF_EXEC_SEQUENTIAL;
+  best.kv_chunk = 512;
+  best.timeout_ns = 2000000000LL;
+  double best_t = simulate(m, best);
+
+  const int grid = T >= 1024 ? 128 : 1;  // nano-batches are multiples of 128 tokens
+  for (int n = 2; n <= 4; ++n) {
+    if (T / grid < n) break;
+    nf_plan_opts o = best;
+    o.executor = NF_EXEC_STREAMS;
+    o.n_attn = n;
+    balanced_bounds(m, T, n, grid, o.attn_bounds);
+    for (int nf_ = 1; nf_ <= 2; ++nf_) {
+      o.n_ffn = nf_;
+      if (nf_ == 1) {
+        o.ffn_bounds[0] = 0;
+        o.ffn_bounds[1] = T;
+      } else {
+        o.ffn_bounds[0] = 0;
+        o.ffn_bounds[1] = o.attn_bounds[n / 2];
+        o.ffn_bounds[2] = T;
+      }
+      for (int k = 2; k <= 15; ++k) {
+        o.attn_sms = std::max(1, num_sms * k / 16);
+        o.gemm_sms = 0;
+        const double t = simulate(m, o);
+        if (t < best_t) {
+          best_t = t;
+          best = o;
+        }
+      }
+    }
+  }
+  *out = best;
+  if (predicted_us) *predicted_us = best_t * 1e6;
+  return NF_OK;
+}

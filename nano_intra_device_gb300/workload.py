@@ -194,23 +194,26 @@ def make_x(shape: Shape, n_tokens: int, seed: int = 0) -> torch.Tensor:
 # --------------------------------------------------------------------------
 # KV pools
 
-def page_fill_counts(shape: Shape, batch: Batch) -> np.ndarray:
+def page_fill_counts(shape: Shape, batch: Batch, appended: bool = False) -> np.ndarray:
     """Per physical page, how many leading positions hold a cached token
-    before the step (0 for pages no sequence owns)."""
+    before the step (after it, with appended=True); 0 for pages no sequence
+    owns."""
     P = shape.page_size
     cnt = np.zeros(batch.num_pages, np.int32)
     for s in range(batch.n_seq):
-        cached = int(batch.seq_lens[s]) - int(batch.q_lens[s])
+        cached = int(batch.seq_lens[s]) - (0 if appended else int(batch.q_lens[s]))
         n_pages = (int(batch.seq_lens[s]) + P - 1) // P
         for j in range(n_pages):
             cnt[batch.block_table[s, j]] = min(P, max(0, cached - j * P))
     return cnt
 
 
-def make_pools(shape: Shape, batch: Batch, device="cpu", seed: int = 3):
+def make_pools(shape: Shape, batch: Batch, device="cpu", seed: int = 3, appended: bool = False):
     """K and V pools ``[num_pages, n_kv, page_size, head_dim]`` bf16.
 
-    Cached positions are N(0,1); every other position is NaN.  On a CUDA
+    Cached positions are N(0,1); every other position is NaN.  With
+    appended=True the positions of this step's tokens count as cached too (a
+    cache as it stands after the step's append).  On a CUDA
     device the values come from torch's CUDA generator (seeded), so that a
     multi-GB pool is drawn in place.
     """
@@ -219,7 +222,7 @@ def make_pools(shape: Shape, batch: Batch, device="cpu", seed: int = 3):
     g = torch.Generator(device=dev).manual_seed(seed)
     k = torch.randn(sz, generator=g, device=dev, dtype=BF16)
     v = torch.randn(sz, generator=g, device=dev, dtype=BF16)
-    cnt = torch.from_numpy(page_fill_counts(shape, batch)).to(dev)
+    cnt = torch.from_numpy(page_fill_counts(shape, batch, appended)).to(dev)
     empty = torch.arange(shape.page_size, device=dev)[None, :] >= cnt[:, None]
     empty = empty[:, None, :, None]
     k.masked_fill_(empty, float("nan"))

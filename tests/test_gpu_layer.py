@@ -1,0 +1,186 @@
+"""The whole layer step on the GPU through nf_layer_step against the oracle:
+every two-way split of the small batch, both executors, the 8B-shaped batch at
+1-4 nano-batches on sampled rows, and the host-buffer entry point."""
+import itertools
+import os
+import tempfile
+
+import numpy as np
+import pytest
+import torch
+
+from nano_intra_device_gb300 import _lib, workload as wl
+from oracle import layer as orc
+from tests.helpers import compare, f64, to_dev
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+class Case:
+    def __init__(self, shape, batch, gain_std=0.1, seed=0):
+        self.shape, self.batch = shape, batch
+        self.w = wl.make_weights(shape, seed=seed, gain_std=gain_std)
+        self.x = wl.make_x(shape, batch.n_tokens, seed=seed)
+        self.kp, self.vp = wl.make_pools(shape, batch, DEV, seed=seed + 3)
+        self.wd = to_dev(self.w)
+        self.xd = self.x.to(DEV)
+        self.bt = torch.from_numpy(batch.block_table).to(DEV)
+        self.sl = torch.from_numpy(batch.seq_lens).to(DEV)
+
+    def oracle(self, rows=None, keep=False):
+        return orc.layer_step(self.shape, orc.weights_f64(self.w), self.x, self.kp, self.vp,
+                              self.batch.block_table, self.batch.seq_lens, self.batch.q_lens,
+                              rows=rows, keep=keep)
+
+    def run(self, opts):
+        kp, vp = self.kp.clone(), self.vp.clone()
+        y = torch.empty_like(self.xd)
+        plan = _lib.Plan(self.shape, self.batch, opts)
+        _lib.layer_step(plan, self.wd, self.xd, kp, vp, self.bt, self.sl, y)
+        plan.poll()
+        return plan, y, kp, vp
+
+
+def _check_layer(case, ref, y, kp, vp, rows):
+    P = case.shape.page_size
+    yg = f64(y)[rows]
+    compare(yg, ref["y"], "y")
+    compare(yg - f64(case.x)[rows], ref["y"] - f64(case.x)[rows], "y - x")
+    sl = torch.as_tensor(ref["slots"], device=DEV)
+    kg = f64(kp[sl // P, :, sl % P, :])
+    vg = f64(vp[sl // P, :, sl % P, :])
+    compare(kg, ref["k_new"], "appended k")
+    compare(vg, ref["v_new"], "appended v")
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    c = Case(wl.tiny_shape(), wl.tiny_batch())
+    return c, c.oracle(keep=True)
+
+
+@pytest.mark.parametrize("executor", [_lib.NF_EXEC_SEQUENTIAL, _lib.NF_EXEC_STREAMS])
+def test_tiny_every_two_way_split(tiny, executor):
+    case, ref = tiny
+    T = case.batch.n_tokens
+    rows = np.arange(T)
+    first = None
+    for cut in range(1, T):
+        opts = _lib.make_opts(T, [0, cut, T], [0, cut, T], executor=executor, attn_sms=20,
+                              kv_chunk=32)
+        plan, y, kp, vp = case.run(opts)
+        plan.close()
+        _check_layer(case, ref, y, kp, vp, rows)
+        if first is None:
+            first = y.clone()
+        else:  # the split never changes the bits
+            assert torch.equal(y, first), f"split {cut} changed the result"
+
+
+def test_tiny_intermediates_and_untouched_pool(tiny):
+    case, ref = tiny
+    T = case.batch.n_tokens
+    s = case.shape
+    plan, y, kp, vp = case.run(_lib.make_opts(T, [0, 18, T], kv_chunk=32))
+    compare(f64(plan.buffer(_lib.NF_BUF_N1, torch.bfloat16, (T, s.hidden))), ref["n1"], "n1")
+    compare(f64(plan.buffer(_lib.NF_BUF_Q, torch.bfloat16, (T, s.n_q, s.head_dim))), ref["q"], "q")
+    compare(f64(plan.buffer(_lib.NF_BUF_O, torch.bfloat16, (T, s.n_q, s.head_dim))), ref["o"], "o")
+    compare(f64(plan.buffer(_lib.NF_BUF_H, torch.bfloat16, (T, s.hidden))), ref["h"], "h")
+    compare(f64(plan.buffer(_lib.NF_BUF_N2, torch.bfloat16, (T, s.hidden))), ref["n2"], "n2")
+    compare(f64(plan.buffer(_lib.NF_BUF_A, torch.bfloat16, (T, s.ffn))), ref["a"], "a")
+    plan.close()
+    # nothing but this step's slots changed in the pools (NaN poison included)
+    P = s.page_size
+    mask = torch.ones(case.kp.shape[0] * P, dtype=torch.bool)
+    mask[torch.as_tensor(ref["slots"])] = False
+    def flat(t):
+        return t.permute(0, 2, 1, 3).reshape(-1, s.n_kv * s.head_dim).cpu()[mask]
+    assert torch.equal(flat(kp).isnan(), flat(case.kp).isnan())
+    assert torch.equal(torch.nan_to_num(flat(kp)), torch.nan_to_num(flat(case.kp)))
+    assert torch.equal(torch.nan_to_num(flat(vp)), torch.nan_to_num(flat(case.vp)))
+
+
+@pytest.mark.parametrize("ab,fb", [([0, 5, 19, 36], [0, 19, 36]), ([0, 1, 2, 3, 36], [0, 36]),
+                                   ([0, 4, 36], [0, 2, 4, 30, 36])])
+def test_tiny_multiway_splits_both_executors(tiny, ab, fb):
+    case, ref = tiny
+    T = case.batch.n_tokens
+    for ex in (_lib.NF_EXEC_SEQUENTIAL, _lib.NF_EXEC_STREAMS):
+        plan, y, kp, vp = case.run(_lib.make_opts(T, ab, fb, executor=ex, attn_sms=16, kv_chunk=16))
+        plan.close()
+        _check_layer(case, ref, y, kp, vp, np.arange(T))
+
+
+def test_tiny_host_entry_point_matches_device(tiny):
+    case, ref = tiny
+    T = case.batch.n_tokens
+    opts = _lib.make_opts(T, [0, 18, T], executor=_lib.NF_EXEC_STREAMS, attn_sms=30)
+    plan, y, _, _ = case.run(opts)
+    kp, vp = case.kp.clone(), case.vp.clone()
+    yh = torch.empty(T, case.shape.hidden, dtype=torch.bfloat16).pin_memory()
+    _lib.layer_step_host(plan, case.wd, case.x.pin_memory(), kp, vp,
+                         torch.from_numpy(case.batch.block_table), torch.from_numpy(case.batch.seq_lens), yh)
+    plan.close()
+    assert torch.equal(yh, y.cpu())
+
+
+def test_plan_save_load_and_search(tiny, tmp_path):
+    case, ref = tiny
+    T = case.batch.n_tokens
+    plan = _lib.Plan(case.shape, case.batch, None)          # library search
+    o, n = plan.info()
+    assert n == T and o.attn_bounds[0] == 0 and o.attn_bounds[o.n_attn] == T
+    path = str(tmp_path / "plan.txt")
+    _lib.check(_lib.lib().nf_plan_save(plan.h, path.encode()))
+    h = _lib.ctypes.c_void_p()
+    _lib.check(_lib.lib().nf_plan_load(path.encode(), _lib.ctypes.byref(h)))
+    p2 = _lib.Plan.from_handle(h)
+    o2, n2 = p2.info()
+    assert n2 == T and list(o2.attn_bounds) == list(o.attn_bounds) and o2.attn_sms == o.attn_sms
+    kp, vp = case.kp.clone(), case.vp.clone()
+    y = torch.empty_like(case.xd)
+    _lib.layer_step(p2, case.wd, case.xd, kp, vp, case.bt, case.sl, y)
+    p2.poll()
+    _check_layer(case, ref, y, kp, vp, np.arange(T))
+    plan.close()
+    p2.close()
+
+
+def test_prefill_with_prefix_and_several_chunks():
+    shape = wl.tiny_shape()
+    b = wl.make_batch(shape, [1, 2, 100, 31], [7, 20, 1], [0, 45, 16], seed_bt=11)
+    case = Case(shape, b, gain_std=0.2, seed=4)
+    ref = case.oracle()
+    T = b.n_tokens
+    for ab in ([0, T], [0, 3, 9, 20, T]):
+        plan, y, kp, vp = case.run(_lib.make_opts(T, ab, executor=_lib.NF_EXEC_STREAMS,
+                                                  attn_sms=12, kv_chunk=48))
+        plan.close()
+        _check_layer(case, ref, y, kp, vp, np.arange(T))
+
+
+# ------------------------------------------------------------ 8B-shaped
+@pytest.fixture(scope="module")
+def big():
+    shape, b = wl.llama8b_shape(), wl.llama8b_batch()
+    case = Case(shape, b, gain_std=0.0, seed=0)
+    T = b.n_tokens
+    rng = np.random.default_rng(1)
+    ctx = b.seq_lens[: b.n_decode]
+    rows = sorted(set([0, 1023, 1024, b.n_decode - 1, int(np.argmax(ctx)), int(np.argmin(ctx))] +
+                      rng.choice(b.n_decode, 24, replace=False).tolist() +
+                      [b.n_decode, T - 1] + (b.n_decode + rng.choice(256, 6, replace=False)).tolist()))
+    return case, rows, case.oracle(rows=rows)
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4])
+def test_llama8b_sampled_rows_by_nano_batch_count(big, n):
+    case, rows, ref = big
+    T = case.batch.n_tokens
+    ab = [0] + [int(round(T * i / n / 128)) * 128 for i in range(1, n)] + [T]
+    ex = _lib.NF_EXEC_SEQUENTIAL if n == 1 else _lib.NF_EXEC_STREAMS
+    plan, y, kp, vp = case.run(_lib.make_opts(T, ab, ab, executor=ex, attn_sms=96))
+    plan.close()
+    _check_layer(case, ref, y, kp, vp, np.asarray(rows))
+    assert torch.isfinite(y).all()
