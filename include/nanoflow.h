@@ -63,7 +63,7 @@ typedef enum {
 
 /* Shape of one Llama-style decoder layer.  head_dim in {64, 128};
  * n_q_heads a multiple of n_kv_heads with n_q/n_kv in {1, 2, 4, 8};
- * hidden and ffn multiples of 64; page_size = 16. */
+ * hidden and ffn multiples of 16; page_size = 16. */
 typedef struct {
   int32_t hidden;
   int32_t n_q_heads;

@@ -136,10 +136,10 @@ const void* buf_ptr(nf_plan p, int which) {
 
 nf_status check_shape(const nf_model_shape* s) {
   if (!s) return fail(NF_ERR_INVALID_ARG, "shape is NULL");
-  if (s->hidden <= 0 || s->hidden % 64)
-    return fail(NF_ERR_INVALID_ARG, "hidden must be a positive multiple of 64 (got %d)", s->hidden);
-  if (s->ffn <= 0 || s->ffn % 64)
-    return fail(NF_ERR_INVALID_ARG, "ffn must be a positive multiple of 64 (got %d)", s->ffn);
+  if (s->hidden <= 0 || s->hidden % 16)
+    return fail(NF_ERR_INVALID_ARG, "hidden must be a positive multiple of 16 (got %d)", s->hidden);
+  if (s->ffn <= 0 || s->ffn % 16)
+    return fail(NF_ERR_INVALID_ARG, "ffn must be a positive multiple of 16 (got %d)", s->ffn);
   if (s->head_dim != 64 && s->head_dim != 128)
     return fail(NF_ERR_INVALID_ARG, "head_dim must be 64 or 128 (got %d)", s->head_dim);
   if (s->n_kv_heads <= 0 || s->n_q_heads <= 0 || s->n_q_heads % s->n_kv_heads)

@@ -33,9 +33,15 @@ constexpr int ATT_STAGES = 3;
 constexpr int ATT_P = 16;              // page size the kernel is built for
 constexpr int ATT_MIN_SMEM = 120 * 1024;  // > half an SM: one CTA per SM
 
+// Floats of one split-KV partial record: acc [GRP][d], then m [GRP] and
+// l [GRP], padded so every record starts on a 16-byte boundary (the record is
+// written and read with 16-byte vector accesses).
+__host__ __device__ constexpr int partial_rec_floats(int grp, int head_dim) {
+  return grp * head_dim + ((2 * grp + 3) / 4) * 4;
+}
+
 int attn_partial_floats(int n_q, int n_kv, int head_dim) {
-  const int grp = n_q / n_kv;
-  return grp * head_dim + 2 * grp;
+  return partial_rec_floats(n_q / n_kv, head_dim);
 }
 
 int attn_smem_bytes(int head_dim, int page_size) {
@@ -249,7 +255,8 @@ __global__ void __launch_bounds__(ATT_WARPS * 32, 1) attn_kernel(const AttnArgs 
       continue;
     }
     // several pieces: publish this one, the last finisher merges
-    constexpr int REC = GRP * D + 2 * GRP;
+    constexpr int REC = partial_rec_floats(GRP, D);
+    static_assert(REC % 4 == 0, "partial records must stay 16-byte aligned");
     const size_t row_rec = static_cast<size_t>(t) * a.max_chunks;
     float* rec = a.partials + ((row_rec + c) * n_kv + g) * REC;
 #pragma unroll
