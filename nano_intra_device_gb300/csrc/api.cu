@@ -12,6 +12,7 @@
 #include "../../include/nanoflow.h"
 #include "common.cuh"
 #include "kernels.h"
+#include "internal.h"
 
 using nf::GemmArgs;
 
@@ -171,6 +172,8 @@ nf_status check_opts(const nf_plan_opts* o, int T, int num_sms) {
   if (o->attn_sms < 0 || o->attn_sms > num_sms || o->gemm_sms < 0 || o->gemm_sms > num_sms)
     return fail(NF_ERR_INVALID_ARG, "SM shares must lie in [0, %d]", num_sms);
   if (o->timeout_ns <= 0) return fail(NF_ERR_INVALID_ARG, "timeout_ns must be positive");
+  if (o->attn_warps != 8 && o->attn_warps != 10 && o->attn_warps != 12)
+    return fail(NF_ERR_INVALID_ARG, "attn_warps must be 8, 10 or 12");
   return NF_OK;
 }
 
@@ -310,6 +313,7 @@ nf_status build_plan(const nf_model_shape* shape, const nf_batch_desc* batch,
   }
   if (p->opts.kv_chunk == 0) p->opts.kv_chunk = 512;
   if (p->opts.timeout_ns == 0) p->opts.timeout_ns = kDefaultTimeoutNs;
+  if (p->opts.attn_warps == 0) p->opts.attn_warps = 8;
   nf_status s = check_opts(&p->opts, p->T, num_sms);
   if (s != NF_OK) {
     delete p;
@@ -449,6 +453,7 @@ nf_status run_attention(nf_plan p, int seg, const void* q, const void* kp, const
   a.kv_chunk = p->opts.kv_chunk;
   a.max_chunks = p->max_chunks;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p->shape.head_dim));
+  a.warps = p->opts.attn_warps;
   a.status = p->status;
   a.timeout_ns = (unsigned long long)p->opts.timeout_ns;
   NF_CUDA(nf::launch_attention(a, grid, st));
@@ -619,6 +624,14 @@ nf_status layer_step(nf_plan p, const nf_layer_weights* w, const void* x, void* 
 
 }  // namespace
 
+nf_status nf::attention_on(nf_plan p, const void* q, const void* kp, const void* vp,
+                           const int32_t* bt, const int32_t* sl, void* o, int grid,
+                           cudaStream_t st) {
+  NF_TRY(run_meta(p, bt, sl, st));
+  for (int i = 0; i < p->opts.n_attn; ++i) NF_TRY(run_attention(p, i, q, kp, vp, bt, o, grid, st));
+  return NF_OK;
+}
+
 // ============================================================== C ABI
 extern "C" {
 
@@ -658,8 +671,8 @@ nf_status nf_plan_save(nf_plan p, const char* path) {
   for (int i = 0; i <= o.n_attn; ++i) std::fprintf(f, " %d", o.attn_bounds[i]);
   std::fprintf(f, "\nffn %d", o.n_ffn);
   for (int i = 0; i <= o.n_ffn; ++i) std::fprintf(f, " %d", o.ffn_bounds[i]);
-  std::fprintf(f, "\nexec %d %d %d %d %d %lld\n", o.executor, o.attn_sms, o.gemm_sms, o.kv_chunk,
-               o.validate, (long long)o.timeout_ns);
+  std::fprintf(f, "\nexec %d %d %d %d %d %lld %d\n", o.executor, o.attn_sms, o.gemm_sms,
+               o.kv_chunk, o.validate, (long long)o.timeout_ns, o.attn_warps);
   std::fclose(f);
   return NF_OK;
 }
@@ -688,8 +701,8 @@ nf_status nf_plan_load(const char* path, nf_plan* out) {
   for (int i = 0; ok && i <= o.n_attn; ++i) ok = std::fscanf(f, " %d", &o.attn_bounds[i]) == 1;
   ok = ok && std::fscanf(f, " ffn %d", &o.n_ffn) == 1 && o.n_ffn >= 1 && o.n_ffn <= NF_MAX_NANO;
   for (int i = 0; ok && i <= o.n_ffn; ++i) ok = std::fscanf(f, " %d", &o.ffn_bounds[i]) == 1;
-  ok = ok && std::fscanf(f, " exec %d %d %d %d %d %lld", &o.executor, &o.attn_sms, &o.gemm_sms,
-                         &o.kv_chunk, &o.validate, &tmo) == 6;
+  ok = ok && std::fscanf(f, " exec %d %d %d %d %d %lld %d", &o.executor, &o.attn_sms,
+                         &o.gemm_sms, &o.kv_chunk, &o.validate, &tmo, &o.attn_warps) == 7;
   std::fclose(f);
   if (!ok) return fail(NF_ERR_INVALID_ARG, "%s is not a plan file", path);
   o.timeout_ns = tmo;

@@ -13,7 +13,7 @@
 // grid of S CTAs (one per SM) is the SM share of the nano-operation.
 // Per piece the warp:
 //   * stages each (page, KV head) block of K and of V (P x d bf16, contiguous)
-//     into shared memory with 1-D bulk copies (TMA engine), ATT_STAGES pages in
+//     into shared memory with 1-D bulk copies (TMA engine), STAGES pages in
 //     flight per warp, completion on an mbarrier;
 //   * lane (ts = lane/8, dg = lane%8) owns tokens ts, ts+4, ts+8, ts+12 of a
 //     page and the 8*NCH dims {ch*64 + dg*8 ...}: 16-byte, conflict-free loads;
@@ -28,8 +28,6 @@
 
 namespace nf {
 
-constexpr int ATT_WARPS = 8;
-constexpr int ATT_STAGES = 3;
 constexpr int ATT_P = 16;              // page size the kernel is built for
 constexpr int ATT_MIN_SMEM = 120 * 1024;  // > half an SM: one CTA per SM
 
@@ -44,38 +42,40 @@ int attn_partial_floats(int n_q, int n_kv, int head_dim) {
   return partial_rec_floats(n_q / n_kv, head_dim);
 }
 
-int attn_smem_bytes(int head_dim, int page_size) {
+static int attn_smem_bytes_cfg(int head_dim, int page_size, int warps, int stages) {
   const int blk = page_size * head_dim * 2;
-  const int need = ATT_WARPS * (ATT_STAGES * 2 * blk + ATT_STAGES * 8) + 128;
+  const int need = warps * (stages * 2 * blk + stages * 8) + 128;
   return need < ATT_MIN_SMEM ? ATT_MIN_SMEM : need;
 }
 
+// 8*NCH bf16 of one row -> NCH*4 fp32 pairs (dims ch*64 + dg*8 + 0..7).
 template <int NCH>
-__device__ __forceinline__ void load_row8(const uint8_t* base, int dg, float (&out)[NCH * 8]) {
+__device__ __forceinline__ void load_row_pairs(const uint8_t* base, int dg,
+                                               float2 (&out)[NCH * 4]) {
 #pragma unroll
   for (int ch = 0; ch < NCH; ++ch) {
     const uint4 u = *reinterpret_cast<const uint4*>(base + (ch * 64 + dg * 8) * 2);
-    out[ch * 8 + 0] = bf16lo(u.x); out[ch * 8 + 1] = bf16hi(u.x);
-    out[ch * 8 + 2] = bf16lo(u.y); out[ch * 8 + 3] = bf16hi(u.y);
-    out[ch * 8 + 4] = bf16lo(u.z); out[ch * 8 + 5] = bf16hi(u.z);
-    out[ch * 8 + 6] = bf16lo(u.w); out[ch * 8 + 7] = bf16hi(u.w);
+    out[ch * 4 + 0] = make_float2(bf16lo(u.x), bf16hi(u.x));
+    out[ch * 4 + 1] = make_float2(bf16lo(u.y), bf16hi(u.y));
+    out[ch * 4 + 2] = make_float2(bf16lo(u.z), bf16hi(u.z));
+    out[ch * 4 + 3] = make_float2(bf16lo(u.w), bf16hi(u.w));
   }
 }
 
-template <int GRP, int NCH>
-__global__ void __launch_bounds__(ATT_WARPS * 32, 1) attn_kernel(const AttnArgs a) {
+template <int GRP, int NCH, int WARPS, int STAGES>
+__global__ void __launch_bounds__(WARPS * 32, 1) attn_kernel(const AttnArgs a) {
   constexpr int D = NCH * 64;
   constexpr int P = ATT_P;
   constexpr int BLK = P * D * 2;  // bytes of one (page, KV head) block
-  constexpr int E = NCH * 8;      // dims per lane
+  constexpr int E2 = NCH * 4;     // dim pairs per lane
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ts = lane >> 3, dg = lane & 7;
-  uint8_t* ring = smem + warp * (ATT_STAGES * 2 * BLK);
+  uint8_t* ring = smem + warp * (STAGES * 2 * BLK);
   uint64_t* bar =
-      reinterpret_cast<uint64_t*>(smem + ATT_WARPS * ATT_STAGES * 2 * BLK) + warp * ATT_STAGES;
+      reinterpret_cast<uint64_t*>(smem + WARPS * STAGES * 2 * BLK) + warp * STAGES;
   if (lane == 0) {
-    for (int s = 0; s < ATT_STAGES; ++s) mbar_init(&bar[s], 1);
+    for (int s = 0; s < STAGES; ++s) mbar_init(&bar[s], 1);
     fence_mbar_init();
   }
   __syncwarp();
@@ -104,7 +104,7 @@ __global__ void __launch_bounds__(ATT_WARPS * 32, 1) attn_kernel(const AttnArgs 
     const int* bt = a.block_table + static_cast<size_t>(s) * a.max_pages + b0 / P;
 
     auto issue = [&](int k) {
-      const uint32_t st = (gk + k) % ATT_STAGES;
+      const uint32_t st = (gk + k) % STAGES;
       int page = bt[k];
       if (page < 0 || page >= a.num_pages) {  // never read outside the pool
         raise_status(a.status, ST_BAD_PAGE);
@@ -118,39 +118,41 @@ __global__ void __launch_bounds__(ATT_WARPS * 32, 1) attn_kernel(const AttnArgs 
     };
     int issued = 0;  // pages of this piece whose copies were started (lane 0)
     if (lane == 0) {
-      const int pre = npg < ATT_STAGES ? npg : ATT_STAGES;
+      const int pre = npg < STAGES ? npg : STAGES;
       for (int k = 0; k < pre; ++k) issue(k);
       issued = pre;
     }
 
     // q of the GRP heads of this KV group, scaled to base-2 logits
-    float qv[GRP][E];
+    float2 qv[GRP][E2];
 #pragma unroll
     for (int h = 0; h < GRP; ++h) {
       const uint8_t* qrow = reinterpret_cast<const uint8_t*>(
           a.q + (static_cast<size_t>(t) * n_q + g * GRP + h) * D);
-      load_row8<NCH>(qrow, dg, qv[h]);
+      load_row_pairs<NCH>(qrow, dg, qv[h]);
+      const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
 #pragma unroll
-      for (int e = 0; e < E; ++e) qv[h][e] *= a.scale_log2;
+      for (int e = 0; e < E2; ++e) qv[h][e] = __fmul2_rn(qv[h][e], sc2);
     }
-    float m[GRP], l[GRP], acc[GRP][E];
+    float m[GRP], l[GRP];
+    float2 acc[GRP][E2];
 #pragma unroll
     for (int h = 0; h < GRP; ++h) {
       m[h] = -INFINITY;
       l[h] = 0.f;
 #pragma unroll
-      for (int e = 0; e < E; ++e) acc[h][e] = 0.f;
+      for (int e = 0; e < E2; ++e) acc[h][e] = make_float2(0.f, 0.f);
     }
 
     for (int k = 0; k < npg; ++k) {
-      const uint32_t st = (gk + k) % ATT_STAGES;
-      const uint32_t par = ((gk + k) / ATT_STAGES) & 1;
+      const uint32_t st = (gk + k) % STAGES;
+      const uint32_t par = ((gk + k) / STAGES) & 1;
       const bool got = __all_sync(0xffffffffu, mbar_wait(&bar[st], par, a.timeout_ns));
       if (!got) {
         // drain: every copy this warp started must land before the CTA exits
         if (lane == 0)
           for (int kk = k; kk < issued; ++kk)
-            mbar_wait(&bar[(gk + kk) % ATT_STAGES], ((gk + kk) / ATT_STAGES) & 1, a.timeout_ns);
+            mbar_wait(&bar[(gk + kk) % STAGES], ((gk + kk) / STAGES) & 1, a.timeout_ns);
         failed = true;
         break;
       }
@@ -162,14 +164,14 @@ __global__ void __launch_bounds__(ATT_WARPS * 32, 1) attn_kernel(const AttnArgs 
       for (int jj = 0; jj < 4; ++jj) {
         const int j = ts + 4 * jj;
         valid[jj] = k * P + j < n;
-        float kv[E];
-        load_row8<NCH>(kb + j * D * 2, dg, kv);
+        float2 kv[E2];
+        load_row_pairs<NCH>(kb + j * D * 2, dg, kv);
 #pragma unroll
         for (int h = 0; h < GRP; ++h) {
-          float dot = 0.f;
+          float2 d2 = __fmul2_rn(qv[h][0], kv[0]);
 #pragma unroll
-          for (int e = 0; e < E; ++e) dot = fmaf(qv[h][e], kv[e], dot);
-          sc[jj][h] = dot;
+          for (int e = 1; e < E2; ++e) d2 = __ffma2_rn(qv[h][e], kv[e], d2);
+          sc[jj][h] = d2.x + d2.y;
         }
       }
 #pragma unroll
@@ -190,9 +192,10 @@ __global__ void __launch_bounds__(ATT_WARPS * 32, 1) attn_kernel(const AttnArgs 
         const float mn = fmaxf(m[h], mx);
         if (mn > m[h]) {  // warp-uniform
           const float corr = exp2f(m[h] - mn);
+          const float2 c2 = make_float2(corr, corr);
           l[h] *= corr;
 #pragma unroll
-          for (int e = 0; e < E; ++e) acc[h][e] *= corr;
+          for (int e = 0; e < E2; ++e) acc[h][e] = __fmul2_rn(acc[h][e], c2);
           m[h] = mn;
         }
 #pragma unroll
@@ -205,18 +208,20 @@ __global__ void __launch_bounds__(ATT_WARPS * 32, 1) attn_kernel(const AttnArgs 
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) {
         if (valid[jj]) {  // positions past the piece may hold anything (even NaN)
-          float vv[E];
-          load_row8<NCH>(vb + (ts + 4 * jj) * D * 2, dg, vv);
+          float2 vv[E2];
+          load_row_pairs<NCH>(vb + (ts + 4 * jj) * D * 2, dg, vv);
 #pragma unroll
-          for (int h = 0; h < GRP; ++h)
+          for (int h = 0; h < GRP; ++h) {
+            const float2 p2 = make_float2(sc[jj][h], sc[jj][h]);
 #pragma unroll
-            for (int e = 0; e < E; ++e) acc[h][e] = fmaf(sc[jj][h], vv[e], acc[h][e]);
+            for (int e = 0; e < E2; ++e) acc[h][e] = __ffma2_rn(p2, vv[e], acc[h][e]);
+          }
         }
       }
       __syncwarp();
-      if (lane == 0 && k + ATT_STAGES < npg) {
+      if (lane == 0 && k + STAGES < npg) {
         fence_proxy_async_smem();
-        issue(k + ATT_STAGES);
+        issue(k + STAGES);
         ++issued;
       }
     }
@@ -229,9 +234,11 @@ __global__ void __launch_bounds__(ATT_WARPS * 32, 1) attn_kernel(const AttnArgs 
       l[h] += __shfl_xor_sync(0xffffffffu, l[h], 8);
       l[h] += __shfl_xor_sync(0xffffffffu, l[h], 16);
 #pragma unroll
-      for (int e = 0; e < E; ++e) {
-        acc[h][e] += __shfl_xor_sync(0xffffffffu, acc[h][e], 8);
-        acc[h][e] += __shfl_xor_sync(0xffffffffu, acc[h][e], 16);
+      for (int e = 0; e < E2; ++e) {
+        acc[h][e].x += __shfl_xor_sync(0xffffffffu, acc[h][e].x, 8);
+        acc[h][e].y += __shfl_xor_sync(0xffffffffu, acc[h][e].y, 8);
+        acc[h][e].x += __shfl_xor_sync(0xffffffffu, acc[h][e].x, 16);
+        acc[h][e].y += __shfl_xor_sync(0xffffffffu, acc[h][e].y, 16);
       }
     }
     const int nch = a.tok_nchunks[t];
@@ -244,11 +251,11 @@ __global__ void __launch_bounds__(ATT_WARPS * 32, 1) attn_kernel(const AttnArgs 
 #pragma unroll
         for (int ch = 0; ch < NCH; ++ch) {
           uint4 u;
-          const float* v = &acc[h][ch * 8];
-          u.x = pack_bf16(v[0] * inv, v[1] * inv);
-          u.y = pack_bf16(v[2] * inv, v[3] * inv);
-          u.z = pack_bf16(v[4] * inv, v[5] * inv);
-          u.w = pack_bf16(v[6] * inv, v[7] * inv);
+          const float2* v = &acc[h][ch * 4];
+          u.x = pack_bf16(v[0].x * inv, v[0].y * inv);
+          u.y = pack_bf16(v[1].x * inv, v[1].y * inv);
+          u.z = pack_bf16(v[2].x * inv, v[2].y * inv);
+          u.w = pack_bf16(v[3].x * inv, v[3].y * inv);
           *reinterpret_cast<uint4*>(orow + ch * 64 + dg * 8) = u;
         }
       }
@@ -265,10 +272,9 @@ __global__ void __launch_bounds__(ATT_WARPS * 32, 1) attn_kernel(const AttnArgs 
 #pragma unroll
       for (int ch = 0; ch < NCH; ++ch) {
         float4* dst = reinterpret_cast<float4*>(rec + h * D + ch * 64 + dg * 8);
-        dst[0] = make_float4(acc[h][ch * 8 + 0], acc[h][ch * 8 + 1], acc[h][ch * 8 + 2],
-                             acc[h][ch * 8 + 3]);
-        dst[1] = make_float4(acc[h][ch * 8 + 4], acc[h][ch * 8 + 5], acc[h][ch * 8 + 6],
-                             acc[h][ch * 8 + 7]);
+        const float2* v = &acc[h][ch * 4];
+        dst[0] = make_float4(v[0].x, v[0].y, v[1].x, v[1].y);
+        dst[1] = make_float4(v[2].x, v[2].y, v[3].x, v[3].y);
       }
     }
     if (lane == 0) {
@@ -293,9 +299,9 @@ __global__ void __launch_bounds__(ATT_WARPS * 32, 1) attn_kernel(const AttnArgs 
         const float* r = a.partials + ((row_rec + cc) * n_kv + g) * REC;
         M = fmaxf(M, __ldcg(r + GRP * D + h));
       }
-      float L = 0.f, O[E];
+      float L = 0.f, O[NCH * 8];
 #pragma unroll
-      for (int e = 0; e < E; ++e) O[e] = 0.f;
+      for (int e = 0; e < NCH * 8; ++e) O[e] = 0.f;
       for (int cc = 0; cc < nch; ++cc) {
         const float* r = a.partials + ((row_rec + cc) * n_kv + g) * REC;
         const float w = exp2f(__ldcg(r + GRP * D + h) - M);
@@ -327,18 +333,27 @@ __global__ void __launch_bounds__(ATT_WARPS * 32, 1) attn_kernel(const AttnArgs 
   if (failed) raise_status(a.status, ST_TIMEOUT);
 }
 
-template <int GRP, int NCH>
+template <int GRP, int NCH, int WARPS, int STAGES>
 static cudaError_t launch_t(const AttnArgs& a, int grid, cudaStream_t stream) {
-  const int smem = attn_smem_bytes(NCH * 64, ATT_P);
+  const int smem = attn_smem_bytes_cfg(NCH * 64, ATT_P, WARPS, STAGES);
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(attn_kernel<GRP, NCH>,
+    cudaError_t e = cudaFuncSetAttribute(attn_kernel<GRP, NCH, WARPS, STAGES>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  attn_kernel<GRP, NCH><<<grid, ATT_WARPS * 32, smem, stream>>>(a);
+  attn_kernel<GRP, NCH, WARPS, STAGES><<<grid, WARPS * 32, smem, stream>>>(a);
   return cudaGetLastError();
+}
+
+template <int GRP, int NCH>
+static cudaError_t launch_cfg(const AttnArgs& a, int grid, cudaStream_t stream) {
+  switch (a.warps) {
+    case 10: return launch_t<GRP, NCH, 10, 2>(a, grid, stream);
+    case 12: return launch_t<GRP, NCH, 12, 2>(a, grid, stream);
+    default: return launch_t<GRP, NCH, 8, 3>(a, grid, stream);
+  }
 }
 
 cudaError_t launch_attention(const AttnArgs& a, int grid, cudaStream_t stream) {
@@ -346,7 +361,7 @@ cudaError_t launch_attention(const AttnArgs& a, int grid, cudaStream_t stream) {
   const int grp = a.n_q / a.n_kv;
   const int nch = a.head_dim / 64;
 #define NF_ATT_CASE(G, N) \
-  if (grp == G && nch == N) return launch_t<G, N>(a, grid, stream);
+  if (grp == G && nch == N) return launch_cfg<G, N>(a, grid, stream);
   NF_ATT_CASE(1, 1) NF_ATT_CASE(2, 1) NF_ATT_CASE(4, 1) NF_ATT_CASE(8, 1)
   NF_ATT_CASE(1, 2) NF_ATT_CASE(2, 2) NF_ATT_CASE(4, 2) NF_ATT_CASE(8, 2)
 #undef NF_ATT_CASE

@@ -89,11 +89,11 @@ struct AttnArgs {
   int seg;                   // which attention nano-batch
   int n_q, n_kv, head_dim, page_size, max_pages, num_pages, kv_chunk, max_chunks;
   float scale_log2;          // log2(e) / sqrt(d)
+  int warps;                 // warps per CTA: 8 (3 pages in flight each), 10 or 12 (2 each)
   uint32_t* status;
   unsigned long long timeout_ns;
 };
 int attn_partial_floats(int n_q, int n_kv, int head_dim);  // floats per (row, chunk, kv head)
 cudaError_t launch_attention(const AttnArgs& a, int grid, cudaStream_t stream);
-int attn_smem_bytes(int head_dim, int page_size);
 
 }  // namespace nf

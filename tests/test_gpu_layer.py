@@ -46,7 +46,11 @@ def _check_layer(case, ref, y, kp, vp, rows):
     P = case.shape.page_size
     yg = f64(y)[rows]
     compare(yg, ref["y"], "y")
-    compare(yg - f64(case.x)[rows], ref["y"] - f64(case.x)[rows], "y - x")
+    # y - x isolates the attention and FFN terms; its error floor is the bf16
+    # rounding of y itself (rms ~ 2^-9 |y|), large next to a small delta
+    dref = ref["y"] - f64(case.x)[rows]
+    floor = 2.0 ** -8 * np.sqrt(np.mean(ref["y"] ** 2)) / max(np.sqrt(np.mean(dref ** 2)), 1e-30)
+    compare(yg - f64(case.x)[rows], dref, "y - x", rel_l2=1e-2 + floor)
     sl = torch.as_tensor(ref["slots"], device=DEV)
     kg = f64(kp[sl // P, :, sl % P, :])
     vg = f64(vp[sl // P, :, sl % P, :])
