@@ -296,7 +296,7 @@ def main():
     # the best predicted plans, the last step of the plan search)
     searched = make_plan(None)
     so, _ = searched.info()
-    cands = [("search", searched)]
+    cands = [("search", searched), ("sequential", make_plan(_lib.make_opts(T)))]
     if args.plan == "auto":
         for n in (2, 3):
             ab = [0] + [int(round(T * i / n / 128)) * 128 for i in range(1, n)] + [T]

@@ -134,14 +134,30 @@ __global__ void __launch_bounds__(WARPS * 32, 1) attn_kernel(const AttnArgs a) {
 #pragma unroll
       for (int e = 0; e < E2; ++e) qv[h][e] = __fmul2_rn(qv[h][e], sc2);
     }
-    float m[GRP], l[GRP];
+    // Softmax state.  m_ref[h] is a warp-uniform reference maximum of head h
+    // (base-2 logits); probabilities are exp2(s - m_ref) and the reference is
+    // only raised when a score exceeds it by more than kLazy, so p <= 2^kLazy.
+    // Each lane's value slots always hold the same heads (see below), so the
+    // lane keeps its share of the denominators per slot (lslot).
+    constexpr int V = 4 * GRP;                 // (token slot, head) values per lane
+    constexpr bool kTransposed = V >= 8;       // scores reduced by transposition
+    constexpr int R = kTransposed ? V / 8 : V; // totals a lane holds after the reduction
+    constexpr float kLazy = 8.0f;
+    float m_ref[GRP], lslot[R], msel[R];
+    int hsel[R];                               // head of each slot
     float2 acc[GRP][E2];
 #pragma unroll
     for (int h = 0; h < GRP; ++h) {
-      m[h] = -INFINITY;
-      l[h] = 0.f;
+      m_ref[h] = -INFINITY;
 #pragma unroll
       for (int e = 0; e < E2; ++e) acc[h][e] = make_float2(0.f, 0.f);
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const int idx = kTransposed ? dg * R + r : r;
+      hsel[r] = idx % GRP;
+      lslot[r] = 0.f;
+      msel[r] = -INFINITY;
     }
 
     for (int k = 0; k < npg; ++k) {
@@ -158,61 +174,110 @@ __global__ void __launch_bounds__(WARPS * 32, 1) attn_kernel(const AttnArgs a) {
       }
       const uint8_t* kb = ring + st * 2 * BLK;
       const uint8_t* vb = kb + BLK;
-      float sc[4][GRP];
-      bool valid[4];
+
+      // partial q.k over this lane's dims: v[jj * GRP + h], token ts + 4 jj
+      float v[V];
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) {
-        const int j = ts + 4 * jj;
-        valid[jj] = k * P + j < n;
         float2 kv[E2];
-        load_row_pairs<NCH>(kb + j * D * 2, dg, kv);
+        load_row_pairs<NCH>(kb + (ts + 4 * jj) * D * 2, dg, kv);
 #pragma unroll
         for (int h = 0; h < GRP; ++h) {
-          float2 d2 = __fmul2_rn(qv[h][0], kv[0]);
+          float2 d0 = __fmul2_rn(qv[h][0], kv[0]);
+          float2 d1 = __fmul2_rn(qv[h][1], kv[1]);
 #pragma unroll
-          for (int e = 1; e < E2; ++e) d2 = __ffma2_rn(qv[h][e], kv[e], d2);
-          sc[jj][h] = d2.x + d2.y;
+          for (int e = 2; e < E2; e += 2) {
+            d0 = __ffma2_rn(qv[h][e], kv[e], d0);
+            d1 = __ffma2_rn(qv[h][e + 1], kv[e + 1], d1);
+          }
+          v[jj * GRP + h] = (d0.x + d0.y) + (d1.x + d1.y);
         }
       }
+      // Sum over the 8 dim-group lanes.  Transposed form: at each level a
+      // lane keeps half of its values and adds the partner's matching half, so
+      // after three levels lane dg holds the totals of values dg*R .. dg*R+R-1.
+      if constexpr (kTransposed) {
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj)
+        for (int lvl = 0; lvl < 3; ++lvl) {
+          const int mask = 4 >> lvl;
+          const int half = V >> (lvl + 1);
+          const bool upper = (lane & mask) != 0;
+#pragma unroll
+          for (int i = 0; i < half; ++i) {
+            const float keep = upper ? v[i + half] : v[i];
+            const float send = upper ? v[i] : v[i + half];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+          v[i] += __shfl_xor_sync(0xffffffffu, v[i], 1);
+          v[i] += __shfl_xor_sync(0xffffffffu, v[i], 2);
+          v[i] += __shfl_xor_sync(0xffffffffu, v[i], 4);
+        }
+      }
+      bool valid[R];
+      bool raise = false;
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int idx = kTransposed ? dg * R + r : r;
+        valid[r] = k * P + ts + 4 * (idx / GRP) < n;
+        raise |= valid[r] && v[r] > msel[r] + kLazy;
+      }
+      if (__any_sync(0xffffffffu, raise)) {  // rare: move the reference maxima up
 #pragma unroll
         for (int h = 0; h < GRP; ++h) {
-          float v = sc[jj][h];
-          v += __shfl_xor_sync(0xffffffffu, v, 1);
-          v += __shfl_xor_sync(0xffffffffu, v, 2);
-          v += __shfl_xor_sync(0xffffffffu, v, 4);
-          sc[jj][h] = valid[jj] ? v : -INFINITY;
+          float x = -INFINITY;
+#pragma unroll
+          for (int r = 0; r < R; ++r)
+            if (valid[r] && hsel[r] == h) x = fmaxf(x, v[r]);
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+          const float mn = fmaxf(m_ref[h], x);
+          if (mn > m_ref[h]) {  // warp-uniform
+            const float corr = exp2f(m_ref[h] - mn);
+            const float2 c2 = make_float2(corr, corr);
+#pragma unroll
+            for (int e = 0; e < E2; ++e) acc[h][e] = __fmul2_rn(acc[h][e], c2);
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+              if (hsel[r] == h) lslot[r] *= corr;
+            m_ref[h] = mn;
+          }
         }
 #pragma unroll
-      for (int h = 0; h < GRP; ++h) {
-        float mx = fmaxf(fmaxf(sc[0][h], sc[1][h]), fmaxf(sc[2][h], sc[3][h]));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        const float mn = fmaxf(m[h], mx);
-        if (mn > m[h]) {  // warp-uniform
-          const float corr = exp2f(m[h] - mn);
-          const float2 c2 = make_float2(corr, corr);
-          l[h] *= corr;
+        for (int r = 0; r < R; ++r) {
+          float mm = m_ref[0];
 #pragma unroll
-          for (int e = 0; e < E2; ++e) acc[h][e] = __fmul2_rn(acc[h][e], c2);
-          m[h] = mn;
+          for (int h = 1; h < GRP; ++h) mm = hsel[r] == h ? m_ref[h] : mm;
+          msel[r] = mm;
         }
+      }
+      float pr[R];
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const float p = valid[jj] ? exp2f(sc[jj][h] - m[h]) : 0.f;
-          sc[jj][h] = p;
-          l[h] += p;
-        }
+      for (int r = 0; r < R; ++r) {
+        pr[r] = valid[r] ? exp2f(v[r] - msel[r]) : 0.f;
+        lslot[r] += pr[r];
+      }
+      // probabilities of this lane's tokens for every head
+      float pg[V];
+      if constexpr (kTransposed) {
+#pragma unroll
+        for (int i = 0; i < V; ++i)
+          pg[i] = __shfl_sync(0xffffffffu, pr[i % R], (lane & 24) | (i / R));
+      } else {
+#pragma unroll
+        for (int i = 0; i < V; ++i) pg[i] = pr[i];
       }
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) {
-        if (valid[jj]) {  // positions past the piece may hold anything (even NaN)
+        if (k * P + ts + 4 * jj < n) {  // positions past the piece may hold anything (even NaN)
           float2 vv[E2];
           load_row_pairs<NCH>(vb + (ts + 4 * jj) * D * 2, dg, vv);
 #pragma unroll
           for (int h = 0; h < GRP; ++h) {
-            const float2 p2 = make_float2(sc[jj][h], sc[jj][h]);
+            const float2 p2 = make_float2(pg[jj * GRP + h], pg[jj * GRP + h]);
 #pragma unroll
             for (int e = 0; e < E2; ++e) acc[h][e] = __ffma2_rn(p2, vv[e], acc[h][e]);
           }
@@ -228,11 +293,26 @@ __global__ void __launch_bounds__(WARPS * 32, 1) attn_kernel(const AttnArgs a) {
     if (failed) break;
     gk += npg;
 
-    // merge the four token slots
+    // denominators: gather each head's slots from every lane that holds them
+    float l[GRP], m[GRP];
 #pragma unroll
     for (int h = 0; h < GRP; ++h) {
-      l[h] += __shfl_xor_sync(0xffffffffu, l[h], 8);
-      l[h] += __shfl_xor_sync(0xffffffffu, l[h], 16);
+      float x = 0.f;
+#pragma unroll
+      for (int r = 0; r < R; ++r) x += hsel[r] == h ? lslot[r] : 0.f;
+      if constexpr (kTransposed) {
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+      } else {
+        x += __shfl_xor_sync(0xffffffffu, x, 8);
+        x += __shfl_xor_sync(0xffffffffu, x, 16);
+      }
+      l[h] = x;
+      m[h] = m_ref[h];
+    }
+    // merge the four token slots of the accumulators
+#pragma unroll
+    for (int h = 0; h < GRP; ++h) {
 #pragma unroll
       for (int e = 0; e < E2; ++e) {
         acc[h][e].x += __shfl_xor_sync(0xffffffffu, acc[h][e].x, 8);
