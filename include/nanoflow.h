@@ -207,6 +207,39 @@ nf_status nf_step_metadata(nf_plan plan, const int32_t* block_table, const int32
 nf_status nf_attention(nf_plan plan, const void* q, const void* k_pool, const void* v_pool,
                        const int32_t* block_table, const int32_t* seq_lens, void* o, void* stream);
 
+/* Size of the fixed device working memory of nf_attention_noalloc. */
+#define NF_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/* nf_attention for callers that cannot allocate device memory.  No counterpart
+ * on the pages: it exists for callers of this library that must not call
+ * cudaMalloc, e.g. a host runtime that owns all device memory through its own
+ * pool and gives an operator only its input and output pointers, or a hot
+ * loop that cannot take the device synchronisation an allocation may cause.
+ * It needs no plan.  Inputs and outputs are those of nf_attention (shape and
+ * batch structure as for nf_plan_create; q, o device [T, n_q, head_dim];
+ * pools, block table and seq_lens device, the cache already holding this
+ * step's K/V).  Its working memory (token map, work list, counters, split-KV
+ * partials with 2048-position pieces) is one static device array of
+ * NF_NOALLOC_SCRATCH_BYTES, present on every GPU that loads the library until
+ * the process exits.  A batch that needs more returns NF_ERR_INVALID_ARG
+ * with the required size in nf_last_error(); the need is about
+ * T * ceil(max_pages_per_seq * 16 / 2048) * n_kv * (head_dim * n_q / n_kv + 8) * 4
+ * bytes plus 40 bytes per token (e.g. 1024 tokens of the Llama-3-8B shape
+ * with contexts up to 2048 fit).
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * Every call uses the same array and overwrites what the previous call left;
+ * the counters that must start at zero are cleared by each call.  Calls whose
+ * work overlaps on the GPU (two streams, or two threads) race on the array and
+ * give wrong results: serialise them.  Device-side page-id checks still keep
+ * every read inside the pool, but their status is not reported here.  This
+ * call allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ * routine. */
+nf_status nf_attention_noalloc(const nf_model_shape* shape, const nf_batch_desc* batch,
+                               const void* q, const void* k_pool, const void* v_pool,
+                               const int32_t* block_table, const int32_t* seq_lens, void* o,
+                               void* stream);
+
 /* RMSNorm of rows [0, rows): out = x * g / sqrt(mean(x^2) + eps), fp32
  * arithmetic, bf16 out.  x, out: device [rows, hidden]; g: device [hidden]. */
 nf_status nf_rmsnorm(const void* x, const void* g, void* out, int32_t rows, int32_t hidden,

@@ -69,6 +69,7 @@ _SIGS = {
     "nf_device_sm_count": (c_int32, []),
     "nf_step_metadata": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p]),
     "nf_attention": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "nf_attention_noalloc": (c_int, [POINTER(nf_model_shape), POINTER(nf_batch_desc), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     "nf_rmsnorm": (c_int, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_float, c_void_p]),
     "nf_gemm": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32, c_int32, c_void_p]),
     "nf_plan_buffer_size": (c_int, [c_void_p, c_int32, POINTER(c_size_t)]),
@@ -245,6 +246,16 @@ def step_metadata(plan: Plan, block_table, seq_lens, stream=None):
 def attention(plan: Plan, q, k_pool, v_pool, block_table, seq_lens, o, stream=None):
     check(lib().nf_attention(plan.h, ptr(q), ptr(k_pool), ptr(v_pool), ptr(block_table),
                              ptr(seq_lens), ptr(o), stream_handle(stream)))
+
+
+def attention_noalloc(shape, batch, q, k_pool, v_pool, block_table, seq_lens, o, stream=None):
+    """nf_attention_noalloc: attention without a plan and without any device
+    allocation (fixed working memory inside the library)."""
+    s = make_shape(shape)
+    b = make_batch_desc(batch, hint=False)
+    check(lib().nf_attention_noalloc(ctypes.byref(s), ctypes.byref(b), ptr(q), ptr(k_pool),
+                                     ptr(v_pool), ptr(block_table), ptr(seq_lens), ptr(o),
+                                     stream_handle(stream)))
 
 
 def rmsnorm(x, g, out, eps, stream=None):

@@ -632,6 +632,11 @@ nf_status nf::attention_on(nf_plan p, const void* q, const void* kp, const void*
   return NF_OK;
 }
 
+nf_status nf::set_last_error(nf_status code, const char* msg) {
+  g_err = msg ? msg : "";
+  return code;
+}
+
 // ============================================================== C ABI
 extern "C" {
 
