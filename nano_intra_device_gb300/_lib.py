@@ -142,7 +142,7 @@ def make_batch_desc(batch, hint=True):
 
 
 def make_opts(T, attn_bounds=None, ffn_bounds=None, executor=NF_EXEC_SEQUENTIAL, attn_sms=0,
-              gemm_sms=0, kv_chunk=512, validate=0, timeout_ns=2_000_000_000,
+              gemm_sms=0, kv_chunk=1024, validate=0, timeout_ns=2_000_000_000,
               attn_warps=0) -> nf_plan_opts:
     ab = list(attn_bounds) if attn_bounds is not None else [0, T]
     fb = list(ffn_bounds) if ffn_bounds is not None else list(ab)

@@ -311,7 +311,7 @@ nf_status build_plan(const nf_model_shape* shape, const nf_batch_desc* batch,
       return s;
     }
   }
-  if (p->opts.kv_chunk == 0) p->opts.kv_chunk = 512;
+  if (p->opts.kv_chunk == 0) p->opts.kv_chunk = 1024;
   if (p->opts.timeout_ns == 0) p->opts.timeout_ns = kDefaultTimeoutNs;
   if (p->opts.attn_warps == 0) p->opts.attn_warps = 8;
   nf_status s = check_opts(&p->opts, p->T, num_sms);

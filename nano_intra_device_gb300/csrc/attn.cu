@@ -30,6 +30,7 @@ namespace nf {
 
 constexpr int ATT_P = 16;              // page size the kernel is built for
 constexpr int ATT_MIN_SMEM = 120 * 1024;  // > half an SM: one CTA per SM
+constexpr int ATT_MAX_PIECE_PAGES = 2048 / ATT_P;  // longest split-KV piece, in pages
 
 // Floats of one split-KV partial record: acc [GRP][d], then m [GRP] and
 // l [GRP], padded so every record starts on a 16-byte boundary (the record is
@@ -44,7 +45,7 @@ int attn_partial_floats(int n_q, int n_kv, int head_dim) {
 
 static int attn_smem_bytes_cfg(int head_dim, int page_size, int warps, int stages) {
   const int blk = page_size * head_dim * 2;
-  const int need = warps * (stages * 2 * blk + stages * 8) + 128;
+  const int need = warps * (stages * 2 * blk + stages * 8 + ATT_MAX_PIECE_PAGES * 4) + 128;
   return need < ATT_MIN_SMEM ? ATT_MIN_SMEM : need;
 }
 
@@ -74,6 +75,8 @@ __global__ void __launch_bounds__(WARPS * 32, 1) attn_kernel(const AttnArgs a) {
   uint8_t* ring = smem + warp * (STAGES * 2 * BLK);
   uint64_t* bar =
       reinterpret_cast<uint64_t*>(smem + WARPS * STAGES * 2 * BLK) + warp * STAGES;
+  int* wpages = reinterpret_cast<int*>(smem + WARPS * STAGES * 2 * BLK + WARPS * STAGES * 8) +
+                warp * ATT_MAX_PIECE_PAGES;
   if (lane == 0) {
     for (int s = 0; s < STAGES; ++s) mbar_init(&bar[s], 1);
     fence_mbar_init();
@@ -89,11 +92,14 @@ __global__ void __launch_bounds__(WARPS * 32, 1) attn_kernel(const AttnArgs a) {
   uint32_t gk = 0;  // pages this warp has consumed (ring position)
   bool failed = false;
 
+  // the next piece is claimed one piece ahead, so the atomic's latency hides
+  // behind the current piece
+  int next_idx = 0;
+  if (lane == 0) next_idx = atomicAdd(&a.fetch[seg], 1);
   for (;;) {
-    int idx = 0;
-    if (lane == 0) idx = atomicAdd(&a.fetch[seg], 1);
-    idx = __shfl_sync(0xffffffffu, idx, 0);
+    const int idx = __shfl_sync(0xffffffffu, next_idx, 0);
     if (idx >= total) break;
+    if (lane == 0) next_idx = atomicAdd(&a.fetch[seg], 1);
     const int pair = begin + idx / n_kv, g = idx % n_kv;
     const int t = a.items[2 * pair], c = a.items[2 * pair + 1];
     const int s = a.tok_seq[t];
@@ -101,16 +107,24 @@ __global__ void __launch_bounds__(WARPS * 32, 1) attn_kernel(const AttnArgs a) {
     const int b0 = c * C;
     const int n = min(C, ctx - b0);
     const int npg = (n + P - 1) / P;
-    const int* bt = a.block_table + static_cast<size_t>(s) * a.max_pages + b0 / P;
+    // the piece's page ids, checked once and kept in shared memory for issue()
+    {
+      const int* bt = a.block_table + static_cast<size_t>(s) * a.max_pages + b0 / P;
+      for (int i = lane; i < npg; i += 32) {
+        int page = bt[i];
+        if (page < 0 || page >= a.num_pages) {  // never read outside the pool
+          raise_status(a.status, ST_BAD_PAGE);
+          page = 0;
+        }
+        wpages[i] = page;
+      }
+      __syncwarp();
+    }
 
     auto issue = [&](int k) {
       const uint32_t st = (gk + k) % STAGES;
-      int page = bt[k];
-      if (page < 0 || page >= a.num_pages) {  // never read outside the pool
-        raise_status(a.status, ST_BAD_PAGE);
-        page = 0;
-      }
-      const size_t off = static_cast<size_t>(page) * page_stride + static_cast<size_t>(g) * P * D;
+      const size_t off =
+          static_cast<size_t>(wpages[k]) * page_stride + static_cast<size_t>(g) * P * D;
       uint8_t* kb = ring + st * 2 * BLK;
       mbar_arrive_expect_tx(&bar[st], 2 * BLK);
       bulk_g2s_evict_first(kb, a.k_pool + off, BLK, &bar[st], policy);
@@ -160,23 +174,8 @@ __global__ void __launch_bounds__(WARPS * 32, 1) attn_kernel(const AttnArgs a) {
       msel[r] = -INFINITY;
     }
 
-    for (int k = 0; k < npg; ++k) {
-      const uint32_t st = (gk + k) % STAGES;
-      const uint32_t par = ((gk + k) / STAGES) & 1;
-      const bool got = __all_sync(0xffffffffu, mbar_wait(&bar[st], par, a.timeout_ns));
-      if (!got) {
-        // drain: every copy this warp started must land before the CTA exits
-        if (lane == 0)
-          for (int kk = k; kk < issued; ++kk)
-            mbar_wait(&bar[(gk + kk) % STAGES], ((gk + kk) / STAGES) & 1, a.timeout_ns);
-        failed = true;
-        break;
-      }
-      const uint8_t* kb = ring + st * 2 * BLK;
-      const uint8_t* vb = kb + BLK;
-
-      // partial q.k over this lane's dims: v[jj * GRP + h], token ts + 4 jj
-      float v[V];
+    // partial q.k of one page over this lane's dims: v[jj * GRP + h], token ts + 4 jj
+    auto partial_qk = [&](const uint8_t* kb, float (&v)[V]) {
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) {
         float2 kv[E2];
@@ -193,6 +192,40 @@ __global__ void __launch_bounds__(WARPS * 32, 1) attn_kernel(const AttnArgs a) {
           v[jj * GRP + h] = (d0.x + d0.y) + (d1.x + d1.y);
         }
       }
+    };
+    auto page_ready = [&](int k) {
+      return __all_sync(0xffffffffu, mbar_wait(&bar[(gk + k) % STAGES], ((gk + k) / STAGES) & 1,
+                                               a.timeout_ns));
+    };
+    // on a failed wait: every copy this warp started must land before the CTA exits
+    auto drain_from = [&](int k) {
+      if (lane == 0)
+        for (int kk = k; kk < issued; ++kk)
+          mbar_wait(&bar[(gk + kk) % STAGES], ((gk + kk) / STAGES) & 1, a.timeout_ns);
+    };
+
+    // Software pipeline: the partial q.k of page k+1 is computed before the
+    // softmax and PV of page k, so the two dependency chains overlap.
+    float vq[V];
+    if (page_ready(0)) {
+      partial_qk(ring + (gk % STAGES) * 2 * BLK, vq);
+    } else {
+      drain_from(0);
+      failed = true;
+    }
+    for (int k = 0; k < npg && !failed; ++k) {
+      float v[V];
+#pragma unroll
+      for (int i = 0; i < V; ++i) v[i] = vq[i];
+      if (k + 1 < npg) {
+        if (!page_ready(k + 1)) {
+          drain_from(k + 1);
+          failed = true;
+          break;
+        }
+        partial_qk(ring + ((gk + k + 1) % STAGES) * 2 * BLK, vq);
+      }
+      const uint8_t* vb = ring + ((gk + k) % STAGES) * 2 * BLK + BLK;
       // Sum over the 8 dim-group lanes.  Transposed form: at each level a
       // lane keeps half of its values and adds the partner's matching half, so
       // after three levels lane dg holds the totals of values dg*R .. dg*R+R-1.

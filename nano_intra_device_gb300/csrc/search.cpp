@@ -183,7 +183,7 @@ extern "C" nf_status nf_plan_search(const nf_model_shape* shape, const nf_batch_
   best.n_ffn = 1;
   best.ffn_bounds[1] = T;
   best.executor = NF_EXEC_SEQUENTIAL;
-  best.kv_chunk = 512;
+  best.kv_chunk = 1024;
   best.attn_warps = 8;
   best.timeout_ns = 2000000000LL;
   double best_t = simulate(m, best);
