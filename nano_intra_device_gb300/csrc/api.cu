@@ -172,8 +172,11 @@ nf_status check_opts(const nf_plan_opts* o, int T, int num_sms) {
   if (o->attn_sms < 0 || o->attn_sms > num_sms || o->gemm_sms < 0 || o->gemm_sms > num_sms)
     return fail(NF_ERR_INVALID_ARG, "SM shares must lie in [0, %d]", num_sms);
   if (o->timeout_ns <= 0) return fail(NF_ERR_INVALID_ARG, "timeout_ns must be positive");
-  if (o->attn_warps != 8 && o->attn_warps != 10 && o->attn_warps != 12)
-    return fail(NF_ERR_INVALID_ARG, "attn_warps must be 8, 10 or 12");
+  if (o->attn_warps != 4 && o->attn_warps != 5 && o->attn_warps != 8 && o->attn_warps != 10 &&
+      o->attn_warps != 12)
+    return fail(NF_ERR_INVALID_ARG, "attn_warps must be 4, 5, 8, 10 or 12");
+  if (o->gemm_stages < 2 || o->gemm_stages > 4)
+    return fail(NF_ERR_INVALID_ARG, "gemm_stages must be 2, 3 or 4");
   return NF_OK;
 }
 
@@ -314,6 +317,7 @@ nf_status build_plan(const nf_model_shape* shape, const nf_batch_desc* batch,
   if (p->opts.kv_chunk == 0) p->opts.kv_chunk = 1024;
   if (p->opts.timeout_ns == 0) p->opts.timeout_ns = kDefaultTimeoutNs;
   if (p->opts.attn_warps == 0) p->opts.attn_warps = 8;
+  if (p->opts.gemm_stages == 0) p->opts.gemm_stages = 4;
   nf_status s = check_opts(&p->opts, p->T, num_sms);
   if (s != NF_OK) {
     delete p;
@@ -349,6 +353,7 @@ nf_status refresh_weight_maps(nf_plan p, const nf_layer_weights* w) {
 
 GemmArgs base_args(nf_plan p) {
   GemmArgs g{};
+  g.stages = p->opts.gemm_stages;
   g.status = p->status;
   g.timeout_ns = (unsigned long long)p->opts.timeout_ns;
   g.n_q = p->shape.n_q_heads;
@@ -676,8 +681,8 @@ nf_status nf_plan_save(nf_plan p, const char* path) {
   for (int i = 0; i <= o.n_attn; ++i) std::fprintf(f, " %d", o.attn_bounds[i]);
   std::fprintf(f, "\nffn %d", o.n_ffn);
   for (int i = 0; i <= o.n_ffn; ++i) std::fprintf(f, " %d", o.ffn_bounds[i]);
-  std::fprintf(f, "\nexec %d %d %d %d %d %lld %d\n", o.executor, o.attn_sms, o.gemm_sms,
-               o.kv_chunk, o.validate, (long long)o.timeout_ns, o.attn_warps);
+  std::fprintf(f, "\nexec %d %d %d %d %d %lld %d %d\n", o.executor, o.attn_sms, o.gemm_sms,
+               o.kv_chunk, o.validate, (long long)o.timeout_ns, o.attn_warps, o.gemm_stages);
   std::fclose(f);
   return NF_OK;
 }
@@ -706,8 +711,9 @@ nf_status nf_plan_load(const char* path, nf_plan* out) {
   for (int i = 0; ok && i <= o.n_attn; ++i) ok = std::fscanf(f, " %d", &o.attn_bounds[i]) == 1;
   ok = ok && std::fscanf(f, " ffn %d", &o.n_ffn) == 1 && o.n_ffn >= 1 && o.n_ffn <= NF_MAX_NANO;
   for (int i = 0; ok && i <= o.n_ffn; ++i) ok = std::fscanf(f, " %d", &o.ffn_bounds[i]) == 1;
-  ok = ok && std::fscanf(f, " exec %d %d %d %d %d %lld %d", &o.executor, &o.attn_sms,
-                         &o.gemm_sms, &o.kv_chunk, &o.validate, &tmo, &o.attn_warps) == 7;
+  ok = ok && std::fscanf(f, " exec %d %d %d %d %d %lld %d %d", &o.executor, &o.attn_sms,
+                         &o.gemm_sms, &o.kv_chunk, &o.validate, &tmo, &o.attn_warps,
+                         &o.gemm_stages) == 8;
   std::fclose(f);
   if (!ok) return fail(NF_ERR_INVALID_ARG, "%s is not a plan file", path);
   o.timeout_ns = tmo;
@@ -834,6 +840,7 @@ nf_status nf_gemm(const void* A, const void* B, void* C, const void* R, int32_t 
   g.ldr = N;
   g.status = global_status();
   g.timeout_ns = kDefaultTimeoutNs;
+  g.stages = 4;
   const int cap = (max_sms > 0 && max_sms < sms) ? max_sms : sms;
   NF_CUDA(nf::launch_gemm(epilogue, ta, tb, tb2, g, cap_grid(g.m_tiles * g.n_tiles, cap),
                           static_cast<cudaStream_t>(stream)));

@@ -43,10 +43,16 @@ int attn_partial_floats(int n_q, int n_kv, int head_dim) {
   return partial_rec_floats(n_q / n_kv, head_dim);
 }
 
-static int attn_smem_bytes_cfg(int head_dim, int page_size, int warps, int stages) {
+// Dynamic shared memory of an attention CTA: per warp its ring, barriers and
+// page-id list.  `share` configurations leave room for one GEMM CTA (two ring
+// stages) on the same SM; the 4-warp one is padded past half an SM so that two
+// attention CTAs never pair up on one SM instead.
+static int attn_smem_bytes_cfg(int head_dim, int page_size, int warps, int stages, bool share) {
   const int blk = page_size * head_dim * 2;
   const int need = warps * (stages * 2 * blk + stages * 8 + ATT_MAX_PIECE_PAGES * 4) + 128;
-  return need < ATT_MIN_SMEM ? ATT_MIN_SMEM : need;
+  if (!share) return need < ATT_MIN_SMEM ? ATT_MIN_SMEM : need;
+  const int half_sm = 117 * 1024;
+  return (warps == 4 && need < half_sm) ? half_sm : need;
 }
 
 // 8*NCH bf16 of one row -> NCH*4 fp32 pairs (dims ch*64 + dg*8 + 0..7).
@@ -448,7 +454,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) attn_kernel(const AttnArgs a) {
 
 template <int GRP, int NCH, int WARPS, int STAGES>
 static cudaError_t launch_t(const AttnArgs& a, int grid, cudaStream_t stream) {
-  const int smem = attn_smem_bytes_cfg(NCH * 64, ATT_P, WARPS, STAGES);
+  const int smem = attn_smem_bytes_cfg(NCH * 64, ATT_P, WARPS, STAGES, WARPS < 8);
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(attn_kernel<GRP, NCH, WARPS, STAGES>,
@@ -463,6 +469,8 @@ static cudaError_t launch_t(const AttnArgs& a, int grid, cudaStream_t stream) {
 template <int GRP, int NCH>
 static cudaError_t launch_cfg(const AttnArgs& a, int grid, cudaStream_t stream) {
   switch (a.warps) {
+    case 4: return launch_t<GRP, NCH, 4, 3>(a, grid, stream);
+    case 5: return launch_t<GRP, NCH, 5, 2>(a, grid, stream);
     case 10: return launch_t<GRP, NCH, 10, 2>(a, grid, stream);
     case 12: return launch_t<GRP, NCH, 12, 2>(a, grid, stream);
     default: return launch_t<GRP, NCH, 8, 3>(a, grid, stream);

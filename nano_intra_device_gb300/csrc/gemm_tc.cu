@@ -18,18 +18,21 @@
 namespace nf {
 
 constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int STAGES = 4;
+constexpr int MAX_STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int GEMM_THREADS = 192;
-constexpr int GEMM_SMEM = STAGES * STAGE_BYTES + 1024 + 256;
+// Dynamic shared memory of a CTA with `stages` ring stages: the ring, slack to
+// align it to 1024 bytes, and the barrier block.  4 stages fill an SM (one CTA
+// per SM, exclusive); 3 or 2 leave room for an attention CTA beside it.
+constexpr int gemm_smem_bytes(int stages) { return stages * STAGE_BYTES + 1024 + 256; }
 constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
 
 struct GemmSmemTail {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+  uint64_t full[MAX_STAGES];
+  uint64_t empty[MAX_STAGES];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -80,7 +83,7 @@ __device__ __forceinline__ void tmem_load32(uint32_t taddr, float* v) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-template <int EPI>
+template <int EPI, int STAGES>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmB2, const GemmArgs args) {
@@ -125,7 +128,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t st = 0, ph = 0;
-      uint32_t issued_mask = 0, last_ph[STAGES] = {0, 0, 0, 0};
+      uint32_t issued_mask = 0, last_ph[MAX_STAGES] = {0, 0, 0, 0};
       bool ok = true;
       for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
         const int tm = t % args.m_tiles, tn = t / args.m_tiles;
@@ -347,19 +350,31 @@ int gemm_tiles(int epi, int m_rows, int N) {
   return ((m_rows + BM - 1) / BM) * ((N + bn - 1) / bn);
 }
 
-template <int EPI>
+template <int EPI, int STAGES>
 static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB,
                               const CUtensorMap& tmB2, const GemmArgs& args, int grid,
                               cudaStream_t stream) {
   static bool attr_set = false;  // per process; the attribute is per function
+  constexpr int smem = gemm_smem_bytes(STAGES);
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI, STAGES>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  gemm_tc_kernel<EPI><<<grid, GEMM_THREADS, GEMM_SMEM, stream>>>(tmA, tmB, tmB2, args);
+  gemm_tc_kernel<EPI, STAGES><<<grid, GEMM_THREADS, smem, stream>>>(tmA, tmB, tmB2, args);
   return cudaGetLastError();
+}
+
+template <int EPI>
+static cudaError_t launch_epi(const CUtensorMap& tmA, const CUtensorMap& tmB,
+                              const CUtensorMap& tmB2, const GemmArgs& args, int grid,
+                              cudaStream_t stream) {
+  switch (args.stages) {
+    case 2: return launch_one<EPI, 2>(tmA, tmB, tmB2, args, grid, stream);
+    case 3: return launch_one<EPI, 3>(tmA, tmB, tmB2, args, grid, stream);
+    default: return launch_one<EPI, 4>(tmA, tmB, tmB2, args, grid, stream);
+  }
 }
 
 cudaError_t launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB,
@@ -367,10 +382,10 @@ cudaError_t launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB,
                         cudaStream_t stream) {
   if (grid <= 0) return cudaSuccess;
   switch (epi) {
-    case EPI_STORE: return launch_one<EPI_STORE>(tmA, tmB, tmB2, args, grid, stream);
-    case EPI_RESID: return launch_one<EPI_RESID>(tmA, tmB, tmB2, args, grid, stream);
-    case EPI_SWIGLU: return launch_one<EPI_SWIGLU>(tmA, tmB, tmB2, args, grid, stream);
-    case EPI_QKV: return launch_one<EPI_QKV>(tmA, tmB, tmB2, args, grid, stream);
+    case EPI_STORE: return launch_epi<EPI_STORE>(tmA, tmB, tmB2, args, grid, stream);
+    case EPI_RESID: return launch_epi<EPI_RESID>(tmA, tmB, tmB2, args, grid, stream);
+    case EPI_SWIGLU: return launch_epi<EPI_SWIGLU>(tmA, tmB, tmB2, args, grid, stream);
+    case EPI_QKV: return launch_epi<EPI_QKV>(tmA, tmB, tmB2, args, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -27,6 +27,7 @@ struct GemmArgs {
   __nv_bfloat16* v_pool;
   int n_q, n_kv, head_dim, page_size;
   float log2_theta;
+  int stages;           // ring stages: 4 (fills an SM), 3 or 2 (room for attention)
   uint32_t* status;
   unsigned long long timeout_ns;
 };
@@ -89,7 +90,8 @@ struct AttnArgs {
   int seg;                   // which attention nano-batch
   int n_q, n_kv, head_dim, page_size, max_pages, num_pages, kv_chunk, max_chunks;
   float scale_log2;          // log2(e) / sqrt(d)
-  int warps;                 // warps per CTA: 8 (3 pages in flight each), 10 or 12 (2 each)
+  int warps;                 // warps per CTA: 8 (3 pages in flight each), 10 or 12 (2 each);
+                             // 4 (3 each) or 5 (2 each) leave room for a 2-stage GEMM CTA
   uint32_t* status;
   unsigned long long timeout_ns;
 };

@@ -214,7 +214,7 @@ extern "C" nf_status nf_profile(const nf_model_shape* shape, int32_t max_tokens,
 
   // 4) attention beside a GEMM on the other SMs (the measured R -> P table)
   js += "  \"overlap\": [";
-  double fac_sum = 0;
+  double fac_sum = 0, gfac_sum = 0;
   int fac_n = 0;
   for (int k = 3; k <= 6; ++k) {
     const int Sa = sms * k / 8, Sg = sms - Sa;
@@ -244,6 +244,7 @@ extern "C" nf_status nf_profile(const nf_model_shape* shape, int32_t max_tokens,
     const double p_attn = alone_a / ta;
     const double p_gemm = alone_g * reps / tg;
     fac_sum += p_attn;
+    gfac_sum += p_gemm;
     ++fac_n;
     std::snprintf(buf, sizeof(buf),
                   "%s{\"attn_sms\": %d, \"gemm_sms\": %d, \"attn_alone_ms\": %.5g, "
@@ -253,6 +254,7 @@ extern "C" nf_status nf_profile(const nf_model_shape* shape, int32_t max_tokens,
   }
   js += "],\n";
   add("overlap_bw_factor", fac_sum / fac_n);
+  add("overlap_gemm_factor", gfac_sum / fac_n);
   // launch cost: a one-tile GEMM
   add("gemm_launch_s", time_ms([&] { nf_gemm(A, W, C, nullptr, 128, 256, 64, 0, 0, sa); }, sa, 9) * 1e-3);
   add("attn_launch_s", 4e-6);

@@ -30,13 +30,16 @@
 
 namespace {
 
+// Defaults are GB300 measurements of this library's kernels (nf_profile on the
+// 8B-shaped layer); a profile file overrides them.
 struct Rates {
-  double gemm_flops_per_sm = 1.9e15 / 152 * 0.75;  // sustained per-SM tensor rate
-  double hbm_bps = 6.8e12 * 0.9;                   // achievable HBM bandwidth
-  double attn_bps_per_sm = 60e9;                   // attention bytes/s one SM sustains
+  double gemm_flops_per_sm = 12.6e12;  // tensor rate of a GEMM confined to S SMs, per SM
+  double hbm_bps = 6.4e12;             // attention bandwidth with every SM
+  double attn_bps_per_sm = 44e9;       // attention bytes/s one SM sustains
   double gemm_launch_s = 4e-6;
   double attn_launch_s = 4e-6;
-  double overlap_bw_factor = 0.92;                 // HBM share attention keeps next to GEMMs
+  double overlap_bw_factor = 0.94;     // attention speed kept beside a GEMM on other SMs
+  double overlap_gemm_factor = 0.95;   // GEMM speed kept beside attention on other SMs
 };
 
 double json_number(const std::string& s, const char* key, double dflt) {
@@ -63,6 +66,7 @@ bool load_rates(const char* path, Rates* r) {
   r->gemm_launch_s = json_number(s, "gemm_launch_s", r->gemm_launch_s);
   r->attn_launch_s = json_number(s, "attn_launch_s", r->attn_launch_s);
   r->overlap_bw_factor = json_number(s, "overlap_bw_factor", r->overlap_bw_factor);
+  r->overlap_gemm_factor = json_number(s, "overlap_gemm_factor", r->overlap_gemm_factor);
   return true;
 }
 
@@ -115,8 +119,9 @@ double simulate(const Model& m, const nf_plan_opts& o) {
   const int gsm = o.gemm_sms > 0 ? o.gemm_sms : std::max(1, all - attn_sms);
   double tg = 0, ta = 0;
   std::vector<double> q_done(n), a_done(n);
+  const double slow = 1.0 / m.r.overlap_gemm_factor;
   for (int i = 0; i < n; ++i) {
-    tg += m.qkv_time(o.attn_bounds[i + 1] - o.attn_bounds[i], i == 0 ? all : gsm);
+    tg += m.qkv_time(o.attn_bounds[i + 1] - o.attn_bounds[i], i == 0 ? all : gsm) * (i == 0 ? 1.0 : slow);
     q_done[i] = tg;
   }
   for (int i = 0; i < n; ++i) {
@@ -128,9 +133,10 @@ double simulate(const Model& m, const nf_plan_opts& o) {
   for (int i = 0; i < n; ++i) {
     tg = std::max(tg, a_done[i]);
     const int S = (i == n - 1) ? all : gsm;
-    tg += m.o_time(o.attn_bounds[i + 1] - o.attn_bounds[i], S);
+    const double f = (i == n - 1) ? 1.0 : slow;
+    tg += m.o_time(o.attn_bounds[i + 1] - o.attn_bounds[i], S) * f;
     while (next_ffn < o.n_ffn && o.ffn_bounds[next_ffn + 1] <= o.attn_bounds[i + 1]) {
-      tg += m.ffn_time(o.ffn_bounds[next_ffn + 1] - o.ffn_bounds[next_ffn], S);
+      tg += m.ffn_time(o.ffn_bounds[next_ffn + 1] - o.ffn_bounds[next_ffn], S) * f;
       ++next_ffn;
     }
   }
@@ -185,6 +191,7 @@ extern "C" nf_status nf_plan_search(const nf_model_shape* shape, const nf_batch_
   best.executor = NF_EXEC_SEQUENTIAL;
   best.kv_chunk = 1024;
   best.attn_warps = 8;
+  best.gemm_stages = 4;
   best.timeout_ns = 2000000000LL;
   double best_t = simulate(m, best);
 
