@@ -107,8 +107,9 @@ typedef struct {
   int32_t attn_sms;   /* SMs for attention while it overlaps GEMMs (0 = automatic) */
   int32_t gemm_sms;   /* SMs for a GEMM while it overlaps attention (0 = the rest) */
   int32_t kv_chunk;   /* split-KV piece in tokens, multiple of page_size, <= 2048 (0 = 1024) */
-  int32_t attn_warps; /* warps per attention CTA: 8, 10 or 12 fill an SM; 4 or 5 share
-                         each SM with one GEMM CTA of gemm_stages = 2 (0 = 8) */
+  int32_t attn_warps; /* warps per attention CTA: 8, or 12 / 16 as warp pairs that split
+                         head_dim 128, fill an SM; 4 or 5 share each SM with one GEMM
+                         CTA of gemm_stages = 2 (0 = 8) */
   int32_t gemm_stages; /* shared-memory ring stages of the GEMM kernel: 4 fills an SM;
                           2 lets an attention CTA of 4 or 5 warps run on the same SM (0 = 4) */
   int32_t validate;   /* 1 = check page ids and lengths on the device */

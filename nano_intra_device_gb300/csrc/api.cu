@@ -172,9 +172,9 @@ nf_status check_opts(const nf_plan_opts* o, int T, int num_sms) {
   if (o->attn_sms < 0 || o->attn_sms > num_sms || o->gemm_sms < 0 || o->gemm_sms > num_sms)
     return fail(NF_ERR_INVALID_ARG, "SM shares must lie in [0, %d]", num_sms);
   if (o->timeout_ns <= 0) return fail(NF_ERR_INVALID_ARG, "timeout_ns must be positive");
-  if (o->attn_warps != 4 && o->attn_warps != 5 && o->attn_warps != 8 && o->attn_warps != 10 &&
-      o->attn_warps != 12)
-    return fail(NF_ERR_INVALID_ARG, "attn_warps must be 4, 5, 8, 10 or 12");
+  if (o->attn_warps != 4 && o->attn_warps != 5 && o->attn_warps != 8 && o->attn_warps != 12 &&
+      o->attn_warps != 16)
+    return fail(NF_ERR_INVALID_ARG, "attn_warps must be 4, 5, 8, 12 or 16");
   if (o->gemm_stages < 2 || o->gemm_stages > 4)
     return fail(NF_ERR_INVALID_ARG, "gemm_stages must be 2, 3 or 4");
   return NF_OK;

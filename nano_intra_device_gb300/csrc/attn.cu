@@ -32,13 +32,6 @@ constexpr int ATT_P = 16;              // page size the kernel is built for
 constexpr int ATT_MIN_SMEM = 120 * 1024;  // > half an SM: one CTA per SM
 constexpr int ATT_MAX_PIECE_PAGES = 2048 / ATT_P;  // longest split-KV piece, in pages
 
-// Floats of one split-KV partial record: acc [GRP][d], then m [GRP] and
-// l [GRP], padded so every record starts on a 16-byte boundary (the record is
-// written and read with 16-byte vector accesses).
-__host__ __device__ constexpr int partial_rec_floats(int grp, int head_dim) {
-  return grp * head_dim + ((2 * grp + 3) / 4) * 4;
-}
-
 int attn_partial_floats(int n_q, int n_kv, int head_dim) {
   return partial_rec_floats(n_q / n_kv, head_dim);
 }
@@ -471,8 +464,10 @@ static cudaError_t launch_cfg(const AttnArgs& a, int grid, cudaStream_t stream) 
   switch (a.warps) {
     case 4: return launch_t<GRP, NCH, 4, 3>(a, grid, stream);
     case 5: return launch_t<GRP, NCH, 5, 2>(a, grid, stream);
-    case 10: return launch_t<GRP, NCH, 10, 2>(a, grid, stream);
-    case 12: return launch_t<GRP, NCH, 12, 2>(a, grid, stream);
+    case 12:
+    case 16:  // warp pairs split the head dims (head_dim 128 only)
+      if (NCH == 2) return launch_attention_pair(a, grid, stream);
+      return launch_t<GRP, NCH, 8, 3>(a, grid, stream);
     default: return launch_t<GRP, NCH, 8, 3>(a, grid, stream);
   }
 }

@@ -90,12 +90,20 @@ struct AttnArgs {
   int seg;                   // which attention nano-batch
   int n_q, n_kv, head_dim, page_size, max_pages, num_pages, kv_chunk, max_chunks;
   float scale_log2;          // log2(e) / sqrt(d)
-  int warps;                 // warps per CTA: 8 (3 pages in flight each), 10 or 12 (2 each);
-                             // 4 (3 each) or 5 (2 each) leave room for a 2-stage GEMM CTA
+  int warps;                 // warps per CTA: 8 (3 pages in flight each); 12 or 16: warp
+                             // pairs (head_dim 128); 4 or 5 leave room for a 2-stage GEMM CTA
   uint32_t* status;
   unsigned long long timeout_ns;
 };
 int attn_partial_floats(int n_q, int n_kv, int head_dim);  // floats per (row, chunk, kv head)
+// Floats of one split-KV partial record: acc [GRP][d], then m [GRP] and
+// l [GRP], padded so every record starts on a 16-byte boundary (the record is
+// written and read with 16-byte vector accesses).
+__host__ __device__ constexpr int partial_rec_floats(int grp, int head_dim) {
+  return grp * head_dim + ((2 * grp + 3) / 4) * 4;
+}
+// Warp-pair variant for head_dim 128 (warps 12: 6 pairs x 4 stages; 16: 8 pairs x 3).
+cudaError_t launch_attention_pair(const AttnArgs& a, int grid, cudaStream_t stream);
 cudaError_t launch_attention(const AttnArgs& a, int grid, cudaStream_t stream);
 
 }  // namespace nf

@@ -137,7 +137,7 @@ def test_metadata_flags_bad_page_without_faulting():
 
 
 # -------------------------------------------------------------- attention
-def _attention_case(shape, batch, rows, bounds, kv_chunk, seed=0):
+def _attention_case(shape, batch, rows, bounds, kv_chunk, seed=0, warps=0):
     T = batch.n_tokens
     kp, vp = wl.make_pools(shape, batch, DEV, seed=seed + 3, appended=True)
     q = _rand(T, shape.n_q, shape.head_dim, seed=seed + 20)
@@ -152,7 +152,7 @@ def _attention_case(shape, batch, rows, bounds, kv_chunk, seed=0):
         K = f64(kp[pages, :, offs, :])
         V = f64(vp[pages, :, offs, :])
         ref[t] = orc.attention_one(f64(q[t]), K, V, shape.n_q, shape.n_kv)
-    plan = _lib.Plan(shape, batch, _lib.make_opts(T, bounds, kv_chunk=kv_chunk))
+    plan = _lib.Plan(shape, batch, _lib.make_opts(T, bounds, kv_chunk=kv_chunk, attn_warps=warps))
     o = torch.empty(T, shape.n_q, shape.head_dim, dtype=torch.bfloat16, device=DEV)
     _lib.attention(plan, q.to(DEV), kp, vp, torch.from_numpy(batch.block_table).to(DEV),
                    torch.from_numpy(batch.seq_lens).to(DEV), o)
@@ -170,13 +170,16 @@ def test_attention_tiny_all_rows(kv_chunk):
 
 
 @pytest.mark.parametrize("grp,d", [(1, 64), (2, 128), (4, 128), (8, 128), (8, 64)])
-def test_attention_gqa_and_head_dims(grp, d):
+@pytest.mark.parametrize("warps", [8, 4, 5, 12, 16])
+def test_attention_gqa_and_head_dims(grp, d, warps):
     shape = wl.Shape(hidden=512, n_q=2 * grp, n_kv=2, head_dim=d, ffn=512)
     b = wl.make_batch(shape, [1, 15, 16, 17, 700, 1100], [9], [40], seed_bt=7)
-    _attention_case(shape, b, list(range(b.n_tokens)), [0, 3, b.n_tokens], 256, seed=grp)
+    _attention_case(shape, b, list(range(b.n_tokens)), [0, 3, b.n_tokens], 256, seed=grp,
+                    warps=warps)
 
 
-def test_attention_llama8b_sampled_rows():
+@pytest.mark.parametrize("warps", [8, 12, 16])
+def test_attention_llama8b_sampled_rows(warps):
     b = wl.llama8b_batch()
     T = b.n_tokens
     ctx = b.seq_lens[: b.n_decode]
@@ -185,4 +188,4 @@ def test_attention_llama8b_sampled_rows():
                       rng.choice(b.n_decode, 40, replace=False).tolist() +
                       [b.n_decode, b.n_decode + 1, T - 1] +
                       (b.n_decode + rng.choice(256, 8, replace=False)).tolist()))
-    _attention_case(wl.llama8b_shape(), b, rows, [0, 1024, T], 512)
+    _attention_case(wl.llama8b_shape(), b, rows, [0, 1024, T], 512, warps=warps)

@@ -178,13 +178,15 @@ def big():
     return case, rows, case.oracle(rows=rows)
 
 
-@pytest.mark.parametrize("n", [1, 2, 3, 4])
-def test_llama8b_sampled_rows_by_nano_batch_count(big, n):
+@pytest.mark.parametrize("n,warps,stages", [(1, 8, 4), (2, 8, 4), (3, 16, 4), (4, 12, 4),
+                                            (2, 4, 2), (1, 16, 4)])
+def test_llama8b_sampled_rows_by_nano_batch_count(big, n, warps, stages):
     case, rows, ref = big
     T = case.batch.n_tokens
     ab = [0] + [int(round(T * i / n / 128)) * 128 for i in range(1, n)] + [T]
     ex = _lib.NF_EXEC_SEQUENTIAL if n == 1 else _lib.NF_EXEC_STREAMS
-    plan, y, kp, vp = case.run(_lib.make_opts(T, ab, ab, executor=ex, attn_sms=96))
+    plan, y, kp, vp = case.run(_lib.make_opts(T, ab, ab, executor=ex, attn_sms=96,
+                                              attn_warps=warps, gemm_stages=stages))
     plan.close()
     _check_layer(case, ref, y, kp, vp, np.asarray(rows))
     assert torch.isfinite(y).all()
