@@ -39,6 +39,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from nano_intra_device_gb300 import costmodel as cm  # noqa: E402
+from nano_intra_device_gb300 import replicas  # noqa: E402
 from nano_intra_device_gb300 import workload as wl  # noqa: E402
 
 METRIC = "tokens/s per GB300 for mixed prefill+decode layer step; % of layer roofline"
@@ -200,31 +201,18 @@ def cpu_cores():
         return os.cpu_count()
 
 
-# ---------------------------------------------------------------- distributed
+# ---------------------------------------------------------------- replicas
 def dist_setup(n):
-    rank, world, local = 0, 1, 0
-    if "WORLD_SIZE" in os.environ and int(os.environ["WORLD_SIZE"]) > 1:
-        import torch.distributed as dist
-        local = int(os.environ.get("LOCAL_RANK", 0))
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-        rank, world = dist.get_rank(), dist.get_world_size()
-    return rank, world, local
+    """One process per GPU, each an independent replica (no data-path collective)."""
+    return replicas.setup()
 
 
 def barrier(world):
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
+    replicas.barrier(world)
 
 
 def max_over_ranks(v, world):
-    if world == 1:
-        return v
-    import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+    return replicas.max_over_ranks(v, world)
 
 
 # --------------------------------------------------------------- reference
@@ -430,9 +418,7 @@ def main():
     if rank == 0:
         print(json.dumps(line), flush=True)
     plan.close()
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
+    replicas.teardown(world)
 
 
 if __name__ == "__main__":
