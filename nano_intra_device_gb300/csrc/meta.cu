@@ -32,19 +32,30 @@ __device__ __forceinline__ int upper_index(const int* bounds, int n, int t) {
   return lo;
 }
 
+constexpr int META_SMEM_SEQ = 8192;  // sequences whose token starts fit in shared memory
+
 __global__ void __launch_bounds__(META_THREADS) meta_kernel(const MetaArgs a) {
   __shared__ int hist[META_MAX_SEG * META_MAX_BUCKETS];
   __shared__ int cursor[META_MAX_SEG * META_MAX_BUCKETS];
+  __shared__ int sbegin[META_SMEM_SEQ + 1];
+  __shared__ int sseg[META_MAX_SEG + 1];
   const int P = a.page_size, C = a.kv_chunk;
   const int nb = C / P;  // buckets: pieces of 1..nb pages
   for (int i = threadIdx.x; i < META_MAX_SEG * META_MAX_BUCKETS; i += META_THREADS) hist[i] = 0;
+  // the token starts of the sequences and the nano-batch bounds are searched
+  // once per token: keep them in shared memory when they fit
+  const bool in_smem = a.n_seq <= META_SMEM_SEQ;
+  if (in_smem)
+    for (int i = threadIdx.x; i <= a.n_seq; i += META_THREADS) sbegin[i] = a.tok_begin[i];
+  for (int i = threadIdx.x; i <= a.n_seg; i += META_THREADS) sseg[i] = a.seg_bounds[i];
   __syncthreads();
+  const int* tb = in_smem ? sbegin : a.tok_begin;
 
   // pass 1: token map, slots, piece histogram
   for (int t = threadIdx.x; t < a.n_tok; t += META_THREADS) {
-    const int s = upper_index(a.tok_begin, a.n_seq, t);
+    const int s = upper_index(tb, a.n_seq, t);
     const int L = a.seq_lens[s], q = a.q_lens[s];
-    int pos = L - q + (t - a.tok_begin[s]);
+    int pos = L - q + (t - tb[s]);
     bool ok = true;
     if (q < 1 || L < q || pos >= a.max_pages * P) {
       raise_status(a.status, ST_BAD_LEN);
@@ -79,7 +90,7 @@ __global__ void __launch_bounds__(META_THREADS) meta_kernel(const MetaArgs a) {
     a.tok_pos[t] = pos;
     a.tok_slot[t] = slot;
     a.tok_nchunks[t] = nch;
-    const int seg = upper_index(a.seg_bounds, a.n_seg, t);
+    const int seg = upper_index(sseg, a.n_seg, t);
     for (int c = 0; c < nch; ++c) {
       const int len = min(C, ctx - c * C);
       const int npg = (len + P - 1) / P;
@@ -107,7 +118,7 @@ __global__ void __launch_bounds__(META_THREADS) meta_kernel(const MetaArgs a) {
   for (int t = threadIdx.x; t < a.n_tok; t += META_THREADS) {
     const int ctx = a.tok_pos[t] + 1;
     const int nch = a.tok_nchunks[t];
-    const int seg = upper_index(a.seg_bounds, a.n_seg, t);
+    const int seg = upper_index(sseg, a.n_seg, t);
     for (int c = 0; c < nch; ++c) {
       const int len = min(C, ctx - c * C);
       const int npg = (len + P - 1) / P;

@@ -267,3 +267,34 @@ def layer_step(shape, w64: dict, x, k_pool, v_pool, block_table, seq_lens, q_len
                    q=np.stack([qrow[t] for t in rows.tolist()]),
                    o=o, h=h, n2=n2, a=a)
     return out
+
+
+# --------------------------------------------------------------------------
+# a stack of layers with embedding and LM head
+
+def stack_step(shape, embed, norm_f, lm_head, layers64: list, tokens, pools: list, block_table,
+               seq_lens, q_lens, rows=None) -> dict:
+    """A decoder stack over one mixed step: x = embed[tokens]; each layer's step
+    (its own K/V pools, the shared block table and lengths); logits =
+    RMSNorm(x; norm_f) lm_head^T.
+
+    layers64: float64 weight dicts, one per layer (see weights_f64); pools:
+    (k_pool, v_pool) per layer.  rows: the tokens whose logits are wanted;
+    every layer computes the rows those need (their earlier prefill rows).
+    Returns {"rows", "logits" [len(rows), vocab], "x_final"}.
+    """
+    q_lens = np.asarray(q_lens, np.int64)
+    seq_lens = np.asarray(seq_lens, np.int64)
+    seq, _ = token_map(q_lens, seq_lens)
+    T = len(seq)
+    rows = np.arange(T, dtype=np.int64) if rows is None else np.asarray(rows, np.int64)
+    need = _needed_rows(seq, rows)
+    E = f64(embed)
+    x = np.zeros((T, shape.hidden))
+    x[need] = E[np.asarray(tokens)[need]]
+    for w64, (kp, vp) in zip(layers64, pools):
+        out = layer_step(shape, w64, x, kp, vp, block_table, seq_lens, q_lens, rows=need)
+        x = x.copy()
+        x[need] = out["y"]
+    xf = rmsnorm(x[rows], f64(norm_f), shape.rms_eps)
+    return {"rows": rows, "logits": xf @ f64(lm_head).T, "x_final": x[rows]}

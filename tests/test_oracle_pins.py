@@ -356,3 +356,52 @@ def test_silu_values():
     z = np.array([0.0, 1.0, -1.0, 20.0])
     np.testing.assert_allclose(orc.silu(z), [0.0, 1 / (1 + math.exp(-1)), -1 / (1 + math.e), 20 / (1 + math.exp(-20))],
                                rtol=1e-15)
+
+
+# ------------------------------------------------------------------ stack
+
+def _stack_inputs(n_layers=2, vocab=97):
+    shape = wl.tiny_shape()
+    b = wl.tiny_batch()
+    g = torch.Generator().manual_seed(11)
+    embed = torch.randn(vocab, shape.hidden, generator=g).to(torch.bfloat16)
+    lm_head = (torch.randn(vocab, shape.hidden, generator=g) * 0.02).to(torch.bfloat16)
+    norm_f = (1 + 0.1 * torch.randn(shape.hidden, generator=g)).to(torch.bfloat16)
+    tokens = torch.randint(0, vocab, (b.n_tokens,), generator=g).numpy()
+    layers = [wl.make_weights(shape, seed=20 + i, gain_std=0.1) for i in range(n_layers)]
+    pools = [wl.make_pools(shape, b, "cpu", seed=40 + i) for i in range(n_layers)]
+    return shape, b, embed, norm_f, lm_head, tokens, layers, pools
+
+
+def test_stack_one_layer_is_embed_layer_head():
+    shape, b, embed, norm_f, lm_head, tokens, layers, pools = _stack_inputs(1)
+    w64 = [orc.weights_f64(layers[0])]
+    st = orc.stack_step(shape, embed, norm_f, lm_head, w64, tokens, pools, b.block_table,
+                        b.seq_lens, b.q_lens)
+    x = embed[torch.as_tensor(tokens)]
+    lay = orc.layer_step(shape, w64[0], x, pools[0][0], pools[0][1], b.block_table, b.seq_lens,
+                         b.q_lens)
+    ref = orc.rmsnorm(lay["y"], orc.f64(norm_f), shape.rms_eps) @ orc.f64(lm_head).T
+    np.testing.assert_allclose(st["logits"], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_stack_with_silent_layers_is_a_normed_embedding_lookup():
+    shape, b, embed, norm_f, lm_head, tokens, layers, pools = _stack_inputs(3)
+    zero = [{k: (torch.zeros_like(v) if k.startswith("w_") else v) for k, v in L.items()}
+            for L in layers]
+    st = orc.stack_step(shape, embed, norm_f, lm_head, [orc.weights_f64(z) for z in zero], tokens,
+                        pools, b.block_table, b.seq_lens, b.q_lens)
+    e = orc.f64(embed)[tokens]
+    ref = (e / np.sqrt(np.mean(e * e, -1, keepdims=True) + shape.rms_eps)) * orc.f64(norm_f)
+    np.testing.assert_allclose(st["logits"], ref @ orc.f64(lm_head).T, rtol=1e-12, atol=1e-12)
+
+
+def test_stack_rows_subset_equals_full():
+    shape, b, embed, norm_f, lm_head, tokens, layers, pools = _stack_inputs(2)
+    w64 = [orc.weights_f64(L) for L in layers]
+    full = orc.stack_step(shape, embed, norm_f, lm_head, w64, tokens, pools, b.block_table,
+                          b.seq_lens, b.q_lens)
+    rows = [1, 4, 20, 35]
+    sub = orc.stack_step(shape, embed, norm_f, lm_head, w64, tokens, pools, b.block_table,
+                         b.seq_lens, b.q_lens, rows=rows)
+    np.testing.assert_allclose(sub["logits"], full["logits"][rows], rtol=1e-12, atol=1e-12)
