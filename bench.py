@@ -57,6 +57,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-ablation", action="store_true")
     ap.add_argument("--plan", default="auto", help="auto | search | n=<k>,sms=<s>")
+    ap.add_argument("--workload", default="layer", choices=["layer", "stack"],
+                    help="layer: the single 8B-shaped layer step (default); stack: the 32-layer "
+                         "8B-shaped stack with embedding and LM head, decode batches")
+    ap.add_argument("--batch", type=int, default=256, help="decode requests of the stack workload")
     return ap.parse_args()
 
 
@@ -258,10 +262,71 @@ def time_steps(fn, steps, warmup, world, stream):
     return e0.elapsed_time(e1) / steps
 
 
+def run_stack(args):
+    """32-layer 8B-shaped stack, decode-only batch, eager and CUDA-graph replay."""
+    from nano_intra_device_gb300 import _lib
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    shape = wl.llama8b_shape()
+    L, vocab, B = 32, 128256, args.batch
+    ctx = wl.lognormal_contexts(B, 600.0, 1.0, 1, 8192, seed=1)
+    batch = wl.make_batch(shape, ctx, [], None, seed_bt=2, slack=0.01, max_pages=8192 // 16)
+    g = torch.Generator(device=dev).manual_seed(0)
+
+    def rn(*sz, std=0.02):
+        return (torch.randn(*sz, generator=g, device=dev) * std).to(torch.bfloat16)
+    H, F = shape.hidden, shape.ffn
+    layers = [{"w_qkv": rn(shape.qkv_rows, H), "w_o": rn(H, shape.n_q * shape.head_dim),
+               "w_gate_up": rn(2 * F, H), "w_down": rn(H, F),
+               "norm1": torch.ones(H, dtype=torch.bfloat16, device=dev),
+               "norm2": torch.ones(H, dtype=torch.bfloat16, device=dev)} for _ in range(L)]
+    embed, lm_head = rn(vocab, H, std=1.0), rn(vocab, H)
+    norm_f = torch.ones(H, dtype=torch.bfloat16, device=dev)
+    pools = [wl.make_pools(shape, batch, dev, seed=100 + l) for l in range(L)]
+    tokens = torch.randint(0, vocab, (B,), generator=g, device=dev, dtype=torch.int32)
+    bt = torch.from_numpy(batch.block_table).to(dev)
+    sl = torch.from_numpy(batch.seq_lens).to(dev)
+    logits = torch.empty(B, vocab, dtype=torch.bfloat16, device=dev)
+    plan = _lib.Plan(shape, batch, None)
+    sa = _lib.StackArgs(embed, norm_f, lm_head, layers, pools)
+    stream = torch.cuda.current_stream()
+    step = lambda: _lib.stack_step(plan, sa, tokens, bt, sl, logits)  # noqa: E731
+    eager_ms = time_steps(step, args.steps, args.warmup, 1, stream)
+    graph = torch.cuda.CUDAGraph()
+    s2 = torch.cuda.Stream()
+    s2.wait_stream(stream)
+    with torch.cuda.stream(s2):
+        step()
+    stream.wait_stream(s2)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph):
+        step()
+    graph_ms = time_steps(graph.replay, args.steps, args.warmup, 1, stream)
+    plan.poll()
+    pk = peaks()
+    work = cm.stack_work(shape, batch.seq_lens, batch.q_lens, L, vocab)
+    rf = cm.roofline_time(work, pk["bf16_tflops_sustained"] * 1e12, pk["hbm_gbs"] * 1e9)
+    ms = min(eager_ms, graph_ms)
+    line = {"metric": "end-to-end layer-stack tokens/s (decode step, 32 layers + LM head)",
+            "value": B / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "eager_ms": eager_ms, "graph_ms": graph_ms,
+            "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"llama3-8b-shaped 32-layer stack, vocab {vocab}, {B} decode "
+                                   "requests (lognormal KV median 600, sigma 1, clip [1,8192])",
+                       "kv_read_gb_per_step": L * work["layer"]["kv_read_bytes"] / 1e9,
+                       "plan": _lib.opts_dict(plan.info()[0])},
+            "stack_roofline": {"frac": rf["t_roof"] / (ms * 1e-3), "t_roof_ms": rf["t_roof"] * 1e3,
+                               "bound": rf["bound"], "flops": work["flops"], "bytes": work["bytes"]}}
+    print(json.dumps(line), flush=True)
+    plan.close()
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload == "stack":
+        return run_stack(args)
     from nano_intra_device_gb300 import _lib
 
     rank, world, local = dist_setup(args.gpus)

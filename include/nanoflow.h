@@ -167,6 +167,32 @@ nf_status nf_layer_step(nf_plan plan, const nf_layer_weights* w, const void* x, 
                         void* v_pool, const int32_t* block_table, const int32_t* seq_lens, void* y,
                         void* stream);
 
+/* A stack of decoder layers over one mixed step ("NanoFlow: Towards Optimal
+ * LLM Serving Throughput", "Example Pipelines for Different Model Scales": the
+ * per-layer pipeline repeated over the model): x = embed[tokens], then every
+ * layer l with its own weights and K/V pools (the block table and lengths are
+ * shared), then logits = RMSNorm(x; norm_f) lm_head^T.
+ * embed, lm_head: device [vocab, H] bf16, vocab a multiple of 8; norm_f: [H].
+ * layers: HOST array [n_layers] of device weight sets.
+ * tokens: device int32 [T] token ids (an id outside [0, vocab) gives a zero
+ *   row and sets the device status NF_ERR_DEVICE).
+ * k_pools, v_pools: HOST arrays [n_layers] of device pools, laid out as for
+ *   nf_layer_step.  logits: device [T, vocab] bf16.
+ * The first call for a given n_layers may allocate (activation buffers and
+ * one split-KV counter set per layer) and synchronizes the device once;
+ * later calls only enqueue work and can be captured in a CUDA graph. */
+typedef struct {
+  const void* embed;
+  const void* norm_f;
+  const void* lm_head;
+  int32_t vocab;
+  int32_t n_layers;
+  const nf_layer_weights* layers;
+} nf_stack_weights;
+nf_status nf_stack_step(nf_plan plan, const nf_stack_weights* w, const int32_t* tokens,
+                        void* const* k_pools, void* const* v_pools, const int32_t* block_table,
+                        const int32_t* seq_lens, void* logits, void* stream);
+
 /* The same step with the per-step inputs and the output in HOST memory:
  * x_host [T, H] bf16, block_table_host and seq_lens_host as above, y_host
  * [T, H].  Copies them through plan-owned device staging buffers on `stream`

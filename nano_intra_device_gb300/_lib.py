@@ -57,6 +57,11 @@ class nf_layer_weights(Structure):
     _fields_ = [(n, c_void_p) for n in ("norm1", "w_qkv", "w_o", "norm2", "w_gate_up", "w_down")]
 
 
+class nf_stack_weights(Structure):
+    _fields_ = [("embed", c_void_p), ("norm_f", c_void_p), ("lm_head", c_void_p),
+                ("vocab", c_int32), ("n_layers", c_int32), ("layers", POINTER(nf_layer_weights))]
+
+
 _SIGS = {
     "nf_plan_create": (c_int, [POINTER(nf_model_shape), POINTER(nf_batch_desc), POINTER(nf_plan_opts), POINTER(c_void_p)]),
     "nf_plan_info": (c_int, [c_void_p, POINTER(nf_plan_opts), POINTER(c_int32)]),
@@ -66,6 +71,7 @@ _SIGS = {
     "nf_layer_step": (c_int, [c_void_p, POINTER(nf_layer_weights), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     "nf_layer_step_host": (c_int, [c_void_p, POINTER(nf_layer_weights), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     "nf_plan_poll": (c_int, [c_void_p, c_int]),
+    "nf_stack_step": (c_int, [c_void_p, POINTER(nf_stack_weights), c_void_p, POINTER(c_void_p), POINTER(c_void_p), c_void_p, c_void_p, c_void_p, c_void_p]),
     "nf_last_error": (c_char_p, []),
     "nf_device_sm_count": (c_int32, []),
     "nf_step_metadata": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p]),
@@ -233,6 +239,23 @@ def layer_step(plan: Plan, w: dict, x, k_pool, v_pool, block_table, seq_lens, y,
     ws = make_weights_struct(w)
     check(lib().nf_layer_step(plan.h, ctypes.byref(ws), ptr(x), ptr(k_pool), ptr(v_pool),
                               ptr(block_table), ptr(seq_lens), ptr(y), stream_handle(stream)))
+
+
+class StackArgs:
+    """Keeps the ctypes arrays of one stack's weights and pools alive."""
+
+    def __init__(self, embed, norm_f, lm_head, layers: list, pools: list):
+        self.layer_structs = (nf_layer_weights * len(layers))(*[make_weights_struct(w) for w in layers])
+        self.w = nf_stack_weights(embed.data_ptr(), norm_f.data_ptr(), lm_head.data_ptr(),
+                                  embed.shape[0], len(layers), self.layer_structs)
+        self.kps = (c_void_p * len(pools))(*[k.data_ptr() for k, _ in pools])
+        self.vps = (c_void_p * len(pools))(*[v.data_ptr() for _, v in pools])
+        self._keep = (embed, norm_f, lm_head, layers, pools)
+
+
+def stack_step(plan: Plan, args: StackArgs, tokens, block_table, seq_lens, logits, stream=None):
+    check(lib().nf_stack_step(plan.h, ctypes.byref(args.w), ptr(tokens), args.kps, args.vps,
+                              ptr(block_table), ptr(seq_lens), ptr(logits), stream_handle(stream)))
 
 
 def layer_step_host(plan: Plan, w: dict, x_host, k_pool, v_pool, bt_host, sl_host, y_host, stream=None):

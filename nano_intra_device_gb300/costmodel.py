@@ -111,3 +111,19 @@ def decode_attention_bytes(shape, seq_lens, q_lens, elem_bytes: int = 2) -> int:
     kv_tok = 2 * shape.n_kv * shape.head_dim * elem_bytes
     n = int(dec.sum())
     return int(seq_lens[dec].sum()) * kv_tok + 2 * n * shape.n_q * shape.head_dim * elem_bytes
+
+
+def stack_work(shape, seq_lens, q_lens, n_layers: int, vocab: int, elem_bytes: int = 2) -> dict:
+    """Algorithmic work of a stack step: n_layers layer steps (each reads its own
+    K/V and weights once), the embedding rows gathered, the final norm and the
+    LM head (its weights read once, 2*T*H*vocab FLOPs)."""
+    lw = step_work(shape, seq_lens, q_lens, elem_bytes)
+    T = lw["tokens"]
+    H = shape.hidden
+    head_flops = 2 * T * H * vocab
+    head_bytes = vocab * H * elem_bytes + T * vocab * elem_bytes
+    flops = n_layers * lw["flops"] + head_flops
+    # per layer: weights + K/V once; activations stay on chip or in L2 between kernels
+    per_layer_bytes = lw["weight_bytes"] + lw["kv_read_bytes"] + lw["kv_write_bytes"]
+    byts = n_layers * per_layer_bytes + head_bytes + T * H * elem_bytes
+    return {"tokens": T, "flops": flops, "bytes": byts, "layer": lw}

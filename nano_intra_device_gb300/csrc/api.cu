@@ -2,6 +2,7 @@
 // entry points.  Host code; every arithmetic step runs in the kernels.
 #include <algorithm>
 #include <cmath>
+#include <utility>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -84,9 +85,22 @@ struct nf_plan_s {
   std::vector<cudaEvent_t> ev;
   // tensor maps over plan buffers (A operands)
   CUtensorMap tm_n1{}, tm_o{}, tm_n2{}, tm_a{};
-  // tensor maps over the weights, rebuilt when the pointers change
+  // tensor maps over the weights in use, and a cache of every weight set seen
+  // (a stack reuses one plan for all its layers)
   const void* wkey[4] = {nullptr, nullptr, nullptr, nullptr};
   CUtensorMap tm_wqkv{}, tm_wo{}, tm_wg{}, tm_wu{}, tm_wd{};
+  struct WeightMaps {
+    const void* key[4];
+    CUtensorMap qkv, o, g, u, d;
+  };
+  std::vector<WeightMaps> wcache;
+  // split-KV counters: one set per layer of a stack step (zeroed by the metadata kernel)
+  int counter_sets = 1, cur_set = 0;
+  // stack: activations between layers, and the LM head's tensor map
+  __nv_bfloat16 *xa = nullptr, *xb = nullptr;
+  const void* lm_key = nullptr;
+  int lm_vocab = 0;
+  CUtensorMap tm_lm{};
   // tracing
   struct TraceRec {
     int op, nano, step;
@@ -185,7 +199,7 @@ void free_plan(nf_plan p) {
   void* bufs[] = {p->d_q_lens, p->d_tok_begin, p->d_seg_bounds, p->tok_seq, p->tok_pos,
                   p->tok_slot, p->tok_nchunks, p->items, p->seg_items, p->fetch, p->row_done,
                   p->partials, p->status, p->n1, p->q, p->o, p->h, p->n2, p->a, p->x_stage,
-                  p->y_stage, p->bt_stage, p->sl_stage};
+                  p->y_stage, p->bt_stage, p->sl_stage, p->xa, p->xb};
   for (void* b : bufs)
     if (b) cudaFree(b);
   for (cudaEvent_t e : p->ev) cudaEventDestroy(e);
@@ -337,6 +351,17 @@ nf_status build_plan(const nf_model_shape* shape, const nf_batch_desc* batch,
 nf_status refresh_weight_maps(nf_plan p, const nf_layer_weights* w) {
   const void* key[4] = {w->w_qkv, w->w_o, w->w_gate_up, w->w_down};
   if (std::memcmp(key, p->wkey, sizeof(key)) == 0) return NF_OK;
+  for (const auto& c : p->wcache) {
+    if (std::memcmp(key, c.key, sizeof(key)) == 0) {
+      p->tm_wqkv = c.qkv;
+      p->tm_wo = c.o;
+      p->tm_wg = c.g;
+      p->tm_wu = c.u;
+      p->tm_wd = c.d;
+      std::memcpy(p->wkey, key, sizeof(key));
+      return NF_OK;
+    }
+  }
   const nf_model_shape& s = p->shape;
   const uint64_t H = s.hidden, F = s.ffn, QD = (uint64_t)s.n_q_heads * s.head_dim;
   const uint64_t NQKV = (uint64_t)(s.n_q_heads + 2 * s.n_kv_heads) * s.head_dim;
@@ -348,6 +373,16 @@ nf_status refresh_weight_maps(nf_plan p, const nf_layer_weights* w) {
       !nf::make_tmap_bf16(&p->tm_wd, w->w_down, H, F, 256))
     return fail(NF_ERR_INVALID_ARG, "weight tensor maps: pointers must be 16-byte aligned");
   std::memcpy(p->wkey, key, sizeof(key));
+  if (p->wcache.size() < 1024) {
+    nf_plan_s::WeightMaps c;
+    std::memcpy(c.key, key, sizeof(key));
+    c.qkv = p->tm_wqkv;
+    c.o = p->tm_wo;
+    c.g = p->tm_wg;
+    c.u = p->tm_wu;
+    c.d = p->tm_wd;
+    p->wcache.push_back(c);
+  }
   return NF_OK;
 }
 
@@ -425,6 +460,8 @@ nf_status run_meta(nf_plan p, const int32_t* bt, const int32_t* sl, cudaStream_t
   m.seg_items = p->seg_items;
   m.fetch = p->fetch;
   m.row_done = p->row_done;
+  m.counter_sets = p->counter_sets;
+  m.fetch_stride = NF_MAX_NANO;
   m.status = p->status;
   m.validate = p->opts.validate;
   NF_CUDA(nf::launch_meta(m, st));
@@ -445,8 +482,8 @@ nf_status run_attention(nf_plan p, int seg, const void* q, const void* kp, const
   a.tok_nchunks = p->tok_nchunks;
   a.items = p->items;
   a.seg_items = p->seg_items;
-  a.fetch = p->fetch;
-  a.row_done = p->row_done;
+  a.fetch = p->fetch + (size_t)p->cur_set * NF_MAX_NANO;
+  a.row_done = p->row_done + (size_t)p->cur_set * p->T * p->shape.n_kv_heads;
   a.partials = p->partials;
   a.seg = seg;
   a.n_q = p->shape.n_q_heads;
@@ -558,8 +595,11 @@ nf_status check_step_args(nf_plan p, const nf_layer_weights* w, const void* x, v
   return NF_OK;
 }
 
+// One layer.  with_meta: run the metadata kernel first (a stack runs it once
+// per step and then gives each layer its own counter set, p->cur_set).
 nf_status layer_step(nf_plan p, const nf_layer_weights* w, const void* x, void* kp, void* vp,
-                     const int32_t* bt, const int32_t* sl, void* y, cudaStream_t st) {
+                     const int32_t* bt, const int32_t* sl, void* y, cudaStream_t st,
+                     bool with_meta = true) {
   NF_TRY(refresh_weight_maps(p, w));
   if (p->trace_left > 0) {
     p->trace_s0 = pooled_event(p);
@@ -578,7 +618,7 @@ nf_status layer_step(nf_plan p, const nf_layer_weights* w, const void* x, void* 
   const nf_plan_opts& o = p->opts;
   const int all = p->num_sms;
   if (o.executor == NF_EXEC_SEQUENTIAL) {
-    NF_TRY(run_meta(p, bt, sl, st));
+    if (with_meta) NF_TRY(run_meta(p, bt, sl, st));
     for (int i = 0; i < o.n_attn; ++i) {
       const int r0 = o.attn_bounds[i], r1 = o.attn_bounds[i + 1];
       NF_TRY(run_qkv(p, w, x, kp, vp, r0, r1, all, st, i));
@@ -600,7 +640,7 @@ nf_status layer_step(nf_plan p, const nf_layer_weights* w, const void* x, void* 
   NF_CUDA(cudaEventRecord(ev_start, st));
   NF_CUDA(cudaStreamWaitEvent(p->s_gemm, ev_start, 0));
   NF_CUDA(cudaStreamWaitEvent(p->s_attn, ev_start, 0));
-  NF_TRY(run_meta(p, bt, sl, p->s_gemm));
+  if (with_meta) NF_TRY(run_meta(p, bt, sl, p->s_gemm));
   for (int i = 0; i < n; ++i) {
     NF_TRY(run_qkv(p, w, x, kp, vp, o.attn_bounds[i], o.attn_bounds[i + 1],
                    i == 0 ? all : gemm_overlap, p->s_gemm, i));
@@ -732,6 +772,75 @@ nf_status nf_layer_step(nf_plan plan, const nf_layer_weights* w, const void* x, 
   NF_TRY(check_step_args(plan, w, x, k_pool, v_pool, block_table, seq_lens, y));
   return layer_step(plan, w, x, k_pool, v_pool, block_table, seq_lens, y,
                     static_cast<cudaStream_t>(stream));
+}
+
+nf_status nf_stack_step(nf_plan p, const nf_stack_weights* sw, const int32_t* tokens,
+                        void* const* k_pools, void* const* v_pools, const int32_t* bt,
+                        const int32_t* sl, void* logits, void* stream) {
+  if (!p || !sw || !tokens || !k_pools || !v_pools || !bt || !sl || !logits)
+    return fail(NF_ERR_INVALID_ARG, "NULL argument");
+  if (sw->n_layers < 1 || !sw->layers || !sw->embed || !sw->norm_f || !sw->lm_head)
+    return fail(NF_ERR_INVALID_ARG, "stack weights incomplete");
+  if (sw->vocab < 8 || sw->vocab % 8)
+    return fail(NF_ERR_INVALID_ARG, "vocab must be a positive multiple of 8 (got %d)", sw->vocab);
+  if (!aligned16(sw->embed) || !aligned16(sw->norm_f) || !aligned16(sw->lm_head) ||
+      !aligned16(logits))
+    return fail(NF_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  const size_t xb = (size_t)p->T * p->shape.hidden * 2;
+  if (!p->xa) {
+    NF_TRY(dalloc(&p->xa, xb));
+    NF_TRY(dalloc(&p->xb, xb));
+  }
+  if (p->counter_sets < sw->n_layers) {  // one split-KV counter set per layer
+    NF_CUDA(cudaDeviceSynchronize());
+    cudaFree(p->fetch);
+    cudaFree(p->row_done);
+    p->fetch = nullptr;
+    p->row_done = nullptr;
+    NF_TRY(dalloc(&p->fetch, (size_t)NF_MAX_NANO * sw->n_layers * 4));
+    NF_TRY(dalloc(&p->row_done, (size_t)p->T * p->shape.n_kv_heads * sw->n_layers * 4));
+    p->counter_sets = sw->n_layers;
+  }
+  if (p->lm_key != sw->lm_head || p->lm_vocab != sw->vocab) {
+    if (!nf::make_tmap_bf16(&p->tm_lm, sw->lm_head, sw->vocab, p->shape.hidden, 256))
+      return fail(NF_ERR_INVALID_ARG, "LM head tensor map failed");
+    p->lm_key = sw->lm_head;
+    p->lm_vocab = sw->vocab;
+  }
+  for (int l = 0; l < sw->n_layers; ++l) {
+    NF_TRY(check_step_args(p, &sw->layers[l], p->xa, k_pools[l], v_pools[l], bt, sl, p->xb));
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const nf_model_shape& s = p->shape;
+  // embedding, then the step metadata once for every layer
+  NF_CUDA(nf::launch_embed(tokens, static_cast<const __nv_bfloat16*>(sw->embed), p->xa, p->T,
+                           s.hidden, sw->vocab, p->status, st));
+  NF_TRY(run_meta(p, bt, sl, st));
+  __nv_bfloat16 *cur = p->xa, *nxt = p->xb;
+  for (int l = 0; l < sw->n_layers; ++l) {
+    p->cur_set = l;
+    const nf_status r = layer_step(p, &sw->layers[l], cur, k_pools[l], v_pools[l], bt, sl, nxt, st,
+                                   /*with_meta=*/false);
+    p->cur_set = 0;
+    if (r != NF_OK) return r;
+    std::swap(cur, nxt);
+  }
+  // final RMSNorm and the LM head: logits = RMSNorm(x) lm_head^T
+  NF_CUDA(nf::launch_rmsnorm(cur, static_cast<const __nv_bfloat16*>(sw->norm_f), p->n1, 0, p->T,
+                             s.hidden, s.rms_eps, st));
+  GemmArgs g = base_args(p);
+  g.stages = 4;
+  g.m_begin = 0;
+  g.m_end = p->T;
+  g.N = sw->vocab;
+  g.K = s.hidden;
+  g.m_tiles = (p->T + 127) / 128;
+  g.n_tiles = (sw->vocab + 255) / 256;
+  g.C = static_cast<__nv_bfloat16*>(logits);
+  g.ldc = sw->vocab;
+  NF_CUDA(nf::launch_gemm(nf::EPI_STORE, p->tm_n1, p->tm_lm, p->tm_lm, g,
+                          cap_grid(g.m_tiles * g.n_tiles, p->num_sms), st));
+  return NF_OK;
 }
 
 nf_status nf_layer_step_host(nf_plan p, const nf_layer_weights* w, const void* x_host,

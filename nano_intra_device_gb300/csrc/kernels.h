@@ -49,6 +49,11 @@ int gemm_tiles(int epi, int m_rows, int N);
 cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* g, __nv_bfloat16* out,
                            int row_begin, int row_end, int hidden, float eps, cudaStream_t stream);
 
+// Embedding lookup: x[t] = embed[tokens[t]] (rows of H bf16); an id outside
+// [0, vocab) flags ST_BAD_LEN and writes a zero row.
+cudaError_t launch_embed(const int* tokens, const __nv_bfloat16* embed, __nv_bfloat16* x, int n_tok,
+                         int hidden, int vocab, uint32_t* status, cudaStream_t stream);
+
 // ---------------------------------------------------------- step metadata
 struct MetaArgs {
   const int* seq_lens;      // device [n_seq]
@@ -65,8 +70,10 @@ struct MetaArgs {
   int* tok_nchunks;         // out [n_tok]
   int* items;               // out [2 * item_capacity] (row, chunk)
   int* seg_items;           // out [n_seg + 1] segment starts in items
-  int* fetch;               // out [n_seg] dynamic fetch counters, zeroed
-  int* row_done;            // out [n_tok * n_kv] split-combine counters, zeroed
+  int* fetch;               // out [counter_sets * n_seg] dynamic fetch counters, zeroed
+  int* row_done;            // out [counter_sets * n_tok * n_kv] split-combine counters, zeroed
+  int counter_sets;         // one set per layer that attends with this metadata
+  int fetch_stride;         // fetch counters per set
   uint32_t* status;
   int validate;
 };

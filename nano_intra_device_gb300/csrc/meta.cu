@@ -129,8 +129,12 @@ __global__ void __launch_bounds__(META_THREADS) meta_kernel(const MetaArgs a) {
       }
     }
   }
-  for (int i = threadIdx.x; i < a.n_seg; i += META_THREADS) a.fetch[i] = 0;
-  for (int i = threadIdx.x; i < a.n_tok * a.n_kv; i += META_THREADS) a.row_done[i] = 0;
+  const int sets = a.counter_sets > 0 ? a.counter_sets : 1;
+  for (int i = threadIdx.x; i < a.fetch_stride * sets; i += META_THREADS) a.fetch[i] = 0;
+  const int4 z = make_int4(0, 0, 0, 0);
+  const int n_done = a.n_tok * a.n_kv * sets;  // multiple of 4: row_done is 16-byte aligned
+  for (int i = threadIdx.x; i < n_done / 4; i += META_THREADS) reinterpret_cast<int4*>(a.row_done)[i] = z;
+  for (int i = (n_done / 4) * 4 + threadIdx.x; i < n_done; i += META_THREADS) a.row_done[i] = 0;
 }
 
 cudaError_t launch_meta(const MetaArgs& a, cudaStream_t stream) {

@@ -53,4 +53,28 @@ cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* g, __nv_
   return cudaGetLastError();
 }
 
+// Embedding lookup, one CTA per token: the row is copied with 16-byte accesses.
+__global__ void __launch_bounds__(RMS_THREADS)
+    embed_kernel(const int* __restrict__ tokens, const __nv_bfloat16* __restrict__ embed,
+                 __nv_bfloat16* __restrict__ x, int hidden, int vocab, uint32_t* status) {
+  const int t = blockIdx.x;
+  const int id = tokens[t];
+  uint4* dst = reinterpret_cast<uint4*>(x + static_cast<size_t>(t) * hidden);
+  const int nvec = hidden / 8;
+  if (id < 0 || id >= vocab) {
+    if (threadIdx.x == 0) raise_status(status, ST_BAD_LEN);
+    for (int i = threadIdx.x; i < nvec; i += RMS_THREADS) dst[i] = make_uint4(0, 0, 0, 0);
+    return;
+  }
+  const uint4* src = reinterpret_cast<const uint4*>(embed + static_cast<size_t>(id) * hidden);
+  for (int i = threadIdx.x; i < nvec; i += RMS_THREADS) dst[i] = src[i];
+}
+
+cudaError_t launch_embed(const int* tokens, const __nv_bfloat16* embed, __nv_bfloat16* x, int n_tok,
+                         int hidden, int vocab, uint32_t* status, cudaStream_t stream) {
+  if (n_tok <= 0) return cudaSuccess;
+  embed_kernel<<<n_tok, RMS_THREADS, 0, stream>>>(tokens, embed, x, hidden, vocab, status);
+  return cudaGetLastError();
+}
+
 }  // namespace nf

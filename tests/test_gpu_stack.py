@@ -1,0 +1,101 @@
+"""A stack of layers (embedding, layers with their own KV pools, final norm,
+LM head) through nf_stack_step against the oracle, and the same step replayed
+from a CUDA graph."""
+import numpy as np
+import pytest
+import torch
+
+from nano_intra_device_gb300 import _lib, workload as wl
+from oracle import layer as orc
+from tests.helpers import compare, f64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _stack(shape, batch, n_layers, vocab, seed=0, gain_std=0.1):
+    g = torch.Generator().manual_seed(seed + 100)
+    embed = torch.randn(vocab, shape.hidden, generator=g).to(torch.bfloat16)
+    lm_head = (torch.randn(vocab, shape.hidden, generator=g) * 0.02).to(torch.bfloat16)
+    norm_f = (1 + 0.1 * torch.randn(shape.hidden, generator=g)).to(torch.bfloat16)
+    tokens = torch.randint(0, vocab, (batch.n_tokens,), generator=g).to(torch.int32)
+    layers = [wl.make_weights(shape, seed=seed + 10 + i, gain_std=gain_std) for i in range(n_layers)]
+    pools = [wl.make_pools(shape, batch, DEV, seed=seed + 50 + i) for i in range(n_layers)]
+    return embed, norm_f, lm_head, tokens, layers, pools
+
+
+def _run(shape, batch, opts, embed, norm_f, lm_head, tokens, layers, pools):
+    plan = _lib.Plan(shape, batch, opts)
+    dl = [{k: v.to(DEV) for k, v in w.items()} for w in layers]
+    dp = [(k.clone(), v.clone()) for k, v in pools]
+    args = _lib.StackArgs(embed.to(DEV), norm_f.to(DEV), lm_head.to(DEV), dl, dp)
+    logits = torch.empty(batch.n_tokens, embed.shape[0], dtype=torch.bfloat16, device=DEV)
+    bt = torch.from_numpy(batch.block_table).to(DEV)
+    sl = torch.from_numpy(batch.seq_lens).to(DEV)
+    tok = tokens.to(DEV)
+    _lib.stack_step(plan, args, tok, bt, sl, logits)
+    plan.poll()
+    return plan, args, logits, (tok, bt, sl), dp
+
+
+@pytest.mark.parametrize("executor,bounds", [(_lib.NF_EXEC_SEQUENTIAL, None),
+                                             (_lib.NF_EXEC_STREAMS, [0, 20, 36])])
+def test_tiny_stack_matches_oracle(executor, bounds):
+    shape, batch = wl.tiny_shape(), wl.tiny_batch()
+    embed, norm_f, lm_head, tokens, layers, pools = _stack(shape, batch, 3, 96)
+    ref = orc.stack_step(shape, embed, norm_f, lm_head, [orc.weights_f64(w) for w in layers],
+                         tokens.numpy(), pools, batch.block_table, batch.seq_lens, batch.q_lens)
+    T = batch.n_tokens
+    opts = _lib.make_opts(T, bounds, executor=executor, attn_sms=24, kv_chunk=32)
+    plan, args, logits, _, dp = _run(shape, batch, opts, embed, norm_f, lm_head, tokens, layers, pools)
+    plan.close()
+    compare(f64(logits), ref["logits"], "stack logits")
+    # each layer appended this step's K/V into its own pool
+    seq, pos = orc.token_map(batch.q_lens, batch.seq_lens)
+    slots = orc.slot_of(seq, pos, batch.block_table, shape.page_size)
+    P = shape.page_size
+    for (k, v) in dp:
+        sl_ = torch.as_tensor(slots, device=DEV)
+        assert torch.isfinite(k[sl_ // P, :, sl_ % P, :]).all()
+        assert torch.isfinite(v[sl_ // P, :, sl_ % P, :]).all()
+
+
+def test_llama8b_shaped_two_layer_stack_sampled_rows():
+    shape = wl.llama8b_shape()
+    ctx = wl.lognormal_contexts(96, 600.0, 1.0, 1, 4096, seed=1)
+    batch = wl.make_batch(shape, ctx, [32], None, seed_bt=2, max_pages=4096 // 16)
+    embed, norm_f, lm_head, tokens, layers, pools = _stack(shape, batch, 2, 32000, gain_std=0.0)
+    rows = [0, 5, int(np.argmax(ctx)), 95, 96, 127]
+    ref = orc.stack_step(shape, embed, norm_f, lm_head, [orc.weights_f64(w) for w in layers],
+                         tokens.numpy(), pools, batch.block_table, batch.seq_lens, batch.q_lens,
+                         rows=rows)
+    plan, args, logits, _, _ = _run(shape, batch, _lib.make_opts(batch.n_tokens), embed, norm_f,
+                                    lm_head, tokens, layers, pools)
+    plan.close()
+    compare(f64(logits)[rows], ref["logits"], "8B-shaped stack logits")
+
+
+def test_stack_cuda_graph_replay_equals_eager():
+    shape = wl.llama8b_shape()
+    ctx = wl.lognormal_contexts(64, 600.0, 1.0, 1, 2048, seed=3)
+    batch = wl.make_batch(shape, ctx, [], None, seed_bt=4, max_pages=2048 // 16)
+    embed, norm_f, lm_head, tokens, layers, pools = _stack(shape, batch, 4, 8192, gain_std=0.0)
+    plan, args, logits, (tok, bt, sl), dp = _run(shape, batch, _lib.make_opts(batch.n_tokens), embed,
+                                                 norm_f, lm_head, tokens, layers, pools)
+    eager = logits.clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):                      # warm path before capture
+        _lib.stack_step(plan, args, tok, bt, sl, logits, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        _lib.stack_step(plan, args, tok, bt, sl, logits)
+    logits.zero_()
+    graph.replay()
+    graph.replay()
+    torch.cuda.synchronize()
+    plan.poll()
+    assert torch.equal(logits, eager)
+    plan.close()
