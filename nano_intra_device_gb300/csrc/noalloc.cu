@@ -152,6 +152,8 @@ extern "C" nf_status nf_attention_noalloc(const nf_model_shape* shape, const nf_
   m.seg_items = reinterpret_cast<int*>(base + o_segi);
   m.fetch = reinterpret_cast<int*>(base + o_fetch);     // zeroed by the metadata kernel
   m.row_done = reinterpret_cast<int*>(base + o_done);   // zeroed by the metadata kernel
+  m.counter_sets = 1;
+  m.fetch_stride = 1;
   m.status = reinterpret_cast<uint32_t*>(base + o_status);
   m.validate = 0;
   if (nf::launch_meta(m, cs) != cudaSuccess)

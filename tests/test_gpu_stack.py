@@ -7,7 +7,19 @@ import torch
 
 from nano_intra_device_gb300 import _lib, workload as wl
 from oracle import layer as orc
-from tests.helpers import compare, f64
+from tests.helpers import MAX_ABS, REL_L2, compare, f64
+
+
+def compare_stack(gpu, ref, name, n_layers):
+    """A stack composes n_layers layers, each rounding its output to bf16, so the
+    error grows like sqrt(n_layers + 1) (the +1 is the final norm and head):
+    both bounds of a single layer are scaled by that factor."""
+    k = float(np.sqrt(n_layers + 1))
+    d = np.asarray(gpu, np.float64) - np.asarray(ref, np.float64)
+    rl = float(np.linalg.norm(d) / np.linalg.norm(ref))
+    print(f"{name}: rel-L2 {rl:.4g}, max-abs {np.abs(d).max():.4g}, "
+          f"p99.9 {np.quantile(np.abs(d), 0.999):.4g}, rms(ref) {np.sqrt(np.mean(ref ** 2)):.4g}")
+    return compare(gpu, ref, name, rel_l2=REL_L2 * k, max_abs=MAX_ABS * k)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -49,7 +61,7 @@ def test_tiny_stack_matches_oracle(executor, bounds):
     opts = _lib.make_opts(T, bounds, executor=executor, attn_sms=24, kv_chunk=32)
     plan, args, logits, _, dp = _run(shape, batch, opts, embed, norm_f, lm_head, tokens, layers, pools)
     plan.close()
-    compare(f64(logits), ref["logits"], "stack logits")
+    compare_stack(f64(logits), ref["logits"], "stack logits", 3)
     # each layer appended this step's K/V into its own pool
     seq, pos = orc.token_map(batch.q_lens, batch.seq_lens)
     slots = orc.slot_of(seq, pos, batch.block_table, shape.page_size)
@@ -72,7 +84,7 @@ def test_llama8b_shaped_two_layer_stack_sampled_rows():
     plan, args, logits, _, _ = _run(shape, batch, _lib.make_opts(batch.n_tokens), embed, norm_f,
                                     lm_head, tokens, layers, pools)
     plan.close()
-    compare(f64(logits)[rows], ref["logits"], "8B-shaped stack logits")
+    compare_stack(f64(logits)[rows], ref["logits"], "8B-shaped stack logits", 2)
 
 
 def test_stack_cuda_graph_replay_equals_eager():
