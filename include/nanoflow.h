@@ -112,6 +112,8 @@ typedef struct {
                          CTA of gemm_stages = 2 (0 = 8) */
   int32_t gemm_stages; /* shared-memory ring stages of the GEMM kernel: 4 fills an SM;
                           2 lets an attention CTA of 4 or 5 warps run on the same SM (0 = 4) */
+  int32_t gemm_split_k; /* 0: split K across CTAs when a GEMM has fewer output tiles than
+                           half its SMs; 1: never split */
   int32_t validate;   /* 1 = check page ids and lengths on the device */
   int64_t timeout_ns; /* limit of every device-side wait (0 = 2e9) */
 } nf_plan_opts;
@@ -282,7 +284,11 @@ nf_status nf_rmsnorm(const void* x, const void* g, void* out, int32_t rows, int3
  *   NF_EPI_RESID   C[M, N] = R[M, N] + acc          (R device [M, N])
  *   NF_EPI_SWIGLU  B holds 2F rows (gate rows then up rows), N = F:
  *                  C[M, F] = silu(A Bg^T) * (A Bu^T)
- * max_sms caps the persistent grid (0 = all SMs). */
+ * max_sms caps the persistent grid (0 = all SMs).  A GEMM with fewer 128 x 256
+ * output tiles than half the SMs splits K across CTAs (split-K, fp32 partials
+ * summed before the epilogue, the same result up to fp32 rounding order); its
+ * partials use one workspace shared by every nf_gemm call (allocated on first
+ * use), so such calls must not run concurrently on different streams. */
 typedef enum { NF_EPI_STORE = 0, NF_EPI_RESID = 1, NF_EPI_SWIGLU = 2 } nf_epilogue;
 nf_status nf_gemm(const void* A, const void* B, void* C, const void* R, int32_t M, int32_t N,
                   int32_t K, int32_t epilogue, int32_t max_sms, void* stream);

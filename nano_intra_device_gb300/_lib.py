@@ -41,7 +41,7 @@ class nf_plan_opts(Structure):
                 ("n_ffn", c_int32), ("ffn_bounds", c_int32 * (NF_MAX_NANO + 1)),
                 ("executor", c_int32), ("attn_sms", c_int32), ("gemm_sms", c_int32),
                 ("kv_chunk", c_int32), ("attn_warps", c_int32), ("gemm_stages", c_int32),
-                ("validate", c_int32),
+                ("gemm_split_k", c_int32), ("validate", c_int32),
                 ("timeout_ns", c_int64)]
 
 
@@ -150,7 +150,7 @@ def make_batch_desc(batch, hint=True):
 
 def make_opts(T, attn_bounds=None, ffn_bounds=None, executor=NF_EXEC_SEQUENTIAL, attn_sms=0,
               gemm_sms=0, kv_chunk=1024, validate=0, timeout_ns=2_000_000_000,
-              attn_warps=0, gemm_stages=0) -> nf_plan_opts:
+              attn_warps=0, gemm_stages=0, gemm_split_k=0) -> nf_plan_opts:
     ab = list(attn_bounds) if attn_bounds is not None else [0, T]
     fb = list(ffn_bounds) if ffn_bounds is not None else list(ab)
     o = nf_plan_opts()
@@ -164,6 +164,7 @@ def make_opts(T, attn_bounds=None, ffn_bounds=None, executor=NF_EXEC_SEQUENTIAL,
     o.kv_chunk, o.validate, o.timeout_ns = kv_chunk, validate, timeout_ns
     o.attn_warps = attn_warps
     o.gemm_stages = gemm_stages
+    o.gemm_split_k = gemm_split_k
     return o
 
 
@@ -172,7 +173,8 @@ def opts_dict(o: nf_plan_opts) -> dict:
             "ffn_bounds": list(o.ffn_bounds[: o.n_ffn + 1]),
             "executor": "streams" if o.executor == NF_EXEC_STREAMS else "sequential",
             "attn_sms": o.attn_sms, "gemm_sms": o.gemm_sms, "kv_chunk": o.kv_chunk,
-            "attn_warps": o.attn_warps, "gemm_stages": o.gemm_stages}
+            "attn_warps": o.attn_warps, "gemm_stages": o.gemm_stages,
+            "gemm_split_k": o.gemm_split_k}
 
 
 def make_weights_struct(w: dict) -> nf_layer_weights:

@@ -45,6 +45,14 @@ int device_sms() {
   return n;
 }
 
+struct GlobalSplitWs {
+  float* part = nullptr;
+  int* cnt = nullptr;
+};
+
+// Split-K workspace of nf_gemm (no plan): allocated on first use.
+GlobalSplitWs* global_split_ws();
+
 // Status word for entry points that run without a plan (nf_gemm, nf_rmsnorm).
 uint32_t* global_status() {
   static uint32_t* p = nullptr;
@@ -56,6 +64,39 @@ uint32_t* global_status() {
 }
 
 constexpr int64_t kDefaultTimeoutNs = 2000000000LL;
+
+// Split-K: used when a GEMM has fewer output tiles than half the SMs (small
+// decode batches), so that every SM still works.  Each split keeps at least 4
+// K-blocks; tiles x splits never exceeds the SM count, which bounds the
+// workspace of fp32 partial tiles (128 x 256 each).
+constexpr int kSplitMaxTiles = 256;
+constexpr int kSplitMaxUnits = 256;
+constexpr size_t kSplitPartBytes = (size_t)kSplitMaxUnits * 128 * 256 * 4;
+
+GlobalSplitWs* global_split_ws() {
+  static GlobalSplitWs ws;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    if (cudaMalloc(&ws.part, kSplitPartBytes) != cudaSuccess ||
+        cudaMalloc(&ws.cnt, kSplitMaxTiles * 4) != cudaSuccess ||
+        cudaMemset(ws.cnt, 0, kSplitMaxTiles * 4) != cudaSuccess) {
+      ws.part = nullptr;
+      ws.cnt = nullptr;
+      cudaGetLastError();
+    }
+  });
+  return &ws;
+}
+
+int choose_splits(int tiles, int K, int sms) {
+  if (tiles <= 0 || tiles * 2 > sms || tiles > kSplitMaxTiles) return 1;
+  const int nk = (K + 63) / 64;
+  int s = sms / tiles;
+  s = s < nk / 4 ? s : nk / 4;
+  s = s < 16 ? s : 16;
+  if (tiles * s > kSplitMaxUnits) s = kSplitMaxUnits / tiles;
+  return s > 1 ? s : 1;
+}
 
 }  // namespace
 
@@ -94,6 +135,9 @@ struct nf_plan_s {
     CUtensorMap qkv, o, g, u, d;
   };
   std::vector<WeightMaps> wcache;
+  // split-K GEMM workspace: fp32 partial tiles and per-tile arrival counters
+  float* gemm_part = nullptr;
+  int* gemm_cnt = nullptr;
   // split-KV counters: one set per layer of a stack step (zeroed by the metadata kernel)
   int counter_sets = 1, cur_set = 0;
   // stack: activations between layers, and the LM head's tensor map
@@ -191,6 +235,8 @@ nf_status check_opts(const nf_plan_opts* o, int T, int num_sms) {
     return fail(NF_ERR_INVALID_ARG, "attn_warps must be 4, 5, 8, 12 or 16");
   if (o->gemm_stages < 2 || o->gemm_stages > 4)
     return fail(NF_ERR_INVALID_ARG, "gemm_stages must be 2, 3 or 4");
+  if (o->gemm_split_k != 0 && o->gemm_split_k != 1)
+    return fail(NF_ERR_INVALID_ARG, "gemm_split_k must be 0 (automatic) or 1 (never)");
   return NF_OK;
 }
 
@@ -199,7 +245,8 @@ void free_plan(nf_plan p) {
   void* bufs[] = {p->d_q_lens, p->d_tok_begin, p->d_seg_bounds, p->tok_seq, p->tok_pos,
                   p->tok_slot, p->tok_nchunks, p->items, p->seg_items, p->fetch, p->row_done,
                   p->partials, p->status, p->n1, p->q, p->o, p->h, p->n2, p->a, p->x_stage,
-                  p->y_stage, p->bt_stage, p->sl_stage, p->xa, p->xb};
+                  p->y_stage, p->bt_stage, p->sl_stage, p->xa, p->xb, p->gemm_part,
+                  p->gemm_cnt};
   for (void* b : bufs)
     if (b) cudaFree(b);
   for (cudaEvent_t e : p->ev) cudaEventDestroy(e);
@@ -259,6 +306,9 @@ nf_status alloc_plan(nf_plan p) {
   NF_TRY(dalloc(&p->h, T * H * 2));
   NF_TRY(dalloc(&p->n2, T * H * 2));
   NF_TRY(dalloc(&p->a, T * F * 2));
+  NF_TRY(dalloc(&p->gemm_part, kSplitPartBytes));
+  NF_TRY(dalloc(&p->gemm_cnt, kSplitMaxTiles * 4));
+  NF_CUDA(cudaMemset(p->gemm_cnt, 0, kSplitMaxTiles * 4));
   NF_CUDA(cudaMemset(p->status, 0, 4));
   NF_CUDA(cudaMemcpy(p->d_q_lens, p->q_lens.data(), p->n_seq * 4, cudaMemcpyHostToDevice));
   NF_CUDA(cudaMemcpy(p->d_tok_begin, p->tok_begin.data(), (p->n_seq + 1) * 4,
@@ -389,6 +439,9 @@ nf_status refresh_weight_maps(nf_plan p, const nf_layer_weights* w) {
 GemmArgs base_args(nf_plan p) {
   GemmArgs g{};
   g.stages = p->opts.gemm_stages;
+  g.splits = 1;
+  g.part = p->gemm_part;
+  g.tile_cnt = p->gemm_cnt;
   g.status = p->status;
   g.timeout_ns = (unsigned long long)p->opts.timeout_ns;
   g.n_q = p->shape.n_q_heads;
@@ -522,8 +575,9 @@ nf_status run_qkv(nf_plan p, const nf_layer_weights* w, const void* x, void* kp,
   g.q_out = p->q;
   g.k_pool = static_cast<__nv_bfloat16*>(kp);
   g.v_pool = static_cast<__nv_bfloat16*>(vp);
+  g.splits = p->opts.gemm_split_k ? 1 : choose_splits(g.m_tiles * g.n_tiles, g.K, grid);
   NF_CUDA(nf::launch_gemm(nf::EPI_QKV, p->tm_n1, p->tm_wqkv, p->tm_wqkv, g,
-                          cap_grid(g.m_tiles * g.n_tiles, grid), st));
+                          cap_grid(g.m_tiles * g.n_tiles * g.splits, grid), st));
   return NF_OK;
 }
 
@@ -542,8 +596,9 @@ nf_status run_oproj(nf_plan p, const void* x, int r0, int r1, int grid, cudaStre
   g.ldc = s.hidden;
   g.R = static_cast<const __nv_bfloat16*>(x);
   g.ldr = s.hidden;
+  g.splits = p->opts.gemm_split_k ? 1 : choose_splits(g.m_tiles * g.n_tiles, g.K, grid);
   NF_CUDA(nf::launch_gemm(nf::EPI_RESID, p->tm_o, p->tm_wo, p->tm_wo, g,
-                          cap_grid(g.m_tiles * g.n_tiles, grid), st));
+                          cap_grid(g.m_tiles * g.n_tiles * g.splits, grid), st));
   return NF_OK;
 }
 
@@ -562,8 +617,9 @@ nf_status run_ffn(nf_plan p, const nf_layer_weights* w, void* y, int r0, int r1,
   g.n_tiles = (g.N + 127) / 128;
   g.C = p->a;
   g.ldc = s.ffn;
+  g.splits = p->opts.gemm_split_k ? 1 : choose_splits(g.m_tiles * g.n_tiles, g.K, grid);
   NF_CUDA(nf::launch_gemm(nf::EPI_SWIGLU, p->tm_n2, p->tm_wg, p->tm_wu, g,
-                          cap_grid(g.m_tiles * g.n_tiles, grid), st));
+                          cap_grid(g.m_tiles * g.n_tiles * g.splits, grid), st));
   GemmArgs d = base_args(p);
   d.m_begin = r0;
   d.m_end = r1;
@@ -575,8 +631,9 @@ nf_status run_ffn(nf_plan p, const nf_layer_weights* w, void* y, int r0, int r1,
   d.ldc = s.hidden;
   d.R = p->h;
   d.ldr = s.hidden;
+  d.splits = p->opts.gemm_split_k ? 1 : choose_splits(d.m_tiles * d.n_tiles, d.K, grid);
   NF_CUDA(nf::launch_gemm(nf::EPI_RESID, p->tm_a, p->tm_wd, p->tm_wd, d,
-                          cap_grid(d.m_tiles * d.n_tiles, grid), st));
+                          cap_grid(d.m_tiles * d.n_tiles * d.splits, grid), st));
   return NF_OK;
 }
 
@@ -721,8 +778,9 @@ nf_status nf_plan_save(nf_plan p, const char* path) {
   for (int i = 0; i <= o.n_attn; ++i) std::fprintf(f, " %d", o.attn_bounds[i]);
   std::fprintf(f, "\nffn %d", o.n_ffn);
   for (int i = 0; i <= o.n_ffn; ++i) std::fprintf(f, " %d", o.ffn_bounds[i]);
-  std::fprintf(f, "\nexec %d %d %d %d %d %lld %d %d\n", o.executor, o.attn_sms, o.gemm_sms,
-               o.kv_chunk, o.validate, (long long)o.timeout_ns, o.attn_warps, o.gemm_stages);
+  std::fprintf(f, "\nexec %d %d %d %d %d %lld %d %d %d\n", o.executor, o.attn_sms, o.gemm_sms,
+               o.kv_chunk, o.validate, (long long)o.timeout_ns, o.attn_warps, o.gemm_stages,
+               o.gemm_split_k);
   std::fclose(f);
   return NF_OK;
 }
@@ -751,9 +809,9 @@ nf_status nf_plan_load(const char* path, nf_plan* out) {
   for (int i = 0; ok && i <= o.n_attn; ++i) ok = std::fscanf(f, " %d", &o.attn_bounds[i]) == 1;
   ok = ok && std::fscanf(f, " ffn %d", &o.n_ffn) == 1 && o.n_ffn >= 1 && o.n_ffn <= NF_MAX_NANO;
   for (int i = 0; ok && i <= o.n_ffn; ++i) ok = std::fscanf(f, " %d", &o.ffn_bounds[i]) == 1;
-  ok = ok && std::fscanf(f, " exec %d %d %d %d %d %lld %d %d", &o.executor, &o.attn_sms,
+  ok = ok && std::fscanf(f, " exec %d %d %d %d %d %lld %d %d %d", &o.executor, &o.attn_sms,
                          &o.gemm_sms, &o.kv_chunk, &o.validate, &tmo, &o.attn_warps,
-                         &o.gemm_stages) == 8;
+                         &o.gemm_stages, &o.gemm_split_k) == 9;
   std::fclose(f);
   if (!ok) return fail(NF_ERR_INVALID_ARG, "%s is not a plan file", path);
   o.timeout_ns = tmo;
@@ -838,8 +896,9 @@ nf_status nf_stack_step(nf_plan p, const nf_stack_weights* sw, const int32_t* to
   g.n_tiles = (sw->vocab + 255) / 256;
   g.C = static_cast<__nv_bfloat16*>(logits);
   g.ldc = sw->vocab;
+  g.splits = p->opts.gemm_split_k ? 1 : choose_splits(g.m_tiles * g.n_tiles, g.K, p->num_sms);
   NF_CUDA(nf::launch_gemm(nf::EPI_STORE, p->tm_n1, p->tm_lm, p->tm_lm, g,
-                          cap_grid(g.m_tiles * g.n_tiles, p->num_sms), st));
+                          cap_grid(g.m_tiles * g.n_tiles * g.splits, p->num_sms), st));
   return NF_OK;
 }
 
@@ -951,7 +1010,18 @@ nf_status nf_gemm(const void* A, const void* B, void* C, const void* R, int32_t 
   g.timeout_ns = kDefaultTimeoutNs;
   g.stages = 4;
   const int cap = (max_sms > 0 && max_sms < sms) ? max_sms : sms;
-  NF_CUDA(nf::launch_gemm(epilogue, ta, tb, tb2, g, cap_grid(g.m_tiles * g.n_tiles, cap),
+  g.splits = 1;
+  const int splits = choose_splits(g.m_tiles * g.n_tiles, K, cap);
+  if (splits > 1) {
+    GlobalSplitWs* ws = global_split_ws();
+    if (ws->part) {
+      g.splits = splits;
+      g.part = ws->part;
+      g.tile_cnt = ws->cnt;
+    }
+  }
+  NF_CUDA(nf::launch_gemm(epilogue, ta, tb, tb2, g,
+                          cap_grid(g.m_tiles * g.n_tiles * g.splits, cap),
                           static_cast<cudaStream_t>(stream)));
   return NF_OK;
 }

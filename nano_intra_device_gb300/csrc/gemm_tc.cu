@@ -36,8 +36,10 @@ struct GemmSmemTail {
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
+  uint64_t epi_sync;   // rendezvous of the 4 epilogue warps (split-K)
   uint32_t tmem_base;
   int abort;
+  int last;            // this CTA finishes the tile's last split (split-K)
 };
 
 __device__ __forceinline__ void store32_bf16(__nv_bfloat16* dst, const float* v) {
@@ -94,7 +96,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int total_tiles = args.m_tiles * args.n_tiles;
+  // Work units: (output tile, K split).  The splits of one tile are adjacent
+  // unit numbers, so they run on different CTAs at the same time.
+  const int splits = args.splits > 1 ? args.splits : 1;
+  const int total_tiles = args.m_tiles * args.n_tiles * splits;
   const int nk = (args.K + BK - 1) / BK;
   const uint64_t tmo = args.timeout_ns;
 
@@ -108,6 +113,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       mbar_init(&tail->tempty[a], 128);
     }
     mbar_init(&tail->drain, 1);
+    mbar_init(&tail->epi_sync, 4);
     tail->abort = 0;
     fence_mbar_init();
     prefetch_tensormap(&tmA);
@@ -130,10 +136,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       uint32_t st = 0, ph = 0;
       uint32_t issued_mask = 0, last_ph[MAX_STAGES] = {0, 0, 0, 0};
       bool ok = true;
-      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+      for (int u = blockIdx.x; u < total_tiles && ok; u += gridDim.x) {
+        const int t = u / splits, sp = u % splits;
         const int tm = t % args.m_tiles, tn = t / args.m_tiles;
         const int m0 = args.m_begin + tm * BM;
-        for (int kb = 0; kb < nk; ++kb) {
+        const int kb0 = sp * nk / splits, kb1 = (sp + 1) * nk / splits;
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&tail->empty[st], ph ^ 1, tmo, abort_flag)) {
             ok = false;
             break;
@@ -169,14 +177,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     if (lane == 0) {
       uint32_t st = 0, ph = 0, acc = 0, aph = 0;
       bool ok = true, any = false;
-      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+      for (int u = blockIdx.x; u < total_tiles && ok; u += gridDim.x) {
+        const int sp = u % splits;
+        const int kb0 = sp * nk / splits, kb1 = (sp + 1) * nk / splits;
         if (!mbar_wait(&tail->tempty[acc], aph ^ 1, tmo, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < nk; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&tail->full[st], ph, tmo, abort_flag)) {
             ok = false;
             break;
@@ -188,7 +198,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
             // advance 16 bf16 = 32 bytes along K inside the swizzled row
-            tc_mma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, IDESC, (kb | k) != 0);
+            tc_mma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, IDESC, (kb != kb0) || (k != 0));
           }
           any = true;
           tc_commit(&tail->empty[st]);
@@ -217,8 +227,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     // ---------------------------------------------------------- epilogue
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const int row_in_tile = quarter * 32 + lane;
-    uint32_t acc = 0, aph = 0;
-    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+    uint32_t acc = 0, aph = 0, esync = 0;
+    // rendezvous of the four epilogue warps (bounded)
+    auto epi_sync = [&]() -> bool {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tail->epi_sync);
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&tail->epi_sync, esync & 1, tmo, abort_flag));
+      ++esync;
+      return ok;
+    };
+    for (int u = blockIdx.x; u < total_tiles; u += gridDim.x) {
+      const int t = u / splits, sp = u % splits;
       // the wait result must be warp-uniform: tcgen05.ld below is .sync.aligned
       const bool got = __all_sync(0xffffffffu, mbar_wait(&tail->tfull[acc], aph, tmo, abort_flag));
       if (!got) {
@@ -232,12 +251,95 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const bool row_ok = m < args.m_end;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
       float v[32];
+      // Split-K: publish this split's fp32 tile, and let the CTA that finishes
+      // the tile's last split add the others and run the epilogue.
+      bool reduce = false;
+      float* part_tile = nullptr;
+      if (splits > 1) {
+        // Partial layout per split: float4 (chunk c of 32 columns, quad i, row),
+        // rows fastest, so a warp's 32 rows write 512 contiguous bytes.
+        part_tile = args.part + static_cast<size_t>(t) * splits * BM * BN;
+        float4* mine = reinterpret_cast<float4*>(part_tile + static_cast<size_t>(sp) * BM * BN) +
+                       row_in_tile;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          tmem_load32(tbase + c * 32, v);
+          if (row_ok) {  // rows past the range are never read back
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              mine[(c * 8 + i) * BM] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          }
+        }
+        __threadfence();
+        bool ok = epi_sync();
+        if (ok && warp == 2 && lane == 0)
+          tail->last = atomicAdd(&args.tile_cnt[t], 1) == splits - 1;
+        ok = ok && epi_sync();
+        if (!ok) {
+          raise_status(args.status, ST_TIMEOUT);
+          *abort_flag = 1;
+          break;
+        }
+        if (!tail->last) {  // another split finishes this tile
+          tc_fence_before();
+          mbar_arrive(&tail->tempty[acc]);
+          if (++acc == 2) {
+            acc = 0;
+            aph ^= 1;
+          }
+          continue;
+        }
+        __threadfence();
+        reduce = true;
+        if (warp == 2 && lane == 0) args.tile_cnt[t] = 0;  // ready for the next GEMM
+      }
+      // 32 accumulator columns starting at column col.  Split-K: the sum of the
+      // splits' partials, always in split order, so the result does not depend
+      // on which CTA arrived last.
+      auto fetch32 = [&](int col, float* out) {
+        tmem_load32(tbase + col, out);  // keeps every lane in the .sync.aligned load
+        if (reduce && row_ok) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) out[i] = 0.f;
+          const float4* src = reinterpret_cast<const float4*>(part_tile) + (col / 32) * 8 * BM +
+                              row_in_tile;
+          constexpr int kSplit4 = BM * BN / 4;  // float4 per split
+          // two splits' loads in flight at a time; the sum stays in split order
+          for (int o = 0; o < splits; o += 2) {
+            const bool two = o + 1 < splits;
+            float4 x[8], y[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[i] = __ldcg(src + static_cast<size_t>(o) * kSplit4 + i * BM);
+            if (two) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                y[i] = __ldcg(src + static_cast<size_t>(o + 1) * kSplit4 + i * BM);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              out[4 * i] += x[i].x;
+              out[4 * i + 1] += x[i].y;
+              out[4 * i + 2] += x[i].z;
+              out[4 * i + 3] += x[i].w;
+            }
+            if (two) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                out[4 * i] += y[i].x;
+                out[4 * i + 1] += y[i].y;
+                out[4 * i + 2] += y[i].z;
+                out[4 * i + 3] += y[i].w;
+              }
+            }
+          }
+        }
+      };
 
       if (EPI == EPI_STORE || EPI == EPI_RESID) {
         __nv_bfloat16* crow = args.C + static_cast<size_t>(m) * args.ldc;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
-          tmem_load32(tbase + c * 32, v);
+          fetch32(c * 32, v);
           const int n = tn * BN + c * 32;
           if (row_ok && n < args.N) {
             if (EPI == EPI_RESID) {
@@ -261,8 +363,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         float u[32];
 #pragma unroll 1
         for (int c = 0; c < BN / 64; ++c) {
-          tmem_load32(tbase + c * 32, v);            // gate columns
-          tmem_load32(tbase + BN / 2 + c * 32, u);   // matching up columns
+          fetch32(c * 32, v);            // gate columns
+          fetch32(BN / 2 + c * 32, u);   // matching up columns
           const int n = tn * (BN / 2) + c * 32;
           if (row_ok && n < args.N) {
 #pragma unroll
@@ -295,13 +397,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     static_cast<size_t>(g) * P * d + static_cast<size_t>(slot % P) * d;
             }
           }
-          const uint32_t hb = tbase + hh * d;
+          const int hb = hh * d;  // first accumulator column of this head
           if (is_q || is_k) {
             float w[32];
 #pragma unroll 1
             for (int j0 = 0; j0 < d / 2; j0 += 32) {
-              tmem_load32(hb + j0, v);
-              tmem_load32(hb + d / 2 + j0, w);
+              fetch32(hb + j0, v);
+              fetch32(hb + d / 2 + j0, w);
               if (dst != nullptr) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
@@ -320,7 +422,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           } else {
 #pragma unroll 1
             for (int j0 = 0; j0 < d; j0 += 32) {
-              tmem_load32(hb + j0, v);
+              fetch32(hb + j0, v);
               if (dst != nullptr) store32_bf16(dst + j0, v);
             }
           }

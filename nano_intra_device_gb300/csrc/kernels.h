@@ -28,6 +28,12 @@ struct GemmArgs {
   int n_q, n_kv, head_dim, page_size;
   float log2_theta;
   int stages;           // ring stages: 4 (fills an SM), 3 or 2 (room for attention)
+  // split-K (for few output tiles): each tile's K range is cut into `splits`
+  // pieces on different CTAs; fp32 partials in `part` [tiles][splits][128][BN],
+  // per-tile arrival counters `tile_cnt` (zero between launches)
+  int splits;
+  float* part;
+  int* tile_cnt;
   uint32_t* status;
   unsigned long long timeout_ns;
 };

@@ -19,7 +19,9 @@ def _rand(*shape, std=1.0, seed=0):
 
 # ------------------------------------------------------------------- GEMM
 GEMM_SHAPES = [(128, 256, 64), (36, 512, 256), (300, 688, 256), (1, 8, 8), (129, 264, 200),
-               (1024, 1024, 4096), (2048, 6144, 4096), (640, 4096, 14336)]
+               (1024, 1024, 4096), (2048, 6144, 4096), (640, 4096, 14336),
+               # few output tiles: split-K across CTAs
+               (64, 4096, 14336), (128, 6144, 4096), (8, 1024, 4096), (256, 2048, 8192)]
 
 
 @pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
@@ -32,7 +34,7 @@ def test_gemm_store_matches_float64(M, N, K):
     compare(f64(C), ref, f"gemm {M}x{N}x{K}", rel_l2=5e-3)
 
 
-@pytest.mark.parametrize("M,N,K", [(300, 688, 256), (2048, 4096, 4096)])
+@pytest.mark.parametrize("M,N,K", [(300, 688, 256), (2048, 4096, 4096), (64, 4096, 14336)])
 def test_gemm_residual_matches_float64(M, N, K):
     A, B, R = _rand(M, K, seed=3), _rand(N, K, std=0.02, seed=4), _rand(M, N, seed=5)
     C = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
@@ -41,7 +43,8 @@ def test_gemm_residual_matches_float64(M, N, K):
     compare(f64(C), f64(R) + f64(A) @ f64(B).T, "gemm+residual", rel_l2=5e-3)
 
 
-@pytest.mark.parametrize("M,F,K", [(36, 688, 256), (1024, 14336, 4096), (200, 320, 512)])
+@pytest.mark.parametrize("M,F,K", [(36, 688, 256), (1024, 14336, 4096), (200, 320, 512),
+                                   (64, 1024, 4096)])
 def test_gemm_swiglu_matches_float64(M, F, K):
     A, B = _rand(M, K, seed=6), _rand(2 * F, K, std=0.02, seed=7)
     C = torch.empty(M, F, dtype=torch.bfloat16, device=DEV)
@@ -52,12 +55,25 @@ def test_gemm_swiglu_matches_float64(M, F, K):
     compare(f64(C), orc.silu(g) * u, "gemm+swiglu", rel_l2=5e-3)
 
 
+def test_gemm_split_k_repeats_identically():
+    # the per-tile arrival counters reset themselves: a second call splits the same way
+    A, B = _rand(64, 14336, seed=12), _rand(4096, 14336, std=0.02, seed=13)
+    Ad, Bd = A.to(DEV), B.to(DEV)
+    C1 = torch.empty(64, 4096, dtype=torch.bfloat16, device=DEV)
+    C2 = torch.empty_like(C1)
+    _lib.gemm(Ad, Bd, C1)
+    _lib.gemm(Ad, Bd, C2)
+    torch.cuda.synchronize()
+    assert torch.equal(C1, C2)
+
+
 def test_gemm_sm_cap_gives_identical_bits():
-    A, B = _rand(1024, 4096, seed=8), _rand(2048, 4096, std=0.02, seed=9)
+    # 256 output tiles: no split-K at any cap, so the bits must not depend on it
+    A, B = _rand(2048, 4096, seed=8), _rand(4096, 4096, std=0.02, seed=9)
     Ad, Bd = A.to(DEV), B.to(DEV)
     outs = []
     for cap in (0, 7, 64):
-        C = torch.empty(1024, 2048, dtype=torch.bfloat16, device=DEV)
+        C = torch.empty(2048, 4096, dtype=torch.bfloat16, device=DEV)
         _lib.gemm(Ad, Bd, C, max_sms=cap)
         outs.append(C)
     torch.cuda.synchronize()
