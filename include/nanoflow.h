@@ -61,6 +61,12 @@ typedef enum {
                              each kernel capped to its SM share */
 } nf_executor;
 
+typedef enum {
+  NF_ATTN_AUTO = 0, /* tensor-core kernel where supported, else the FMA kernel */
+  NF_ATTN_FMA = 1,  /* dot products on the CUDA cores (packed fp32 FMA) */
+  NF_ATTN_MMA = 2   /* dot products on the tensor cores (mma.sync, bf16 x bf16 -> fp32) */
+} nf_attn_impl;
+
 /* Shape of one Llama-style decoder layer.  head_dim in {64, 128};
  * n_q_heads a multiple of n_kv_heads with n_q/n_kv in {1, 2, 4, 8};
  * hidden and ffn multiples of 16; page_size = 16. */
@@ -107,13 +113,19 @@ typedef struct {
   int32_t attn_sms;   /* SMs for attention while it overlaps GEMMs (0 = automatic) */
   int32_t gemm_sms;   /* SMs for a GEMM while it overlaps attention (0 = the rest) */
   int32_t kv_chunk;   /* split-KV piece in tokens, multiple of page_size, <= 2048 (0 = 1024) */
-  int32_t attn_warps; /* warps per attention CTA: 8, or 12 / 16 as warp pairs that split
-                         head_dim 128, fill an SM; 4 or 5 share each SM with one GEMM
-                         CTA of gemm_stages = 2 (0 = 8) */
+  int32_t attn_warps; /* warps per attention CTA (0 = 8).  Tensor-core kernel: 4 ... 8,
+                         10, 12 or 14, each CTA alone on its SM, ring stages per warp as
+                         deep as shared memory allows (4: 7, 5: 5, 6: 4, 7: 4, 8: 3, more
+                         warps: 2 pages).  FMA kernel: 8; 12 / 16 as warp pairs that split
+                         head_dim 128; 4 or 5 share each SM with one GEMM CTA of
+                         gemm_stages = 2 */
   int32_t gemm_stages; /* shared-memory ring stages of the GEMM kernel: 4 fills an SM;
                           2 lets an attention CTA of 4 or 5 warps run on the same SM (0 = 4) */
   int32_t gemm_split_k; /* 0: split K across CTAs when a GEMM has fewer output tiles than
                            half its SMs; 1: never split */
+  int32_t attn_impl;  /* nf_attn_impl.  NF_ATTN_AUTO picks the FMA kernel for its own
+                         attn_warps 4, 5 and 16, else the tensor-core kernel where the
+                         shape allows it */
   int32_t validate;   /* 1 = check page ids and lengths on the device */
   int64_t timeout_ns; /* limit of every device-side wait (0 = 2e9) */
 } nf_plan_opts;

@@ -135,6 +135,13 @@ struct nf_plan_s {
     CUtensorMap qkv, o, g, u, d;
   };
   std::vector<WeightMaps> wcache;
+  // attention: which kernel, and TMA maps over every (K pool, V pool) pair seen
+  bool attn_mma = false;
+  struct PoolMaps {
+    const void *k, *v;
+    CUtensorMap tk, tv;
+  };
+  std::vector<PoolMaps> pcache;
   // split-K GEMM workspace: fp32 partial tiles and per-tile arrival counters
   float* gemm_part = nullptr;
   int* gemm_cnt = nullptr;
@@ -230,13 +237,19 @@ nf_status check_opts(const nf_plan_opts* o, int T, int num_sms) {
   if (o->attn_sms < 0 || o->attn_sms > num_sms || o->gemm_sms < 0 || o->gemm_sms > num_sms)
     return fail(NF_ERR_INVALID_ARG, "SM shares must lie in [0, %d]", num_sms);
   if (o->timeout_ns <= 0) return fail(NF_ERR_INVALID_ARG, "timeout_ns must be positive");
-  if (o->attn_warps != 4 && o->attn_warps != 5 && o->attn_warps != 8 && o->attn_warps != 12 &&
-      o->attn_warps != 16)
-    return fail(NF_ERR_INVALID_ARG, "attn_warps must be 4, 5, 8, 12 or 16");
+  const int aw = o->attn_warps;
+  if (aw < 4 || (aw > 8 && aw != 10 && aw != 12 && aw != 14 && aw != 16))
+    return fail(NF_ERR_INVALID_ARG, "attn_warps must be 4 ... 8, 10, 12, 14 or 16");
   if (o->gemm_stages < 2 || o->gemm_stages > 4)
     return fail(NF_ERR_INVALID_ARG, "gemm_stages must be 2, 3 or 4");
   if (o->gemm_split_k != 0 && o->gemm_split_k != 1)
     return fail(NF_ERR_INVALID_ARG, "gemm_split_k must be 0 (automatic) or 1 (never)");
+  if (o->attn_impl < NF_ATTN_AUTO || o->attn_impl > NF_ATTN_MMA)
+    return fail(NF_ERR_INVALID_ARG, "attn_impl must be 0 (automatic), 1 (FMA) or 2 (MMA)");
+  if (o->attn_impl == NF_ATTN_MMA && aw == 16)
+    return fail(NF_ERR_INVALID_ARG, "the tensor-core attention runs 4 ... 8, 10, 12 or 14 warps");
+  if (o->attn_impl == NF_ATTN_FMA && aw != 4 && aw != 5 && aw != 8 && aw != 12 && aw != 16)
+    return fail(NF_ERR_INVALID_ARG, "the FMA attention runs 4, 5, 8, 12 or 16 warps per CTA");
   return NF_OK;
 }
 
@@ -386,6 +399,26 @@ nf_status build_plan(const nf_model_shape* shape, const nf_batch_desc* batch,
   if (s != NF_OK) {
     delete p;
     return s;
+  }
+  {
+    const nf_model_shape& sh = p->shape;
+    const bool mma_ok = nf::attention_mma_supported(sh.n_q_heads, sh.n_kv_heads, sh.head_dim,
+                                                    sh.page_size, p->num_pages);
+    if (p->opts.attn_impl == NF_ATTN_MMA && !mma_ok) {
+      delete p;
+      return fail(NF_ERR_UNSUPPORTED, "tensor-core attention: unsupported shape or pool size");
+    }
+    // automatic: the tensor cores, except for the FMA kernel's own shared-SM
+    // (4, 5 warps) and warp-pair (16) configurations
+    const int w = p->opts.attn_warps;
+    const bool fma_cfg = w == 4 || w == 5 || w == 16;
+    const bool fma_has = w == 4 || w == 5 || w == 8 || w == 12 || w == 16;
+    p->attn_mma = p->opts.attn_impl == NF_ATTN_MMA ||
+                  (p->opts.attn_impl == NF_ATTN_AUTO && mma_ok && !fma_cfg);
+    if (!p->attn_mma && !fma_has) {
+      delete p;
+      return fail(NF_ERR_UNSUPPORTED, "attn_warps %d needs the tensor-core attention", w);
+    }
   }
   s = alloc_plan(p);
   if (s != NF_OK) {
@@ -551,6 +584,25 @@ nf_status run_attention(nf_plan p, int seg, const void* q, const void* kp, const
   a.warps = p->opts.attn_warps;
   a.status = p->status;
   a.timeout_ns = (unsigned long long)p->opts.timeout_ns;
+  if (p->attn_mma) {
+    const nf_plan_s::PoolMaps* pm = nullptr;
+    for (const auto& c : p->pcache)
+      if (c.k == kp && c.v == vp) pm = &c;
+    if (!pm) {
+      nf_plan_s::PoolMaps c{};
+      c.k = kp;
+      c.v = vp;
+      const nf_model_shape& sh = p->shape;
+      if (!nf::make_pool_tmap(&c.tk, kp, p->num_pages, sh.n_kv_heads, sh.page_size, sh.head_dim) ||
+          !nf::make_pool_tmap(&c.tv, vp, p->num_pages, sh.n_kv_heads, sh.page_size, sh.head_dim))
+        return fail(NF_ERR_INVALID_ARG, "KV pool tensor maps: pools must be 16-byte aligned");
+      if (p->pcache.size() >= 4096) p->pcache.clear();
+      p->pcache.push_back(c);
+      pm = &p->pcache.back();
+    }
+    NF_CUDA(nf::launch_attention_mma(a, pm->tk, pm->tv, grid, st));
+    return NF_OK;
+  }
   NF_CUDA(nf::launch_attention(a, grid, st));
   return NF_OK;
 }
@@ -766,7 +818,7 @@ nf_status nf_plan_save(nf_plan p, const char* path) {
   FILE* f = std::fopen(path, "w");
   if (!f) return fail(NF_ERR_INVALID_ARG, "cannot open %s", path);
   const nf_model_shape& s = p->shape;
-  std::fprintf(f, "nanoflow-plan 1\n");
+  std::fprintf(f, "nanoflow-plan 2\n");
   std::fprintf(f, "shape %d %d %d %d %d %d %.9g %.9g\n", s.hidden, s.n_q_heads, s.n_kv_heads,
                s.head_dim, s.ffn, s.page_size, s.rms_eps, s.rope_theta);
   std::fprintf(f, "batch %d %d %d %d\n", p->n_decode, p->n_prefill, p->max_pages, p->num_pages);
@@ -778,9 +830,9 @@ nf_status nf_plan_save(nf_plan p, const char* path) {
   for (int i = 0; i <= o.n_attn; ++i) std::fprintf(f, " %d", o.attn_bounds[i]);
   std::fprintf(f, "\nffn %d", o.n_ffn);
   for (int i = 0; i <= o.n_ffn; ++i) std::fprintf(f, " %d", o.ffn_bounds[i]);
-  std::fprintf(f, "\nexec %d %d %d %d %d %lld %d %d %d\n", o.executor, o.attn_sms, o.gemm_sms,
-               o.kv_chunk, o.validate, (long long)o.timeout_ns, o.attn_warps, o.gemm_stages,
-               o.gemm_split_k);
+  std::fprintf(f, "\nexec %d %d %d %d %d %lld %d %d %d %d\n", o.executor, o.attn_sms,
+               o.gemm_sms, o.kv_chunk, o.validate, (long long)o.timeout_ns, o.attn_warps,
+               o.gemm_stages, o.gemm_split_k, o.attn_impl);
   std::fclose(f);
   return NF_OK;
 }
@@ -794,7 +846,7 @@ nf_status nf_plan_load(const char* path, nf_plan* out) {
   int nd = 0, np = 0, mp = 0, npg = 0, ver = 0;
   long long tmo = 0;
   std::vector<int> pq;
-  bool ok = std::fscanf(f, " nanoflow-plan %d", &ver) == 1 && ver == 1;
+  bool ok = std::fscanf(f, " nanoflow-plan %d", &ver) == 1 && ver == 2;
   ok = ok && std::fscanf(f, " shape %d %d %d %d %d %d %f %f", &s.hidden, &s.n_q_heads,
                          &s.n_kv_heads, &s.head_dim, &s.ffn, &s.page_size, &s.rms_eps,
                          &s.rope_theta) == 8;
@@ -809,9 +861,9 @@ nf_status nf_plan_load(const char* path, nf_plan* out) {
   for (int i = 0; ok && i <= o.n_attn; ++i) ok = std::fscanf(f, " %d", &o.attn_bounds[i]) == 1;
   ok = ok && std::fscanf(f, " ffn %d", &o.n_ffn) == 1 && o.n_ffn >= 1 && o.n_ffn <= NF_MAX_NANO;
   for (int i = 0; ok && i <= o.n_ffn; ++i) ok = std::fscanf(f, " %d", &o.ffn_bounds[i]) == 1;
-  ok = ok && std::fscanf(f, " exec %d %d %d %d %d %lld %d %d %d", &o.executor, &o.attn_sms,
+  ok = ok && std::fscanf(f, " exec %d %d %d %d %d %lld %d %d %d %d", &o.executor, &o.attn_sms,
                          &o.gemm_sms, &o.kv_chunk, &o.validate, &tmo, &o.attn_warps,
-                         &o.gemm_stages, &o.gemm_split_k) == 9;
+                         &o.gemm_stages, &o.gemm_split_k, &o.attn_impl) == 10;
   std::fclose(f);
   if (!ok) return fail(NF_ERR_INVALID_ARG, "%s is not a plan file", path);
   o.timeout_ns = tmo;

@@ -23,6 +23,7 @@
 //   * a piece that is a row's only chunk writes o directly; otherwise it
 //     writes (acc, m, l) and the warp that finishes the row's last piece merges
 //     them by log-sum-exp.
+#include "attn_merge.cuh"
 #include "common.cuh"
 #include "kernels.h"
 
@@ -396,50 +397,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) attn_kernel(const AttnArgs a) {
         rec[GRP * D + GRP + h] = l[h];
       }
     }
-    __threadfence();
-    __syncwarp();
-    int last = 0;
-    if (lane == 0) last = atomicAdd(&a.row_done[t * n_kv + g], 1) == nch - 1;
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (!last) continue;
-    __threadfence();
-#pragma unroll
-    for (int h = 0; h < GRP; ++h) {
-      if ((h & 3) != ts) continue;
-      float M = -INFINITY;
-      for (int cc = 0; cc < nch; ++cc) {
-        const float* r = a.partials + ((row_rec + cc) * n_kv + g) * REC;
-        M = fmaxf(M, __ldcg(r + GRP * D + h));
-      }
-      float L = 0.f, O[NCH * 8];
-#pragma unroll
-      for (int e = 0; e < NCH * 8; ++e) O[e] = 0.f;
-      for (int cc = 0; cc < nch; ++cc) {
-        const float* r = a.partials + ((row_rec + cc) * n_kv + g) * REC;
-        const float w = exp2f(__ldcg(r + GRP * D + h) - M);
-        L += w * __ldcg(r + GRP * D + GRP + h);
-#pragma unroll
-        for (int ch = 0; ch < NCH; ++ch) {
-          const float4* src = reinterpret_cast<const float4*>(r + h * D + ch * 64 + dg * 8);
-          const float4 x0 = __ldcg(src), x1 = __ldcg(src + 1);
-          O[ch * 8 + 0] += w * x0.x; O[ch * 8 + 1] += w * x0.y;
-          O[ch * 8 + 2] += w * x0.z; O[ch * 8 + 3] += w * x0.w;
-          O[ch * 8 + 4] += w * x1.x; O[ch * 8 + 5] += w * x1.y;
-          O[ch * 8 + 6] += w * x1.z; O[ch * 8 + 7] += w * x1.w;
-        }
-      }
-      const float inv = 1.f / L;
-      __nv_bfloat16* orow = a.o + (static_cast<size_t>(t) * n_q + g * GRP + h) * D;
-#pragma unroll
-      for (int ch = 0; ch < NCH; ++ch) {
-        uint4 u;
-        u.x = pack_bf16(O[ch * 8 + 0] * inv, O[ch * 8 + 1] * inv);
-        u.y = pack_bf16(O[ch * 8 + 2] * inv, O[ch * 8 + 3] * inv);
-        u.z = pack_bf16(O[ch * 8 + 4] * inv, O[ch * 8 + 5] * inv);
-        u.w = pack_bf16(O[ch * 8 + 6] * inv, O[ch * 8 + 7] * inv);
-        *reinterpret_cast<uint4*>(orow + ch * 64 + dg * 8) = u;
-      }
-    }
+    if (finish_piece(a, t, g, nch, lane)) merge_row_partials<GRP, NCH>(a, t, g, nch, lane);
   }
 
   if (failed) raise_status(a.status, ST_TIMEOUT);

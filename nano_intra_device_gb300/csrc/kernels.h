@@ -118,5 +118,14 @@ __host__ __device__ constexpr int partial_rec_floats(int grp, int head_dim) {
 // Warp-pair variant for head_dim 128 (warps 12: 6 pairs x 4 stages; 16: 8 pairs x 3).
 cudaError_t launch_attention_pair(const AttnArgs& a, int grid, cudaStream_t stream);
 cudaError_t launch_attention(const AttnArgs& a, int grid, cudaStream_t stream);
+// Tensor-core variant (mma.sync m16n8k16, bf16 operands, fp32 accumulators) of
+// the same operation with the same records; K and V pages arrive by 2-D TMA
+// copies through maps over the pools viewed as [num_pages * n_kv * 16, d]
+// (make_pool_tmap).  Supported: page 16, d 64 or 128, GQA group 1, 2, 4 or 8.
+bool attention_mma_supported(int n_q, int n_kv, int head_dim, int page_size, int num_pages);
+bool make_pool_tmap(CUtensorMap* map, const void* pool, int num_pages, int n_kv, int page_size,
+                    int head_dim);
+cudaError_t launch_attention_mma(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
+                                 int grid, cudaStream_t stream);
 
 }  // namespace nf
