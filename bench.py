@@ -353,7 +353,7 @@ def main():
     if args.plan == "auto":
         for n in (2, 3):
             ab = [0] + [int(round(T * i / n / 128)) * 128 for i in range(1, n)] + [T]
-            for a_sms in (sms * 9 // 16, sms * 10 // 16, sms * 11 // 16, sms * 12 // 16):
+            for a_sms in (sms * 7 // 16, sms * 8 // 16, sms * 9 // 16, sms * 10 // 16):
                 o = _lib.make_opts(T, ab, ab, executor=_lib.NF_EXEC_STREAMS, attn_sms=a_sms)
                 cands.append((f"n={n},attn_sms={a_sms}", make_plan(o)))
     elif args.plan.startswith("n="):
@@ -395,14 +395,18 @@ def main():
     attn_bytes_per_launch = wk.attn_bytes / n_attn
     attn_ms = sum(attn) / max(1, len(attn))
     achieved = attn_bytes_per_launch / (attn_ms * 1e-3) / 1e9
+    mma = po.attn_impl == _lib.NF_ATTN_MMA
+    src_name = "attn_mma.cu" if mma else "attn.cu"
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "attn_traffic.json")
     if os.path.exists(tpath):
-        tj = json.load(open(tpath))
-        src = open(os.path.join(ROOT, "nano_intra_device_gb300", "csrc", "attn.cu"), "rb").read()
+        tj = json.load(open(tpath)).get(src_name, {})
+        src = open(os.path.join(ROOT, "nano_intra_device_gb300", "csrc", src_name), "rb").read()
         if tj.get("source_sha256") == hashlib.sha256(src).hexdigest():
             traffic = tj.get("bytes_per_launch", {}).get(str(n_attn))
-    roof = {"bound": "hbm", "kernel": "attn_kernel (paged GQA decode attention)",
+    kname = ("attn_mma_kernel (paged GQA attention, tensor cores)" if mma else
+             "attn_kernel (paged GQA attention, CUDA-core FMA)")
+    roof = {"bound": "hbm", "kernel": kname,
             "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
             "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
             "peak_source": pk["source"] + " hbm_gbs (copy)",

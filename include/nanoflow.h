@@ -125,7 +125,7 @@ typedef struct {
                            half its SMs; 1: never split */
   int32_t attn_impl;  /* nf_attn_impl.  NF_ATTN_AUTO picks the FMA kernel for its own
                          attn_warps 4, 5 and 16, else the tensor-core kernel where the
-                         shape allows it */
+                         shape allows it; nf_plan_info reports the kernel chosen */
   int32_t validate;   /* 1 = check page ids and lengths on the device */
   int64_t timeout_ns; /* limit of every device-side wait (0 = 2e9) */
 } nf_plan_opts;

@@ -419,6 +419,7 @@ nf_status build_plan(const nf_model_shape* shape, const nf_batch_desc* batch,
       delete p;
       return fail(NF_ERR_UNSUPPORTED, "attn_warps %d needs the tensor-core attention", w);
     }
+    p->opts.attn_impl = p->attn_mma ? NF_ATTN_MMA : NF_ATTN_FMA;  // nf_plan_info reports the choice
   }
   s = alloc_plan(p);
   if (s != NF_OK) {

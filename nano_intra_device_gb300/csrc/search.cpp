@@ -33,13 +33,21 @@ namespace {
 // Defaults are GB300 measurements of this library's kernels (nf_profile on the
 // 8B-shaped layer); a profile file overrides them.
 struct Rates {
-  double gemm_flops_per_sm = 12.6e12;  // tensor rate of a GEMM confined to S SMs, per SM
-  double hbm_bps = 6.4e12;             // attention bandwidth with every SM
-  double attn_bps_per_sm = 44e9;       // attention bytes/s one SM sustains
+  double gemm_flops_per_sm = 11.45e12; // tensor rate of a GEMM, per SM (all 152 SMs busy)
+  double qkv_row_sm_s = 3.5e-6;        // SM-seconds per token row of the QKV epilogue
+                                       // (RoPE and the K/V append into the pools)
+  double stream_sync_s = 25e-6;        // cost of one cross-stream dependency (event wait,
+                                       // launch, pipeline fill of the waiting kernel)
+  double hbm_bps = 6.75e12;            // attention bandwidth with every SM
+  double attn_bps_per_sm = 78e9;       // attention bytes/s one SM sustains (tensor-core
+                                       // kernel, 8 warps, measured on 57 SMs in the step)
   double gemm_launch_s = 4e-6;
   double attn_launch_s = 4e-6;
-  double overlap_bw_factor = 0.94;     // attention speed kept beside a GEMM on other SMs
-  double overlap_gemm_factor = 0.95;   // GEMM speed kept beside attention on other SMs
+  // Interference measured on the 8B-shaped step with 76 attention SMs: attention
+  // keeps 0.85 of its alone bandwidth beside GEMMs, gate/up + down keep 0.6 ... 0.8
+  // of their per-SM rate beside attention (the lower end for 512-token nano-batches).
+  double overlap_bw_factor = 0.85;     // attention speed kept beside a GEMM on other SMs
+  double overlap_gemm_factor = 0.65;   // GEMM speed kept beside attention on other SMs
 };
 
 double json_number(const std::string& s, const char* key, double dflt) {
@@ -67,6 +75,8 @@ bool load_rates(const char* path, Rates* r) {
   r->attn_launch_s = json_number(s, "attn_launch_s", r->attn_launch_s);
   r->overlap_bw_factor = json_number(s, "overlap_bw_factor", r->overlap_bw_factor);
   r->overlap_gemm_factor = json_number(s, "overlap_gemm_factor", r->overlap_gemm_factor);
+  r->qkv_row_sm_s = json_number(s, "qkv_row_sm_s", r->qkv_row_sm_s);
+  r->stream_sync_s = json_number(s, "stream_sync_s", r->stream_sync_s);
   return true;
 }
 
@@ -86,7 +96,8 @@ struct Model {
   }
   // QKV + O for rows, or RMSNorm-2 + gate/up + down for rows
   double qkv_time(int rows, int S) const {
-    return gemm_time(rows, (s.n_q_heads + 2 * s.n_kv_heads) * s.head_dim, s.hidden, S, 256);
+    return gemm_time(rows, (s.n_q_heads + 2 * s.n_kv_heads) * s.head_dim, s.hidden, S, 256) +
+           rows * r.qkv_row_sm_s / S;
   }
   double o_time(int rows, int S) const {
     return gemm_time(rows, s.hidden, s.n_q_heads * s.head_dim, S, 256);
@@ -124,14 +135,15 @@ double simulate(const Model& m, const nf_plan_opts& o) {
     tg += m.qkv_time(o.attn_bounds[i + 1] - o.attn_bounds[i], i == 0 ? all : gsm) * (i == 0 ? 1.0 : slow);
     q_done[i] = tg;
   }
+  const double sync = m.r.stream_sync_s;
   for (int i = 0; i < n; ++i) {
-    ta = std::max(ta, q_done[i]);
+    ta = std::max(ta, q_done[i] + sync);  // attention i waits for QKV i on the other stream
     ta += m.attn_time(o.attn_bounds[i], o.attn_bounds[i + 1], attn_sms, n > 1);
     a_done[i] = ta;
   }
   int next_ffn = 0;
   for (int i = 0; i < n; ++i) {
-    tg = std::max(tg, a_done[i]);
+    tg = std::max(tg, a_done[i] + sync);  // O projection i waits for attention i
     const int S = (i == n - 1) ? all : gsm;
     const double f = (i == n - 1) ? 1.0 : slow;
     tg += m.o_time(o.attn_bounds[i + 1] - o.attn_bounds[i], S) * f;

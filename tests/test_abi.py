@@ -40,15 +40,17 @@ def _check_plan(o, T, grid):
 
 def test_plan_search_llama8b_follows_the_rates(L, tmp_path):
     shape, batch = wl.llama8b_shape(), wl.llama8b_batch()
-    # with the measured GB300 rates attention needs nearly every SM to reach HBM
+    # with the measured GB300 rates attention needs most of the SMs to reach HBM
     # speed, so splitting the GPU cannot win: the search keeps one nano-batch
     o, t = _lib.plan_search(shape, batch, None, 152)
     _check_plan(o, batch.n_tokens, 128)
     assert o.n_attn == 1 and o.executor == _lib.NF_EXEC_SEQUENTIAL
     assert 1000.0 < t < 3000.0
-    # if one SM streamed attention 3x faster, overlap with an SM split would pay
+    # if one SM streamed attention 1.7x faster and neighbours did not slow each
+    # other down, overlap with an SM split would pay
     prof = tmp_path / "fast_attention.json"
-    prof.write_text('{"attn_bps_per_sm": 132e9, "hbm_bps": 6.4e12, "gemm_flops_per_sm": 12.6e12}')
+    prof.write_text('{"attn_bps_per_sm": 132e9, "hbm_bps": 6.75e12, "gemm_flops_per_sm": 11.45e12, '
+                    '"overlap_bw_factor": 0.95, "overlap_gemm_factor": 0.95}')
     o2, t2 = _lib.plan_search(shape, batch, str(prof), 152)
     _check_plan(o2, batch.n_tokens, 128)
     assert o2.n_attn >= 2 and o2.executor == _lib.NF_EXEC_STREAMS
