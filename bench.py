@@ -57,9 +57,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-ablation", action="store_true")
     ap.add_argument("--plan", default="auto", help="auto | search | n=<k>,sms=<s>")
-    ap.add_argument("--workload", default="layer", choices=["layer", "stack"],
+    ap.add_argument("--workload", default="layer", choices=["layer", "stack", "70b"],
                     help="layer: the single 8B-shaped layer step (default); stack: the 32-layer "
-                         "8B-shaped stack with embedding and LM head, decode batches")
+                         "8B-shaped stack with embedding and LM head, decode batches; 70b: ten "
+                         "70B-shaped layers over a 4096-token mixed step")
     ap.add_argument("--batch", type=int, default=256, help="decode requests of the stack workload")
     return ap.parse_args()
 
@@ -321,12 +322,86 @@ def run_stack(args):
     plan.close()
 
 
+def run_70b(args):
+    """Ten LLaMA-2-70B-shaped layers over one 4096-token mixed step (3584 decode
+    requests, lognormal KV median 1000 clipped to [1, 4096], plus a 512-token
+    prefill chunk), each layer with its own weights and KV pools, through
+    nf_layers_step.  Plans: the search's pick, sequential, and SM-split overlap
+    candidates, each timed; the fastest is reported."""
+    from nano_intra_device_gb300 import _lib
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    shape = wl.llama70b_shape()
+    batch = wl.llama70b_batch()
+    L, T, H, F = 10, batch.n_tokens, shape.hidden, shape.ffn
+    g = torch.Generator(device=dev).manual_seed(0)
+
+    def rn(*sz, std=0.02):
+        return (torch.randn(*sz, generator=g, device=dev) * std).to(torch.bfloat16)
+    layers = [{"w_qkv": rn(shape.qkv_rows, H), "w_o": rn(H, shape.n_q * shape.head_dim),
+               "w_gate_up": rn(2 * F, H), "w_down": rn(H, F),
+               "norm1": torch.ones(H, dtype=torch.bfloat16, device=dev),
+               "norm2": torch.ones(H, dtype=torch.bfloat16, device=dev)} for _ in range(L)]
+    pools = [wl.make_pools(shape, batch, dev, seed=100 + l) for l in range(L)]
+    x = (torch.randn(T, H, generator=g, device=dev)).to(torch.bfloat16)
+    y = torch.empty_like(x)
+    bt = torch.from_numpy(batch.block_table).to(dev)
+    sl = torch.from_numpy(batch.seq_lens).to(dev)
+    la = _lib.LayersArgs(layers, pools)
+    stream = torch.cuda.current_stream()
+    sms = _lib.device_sm_count()
+    cands = [("search", None), ("sequential", _lib.make_opts(T))]
+    for n in (2, 4):
+        ab = [0] + [int(round(T * i / n / 128)) * 128 for i in range(1, n)] + [T]
+        for a_sms in (sms * 4 // 16, sms * 6 // 16, sms * 8 // 16):
+            cands.append((f"n={n},attn_sms={a_sms}",
+                          _lib.make_opts(T, ab, ab, executor=_lib.NF_EXEC_STREAMS, attn_sms=a_sms)))
+    tried = {}
+    for name, o in cands:
+        plan = _lib.Plan(shape, batch, o)
+        tried[name] = (time_steps(lambda: _lib.layers_step(plan, la, x, bt, sl, y), 3, 1, 1, stream),
+                       _lib.opts_dict(plan.info()[0]))
+        plan.poll()
+        plan.close()
+    best = min(tried, key=lambda k: tried[k][0])
+    plan = _lib.Plan(shape, batch, dict(cands)[best])
+    clocks = Clocks()
+    for _ in range(args.warmup):
+        _lib.layers_step(plan, la, x, bt, sl, y)
+    torch.cuda.synchronize()
+    clocks.start()
+    ms = time_steps(lambda: _lib.layers_step(plan, la, x, bt, sl, y), args.steps, 0, 1, stream)
+    clk = clocks.stop()
+    plan.poll()
+    pk = peaks()
+    lw = cm.step_work(shape, batch.seq_lens, batch.q_lens)
+    rf = cm.roofline_time({"flops": L * lw["flops"], "bytes": L * lw["bytes"]},
+                          pk["bf16_tflops_sustained"] * 1e12, pk["hbm_gbs"] * 1e9)
+    line = {"metric": "tokens/s per GB300 for a 10-layer 70B-shaped mixed step; % of its roofline",
+            "value": T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16",
+            "data": "synthetic", "clocks": clk,
+            "config": {"workload": "llama2-70b-shaped, 10 layers, 4096-token step: 3584 decode "
+                                   "(lognormal KV median 1000, sigma 1, clip [1,4096]) + one "
+                                   "512-token prefill chunk, 16-token pages",
+                       "kv_read_gb_per_step": L * lw["kv_read_bytes"] / 1e9,
+                       "plan": dict(tried[best][1], chosen=best)},
+            "roofline_10_layers": {"frac": rf["t_roof"] / (ms * 1e-3), "t_roof_ms": rf["t_roof"] * 1e3,
+                                   "t_flop_ms": rf["t_flop"] * 1e3, "t_byte_ms": rf["t_byte"] * 1e3,
+                                   "bound": rf["bound"]},
+            "candidates_ms": {k: round(v[0], 3) for k, v in tried.items()}}
+    print(json.dumps(line), flush=True)
+    plan.close()
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
     if args.workload == "stack":
         return run_stack(args)
+    if args.workload == "70b":
+        return run_70b(args)
     from nano_intra_device_gb300 import _lib
 
     rank, world, local = dist_setup(args.gpus)

@@ -207,6 +207,20 @@ nf_status nf_stack_step(nf_plan plan, const nf_stack_weights* w, const int32_t* 
                         void* const* k_pools, void* const* v_pools, const int32_t* block_table,
                         const int32_t* seq_lens, void* logits, void* stream);
 
+/* n_layers decoder layers over one mixed step, hidden states in and out
+ * ("NanoFlow: Towards Optimal LLM Serving Throughput", "Example Pipelines for
+ * Different Model Scales": the per-layer pipeline repeated over the layers a
+ * GPU holds): layer l reads the previous layer's output (x for l = 0) and
+ * appends this step's K/V into its own pools; the last layer writes y.
+ * layers, k_pools, v_pools: HOST arrays [n_layers] (device weights and pools
+ * as for nf_layer_step).  x, y: device [T, H] bf16, distinct; x is not
+ * modified.  The step metadata is computed once for all layers.  Allocation
+ * and capture behave as for nf_stack_step. */
+nf_status nf_layers_step(nf_plan plan, const nf_layer_weights* layers, int32_t n_layers,
+                         const void* x, void* const* k_pools, void* const* v_pools,
+                         const int32_t* block_table, const int32_t* seq_lens, void* y,
+                         void* stream);
+
 /* The same step with the per-step inputs and the output in HOST memory:
  * x_host [T, H] bf16, block_table_host and seq_lens_host as above, y_host
  * [T, H].  Copies them through plan-owned device staging buffers on `stream`

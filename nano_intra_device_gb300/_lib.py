@@ -73,6 +73,7 @@ _SIGS = {
     "nf_layer_step_host": (c_int, [c_void_p, POINTER(nf_layer_weights), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     "nf_plan_poll": (c_int, [c_void_p, c_int]),
     "nf_stack_step": (c_int, [c_void_p, POINTER(nf_stack_weights), c_void_p, POINTER(c_void_p), POINTER(c_void_p), c_void_p, c_void_p, c_void_p, c_void_p]),
+    "nf_layers_step": (c_int, [c_void_p, POINTER(nf_layer_weights), c_int32, c_void_p, POINTER(c_void_p), POINTER(c_void_p), c_void_p, c_void_p, c_void_p, c_void_p]),
     "nf_last_error": (c_char_p, []),
     "nf_device_sm_count": (c_int32, []),
     "nf_step_metadata": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p]),
@@ -261,6 +262,22 @@ class StackArgs:
 def stack_step(plan: Plan, args: StackArgs, tokens, block_table, seq_lens, logits, stream=None):
     check(lib().nf_stack_step(plan.h, ctypes.byref(args.w), ptr(tokens), args.kps, args.vps,
                               ptr(block_table), ptr(seq_lens), ptr(logits), stream_handle(stream)))
+
+
+class LayersArgs:
+    """Keeps the ctypes arrays of a run of layers (weights and pools) alive."""
+
+    def __init__(self, layers: list, pools: list):
+        self.n = len(layers)
+        self.layer_structs = (nf_layer_weights * self.n)(*[make_weights_struct(w) for w in layers])
+        self.kps = (c_void_p * len(pools))(*[k.data_ptr() for k, _ in pools])
+        self.vps = (c_void_p * len(pools))(*[v.data_ptr() for _, v in pools])
+        self._keep = (layers, pools)
+
+
+def layers_step(plan: Plan, args: LayersArgs, x, block_table, seq_lens, y, stream=None):
+    check(lib().nf_layers_step(plan.h, args.layer_structs, args.n, ptr(x), args.kps, args.vps,
+                               ptr(block_table), ptr(seq_lens), ptr(y), stream_handle(stream)))
 
 
 def layer_step_host(plan: Plan, w: dict, x_host, k_pool, v_pool, bt_host, sl_host, y_host, stream=None):

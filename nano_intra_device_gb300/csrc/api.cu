@@ -885,6 +885,64 @@ nf_status nf_layer_step(nf_plan plan, const nf_layer_weights* w, const void* x, 
                     static_cast<cudaStream_t>(stream));
 }
 
+namespace {
+// Activation buffers and one split-KV counter set per layer for a run of
+// n_layers layers (allocates, and synchronizes the device, only when it grows).
+nf_status ensure_layers(nf_plan p, int n_layers) {
+  const size_t xb = (size_t)p->T * p->shape.hidden * 2;
+  if (!p->xa) {
+    NF_TRY(dalloc(&p->xa, xb));
+    NF_TRY(dalloc(&p->xb, xb));
+  }
+  if (p->counter_sets < n_layers) {
+    NF_CUDA(cudaDeviceSynchronize());
+    cudaFree(p->fetch);
+    cudaFree(p->row_done);
+    p->fetch = nullptr;
+    p->row_done = nullptr;
+    NF_TRY(dalloc(&p->fetch, (size_t)NF_MAX_NANO * n_layers * 4));
+    NF_TRY(dalloc(&p->row_done, (size_t)p->T * p->shape.n_kv_heads * n_layers * 4));
+    p->counter_sets = n_layers;
+  }
+  return NF_OK;
+}
+
+// Metadata once, then layer l reads `in` (x for l = 0) and writes `out` (y for
+// the last layer), ping-ponging between the plan's activation buffers.
+nf_status run_layers(nf_plan p, const nf_layer_weights* layers, int n_layers, const void* x,
+                     void* const* k_pools, void* const* v_pools, const int32_t* bt,
+                     const int32_t* sl, void* y, cudaStream_t st) {
+  NF_TRY(run_meta(p, bt, sl, st));
+  const void* cur = x;
+  for (int l = 0; l < n_layers; ++l) {
+    // intermediate outputs alternate between xa and xb; the caller makes sure
+    // that y is not the last layer's input
+    void* nxt = l == n_layers - 1 ? y : (cur == p->xa ? (void*)p->xb : (void*)p->xa);
+    p->cur_set = l;
+    const nf_status r = layer_step(p, &layers[l], cur, k_pools[l], v_pools[l], bt, sl, nxt, st,
+                                   /*with_meta=*/false);
+    p->cur_set = 0;
+    if (r != NF_OK) return r;
+    cur = nxt;
+  }
+  return NF_OK;
+}
+}  // namespace
+
+nf_status nf_layers_step(nf_plan p, const nf_layer_weights* layers, int32_t n_layers,
+                         const void* x, void* const* k_pools, void* const* v_pools,
+                         const int32_t* bt, const int32_t* sl, void* y, void* stream) {
+  if (!p || !layers || !x || !k_pools || !v_pools || !bt || !sl || !y)
+    return fail(NF_ERR_INVALID_ARG, "NULL argument");
+  if (n_layers < 1) return fail(NF_ERR_INVALID_ARG, "n_layers must be positive");
+  if (x == y) return fail(NF_ERR_INVALID_ARG, "x and y must be different buffers");
+  NF_TRY(ensure_layers(p, n_layers));
+  for (int l = 0; l < n_layers; ++l)
+    NF_TRY(check_step_args(p, &layers[l], x, k_pools[l], v_pools[l], bt, sl, y));
+  return run_layers(p, layers, n_layers, x, k_pools, v_pools, bt, sl, y,
+                    static_cast<cudaStream_t>(stream));
+}
+
 nf_status nf_stack_step(nf_plan p, const nf_stack_weights* sw, const int32_t* tokens,
                         void* const* k_pools, void* const* v_pools, const int32_t* bt,
                         const int32_t* sl, void* logits, void* stream) {
@@ -897,21 +955,7 @@ nf_status nf_stack_step(nf_plan p, const nf_stack_weights* sw, const int32_t* to
   if (!aligned16(sw->embed) || !aligned16(sw->norm_f) || !aligned16(sw->lm_head) ||
       !aligned16(logits))
     return fail(NF_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
-  const size_t xb = (size_t)p->T * p->shape.hidden * 2;
-  if (!p->xa) {
-    NF_TRY(dalloc(&p->xa, xb));
-    NF_TRY(dalloc(&p->xb, xb));
-  }
-  if (p->counter_sets < sw->n_layers) {  // one split-KV counter set per layer
-    NF_CUDA(cudaDeviceSynchronize());
-    cudaFree(p->fetch);
-    cudaFree(p->row_done);
-    p->fetch = nullptr;
-    p->row_done = nullptr;
-    NF_TRY(dalloc(&p->fetch, (size_t)NF_MAX_NANO * sw->n_layers * 4));
-    NF_TRY(dalloc(&p->row_done, (size_t)p->T * p->shape.n_kv_heads * sw->n_layers * 4));
-    p->counter_sets = sw->n_layers;
-  }
+  NF_TRY(ensure_layers(p, sw->n_layers));
   if (p->lm_key != sw->lm_head || p->lm_vocab != sw->vocab) {
     if (!nf::make_tmap_bf16(&p->tm_lm, sw->lm_head, sw->vocab, p->shape.hidden, 256))
       return fail(NF_ERR_INVALID_ARG, "LM head tensor map failed");
@@ -923,19 +967,13 @@ nf_status nf_stack_step(nf_plan p, const nf_stack_weights* sw, const int32_t* to
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const nf_model_shape& s = p->shape;
-  // embedding, then the step metadata once for every layer
+  // embedding into xa, then the layers (metadata once for all of them); layer
+  // l >= 1 reads xb when l is odd, so the last one writes the other buffer
   NF_CUDA(nf::launch_embed(tokens, static_cast<const __nv_bfloat16*>(sw->embed), p->xa, p->T,
                            s.hidden, sw->vocab, p->status, st));
-  NF_TRY(run_meta(p, bt, sl, st));
-  __nv_bfloat16 *cur = p->xa, *nxt = p->xb;
-  for (int l = 0; l < sw->n_layers; ++l) {
-    p->cur_set = l;
-    const nf_status r = layer_step(p, &sw->layers[l], cur, k_pools[l], v_pools[l], bt, sl, nxt, st,
-                                   /*with_meta=*/false);
-    p->cur_set = 0;
-    if (r != NF_OK) return r;
-    std::swap(cur, nxt);
-  }
+  __nv_bfloat16* last = sw->n_layers % 2 ? p->xb : p->xa;
+  NF_TRY(run_layers(p, sw->layers, sw->n_layers, p->xa, k_pools, v_pools, bt, sl, last, st));
+  const __nv_bfloat16* cur = last;
   // final RMSNorm and the LM head: logits = RMSNorm(x) lm_head^T
   NF_CUDA(nf::launch_rmsnorm(cur, static_cast<const __nv_bfloat16*>(sw->norm_f), p->n1, 0, p->T,
                              s.hidden, s.rms_eps, st));

@@ -89,6 +89,12 @@ def llama8b_shape() -> Shape:
                  rms_eps=1e-5, rope_theta=5e5, page_size=16)
 
 
+def llama70b_shape() -> Shape:
+    """LLaMA-2-70B-shaped layer: GQA group of 8, FFN 28672, RoPE theta 1e4."""
+    return Shape(hidden=8192, n_q=64, n_kv=8, head_dim=128, ffn=28672,
+                 rms_eps=1e-5, rope_theta=1e4, page_size=16)
+
+
 def _assign_pages(seq_lens, page_size, seed_bt, slack, max_pages=None):
     need = [(int(L) + page_size - 1) // page_size for L in seq_lens]
     total = int(sum(need))
@@ -145,6 +151,14 @@ def llama8b_batch(n_decode: int = 1792, prefill: int = 256) -> Batch:
     ctx = lognormal_contexts(n_decode, 600.0, 1.0, 1, 8192, seed=1)
     return make_batch(llama8b_shape(), ctx, [prefill] if prefill else [], None,
                       seed_bt=2, slack=0.01, max_pages=8192 // 16, name="llama8b")
+
+
+def llama70b_batch(n_decode: int = 3584, prefill: int = 512) -> Batch:
+    """3584 decode requests (lognormal median 1000, sigma 1, clip [1, 4096]) and
+    one 512-token prefill chunk starting a prompt; 16-token pages, 1% slack."""
+    ctx = lognormal_contexts(n_decode, 1000.0, 1.0, 1, 4096, seed=1)
+    return make_batch(llama70b_shape(), ctx, [prefill] if prefill else [], None,
+                      seed_bt=2, slack=0.01, max_pages=4096 // 16, name="llama70b")
 
 
 # --------------------------------------------------------------------------

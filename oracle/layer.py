@@ -272,6 +272,33 @@ def layer_step(shape, w64: dict, x, k_pool, v_pool, block_table, seq_lens, q_len
 # --------------------------------------------------------------------------
 # a stack of layers with embedding and LM head
 
+def layers_step(shape, layers64: list, x, pools: list, block_table, seq_lens, q_lens,
+                rows=None) -> dict:
+    """Several decoder layers over one mixed step: layer l takes the previous
+    layer's output (x for the first) and reads its own K/V pools; the block
+    table and lengths are shared ("NanoFlow: Towards Optimal LLM Serving
+    Throughput", "Example Pipelines for Different Model Scales": the per-layer
+    step repeated over the layers).
+
+    layers64: float64 weight dicts; pools: (k_pool, v_pool) per layer; x: [T, H].
+    rows: the tokens whose output is wanted; every layer computes the rows
+    those need (their earlier prefill rows).  Returns {"rows", "y" [len(rows),
+    H], "x_all" [T, H] (rows outside the needed set are left as given)}.
+    """
+    q_lens = np.asarray(q_lens, np.int64)
+    seq_lens = np.asarray(seq_lens, np.int64)
+    seq, _ = token_map(q_lens, seq_lens)
+    T = len(seq)
+    rows = np.arange(T, dtype=np.int64) if rows is None else np.asarray(rows, np.int64)
+    need = _needed_rows(seq, rows)
+    x = np.array(f64(x), copy=True)
+    for w64, (kp, vp) in zip(layers64, pools):
+        out = layer_step(shape, w64, x, kp, vp, block_table, seq_lens, q_lens, rows=need)
+        x = x.copy()
+        x[need] = out["y"]
+    return {"rows": rows, "y": x[rows], "x_all": x}
+
+
 def stack_step(shape, embed, norm_f, lm_head, layers64: list, tokens, pools: list, block_table,
                seq_lens, q_lens, rows=None) -> dict:
     """A decoder stack over one mixed step: x = embed[tokens]; each layer's step
@@ -292,9 +319,6 @@ def stack_step(shape, embed, norm_f, lm_head, layers64: list, tokens, pools: lis
     E = f64(embed)
     x = np.zeros((T, shape.hidden))
     x[need] = E[np.asarray(tokens)[need]]
-    for w64, (kp, vp) in zip(layers64, pools):
-        out = layer_step(shape, w64, x, kp, vp, block_table, seq_lens, q_lens, rows=need)
-        x = x.copy()
-        x[need] = out["y"]
-    xf = rmsnorm(x[rows], f64(norm_f), shape.rms_eps)
-    return {"rows": rows, "logits": xf @ f64(lm_head).T, "x_final": x[rows]}
+    out = layers_step(shape, layers64, x, pools, block_table, seq_lens, q_lens, rows=rows)
+    xf = rmsnorm(out["y"], f64(norm_f), shape.rms_eps)
+    return {"rows": rows, "logits": xf @ f64(lm_head).T, "x_final": out["y"]}

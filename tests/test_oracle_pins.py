@@ -405,3 +405,32 @@ def test_stack_rows_subset_equals_full():
     sub = orc.stack_step(shape, embed, norm_f, lm_head, w64, tokens, pools, b.block_table,
                          b.seq_lens, b.q_lens, rows=rows)
     np.testing.assert_allclose(sub["logits"], full["logits"][rows], rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------------ layers only
+
+def test_layers_with_a_silent_layer_inside_equal_the_others_alone():
+    """A layer whose projection matrices are zero passes x through (h = x,
+    y = h), so inserting one changes nothing downstream."""
+    shape, b, _, _, _, _, layers, pools = _stack_inputs(3)
+    x = wl.make_x(shape, b.n_tokens, seed=5)
+    w64 = [orc.weights_f64(L) for L in layers]
+    zero = orc.weights_f64({k: (torch.zeros_like(v) if k.startswith("w_") else v)
+                            for k, v in layers[1].items()})
+    with_zero = orc.layers_step(shape, [w64[0], zero, w64[2]], x, pools, b.block_table,
+                                b.seq_lens, b.q_lens)
+    without = orc.layers_step(shape, [w64[0], w64[2]], x, [pools[0], pools[2]], b.block_table,
+                              b.seq_lens, b.q_lens)
+    np.testing.assert_allclose(with_zero["y"], without["y"], rtol=1e-12, atol=1e-12)
+
+
+def test_layers_rows_subset_equals_full():
+    """Rows of a prefill chunk need the earlier rows of the chunk in every
+    layer; the subset must still equal the full computation."""
+    shape, b, _, _, _, _, layers, pools = _stack_inputs(2)
+    x = wl.make_x(shape, b.n_tokens, seed=6)
+    w64 = [orc.weights_f64(L) for L in layers]
+    full = orc.layers_step(shape, w64, x, pools, b.block_table, b.seq_lens, b.q_lens)
+    rows = [0, 3, 10, 35]
+    sub = orc.layers_step(shape, w64, x, pools, b.block_table, b.seq_lens, b.q_lens, rows=rows)
+    np.testing.assert_allclose(sub["y"], full["y"][rows], rtol=1e-12, atol=1e-12)
