@@ -47,6 +47,8 @@ class Shape:
     rms_eps: float = 1e-5
     rope_theta: float = 1e4
     page_size: int = 16
+    n_experts: int = 0    # 0: dense SwiGLU FFN; else a mixture of that many SwiGLU experts
+    top_k: int = 2        # experts per token when n_experts > 0
 
     @property
     def qkv_rows(self) -> int:
@@ -161,6 +163,33 @@ def llama70b_batch(n_decode: int = 3584, prefill: int = 512) -> Batch:
                       seed_bt=2, slack=0.01, max_pages=4096 // 16, name="llama70b")
 
 
+def mixtral_shape() -> Shape:
+    """Mixtral-8x7B-shaped layer: Llama-3-8B-like attention, 8 SwiGLU experts of
+    FFN 14336, top-2 routing, RoPE theta 1e6."""
+    return Shape(hidden=4096, n_q=32, n_kv=8, head_dim=128, ffn=14336,
+                 rms_eps=1e-5, rope_theta=1e6, page_size=16, n_experts=8, top_k=2)
+
+
+def tiny_moe_shape() -> Shape:
+    """The small config's attention with 4 SwiGLU experts of FFN 688, top-2."""
+    return Shape(hidden=256, n_q=4, n_kv=2, head_dim=64, ffn=688, rms_eps=1e-5,
+                 rope_theta=1e4, page_size=16, n_experts=4, top_k=2)
+
+
+def moe_batch(n_decode: int = 1920, prefill: int = 128) -> Batch:
+    """1920 decode requests (lognormal median 600, sigma 1, clip [1, 8192]) and
+    one 128-token prefill chunk; 16-token pages, 1% slack."""
+    ctx = lognormal_contexts(n_decode, 600.0, 1.0, 1, 8192, seed=1)
+    return make_batch(mixtral_shape(), ctx, [prefill] if prefill else [], None,
+                      seed_bt=2, slack=0.01, max_pages=8192 // 16, name="mixtral")
+
+
+def make_router_logits(n_tokens: int, n_experts: int, seed: int = 4) -> torch.Tensor:
+    """Router logits N(0, 1) per token and expert, float32 (CPU)."""
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(n_tokens, n_experts, generator=g, dtype=torch.float32)
+
+
 # --------------------------------------------------------------------------
 # weights and activations
 
@@ -196,6 +225,22 @@ def make_weights(shape: Shape, seed: int = 0, gain_std: float = 0.0,
     else:
         w["norm1"] = torch.ones(H, dtype=BF16)
         w["norm2"] = torch.ones(H, dtype=BF16)
+    return w
+
+
+def make_moe_weights(shape: Shape, seed: int = 0, gain_std: float = 0.0,
+                     std: float = 0.02) -> dict:
+    """Attention weights as make_weights, and the experts in place of the dense
+    FFN: w_experts_gate_up [E, 2F, H] (gate rows, then up rows, per expert) and
+    w_experts_down [E, H, F], N(0, std), bf16 (CPU)."""
+    w = make_weights(Shape(shape.hidden, shape.n_q, shape.n_kv, shape.head_dim, 16,
+                           shape.rms_eps, shape.rope_theta, shape.page_size),
+                     seed=seed, gain_std=gain_std, std=std)
+    del w["w_gate_up"], w["w_down"]
+    g = torch.Generator().manual_seed(seed + 2000)
+    E, H, F = shape.n_experts, shape.hidden, shape.ffn
+    w["w_experts_gate_up"] = (torch.randn(E, 2 * F, H, generator=g) * std).to(BF16)
+    w["w_experts_down"] = (torch.randn(E, H, F, generator=g) * std).to(BF16)
     return w
 
 

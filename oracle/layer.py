@@ -25,6 +25,11 @@ reason in the design notes):
 * ``seq_lens`` is the KV length after this step's tokens are appended.
 * GQA: query head h reads KV head h // (n_q / n_kv) (contiguous groups).
 * softmax scale 1/sqrt(d); masked positions are excluded, not -inf-added.
+* mixture-of-experts FFN (the Mixtral-shaped config): router logits are an
+  input of the step; each token takes its top-k experts (ties to the lower
+  index) weighted by a softmax over the selected logits, and the FFN output is
+  the weighted sum of those experts' SwiGLU FFNs.  The pages name only "gate
+  routing" and grouped GEMMs over experts.
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 (closed forms, invariants, brute force and printed values); none is unpinned.
@@ -45,9 +50,29 @@ def f64(t) -> np.ndarray:
     return np.asarray(t, dtype=np.float64)
 
 
+class _LazyExperts:
+    """Per-expert float64 view of a stacked [E, rows, cols] bf16 tensor,
+    converted one expert at a time on first use (the Mixtral-shaped experts
+    hold 1.4 G parameters; a sampled-row check touches a few of them)."""
+
+    def __init__(self, t):
+        self.t = t
+        self.cache = {}
+
+    def __len__(self):
+        return self.t.shape[0]
+
+    def __getitem__(self, e):
+        e = int(e)
+        if e not in self.cache:
+            self.cache[e] = f64(self.t[e])
+        return self.cache[e]
+
+
 def weights_f64(w: dict) -> dict:
-    """Convert a weight dict (bf16 tensors) to float64 arrays once."""
-    return {k: f64(v) for k, v in w.items()}
+    """Convert a weight dict (bf16 tensors) to float64 arrays once (expert
+    stacks lazily, expert by expert)."""
+    return {k: (_LazyExperts(v) if k.startswith("w_experts") else f64(v)) for k, v in w.items()}
 
 
 # --------------------------------------------------------------------------
@@ -155,6 +180,57 @@ def split_kv_items(ctx_len: np.ndarray, chunk: int, row_begin: int = 0, row_end:
 # --------------------------------------------------------------------------
 # the layer step
 
+def route(logits, top_k: int):
+    """Top-k gate routing of a mixture-of-experts FFN ("NanoFlow: Towards
+    Optimal LLM Serving Throughput", MoE models: gate routing, then experts
+    computing on different tokens).  Reading taken: per token the top_k
+    experts by router logit, ties going to the lower expert index, weighted by
+    a softmax over the selected logits.  logits [T, E]; returns (experts
+    [T, top_k] int64, weights [T, top_k] float64), best first."""
+    r = np.asarray(logits, np.float64)
+    T, E = r.shape
+    experts = np.zeros((T, top_k), np.int64)
+    weights = np.zeros((T, top_k))
+    for t in range(T):
+        order = sorted(range(E), key=lambda e: (-r[t, e], e))
+        sel = order[:top_k]
+        z = np.exp(r[t, sel] - r[t, sel].max())
+        experts[t] = sel
+        weights[t] = z / z.sum()
+    return experts, weights
+
+
+def expert_groups(experts, n_experts: int):
+    """The grouped order of the (token, choice) pairs that the expert GEMMs
+    consume: expert by expert, and within an expert by increasing token.
+    Returns (pairs [T*k, 2] of (token, choice), offsets [n_experts + 1])."""
+    experts = np.asarray(experts)
+    pairs, offsets = [], [0]
+    for e in range(n_experts):
+        for t in range(experts.shape[0]):
+            for j in range(experts.shape[1]):
+                if experts[t, j] == e:
+                    pairs.append((t, j))
+        offsets.append(len(pairs))
+    return np.asarray(pairs, np.int64).reshape(-1, 2), np.asarray(offsets, np.int64)
+
+
+def moe_ffn(n2, w64: dict, logits, top_k: int, F: int):
+    """sum over the token's selected experts e of weight_e * FFN_e(n2), with
+    FFN_e(z) = (silu(z W_g,e^T) * (z W_u,e^T)) W_d,e^T; w64["w_experts_gate_up"][e]
+    holds the gate rows then the up rows of expert e, w64["w_experts_down"][e]
+    its down matrix.  n2 [R, H], logits [R, E] for the same rows."""
+    experts, weights = route(logits, top_k)
+    out = np.zeros_like(n2)
+    for i in range(n2.shape[0]):
+        for j in range(top_k):
+            e = int(experts[i, j])
+            gu = w64["w_experts_gate_up"][e]
+            a = silu(n2[i] @ gu[:F].T) * (n2[i] @ gu[F:].T)
+            out[i] += weights[i, j] * (a @ w64["w_experts_down"][e].T)
+    return out
+
+
 def _needed_rows(seq, rows):
     """rows plus every earlier token of the same sequence in this step: a
     prefill row attends to the K/V this step appends for earlier rows of its
@@ -172,7 +248,7 @@ def _needed_rows(seq, rows):
 
 
 def layer_step(shape, w64: dict, x, k_pool, v_pool, block_table, seq_lens, q_lens,
-               rows=None, keep=False) -> dict:
+               rows=None, keep=False, router_logits=None) -> dict:
     """One decoder-layer step over a mixed prefill+decode batch.
 
     shape: a Shape (hidden, n_q, n_kv, head_dim, ffn, rms_eps, rope_theta,
@@ -194,6 +270,9 @@ def layer_step(shape, w64: dict, x, k_pool, v_pool, block_table, seq_lens, q_len
       o = GQA softmax attention over positions 0..pos of the token's sequence;
       h = x + o W_o^T; n2 = RMSNorm(h; g2); a = silu(n2 W_g^T) * (n2 W_u^T);
       y = h + a W_d^T.
+    A mixture-of-experts layer (shape.n_experts > 0, weights w_experts_gate_up
+    and w_experts_down) replaces the last two lines by y = h + moe_ffn(n2)
+    with router_logits [T, n_experts] given for the step.
     """
     H, nq, nkv, d, F = shape.hidden, shape.n_q, shape.n_kv, shape.head_dim, shape.ffn
     P = shape.page_size
@@ -248,10 +327,15 @@ def layer_step(shape, w64: dict, x, k_pool, v_pool, block_table, seq_lens, q_len
     xr = np.stack([xrow[t] for t in rows.tolist()])
     h = xr + o.reshape(len(rows), nq * d) @ w64["w_o"].T
     n2 = rmsnorm(h, w64["norm2"], shape.rms_eps)
-    gate = n2 @ w64["w_gate_up"][:F].T
-    up = n2 @ w64["w_gate_up"][F:].T
-    a = silu(gate) * up
-    y = h + a @ w64["w_down"].T
+    if getattr(shape, "n_experts", 0):
+        lg = np.asarray(router_logits, np.float64)[rows]
+        a = None
+        y = h + moe_ffn(n2, w64, lg, shape.top_k, F)
+    else:
+        gate = n2 @ w64["w_gate_up"][:F].T
+        up = n2 @ w64["w_gate_up"][F:].T
+        a = silu(gate) * up
+        y = h + a @ w64["w_down"].T
 
     out = {
         "rows": rows,

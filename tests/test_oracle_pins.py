@@ -434,3 +434,84 @@ def test_layers_rows_subset_equals_full():
     rows = [0, 3, 10, 35]
     sub = orc.layers_step(shape, w64, x, pools, b.block_table, b.seq_lens, b.q_lens, rows=rows)
     np.testing.assert_allclose(sub["y"], full["y"][rows], rtol=1e-12, atol=1e-12)
+
+
+# --------------------------------------------------------------- MoE (routing)
+
+def test_route_picks_the_largest_logits_with_ties_to_the_lower_index():
+    rng = np.random.default_rng(3)
+    logits = rng.integers(-3, 4, size=(64, 8)).astype(np.float64)   # many ties
+    experts, weights = orc.route(logits, 2)
+    for t in range(64):
+        e0, e1 = experts[t]
+        assert e0 != e1
+        # brute force over all ordered pairs: the chosen pair is the
+        # lexicographically best (higher logit first, then lower index)
+        best = min(((a, b) for a in range(8) for b in range(8) if a != b),
+                   key=lambda ab: (-logits[t, ab[0]], ab[0], -logits[t, ab[1]], ab[1]))
+        assert (e0, e1) == best
+        # softmax over two logits: w0 = 1 / (1 + exp(r1 - r0))
+        w0 = 1.0 / (1.0 + np.exp(logits[t, e1] - logits[t, e0]))
+        np.testing.assert_allclose(weights[t], [w0, 1.0 - w0], rtol=1e-14, atol=1e-15)
+
+
+def test_expert_groups_cover_every_choice_once_in_token_order():
+    rng = np.random.default_rng(4)
+    experts, _ = orc.route(rng.standard_normal((50, 6)), 2)
+    pairs, offs = orc.expert_groups(experts, 6)
+    assert offs[0] == 0 and offs[-1] == 100 and len(pairs) == 100
+    assert sorted(map(tuple, pairs.tolist())) == [(t, j) for t in range(50) for j in range(2)]
+    for e in range(6):
+        grp = pairs[offs[e]:offs[e + 1]]
+        assert all(experts[t, j] == e for t, j in grp)
+        assert list(grp[:, 0]) == sorted(grp[:, 0])          # tokens increase
+
+
+def _moe_dense_pair(E=4, top_k=2):
+    shape = wl.tiny_moe_shape()
+    dense = wl.make_weights(wl.tiny_shape(), seed=5)
+    w = {k: v for k, v in dense.items() if k not in ("w_gate_up", "w_down")}
+    w["w_experts_gate_up"] = dense["w_gate_up"][None].repeat(E, 1, 1)
+    w["w_experts_down"] = dense["w_down"][None].repeat(E, 1, 1)
+    return shape, dense, w
+
+
+def test_moe_with_identical_experts_is_the_dense_ffn():
+    """The routing weights of a token sum to 1, so identical experts give the
+    dense SwiGLU FFN whatever the routing."""
+    shape, dense, w = _moe_dense_pair()
+    d64, m64 = orc.weights_f64(dense), orc.weights_f64(w)
+    rng = np.random.default_rng(6)
+    n2 = rng.standard_normal((9, shape.hidden))
+    logits = rng.standard_normal((9, shape.n_experts))
+    F = shape.ffn
+    ref = (orc.silu(n2 @ d64["w_gate_up"][:F].T) * (n2 @ d64["w_gate_up"][F:].T)) @ d64["w_down"].T
+    np.testing.assert_allclose(orc.moe_ffn(n2, m64, logits, 2, F), ref, rtol=1e-12, atol=1e-12)
+
+
+def test_moe_top1_is_the_argmax_experts_ffn():
+    shape = wl.tiny_moe_shape()
+    w = orc.weights_f64(wl.make_moe_weights(shape, seed=7))
+    rng = np.random.default_rng(8)
+    n2 = rng.standard_normal((5, shape.hidden))
+    logits = rng.standard_normal((5, shape.n_experts))
+    F = shape.ffn
+    got = orc.moe_ffn(n2, w, logits, 1, F)
+    for i in range(5):
+        e = int(np.argmax(logits[i]))
+        gu, dn = w["w_experts_gate_up"][e], w["w_experts_down"][e]
+        ref = (orc.silu(n2[i] @ gu[:F].T) * (n2[i] @ gu[F:].T)) @ dn.T
+        np.testing.assert_allclose(got[i], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_moe_layer_with_identical_experts_equals_the_dense_layer():
+    shape, dense, w = _moe_dense_pair()
+    b = wl.tiny_batch()
+    kp, vp = wl.make_pools(wl.tiny_shape(), b, "cpu", seed=9)
+    x = wl.make_x(shape, b.n_tokens, seed=10)
+    logits = wl.make_router_logits(b.n_tokens, shape.n_experts, seed=11)
+    moe = orc.layer_step(shape, orc.weights_f64(w), x, kp, vp, b.block_table, b.seq_lens,
+                         b.q_lens, router_logits=logits.numpy())
+    den = orc.layer_step(wl.tiny_shape(), orc.weights_f64(dense), x, kp, vp, b.block_table,
+                         b.seq_lens, b.q_lens)
+    np.testing.assert_allclose(moe["y"], den["y"], rtol=1e-12, atol=1e-12)
