@@ -57,10 +57,11 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-ablation", action="store_true")
     ap.add_argument("--plan", default="auto", help="auto | search | n=<k>,sms=<s>")
-    ap.add_argument("--workload", default="layer", choices=["layer", "stack", "70b"],
+    ap.add_argument("--workload", default="layer", choices=["layer", "stack", "70b", "moe"],
                     help="layer: the single 8B-shaped layer step (default); stack: the 32-layer "
                          "8B-shaped stack with embedding and LM head, decode batches; 70b: ten "
-                         "70B-shaped layers over a 4096-token mixed step")
+                         "70B-shaped layers over a 4096-token mixed step; moe: one Mixtral-shaped "
+                         "layer (8 experts, top-2) over a 2048-token mixed step")
     ap.add_argument("--batch", type=int, default=256, help="decode requests of the stack workload")
     return ap.parse_args()
 
@@ -394,6 +395,87 @@ def run_70b(args):
     plan.close()
 
 
+def run_moe(args):
+    """One Mixtral-shaped layer (8 SwiGLU experts of FFN 14336, top-2 routing
+    from N(0, 1) router logits) over a 2048-token mixed step: 1920 decode
+    requests (lognormal KV median 600, sigma 1, clip [1, 8192]) plus a 128-token
+    prefill chunk.  Plans: search, sequential and SM-split overlap candidates,
+    each timed; the fastest is reported."""
+    from nano_intra_device_gb300 import _lib
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    shape, batch = wl.mixtral_shape(), wl.moe_batch()
+    T, H, F, E = batch.n_tokens, shape.hidden, shape.ffn, shape.n_experts
+    g = torch.Generator(device=dev).manual_seed(0)
+
+    def rn(*sz, std=0.02):
+        return (torch.randn(*sz, generator=g, device=dev) * std).to(torch.bfloat16)
+    w = {"w_qkv": rn(shape.qkv_rows, H), "w_o": rn(H, shape.n_q * shape.head_dim),
+         "norm1": torch.ones(H, dtype=torch.bfloat16, device=dev),
+         "norm2": torch.ones(H, dtype=torch.bfloat16, device=dev),
+         "w_experts_gate_up": torch.cat([rn(1, 2 * F, H) for _ in range(E)]),
+         "w_experts_down": torch.cat([rn(1, H, F) for _ in range(E)]),
+         "router_logits": torch.randn(T, E, generator=g, device=dev)}
+    kp, vp = wl.make_pools(shape, batch, dev, seed=3)
+    x = torch.randn(T, H, generator=g, device=dev).to(torch.bfloat16)
+    y = torch.empty_like(x)
+    bt = torch.from_numpy(batch.block_table).to(dev)
+    sl = torch.from_numpy(batch.seq_lens).to(dev)
+    stream = torch.cuda.current_stream()
+    sms = _lib.device_sm_count()
+    cands = [("search", None), ("sequential", _lib.make_opts(T))]
+    for n in (2, 3):
+        ab = [0] + [int(round(T * i / n / 128)) * 128 for i in range(1, n)] + [T]
+        for a_sms in (sms * 6 // 16, sms * 8 // 16, sms * 10 // 16):
+            cands.append((f"n={n},attn_sms={a_sms}",
+                          _lib.make_opts(T, ab, ab, executor=_lib.NF_EXEC_STREAMS, attn_sms=a_sms)))
+    tried, plans = {}, {}
+    for name, o in cands:
+        plan = _lib.Plan(shape, batch, o)
+        tried[name] = time_steps(lambda: _lib.layer_step(plan, w, x, kp, vp, bt, sl, y), 5, 2, 1,
+                                 stream)
+        plan.poll()
+        plans[name] = plan
+    best = min(tried, key=tried.get)
+    plan = plans.pop(best)
+    for p in plans.values():
+        p.close()
+    clocks = Clocks()
+    for _ in range(args.warmup):
+        _lib.layer_step(plan, w, x, kp, vp, bt, sl, y)
+    torch.cuda.synchronize()
+    plan.trace_enable(args.steps)
+    clocks.start()
+    ms = time_steps(lambda: _lib.layer_step(plan, w, x, kp, vp, bt, sl, y), args.steps, 0, 1, stream)
+    clk = clocks.stop()
+    plan.poll()
+    trace = plan.trace_read()
+    plan.trace_enable(0)
+    ops = {}
+    for e in trace:
+        ops.setdefault(f"{e['op']}{e['nano']}", []).append(e["ms"])
+    pk = peaks()
+    work = cm.step_work(shape, batch.seq_lens, batch.q_lens)
+    rf = cm.roofline_time(work, pk["bf16_tflops_sustained"] * 1e12, pk["hbm_gbs"] * 1e9)
+    line = {"metric": "tokens/s per GB300 for a Mixtral-shaped MoE layer step; % of layer roofline",
+            "value": T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16",
+            "data": "synthetic", "clocks": clk,
+            "config": {"workload": "mixtral-8x7b-shaped layer (8 experts x FFN 14336, top-2 from "
+                                   "N(0,1) router logits), 2048-token step: 1920 decode (lognormal "
+                                   "KV median 600, sigma 1, clip [1,8192]) + one 128-token prefill "
+                                   "chunk, 16-token pages",
+                       "kv_read_gb_per_step": work["kv_read_bytes"] / 1e9,
+                       "plan": dict(_lib.opts_dict(plan.info()[0]), chosen=best)},
+            "layer_roofline": {"frac": rf["t_roof"] / (ms * 1e-3), "t_roof_ms": rf["t_roof"] * 1e3,
+                               "t_flop_ms": rf["t_flop"] * 1e3, "t_byte_ms": rf["t_byte"] * 1e3,
+                               "bound": rf["bound"], "flops": work["flops"], "bytes": work["bytes"]},
+            "ops_ms": {k: round(float(np.mean(v)), 4) for k, v in ops.items()},
+            "candidates_ms": {k: round(v, 3) for k, v in tried.items()}}
+    print(json.dumps(line), flush=True)
+    plan.close()
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -402,6 +484,8 @@ def main():
         return run_stack(args)
     if args.workload == "70b":
         return run_70b(args)
+    if args.workload == "moe":
+        return run_moe(args)
     from nano_intra_device_gb300 import _lib
 
     rank, world, local = dist_setup(args.gpus)

@@ -69,7 +69,11 @@ typedef enum {
 
 /* Shape of one Llama-style decoder layer.  head_dim in {64, 128};
  * n_q_heads a multiple of n_kv_heads with n_q/n_kv in {1, 2, 4, 8};
- * hidden and ffn multiples of 16; page_size = 16. */
+ * hidden and ffn multiples of 16; page_size = 16.
+ * n_experts = 0: dense SwiGLU FFN.  n_experts in [1, 64]: a mixture of that
+ * many SwiGLU experts of width ffn, each token routed to top_k (1 or 2) of them
+ * ("NanoFlow: Towards Optimal LLM Serving Throughput", MoE models: gate
+ * routing and a grouped GEMM in which experts compute on different tokens). */
 typedef struct {
   int32_t hidden;
   int32_t n_q_heads;
@@ -79,6 +83,8 @@ typedef struct {
   int32_t page_size;
   float rms_eps;
   float rope_theta;
+  int32_t n_experts;
+  int32_t top_k;
 } nf_model_shape;
 
 /* Structure of the mixed batch a plan serves ("NanoFlow: Towards Optimal LLM
@@ -141,8 +147,16 @@ typedef struct {
   const void* w_qkv;
   const void* w_o;
   const void* norm2;
-  const void* w_gate_up;
-  const void* w_down;
+  const void* w_gate_up;   /* dense FFN (n_experts = 0); NULL for a MoE layer */
+  const void* w_down;      /* dense FFN; NULL for a MoE layer */
+  /* Mixture of experts (n_experts > 0), device:
+   * w_experts_gate_up [E, 2F, H] bf16 (per expert its gate rows, then its up rows),
+   * w_experts_down [E, H, F] bf16, router_logits [T, E] fp32: this step's router
+   * logits, one row per token.  Routing: the top_k logits of a token, ties to
+   * the lower expert index, weighted by a softmax over the selected logits. */
+  const void* w_experts_gate_up;
+  const void* w_experts_down;
+  const void* router_logits;
 } nf_layer_weights;
 
 /* Create a plan for one model shape and batch structure
@@ -335,7 +349,13 @@ typedef enum {
   NF_BUF_O = 7,         /* bf16 [T, n_q * head_dim] */
   NF_BUF_H = 8,         /* bf16 [T, H] */
   NF_BUF_N2 = 9,        /* bf16 [T, H] */
-  NF_BUF_A = 10         /* bf16 [T, F] */
+  NF_BUF_A = 10,        /* bf16 [T, F] */
+  /* mixture of experts, for the last FFN nano-batch of the last step (rows
+   * of the grouped order are counted from that nano-batch's first token): */
+  NF_BUF_MOE_OFF = 11,      /* int32 [E + 1]: first grouped row of each expert */
+  NF_BUF_MOE_PERM = 12,     /* int32 [T * top_k]: token of each grouped row */
+  NF_BUF_MOE_PAIR_ROW = 13, /* int32 [T * top_k]: grouped row of pair (token, choice) */
+  NF_BUF_MOE_PAIR_W = 14    /* fp32 [T * top_k]: routing weight of pair (token, choice) */
 } nf_buffer;
 nf_status nf_plan_buffer_size(nf_plan plan, int32_t which, size_t* bytes);
 nf_status nf_plan_copy_buffer(nf_plan plan, int32_t which, void* dst, size_t bytes);

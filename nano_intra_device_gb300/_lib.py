@@ -22,13 +22,15 @@ NF_EXEC_SEQUENTIAL, NF_EXEC_STREAMS = 0, 1
 NF_ATTN_AUTO, NF_ATTN_FMA, NF_ATTN_MMA = 0, 1, 2
 NF_EPI_STORE, NF_EPI_RESID, NF_EPI_SWIGLU = 0, 1, 2
 (NF_BUF_TOK_SEQ, NF_BUF_TOK_POS, NF_BUF_TOK_SLOT, NF_BUF_ITEMS, NF_BUF_ITEM_SEG, NF_BUF_N1,
- NF_BUF_Q, NF_BUF_O, NF_BUF_H, NF_BUF_N2, NF_BUF_A) = range(11)
+ NF_BUF_Q, NF_BUF_O, NF_BUF_H, NF_BUF_N2, NF_BUF_A, NF_BUF_MOE_OFF, NF_BUF_MOE_PERM,
+ NF_BUF_MOE_PAIR_ROW, NF_BUF_MOE_PAIR_W) = range(15)
 
 
 class nf_model_shape(Structure):
     _fields_ = [("hidden", c_int32), ("n_q_heads", c_int32), ("n_kv_heads", c_int32),
                 ("head_dim", c_int32), ("ffn", c_int32), ("page_size", c_int32),
-                ("rms_eps", c_float), ("rope_theta", c_float)]
+                ("rms_eps", c_float), ("rope_theta", c_float), ("n_experts", c_int32),
+                ("top_k", c_int32)]
 
 
 class nf_batch_desc(Structure):
@@ -55,7 +57,8 @@ NF_OP_NAMES = {0: "meta", 1: "qkv", 2: "attn", 3: "oproj", 4: "ffn"}
 
 
 class nf_layer_weights(Structure):
-    _fields_ = [(n, c_void_p) for n in ("norm1", "w_qkv", "w_o", "norm2", "w_gate_up", "w_down")]
+    _fields_ = [(n, c_void_p) for n in ("norm1", "w_qkv", "w_o", "norm2", "w_gate_up", "w_down",
+                                        "w_experts_gate_up", "w_experts_down", "router_logits")]
 
 
 class nf_stack_weights(Structure):
@@ -138,7 +141,8 @@ def stream_handle(stream=None):
 
 def make_shape(shape) -> nf_model_shape:
     return nf_model_shape(shape.hidden, shape.n_q, shape.n_kv, shape.head_dim, shape.ffn,
-                          shape.page_size, shape.rms_eps, shape.rope_theta)
+                          shape.page_size, shape.rms_eps, shape.rope_theta,
+                          getattr(shape, "n_experts", 0), getattr(shape, "top_k", 0))
 
 
 def make_batch_desc(batch, hint=True):
@@ -182,8 +186,11 @@ def opts_dict(o: nf_plan_opts) -> dict:
 
 
 def make_weights_struct(w: dict) -> nf_layer_weights:
-    return nf_layer_weights(*[w[k].data_ptr() for k in
-                              ("norm1", "w_qkv", "w_o", "norm2", "w_gate_up", "w_down")])
+    """Device pointers of a layer's weights (a MoE layer has w_experts_gate_up,
+    w_experts_down and this step's router_logits instead of w_gate_up/w_down)."""
+    return nf_layer_weights(*[(w[k].data_ptr() if k in w else None) for k in
+                              ("norm1", "w_qkv", "w_o", "norm2", "w_gate_up", "w_down",
+                               "w_experts_gate_up", "w_experts_down", "router_logits")])
 
 
 class Plan:

@@ -8,10 +8,11 @@ throughput Compute / (2 * P_model).  This module states the same quantities
 for ONE decoder-layer step over a concrete mixed batch, counting what the step
 must move at least once:
 
-* FLOPs: 2 * T * P_layer for the projections and FFN, plus the attention
-  products (2 FLOPs per multiply-add, QK^T and PV, per query head and visible
-  position);
-* bytes: bf16 weights once, the KV each sequence reads (its whole visible
+* FLOPs: 2 * T * P_layer for the projections and FFN (for a mixture of
+  experts, top_k experts per token), plus the attention products (2 FLOPs per
+  multiply-add, QK^T and PV, per query head and visible position);
+* bytes: bf16 weights once (every expert of a mixture: a step of thousands of
+  tokens hits them all), the KV each sequence reads (its whole visible
   history, including this step's tokens), the K/V appended, x in and y out.
 
 Nano-batch weight re-reads are not counted: they are the cost of the method,
@@ -57,9 +58,19 @@ def effective_intensity(batch: float, params: float, kv_bytes_per_seq: float) ->
 
 
 def layer_params(shape) -> int:
-    """Weights of one layer's projections and FFN (norm gains excluded)."""
+    """Weights of one layer's projections and FFN (norm gains excluded); a
+    mixture-of-experts layer counts every expert."""
     H, d, F = shape.hidden, shape.head_dim, shape.ffn
-    return H * (shape.n_q + 2 * shape.n_kv) * d + shape.n_q * d * H + 3 * H * F
+    experts = max(1, getattr(shape, "n_experts", 0))
+    return H * (shape.n_q + 2 * shape.n_kv) * d + shape.n_q * d * H + experts * 3 * H * F
+
+
+def active_params(shape) -> int:
+    """Weights one token multiplies: the projections and, for a mixture of
+    experts, top_k experts' FFNs."""
+    H, d, F = shape.hidden, shape.head_dim, shape.ffn
+    k = getattr(shape, "top_k", 1) if getattr(shape, "n_experts", 0) else 1
+    return H * (shape.n_q + 2 * shape.n_kv) * d + shape.n_q * d * H + k * 3 * H * F
 
 
 def step_work(shape, seq_lens, q_lens, elem_bytes: int = 2) -> dict:
@@ -74,7 +85,7 @@ def step_work(shape, seq_lens, q_lens, elem_bytes: int = 2) -> dict:
     for L, q in zip(seq_lens.tolist(), q_lens.tolist()):
         first = L - q + 1
         vis += (first + L) * q // 2 if q > 0 else 0
-    gemm_flops = 2 * T * P
+    gemm_flops = 2 * T * active_params(shape)
     attn_flops = 4 * nq * d * vis
     kv_tok = 2 * nkv * d * elem_bytes
     bytes_w = P * elem_bytes

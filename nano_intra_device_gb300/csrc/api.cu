@@ -132,9 +132,14 @@ struct nf_plan_s {
   CUtensorMap tm_wqkv{}, tm_wo{}, tm_wg{}, tm_wu{}, tm_wd{};
   struct WeightMaps {
     const void* key[4];
-    CUtensorMap qkv, o, g, u, d;
+    CUtensorMap qkv, o, g, u, d;  // a MoE layer keeps its expert maps in g (gate/up) and d
   };
   std::vector<WeightMaps> wcache;
+  // mixture of experts: routing, grouped rows and the expert weight maps
+  int *moe_off = nullptr, *moe_perm = nullptr, *moe_pair_row = nullptr;
+  float *moe_pair_w = nullptr, *moe_out = nullptr;
+  __nv_bfloat16 *moe_a = nullptr, *moe_act = nullptr;
+  CUtensorMap tm_moe_a{}, tm_moe_act{}, tm_egu{}, tm_edn{};
   // attention: which kernel, and TMA maps over every (K pool, V pool) pair seen
   bool attn_mma = false;
   struct PoolMaps {
@@ -179,6 +184,10 @@ size_t buf_bytes(nf_plan p, int which) {
     case NF_BUF_Q:
     case NF_BUF_O: return T * QD * 2;
     case NF_BUF_A: return T * (size_t)p->shape.ffn * 2;
+    case NF_BUF_MOE_OFF: return p->moe_off ? (size_t)(p->shape.n_experts + 1) * 4 : 0;
+    case NF_BUF_MOE_PERM:
+    case NF_BUF_MOE_PAIR_ROW:
+    case NF_BUF_MOE_PAIR_W: return p->moe_off ? T * p->shape.top_k * 4 : 0;
     default: return 0;
   }
 }
@@ -196,6 +205,10 @@ const void* buf_ptr(nf_plan p, int which) {
     case NF_BUF_H: return p->h;
     case NF_BUF_N2: return p->n2;
     case NF_BUF_A: return p->a;
+    case NF_BUF_MOE_OFF: return p->moe_off;
+    case NF_BUF_MOE_PERM: return p->moe_perm;
+    case NF_BUF_MOE_PAIR_ROW: return p->moe_pair_row;
+    case NF_BUF_MOE_PAIR_W: return p->moe_pair_w;
     default: return nullptr;
   }
 }
@@ -216,6 +229,12 @@ nf_status check_shape(const nf_model_shape* s) {
   if (s->page_size != 16) return fail(NF_ERR_INVALID_ARG, "page_size must be 16 (got %d)", s->page_size);
   if (!(s->rms_eps >= 0.f) || !(s->rope_theta > 0.f))
     return fail(NF_ERR_INVALID_ARG, "rms_eps must be >= 0 and rope_theta > 0");
+  if (s->n_experts < 0 || s->n_experts > nf::GEMM_MAX_GROUPS)
+    return fail(NF_ERR_INVALID_ARG, "n_experts must be in [0, %d] (got %d)", nf::GEMM_MAX_GROUPS,
+                s->n_experts);
+  if (s->n_experts > 0 && (s->top_k < 1 || s->top_k > 2 || s->top_k > s->n_experts))
+    return fail(NF_ERR_UNSUPPORTED, "top_k must be 1 or 2 and at most n_experts (got %d)",
+                s->top_k);
   return NF_OK;
 }
 
@@ -259,7 +278,8 @@ void free_plan(nf_plan p) {
                   p->tok_slot, p->tok_nchunks, p->items, p->seg_items, p->fetch, p->row_done,
                   p->partials, p->status, p->n1, p->q, p->o, p->h, p->n2, p->a, p->x_stage,
                   p->y_stage, p->bt_stage, p->sl_stage, p->xa, p->xb, p->gemm_part,
-                  p->gemm_cnt};
+                  p->gemm_cnt, p->moe_off, p->moe_perm, p->moe_pair_row, p->moe_pair_w,
+                  p->moe_a, p->moe_act, p->moe_out};
   for (void* b : bufs)
     if (b) cudaFree(b);
   for (cudaEvent_t e : p->ev) cudaEventDestroy(e);
@@ -319,6 +339,19 @@ nf_status alloc_plan(nf_plan p) {
   NF_TRY(dalloc(&p->h, T * H * 2));
   NF_TRY(dalloc(&p->n2, T * H * 2));
   NF_TRY(dalloc(&p->a, T * F * 2));
+  if (p->shape.n_experts > 0) {
+    const size_t R = T * p->shape.top_k;  // grouped rows: one per (token, choice)
+    NF_TRY(dalloc(&p->moe_off, (nf::GEMM_MAX_GROUPS + 1) * 4));
+    NF_TRY(dalloc(&p->moe_perm, R * 4));
+    NF_TRY(dalloc(&p->moe_pair_row, R * 4));
+    NF_TRY(dalloc(&p->moe_pair_w, R * 4));
+    NF_TRY(dalloc(&p->moe_a, R * H * 2));
+    NF_TRY(dalloc(&p->moe_act, R * F * 2));
+    NF_TRY(dalloc(&p->moe_out, R * H * 4));
+    if (!nf::make_tmap_bf16(&p->tm_moe_a, p->moe_a, R, H, 128) ||
+        !nf::make_tmap_bf16(&p->tm_moe_act, p->moe_act, R, F, 128))
+      return fail(NF_ERR_CUDA, "tensor map creation failed");
+  }
   NF_TRY(dalloc(&p->gemm_part, kSplitPartBytes));
   NF_TRY(dalloc(&p->gemm_cnt, kSplitMaxTiles * 4));
   NF_CUDA(cudaMemset(p->gemm_cnt, 0, kSplitMaxTiles * 4));
@@ -379,6 +412,10 @@ nf_status build_plan(const nf_model_shape* shape, const nf_batch_desc* batch,
     p->tok_begin.push_back(p->tok_begin.back() + q);
   }
   p->T = p->tok_begin.back();
+  if (shape->n_experts > 0 && (int64_t)p->T * shape->top_k > 16384) {
+    delete p;
+    return fail(NF_ERR_UNSUPPORTED, "a MoE step routes at most 16384 (token, expert) pairs");
+  }
   if (batch->seq_lens_hint) p->seq_hint.assign(batch->seq_lens_hint, batch->seq_lens_hint + p->n_seq);
 
   if (opts) {
@@ -433,7 +470,9 @@ nf_status build_plan(const nf_model_shape* shape, const nf_batch_desc* batch,
 }
 
 nf_status refresh_weight_maps(nf_plan p, const nf_layer_weights* w) {
-  const void* key[4] = {w->w_qkv, w->w_o, w->w_gate_up, w->w_down};
+  const bool moe = p->shape.n_experts > 0;
+  const void* key[4] = {w->w_qkv, w->w_o, moe ? w->w_experts_gate_up : w->w_gate_up,
+                        moe ? w->w_experts_down : w->w_down};
   if (std::memcmp(key, p->wkey, sizeof(key)) == 0) return NF_OK;
   for (const auto& c : p->wcache) {
     if (std::memcmp(key, c.key, sizeof(key)) == 0) {
@@ -449,13 +488,22 @@ nf_status refresh_weight_maps(nf_plan p, const nf_layer_weights* w) {
   const nf_model_shape& s = p->shape;
   const uint64_t H = s.hidden, F = s.ffn, QD = (uint64_t)s.n_q_heads * s.head_dim;
   const uint64_t NQKV = (uint64_t)(s.n_q_heads + 2 * s.n_kv_heads) * s.head_dim;
-  const char* up = static_cast<const char*>(w->w_gate_up) + F * H * 2;
   if (!nf::make_tmap_bf16(&p->tm_wqkv, w->w_qkv, NQKV, H, 256) ||
-      !nf::make_tmap_bf16(&p->tm_wo, w->w_o, H, QD, 256) ||
-      !nf::make_tmap_bf16(&p->tm_wg, w->w_gate_up, F, H, 128) ||
-      !nf::make_tmap_bf16(&p->tm_wu, up, F, H, 128) ||
-      !nf::make_tmap_bf16(&p->tm_wd, w->w_down, H, F, 256))
+      !nf::make_tmap_bf16(&p->tm_wo, w->w_o, H, QD, 256))
     return fail(NF_ERR_INVALID_ARG, "weight tensor maps: pointers must be 16-byte aligned");
+  if (moe) {  // one map over every expert's rows: [E * 2F, H] and [E * H, F]
+    const uint64_t E = p->shape.n_experts;
+    if (!nf::make_tmap_bf16(&p->tm_wg, w->w_experts_gate_up, E * 2 * F, H, 128) ||
+        !nf::make_tmap_bf16(&p->tm_wd, w->w_experts_down, E * H, F, 256))
+      return fail(NF_ERR_INVALID_ARG, "expert tensor maps: pointers must be 16-byte aligned");
+    p->tm_wu = p->tm_wg;
+  } else {
+    const char* up = static_cast<const char*>(w->w_gate_up) + F * H * 2;
+    if (!nf::make_tmap_bf16(&p->tm_wg, w->w_gate_up, F, H, 128) ||
+        !nf::make_tmap_bf16(&p->tm_wu, up, F, H, 128) ||
+        !nf::make_tmap_bf16(&p->tm_wd, w->w_down, H, F, 256))
+      return fail(NF_ERR_INVALID_ARG, "weight tensor maps: pointers must be 16-byte aligned");
+  }
   std::memcpy(p->wkey, key, sizeof(key));
   if (p->wcache.size() < 1024) {
     nf_plan_s::WeightMaps c;
@@ -655,12 +703,51 @@ nf_status run_oproj(nf_plan p, const void* x, int r0, int r1, int grid, cudaStre
   return NF_OK;
 }
 
+// Mixture-of-experts FFN of the tokens [r0, r1): route, gather n2 into the
+// expert-grouped order, grouped gate/up GEMM with SwiGLU, grouped down GEMM to
+// fp32 rows, and the weighted combine with the residual.
+nf_status run_moe_ffn(nf_plan p, const nf_layer_weights* w, void* y, int r0, int r1, int grid,
+                      cudaStream_t st) {
+  const nf_model_shape& s = p->shape;
+  const int n = r1 - r0, k = s.top_k, E = s.n_experts;
+  NF_CUDA(nf::launch_moe_route(static_cast<const float*>(w->router_logits), r0, n, E, k,
+                               p->moe_off, p->moe_perm, p->moe_pair_row, p->moe_pair_w, st));
+  NF_CUDA(nf::launch_gather_rows(p->n2, p->moe_perm, p->moe_a, n * k, s.hidden, st));
+  GemmArgs g = base_args(p);
+  g.N = s.ffn;
+  g.K = s.hidden;
+  g.n_tiles = (g.N + 127) / 128;
+  g.C = p->moe_act;
+  g.ldc = s.ffn;
+  g.group_off = p->moe_off;
+  g.n_groups = E;
+  g.b_group_rows = 2 * s.ffn;
+  g.b2_row_off = s.ffn;
+  g.splits = 1;
+  NF_CUDA(nf::launch_gemm(nf::EPI_SWIGLU, p->tm_moe_a, p->tm_wg, p->tm_wg, g, grid, st));
+  GemmArgs d = base_args(p);
+  d.N = s.hidden;
+  d.K = s.ffn;
+  d.n_tiles = (d.N + 255) / 256;
+  d.Cf = p->moe_out;
+  d.ldc = s.hidden;
+  d.group_off = p->moe_off;
+  d.n_groups = E;
+  d.b_group_rows = s.hidden;
+  d.splits = 1;
+  NF_CUDA(nf::launch_gemm(nf::EPI_STORE_F32, p->tm_moe_act, p->tm_wd, p->tm_wd, d, grid, st));
+  NF_CUDA(nf::launch_moe_combine(p->h, p->moe_out, p->moe_pair_row, p->moe_pair_w,
+                                 static_cast<__nv_bfloat16*>(y), r0, n, k, s.hidden, st));
+  return NF_OK;
+}
+
 nf_status run_ffn(nf_plan p, const nf_layer_weights* w, void* y, int r0, int r1, int grid,
                   cudaStream_t st, int nano = 0) {
   TraceScope ts_(p, st, NF_OP_FFN, nano);
   const nf_model_shape& s = p->shape;
   NF_CUDA(nf::launch_rmsnorm(p->h, static_cast<const __nv_bfloat16*>(w->norm2), p->n2, r0, r1,
                              s.hidden, s.rms_eps, st));
+  if (s.n_experts > 0) return run_moe_ffn(p, w, y, r0, r1, grid, st);
   GemmArgs g = base_args(p);
   g.m_begin = r0;
   g.m_end = r1;
@@ -695,11 +782,22 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 nf_status check_step_args(nf_plan p, const nf_layer_weights* w, const void* x, void* kp, void* vp,
                           const int32_t* bt, const int32_t* sl, void* y) {
   if (!p) return fail(NF_ERR_INVALID_ARG, "plan is NULL");
-  if (!w || !w->norm1 || !w->norm2 || !w->w_qkv || !w->w_o || !w->w_gate_up || !w->w_down)
+  if (!w || !w->norm1 || !w->norm2 || !w->w_qkv || !w->w_o)
     return fail(NF_ERR_INVALID_ARG, "a weight pointer is NULL");
+  if (p->shape.n_experts > 0) {
+    if (!w->w_experts_gate_up || !w->w_experts_down || !w->router_logits)
+      return fail(NF_ERR_INVALID_ARG, "a MoE layer needs expert weights and router logits");
+    if (!aligned16(w->w_experts_gate_up) || !aligned16(w->w_experts_down))
+      return fail(NF_ERR_INVALID_ARG, "expert weights must be 16-byte aligned");
+  } else if (!w->w_gate_up || !w->w_down) {
+    return fail(NF_ERR_INVALID_ARG, "a weight pointer is NULL");
+  }
   if (!x || !y || !kp || !vp || !bt || !sl) return fail(NF_ERR_INVALID_ARG, "a pointer is NULL");
   if (x == y) return fail(NF_ERR_INVALID_ARG, "x and y must not alias");
-  const void* ptrs[] = {x, y, kp, vp, w->norm1, w->norm2, w->w_qkv, w->w_o, w->w_gate_up, w->w_down};
+  const bool moe = p->shape.n_experts > 0;
+  const void* ptrs[] = {x, y, kp, vp, w->norm1, w->norm2, w->w_qkv, w->w_o,
+                        moe ? w->w_experts_gate_up : w->w_gate_up,
+                        moe ? w->w_experts_down : w->w_down};
   for (const void* q : ptrs)
     if (!aligned16(q)) return fail(NF_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
   return NF_OK;

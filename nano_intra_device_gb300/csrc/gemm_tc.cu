@@ -27,7 +27,7 @@ constexpr int GEMM_THREADS = 192;
 // Dynamic shared memory of a CTA with `stages` ring stages: the ring, slack to
 // align it to 1024 bytes, and the barrier block.  4 stages fill an SM (one CTA
 // per SM, exclusive); 3 or 2 leave room for an attention CTA beside it.
-constexpr int gemm_smem_bytes(int stages) { return stages * STAGE_BYTES + 1024 + 256; }
+constexpr int gemm_smem_bytes(int stages) { return stages * STAGE_BYTES + 1024 + 640; }
 constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
 
 struct GemmSmemTail {
@@ -40,6 +40,14 @@ struct GemmSmemTail {
   uint32_t tmem_base;
   int abort;
   int last;            // this CTA finishes the tile's last split (split-K)
+  int gpre[GEMM_MAX_GROUPS + 1];  // grouped GEMM: first tile of each group
+};
+static_assert(sizeof(GemmSmemTail) <= 640, "barrier block exceeds its reservation");
+
+// One output tile: A rows [m0, m0 + BM) (rows >= m_lim are not stored), B rows
+// from brow + tn * (columns per tile), split sp of the K range.
+struct GemmTile {
+  int t, sp, m0, m_lim, tn, brow;
 };
 
 __device__ __forceinline__ void store32_bf16(__nv_bfloat16* dst, const float* v) {
@@ -98,8 +106,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   const int lane = threadIdx.x & 31;
   // Work units: (output tile, K split).  The splits of one tile are adjacent
   // unit numbers, so they run on different CTAs at the same time.
-  const int splits = args.splits > 1 ? args.splits : 1;
-  const int total_tiles = args.m_tiles * args.n_tiles * splits;
+  const int splits = args.splits > 1 && args.n_groups == 0 ? args.splits : 1;
   const int nk = (args.K + BK - 1) / BK;
   const uint64_t tmo = args.timeout_ns;
 
@@ -115,6 +122,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     mbar_init(&tail->drain, 1);
     mbar_init(&tail->epi_sync, 4);
     tail->abort = 0;
+    if (args.n_groups > 0) {  // tiles per group from the device-side row offsets
+      int acc = 0;
+      for (int e = 0; e < args.n_groups; ++e) {
+        tail->gpre[e] = acc;
+        const int rows = args.group_off[e + 1] - args.group_off[e];
+        acc += rows > 0 ? ((rows + BM - 1) / BM) * args.n_tiles : 0;
+      }
+      tail->gpre[args.n_groups] = acc;
+    }
     fence_mbar_init();
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmB);
@@ -129,6 +145,32 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = tail->tmem_base;
   volatile int* abort_flag = &tail->abort;
+  const int total_tiles =
+      args.n_groups > 0 ? tail->gpre[args.n_groups] : args.m_tiles * args.n_tiles * splits;
+  auto decode = [&](int u) {
+    GemmTile x;
+    if (args.n_groups > 0) {
+      int e = 0;
+      while (e + 1 < args.n_groups && tail->gpre[e + 1] <= u) ++e;
+      const int local = u - tail->gpre[e];
+      const int g0 = args.group_off[e], g1 = args.group_off[e + 1];
+      const int mt = (g1 - g0 + BM - 1) / BM;
+      x.t = u;
+      x.sp = 0;
+      x.m0 = g0 + (local % mt) * BM;
+      x.m_lim = g1;
+      x.tn = local / mt;
+      x.brow = e * args.b_group_rows;
+    } else {
+      x.t = u / splits;
+      x.sp = u % splits;
+      x.m0 = args.m_begin + (x.t % args.m_tiles) * BM;
+      x.m_lim = args.m_end;
+      x.tn = x.t / args.m_tiles;
+      x.brow = 0;
+    }
+    return x;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
@@ -137,9 +179,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       uint32_t issued_mask = 0, last_ph[MAX_STAGES] = {0, 0, 0, 0};
       bool ok = true;
       for (int u = blockIdx.x; u < total_tiles && ok; u += gridDim.x) {
-        const int t = u / splits, sp = u % splits;
-        const int tm = t % args.m_tiles, tn = t / args.m_tiles;
-        const int m0 = args.m_begin + tm * BM;
+        const GemmTile x = decode(u);
+        const int sp = x.sp, tn = x.tn, m0 = x.m0;
         const int kb0 = sp * nk / splits, kb1 = (sp + 1) * nk / splits;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&tail->empty[st], ph ^ 1, tmo, abort_flag)) {
@@ -151,10 +192,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           mbar_arrive_expect_tx(&tail->full[st], STAGE_BYTES);
           tma_load_2d(sa, &tmA, &tail->full[st], kb * BK, m0);
           if (EPI == EPI_SWIGLU) {
-            tma_load_2d(sb, &tmB, &tail->full[st], kb * BK, tn * (BN / 2));
-            tma_load_2d(sb + B_BYTES / 2, &tmB2, &tail->full[st], kb * BK, tn * (BN / 2));
+            tma_load_2d(sb, &tmB, &tail->full[st], kb * BK, x.brow + tn * (BN / 2));
+            tma_load_2d(sb + B_BYTES / 2, &tmB2, &tail->full[st], kb * BK,
+                        x.brow + args.b2_row_off + tn * (BN / 2));
           } else {
-            tma_load_2d(sb, &tmB, &tail->full[st], kb * BK, tn * BN);
+            tma_load_2d(sb, &tmB, &tail->full[st], kb * BK, x.brow + tn * BN);
           }
           issued_mask |= 1u << st;
           last_ph[st] = ph;
@@ -178,7 +220,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       uint32_t st = 0, ph = 0, acc = 0, aph = 0;
       bool ok = true, any = false;
       for (int u = blockIdx.x; u < total_tiles && ok; u += gridDim.x) {
-        const int sp = u % splits;
+        const int sp = decode(u).sp;
         const int kb0 = sp * nk / splits, kb1 = (sp + 1) * nk / splits;
         if (!mbar_wait(&tail->tempty[acc], aph ^ 1, tmo, abort_flag)) {
           ok = false;
@@ -237,7 +279,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       return ok;
     };
     for (int u = blockIdx.x; u < total_tiles; u += gridDim.x) {
-      const int t = u / splits, sp = u % splits;
+      const GemmTile x = decode(u);
+      const int t = x.t, sp = x.sp;
       // the wait result must be warp-uniform: tcgen05.ld below is .sync.aligned
       const bool got = __all_sync(0xffffffffu, mbar_wait(&tail->tfull[acc], aph, tmo, abort_flag));
       if (!got) {
@@ -246,9 +289,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         break;
       }
       tc_fence_after();
-      const int tm = t % args.m_tiles, tn = t / args.m_tiles;
-      const int m = args.m_begin + tm * BM + row_in_tile;
-      const bool row_ok = m < args.m_end;
+      const int tn = x.tn;
+      const int m = x.m0 + row_in_tile;
+      const bool row_ok = m < x.m_lim;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
       float v[32];
       // Split-K: publish this split's fp32 tile, and let the CTA that finishes
@@ -356,6 +399,20 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               }
             }
             store_row_chunk(crow, n, args.N, v);
+          }
+        }
+      } else if (EPI == EPI_STORE_F32) {
+        float* crow = args.Cf + static_cast<size_t>(m) * args.ldc;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          fetch32(c * 32, v);
+          const int n = tn * BN + c * 32;
+          if (row_ok && n < args.N) {
+            float4* d4 = reinterpret_cast<float4*>(crow + n);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              if (n + 4 * i + 4 <= args.N)
+                d4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
           }
         }
       } else if (EPI == EPI_SWIGLU) {
@@ -483,11 +540,15 @@ cudaError_t launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB,
                         const CUtensorMap& tmB2, const GemmArgs& args, int grid,
                         cudaStream_t stream) {
   if (grid <= 0) return cudaSuccess;
+  if (args.n_groups < 0 || args.n_groups > GEMM_MAX_GROUPS ||
+      (args.n_groups > 0 && (!args.group_off || args.splits > 1)))
+    return cudaErrorInvalidValue;
   switch (epi) {
     case EPI_STORE: return launch_epi<EPI_STORE>(tmA, tmB, tmB2, args, grid, stream);
     case EPI_RESID: return launch_epi<EPI_RESID>(tmA, tmB, tmB2, args, grid, stream);
     case EPI_SWIGLU: return launch_epi<EPI_SWIGLU>(tmA, tmB, tmB2, args, grid, stream);
     case EPI_QKV: return launch_epi<EPI_QKV>(tmA, tmB, tmB2, args, grid, stream);
+    case EPI_STORE_F32: return launch_epi<EPI_STORE_F32>(tmA, tmB, tmB2, args, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -8,7 +8,8 @@
 namespace nf {
 
 // ------------------------------------------------------------------ GEMM
-enum GemmEpi : int { EPI_STORE = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_QKV = 3 };
+enum GemmEpi : int { EPI_STORE = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_QKV = 3, EPI_STORE_F32 = 4 };
+constexpr int GEMM_MAX_GROUPS = 64;
 
 struct GemmArgs {
   int m_begin, m_end;   // output rows [m_begin, m_end)
@@ -34,6 +35,16 @@ struct GemmArgs {
   int splits;
   float* part;
   int* tile_cnt;
+  // grouped GEMM (mixture of experts): with n_groups > 0, row group e of A is
+  // [group_off[e], group_off[e+1]) (device array: the sizes are known only on
+  // the GPU) and multiplies the B rows from e * b_group_rows; tiles are
+  // enumerated on the device.  For SwiGLU the up rows of a group start
+  // b2_row_off rows after its gate rows (tmB2 may then be tmB).  No split-K.
+  const int* group_off;
+  int n_groups;
+  int b_group_rows;
+  int b2_row_off;
+  float* Cf;            // EPI_STORE_F32 output, row stride ldc
   uint32_t* status;
   unsigned long long timeout_ns;
 };
@@ -50,6 +61,25 @@ cudaError_t launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB,
                         cudaStream_t stream);
 int gemm_block_n(int epi);
 int gemm_tiles(int epi, int m_rows, int N);
+
+// ------------------------------------------------------ mixture of experts
+// Top-k routing of the tokens [r0, r0 + n) from router logits [*, E] fp32
+// (ties to the lower expert index, weights = softmax over the selected logits)
+// and their grouping by expert: rows of the grouped order are pairs (token,
+// choice), expert by expert, tokens increasing within an expert.  Writes
+// group_off [E + 1], perm_tok [n * k] (token of each grouped row), pair_row
+// [n * k] (grouped row of pair t * k + j) and pair_w [n * k].  One CTA.
+cudaError_t launch_moe_route(const float* logits, int r0, int n, int n_experts, int top_k,
+                             int* group_off, int* perm_tok, int* pair_row, float* pair_w,
+                             cudaStream_t stream);
+// dst[row] = src[perm_tok[row]] for row < rows (bf16 rows of `cols`, cols % 8 == 0).
+cudaError_t launch_gather_rows(const __nv_bfloat16* src, const int* perm_tok, __nv_bfloat16* dst,
+                               int rows, int cols, cudaStream_t stream);
+// y[t] = h[t] + sum_j pair_w[i k + j] * part[pair_row[i k + j]] for t = r0 + i, i < n
+// (fp32 sum in choice order, one bf16 rounding).
+cudaError_t launch_moe_combine(const __nv_bfloat16* h, const float* part, const int* pair_row,
+                               const float* pair_w, __nv_bfloat16* y, int r0, int n, int top_k,
+                               int hidden, cudaStream_t stream);
 
 // --------------------------------------------------------------- RMSNorm
 cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* g, __nv_bfloat16* out,

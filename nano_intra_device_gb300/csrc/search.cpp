@@ -103,6 +103,7 @@ struct Model {
     return gemm_time(rows, s.hidden, s.n_q_heads * s.head_dim, S, 256);
   }
   double ffn_time(int rows, int S) const {
+    if (s.n_experts > 0) rows *= s.top_k;  // every token runs top_k experts
     return gemm_time(rows, s.ffn, s.hidden, S, 128) + gemm_time(rows, s.hidden, s.ffn, S, 256);
   }
   double attn_time(int r0, int r1, int S, bool overlapped) const {

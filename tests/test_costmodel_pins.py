@@ -73,3 +73,17 @@ def test_nanobatch_examples_from_pages_are_multiples_of_128():
     assert sum(e["sizes"]) == e["b_dense"] and all(s % 128 == 0 for s in e["sizes"])
     s = GOLD["nanobatch_example"]["split"]
     assert s[-1] == GOLD["nanobatch_example"]["b_dense"]
+
+
+def test_moe_work_counts_top_k_experts_for_flops_and_all_for_bytes():
+    """Mixtral-shaped layer, 2048 tokens: FLOPs use the projections plus two
+    experts per token, the weight bytes all eight experts (closed forms)."""
+    shape = wl.mixtral_shape()
+    H, F = shape.hidden, shape.ffn
+    attn = H * (32 + 16) * 128 + 32 * 128 * H
+    seq = np.array([1] * 10)
+    q = np.ones(10, np.int64)
+    w = cm.step_work(shape, seq, q)
+    assert w["gemm_flops"] == 2 * 10 * (attn + 2 * 3 * H * F)
+    assert w["weight_bytes"] == 2 * (attn + 8 * 3 * H * F)
+    assert abs(w["weight_bytes"] / 1e9 - 2.90) < 0.01
