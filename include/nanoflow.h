@@ -119,19 +119,20 @@ typedef struct {
   int32_t attn_sms;   /* SMs for attention while it overlaps GEMMs (0 = automatic) */
   int32_t gemm_sms;   /* SMs for a GEMM while it overlaps attention (0 = the rest) */
   int32_t kv_chunk;   /* split-KV piece in tokens, multiple of page_size, <= 2048 (0 = 1024) */
-  int32_t attn_warps; /* warps per attention CTA (0 = 8).  Tensor-core kernel: 4 ... 8,
-                         10, 12 or 14, each CTA alone on its SM, ring stages per warp as
-                         deep as shared memory allows (4: 7, 5: 5, 6: 4, 7: 4, 8: 3, more
-                         warps: 2 pages).  FMA kernel: 8; 12 / 16 as warp pairs that split
-                         head_dim 128; 4 or 5 share each SM with one GEMM CTA of
+  int32_t attn_warps; /* warps per attention CTA (0 = 8).  Tensor-core kernel: 4 shares
+                         each SM with one GEMM CTA of gemm_stages = 2 (3-page rings, 117 KB,
+                         <= 128 registers a thread); 5 ... 8, 10, 12 or 14 fill an SM, ring
+                         stages per warp as deep as shared memory allows (5: 5, 6: 4, 7: 4,
+                         8: 3, more warps: 2 pages).  FMA kernel: 8; 12 / 16 as warp pairs
+                         that split head_dim 128; 4 or 5 share each SM with one GEMM CTA of
                          gemm_stages = 2 */
   int32_t gemm_stages; /* shared-memory ring stages of the GEMM kernel: 4 fills an SM;
                           2 lets an attention CTA of 4 or 5 warps run on the same SM (0 = 4) */
   int32_t gemm_split_k; /* 0: split K across CTAs when a GEMM has fewer output tiles than
                            half its SMs; 1: never split */
   int32_t attn_impl;  /* nf_attn_impl.  NF_ATTN_AUTO picks the FMA kernel for its own
-                         attn_warps 4, 5 and 16, else the tensor-core kernel where the
-                         shape allows it; nf_plan_info reports the kernel chosen */
+                         attn_warps 5 and 16, else the tensor-core kernel where the shape
+                         allows it; nf_plan_info reports the kernel chosen */
   int32_t validate;   /* 1 = check page ids and lengths on the device */
   int64_t timeout_ns; /* limit of every device-side wait (0 = 2e9) */
 } nf_plan_opts;

@@ -445,10 +445,10 @@ nf_status build_plan(const nf_model_shape* shape, const nf_batch_desc* batch,
       delete p;
       return fail(NF_ERR_UNSUPPORTED, "tensor-core attention: unsupported shape or pool size");
     }
-    // automatic: the tensor cores, except for the FMA kernel's own shared-SM
-    // (4, 5 warps) and warp-pair (16) configurations
+    // automatic: the tensor cores, except for the FMA kernel's own 5-warp
+    // shared-SM and 16-warp warp-pair configurations
     const int w = p->opts.attn_warps;
-    const bool fma_cfg = w == 4 || w == 5 || w == 16;
+    const bool fma_cfg = w == 5 || w == 16;
     const bool fma_has = w == 4 || w == 5 || w == 8 || w == 12 || w == 16;
     p->attn_mma = p->opts.attn_impl == NF_ATTN_MMA ||
                   (p->opts.attn_impl == NF_ATTN_AUTO && mma_ok && !fma_cfg);

@@ -74,14 +74,22 @@ __device__ __forceinline__ uint32_t page_chunk_off(int pos, int ci) {
   return static_cast<uint32_t>(box * (AMMA_P * 128) + pos * 128 + ((c ^ (pos & 7)) << 4));
 }
 
+// The 4-warp configuration shares its SM with one GEMM CTA of 2 ring stages
+// (98 KB, <= 248 registers a thread): it takes 117 KB (more than half an SM, so
+// two attention CTAs never pair up) and at most 128 registers a thread.  The
+// others fill an SM alone.
+constexpr int AMMA_SHARE_WARPS = 4;
+constexpr int AMMA_SHARE_SMEM = 117 * 1024;
+
 static int amma_smem_bytes(int head_dim, int warps, int stages) {
   const int slot = 2 * AMMA_P * head_dim * 2;  // K and V of one (page, KV head)
   const int need = 1024 + warps * stages * (slot + 8);
-  return need < AMMA_MIN_SMEM ? AMMA_MIN_SMEM : need;
+  const int floor = warps == AMMA_SHARE_WARPS ? AMMA_SHARE_SMEM : AMMA_MIN_SMEM;
+  return need < floor ? floor : need;
 }
 
 template <int GRP, int NCH, int WARPS, int STAGES>
-__global__ void __launch_bounds__(WARPS * 32, 1)
+__global__ void __launch_bounds__(WARPS * 32, WARPS == AMMA_SHARE_WARPS ? 4 : 1)
     attn_mma_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                     const AttnArgs a) {
   constexpr int D = NCH * 64;
@@ -432,7 +440,7 @@ cudaError_t launch_attention_mma(const AttnArgs& a, const CUtensorMap& tk, const
   // warps per CTA -> ring stages per warp: as deep as 227 KB of shared memory allows
 #define NF_AMMA_CFG(G, N)                                             \
   switch (a.warps) {                                                  \
-    case 4: return launch_mma_t<G, N, 4, 7>(a, tk, tv, grid, stream); \
+    case 4: return launch_mma_t<G, N, 4, 3>(a, tk, tv, grid, stream); \
     case 5: return launch_mma_t<G, N, 5, 5>(a, tk, tv, grid, stream); \
     case 6: return launch_mma_t<G, N, 6, 4>(a, tk, tv, grid, stream); \
     case 7: return launch_mma_t<G, N, 7, 4>(a, tk, tv, grid, stream); \
