@@ -88,7 +88,7 @@ static int amma_smem_bytes(int head_dim, int warps, int stages) {
   return need < floor ? floor : need;
 }
 
-template <int GRP, int NCH, int WARPS, int STAGES>
+template <int GRP, int NCH, int WARPS, int STAGES, int PPI>
 __global__ void __launch_bounds__(WARPS * 32, WARPS == AMMA_SHARE_WARPS ? 4 : 1)
     attn_mma_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                     const AttnArgs a) {
@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(WARPS * 32, WARPS == AMMA_SHARE_WARPS ? 4 : 1)
   constexpr int SLOT = 2 * BLK;
   constexpr int KS = D / 16;        // k-steps of S, m-tiles of O
   static_assert(GRP >= 1 && GRP <= 8, "the GQA group must fit the 8 columns of a tile");
-  static_assert(STAGES >= 2, "S of page k+1 is formed while page k is still in use");
+  static_assert(STAGES >= 2 * PPI, "S of the next group is formed while this one is in use");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // swizzled boxes: 1 KB aligned
@@ -244,45 +244,79 @@ __global__ void __launch_bounds__(WARPS * 32, WARPS == AMMA_SHARE_WARPS ? 4 : 1)
           mbar_wait(&bar[(gk + kk) % STAGES], ((gk + kk) / STAGES) & 1, a.timeout_ns);
     };
 
-    // Software pipeline: S of page k+1 is formed before the softmax and PV of
-    // page k.  (rs, rph): ring slot and barrier phase of page k.
+    // Software pipeline over groups of PPI pages: S of the next group is formed
+    // before the softmax and PV of the current one.  (rs, rph): ring slot and
+    // barrier phase of the group's first page; page i of a group sits i slots on.
+    auto slot_at = [&](uint32_t base, uint32_t ph, int i, uint32_t& st, uint32_t& p) {
+      st = base + i;
+      p = ph;
+      if (st >= STAGES) {
+        st -= STAGES;
+        p ^= 1;
+      }
+    };
     uint32_t rs = gk % STAGES, rph = (gk / STAGES) & 1;
-    float sn[4];
-    if (slot_ready(rs, rph)) {
-      qk(ring_u32 + rs * SLOT, sn);
-    } else {
-      drain_from(0);
-      failed = true;
-    }
-    for (int k = 0; k < npg && !failed; ++k) {
-      const uint32_t slot = ring_u32 + rs * SLOT;
-      uint32_t ns = rs + 1, nph = rph;
-      if (ns == STAGES) {
-        ns = 0;
-        nph ^= 1;
-      }
-      float sc[4] = {sn[0], sn[1], sn[2], sn[3]};  // raw q.k: (pos lr, h0), (lr, h1), (lr+8, h0), (lr+8, h1)
-      if (k + 1 < npg) {
-        if (!slot_ready(ns, nph)) {
-          drain_from(k + 1);
+    float sn[PPI][4];
+#pragma unroll
+    for (int i = 0; i < PPI; ++i) {
+      if (i < npg && !failed) {
+        uint32_t st, ph;
+        slot_at(rs, rph, i, st, ph);
+        if (slot_ready(st, ph)) {
+          qk(ring_u32 + st * SLOT, sn[i]);
+        } else {
+          drain_from(i);
           failed = true;
-          break;
         }
-        qk(ring_u32 + ns * SLOT, sn);
       }
-      const int kb = k * P;
-      const bool partial = kb + P > n;  // only a piece's last page (warp-uniform)
-      if (partial) {  // positions past the piece may hold anything, even NaN
-        const bool v0 = kb + lr < n, v1 = kb + lr + 8 < n;
-        sc[0] = v0 ? sc[0] : -INFINITY;
-        sc[1] = v0 ? sc[1] : -INFINITY;
-        sc[2] = v1 ? sc[2] : -INFINITY;
-        sc[3] = v1 ? sc[3] : -INFINITY;
+    }
+    for (int k = 0; k < npg && !failed; k += PPI) {
+      uint32_t ns, nph;  // first slot of the next group
+      slot_at(rs, rph, PPI, ns, nph);
+      float sc[PPI][4];
+#pragma unroll
+      for (int i = 0; i < PPI; ++i)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) sc[i][r] = sn[i][r];  // raw q.k: (pos lr, h0), (lr, h1), (lr+8, h0), (lr+8, h1)
+#pragma unroll
+      for (int i = 0; i < PPI; ++i) {
+        if (k + PPI + i < npg && !failed) {
+          uint32_t st, ph;
+          slot_at(ns, nph, i, st, ph);
+          if (slot_ready(st, ph)) {
+            qk(ring_u32 + st * SLOT, sn[i]);
+          } else {
+            drain_from(k + PPI + i);
+            failed = true;
+          }
+        }
+      }
+      if (failed) break;
+      // positions past the piece (the last page's tail, or a missing last page
+      // of the group) may hold anything, even NaN: they become -inf
+      const bool tail = (k + PPI) * P > n;  // warp-uniform
+      if (tail) {
+#pragma unroll
+        for (int i = 0; i < PPI; ++i) {
+          const int kb = (k + i) * P;
+          const bool v0 = kb + lr < n, v1 = kb + lr + 8 < n;
+          sc[i][0] = v0 ? sc[i][0] : -INFINITY;
+          sc[i][1] = v0 ? sc[i][1] : -INFINITY;
+          sc[i][2] = v1 ? sc[i][2] : -INFINITY;
+          sc[i][3] = v1 ? sc[i][3] : -INFINITY;
+        }
       }
       // Lazy softmax: p = 2^(s * scale - m) with m only raised when some score
       // passes it by more than kLazy, so p <= 2^kLazy; no lane then needs the
       // column maximum, which costs shuffles.
-      const float x0 = fmaxf(sc[0], sc[2]) * scale, x1 = fmaxf(sc[1], sc[3]) * scale;
+      float x0 = fmaxf(sc[0][0], sc[0][2]), x1 = fmaxf(sc[0][1], sc[0][3]);
+#pragma unroll
+      for (int i = 1; i < PPI; ++i) {
+        x0 = fmaxf(x0, fmaxf(sc[i][0], sc[i][2]));
+        x1 = fmaxf(x1, fmaxf(sc[i][1], sc[i][3]));
+      }
+      x0 *= scale;
+      x1 *= scale;
       if (__any_sync(0xffffffffu, x0 > m0 + kLazy || x1 > m1 + kLazy)) {
         float y0 = x0, y1 = x1;
 #pragma unroll
@@ -304,39 +338,55 @@ __global__ void __launch_bounds__(WARPS * 32, WARPS == AMMA_SHARE_WARPS ? 4 : 1)
         m0 = n0;
         m1 = n1;
       }
-      const uint32_t p01 = pack_bf16(ex2_approx(fmaf(sc[0], scale, -m0)),
-                                     ex2_approx(fmaf(sc[1], scale, -m1)));
-      const uint32_t p23 = pack_bf16(ex2_approx(fmaf(sc[2], scale, -m0)),
-                                     ex2_approx(fmaf(sc[3], scale, -m1)));
-      l0 += bf16lo(p01) + bf16lo(p23);
-      l1 += bf16hi(p01) + bf16hi(p23);
-      // P^T operand: (positions 2 lc (+1), head lr) and positions + 8
-      const uint32_t pb0 = movmatrix_trans(p01);
-      const uint32_t pb1 = movmatrix_trans(p23);
-      if (!partial) {
 #pragma unroll
-        for (int mi = 0; mi < KS; ++mi) {
-          uint32_t vf[4];
-          ldsm_x4_trans(slot + voff[mi], vf);
-          mma_16816(o[mi], vf, pb0, pb1);
-        }
-      } else {  // rows past the piece read row 0 instead (weighted 0)
-        const bool past = kb + v_row >= n;
+      for (int i = 0; i < PPI; ++i) {
+        if (k + i >= npg) break;  // warp-uniform
+        const uint32_t p01 = pack_bf16(ex2_approx(fmaf(sc[i][0], scale, -m0)),
+                                       ex2_approx(fmaf(sc[i][1], scale, -m1)));
+        const uint32_t p23 = pack_bf16(ex2_approx(fmaf(sc[i][2], scale, -m0)),
+                                       ex2_approx(fmaf(sc[i][3], scale, -m1)));
+        l0 += bf16lo(p01) + bf16lo(p23);
+        l1 += bf16hi(p01) + bf16hi(p23);
+        // P^T operand: (positions 2 lc (+1), head lr) and positions + 8
+        const uint32_t pb0 = movmatrix_trans(p01);
+        const uint32_t pb1 = movmatrix_trans(p23);
+        uint32_t st, ph;
+        slot_at(rs, rph, i, st, ph);
+        const uint32_t slot = ring_u32 + st * SLOT;
+        const int kb = (k + i) * P;
+        if (kb + P <= n) {
 #pragma unroll
-        for (int mi = 0; mi < KS; ++mi) {
-          uint32_t vf[4];
-          ldsm_x4_trans(slot + (past ? BLK + page_chunk_off(0, 2 * mi + v_ci) : voff[mi]), vf);
-          mma_16816(o[mi], vf, pb0, pb1);
+          for (int mi = 0; mi < KS; ++mi) {
+            uint32_t vf[4];
+            ldsm_x4_trans(slot + voff[mi], vf);
+            mma_16816(o[mi], vf, pb0, pb1);
+          }
+        } else {  // rows past the piece read row 0 instead (weighted 0)
+          const bool past = kb + v_row >= n;
+#pragma unroll
+          for (int mi = 0; mi < KS; ++mi) {
+            uint32_t vf[4];
+            ldsm_x4_trans(slot + (past ? BLK + page_chunk_off(0, 2 * mi + v_ci) : voff[mi]), vf);
+            mma_16816(o[mi], vf, pb0, pb1);
+          }
         }
       }
-      if (k + STAGES < npg) {  // refill this slot with page k + STAGES
-        const int pg = page_id(k + STAGES);
-        __syncwarp();
-        if (lane == 0) {
-          fence_proxy_async_smem();
-          issue_into(rs, pg);
+      // refill the group's slots with the pages STAGES further on
+      int pg[PPI];
+#pragma unroll
+      for (int i = 0; i < PPI; ++i) pg[i] = k + i + STAGES < npg ? page_id(k + i + STAGES) : -1;
+      __syncwarp();
+      if (lane == 0 && pg[0] >= 0) fence_proxy_async_smem();
+#pragma unroll
+      for (int i = 0; i < PPI; ++i) {
+        if (pg[i] >= 0) {
+          if (lane == 0) {
+            uint32_t st, ph;
+            slot_at(rs, rph, i, st, ph);
+            issue_into(st, pg[i]);
+          }
+          ++issued;
         }
-        ++issued;
       }
       rs = ns;
       rph = nph;
@@ -402,18 +452,18 @@ __global__ void __launch_bounds__(WARPS * 32, WARPS == AMMA_SHARE_WARPS ? 4 : 1)
   if (failed) raise_status(a.status, ST_TIMEOUT);
 }
 
-template <int GRP, int NCH, int WARPS, int STAGES>
+template <int GRP, int NCH, int WARPS, int STAGES, int PPI>
 static cudaError_t launch_mma_t(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
                                 int grid, cudaStream_t stream) {
   const int smem = amma_smem_bytes(NCH * 64, WARPS, STAGES);
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel<GRP, NCH, WARPS, STAGES>,
+    cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel<GRP, NCH, WARPS, STAGES, PPI>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  attn_mma_kernel<GRP, NCH, WARPS, STAGES><<<grid, WARPS * 32, smem, stream>>>(tk, tv, a);
+  attn_mma_kernel<GRP, NCH, WARPS, STAGES, PPI><<<grid, WARPS * 32, smem, stream>>>(tk, tv, a);
   return cudaGetLastError();
 }
 
@@ -437,18 +487,20 @@ cudaError_t launch_attention_mma(const AttnArgs& a, const CUtensorMap& tk, const
   if (grid <= 0 || !attention_mma_supported(a.n_q, a.n_kv, a.head_dim, a.page_size, a.num_pages))
     return cudaErrorInvalidValue;
   const int grp = a.n_q / a.n_kv, nch = a.head_dim / 64;
-  // warps per CTA -> ring stages per warp: as deep as 227 KB of shared memory allows
-#define NF_AMMA_CFG(G, N)                                             \
-  switch (a.warps) {                                                  \
-    case 4: return launch_mma_t<G, N, 4, 3>(a, tk, tv, grid, stream); \
-    case 5: return launch_mma_t<G, N, 5, 5>(a, tk, tv, grid, stream); \
-    case 6: return launch_mma_t<G, N, 6, 4>(a, tk, tv, grid, stream); \
-    case 7: return launch_mma_t<G, N, 7, 4>(a, tk, tv, grid, stream); \
-    case 8: return launch_mma_t<G, N, 8, 3>(a, tk, tv, grid, stream); \
-    case 10: return launch_mma_t<G, N, 10, 2>(a, tk, tv, grid, stream); \
-    case 12: return launch_mma_t<G, N, 12, 2>(a, tk, tv, grid, stream); \
-    case 14: return launch_mma_t<G, N, 14, 2>(a, tk, tv, grid, stream); \
-    default: return cudaErrorInvalidValue;                            \
+  // warps per CTA -> ring stages per warp (as deep as 227 KB of shared memory
+  // allows) and pages per iteration (two pages per iteration measured slower
+  // than one on every configuration, so all use one)
+#define NF_AMMA_CFG(G, N)                                                  \
+  switch (a.warps) {                                                       \
+    case 4: return launch_mma_t<G, N, 4, 3, 1>(a, tk, tv, grid, stream);   \
+    case 5: return launch_mma_t<G, N, 5, 5, 1>(a, tk, tv, grid, stream);   \
+    case 6: return launch_mma_t<G, N, 6, 4, 1>(a, tk, tv, grid, stream);   \
+    case 7: return launch_mma_t<G, N, 7, 4, 1>(a, tk, tv, grid, stream);   \
+    case 8: return launch_mma_t<G, N, 8, 3, 1>(a, tk, tv, grid, stream);   \
+    case 10: return launch_mma_t<G, N, 10, 2, 1>(a, tk, tv, grid, stream); \
+    case 12: return launch_mma_t<G, N, 12, 2, 1>(a, tk, tv, grid, stream); \
+    case 14: return launch_mma_t<G, N, 14, 2, 1>(a, tk, tv, grid, stream); \
+    default: return cudaErrorInvalidValue;                                 \
   }
 #define NF_AMMA_CASE(G, N) \
   if (grp == G && nch == N) { NF_AMMA_CFG(G, N) }
