@@ -169,6 +169,18 @@ typedef struct {
 nf_status nf_plan_create(const nf_model_shape* shape, const nf_batch_desc* batch,
                          const nf_plan_opts* opts, nf_plan* out);
 
+/* Give the plan the structure of the next step's batch (the runtime's batch
+ * formation changes it every iteration): at most the sequences and tokens the
+ * plan was created for, the same max_pages_per_seq and num_pages.  opts: a
+ * new split and SM shares for it (kv_chunk, attn_impl and attn_warps must stay
+ * as created; 0 fields take the plan's values), or NULL to keep the current
+ * split, or to fall back to one sequential nano-batch when the token count
+ * changed.  The device copies are enqueued on `stream` (pinned staging, no
+ * allocation after the first call); steps enqueued after it on that stream see
+ * the new batch.  A plan serves one stream at a time. */
+nf_status nf_plan_set_batch(nf_plan plan, const nf_batch_desc* batch, const nf_plan_opts* opts,
+                            void* stream);
+
 /* The plan's split and resources, and the batch's token count. */
 nf_status nf_plan_info(nf_plan plan, nf_plan_opts* out, int32_t* n_tokens);
 
@@ -401,6 +413,80 @@ nf_status nf_profile(const nf_model_shape* shape, int32_t max_tokens, int32_t me
 nf_status nf_plan_search(const nf_model_shape* shape, const nf_batch_desc* batch,
                          const char* profile_json, int32_t num_sms, nf_plan_opts* out,
                          double* predicted_us);
+
+/* ---------------------------------------------------------------------------
+ * Runtime around the step ("NanoFlow: Towards Optimal LLM Serving Throughput",
+ * "The NanoFlow Runtime System"): requests in, greedy tokens out.
+ *
+ * Batch formation keeps a constant token budget b_dense per iteration: every
+ * decoding request gets one token first, then prompts are cut into chunks,
+ * first come first served, that fill the rest.  nf_runtime_step forms the next
+ * iteration and enqueues it (token composition from each request's previous
+ * output kept on the device, the stack step, argmax sampling, an asynchronous
+ * copy of the sampled tokens) without waiting for the GPU; the tokens of an
+ * iteration are taken in when the iteration two later is formed, so a request
+ * that produced eos_token runs one more (wasted) iteration, as in the pages.
+ * KV pages of every layer share one page allocator of num_pages pages; a
+ * finished request returns its pages and its token slot.  The plan follows
+ * each batch (nf_plan_set_batch); the plan search runs again when the decode
+ * share of the batch moved by more than replan_threshold since the last search
+ * or the token count changed (the pages' pipeline is static; this re-plans it
+ * online). */
+typedef struct nf_runtime_s* nf_runtime;
+typedef struct {
+  int32_t b_dense;            /* tokens per iteration */
+  int32_t max_requests;       /* requests admitted at once (device token slots) */
+  int32_t max_pages_per_seq;  /* block-table width: longest prompt + output */
+  int32_t num_pages;          /* pages in each layer's K and V pools */
+  int32_t vocab;              /* the LM head's rows, a multiple of 8 */
+  int32_t eos_token;          /* -1: requests end after max_new_tokens only */
+  float replan_threshold;     /* < 0: never re-plan (one sequential nano-batch) */
+  int32_t host_only;          /* 1: no device resources; batches are formed with
+                                 nf_runtime_form and results given with
+                                 nf_runtime_apply (the scheduler alone) */
+} nf_runtime_opts;
+
+/* One iteration's batch as formed (arrays owned by the runtime, valid until the
+ * same iteration slot is formed again, two iterations later).  Rows: decode
+ * sequences first (one row each), then the prompt chunks. */
+typedef struct {
+  int32_t iteration;
+  int32_t n_tokens;
+  int32_t n_decode;               /* decode sequences (= decode rows) */
+  int32_t n_prefill;              /* prompt chunks */
+  const int32_t* row_request;     /* [n_tokens] request id */
+  const int32_t* row_pos;         /* [n_tokens] position in the request's sequence */
+  const int32_t* row_token;       /* [n_tokens] prompt token, or -1: the request's last output */
+  const int32_t* row_emit;        /* [n_tokens] 1 where the row's output is the request's next token */
+  const int32_t* seq_lens;        /* [n_decode + n_prefill] KV length after the step */
+  const int32_t* block_table;     /* [n_decode + n_prefill][max_pages_per_seq], -1 past the end */
+  const int32_t* prefill_q_lens;  /* [n_prefill] */
+  int32_t replanned;              /* the plan search ran for this batch */
+  int32_t free_pages;             /* pages left after forming it */
+} nf_runtime_batch;
+
+nf_status nf_runtime_create(const nf_model_shape* shape, const nf_runtime_opts* opts,
+                            nf_runtime* out);
+/* Waits for the iterations in flight, then frees everything. */
+void nf_runtime_destroy(nf_runtime rt);
+/* A request: prompt tokens (host, copied), at most max_new_tokens outputs. */
+nf_status nf_runtime_submit(nf_runtime rt, const int32_t* prompt, int32_t prompt_len,
+                            int32_t max_new_tokens, int32_t* id);
+/* Form and enqueue the next iteration on `stream` (see above).  A batch of 0
+ * tokens means nothing could run (all requests finished). */
+nf_status nf_runtime_step(nf_runtime rt, const nf_stack_weights* w, void* const* k_pools,
+                          void* const* v_pools, void* stream, nf_runtime_batch* out);
+/* Wait for the iterations in flight and take in their tokens. */
+nf_status nf_runtime_sync(nf_runtime rt);
+/* A request's outputs so far (tokens: host, up to cap). */
+nf_status nf_runtime_result(nf_runtime rt, int32_t id, int32_t* finished, int32_t* n_tokens,
+                            int32_t* tokens, int32_t cap);
+nf_status nf_runtime_counts(nf_runtime rt, int32_t* waiting, int32_t* active, int32_t* free_pages);
+/* Host-only runtimes: form the next batch / give the sampled tokens of an
+ * iteration ([n_tokens], read where row_emit is 1).  At most two iterations
+ * may await results. */
+nf_status nf_runtime_form(nf_runtime rt, nf_runtime_batch* out);
+nf_status nf_runtime_apply(nf_runtime rt, int32_t iteration, const int32_t* sampled);
 
 #ifdef __cplusplus
 }

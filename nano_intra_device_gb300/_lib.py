@@ -48,6 +48,21 @@ class nf_plan_opts(Structure):
                 ("timeout_ns", c_int64)]
 
 
+class nf_runtime_opts(Structure):
+    _fields_ = [("b_dense", c_int32), ("max_requests", c_int32), ("max_pages_per_seq", c_int32),
+                ("num_pages", c_int32), ("vocab", c_int32), ("eos_token", c_int32),
+                ("replan_threshold", c_float), ("host_only", c_int32)]
+
+
+class nf_runtime_batch(Structure):
+    _fields_ = [("iteration", c_int32), ("n_tokens", c_int32), ("n_decode", c_int32),
+                ("n_prefill", c_int32), ("row_request", POINTER(c_int32)),
+                ("row_pos", POINTER(c_int32)), ("row_token", POINTER(c_int32)),
+                ("row_emit", POINTER(c_int32)), ("seq_lens", POINTER(c_int32)),
+                ("block_table", POINTER(c_int32)), ("prefill_q_lens", POINTER(c_int32)),
+                ("replanned", c_int32), ("free_pages", c_int32)]
+
+
 class nf_trace_entry(Structure):
     _fields_ = [("op", c_int32), ("nano", c_int32), ("step", c_int32), ("start_ms", c_float),
                 ("ms", c_float)]
@@ -77,6 +92,16 @@ _SIGS = {
     "nf_plan_poll": (c_int, [c_void_p, c_int]),
     "nf_stack_step": (c_int, [c_void_p, POINTER(nf_stack_weights), c_void_p, POINTER(c_void_p), POINTER(c_void_p), c_void_p, c_void_p, c_void_p, c_void_p]),
     "nf_layers_step": (c_int, [c_void_p, POINTER(nf_layer_weights), c_int32, c_void_p, POINTER(c_void_p), POINTER(c_void_p), c_void_p, c_void_p, c_void_p, c_void_p]),
+    "nf_plan_set_batch": (c_int, [c_void_p, POINTER(nf_batch_desc), POINTER(nf_plan_opts), c_void_p]),
+    "nf_runtime_create": (c_int, [POINTER(nf_model_shape), POINTER(nf_runtime_opts), POINTER(c_void_p)]),
+    "nf_runtime_destroy": (None, [c_void_p]),
+    "nf_runtime_submit": (c_int, [c_void_p, POINTER(c_int32), c_int32, c_int32, POINTER(c_int32)]),
+    "nf_runtime_step": (c_int, [c_void_p, POINTER(nf_stack_weights), POINTER(c_void_p), POINTER(c_void_p), c_void_p, POINTER(nf_runtime_batch)]),
+    "nf_runtime_sync": (c_int, [c_void_p]),
+    "nf_runtime_result": (c_int, [c_void_p, c_int32, POINTER(c_int32), POINTER(c_int32), POINTER(c_int32), c_int32]),
+    "nf_runtime_counts": (c_int, [c_void_p, POINTER(c_int32), POINTER(c_int32), POINTER(c_int32)]),
+    "nf_runtime_form": (c_int, [c_void_p, POINTER(nf_runtime_batch)]),
+    "nf_runtime_apply": (c_int, [c_void_p, c_int32, POINTER(c_int32)]),
     "nf_last_error": (c_char_p, []),
     "nf_device_sm_count": (c_int32, []),
     "nf_step_metadata": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p]),
@@ -216,6 +241,14 @@ class Plan:
         check(lib().nf_plan_info(self.h, ctypes.byref(o), ctypes.byref(n)))
         return o, n.value
 
+    def set_batch(self, batch, opts: nf_plan_opts | None = None, stream=None, hint=True):
+        """nf_plan_set_batch: the next steps run `batch` (same page geometry,
+        at most the sequences and tokens the plan was created for)."""
+        self._batch = make_batch_desc(batch, hint)
+        check(lib().nf_plan_set_batch(self.h, ctypes.byref(self._batch),
+                                      ctypes.byref(opts) if opts is not None else None,
+                                      stream_handle(stream)))
+
     def close(self):
         if self.h:
             lib().nf_plan_destroy(self.h)
@@ -336,3 +369,78 @@ def plan_search(shape, batch, profile_json=None, num_sms=152):
 
 def device_sm_count():
     return lib().nf_device_sm_count()
+
+
+# ---------------------------------------------------------------- runtime
+
+class Runtime:
+    """nf_runtime: requests in, greedy tokens out (batch formation, async
+    scheduling, KV pages, online re-planning)."""
+
+    def __init__(self, shape, b_dense, max_requests, max_pages_per_seq, num_pages, vocab,
+                 eos_token=-1, replan_threshold=0.1, host_only=False):
+        self.h = c_void_p()
+        self._shape = make_shape(shape)
+        self.opts = nf_runtime_opts(b_dense, max_requests, max_pages_per_seq, num_pages, vocab,
+                                    eos_token, replan_threshold, 1 if host_only else 0)
+        self.max_pages = max_pages_per_seq
+        check(lib().nf_runtime_create(ctypes.byref(self._shape), ctypes.byref(self.opts),
+                                      ctypes.byref(self.h)))
+
+    def submit(self, prompt, max_new_tokens):
+        arr = (c_int32 * len(prompt))(*[int(t) for t in prompt])
+        rid = c_int32()
+        check(lib().nf_runtime_submit(self.h, arr, len(prompt), max_new_tokens, ctypes.byref(rid)))
+        return rid.value
+
+    @staticmethod
+    def _view(b, max_pages):
+        n, ns = b.n_tokens, b.n_decode + b.n_prefill
+        get = lambda p, k: [p[i] for i in range(k)] if k else []  # noqa: E731
+        return {"iteration": b.iteration, "n_tokens": n, "n_decode": b.n_decode,
+                "n_prefill": b.n_prefill, "row_request": get(b.row_request, n),
+                "row_pos": get(b.row_pos, n), "row_token": get(b.row_token, n),
+                "row_emit": get(b.row_emit, n), "seq_lens": get(b.seq_lens, ns),
+                "block_table": get(b.block_table, ns * max_pages),
+                "prefill_q_lens": get(b.prefill_q_lens, b.n_prefill),
+                "replanned": b.replanned, "free_pages": b.free_pages}
+
+    def form(self):
+        b = nf_runtime_batch()
+        check(lib().nf_runtime_form(self.h, ctypes.byref(b)))
+        return self._view(b, self.max_pages)
+
+    def apply(self, iteration, sampled):
+        arr = (c_int32 * max(1, len(sampled)))(*[int(t) for t in sampled])
+        check(lib().nf_runtime_apply(self.h, iteration, arr))
+
+    def step(self, stack_args, stream=None):
+        b = nf_runtime_batch()
+        check(lib().nf_runtime_step(self.h, ctypes.byref(stack_args.w), stack_args.kps, stack_args.vps,
+                                    stream_handle(stream), ctypes.byref(b)))
+        return self._view(b, self.max_pages)
+
+    def sync(self):
+        check(lib().nf_runtime_sync(self.h))
+
+    def result(self, rid, cap=4096):
+        fin, n = c_int32(), c_int32()
+        toks = (c_int32 * cap)()
+        check(lib().nf_runtime_result(self.h, rid, ctypes.byref(fin), ctypes.byref(n), toks, cap))
+        return bool(fin.value), [toks[i] for i in range(min(n.value, cap))]
+
+    def counts(self):
+        w, a, f = c_int32(), c_int32(), c_int32()
+        check(lib().nf_runtime_counts(self.h, ctypes.byref(w), ctypes.byref(a), ctypes.byref(f)))
+        return w.value, a.value, f.value
+
+    def close(self):
+        if self.h:
+            lib().nf_runtime_destroy(self.h)
+            self.h = c_void_p()
+
+    def __del__(self):  # pragma: no cover
+        try:
+            self.close()
+        except Exception:
+            pass

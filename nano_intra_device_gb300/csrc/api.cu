@@ -105,7 +105,10 @@ struct nf_plan_s {
   int n_decode = 0, n_prefill = 0;
   std::vector<int> prefill_q, seq_hint;
   int max_pages = 0, num_pages = 0;
-  int n_seq = 0, T = 0;
+  int n_seq = 0, T = 0;         // the current batch (nf_plan_set_batch may change it)
+  int seq_cap = 0, T_cap = 0;   // what the workspace was allocated for
+  int* set_stage = nullptr;     // pinned host staging of nf_plan_set_batch (two halves)
+  int set_flip = 0;
   std::vector<int> q_lens, tok_begin;
   nf_plan_opts opts{};
   int num_sms = 0;
@@ -282,6 +285,7 @@ void free_plan(nf_plan p) {
                   p->moe_a, p->moe_act, p->moe_out};
   for (void* b : bufs)
     if (b) cudaFree(b);
+  if (p->set_stage) cudaFreeHost(p->set_stage);
   for (cudaEvent_t e : p->ev) cudaEventDestroy(e);
   for (auto& r : p->trace) {
     cudaEventDestroy(r.b);
@@ -314,14 +318,16 @@ nf_status dalloc(T** ptr, size_t bytes) {
   } while (0)
 
 nf_status alloc_plan(nf_plan p) {
-  const size_t T = p->T, H = p->shape.hidden, F = p->shape.ffn;
+  p->T_cap = p->T;
+  p->seq_cap = p->n_seq;
+  const size_t T = p->T_cap, H = p->shape.hidden, F = p->shape.ffn;
   const size_t QD = (size_t)p->shape.n_q_heads * p->shape.head_dim;
   p->max_chunks = (p->max_pages * p->shape.page_size + p->opts.kv_chunk - 1) / p->opts.kv_chunk;
-  p->item_capacity = p->T * p->max_chunks;
+  p->item_capacity = p->T_cap * p->max_chunks;
   const size_t rec = nf::attn_partial_floats(p->shape.n_q_heads, p->shape.n_kv_heads,
                                              p->shape.head_dim);
-  NF_TRY(dalloc(&p->d_q_lens, p->n_seq * 4));
-  NF_TRY(dalloc(&p->d_tok_begin, (p->n_seq + 1) * 4));
+  NF_TRY(dalloc(&p->d_q_lens, p->seq_cap * 4));
+  NF_TRY(dalloc(&p->d_tok_begin, (p->seq_cap + 1) * 4));
   NF_TRY(dalloc(&p->d_seg_bounds, (NF_MAX_NANO + 1) * 4));
   NF_TRY(dalloc(&p->tok_seq, T * 4));
   NF_TRY(dalloc(&p->tok_pos, T * 4));
@@ -987,7 +993,7 @@ namespace {
 // Activation buffers and one split-KV counter set per layer for a run of
 // n_layers layers (allocates, and synchronizes the device, only when it grows).
 nf_status ensure_layers(nf_plan p, int n_layers) {
-  const size_t xb = (size_t)p->T * p->shape.hidden * 2;
+  const size_t xb = (size_t)p->T_cap * p->shape.hidden * 2;
   if (!p->xa) {
     NF_TRY(dalloc(&p->xa, xb));
     NF_TRY(dalloc(&p->xb, xb));
@@ -999,7 +1005,7 @@ nf_status ensure_layers(nf_plan p, int n_layers) {
     p->fetch = nullptr;
     p->row_done = nullptr;
     NF_TRY(dalloc(&p->fetch, (size_t)NF_MAX_NANO * n_layers * 4));
-    NF_TRY(dalloc(&p->row_done, (size_t)p->T * p->shape.n_kv_heads * n_layers * 4));
+    NF_TRY(dalloc(&p->row_done, (size_t)p->T_cap * p->shape.n_kv_heads * n_layers * 4));
     p->counter_sets = n_layers;
   }
   return NF_OK;
@@ -1099,11 +1105,11 @@ nf_status nf_layer_step_host(nf_plan p, const nf_layer_weights* w, const void* x
     return fail(NF_ERR_INVALID_ARG, "a host pointer is NULL");
   const size_t xb = (size_t)p->T * p->shape.hidden * 2;
   const size_t btb = (size_t)p->n_seq * p->max_pages * 4, slb = (size_t)p->n_seq * 4;
-  if (!p->x_stage) {
-    NF_TRY(dalloc(&p->x_stage, xb));
-    NF_TRY(dalloc(&p->y_stage, xb));
-    NF_TRY(dalloc(&p->bt_stage, btb));
-    NF_TRY(dalloc(&p->sl_stage, slb));
+  if (!p->x_stage) {  // sized for the plan's capacity
+    NF_TRY(dalloc(&p->x_stage, (size_t)p->T_cap * p->shape.hidden * 2));
+    NF_TRY(dalloc(&p->y_stage, (size_t)p->T_cap * p->shape.hidden * 2));
+    NF_TRY(dalloc(&p->bt_stage, (size_t)p->seq_cap * p->max_pages * 4));
+    NF_TRY(dalloc(&p->sl_stage, (size_t)p->seq_cap * 4));
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   NF_CUDA(cudaMemcpyAsync(p->x_stage, x_host, xb, cudaMemcpyHostToDevice, st));
@@ -1113,6 +1119,75 @@ nf_status nf_layer_step_host(nf_plan p, const nf_layer_weights* w, const void* x
   NF_TRY(layer_step(p, w, p->x_stage, k_pool, v_pool, p->bt_stage, p->sl_stage, p->y_stage, st));
   NF_CUDA(cudaMemcpyAsync(y_host, p->y_stage, xb, cudaMemcpyDeviceToHost, st));
   NF_CUDA(cudaStreamSynchronize(st));
+  return NF_OK;
+}
+
+nf_status nf_plan_set_batch(nf_plan p, const nf_batch_desc* b, const nf_plan_opts* opts,
+                            void* stream) {
+  if (!p || !b) return fail(NF_ERR_INVALID_ARG, "plan or batch is NULL");
+  const int n_seq = b->n_decode + b->n_prefill;
+  if (b->n_decode < 0 || b->n_prefill < 0 || n_seq < 1 || n_seq > p->seq_cap)
+    return fail(NF_ERR_INVALID_ARG, "the batch must hold 1 ... %d sequences (got %d)", p->seq_cap,
+                n_seq);
+  if (b->n_prefill > 0 && !b->prefill_q_lens) return fail(NF_ERR_INVALID_ARG, "prefill_q_lens is NULL");
+  if (b->max_pages_per_seq != p->max_pages || b->num_pages != p->num_pages)
+    return fail(NF_ERR_INVALID_ARG, "max_pages_per_seq and num_pages must stay as created");
+  std::vector<int> q_lens, tok_begin{0}, prefill_q;
+  for (int i = 0; i < n_seq; ++i) {
+    const int q = i < b->n_decode ? 1 : b->prefill_q_lens[i - b->n_decode];
+    if (q < 1) return fail(NF_ERR_INVALID_ARG, "prefill_q_lens[%d] must be >= 1", i - b->n_decode);
+    if (i >= b->n_decode) prefill_q.push_back(q);
+    q_lens.push_back(q);
+    tok_begin.push_back(tok_begin.back() + q);
+  }
+  const int T = tok_begin.back();
+  if (T > p->T_cap)
+    return fail(NF_ERR_INVALID_ARG, "the batch holds %d tokens, the plan at most %d", T, p->T_cap);
+  nf_plan_opts o = p->opts;
+  if (opts) {
+    o = *opts;
+    if (o.kv_chunk == 0) o.kv_chunk = p->opts.kv_chunk;
+    if (o.timeout_ns == 0) o.timeout_ns = p->opts.timeout_ns;
+    if (o.attn_warps == 0) o.attn_warps = p->opts.attn_warps;
+    if (o.gemm_stages == 0) o.gemm_stages = p->opts.gemm_stages;
+    if (o.attn_impl == NF_ATTN_AUTO) o.attn_impl = p->opts.attn_impl;
+    if (o.kv_chunk != p->opts.kv_chunk || o.attn_impl != p->opts.attn_impl ||
+        o.attn_warps != p->opts.attn_warps)
+      return fail(NF_ERR_INVALID_ARG,
+                  "kv_chunk, attn_impl and attn_warps must stay as the plan was created");
+  } else if (T != p->T) {  // the old split does not fit: one nano-batch
+    o.n_attn = o.n_ffn = 1;
+    o.attn_bounds[0] = o.ffn_bounds[0] = 0;
+    o.attn_bounds[1] = o.ffn_bounds[1] = T;
+    o.executor = NF_EXEC_SEQUENTIAL;
+  }
+  NF_TRY(check_opts(&o, T, p->num_sms));
+  if (!p->set_stage)
+    NF_CUDA(cudaHostAlloc(&p->set_stage, 2 * (2 * (size_t)p->seq_cap + 2 + NF_MAX_NANO + 1) * 4,
+                          cudaHostAllocDefault));
+  // Two halves, used alternately: a copy enqueued by the previous call may still
+  // be pending when this one writes.
+  int* h = p->set_stage + p->set_flip * (2 * p->seq_cap + 2 + NF_MAX_NANO + 1);
+  p->set_flip ^= 1;
+  std::copy(q_lens.begin(), q_lens.end(), h);
+  std::copy(tok_begin.begin(), tok_begin.end(), h + p->seq_cap);
+  std::copy(o.attn_bounds, o.attn_bounds + o.n_attn + 1, h + 2 * p->seq_cap + 1);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  NF_CUDA(cudaMemcpyAsync(p->d_q_lens, h, n_seq * 4, cudaMemcpyHostToDevice, st));
+  NF_CUDA(cudaMemcpyAsync(p->d_tok_begin, h + p->seq_cap, (n_seq + 1) * 4, cudaMemcpyHostToDevice,
+                          st));
+  NF_CUDA(cudaMemcpyAsync(p->d_seg_bounds, h + 2 * p->seq_cap + 1, (o.n_attn + 1) * 4,
+                          cudaMemcpyHostToDevice, st));
+  p->n_decode = b->n_decode;
+  p->n_prefill = b->n_prefill;
+  p->n_seq = n_seq;
+  p->T = T;
+  p->q_lens = q_lens;
+  p->tok_begin = tok_begin;
+  p->prefill_q = prefill_q;
+  p->seq_hint.clear();
+  if (b->seq_lens_hint) p->seq_hint.assign(b->seq_lens_hint, b->seq_lens_hint + n_seq);
+  p->opts = o;
   return NF_OK;
 }
 

@@ -1,0 +1,114 @@
+"""The runtime on the GPU, and a plan following a changing batch.
+
+The runtime test uses a model whose greedy output is known exactly: every
+layer's projection matrices are zero, so a layer passes its input through
+(h = x, y = h), and the LM head is the embedding shifted by one row, so the
+largest logit of token t is t + 1 (a row's product with itself dominates its
+products with the other random rows).  A request's outputs must then be
+last_prompt_token + 1, + 2, ... (mod vocab): any slip in the token plumbing
+(prompt rows, a decode row's previous output kept on the device, sampling,
+read-back, end token) changes them."""
+import numpy as np
+import pytest
+import torch
+
+from nano_intra_device_gb300 import _lib, workload as wl
+from oracle import layer as orc
+from tests.helpers import compare, f64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def test_plan_follows_a_smaller_batch():
+    """One plan, created for a larger batch, runs a different structure after
+    nf_plan_set_batch (fewer tokens, other prefill chunks) and matches the
+    oracle; then switches back."""
+    shape = wl.tiny_shape()
+    big = wl.make_batch(shape, [17, 33, 48, 64, 20, 9], [32, 12], None, seed_bt=3, max_pages=8)
+    small = wl.make_batch(shape, [5, 40], [7], None, seed_bt=4, max_pages=8)
+    small.num_pages = big.num_pages  # one pool for both
+    plan = _lib.Plan(shape, big, _lib.make_opts(big.n_tokens, [0, 20, big.n_tokens],
+                                                executor=_lib.NF_EXEC_STREAMS, attn_sms=24,
+                                                kv_chunk=32))
+    w = wl.make_weights(shape, seed=5, gain_std=0.1)
+    wd = {k: v.to(DEV) for k, v in w.items()}
+    for batch, opts in ((small, None),
+                        (small, _lib.make_opts(small.n_tokens, [0, 4, small.n_tokens],
+                                               executor=_lib.NF_EXEC_STREAMS, attn_sms=24,
+                                               kv_chunk=32)),
+                        (big, None)):
+        kp, vp = wl.make_pools(shape, batch, DEV, seed=6)
+        x = wl.make_x(shape, batch.n_tokens, seed=7)
+        ref = orc.layer_step(shape, orc.weights_f64(w), x, kp, vp, batch.block_table,
+                             batch.seq_lens, batch.q_lens)
+        plan.set_batch(batch, opts)
+        y = torch.empty(batch.n_tokens, shape.hidden, dtype=torch.bfloat16, device=DEV)
+        _lib.layer_step(plan, wd, x.to(DEV), kp, vp, torch.from_numpy(batch.block_table).to(DEV),
+                        torch.from_numpy(batch.seq_lens).to(DEV), y)
+        plan.poll()
+        assert plan.info()[1] == batch.n_tokens
+        compare(f64(y), ref["y"], f"y after set_batch ({batch.n_tokens} tokens)")
+    with pytest.raises(_lib.NanoflowError):       # more tokens than the plan holds
+        plan.set_batch(wl.make_batch(shape, [4] * 60, [], None, max_pages=8))
+    plan.close()
+
+
+def _successor_model(shape, n_layers, vocab):
+    g = torch.Generator().manual_seed(1)
+    H = shape.hidden
+    embed = torch.randn(vocab, H, generator=g).to(torch.bfloat16)
+    lm_head = torch.roll(embed, shifts=1, dims=0)          # lm_head[v] = embed[v - 1]
+    norm_f = torch.ones(H, dtype=torch.bfloat16)
+    layers = []
+    for i in range(n_layers):
+        w = wl.make_weights(shape, seed=10 + i)
+        layers.append({k: (torch.zeros_like(v) if k.startswith("w_") else v).to(DEV)
+                       for k, v in w.items()})
+    return embed.to(DEV), norm_f.to(DEV), lm_head.to(DEV), layers
+
+
+@pytest.mark.parametrize("replan", [0.1, -1.0])
+def test_runtime_serves_requests_end_to_end(replan):
+    shape = wl.tiny_shape()
+    vocab, L, b_dense, max_pages, num_pages = 96, 2, 40, 8, 64
+    embed, norm_f, lm_head, layers = _successor_model(shape, L, vocab)
+    pools = [(torch.zeros(num_pages, shape.n_kv, 16, shape.head_dim, dtype=torch.bfloat16, device=DEV),
+              torch.zeros(num_pages, shape.n_kv, 16, shape.head_dim, dtype=torch.bfloat16, device=DEV))
+             for _ in range(L)]
+    sa = _lib.StackArgs(embed, norm_f, lm_head, layers, pools)
+    eos = 70
+    rt = _lib.Runtime(shape, b_dense, 8, max_pages, num_pages, vocab, eos_token=eos,
+                      replan_threshold=replan)
+    rng = np.random.default_rng(2)
+    reqs = []
+    for i in range(14):
+        plen = int(rng.integers(1, 60))
+        prompt = rng.integers(0, vocab, plen).tolist()
+        if i == 3:
+            prompt[-1] = 66          # outputs 67, 68, 69, 70 = end token
+        mn = int(rng.integers(1, 30))
+        reqs.append((rt.submit(prompt, mn), prompt, mn))
+    stream = torch.cuda.current_stream()
+    replanned, sizes = 0, []
+    for _ in range(500):
+        b = rt.step(sa, stream)
+        if b["n_tokens"] == 0:
+            break
+        replanned += b["replanned"]
+        sizes.append(b["n_tokens"])
+    rt.sync()
+    for rid, prompt, mn in reqs:
+        fin, toks = rt.result(rid)
+        expect = [(prompt[-1] + 1 + i) % vocab for i in range(mn)]
+        if eos in expect:
+            expect = expect[: expect.index(eos) + 1]
+        assert fin, rid
+        assert toks == expect, (rid, toks, expect)
+    assert rt.counts() == (0, 0, num_pages)
+    assert max(sizes) == b_dense
+    if replan >= 0:
+        assert replanned >= 2      # the mix moved from prompts to decoding
+    else:
+        assert replanned == 0
+    rt.close()
