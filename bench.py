@@ -57,11 +57,12 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-ablation", action="store_true")
     ap.add_argument("--plan", default="auto", help="auto | search | n=<k>,sms=<s>")
-    ap.add_argument("--workload", default="layer", choices=["layer", "stack", "70b", "moe"],
+    ap.add_argument("--workload", default="layer", choices=["layer", "stack", "70b", "moe", "serve"],
                     help="layer: the single 8B-shaped layer step (default); stack: the 32-layer "
                          "8B-shaped stack with embedding and LM head, decode batches; 70b: ten "
                          "70B-shaped layers over a 4096-token mixed step; moe: one Mixtral-shaped "
-                         "layer (8 experts, top-2) over a 2048-token mixed step")
+                         "layer (8 experts, top-2) over a 2048-token mixed step; serve: the "
+                         "runtime serving synthetic requests on the 32-layer 8B-shaped stack")
     ap.add_argument("--batch", type=int, default=256, help="decode requests of the stack workload")
     return ap.parse_args()
 
@@ -476,6 +477,84 @@ def run_moe(args):
     plan.close()
 
 
+def run_serve(args):
+    """The runtime (batch formation, async scheduling, pages, re-planning) serving
+    synthetic requests on the 32-layer 8B-shaped stack with a 128256-token
+    vocabulary: prompts lognormal (median 512, sigma 1, clip [16, 4096]), outputs
+    lognormal (median 200, sigma 0.7, clip [16, 1024]), enough requests queued
+    that every iteration is full.  After warm-up iterations, args.steps
+    iterations are timed (host and device, the runtime's own loop)."""
+    from nano_intra_device_gb300 import _lib
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    shape = wl.llama8b_shape()
+    L, vocab, B = 32, 128256, 2048
+    max_requests, max_pages, num_pages = 768, 320, 40000
+    g = torch.Generator(device=dev).manual_seed(0)
+
+    def rn(*sz, std=0.02):
+        return (torch.randn(*sz, generator=g, device=dev) * std).to(torch.bfloat16)
+    H, F = shape.hidden, shape.ffn
+    layers = [{"w_qkv": rn(shape.qkv_rows, H), "w_o": rn(H, shape.n_q * shape.head_dim),
+               "w_gate_up": rn(2 * F, H), "w_down": rn(H, F),
+               "norm1": torch.ones(H, dtype=torch.bfloat16, device=dev),
+               "norm2": torch.ones(H, dtype=torch.bfloat16, device=dev)} for _ in range(L)]
+    embed, lm_head = rn(vocab, H, std=1.0), rn(vocab, H)
+    norm_f = torch.ones(H, dtype=torch.bfloat16, device=dev)
+    pools = [(torch.zeros(num_pages, shape.n_kv, 16, shape.head_dim, dtype=torch.bfloat16, device=dev),
+              torch.zeros(num_pages, shape.n_kv, 16, shape.head_dim, dtype=torch.bfloat16, device=dev))
+             for _ in range(L)]
+    sa = _lib.StackArgs(embed, norm_f, lm_head, layers, pools)
+    rt = _lib.Runtime(shape, B, max_requests, max_pages, num_pages, vocab, eos_token=-1,
+                      replan_threshold=0.1)
+    rng = np.random.default_rng(5)
+    n_req = 3000
+    plens = np.clip(np.round(np.exp(np.log(512) + rng.standard_normal(n_req))), 16, 4096).astype(int)
+    olens = np.clip(np.round(np.exp(np.log(200) + 0.7 * rng.standard_normal(n_req))), 16, 1024).astype(int)
+    for pl, ol in zip(plens, olens):
+        rt.submit(rng.integers(0, vocab, int(pl)).tolist(), int(ol))
+    stream = torch.cuda.current_stream()
+    # warm-up long enough for the admitted requests to finish their prompts, so
+    # that the timed iterations see the steady decode share
+    warm = max(args.warmup, 400)
+    for _ in range(warm):
+        rt.step(sa, stream)
+    torch.cuda.synchronize()
+    clocks = Clocks()
+    clocks.start()
+    t0 = time.perf_counter()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    tok = dec = replans = full = 0
+    for _ in range(args.steps):
+        b = rt.step(sa, stream)
+        tok += b["n_tokens"]
+        dec += b["n_decode"]
+        replans += b["replanned"]
+        full += b["n_tokens"] == B
+    e1.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    clk = clocks.stop()
+    rt.sync()
+    dev_s = e0.elapsed_time(e1) * 1e-3
+    waiting, active, free_pages = rt.counts()
+    line = {"metric": "serving-loop tokens/s (runtime + 32-layer 8B-shaped stack, greedy decode)",
+            "value": tok / wall, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": warm, "ms_per_step": wall / args.steps * 1e3,
+            "higher_is_better": True, "dtype": "bf16", "data": "synthetic", "clocks": clk,
+            "config": {"workload": f"runtime, b_dense {B}, {L} layers, vocab {vocab}, {n_req} queued "
+                                   "requests: prompts lognormal median 512 sigma 1 clip [16,4096], "
+                                   "outputs lognormal median 200 sigma 0.7 clip [16,1024]",
+                       "max_requests": max_requests, "num_pages": num_pages},
+            "decode_tokens_per_s": dec / wall, "device_ms_per_step": dev_s / args.steps * 1e3,
+            "full_iterations": full, "replans": replans,
+            "state_after": {"waiting": waiting, "active": active, "free_pages": free_pages}}
+    print(json.dumps(line), flush=True)
+    rt.close()
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -486,6 +565,8 @@ def main():
         return run_70b(args)
     if args.workload == "moe":
         return run_moe(args)
+    if args.workload == "serve":
+        return run_serve(args)
     from nano_intra_device_gb300 import _lib
 
     rank, world, local = dist_setup(args.gpus)
