@@ -108,6 +108,7 @@ struct nf_plan_s {
   int n_seq = 0, T = 0;         // the current batch (nf_plan_set_batch may change it)
   int seq_cap = 0, T_cap = 0;   // what the workspace was allocated for
   int* set_stage = nullptr;     // pinned host staging of nf_plan_set_batch (two halves)
+  float2* rope_cs = nullptr;    // RoPE (cos, sin) table [max_pages * page_size][head_dim / 2]
   int set_flip = 0;
   std::vector<int> q_lens, tok_begin;
   nf_plan_opts opts{};
@@ -282,7 +283,7 @@ void free_plan(nf_plan p) {
                   p->partials, p->status, p->n1, p->q, p->o, p->h, p->n2, p->a, p->x_stage,
                   p->y_stage, p->bt_stage, p->sl_stage, p->xa, p->xb, p->gemm_part,
                   p->gemm_cnt, p->moe_off, p->moe_perm, p->moe_pair_row, p->moe_pair_w,
-                  p->moe_a, p->moe_act, p->moe_out};
+                  p->moe_a, p->moe_act, p->moe_out, p->rope_cs};
   for (void* b : bufs)
     if (b) cudaFree(b);
   if (p->set_stage) cudaFreeHost(p->set_stage);
@@ -357,6 +358,20 @@ nf_status alloc_plan(nf_plan p) {
     if (!nf::make_tmap_bf16(&p->tm_moe_a, p->moe_a, R, H, 128) ||
         !nf::make_tmap_bf16(&p->tm_moe_act, p->moe_act, R, F, 128))
       return fail(NF_ERR_CUDA, "tensor map creation failed");
+  }
+  {  // RoPE table for every position a sequence can reach, in double precision
+    const int npos = p->max_pages * p->shape.page_size, half = p->shape.head_dim / 2;
+    std::vector<float> cs((size_t)npos * half * 2);
+    for (int i = 0; i < half; ++i) {
+      const double inv = std::pow((double)p->shape.rope_theta, -2.0 * i / p->shape.head_dim);
+      for (int pos = 0; pos < npos; ++pos) {
+        const double ang = pos * inv;
+        cs[((size_t)pos * half + i) * 2] = (float)std::cos(ang);
+        cs[((size_t)pos * half + i) * 2 + 1] = (float)std::sin(ang);
+      }
+    }
+    NF_TRY(dalloc(&p->rope_cs, cs.size() * 4));
+    NF_CUDA(cudaMemcpy(p->rope_cs, cs.data(), cs.size() * 4, cudaMemcpyHostToDevice));
   }
   NF_TRY(dalloc(&p->gemm_part, kSplitPartBytes));
   NF_TRY(dalloc(&p->gemm_cnt, kSplitMaxTiles * 4));
@@ -537,6 +552,8 @@ GemmArgs base_args(nf_plan p) {
   g.head_dim = p->shape.head_dim;
   g.page_size = p->shape.page_size;
   g.log2_theta = std::log2(p->shape.rope_theta);
+  g.rope_cs = p->rope_cs;
+  g.rope_positions = p->max_pages * p->shape.page_size;
   return g;
 }
 

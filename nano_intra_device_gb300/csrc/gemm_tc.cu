@@ -462,15 +462,30 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               fetch32(hb + j0, v);
               fetch32(hb + d / 2 + j0, w);
               if (dst != nullptr) {
+                if (pos < args.rope_positions) {  // table of (cos, sin), 16-byte loads
+                  const float4* cs = reinterpret_cast<const float4*>(
+                      args.rope_cs + static_cast<size_t>(pos) * (d / 2) + j0);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                  // angle = pos * theta^(-2 i / d)
-                  const float inv_freq = exp2f(-(2.0f * (j0 + i) / d) * args.log2_theta);
-                  float s, c;
-                  sincosf(static_cast<float>(pos) * inv_freq, &s, &c);
-                  const float a = v[i], b = w[i];
-                  v[i] = a * c - b * s;
-                  w[i] = b * c + a * s;
+                  for (int i2 = 0; i2 < 16; ++i2) {
+                    const float4 t = __ldg(cs + i2);
+                    const float a0 = v[2 * i2], b0 = w[2 * i2];
+                    const float a1 = v[2 * i2 + 1], b1 = w[2 * i2 + 1];
+                    v[2 * i2] = a0 * t.x - b0 * t.y;
+                    w[2 * i2] = b0 * t.x + a0 * t.y;
+                    v[2 * i2 + 1] = a1 * t.z - b1 * t.w;
+                    w[2 * i2 + 1] = b1 * t.z + a1 * t.w;
+                  }
+                } else {
+#pragma unroll
+                  for (int i = 0; i < 32; ++i) {
+                    // angle = pos * theta^(-2 i / d)
+                    const float inv_freq = exp2f(-(2.0f * (j0 + i) / d) * args.log2_theta);
+                    float s, c;
+                    sincosf(static_cast<float>(pos) * inv_freq, &s, &c);
+                    const float a = v[i], b = w[i];
+                    v[i] = a * c - b * s;
+                    w[i] = b * c + a * s;
+                  }
                 }
                 store32_bf16(dst + j0, v);
                 store32_bf16(dst + d / 2 + j0, w);

@@ -28,6 +28,11 @@ struct GemmArgs {
   __nv_bfloat16* v_pool;
   int n_q, n_kv, head_dim, page_size;
   float log2_theta;
+  // RoPE table: (cos, sin) of pos * theta^(-2i/d) at [pos][i], i < d/2, for
+  // positions below rope_positions (computed in double precision on the host);
+  // positions past it fall back to sincosf
+  const float2* rope_cs;
+  int rope_positions;
   int stages;           // ring stages: 4 (fills an SM), 3 or 2 (room for attention)
   // split-K (for few output tiles): each tile's K range is cut into `splits`
   // pieces on different CTAs; fp32 partials in `part` [tiles][splits][128][BN],
