@@ -134,9 +134,11 @@ struct nf_plan_s {
   // (a stack reuses one plan for all its layers)
   const void* wkey[4] = {nullptr, nullptr, nullptr, nullptr};
   CUtensorMap tm_wqkv{}, tm_wo{}, tm_wg{}, tm_wu{}, tm_wd{};
+  CUtensorMap tm_wo224{}, tm_wd224{};  // the same with 224-row boxes (224-column tiles)
   struct WeightMaps {
     const void* key[4];
     CUtensorMap qkv, o, g, u, d;  // a MoE layer keeps its expert maps in g (gate/up) and d
+    CUtensorMap o224, d224;
   };
   std::vector<WeightMaps> wcache;
   // mixture of experts: routing, grouped rows and the expert weight maps
@@ -502,6 +504,8 @@ nf_status refresh_weight_maps(nf_plan p, const nf_layer_weights* w) {
       p->tm_wg = c.g;
       p->tm_wu = c.u;
       p->tm_wd = c.d;
+      p->tm_wo224 = c.o224;
+      p->tm_wd224 = c.d224;
       std::memcpy(p->wkey, key, sizeof(key));
       return NF_OK;
     }
@@ -510,7 +514,8 @@ nf_status refresh_weight_maps(nf_plan p, const nf_layer_weights* w) {
   const uint64_t H = s.hidden, F = s.ffn, QD = (uint64_t)s.n_q_heads * s.head_dim;
   const uint64_t NQKV = (uint64_t)(s.n_q_heads + 2 * s.n_kv_heads) * s.head_dim;
   if (!nf::make_tmap_bf16(&p->tm_wqkv, w->w_qkv, NQKV, H, 256) ||
-      !nf::make_tmap_bf16(&p->tm_wo, w->w_o, H, QD, 256))
+      !nf::make_tmap_bf16(&p->tm_wo, w->w_o, H, QD, 256) ||
+      !nf::make_tmap_bf16(&p->tm_wo224, w->w_o, H, QD, 224))
     return fail(NF_ERR_INVALID_ARG, "weight tensor maps: pointers must be 16-byte aligned");
   if (moe) {  // one map over every expert's rows: [E * 2F, H] and [E * H, F]
     const uint64_t E = p->shape.n_experts;
@@ -522,7 +527,8 @@ nf_status refresh_weight_maps(nf_plan p, const nf_layer_weights* w) {
     const char* up = static_cast<const char*>(w->w_gate_up) + F * H * 2;
     if (!nf::make_tmap_bf16(&p->tm_wg, w->w_gate_up, F, H, 128) ||
         !nf::make_tmap_bf16(&p->tm_wu, up, F, H, 128) ||
-        !nf::make_tmap_bf16(&p->tm_wd, w->w_down, H, F, 256))
+        !nf::make_tmap_bf16(&p->tm_wd, w->w_down, H, F, 256) ||
+        !nf::make_tmap_bf16(&p->tm_wd224, w->w_down, H, F, 224))
       return fail(NF_ERR_INVALID_ARG, "weight tensor maps: pointers must be 16-byte aligned");
   }
   std::memcpy(p->wkey, key, sizeof(key));
@@ -534,6 +540,8 @@ nf_status refresh_weight_maps(nf_plan p, const nf_layer_weights* w) {
     c.g = p->tm_wg;
     c.u = p->tm_wu;
     c.d = p->tm_wd;
+    c.o224 = p->tm_wo224;
+    c.d224 = p->tm_wd224;
     p->wcache.push_back(c);
   }
   return NF_OK;
@@ -558,6 +566,19 @@ GemmArgs base_args(nf_plan p) {
 }
 
 int cap_grid(int tiles, int cap) { return tiles < cap ? tiles : cap; }
+
+// Output columns per tile for a residual GEMM of m_tiles row tiles and N
+// columns on `grid` CTAs: 224 when that turns a partial last wave into fewer
+// tile-widths of work (256 tiles on 152 SMs take 2 rounds of 256 columns; 304
+// tiles of 224 columns take 2 rounds of 224), else 256.
+int pick_bn(int m_tiles, int N, int grid) {
+  auto work = [&](int bn) {
+    const int tiles = m_tiles * ((N + bn - 1) / bn);
+    return (double)((tiles + grid - 1) / grid) * bn;
+  };
+  if (m_tiles * ((N + 255) / 256) * 2 <= grid) return 256;  // few tiles: split-K territory
+  return work(224) < work(256) ? 224 : 256;
+}
 
 
 cudaEvent_t pooled_event(nf_plan p) {
@@ -720,8 +741,11 @@ nf_status run_oproj(nf_plan p, const void* x, int r0, int r1, int grid, cudaStre
   g.ldc = s.hidden;
   g.R = static_cast<const __nv_bfloat16*>(x);
   g.ldr = s.hidden;
+  g.bn = pick_bn(g.m_tiles, g.N, grid);
+  g.n_tiles = (g.N + g.bn - 1) / g.bn;
   g.splits = p->opts.gemm_split_k ? 1 : choose_splits(g.m_tiles * g.n_tiles, g.K, grid);
-  NF_CUDA(nf::launch_gemm(nf::EPI_RESID, p->tm_o, p->tm_wo, p->tm_wo, g,
+  const CUtensorMap& wo = g.bn == 224 ? p->tm_wo224 : p->tm_wo;
+  NF_CUDA(nf::launch_gemm(nf::EPI_RESID, p->tm_o, wo, wo, g,
                           cap_grid(g.m_tiles * g.n_tiles * g.splits, grid), st));
   return NF_OK;
 }
@@ -794,8 +818,11 @@ nf_status run_ffn(nf_plan p, const nf_layer_weights* w, void* y, int r0, int r1,
   d.ldc = s.hidden;
   d.R = p->h;
   d.ldr = s.hidden;
+  d.bn = pick_bn(d.m_tiles, d.N, grid);
+  d.n_tiles = (d.N + d.bn - 1) / d.bn;
   d.splits = p->opts.gemm_split_k ? 1 : choose_splits(d.m_tiles * d.n_tiles, d.K, grid);
-  NF_CUDA(nf::launch_gemm(nf::EPI_RESID, p->tm_a, p->tm_wd, p->tm_wd, d,
+  const CUtensorMap& wd = d.bn == 224 ? p->tm_wd224 : p->tm_wd;
+  NF_CUDA(nf::launch_gemm(nf::EPI_RESID, p->tm_a, wd, wd, d,
                           cap_grid(d.m_tiles * d.n_tiles * d.splits, grid), st));
   return NF_OK;
 }

@@ -17,18 +17,21 @@
 
 namespace nf {
 
-constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int BM = 128, BK = 64;
+constexpr int BN_DEFAULT = 256;     // output columns of a tile (224 for the O / down
+                                    // projections when it turns a partial last wave into
+                                    // whole ones)
 constexpr int MAX_STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = BN * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int TMEM_COLS = 2 * BN;
+constexpr int TMEM_COLS = 512;      // two accumulators of up to 256 columns
 constexpr int GEMM_THREADS = 192;
-// Dynamic shared memory of a CTA with `stages` ring stages: the ring, slack to
-// align it to 1024 bytes, and the barrier block.  4 stages fill an SM (one CTA
-// per SM, exclusive); 3 or 2 leave room for an attention CTA beside it.
-constexpr int gemm_smem_bytes(int stages) { return stages * STAGE_BYTES + 1024 + 640; }
-constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+// Dynamic shared memory of a CTA with `stages` ring stages of `bn`-column B
+// tiles: the ring, slack to align it to 1024 bytes, and the barrier block.  4
+// stages fill an SM (one CTA per SM, exclusive); 3 or 2 leave room for an
+// attention CTA beside it.
+constexpr int gemm_smem_bytes(int stages, int bn) {
+  return stages * (A_BYTES + bn * BK * 2) + 1024 + 640;
+}
 
 struct GemmSmemTail {
   uint64_t full[MAX_STAGES];
@@ -93,10 +96,14 @@ __device__ __forceinline__ void tmem_load32(uint32_t taddr, float* v) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-template <int EPI, int STAGES>
+template <int EPI, int STAGES, int BN>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmB2, const GemmArgs args) {
+  constexpr int B_BYTES = BN * BK * 2;
+  constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+  static_assert(BN % 32 == 0 && BN <= 256, "tile width");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -517,37 +524,37 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   }
 }
 
-int gemm_block_n(int epi) { return epi == EPI_SWIGLU ? BN / 2 : BN; }
+int gemm_block_n(int epi) { return epi == EPI_SWIGLU ? BN_DEFAULT / 2 : BN_DEFAULT; }
 
 int gemm_tiles(int epi, int m_rows, int N) {
   const int bn = gemm_block_n(epi);
   return ((m_rows + BM - 1) / BM) * ((N + bn - 1) / bn);
 }
 
-template <int EPI, int STAGES>
+template <int EPI, int STAGES, int BN>
 static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB,
                               const CUtensorMap& tmB2, const GemmArgs& args, int grid,
                               cudaStream_t stream) {
   static bool attr_set = false;  // per process; the attribute is per function
-  constexpr int smem = gemm_smem_bytes(STAGES);
+  constexpr int smem = gemm_smem_bytes(STAGES, BN);
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI, STAGES>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI, STAGES, BN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  gemm_tc_kernel<EPI, STAGES><<<grid, GEMM_THREADS, smem, stream>>>(tmA, tmB, tmB2, args);
+  gemm_tc_kernel<EPI, STAGES, BN><<<grid, GEMM_THREADS, smem, stream>>>(tmA, tmB, tmB2, args);
   return cudaGetLastError();
 }
 
-template <int EPI>
-static cudaError_t launch_epi(const CUtensorMap& tmA, const CUtensorMap& tmB,
-                              const CUtensorMap& tmB2, const GemmArgs& args, int grid,
-                              cudaStream_t stream) {
+template <int EPI, int BN>
+static cudaError_t launch_stages(const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                 const CUtensorMap& tmB2, const GemmArgs& args, int grid,
+                                 cudaStream_t stream) {
   switch (args.stages) {
-    case 2: return launch_one<EPI, 2>(tmA, tmB, tmB2, args, grid, stream);
-    case 3: return launch_one<EPI, 3>(tmA, tmB, tmB2, args, grid, stream);
-    default: return launch_one<EPI, 4>(tmA, tmB, tmB2, args, grid, stream);
+    case 2: return launch_one<EPI, 2, BN>(tmA, tmB, tmB2, args, grid, stream);
+    case 3: return launch_one<EPI, 3, BN>(tmA, tmB, tmB2, args, grid, stream);
+    default: return launch_one<EPI, 4, BN>(tmA, tmB, tmB2, args, grid, stream);
   }
 }
 
@@ -558,12 +565,18 @@ cudaError_t launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB,
   if (args.n_groups < 0 || args.n_groups > GEMM_MAX_GROUPS ||
       (args.n_groups > 0 && (!args.group_off || args.splits > 1)))
     return cudaErrorInvalidValue;
+  const int bn = args.bn ? args.bn : BN_DEFAULT;
+  if (bn == 224) {  // residual epilogue only (the O and down projections)
+    if (epi != EPI_RESID) return cudaErrorInvalidValue;
+    return launch_stages<EPI_RESID, 224>(tmA, tmB, tmB2, args, grid, stream);
+  }
+  if (bn != BN_DEFAULT) return cudaErrorInvalidValue;
   switch (epi) {
-    case EPI_STORE: return launch_epi<EPI_STORE>(tmA, tmB, tmB2, args, grid, stream);
-    case EPI_RESID: return launch_epi<EPI_RESID>(tmA, tmB, tmB2, args, grid, stream);
-    case EPI_SWIGLU: return launch_epi<EPI_SWIGLU>(tmA, tmB, tmB2, args, grid, stream);
-    case EPI_QKV: return launch_epi<EPI_QKV>(tmA, tmB, tmB2, args, grid, stream);
-    case EPI_STORE_F32: return launch_epi<EPI_STORE_F32>(tmA, tmB, tmB2, args, grid, stream);
+    case EPI_STORE: return launch_stages<EPI_STORE, 256>(tmA, tmB, tmB2, args, grid, stream);
+    case EPI_RESID: return launch_stages<EPI_RESID, 256>(tmA, tmB, tmB2, args, grid, stream);
+    case EPI_SWIGLU: return launch_stages<EPI_SWIGLU, 256>(tmA, tmB, tmB2, args, grid, stream);
+    case EPI_QKV: return launch_stages<EPI_QKV, 256>(tmA, tmB, tmB2, args, grid, stream);
+    case EPI_STORE_F32: return launch_stages<EPI_STORE_F32, 256>(tmA, tmB, tmB2, args, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }

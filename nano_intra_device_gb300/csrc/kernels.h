@@ -34,6 +34,7 @@ struct GemmArgs {
   const float2* rope_cs;
   int rope_positions;
   int stages;           // ring stages: 4 (fills an SM), 3 or 2 (room for attention)
+  int bn;               // output columns per tile: 0 or 256; 224 (residual epilogue only)
   // split-K (for few output tiles): each tile's K range is cut into `splits`
   // pieces on different CTAs; fp32 partials in `part` [tiles][splits][128][BN],
   // per-tile arrival counters `tile_cnt` (zero between launches)
