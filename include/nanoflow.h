@@ -128,8 +128,12 @@ typedef struct {
                          gemm_stages = 2 */
   int32_t gemm_stages; /* shared-memory ring stages of the GEMM kernel: 4 fills an SM;
                           2 lets an attention CTA of 4 or 5 warps run on the same SM (0 = 4) */
-  int32_t gemm_split_k; /* 0: split K across CTAs when a GEMM has fewer output tiles than
-                           half its SMs; 1: never split */
+  int32_t gemm_split_k; /* 0: a GEMM of at most 128 tokens runs the weight-row kernel (128
+                           output features x 64 or 128 tokens a tile, K split over the CTAs
+                           of a cluster, partial tiles summed in distributed shared memory);
+                           a larger one splits K across CTAs when it has fewer output tiles
+                           than half its SMs.  1: token-row tiles, never split.  2: token-row
+                           tiles, split as in 0 (no weight-row kernel) */
   int32_t attn_impl;  /* nf_attn_impl.  NF_ATTN_AUTO picks the FMA kernel for its own
                          attn_warps 5 and 16, else the tensor-core kernel where the shape
                          allows it; nf_plan_info reports the kernel chosen */
@@ -345,6 +349,19 @@ nf_status nf_rmsnorm(const void* x, const void* g, void* out, int32_t rows, int3
 typedef enum { NF_EPI_STORE = 0, NF_EPI_RESID = 1, NF_EPI_SWIGLU = 2 } nf_epilogue;
 nf_status nf_gemm(const void* A, const void* B, void* C, const void* R, int32_t M, int32_t N,
                   int32_t K, int32_t epilogue, int32_t max_sms, void* stream);
+
+/* The same product through the weight-row kernel that layer steps use for
+ * nano-operations of at most 128 tokens ("NanoFlow: Towards Optimal LLM
+ * Serving Throughput", "The Intra-Device Parallelism Mechanism": the dense
+ * projections): a tile is 128 rows of B (output columns) x 64 or 128 rows of
+ * A, and K is split over the `splits` CTAs of a thread-block cluster whose
+ * fp32 partial tiles are summed, in rank order, through distributed shared
+ * memory.  Arguments as nf_gemm, with 1 <= M <= 256, N a multiple of 8;
+ * splits 0 = chosen from the shape, else 1 .. 8 and at most ceil(K / 64).
+ * No workspace: calls may run concurrently. */
+nf_status nf_gemm_wrows(const void* A, const void* B, void* C, const void* R, int32_t M,
+                        int32_t N, int32_t K, int32_t epilogue, int32_t splits, int32_t max_sms,
+                        void* stream);
 
 /* Copy one of the plan's device buffers (written by the last step or
  * metadata call on the plan's device) to dst (host or device), synchronously.

@@ -109,6 +109,8 @@ _SIGS = {
     "nf_attention_noalloc": (c_int, [POINTER(nf_model_shape), POINTER(nf_batch_desc), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     "nf_rmsnorm": (c_int, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_float, c_void_p]),
     "nf_gemm": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32, c_int32, c_void_p]),
+    "nf_gemm_wrows": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32,
+                              c_int32, c_int32, c_void_p]),
     "nf_plan_buffer_size": (c_int, [c_void_p, c_int32, POINTER(c_size_t)]),
     "nf_plan_copy_buffer": (c_int, [c_void_p, c_int32, c_void_p, c_size_t]),
     "nf_plan_trace_enable": (c_int, [c_void_p, c_int32]),
@@ -354,6 +356,14 @@ def gemm(A, B, C, R=None, epilogue=NF_EPI_STORE, max_sms=0, stream=None):
     N = C.shape[1]
     check(lib().nf_gemm(ptr(A), ptr(B), ptr(C), ptr(R), M, N, K, epilogue, max_sms,
                         stream_handle(stream)))
+
+
+def gemm_wrows(A, B, C, R=None, epilogue=NF_EPI_STORE, splits=0, max_sms=0, stream=None):
+    """nf_gemm_wrows: the weight-row kernel (M <= 128 rows of A)."""
+    M, K = A.shape
+    N = C.shape[1]
+    check(lib().nf_gemm_wrows(ptr(A), ptr(B), ptr(C), ptr(R), M, N, K, epilogue, splits, max_sms,
+                              stream_handle(stream)))
 
 
 def plan_search(shape, batch, profile_json=None, num_sms=152):

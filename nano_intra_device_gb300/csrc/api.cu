@@ -130,15 +130,21 @@ struct nf_plan_s {
   std::vector<cudaEvent_t> ev;
   // tensor maps over plan buffers (A operands)
   CUtensorMap tm_n1{}, tm_o{}, tm_n2{}, tm_a{};
+  // the same buffers with 64- and 128-row boxes: token tiles of the weight-row
+  // GEMM, indexed as XM_N1 ... XM_A
+  CUtensorMap tm_x64[4]{}, tm_x128[4]{};
   // tensor maps over the weights in use, and a cache of every weight set seen
   // (a stack reuses one plan for all its layers)
   const void* wkey[4] = {nullptr, nullptr, nullptr, nullptr};
   CUtensorMap tm_wqkv{}, tm_wo{}, tm_wg{}, tm_wu{}, tm_wd{};
   CUtensorMap tm_wo224{}, tm_wd224{};  // the same with 224-row boxes (224-column tiles)
+  // weight-row GEMM: QKV with head_dim / 2-row boxes, O and down with 128-row boxes
+  CUtensorMap tm_wqkv_h{}, tm_wo128{}, tm_wd128{};
   struct WeightMaps {
     const void* key[4];
     CUtensorMap qkv, o, g, u, d;  // a MoE layer keeps its expert maps in g (gate/up) and d
     CUtensorMap o224, d224;
+    CUtensorMap qkv_h, o128, d128;
   };
   std::vector<WeightMaps> wcache;
   // mixture of experts: routing, grouped rows and the expert weight maps
@@ -162,7 +168,7 @@ struct nf_plan_s {
   __nv_bfloat16 *xa = nullptr, *xb = nullptr;
   const void* lm_key = nullptr;
   int lm_vocab = 0;
-  CUtensorMap tm_lm{};
+  CUtensorMap tm_lm{}, tm_lm128{};
   // tracing
   struct TraceRec {
     int op, nano, step;
@@ -267,8 +273,9 @@ nf_status check_opts(const nf_plan_opts* o, int T, int num_sms) {
     return fail(NF_ERR_INVALID_ARG, "attn_warps must be 4 ... 8, 10, 12, 14 or 16");
   if (o->gemm_stages < 2 || o->gemm_stages > 4)
     return fail(NF_ERR_INVALID_ARG, "gemm_stages must be 2, 3 or 4");
-  if (o->gemm_split_k != 0 && o->gemm_split_k != 1)
-    return fail(NF_ERR_INVALID_ARG, "gemm_split_k must be 0 (automatic) or 1 (never)");
+  if (o->gemm_split_k < 0 || o->gemm_split_k > 2)
+    return fail(NF_ERR_INVALID_ARG,
+                "gemm_split_k must be 0 (automatic), 1 (never) or 2 (token-row tiles only)");
   if (o->attn_impl < NF_ATTN_AUTO || o->attn_impl > NF_ATTN_MMA)
     return fail(NF_ERR_INVALID_ARG, "attn_impl must be 0 (automatic), 1 (FMA) or 2 (MMA)");
   if (o->attn_impl == NF_ATTN_MMA && aw == 16)
@@ -394,6 +401,14 @@ nf_status alloc_plan(nf_plan p) {
       !nf::make_tmap_bf16(&p->tm_n2, p->n2, T, H, BMr) ||
       !nf::make_tmap_bf16(&p->tm_a, p->a, T, F, BMr))
     return fail(NF_ERR_CUDA, "tensor map creation failed (driver entry point missing?)");
+  {
+    const void* xb[4] = {p->n1, p->o, p->n2, p->a};
+    const uint64_t xc[4] = {H, QD, H, F};
+    for (int i = 0; i < 4; ++i)
+      if (!nf::make_tmap_bf16(&p->tm_x64[i], xb[i], T, xc[i], 64) ||
+          !nf::make_tmap_bf16(&p->tm_x128[i], xb[i], T, xc[i], 128))
+        return fail(NF_ERR_CUDA, "tensor map creation failed");
+  }
   return NF_OK;
 }
 
@@ -506,6 +521,9 @@ nf_status refresh_weight_maps(nf_plan p, const nf_layer_weights* w) {
       p->tm_wd = c.d;
       p->tm_wo224 = c.o224;
       p->tm_wd224 = c.d224;
+      p->tm_wqkv_h = c.qkv_h;
+      p->tm_wo128 = c.o128;
+      p->tm_wd128 = c.d128;
       std::memcpy(p->wkey, key, sizeof(key));
       return NF_OK;
     }
@@ -515,7 +533,9 @@ nf_status refresh_weight_maps(nf_plan p, const nf_layer_weights* w) {
   const uint64_t NQKV = (uint64_t)(s.n_q_heads + 2 * s.n_kv_heads) * s.head_dim;
   if (!nf::make_tmap_bf16(&p->tm_wqkv, w->w_qkv, NQKV, H, 256) ||
       !nf::make_tmap_bf16(&p->tm_wo, w->w_o, H, QD, 256) ||
-      !nf::make_tmap_bf16(&p->tm_wo224, w->w_o, H, QD, 224))
+      !nf::make_tmap_bf16(&p->tm_wo224, w->w_o, H, QD, 224) ||
+      !nf::make_tmap_bf16(&p->tm_wqkv_h, w->w_qkv, NQKV, H, s.head_dim / 2) ||
+      !nf::make_tmap_bf16(&p->tm_wo128, w->w_o, H, QD, 128))
     return fail(NF_ERR_INVALID_ARG, "weight tensor maps: pointers must be 16-byte aligned");
   if (moe) {  // one map over every expert's rows: [E * 2F, H] and [E * H, F]
     const uint64_t E = p->shape.n_experts;
@@ -528,7 +548,8 @@ nf_status refresh_weight_maps(nf_plan p, const nf_layer_weights* w) {
     if (!nf::make_tmap_bf16(&p->tm_wg, w->w_gate_up, F, H, 128) ||
         !nf::make_tmap_bf16(&p->tm_wu, up, F, H, 128) ||
         !nf::make_tmap_bf16(&p->tm_wd, w->w_down, H, F, 256) ||
-        !nf::make_tmap_bf16(&p->tm_wd224, w->w_down, H, F, 224))
+        !nf::make_tmap_bf16(&p->tm_wd224, w->w_down, H, F, 224) ||
+        !nf::make_tmap_bf16(&p->tm_wd128, w->w_down, H, F, 128))
       return fail(NF_ERR_INVALID_ARG, "weight tensor maps: pointers must be 16-byte aligned");
   }
   std::memcpy(p->wkey, key, sizeof(key));
@@ -542,6 +563,9 @@ nf_status refresh_weight_maps(nf_plan p, const nf_layer_weights* w) {
     c.d = p->tm_wd;
     c.o224 = p->tm_wo224;
     c.d224 = p->tm_wd224;
+    c.qkv_h = p->tm_wqkv_h;
+    c.o128 = p->tm_wo128;
+    c.d128 = p->tm_wd128;
     p->wcache.push_back(c);
   }
   return NF_OK;
@@ -578,6 +602,75 @@ int pick_bn(int m_tiles, int N, int grid) {
   };
   if (m_tiles * ((N + 255) / 256) * 2 <= grid) return 256;  // few tiles: split-K territory
   return work(224) < work(256) ? 224 : 256;
+}
+
+// Weight-row GEMM (gemm_wrows.cu) for nano-operations of few tokens: the
+// token tile, the cluster size (K splits) and the cluster count.  Measured on
+// GB300: one CTA streams weights at about 40 GB/s (a ring of 128 KB in
+// flight), the device as a whole at up to 6.4 TB/s, and each tile ends in an
+// exchange round of a few microseconds.  The time of a choice is the larger of
+// the per-CTA stream and the weight stream at min(HBM, CTAs x per-CTA rate),
+// plus one exchange per wave of tiles.  A cluster of several CTAs waits for its
+// slowest member at every tile, which measured far slower than the model when
+// clusters walk several tiles, so K is split only when every tile has its own
+// cluster.  Two-operand tiles (QKV, SwiGLU) with 128 tokens have a 3-stage
+// ring and lost to the token-row tiles: they take at most 64 tokens.
+constexpr int kWrMaxTokens = 128;       // larger nano-operations take token-row tiles
+constexpr int kWrMaxTokensDual = 64;
+constexpr double kWrSmRate = 40e9;      // weight bytes/s one CTA streams
+constexpr double kWrHbm = 6.4e12;       // weight bytes/s of the device
+constexpr double kWrExchange1 = 2.0e-6; // seconds of a tile's epilogue, cluster of one
+constexpr double kWrExchange = 4.0e-6;  // the same with an exchange between CTAs
+
+struct WrChoice {
+  int tok = 0, splits = 0, clusters = 0;  // splits = 0: not available
+};
+
+WrChoice wr_choose(int epi, int n_tok, int w_tiles, int K, int cap, int force_splits = 0) {
+  WrChoice best;
+  if (n_tok < 1 || n_tok > 256 || w_tiles < 1 || cap < 1) return best;
+  const int tok = n_tok <= 64 ? 64 : 128;
+  const int tiles = w_tiles * ((n_tok + tok - 1) / tok);
+  const int nk = (K + 63) / 64;
+  const double kb_bytes = (epi == nf::EPI_SWIGLU || epi == nf::EPI_QKV ? 2.0 : 1.0) * 128 * 64 * 2;
+  const double w_total = (double)w_tiles * nk * kb_bytes;  // a second token tile hits L2
+  double best_t = 1e30;
+  for (int sp = 1; sp <= 8 && sp <= nk; ++sp) {
+    if (force_splits > 0 && sp != force_splits) continue;
+    const int fit = nf::gemm_wrows_max_clusters(epi, tok, sp);
+    const int cl = std::min(tiles, std::min(fit, cap / sp));
+    if (cl < 1) continue;
+    const int waves = (tiles + cl - 1) / cl;
+    if (sp > 1 && waves > 1 && force_splits == 0) continue;
+    const double per_cta = (double)waves * ((nk + sp - 1) / sp) * kb_bytes;
+    const double rate = std::min(kWrHbm, (double)cl * sp * kWrSmRate);
+    const double t = std::max(per_cta / kWrSmRate, w_total / rate) +
+                     waves * (sp > 1 ? kWrExchange : kWrExchange1);
+    if (t < best_t * 0.99) {  // ties go to the smaller cluster
+      best_t = t;
+      best.tok = tok;
+      best.splits = sp;
+      best.clusters = cl;
+    }
+  }
+  return best;
+}
+
+enum { XM_N1 = 0, XM_O = 1, XM_N2 = 2, XM_A = 3 };
+const CUtensorMap& xmap(nf_plan p, int which, int tok) {
+  return tok == 64 ? p->tm_x64[which] : p->tm_x128[which];
+}
+
+// The plan lets small nano-operations take the weight-row GEMM (gemm_split_k 0).
+bool use_wrows(nf_plan p, int n_tok, bool dual = false) {
+  return p->opts.gemm_split_k == 0 && n_tok >= 1 &&
+         n_tok <= (dual ? kWrMaxTokensDual : kWrMaxTokens);
+}
+
+// The QKV weight-row tile pairs the two halves of 256 / head_dim heads.
+bool qkv_wrows_ok(const nf_model_shape& s) {
+  const int d = s.head_dim;
+  return d >= 16 && d <= 256 && 256 % d == 0 && (d / 2) % 8 == 0;
 }
 
 
@@ -720,7 +813,20 @@ nf_status run_qkv(nf_plan p, const nf_layer_weights* w, const void* x, void* kp,
   g.q_out = p->q;
   g.k_pool = static_cast<__nv_bfloat16*>(kp);
   g.v_pool = static_cast<__nv_bfloat16*>(vp);
-  g.splits = p->opts.gemm_split_k ? 1 : choose_splits(g.m_tiles * g.n_tiles, g.K, grid);
+  if (use_wrows(p, r1 - r0, true) && qkv_wrows_ok(s)) {
+    const int hp = 256 / s.head_dim;
+    const int w_tiles = (s.n_q_heads + 2 * s.n_kv_heads + hp - 1) / hp;
+    const WrChoice c = wr_choose(nf::EPI_QKV, r1 - r0, w_tiles, g.K, grid);
+    if (c.splits) {
+      g.n_tiles = w_tiles;
+      g.m_tiles = (r1 - r0 + c.tok - 1) / c.tok;
+      g.splits = c.splits;
+      NF_CUDA(nf::launch_gemm_wrows(nf::EPI_QKV, c.tok, p->tm_wqkv_h, p->tm_wqkv_h,
+                                    xmap(p, XM_N1, c.tok), g, c.clusters, true, st));
+      return NF_OK;
+    }
+  }
+  g.splits = p->opts.gemm_split_k == 1 ? 1 : choose_splits(g.m_tiles * g.n_tiles, g.K, grid);
   NF_CUDA(nf::launch_gemm(nf::EPI_QKV, p->tm_n1, p->tm_wqkv, p->tm_wqkv, g,
                           cap_grid(g.m_tiles * g.n_tiles * g.splits, grid), st));
   return NF_OK;
@@ -741,9 +847,21 @@ nf_status run_oproj(nf_plan p, const void* x, int r0, int r1, int grid, cudaStre
   g.ldc = s.hidden;
   g.R = static_cast<const __nv_bfloat16*>(x);
   g.ldr = s.hidden;
+  if (use_wrows(p, r1 - r0)) {
+    const int w_tiles = (g.N + 127) / 128;
+    const WrChoice c = wr_choose(nf::EPI_RESID, r1 - r0, w_tiles, g.K, grid);
+    if (c.splits) {
+      g.n_tiles = w_tiles;
+      g.m_tiles = (r1 - r0 + c.tok - 1) / c.tok;
+      g.splits = c.splits;
+      NF_CUDA(nf::launch_gemm_wrows(nf::EPI_RESID, c.tok, p->tm_wo128, p->tm_wo128,
+                                    xmap(p, XM_O, c.tok), g, c.clusters, true, st));
+      return NF_OK;
+    }
+  }
   g.bn = pick_bn(g.m_tiles, g.N, grid);
   g.n_tiles = (g.N + g.bn - 1) / g.bn;
-  g.splits = p->opts.gemm_split_k ? 1 : choose_splits(g.m_tiles * g.n_tiles, g.K, grid);
+  g.splits = p->opts.gemm_split_k == 1 ? 1 : choose_splits(g.m_tiles * g.n_tiles, g.K, grid);
   const CUtensorMap& wo = g.bn == 224 ? p->tm_wo224 : p->tm_wo;
   NF_CUDA(nf::launch_gemm(nf::EPI_RESID, p->tm_o, wo, wo, g,
                           cap_grid(g.m_tiles * g.n_tiles * g.splits, grid), st));
@@ -804,9 +922,21 @@ nf_status run_ffn(nf_plan p, const nf_layer_weights* w, void* y, int r0, int r1,
   g.n_tiles = (g.N + 127) / 128;
   g.C = p->a;
   g.ldc = s.ffn;
-  g.splits = p->opts.gemm_split_k ? 1 : choose_splits(g.m_tiles * g.n_tiles, g.K, grid);
-  NF_CUDA(nf::launch_gemm(nf::EPI_SWIGLU, p->tm_n2, p->tm_wg, p->tm_wu, g,
-                          cap_grid(g.m_tiles * g.n_tiles * g.splits, grid), st));
+  const bool wr = use_wrows(p, r1 - r0);
+  WrChoice c;
+  if (use_wrows(p, r1 - r0, true)) c = wr_choose(nf::EPI_SWIGLU, r1 - r0, (g.N + 127) / 128, g.K, grid);
+  if (c.splits) {
+    g.n_tiles = (g.N + 127) / 128;
+    g.m_tiles = (r1 - r0 + c.tok - 1) / c.tok;
+    g.splits = c.splits;
+    g.b2_row_off = 0;  // tm_wu starts at the up rows
+    NF_CUDA(nf::launch_gemm_wrows(nf::EPI_SWIGLU, c.tok, p->tm_wg, p->tm_wu,
+                                  xmap(p, XM_N2, c.tok), g, c.clusters, true, st));
+  } else {
+    g.splits = p->opts.gemm_split_k == 1 ? 1 : choose_splits(g.m_tiles * g.n_tiles, g.K, grid);
+    NF_CUDA(nf::launch_gemm(nf::EPI_SWIGLU, p->tm_n2, p->tm_wg, p->tm_wu, g,
+                            cap_grid(g.m_tiles * g.n_tiles * g.splits, grid), st));
+  }
   GemmArgs d = base_args(p);
   d.m_begin = r0;
   d.m_end = r1;
@@ -818,9 +948,21 @@ nf_status run_ffn(nf_plan p, const nf_layer_weights* w, void* y, int r0, int r1,
   d.ldc = s.hidden;
   d.R = p->h;
   d.ldr = s.hidden;
+  if (wr) {
+    const int w_tiles = (d.N + 127) / 128;
+    const WrChoice cd = wr_choose(nf::EPI_RESID, r1 - r0, w_tiles, d.K, grid);
+    if (cd.splits) {
+      d.n_tiles = w_tiles;
+      d.m_tiles = (r1 - r0 + cd.tok - 1) / cd.tok;
+      d.splits = cd.splits;
+      NF_CUDA(nf::launch_gemm_wrows(nf::EPI_RESID, cd.tok, p->tm_wd128, p->tm_wd128,
+                                    xmap(p, XM_A, cd.tok), d, cd.clusters, true, st));
+      return NF_OK;
+    }
+  }
   d.bn = pick_bn(d.m_tiles, d.N, grid);
   d.n_tiles = (d.N + d.bn - 1) / d.bn;
-  d.splits = p->opts.gemm_split_k ? 1 : choose_splits(d.m_tiles * d.n_tiles, d.K, grid);
+  d.splits = p->opts.gemm_split_k == 1 ? 1 : choose_splits(d.m_tiles * d.n_tiles, d.K, grid);
   const CUtensorMap& wd = d.bn == 224 ? p->tm_wd224 : p->tm_wd;
   NF_CUDA(nf::launch_gemm(nf::EPI_RESID, p->tm_a, wd, wd, d,
                           cap_grid(d.m_tiles * d.n_tiles * d.splits, grid), st));
@@ -1105,7 +1247,8 @@ nf_status nf_stack_step(nf_plan p, const nf_stack_weights* sw, const int32_t* to
     return fail(NF_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
   NF_TRY(ensure_layers(p, sw->n_layers));
   if (p->lm_key != sw->lm_head || p->lm_vocab != sw->vocab) {
-    if (!nf::make_tmap_bf16(&p->tm_lm, sw->lm_head, sw->vocab, p->shape.hidden, 256))
+    if (!nf::make_tmap_bf16(&p->tm_lm, sw->lm_head, sw->vocab, p->shape.hidden, 256) ||
+        !nf::make_tmap_bf16(&p->tm_lm128, sw->lm_head, sw->vocab, p->shape.hidden, 128))
       return fail(NF_ERR_INVALID_ARG, "LM head tensor map failed");
     p->lm_key = sw->lm_head;
     p->lm_vocab = sw->vocab;
@@ -1135,7 +1278,19 @@ nf_status nf_stack_step(nf_plan p, const nf_stack_weights* sw, const int32_t* to
   g.n_tiles = (sw->vocab + 255) / 256;
   g.C = static_cast<__nv_bfloat16*>(logits);
   g.ldc = sw->vocab;
-  g.splits = p->opts.gemm_split_k ? 1 : choose_splits(g.m_tiles * g.n_tiles, g.K, p->num_sms);
+  if (use_wrows(p, p->T)) {
+    const int w_tiles = (sw->vocab + 127) / 128;
+    const WrChoice c = wr_choose(nf::EPI_STORE, p->T, w_tiles, g.K, p->num_sms);
+    if (c.splits) {
+      g.n_tiles = w_tiles;
+      g.m_tiles = (p->T + c.tok - 1) / c.tok;
+      g.splits = c.splits;
+      NF_CUDA(nf::launch_gemm_wrows(nf::EPI_STORE, c.tok, p->tm_lm128, p->tm_lm128,
+                                    xmap(p, XM_N1, c.tok), g, c.clusters, true, st));
+      return NF_OK;
+    }
+  }
+  g.splits = p->opts.gemm_split_k == 1 ? 1 : choose_splits(g.m_tiles * g.n_tiles, g.K, p->num_sms);
   NF_CUDA(nf::launch_gemm(nf::EPI_STORE, p->tm_n1, p->tm_lm, p->tm_lm, g,
                           cap_grid(g.m_tiles * g.n_tiles * g.splits, p->num_sms), st));
   return NF_OK;
@@ -1331,6 +1486,51 @@ nf_status nf_gemm(const void* A, const void* B, void* C, const void* R, int32_t 
   NF_CUDA(nf::launch_gemm(epilogue, ta, tb, tb2, g,
                           cap_grid(g.m_tiles * g.n_tiles * g.splits, cap),
                           static_cast<cudaStream_t>(stream)));
+  return NF_OK;
+}
+
+nf_status nf_gemm_wrows(const void* A, const void* B, void* C, const void* R, int32_t M,
+                        int32_t N, int32_t K, int32_t epilogue, int32_t splits, int32_t max_sms,
+                        void* stream) {
+  if (!A || !B || !C) return fail(NF_ERR_INVALID_ARG, "NULL argument");
+  if (M < 1 || M > 256 || N < 8 || K < 8 || N % 8 || K % 8)
+    return fail(NF_ERR_INVALID_ARG, "need 1 <= M <= 256 and N, K positive multiples of 8");
+  if (epilogue < NF_EPI_STORE || epilogue > NF_EPI_SWIGLU)
+    return fail(NF_ERR_INVALID_ARG, "unknown epilogue %d", epilogue);
+  if (epilogue == NF_EPI_RESID && !R) return fail(NF_ERR_INVALID_ARG, "residual R is NULL");
+  if (splits < 0 || splits > 8 || splits > (K + 63) / 64)
+    return fail(NF_ERR_INVALID_ARG, "splits must be 0 or 1 .. min(8, ceil(K / 64))");
+  if (!aligned16(A) || !aligned16(B) || !aligned16(C) || (R && !aligned16(R)))
+    return fail(NF_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  const int sms = device_sms();
+  if (sms <= 0) return fail(NF_ERR_CUDA, "no CUDA device");
+  const int cap = (max_sms > 0 && max_sms < sms) ? max_sms : sms;
+  const int w_tiles = (N + 127) / 128;
+  const WrChoice c = wr_choose(epilogue, M, w_tiles, K, cap, splits);
+  if (!c.splits) return fail(NF_ERR_UNSUPPORTED, "no cluster of %d CTAs fits in %d SMs", splits, cap);
+  CUtensorMap tw, tw2, tx;
+  bool ok = nf::make_tmap_bf16(&tx, A, M, K, c.tok) && nf::make_tmap_bf16(&tw, B, N, K, 128);
+  if (epilogue == NF_EPI_SWIGLU)
+    ok = ok && nf::make_tmap_bf16(&tw2, static_cast<const char*>(B) + (size_t)N * K * 2, N, K, 128);
+  else
+    tw2 = tw;
+  if (!ok) return fail(NF_ERR_CUDA, "tensor map creation failed");
+  GemmArgs g{};
+  g.m_begin = 0;
+  g.m_end = M;
+  g.N = N;
+  g.K = K;
+  g.n_tiles = w_tiles;
+  g.m_tiles = (M + c.tok - 1) / c.tok;
+  g.splits = c.splits;
+  g.C = static_cast<__nv_bfloat16*>(C);
+  g.ldc = N;
+  g.R = static_cast<const __nv_bfloat16*>(R);
+  g.ldr = N;
+  g.status = global_status();
+  g.timeout_ns = kDefaultTimeoutNs;
+  NF_CUDA(nf::launch_gemm_wrows(epilogue, c.tok, tw, tw2, tx, g, c.clusters, false,
+                                static_cast<cudaStream_t>(stream)));
   return NF_OK;
 }
 

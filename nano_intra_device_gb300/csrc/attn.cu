@@ -69,6 +69,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) attn_kernel(const AttnArgs a) {
   constexpr int P = ATT_P;
   constexpr int BLK = P * D * 2;  // bytes of one (page, KV head) block
   constexpr int E2 = NCH * 4;     // dim pairs per lane
+  pdl_trigger();
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ts = lane >> 3, dg = lane & 7;

@@ -100,6 +100,7 @@ __global__ void __launch_bounds__(WARPS * 32, WARPS == AMMA_SHARE_WARPS ? 4 : 1)
   constexpr int KS = D / 16;        // k-steps of S, m-tiles of O
   static_assert(GRP >= 1 && GRP <= 8, "the GQA group must fit the 8 columns of a tile");
   static_assert(STAGES >= 2 * PPI, "S of the next group is formed while this one is in use");
+  pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // swizzled boxes: 1 KB aligned

@@ -55,6 +55,7 @@ __global__ void __launch_bounds__(PAIRS * 64, 1) attn_pair_kernel(const AttnArgs
   constexpr int R = kTransposed ? V / 8 : V; // totals a lane holds after the reduction
   constexpr float kLazy = 8.0f;
   using Smem = PairSmem<STAGES, R>;
+  pdl_trigger();
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int pair = warp >> 1, half = warp & 1;

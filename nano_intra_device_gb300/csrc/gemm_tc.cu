@@ -104,6 +104,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
   static_assert(BN % 32 == 0 && BN <= 256, "tile width");
+  pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);

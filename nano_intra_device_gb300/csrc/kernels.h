@@ -68,6 +68,25 @@ cudaError_t launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB,
 int gemm_block_n(int epi);
 int gemm_tiles(int epi, int m_rows, int N);
 
+// Weight-row GEMM for few tokens (gemm_wrows.cu): tiles of 128 output
+// features x tok tokens (tok = 64 or 128), the tokens [m_begin, m_end).
+// tmW: weight rows, 128-row boxes (QKV: head_dim / 2-row boxes; SwiGLU: the
+// gate rows, tmW2 the up rows from b2_row_off); tmX: the tokens' activations,
+// tok-row boxes.  n_tiles = weight tiles (ceil(N / 128); QKV: ceil(heads /
+// (256 / head_dim))), m_tiles = token tiles, splits = CTAs per cluster (1..8,
+// at most the K blocks of 64), which split K and sum through distributed
+// shared memory.  grid = clusters x splits CTAs.  EPI_STORE, EPI_RESID,
+// EPI_SWIGLU, EPI_QKV; N a multiple of 4.  programmatic: launch as a
+// programmatic dependent of the kernel ahead in the stream, which must be one
+// of this library's kernels launched after every write to the weights (the
+// first ring of weights is read before that kernel has finished).
+cudaError_t launch_gemm_wrows(int epi, int tok, const CUtensorMap& tmW, const CUtensorMap& tmW2,
+                              const CUtensorMap& tmX, const GemmArgs& args, int clusters,
+                              bool programmatic, cudaStream_t stream);
+// Clusters of `cluster` CTAs of that kernel that fit on the device at once
+// (0 when the query fails).  Cached per process.
+int gemm_wrows_max_clusters(int epi, int tok, int cluster);
+
 // ------------------------------------------------------ mixture of experts
 // Top-k routing of the tokens [r0, r0 + n) from router logits [*, E] fp32
 // (ties to the lower expert index, weights = softmax over the selected logits)

@@ -11,6 +11,7 @@ constexpr int RMS_THREADS = 128;
 __global__ void __launch_bounds__(RMS_THREADS)
     rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ g,
                    __nv_bfloat16* __restrict__ out, int row_begin, int hidden, float eps) {
+  pdl_trigger();
   const int row = row_begin + blockIdx.x;
   const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(row) * hidden);
   const uint4* gr = reinterpret_cast<const uint4*>(g);

@@ -67,6 +67,71 @@ def test_gemm_split_k_repeats_identically():
     assert torch.equal(C1, C2)
 
 
+# weight-row kernel: (M tokens, N, K, splits); ragged N (136, 688), K not a
+# multiple of 64 (200), one and two token tiles' sizes, every cluster size
+WROWS_SHAPES = [(1, 136, 64, 1), (17, 256, 200, 0), (64, 4096, 4096, 0), (64, 4096, 14336, 4),
+                (65, 688, 256, 4), (128, 1024, 4096, 8), (36, 512, 256, 3), (100, 6144, 4096, 6),
+                (8, 1024, 512, 2), (64, 2048, 4096, 5), (64, 2048, 4096, 7),
+                # two 128-token tiles
+                (256, 4096, 4096, 0), (200, 1032, 512, 3)]
+
+
+@pytest.mark.parametrize("M,N,K,splits", WROWS_SHAPES)
+def test_gemm_wrows_store_matches_float64(M, N, K, splits):
+    A, B = _rand(M, K, seed=21), _rand(N, K, std=0.02, seed=22)
+    C = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
+    _lib.gemm_wrows(A.to(DEV), B.to(DEV), C, splits=splits)
+    torch.cuda.synchronize()
+    compare(f64(C), f64(A) @ f64(B).T, f"wrows {M}x{N}x{K}/{splits}", rel_l2=5e-3)
+
+
+@pytest.mark.parametrize("M,N,K,splits", [(64, 4096, 14336, 0), (33, 688, 256, 2), (128, 512, 1024, 8)])
+def test_gemm_wrows_residual_matches_float64(M, N, K, splits):
+    A, B, R = _rand(M, K, seed=23), _rand(N, K, std=0.02, seed=24), _rand(M, N, seed=25)
+    C = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
+    _lib.gemm_wrows(A.to(DEV), B.to(DEV), C, R=R.to(DEV), epilogue=_lib.NF_EPI_RESID, splits=splits)
+    torch.cuda.synchronize()
+    compare(f64(C), f64(R) + f64(A) @ f64(B).T, "wrows+residual", rel_l2=5e-3)
+
+
+@pytest.mark.parametrize("M,F,K,splits", [(36, 688, 256, 0), (64, 14336, 4096, 0), (120, 320, 512, 3),
+                                          (1, 1024, 4096, 8)])
+def test_gemm_wrows_swiglu_matches_float64(M, F, K, splits):
+    A, B = _rand(M, K, seed=26), _rand(2 * F, K, std=0.02, seed=27)
+    C = torch.empty(M, F, dtype=torch.bfloat16, device=DEV)
+    _lib.gemm_wrows(A.to(DEV), B.to(DEV), C, epilogue=_lib.NF_EPI_SWIGLU, splits=splits)
+    torch.cuda.synchronize()
+    g = f64(A) @ f64(B[:F]).T
+    u = f64(A) @ f64(B[F:]).T
+    compare(f64(C), orc.silu(g) * u, "wrows+swiglu", rel_l2=5e-3)
+
+
+def test_gemm_wrows_sum_is_timing_independent_and_leaves_other_rows():
+    """The cluster's partial tiles are added in rank order: repeated calls give
+    the same bits; rows of C past M are never written."""
+    A, B = _rand(64, 14336, seed=28), _rand(4096, 14336, std=0.02, seed=29)
+    Ad, Bd = A.to(DEV), B.to(DEV)
+    outs = []
+    for _ in range(3):
+        C = torch.full((80, 4096), 7.0, dtype=torch.bfloat16, device=DEV)
+        _lib.gemm_wrows(Ad, Bd, C[:64], splits=8)
+        outs.append(C)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    assert bool((outs[0][64:] == 7.0).all())
+
+
+def test_gemm_wrows_rejects_what_it_cannot_do():
+    A, B = _rand(257, 256, seed=1).to(DEV), _rand(256, 256, seed=2).to(DEV)
+    C = torch.empty(257, 256, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(_lib.NanoflowError):
+        _lib.gemm_wrows(A, B, C)                      # more than 256 rows of A
+    with pytest.raises(_lib.NanoflowError):
+        _lib.gemm_wrows(A[:64], B, C[:64], splits=5)  # 4 K blocks cannot take 5 splits
+    with pytest.raises(_lib.NanoflowError):
+        _lib.gemm_wrows(A[:64], B, C[:64], splits=9)
+
+
 def test_gemm_sm_cap_gives_identical_bits():
     # 256 output tiles: no split-K at any cap, so the bits must not depend on it
     A, B = _rand(2048, 4096, seed=8), _rand(4096, 4096, std=0.02, seed=9)

@@ -116,6 +116,19 @@ def test_tiny_multiway_splits_both_executors(tiny, ab, fb):
         _check_layer(case, ref, y, kp, vp, np.arange(T))
 
 
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_tiny_gemm_kinds_match_the_oracle(tiny, mode):
+    """gemm_split_k 0: the weight-row kernel (every nano-operation here has at
+    most 128 tokens); 1: token-row tiles; 2: token-row tiles split over K."""
+    case, ref = tiny
+    T = case.batch.n_tokens
+    for ab, ex in (([0, T], _lib.NF_EXEC_SEQUENTIAL), ([0, 18, T], _lib.NF_EXEC_STREAMS)):
+        plan, y, kp, vp = case.run(_lib.make_opts(T, ab, ab, executor=ex, attn_sms=20,
+                                                  kv_chunk=32, gemm_split_k=mode))
+        plan.close()
+        _check_layer(case, ref, y, kp, vp, np.arange(T))
+
+
 def test_tiny_host_entry_point_matches_device(tiny):
     case, ref = tiny
     T = case.batch.n_tokens
@@ -190,3 +203,19 @@ def test_llama8b_sampled_rows_by_nano_batch_count(big, n, warps, stages):
     plan.close()
     _check_layer(case, ref, y, kp, vp, np.asarray(rows))
     assert torch.isfinite(y).all()
+
+
+@pytest.mark.parametrize("n_tok,nano", [(64, 1), (100, 1), (128, 2), (17, 1)])
+def test_llama8b_small_decode_batches(n_tok, nano):
+    """Decode-sized batches of the 8B shape: every GEMM on the weight-row kernel
+    (token tiles of 64 and 128; head_dim 128 pairs two heads per QKV tile)."""
+    shape = wl.llama8b_shape()
+    ctx = wl.lognormal_contexts(n_tok, 600.0, 1.0, 1, 8192, seed=n_tok)
+    b = wl.make_batch(shape, ctx, [], None, seed_bt=3, slack=0.01, max_pages=8192 // 16)
+    case = Case(shape, b, gain_std=0.0, seed=1)
+    ref = case.oracle()
+    ab = [0, n_tok] if nano == 1 else [0, n_tok // 2, n_tok]
+    ex = _lib.NF_EXEC_SEQUENTIAL if nano == 1 else _lib.NF_EXEC_STREAMS
+    plan, y, kp, vp = case.run(_lib.make_opts(n_tok, ab, ab, executor=ex, attn_sms=64))
+    plan.close()
+    _check_layer(case, ref, y, kp, vp, np.arange(n_tok))
