@@ -19,6 +19,9 @@
 //    operands into two accumulators, and QKV the first and the second half of
 //    each head's dimensions, so that every pair the epilogue combines (gate
 //    with up, RoPE's dimensions i and i + d/2) is in one thread;
+//  * when every CTA has at most one tile (the usual case: clusters are sized
+//    so), the exchange copy reuses the ring, which is idle by then, and the
+//    ring gets the room: more weight bytes in flight per SM;
 //  * launched as a programmatic dependent, a CTA fills its ring with weights
 //    (which no kernel writes) before it waits for the kernel ahead of it, so
 //    the weight stream starts while that kernel finishes;
@@ -36,24 +39,28 @@ constexpr int WR_BM = 128;             // weight rows (output features) per tile
 constexpr int WR_BK = 64;              // K per ring stage: one 128-byte swizzled row
 constexpr int WR_XC = 64;              // tokens per exchange round
 constexpr int WR_THREADS = 192;
-constexpr int WR_MAX_STAGES = 8;
+constexpr int WR_MAX_STAGES = 12;
 constexpr int WR_MAX_CLUSTER = 8;      // portable cluster size
 constexpr int WR_SMEM_LIMIT = 232448;  // opt-in shared memory of a CTA
 constexpr int WR_TAIL = 512;
 
-template <int EPI, int TOK>
+// ONE: every CTA has at most one tile, and the exchange copy (XBUF) reuses
+// the ring; otherwise it has room of its own.
+template <int EPI, int TOK, bool ONE>
 struct WrCfg {
   static constexpr int NA = (EPI == EPI_SWIGLU || EPI == EPI_QKV) ? 2 : 1;  // A operands
   static constexpr int W_BYTES = WR_BM * WR_BK * 2;
   static constexpr int X_BYTES = TOK * WR_BK * 2;
   static constexpr int STAGE = NA * W_BYTES + X_BYTES;
   static constexpr int XBUF = NA * WR_XC * WR_BM * 4;  // fp32 copy of one round
-  static constexpr int FIT = (WR_SMEM_LIMIT - 1024 - WR_TAIL - XBUF) / STAGE;
+  static constexpr int FIT = (WR_SMEM_LIMIT - 1024 - WR_TAIL - (ONE ? 0 : XBUF)) / STAGE;
   static constexpr int STAGES = FIT < WR_MAX_STAGES ? FIT : WR_MAX_STAGES;
-  static constexpr int SMEM = 1024 + STAGES * STAGE + XBUF + WR_TAIL;
+  static constexpr int RING = STAGES * STAGE;
+  static constexpr int SMEM =
+      1024 + (ONE ? (RING > XBUF ? RING : XBUF) : RING + XBUF) + WR_TAIL;
   static constexpr int ACC = NA * TOK;  // TMEM columns of one accumulator set
   static constexpr int TMEM = 2 * ACC;  // double buffered
-  static_assert(STAGES >= 2, "ring");
+  static_assert(STAGES >= 2 && SMEM <= WR_SMEM_LIMIT, "ring");
   static_assert(TMEM == 128 || TMEM == 256 || TMEM == 512, "TMEM allocation");
   static_assert(TOK % WR_XC == 0 && TOK <= 256, "token tile");
 };
@@ -84,20 +91,20 @@ __device__ __forceinline__ uint2 pack4_bf16(float a, float b, float c, float d) 
   return make_uint2(pack_bf16(a, b), pack_bf16(c, d));
 }
 
-template <int EPI, int TOK>
+template <int EPI, int TOK, bool ONE>
 __global__ void __launch_bounds__(WR_THREADS, 1)
     gemm_wrows_kernel(const __grid_constant__ CUtensorMap tmW,
                       const __grid_constant__ CUtensorMap tmW2,
                       const __grid_constant__ CUtensorMap tmX, const GemmArgs args) {
-  using Cfg = WrCfg<EPI, TOK>;
+  using Cfg = WrCfg<EPI, TOK, ONE>;
   pdl_trigger();
   constexpr int NA = Cfg::NA, STAGES = Cfg::STAGES;
   constexpr uint32_t IDESC = idesc_bf16_f32(WR_BM, TOK);
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-  float* xbuf = reinterpret_cast<float*>(smem + STAGES * Cfg::STAGE);
-  WrTail* tail = reinterpret_cast<WrTail*>(smem + STAGES * Cfg::STAGE + Cfg::XBUF);
+  float* xbuf = reinterpret_cast<float*>(ONE ? smem : smem + Cfg::RING);
+  WrTail* tail = reinterpret_cast<WrTail*>(smem + Cfg::SMEM - 1024 - WR_TAIL);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -482,26 +489,26 @@ __global__ void __launch_bounds__(WR_THREADS, 1)
   cluster_sync_all();  // no CTA leaves while a peer may still address it
 }
 
-template <int EPI, int TOK>
+template <int EPI, int TOK, bool ONE>
 cudaError_t wr_prepare() {
   static bool done = false;  // per process; the attribute is per function
   if (!done) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_wrows_kernel<EPI, TOK>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_wrows_kernel<EPI, TOK, ONE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         WrCfg<EPI, TOK>::SMEM);
+                                         WrCfg<EPI, TOK, ONE>::SMEM);
     if (e != cudaSuccess) return e;
     done = true;
   }
   return cudaSuccess;
 }
 
-template <int EPI, int TOK>
+template <int EPI, int TOK, bool ONE>
 void wr_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* at, int clusters, int S,
                cudaStream_t stream) {
   *cfg = cudaLaunchConfig_t{};
   cfg->gridDim = dim3(static_cast<unsigned>(clusters * S), 1, 1);
   cfg->blockDim = dim3(WR_THREADS, 1, 1);
-  cfg->dynamicSmemBytes = WrCfg<EPI, TOK>::SMEM;
+  cfg->dynamicSmemBytes = WrCfg<EPI, TOK, ONE>::SMEM;
   cfg->stream = stream;
   at[0].id = cudaLaunchAttributeClusterDimension;
   at[0].val.clusterDim.x = static_cast<unsigned>(S);
@@ -511,23 +518,24 @@ void wr_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* at, int clusters, i
   cfg->numAttrs = 1;
 }
 
-template <int EPI, int TOK>
+template <int EPI, int TOK, bool ONE>
 cudaError_t wr_launch(const CUtensorMap& tmW, const CUtensorMap& tmW2, const CUtensorMap& tmX,
                       const GemmArgs& args, int clusters, bool programmatic,
                       cudaStream_t stream) {
-  cudaError_t e = wr_prepare<EPI, TOK>();
+  cudaError_t e = wr_prepare<EPI, TOK, ONE>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute at[2];
-  wr_config<EPI, TOK>(&cfg, at, clusters, args.splits, stream);
+  wr_config<EPI, TOK, ONE>(&cfg, at, clusters, args.splits, stream);
   if (programmatic) {
     at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.numAttrs = 2;
   }
-  return cudaLaunchKernelEx(&cfg, gemm_wrows_kernel<EPI, TOK>, tmW, tmW2, tmX, args);
+  return cudaLaunchKernelEx(&cfg, gemm_wrows_kernel<EPI, TOK, ONE>, tmW, tmW2, tmX, args);
 }
 
+// Both variants take one SM per CTA, so one query serves them.
 template <int EPI, int TOK>
 int wr_max_clusters(int S) {
   static int cache[WR_MAX_CLUSTER + 1] = {};
@@ -535,15 +543,25 @@ int wr_max_clusters(int S) {
     int n = 0;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute at[1];
-    wr_config<EPI, TOK>(&cfg, at, 1, S, nullptr);
-    if (wr_prepare<EPI, TOK>() != cudaSuccess ||
-        cudaOccupancyMaxActiveClusters(&n, gemm_wrows_kernel<EPI, TOK>, &cfg) != cudaSuccess) {
+    wr_config<EPI, TOK, false>(&cfg, at, 1, S, nullptr);
+    if (wr_prepare<EPI, TOK, false>() != cudaSuccess ||
+        cudaOccupancyMaxActiveClusters(&n, gemm_wrows_kernel<EPI, TOK, false>, &cfg) !=
+            cudaSuccess) {
       cudaGetLastError();
       n = 0;
     }
     cache[S] = n > 0 ? n : -1;
   }
   return cache[S] > 0 ? cache[S] : 0;
+}
+
+template <int EPI, int TOK>
+cudaError_t wr_launch_any(const CUtensorMap& tmW, const CUtensorMap& tmW2, const CUtensorMap& tmX,
+                          const GemmArgs& args, int clusters, bool programmatic,
+                          cudaStream_t stream) {
+  if (clusters >= args.n_tiles * args.m_tiles)  // at most one tile per CTA
+    return wr_launch<EPI, TOK, true>(tmW, tmW2, tmX, args, clusters, programmatic, stream);
+  return wr_launch<EPI, TOK, false>(tmW, tmW2, tmX, args, clusters, programmatic, stream);
 }
 
 }  // namespace
@@ -579,17 +597,18 @@ cudaError_t launch_gemm_wrows(int epi, int tok, const CUtensorMap& tmW, const CU
   if (!t64 && tok != 128) return cudaErrorInvalidValue;
   switch (epi) {
     case EPI_STORE:
-      return t64 ? wr_launch<EPI_STORE, 64>(tmW, tmW2, tmX, args, clusters, programmatic, stream)
-                 : wr_launch<EPI_STORE, 128>(tmW, tmW2, tmX, args, clusters, programmatic, stream);
+      return t64 ? wr_launch_any<EPI_STORE, 64>(tmW, tmW2, tmX, args, clusters, programmatic, stream)
+                 : wr_launch_any<EPI_STORE, 128>(tmW, tmW2, tmX, args, clusters, programmatic, stream);
     case EPI_RESID:
-      return t64 ? wr_launch<EPI_RESID, 64>(tmW, tmW2, tmX, args, clusters, programmatic, stream)
-                 : wr_launch<EPI_RESID, 128>(tmW, tmW2, tmX, args, clusters, programmatic, stream);
+      return t64 ? wr_launch_any<EPI_RESID, 64>(tmW, tmW2, tmX, args, clusters, programmatic, stream)
+                 : wr_launch_any<EPI_RESID, 128>(tmW, tmW2, tmX, args, clusters, programmatic, stream);
     case EPI_SWIGLU:
-      return t64 ? wr_launch<EPI_SWIGLU, 64>(tmW, tmW2, tmX, args, clusters, programmatic, stream)
-                 : wr_launch<EPI_SWIGLU, 128>(tmW, tmW2, tmX, args, clusters, programmatic, stream);
+      return t64 ? wr_launch_any<EPI_SWIGLU, 64>(tmW, tmW2, tmX, args, clusters, programmatic, stream)
+                 : wr_launch_any<EPI_SWIGLU, 128>(tmW, tmW2, tmX, args, clusters, programmatic,
+                                                  stream);
     case EPI_QKV:
-      return t64 ? wr_launch<EPI_QKV, 64>(tmW, tmW2, tmX, args, clusters, programmatic, stream)
-                 : wr_launch<EPI_QKV, 128>(tmW, tmW2, tmX, args, clusters, programmatic, stream);
+      return t64 ? wr_launch_any<EPI_QKV, 64>(tmW, tmW2, tmX, args, clusters, programmatic, stream)
+                 : wr_launch_any<EPI_QKV, 128>(tmW, tmW2, tmX, args, clusters, programmatic, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -6,6 +6,7 @@ of warm-up launches and then the launches to capture, and exits.
 
     python -m nano_intra_device_gb300.profcase attn --decode 512
     python -m nano_intra_device_gb300.profcase gemm --m 1024 --n 6144 --k 4096
+    python -m nano_intra_device_gb300.profcase wrows --m 64 --n 14336 --k 4096 --epi 2
     python -m nano_intra_device_gb300.profcase step --decode 1792 --prefill 256 --nano 2 --sms 96
 """
 from __future__ import annotations
@@ -55,6 +56,19 @@ def case_gemm(a):
     print(f"gemm case: {a.m}x{a.n}x{a.k} epilogue {a.epi}")
 
 
+def case_wrows(a):
+    """The weight-row GEMM of decode-sized nano-operations (nf_gemm_wrows)."""
+    A = torch.randn(a.m, a.k, device="cuda").to(torch.bfloat16)
+    nb = 2 * a.n if a.epi == 2 else a.n
+    B = (torch.randn(nb, a.k, device="cuda") * 0.02).to(torch.bfloat16)
+    C = torch.empty(a.m, a.n, device="cuda", dtype=torch.bfloat16)
+    R = torch.randn(a.m, a.n, device="cuda").to(torch.bfloat16) if a.epi == 1 else None
+    for _ in range(a.warmup + a.launches):
+        _lib.gemm_wrows(A, B, C, R=R, epilogue=a.epi, splits=a.splits, max_sms=a.sms)
+    torch.cuda.synchronize()
+    print(f"wrows case: {a.m}x{a.n}x{a.k} epilogue {a.epi} splits {a.splits}")
+
+
 def case_step(a):
     shape, b = _batch(a.decode, a.prefill)
     T = b.n_tokens
@@ -76,7 +90,7 @@ def case_step(a):
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["attn", "gemm", "step"])
+    ap.add_argument("case", choices=["attn", "gemm", "wrows", "step"])
     ap.add_argument("--decode", type=int, default=512)
     ap.add_argument("--prefill", type=int, default=0)
     ap.add_argument("--chunk", type=int, default=512)
@@ -85,11 +99,12 @@ def main(argv=None):
     ap.add_argument("--k", type=int, default=4096)
     ap.add_argument("--epi", type=int, default=0)
     ap.add_argument("--sms", type=int, default=0)
+    ap.add_argument("--splits", type=int, default=0)
     ap.add_argument("--nano", type=int, default=2)
     ap.add_argument("--warmup", type=int, default=2)
     ap.add_argument("--launches", type=int, default=2)
     a = ap.parse_args(argv)
-    {"attn": case_attn, "gemm": case_gemm, "step": case_step}[a.case](a)
+    {"attn": case_attn, "gemm": case_gemm, "wrows": case_wrows, "step": case_step}[a.case](a)
 
 
 if __name__ == "__main__":
