@@ -447,7 +447,8 @@ __global__ void __launch_bounds__(WARPS * 32, WARPS == AMMA_SHARE_WARPS ? 4 : 1)
         rec[GRP * D + GRP + h1] = l1;
       }
     }
-    if (finish_piece(a, t, g, nch, lane)) merge_row_partials<GRP, NCH>(a, t, g, nch, lane);
+    if (finish_piece(a, t, g, nch, lane))
+      merge_row_partials<GRP, NCH, (WARPS <= 8 && GRP <= 4) ? 4 : 2>(a, t, g, nch, lane);
   }
 
   if (failed) raise_status(a.status, ST_TIMEOUT);
