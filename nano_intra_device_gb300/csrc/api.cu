@@ -159,6 +159,13 @@ struct nf_plan_s {
     CUtensorMap tk, tv;
   };
   std::vector<PoolMaps> pcache;
+  // prefill-chunk attention: tiles of rows (first, end, sequence, 0) of every
+  // attention nano-batch, nano-batch i's from pf_seg[i]; pinned staging for
+  // nf_plan_set_batch (two halves)
+  int4* pf_tiles = nullptr;
+  int4* pf_stage = nullptr;
+  int pf_flip = 0;
+  int pf_seg[NF_MAX_NANO + 1] = {};
   // split-K GEMM workspace: fp32 partial tiles and per-tile arrival counters
   float* gemm_part = nullptr;
   int* gemm_cnt = nullptr;
@@ -292,10 +299,11 @@ void free_plan(nf_plan p) {
                   p->partials, p->status, p->n1, p->q, p->o, p->h, p->n2, p->a, p->x_stage,
                   p->y_stage, p->bt_stage, p->sl_stage, p->xa, p->xb, p->gemm_part,
                   p->gemm_cnt, p->moe_off, p->moe_perm, p->moe_pair_row, p->moe_pair_w,
-                  p->moe_a, p->moe_act, p->moe_out, p->rope_cs};
+                  p->moe_a, p->moe_act, p->moe_out, p->rope_cs, p->pf_tiles};
   for (void* b : bufs)
     if (b) cudaFree(b);
   if (p->set_stage) cudaFreeHost(p->set_stage);
+  if (p->pf_stage) cudaFreeHost(p->pf_stage);
   for (cudaEvent_t e : p->ev) cudaEventDestroy(e);
   for (auto& r : p->trace) {
     cudaEventDestroy(r.b);
@@ -326,6 +334,25 @@ nf_status dalloc(T** ptr, size_t bytes) {
     nf_status s_ = (expr);          \
     if (s_ != NF_OK) return s_;     \
   } while (0)
+
+// Tiles of prefill-chunk rows for the prefill attention kernel, attention
+// nano-batch by nano-batch (rows of a chunk inside the nano-batch, at most
+// prefill_tile_rows of them a tile); seg[i] = first tile of nano-batch i.
+// At most T tiles: they are disjoint runs of rows.
+void build_prefill_tiles(const nf_plan_s* p, int n_decode, int n_seq, const std::vector<int>& tok_begin,
+                         const nf_plan_opts& o, std::vector<int4>& tiles, int* seg) {
+  tiles.clear();
+  const int qp = nf::prefill_tile_rows(p->shape.n_q_heads, p->shape.n_kv_heads);
+  for (int i = 0; i < o.n_attn; ++i) {
+    seg[i] = (int)tiles.size();
+    const int a = o.attn_bounds[i], b = o.attn_bounds[i + 1];
+    for (int j = n_decode; j < n_seq; ++j) {
+      const int lo = std::max(a, tok_begin[j]), hi = std::min(b, tok_begin[j + 1]);
+      for (int r = lo; r < hi; r += qp) tiles.push_back(make_int4(r, std::min(r + qp, hi), j, 0));
+    }
+  }
+  seg[o.n_attn] = (int)tiles.size();
+}
 
 nf_status alloc_plan(nf_plan p) {
   p->T_cap = p->T;
@@ -391,6 +418,14 @@ nf_status alloc_plan(nf_plan p) {
                      cudaMemcpyHostToDevice));
   NF_CUDA(cudaMemcpy(p->d_seg_bounds, p->opts.attn_bounds, (p->opts.n_attn + 1) * 4,
                      cudaMemcpyHostToDevice));
+  NF_TRY(dalloc(&p->pf_tiles, T * sizeof(int4)));
+  {
+    std::vector<int4> tiles;
+    build_prefill_tiles(p, p->n_decode, p->n_seq, p->tok_begin, p->opts, tiles, p->pf_seg);
+    if (!tiles.empty())
+      NF_CUDA(cudaMemcpy(p->pf_tiles, tiles.data(), tiles.size() * sizeof(int4),
+                         cudaMemcpyHostToDevice));
+  }
   NF_CUDA(cudaStreamCreateWithFlags(&p->s_gemm, cudaStreamNonBlocking));
   NF_CUDA(cudaStreamCreateWithFlags(&p->s_attn, cudaStreamNonBlocking));
   p->ev.resize(2 + 2 * NF_MAX_NANO);
@@ -768,6 +803,8 @@ nf_status run_attention(nf_plan p, int seg, const void* q, const void* kp, const
   a.max_chunks = p->max_chunks;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p->shape.head_dim));
   a.warps = p->opts.attn_warps;
+  a.prefill_elsewhere = p->attn_mma && p->n_prefill > 0;
+  a.n_decode_seqs = p->n_decode;
   a.status = p->status;
   a.timeout_ns = (unsigned long long)p->opts.timeout_ns;
   if (p->attn_mma) {
@@ -786,7 +823,12 @@ nf_status run_attention(nf_plan p, int seg, const void* q, const void* kp, const
       p->pcache.push_back(c);
       pm = &p->pcache.back();
     }
-    NF_CUDA(nf::launch_attention_mma(a, pm->tk, pm->tv, grid, st));
+    // the prefill tiles first; the decode kernel then starts, as their
+    // programmatic dependent, on the SMs they leave free
+    const int n_pf = a.prefill_elsewhere ? p->pf_seg[seg + 1] - p->pf_seg[seg] : 0;
+    if (n_pf > 0)
+      NF_CUDA(nf::launch_attention_prefill(a, pm->tk, pm->tv, p->pf_tiles + p->pf_seg[seg], n_pf, st));
+    NF_CUDA(nf::launch_attention_mma(a, pm->tk, pm->tv, grid, n_pf > 0, st));
     return NF_OK;
   }
   NF_CUDA(nf::launch_attention(a, grid, st));
@@ -1377,6 +1419,20 @@ nf_status nf_plan_set_batch(nf_plan p, const nf_batch_desc* b, const nf_plan_opt
                           st));
   NF_CUDA(cudaMemcpyAsync(p->d_seg_bounds, h + 2 * p->seq_cap + 1, (o.n_attn + 1) * 4,
                           cudaMemcpyHostToDevice, st));
+  {
+    std::vector<int4> tiles;
+    int seg[NF_MAX_NANO + 1];
+    build_prefill_tiles(p, b->n_decode, n_seq, tok_begin, o, tiles, seg);
+    if (!p->pf_stage)
+      NF_CUDA(cudaHostAlloc(&p->pf_stage, 2 * (size_t)p->T_cap * sizeof(int4), cudaHostAllocDefault));
+    int4* hp = p->pf_stage + (size_t)p->pf_flip * p->T_cap;
+    p->pf_flip ^= 1;
+    std::copy(tiles.begin(), tiles.end(), hp);
+    if (!tiles.empty())
+      NF_CUDA(cudaMemcpyAsync(p->pf_tiles, hp, tiles.size() * sizeof(int4), cudaMemcpyHostToDevice,
+                              st));
+    std::copy(seg, seg + o.n_attn + 1, p->pf_seg);
+  }
   p->n_decode = b->n_decode;
   p->n_prefill = b->n_prefill;
   p->n_seq = n_seq;

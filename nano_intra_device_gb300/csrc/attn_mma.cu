@@ -26,53 +26,12 @@
 #include "attn_merge.cuh"
 #include "common.cuh"
 #include "kernels.h"
+#include "mma_frag.cuh"
 
 namespace nf {
 
-constexpr int AMMA_P = 16;                           // page size the kernel is built for
 constexpr int AMMA_MAX_PIECE_PAGES = 2048 / AMMA_P;  // longest piece: 4 page ids per lane
 constexpr int AMMA_MIN_SMEM = 120 * 1024;            // > half an SM: one CTA per SM
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr)
-               : "memory");
-}
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr)
-               : "memory");
-}
-// Transpose of an 8x8 b16 matrix held one pair per lane in fragment layout.
-__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
-  uint32_t y;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
-  return y;
-}
-// 2^x by the SFU (ex2.approx, relative error near 2^-22; 0 for -inf)
-__device__ __forceinline__ float ex2_approx(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-// d += a . b  (m16n8k16, bf16 inputs, fp32 accumulators)
-__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                          uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
-      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// Byte offset of the 16-byte chunk `ci` (8 bf16 from dim 8*ci) of position
-// `pos` inside one page block of K or V: 64-column boxes of 16 rows x 128 bytes,
-// each 1024-byte half-box swizzled by (row % 8).
-__device__ __forceinline__ uint32_t page_chunk_off(int pos, int ci) {
-  const int box = ci >> 3, c = ci & 7;
-  return static_cast<uint32_t>(box * (AMMA_P * 128) + pos * 128 + ((c ^ (pos & 7)) << 4));
-}
 
 // The 4-warp configuration shares its SM with one GEMM CTA of 2 ring stages
 // (98 KB, <= 248 registers a thread): it takes 117 KB (more than half an SM, so
@@ -150,6 +109,7 @@ __global__ void __launch_bounds__(WARPS * 32, WARPS == AMMA_SHARE_WARPS ? 4 : 1)
     const int pair = begin + idx / n_kv, g = idx % n_kv;
     const int t = a.items[2 * pair], c = a.items[2 * pair + 1];
     const int s = a.tok_seq[t];
+    if (a.prefill_elsewhere && s >= a.n_decode_seqs) continue;  // the prefill kernel's row
     const int ctx = a.tok_pos[t] + 1;
     const int b0 = c * C;
     const int n = min(C, ctx - b0);
@@ -452,11 +412,15 @@ __global__ void __launch_bounds__(WARPS * 32, WARPS == AMMA_SHARE_WARPS ? 4 : 1)
   }
 
   if (failed) raise_status(a.status, ST_TIMEOUT);
+  // Launched as a programmatic dependent of the prefill kernel of the same
+  // nano-batch (which writes other rows of o), this grid completes only after
+  // that one, so whatever follows sees both.
+  pdl_wait();
 }
 
 template <int GRP, int NCH, int WARPS, int STAGES, int PPI>
 static cudaError_t launch_mma_t(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
-                                int grid, cudaStream_t stream) {
+                                int grid, bool programmatic, cudaStream_t stream) {
   const int smem = amma_smem_bytes(NCH * 64, WARPS, STAGES);
   static bool attr = false;
   if (!attr) {
@@ -465,8 +429,17 @@ static cudaError_t launch_mma_t(const AttnArgs& a, const CUtensorMap& tk, const 
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  attn_mma_kernel<GRP, NCH, WARPS, STAGES, PPI><<<grid, WARPS * 32, smem, stream>>>(tk, tv, a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(WARPS * 32, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = programmatic ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, attn_mma_kernel<GRP, NCH, WARPS, STAGES, PPI>, tk, tv, a);
 }
 
 bool attention_mma_supported(int n_q, int n_kv, int head_dim, int page_size, int num_pages) {
@@ -485,7 +458,7 @@ bool make_pool_tmap(CUtensorMap* map, const void* pool, int num_pages, int n_kv,
 }
 
 cudaError_t launch_attention_mma(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
-                                 int grid, cudaStream_t stream) {
+                                 int grid, bool programmatic, cudaStream_t stream) {
   if (grid <= 0 || !attention_mma_supported(a.n_q, a.n_kv, a.head_dim, a.page_size, a.num_pages))
     return cudaErrorInvalidValue;
   const int grp = a.n_q / a.n_kv, nch = a.head_dim / 64;
@@ -494,14 +467,14 @@ cudaError_t launch_attention_mma(const AttnArgs& a, const CUtensorMap& tk, const
   // than one on every configuration, so all use one)
 #define NF_AMMA_CFG(G, N)                                                  \
   switch (a.warps) {                                                       \
-    case 4: return launch_mma_t<G, N, 4, 3, 1>(a, tk, tv, grid, stream);   \
-    case 5: return launch_mma_t<G, N, 5, 5, 1>(a, tk, tv, grid, stream);   \
-    case 6: return launch_mma_t<G, N, 6, 4, 1>(a, tk, tv, grid, stream);   \
-    case 7: return launch_mma_t<G, N, 7, 4, 1>(a, tk, tv, grid, stream);   \
-    case 8: return launch_mma_t<G, N, 8, 3, 1>(a, tk, tv, grid, stream);   \
-    case 10: return launch_mma_t<G, N, 10, 2, 1>(a, tk, tv, grid, stream); \
-    case 12: return launch_mma_t<G, N, 12, 2, 1>(a, tk, tv, grid, stream); \
-    case 14: return launch_mma_t<G, N, 14, 2, 1>(a, tk, tv, grid, stream); \
+    case 4: return launch_mma_t<G, N, 4, 3, 1>(a, tk, tv, grid, programmatic, stream);   \
+    case 5: return launch_mma_t<G, N, 5, 5, 1>(a, tk, tv, grid, programmatic, stream);   \
+    case 6: return launch_mma_t<G, N, 6, 4, 1>(a, tk, tv, grid, programmatic, stream);   \
+    case 7: return launch_mma_t<G, N, 7, 4, 1>(a, tk, tv, grid, programmatic, stream);   \
+    case 8: return launch_mma_t<G, N, 8, 3, 1>(a, tk, tv, grid, programmatic, stream);   \
+    case 10: return launch_mma_t<G, N, 10, 2, 1>(a, tk, tv, grid, programmatic, stream); \
+    case 12: return launch_mma_t<G, N, 12, 2, 1>(a, tk, tv, grid, programmatic, stream); \
+    case 14: return launch_mma_t<G, N, 14, 2, 1>(a, tk, tv, grid, programmatic, stream); \
     default: return cudaErrorInvalidValue;                                 \
   }
 #define NF_AMMA_CASE(G, N) \

@@ -160,6 +160,10 @@ struct AttnArgs {
   float scale_log2;          // log2(e) / sqrt(d)
   int warps;                 // warps per CTA: 8 (3 pages in flight each); 12 or 16: warp
                              // pairs (head_dim 128); 4 or 5 leave room for a 2-stage GEMM CTA
+  // tensor-core decode kernel: with prefill_elsewhere set, rows of sequences
+  // n_decode_seqs and up (the prefill chunks) are left to the prefill kernel
+  int prefill_elsewhere;
+  int n_decode_seqs;
   uint32_t* status;
   unsigned long long timeout_ns;
 };
@@ -180,7 +184,18 @@ cudaError_t launch_attention(const AttnArgs& a, int grid, cudaStream_t stream);
 bool attention_mma_supported(int n_q, int n_kv, int head_dim, int page_size, int num_pages);
 bool make_pool_tmap(CUtensorMap* map, const void* pool, int num_pages, int n_kv, int page_size,
                     int head_dim);
+// programmatic: launch as a programmatic dependent of the kernel ahead (the
+// prefill kernel of the same nano-batch); the grid waits for it before it ends.
 cudaError_t launch_attention_mma(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
-                                 int grid, cudaStream_t stream);
+                                 int grid, bool programmatic, cudaStream_t stream);
+// Causal attention of prefill-chunk rows (attn_prefill.cu), flash style on the
+// tensor cores: tiles[i] = (first row, end row, sequence, 0), rows of one
+// prefill sequence, at most prefill_tile_rows(n_q, n_kv) of them; one CTA per
+// (tile, KV head) writes o for the tile's rows.  Same shapes as
+// attention_mma_supported; K/V through the same pool maps.
+int prefill_tile_rows(int n_q, int n_kv);
+cudaError_t launch_attention_prefill(const AttnArgs& a, const CUtensorMap& tk,
+                                     const CUtensorMap& tv, const int4* tiles, int n_tiles,
+                                     cudaStream_t stream);
 
 }  // namespace nf
