@@ -58,7 +58,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_kv = a.n_kv;
   const int g = blockIdx.x % n_kv;
-  const int4 tl = tiles[blockIdx.x / n_kv];
+  // tiles of a chunk are listed by increasing position, so a later tile reads
+  // more pages: the grid takes them from the end, longest first
+  const int4 tl = tiles[gridDim.x / n_kv - 1 - blockIdx.x / n_kv];
   const int t0 = tl.x, t1 = tl.y, sq = tl.z;  // rows [t0, t1) of sequence sq
   const int last_pos = a.tok_pos[t1 - 1];
   const int npages = last_pos / AMMA_P + 1;
