@@ -256,7 +256,12 @@ nf_status nf_layers_step(nf_plan plan, const nf_layer_weights* layers, int32_t n
  * x_host [T, H] bf16, block_table_host and seq_lens_host as above, y_host
  * [T, H].  Copies them through plan-owned device staging buffers on `stream`
  * and synchronizes the stream before returning (y_host is then valid).
- * Pinned host memory gives full copy bandwidth; pageable memory works. */
+ * Pinned host memory gives full copy bandwidth; pageable memory works.  With
+ * pinned buffers (and no capture or trace in progress) the second call with the
+ * same pointers captures the copies and the step into a CUDA graph, and later
+ * calls replay it on a plan-owned stream ordered after `stream`: one launch per
+ * step instead of one per copy and kernel.  nf_plan_set_batch invalidates the
+ * captured graphs.  The host buffers' contents are read at each call. */
 nf_status nf_layer_step_host(nf_plan plan, const nf_layer_weights* w, const void* x_host,
                              void* k_pool, void* v_pool, const int32_t* block_table_host,
                              const int32_t* seq_lens_host, void* y_host, void* stream);

@@ -142,6 +142,37 @@ def test_tiny_host_entry_point_matches_device(tiny):
     assert torch.equal(yh, y.cpu())
 
 
+@pytest.mark.parametrize("executor", [_lib.NF_EXEC_SEQUENTIAL, _lib.NF_EXEC_STREAMS])
+def test_host_entry_point_graph_replay_reads_fresh_inputs(tiny, executor):
+    """Pinned host buffers: the first call runs directly, the second captures a
+    graph and later calls replay it.  Every call must read the host buffers
+    anew (a different x each time) and match the device entry point bit for bit;
+    after nf_plan_set_batch (another nano-batch split) the old graph is not
+    reused."""
+    case, _ = tiny
+    T, H = case.batch.n_tokens, case.shape.hidden
+    bt, sl = torch.from_numpy(case.batch.block_table), torch.from_numpy(case.batch.seq_lens)
+    xh = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
+    yh = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
+    bth, slh = bt.pin_memory(), sl.pin_memory()
+    plan = _lib.Plan(case.shape, case.batch,
+                     _lib.make_opts(T, [0, 18, T], executor=executor, attn_sms=30))
+    kp, vp = case.kp.clone(), case.vp.clone()   # the same pools every call: one graph
+    for i, bounds in enumerate([None] * 4 + [[0, 7, T]] * 2):
+        if bounds is not None and i == 4:
+            plan.set_batch(case.batch, _lib.make_opts(T, bounds, executor=executor, attn_sms=30))
+        x = wl.make_x(case.shape, T, seed=100 + i)
+        xh.copy_(x)
+        _lib.layer_step_host(plan, case.wd, xh, kp, vp, bth, slh, yh)
+        kd, vd = case.kp.clone(), case.vp.clone()
+        yd = torch.empty(T, H, dtype=torch.bfloat16, device=DEV)
+        _lib.layer_step(plan, case.wd, x.to(DEV), kd, vd, bt.to(DEV), sl.to(DEV), yd)
+        torch.cuda.synchronize()
+        assert torch.equal(yh, yd.cpu()), f"call {i}"
+    plan.poll()
+    plan.close()
+
+
 def test_plan_save_load_and_search(tiny, tmp_path):
     case, ref = tiny
     T = case.batch.n_tokens
