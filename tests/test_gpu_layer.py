@@ -236,7 +236,7 @@ def test_llama8b_sampled_rows_by_nano_batch_count(big, n, warps, stages):
     assert torch.isfinite(y).all()
 
 
-@pytest.mark.parametrize("n_tok,nano", [(64, 1), (100, 1), (128, 2), (17, 1)])
+@pytest.mark.parametrize("n_tok,nano", [(64, 1), (100, 1), (128, 2), (17, 1), (256, 1)])
 def test_llama8b_small_decode_batches(n_tok, nano):
     """Decode-sized batches of the 8B shape: every GEMM on the weight-row kernel
     (token tiles of 64 and 128; head_dim 128 pairs two heads per QKV tile)."""
