@@ -266,6 +266,23 @@ nf_status nf_layer_step_host(nf_plan plan, const nf_layer_weights* w, const void
                              void* k_pool, void* v_pool, const int32_t* block_table_host,
                              const int32_t* seq_lens_host, void* y_host, void* stream);
 
+/* The same step, pipelined: enqueues the copies of the inputs on a plan-owned
+ * copy stream into one of two staging slots, the step on `stream`, and the copy
+ * of y back to y_host on a second plan-owned copy stream, and returns without
+ * waiting.  Consecutive calls overlap one step's copies with the neighbouring
+ * steps' compute (events keep a slot from being refilled before the step that
+ * read it has finished, and from being rewritten before its y was copied out).
+ * Host buffers should be pinned; x_host, block_table_host and seq_lens_host
+ * must stay unchanged, and y_host unread, until nf_plan_host_wait returns.
+ * Steps run in call order on `stream` (the KV pools carry from one to the next). */
+nf_status nf_layer_step_host_async(nf_plan plan, const nf_layer_weights* w, const void* x_host,
+                                   void* k_pool, void* v_pool, const int32_t* block_table_host,
+                                   const int32_t* seq_lens_host, void* y_host, void* stream);
+
+/* Wait until every step enqueued by nf_layer_step_host_async has copied its y
+ * out to the host. */
+nf_status nf_plan_host_wait(nf_plan plan);
+
 /* Report device-side errors of earlier steps.  wait != 0 synchronizes the
  * device first.  Returns NF_OK, NF_ERR_TIMEOUT or NF_ERR_DEVICE (and clears
  * the status word), or NF_ERR_CUDA for an asynchronous CUDA error. */

@@ -89,6 +89,9 @@ _SIGS = {
     "nf_plan_destroy": (None, [c_void_p]),
     "nf_layer_step": (c_int, [c_void_p, POINTER(nf_layer_weights), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     "nf_layer_step_host": (c_int, [c_void_p, POINTER(nf_layer_weights), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "nf_layer_step_host_async": (c_int, [c_void_p, POINTER(nf_layer_weights), c_void_p, c_void_p, c_void_p, c_void_p,
+                                         c_void_p, c_void_p, c_void_p]),
+    "nf_plan_host_wait": (c_int, [c_void_p]),
     "nf_plan_poll": (c_int, [c_void_p, c_int]),
     "nf_stack_step": (c_int, [c_void_p, POINTER(nf_stack_weights), c_void_p, POINTER(c_void_p), POINTER(c_void_p), c_void_p, c_void_p, c_void_p, c_void_p]),
     "nf_layers_step": (c_int, [c_void_p, POINTER(nf_layer_weights), c_int32, c_void_p, POINTER(c_void_p), POINTER(c_void_p), c_void_p, c_void_p, c_void_p, c_void_p]),
@@ -326,6 +329,19 @@ def layer_step_host(plan: Plan, w: dict, x_host, k_pool, v_pool, bt_host, sl_hos
     ws = make_weights_struct(w)
     check(lib().nf_layer_step_host(plan.h, ctypes.byref(ws), ptr(x_host), ptr(k_pool), ptr(v_pool),
                                    ptr(bt_host), ptr(sl_host), ptr(y_host), stream_handle(stream)))
+
+
+def layer_step_host_async(plan: Plan, w: dict, x_host, k_pool, v_pool, bt_host, sl_host, y_host,
+                          stream=None):
+    """nf_layer_step_host_async: enqueue a host-buffer step (pipelined copies);
+    host_wait(plan) waits for every enqueued y."""
+    ws = make_weights_struct(w)
+    check(lib().nf_layer_step_host_async(plan.h, ctypes.byref(ws), ptr(x_host), ptr(k_pool), ptr(v_pool),
+                                         ptr(bt_host), ptr(sl_host), ptr(y_host), stream_handle(stream)))
+
+
+def host_wait(plan: Plan):
+    check(lib().nf_plan_host_wait(plan.h))
 
 
 def step_metadata(plan: Plan, block_table, seq_lens, stream=None):

@@ -197,6 +197,15 @@ struct nf_plan_s {
   uint64_t batch_version = 0;
   cudaStream_t s_host = nullptr;
   cudaEvent_t ev_host = nullptr;
+  // pipelined host-buffer steps: two staging slots, a stream for the copies in
+  // and one for the copies out; per slot: inputs landed, step done, y copied out
+  struct HostPipe {
+    __nv_bfloat16 *x[2] = {nullptr, nullptr}, *y[2] = {nullptr, nullptr};
+    int *bt[2] = {nullptr, nullptr}, *sl[2] = {nullptr, nullptr};
+    cudaStream_t s_in = nullptr, s_out = nullptr;
+    cudaEvent_t in_done[2] = {}, step_done[2] = {}, out_done[2] = {};
+    int next = 0;
+  } pipe;
 };
 
 namespace {
@@ -320,6 +329,16 @@ void free_plan(nf_plan p) {
     if (h.exec) cudaGraphExecDestroy(h.exec);
   if (p->s_host) cudaStreamDestroy(p->s_host);
   if (p->ev_host) cudaEventDestroy(p->ev_host);
+  for (int i = 0; i < 2; ++i) {
+    void* pb[] = {p->pipe.x[i], p->pipe.y[i], p->pipe.bt[i], p->pipe.sl[i]};
+    for (void* b : pb)
+      if (b) cudaFree(b);
+    cudaEvent_t pe[] = {p->pipe.in_done[i], p->pipe.step_done[i], p->pipe.out_done[i]};
+    for (cudaEvent_t e : pe)
+      if (e) cudaEventDestroy(e);
+  }
+  if (p->pipe.s_in) cudaStreamDestroy(p->pipe.s_in);
+  if (p->pipe.s_out) cudaStreamDestroy(p->pipe.s_out);
   for (cudaEvent_t e : p->ev) cudaEventDestroy(e);
   for (auto& r : p->trace) {
     cudaEventDestroy(r.b);
@@ -1455,6 +1474,56 @@ nf_status nf_layer_step_host(nf_plan p, const nf_layer_weights* w, const void* x
   }
   NF_CUDA(cudaGraphLaunch(hg->exec, p->s_host));
   NF_CUDA(cudaStreamSynchronize(p->s_host));
+  return NF_OK;
+}
+
+nf_status nf_layer_step_host_async(nf_plan p, const nf_layer_weights* w, const void* x_host,
+                                   void* k_pool, void* v_pool, const int32_t* bt_host,
+                                   const int32_t* sl_host, void* y_host, void* stream) {
+  if (!p) return fail(NF_ERR_INVALID_ARG, "plan is NULL");
+  if (!w || !x_host || !y_host || !bt_host || !sl_host)
+    return fail(NF_ERR_INVALID_ARG, "a host pointer is NULL");
+  auto& q = p->pipe;
+  if (!q.s_in) {
+    for (int i = 0; i < 2; ++i) {
+      NF_TRY(dalloc(&q.x[i], (size_t)p->T_cap * p->shape.hidden * 2));
+      NF_TRY(dalloc(&q.y[i], (size_t)p->T_cap * p->shape.hidden * 2));
+      NF_TRY(dalloc(&q.bt[i], (size_t)p->seq_cap * p->max_pages * 4));
+      NF_TRY(dalloc(&q.sl[i], (size_t)p->seq_cap * 4));
+      NF_CUDA(cudaEventCreateWithFlags(&q.in_done[i], cudaEventDisableTiming));
+      NF_CUDA(cudaEventCreateWithFlags(&q.step_done[i], cudaEventDisableTiming));
+      NF_CUDA(cudaEventCreateWithFlags(&q.out_done[i], cudaEventDisableTiming));
+    }
+    NF_CUDA(cudaStreamCreateWithFlags(&q.s_in, cudaStreamNonBlocking));
+    NF_CUDA(cudaStreamCreateWithFlags(&q.s_out, cudaStreamNonBlocking));
+  }
+  const int s = q.next;
+  NF_TRY(check_step_args(p, w, q.x[s], k_pool, v_pool, q.bt[s], q.sl[s], q.y[s]));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t xb = (size_t)p->T * p->shape.hidden * 2;
+  const size_t btb = (size_t)p->n_seq * p->max_pages * 4, slb = (size_t)p->n_seq * 4;
+  // inputs into slot s once the step two calls back (the slot's last reader) is done
+  NF_CUDA(cudaStreamWaitEvent(q.s_in, q.step_done[s], 0));
+  NF_CUDA(cudaMemcpyAsync(q.x[s], x_host, xb, cudaMemcpyHostToDevice, q.s_in));
+  NF_CUDA(cudaMemcpyAsync(q.bt[s], bt_host, btb, cudaMemcpyHostToDevice, q.s_in));
+  NF_CUDA(cudaMemcpyAsync(q.sl[s], sl_host, slb, cudaMemcpyHostToDevice, q.s_in));
+  NF_CUDA(cudaEventRecord(q.in_done[s], q.s_in));
+  // the step, once its inputs landed and the slot's previous y was copied out
+  NF_CUDA(cudaStreamWaitEvent(st, q.in_done[s], 0));
+  NF_CUDA(cudaStreamWaitEvent(st, q.out_done[s], 0));
+  NF_TRY(layer_step(p, w, q.x[s], k_pool, v_pool, q.bt[s], q.sl[s], q.y[s], st));
+  NF_CUDA(cudaEventRecord(q.step_done[s], st));
+  // y out
+  NF_CUDA(cudaStreamWaitEvent(q.s_out, q.step_done[s], 0));
+  NF_CUDA(cudaMemcpyAsync(y_host, q.y[s], xb, cudaMemcpyDeviceToHost, q.s_out));
+  NF_CUDA(cudaEventRecord(q.out_done[s], q.s_out));
+  q.next = s ^ 1;
+  return NF_OK;
+}
+
+nf_status nf_plan_host_wait(nf_plan p) {
+  if (!p) return fail(NF_ERR_INVALID_ARG, "plan is NULL");
+  if (p->pipe.s_out) NF_CUDA(cudaStreamSynchronize(p->pipe.s_out));
   return NF_OK;
 }
 

@@ -173,6 +173,33 @@ def test_host_entry_point_graph_replay_reads_fresh_inputs(tiny, executor):
     plan.close()
 
 
+@pytest.mark.parametrize("executor", [_lib.NF_EXEC_SEQUENTIAL, _lib.NF_EXEC_STREAMS])
+def test_host_entry_point_pipelined_steps(tiny, executor):
+    """nf_layer_step_host_async: five steps enqueued back to back (different x,
+    separate y buffers; the staging slots alternate), then one wait; each y
+    matches the device entry point bit for bit."""
+    case, _ = tiny
+    T, H = case.batch.n_tokens, case.shape.hidden
+    bt, sl = torch.from_numpy(case.batch.block_table), torch.from_numpy(case.batch.seq_lens)
+    bth, slh = bt.pin_memory(), sl.pin_memory()
+    plan = _lib.Plan(case.shape, case.batch,
+                     _lib.make_opts(T, [0, 18, T], executor=executor, attn_sms=30))
+    kp, vp = case.kp.clone(), case.vp.clone()
+    xs = [wl.make_x(case.shape, T, seed=200 + i).pin_memory() for i in range(5)]
+    ys = [torch.empty(T, H, dtype=torch.bfloat16).pin_memory() for _ in range(5)]
+    for xh, yh in zip(xs, ys):
+        _lib.layer_step_host_async(plan, case.wd, xh, kp, vp, bth, slh, yh)
+    _lib.host_wait(plan)
+    for i, (xh, yh) in enumerate(zip(xs, ys)):
+        kd, vd = case.kp.clone(), case.vp.clone()
+        yd = torch.empty(T, H, dtype=torch.bfloat16, device=DEV)
+        _lib.layer_step(plan, case.wd, xh.to(DEV), kd, vd, bt.to(DEV), sl.to(DEV), yd)
+        torch.cuda.synchronize()
+        assert torch.equal(yh, yd.cpu()), f"step {i}"
+    plan.poll()
+    plan.close()
+
+
 def test_plan_save_load_and_search(tiny, tmp_path):
     case, ref = tiny
     T = case.batch.n_tokens
