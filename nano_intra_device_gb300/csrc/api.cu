@@ -676,15 +676,16 @@ int pick_bn(int m_tiles, int N, int grid) {
 
 // Weight-row GEMM (gemm_wrows.cu) for nano-operations of few tokens: the
 // token tile, the cluster size (K splits) and the cluster count.  Measured on
-// GB300: one CTA streams weights at about 40 GB/s (a ring of 128 KB in
-// flight), the device as a whole at up to 6.4 TB/s, and each tile ends in an
-// exchange round of a few microseconds.  The time of a choice is the larger of
+// GB300: with most SMs streaming, one CTA pulls weights at about 40 GB/s (its
+// share of the device's read bandwidth; alone it reaches ~110 GB/s), the
+// device as a whole up to 6.4 TB/s, and each tile ends in an exchange round of
+// a few microseconds.  The time of a choice is the larger of
 // the per-CTA stream and the weight stream at min(HBM, CTAs x per-CTA rate),
 // plus one exchange per wave of tiles.  A cluster of several CTAs waits for its
 // slowest member at every tile, which measured far slower than the model when
 // clusters walk several tiles, so K is split only when every tile has its own
-// cluster.  Two-operand tiles (QKV, SwiGLU) with 128 tokens have a 3-stage
-// ring and lost to the token-row tiles: they take at most 64 tokens.
+// cluster.  Two-operand tiles (QKV, SwiGLU) with 128 tokens measured slower
+// than the token-row tiles (gate/up 72 vs 64 us): they take at most 64 tokens.
 constexpr int kWrMaxTokens = 128;       // larger nano-operations take token-row tiles
 constexpr int kWrMaxTokensDual = 64;
 constexpr double kWrSmRate = 40e9;      // weight bytes/s one CTA streams
