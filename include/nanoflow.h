@@ -238,6 +238,17 @@ nf_status nf_stack_step(nf_plan plan, const nf_stack_weights* w, const int32_t* 
                         void* const* k_pools, void* const* v_pools, const int32_t* block_table,
                         const int32_t* seq_lens, void* logits, void* stream);
 
+/* The same step with logits only for the rows that need them (a serving loop
+ * samples one token per emitting row): rows [n_rows] are device int32 token
+ * indices in [0, T) (an index outside makes nf_plan_poll report NF_ERR_DEVICE and
+ * gives a zero row), logits [n_rows, vocab] row i for token rows[i].  The last
+ * hidden states of those rows are gathered before the final RMSNorm, so the
+ * LM head multiplies n_rows rows instead of T.  0 <= n_rows <= T. */
+nf_status nf_stack_step_rows(nf_plan plan, const nf_stack_weights* w, const int32_t* tokens,
+                             void* const* k_pools, void* const* v_pools,
+                             const int32_t* block_table, const int32_t* seq_lens,
+                             const int32_t* rows, int32_t n_rows, void* logits, void* stream);
+
 /* n_layers decoder layers over one mixed step, hidden states in and out
  * ("NanoFlow: Towards Optimal LLM Serving Throughput", "Example Pipelines for
  * Different Model Scales": the per-layer pipeline repeated over the layers a

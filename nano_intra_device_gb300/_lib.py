@@ -94,6 +94,8 @@ _SIGS = {
     "nf_plan_host_wait": (c_int, [c_void_p]),
     "nf_plan_poll": (c_int, [c_void_p, c_int]),
     "nf_stack_step": (c_int, [c_void_p, POINTER(nf_stack_weights), c_void_p, POINTER(c_void_p), POINTER(c_void_p), c_void_p, c_void_p, c_void_p, c_void_p]),
+    "nf_stack_step_rows": (c_int, [c_void_p, POINTER(nf_stack_weights), c_void_p, POINTER(c_void_p), POINTER(c_void_p),
+                                   c_void_p, c_void_p, c_void_p, c_int32, c_void_p, c_void_p]),
     "nf_layers_step": (c_int, [c_void_p, POINTER(nf_layer_weights), c_int32, c_void_p, POINTER(c_void_p), POINTER(c_void_p), c_void_p, c_void_p, c_void_p, c_void_p]),
     "nf_plan_set_batch": (c_int, [c_void_p, POINTER(nf_batch_desc), POINTER(nf_plan_opts), c_void_p]),
     "nf_runtime_create": (c_int, [POINTER(nf_model_shape), POINTER(nf_runtime_opts), POINTER(c_void_p)]),
@@ -307,6 +309,14 @@ class StackArgs:
 def stack_step(plan: Plan, args: StackArgs, tokens, block_table, seq_lens, logits, stream=None):
     check(lib().nf_stack_step(plan.h, ctypes.byref(args.w), ptr(tokens), args.kps, args.vps,
                               ptr(block_table), ptr(seq_lens), ptr(logits), stream_handle(stream)))
+
+
+def stack_step_rows(plan: Plan, args: StackArgs, tokens, block_table, seq_lens, rows, logits,
+                    stream=None):
+    """nf_stack_step_rows: logits [len(rows), vocab] for the listed token rows only."""
+    check(lib().nf_stack_step_rows(plan.h, ctypes.byref(args.w), ptr(tokens), args.kps, args.vps,
+                                   ptr(block_table), ptr(seq_lens), ptr(rows), rows.numel(),
+                                   ptr(logits), stream_handle(stream)))
 
 
 class LayersArgs:

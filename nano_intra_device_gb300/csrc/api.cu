@@ -955,7 +955,8 @@ nf_status run_moe_ffn(nf_plan p, const nf_layer_weights* w, void* y, int r0, int
   const int n = r1 - r0, k = s.top_k, E = s.n_experts;
   NF_CUDA(nf::launch_moe_route(static_cast<const float*>(w->router_logits), r0, n, E, k,
                                p->moe_off, p->moe_perm, p->moe_pair_row, p->moe_pair_w, st));
-  NF_CUDA(nf::launch_gather_rows(p->n2, p->moe_perm, p->moe_a, n * k, s.hidden, st));
+  NF_CUDA(nf::launch_gather_rows(p->n2, p->moe_perm, p->moe_a, n * k, s.hidden, p->T, p->status,
+                                 st));
   GemmArgs g = base_args(p);
   g.N = s.ffn;
   g.K = s.hidden;
@@ -1311,9 +1312,13 @@ nf_status nf_layers_step(nf_plan p, const nf_layer_weights* layers, int32_t n_la
                     static_cast<cudaStream_t>(stream));
 }
 
-nf_status nf_stack_step(nf_plan p, const nf_stack_weights* sw, const int32_t* tokens,
-                        void* const* k_pools, void* const* v_pools, const int32_t* bt,
-                        const int32_t* sl, void* logits, void* stream) {
+namespace {
+// The stack step; select: logits only for the n_rows rows listed in `rows`
+// (device indices), gathered after the last layer, in that order.
+nf_status stack_step(nf_plan p, const nf_stack_weights* sw, const int32_t* tokens,
+                     void* const* k_pools, void* const* v_pools, const int32_t* bt,
+                     const int32_t* sl, bool select, const int32_t* rows, int n_rows,
+                     void* logits, void* stream) {
   if (!p || !sw || !tokens || !k_pools || !v_pools || !bt || !sl || !logits)
     return fail(NF_ERR_INVALID_ARG, "NULL argument");
   if (sw->n_layers < 1 || !sw->layers || !sw->embed || !sw->norm_f || !sw->lm_head)
@@ -1343,35 +1348,62 @@ nf_status nf_stack_step(nf_plan p, const nf_stack_weights* sw, const int32_t* to
   __nv_bfloat16* last = sw->n_layers % 2 ? p->xb : p->xa;
   NF_TRY(run_layers(p, sw->layers, sw->n_layers, p->xa, k_pools, v_pools, bt, sl, last, st));
   const __nv_bfloat16* cur = last;
-  // final RMSNorm and the LM head: logits = RMSNorm(x) lm_head^T
-  NF_CUDA(nf::launch_rmsnorm(cur, static_cast<const __nv_bfloat16*>(sw->norm_f), p->n1, 0, p->T,
-                             s.hidden, s.rms_eps, st));
+  // final RMSNorm and the LM head: logits = RMSNorm(x) lm_head^T, for every
+  // row, or for the selected rows gathered first (into n1, normalised into n2)
+  const int M = select ? n_rows : p->T;
+  if (M == 0) return NF_OK;
+  const int xm = select ? XM_N2 : XM_N1;
+  if (select) {
+    NF_CUDA(nf::launch_gather_rows(cur, rows, p->n1, n_rows, s.hidden, p->T, p->status, st));
+    NF_CUDA(nf::launch_rmsnorm(p->n1, static_cast<const __nv_bfloat16*>(sw->norm_f), p->n2, 0,
+                               n_rows, s.hidden, s.rms_eps, st));
+  } else {
+    NF_CUDA(nf::launch_rmsnorm(cur, static_cast<const __nv_bfloat16*>(sw->norm_f), p->n1, 0, p->T,
+                               s.hidden, s.rms_eps, st));
+  }
   GemmArgs g = base_args(p);
   g.stages = 4;
   g.m_begin = 0;
-  g.m_end = p->T;
+  g.m_end = M;
   g.N = sw->vocab;
   g.K = s.hidden;
-  g.m_tiles = (p->T + 127) / 128;
+  g.m_tiles = (M + 127) / 128;
   g.n_tiles = (sw->vocab + 255) / 256;
   g.C = static_cast<__nv_bfloat16*>(logits);
   g.ldc = sw->vocab;
-  if (use_wrows(p, p->T)) {
+  if (use_wrows(p, M)) {
     const int w_tiles = (sw->vocab + 127) / 128;
-    const WrChoice c = wr_choose(nf::EPI_STORE, p->T, w_tiles, g.K, p->num_sms);
+    const WrChoice c = wr_choose(nf::EPI_STORE, M, w_tiles, g.K, p->num_sms);
     if (c.splits) {
       g.n_tiles = w_tiles;
-      g.m_tiles = (p->T + c.tok - 1) / c.tok;
+      g.m_tiles = (M + c.tok - 1) / c.tok;
       g.splits = c.splits;
       NF_CUDA(nf::launch_gemm_wrows(nf::EPI_STORE, c.tok, p->tm_lm128, p->tm_lm128,
-                                    xmap(p, XM_N1, c.tok), g, c.clusters, true, st));
+                                    xmap(p, xm, c.tok), g, c.clusters, true, st));
       return NF_OK;
     }
   }
   g.splits = p->opts.gemm_split_k == 1 ? 1 : choose_splits(g.m_tiles * g.n_tiles, g.K, p->num_sms);
-  NF_CUDA(nf::launch_gemm(nf::EPI_STORE, p->tm_n1, p->tm_lm, p->tm_lm, g,
+  NF_CUDA(nf::launch_gemm(nf::EPI_STORE, select ? p->tm_n2 : p->tm_n1, p->tm_lm, p->tm_lm, g,
                           cap_grid(g.m_tiles * g.n_tiles * g.splits, p->num_sms), st));
   return NF_OK;
+}
+}  // namespace
+
+nf_status nf_stack_step(nf_plan p, const nf_stack_weights* sw, const int32_t* tokens,
+                        void* const* k_pools, void* const* v_pools, const int32_t* bt,
+                        const int32_t* sl, void* logits, void* stream) {
+  return stack_step(p, sw, tokens, k_pools, v_pools, bt, sl, false, nullptr, 0, logits, stream);
+}
+
+nf_status nf_stack_step_rows(nf_plan p, const nf_stack_weights* sw, const int32_t* tokens,
+                             void* const* k_pools, void* const* v_pools, const int32_t* bt,
+                             const int32_t* sl, const int32_t* rows, int32_t n_rows, void* logits,
+                             void* stream) {
+  if (!p) return fail(NF_ERR_INVALID_ARG, "plan is NULL");
+  if (n_rows < 0 || n_rows > p->T || (n_rows > 0 && !rows))
+    return fail(NF_ERR_INVALID_ARG, "n_rows must be in [0, %d] with a row list", p->T);
+  return stack_step(p, sw, tokens, k_pools, v_pools, bt, sl, true, rows, n_rows, logits, stream);
 }
 
 namespace {

@@ -97,9 +97,11 @@ int gemm_wrows_max_clusters(int epi, int tok, int cluster);
 cudaError_t launch_moe_route(const float* logits, int r0, int n, int n_experts, int top_k,
                              int* group_off, int* perm_tok, int* pair_row, float* pair_w,
                              cudaStream_t stream);
-// dst[row] = src[perm_tok[row]] for row < rows (bf16 rows of `cols`, cols % 8 == 0).
+// dst[row] = src[perm_tok[row]] for row < rows (bf16 rows of `cols`, cols % 8 == 0);
+// an index outside [0, src_rows) gives a zero row and flags ST_BAD_LEN.
 cudaError_t launch_gather_rows(const __nv_bfloat16* src, const int* perm_tok, __nv_bfloat16* dst,
-                               int rows, int cols, cudaStream_t stream);
+                               int rows, int cols, int src_rows, uint32_t* status,
+                               cudaStream_t stream);
 // y[t] = h[t] + sum_j pair_w[i k + j] * part[pair_row[i k + j]] for t = r0 + i, i < n
 // (fp32 sum in choice order, one bf16 rounding).
 cudaError_t launch_moe_combine(const __nv_bfloat16* h, const float* part, const int* pair_row,

@@ -126,21 +126,30 @@ cudaError_t launch_moe_route(const float* logits, int r0, int n, int n_experts, 
 }
 
 __global__ void gather_rows_kernel(const uint4* __restrict__ src, const int* __restrict__ perm_tok,
-                                   uint4* __restrict__ dst, int rows, int vec_per_row) {
+                                   uint4* __restrict__ dst, int rows, int vec_per_row, int src_rows,
+                                   uint32_t* status) {
   for (int row = blockIdx.x; row < rows; row += gridDim.x) {
-    const uint4* s = src + static_cast<size_t>(perm_tok[row]) * vec_per_row;
+    const int from = perm_tok[row];
     uint4* d = dst + static_cast<size_t>(row) * vec_per_row;
+    if (from < 0 || from >= src_rows) {  // never read outside src: a zero row, flagged
+      if (threadIdx.x == 0) raise_status(status, ST_BAD_LEN);
+      for (int i = threadIdx.x; i < vec_per_row; i += blockDim.x) d[i] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
+    const uint4* s = src + static_cast<size_t>(from) * vec_per_row;
     for (int i = threadIdx.x; i < vec_per_row; i += blockDim.x) d[i] = s[i];
   }
 }
 
 cudaError_t launch_gather_rows(const __nv_bfloat16* src, const int* perm_tok, __nv_bfloat16* dst,
-                               int rows, int cols, cudaStream_t stream) {
+                               int rows, int cols, int src_rows, uint32_t* status,
+                               cudaStream_t stream) {
   if (cols % 8 || rows < 0) return cudaErrorInvalidValue;
   if (rows == 0) return cudaSuccess;
   const int grid = rows < 2048 ? rows : 2048;
   gather_rows_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const uint4*>(src), perm_tok,
-                                               reinterpret_cast<uint4*>(dst), rows, cols / 8);
+                                               reinterpret_cast<uint4*>(dst), rows, cols / 8,
+                                               src_rows, status);
   return cudaGetLastError();
 }
 

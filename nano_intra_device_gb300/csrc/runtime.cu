@@ -217,17 +217,15 @@ __global__ void compose_tokens_kernel(const int* row_token, const int* row_slot,
   if (t < n) tokens[t] = row_token[t] >= 0 ? row_token[t] : next_tok[row_slot[t]];
 }
 
-// Greedy sampling of the emitting rows: the index of the largest logit, the
-// lowest index on ties; written to the request's token slot and the row.
-__global__ void __launch_bounds__(256) sample_kernel(const __nv_bfloat16* logits, const int* row_emit,
+// Greedy sampling of the emitting rows: block i takes logits row i, which
+// belongs to token row rows[i]; the index of the largest logit, the lowest
+// index on ties, goes to the request's token slot and to sampled[rows[i]]
+// (rows that emit nothing hold -1, set before).
+__global__ void __launch_bounds__(256) sample_kernel(const __nv_bfloat16* logits, const int* rows,
                                                      const int* row_slot, int* next_tok, int* sampled,
                                                      int vocab) {
-  const int t = blockIdx.x;
-  if (!row_emit[t]) {
-    if (threadIdx.x == 0) sampled[t] = -1;
-    return;
-  }
-  const __nv_bfloat16* row = logits + (size_t)t * vocab;
+  const int t = rows[blockIdx.x];
+  const __nv_bfloat16* row = logits + (size_t)blockIdx.x * vocab;
   float best = -INFINITY;
   int bi = vocab;
   for (int v = threadIdx.x; v < vocab; v += blockDim.x) {
@@ -291,7 +289,7 @@ namespace {
 
 size_t in_ints(const nf_runtime_s* rt) {
   const size_t T = rt->opts.b_dense;
-  return 3 * T + T * rt->opts.max_pages_per_seq + T;
+  return 4 * T + T * rt->opts.max_pages_per_seq + T;
 }
 
 void free_rt(nf_runtime rt) {
@@ -347,7 +345,7 @@ nf_status nf_runtime_create(const nf_model_shape* shape, const nf_runtime_opts* 
   const size_t T = o->b_dense;
   bool ok = s == NF_OK && dalloc((void**)&rt->d_next, (size_t)o->max_requests * 4) &&
             dalloc((void**)&rt->d_tokens, T * 4) && dalloc((void**)&rt->d_sampled, T * 4) &&
-            dalloc((void**)&rt->d_rows, 3 * T * 4) &&
+            dalloc((void**)&rt->d_rows, 4 * T * 4) &&
             dalloc((void**)&rt->d_bt, T * o->max_pages_per_seq * 4) &&
             dalloc((void**)&rt->d_sl, T * 4) &&
             dalloc((void**)&rt->d_logits, T * (size_t)o->vocab * 2);
@@ -467,12 +465,18 @@ nf_status nf_runtime_step(nf_runtime rt, const nf_stack_weights* w, void* const*
   std::copy(rec.row_token.begin(), rec.row_token.end(), h);
   std::copy(rec.row_slot.begin(), rec.row_slot.end(), h + T);
   std::copy(rec.row_emit.begin(), rec.row_emit.end(), h + 2 * T);
-  int* hbt = h + 3 * (size_t)rt->opts.b_dense;
+  // emitting rows, in row order (the LM head runs on these only)
+  int* hrows = h + 3 * (size_t)T;
+  int n_emit = 0;
+  for (int t = 0; t < T; ++t)
+    if (rec.row_emit[t]) hrows[n_emit++] = t;
+  int* hbt = h + 4 * (size_t)rt->opts.b_dense;
   std::copy(rec.block_table.begin(), rec.block_table.end(), hbt);
   int* hsl = hbt + (size_t)rt->opts.b_dense * MP;
   std::copy(rec.seq_lens.begin(), rec.seq_lens.end(), hsl);
-  // the rows' three arrays go to d_rows as [token | slot | emit], each T long
-  if (cudaMemcpyAsync(rt->d_rows, h, 3 * (size_t)T * 4, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+  // the rows' arrays go to d_rows as [token | slot | emit | emitting rows]
+  if (cudaMemcpyAsync(rt->d_rows, h, (3 * (size_t)T + n_emit) * 4, cudaMemcpyHostToDevice, st) !=
+          cudaSuccess ||
       cudaMemcpyAsync(rt->d_bt, hbt, (size_t)n_seq * MP * 4, cudaMemcpyHostToDevice, st) != cudaSuccess ||
       cudaMemcpyAsync(rt->d_sl, hsl, (size_t)n_seq * 4, cudaMemcpyHostToDevice, st) != cudaSuccess)
     return rfail(NF_ERR_CUDA, "runtime input copies failed");
@@ -506,13 +510,17 @@ nf_status nf_runtime_step(nf_runtime rt, const nf_stack_weights* w, void* const*
   }
   const int* d_tok = rt->d_rows;
   const int* d_slot = rt->d_rows + T;
-  const int* d_emit = rt->d_rows + 2 * T;
+  const int* d_sel = rt->d_rows + 3 * T;
   compose_tokens_kernel<<<(T + 255) / 256, 256, 0, st>>>(d_tok, d_slot, rt->d_next, rt->d_tokens, T);
   if (cudaGetLastError() != cudaSuccess) return rfail(NF_ERR_CUDA, "token compose failed");
-  RT_TRY(nf_stack_step(rt->plan, w, rt->d_tokens, k_pools, v_pools, rt->d_bt, rt->d_sl, rt->d_logits,
-                       stream));
-  sample_kernel<<<T, 256, 0, st>>>(rt->d_logits, d_emit, d_slot, rt->d_next, rt->d_sampled,
-                                   rt->opts.vocab);
+  // logits for the emitting rows only, then one sampling block per such row
+  RT_TRY(nf_stack_step_rows(rt->plan, w, rt->d_tokens, k_pools, v_pools, rt->d_bt, rt->d_sl, d_sel,
+                            n_emit, rt->d_logits, stream));
+  if (cudaMemsetAsync(rt->d_sampled, 0xFF, (size_t)T * 4, st) != cudaSuccess)  // -1: no token
+    return rfail(NF_ERR_CUDA, "runtime sampling failed");
+  if (n_emit > 0)
+    sample_kernel<<<n_emit, 256, 0, st>>>(rt->d_logits, d_sel, d_slot, rt->d_next, rt->d_sampled,
+                                          rt->opts.vocab);
   if (cudaGetLastError() != cudaSuccess ||
       cudaMemcpyAsync(rt->h_out[k], rt->d_sampled, (size_t)T * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
       cudaEventRecord(rt->done[k], st) != cudaSuccess)

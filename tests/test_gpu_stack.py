@@ -72,6 +72,36 @@ def test_tiny_stack_matches_oracle(executor, bounds):
         assert torch.isfinite(v[sl_ // P, :, sl_ % P, :]).all()
 
 
+def test_stack_logits_for_selected_rows_only():
+    """nf_stack_step_rows: logits of listed rows (any order) equal those rows of
+    the full step within the GEMM's rounding; no rows is valid; a row index
+    outside the batch is reported by poll, never read."""
+    shape, batch = wl.tiny_shape(), wl.tiny_batch()
+    embed, norm_f, lm_head, tokens, layers, pools = _stack(shape, batch, 2, 96)
+    T = batch.n_tokens
+    opts = _lib.make_opts(T, None, kv_chunk=32)
+    plan, args, full, (tok, bt, sl), _ = _run(shape, batch, opts, embed, norm_f, lm_head, tokens,
+                                              layers, pools)
+    for sel in ([35, 0, 3, 17, 4], list(range(T)), [2]):
+        rows = torch.tensor(sel, dtype=torch.int32, device=DEV)
+        part = torch.empty(len(sel), embed.shape[0], dtype=torch.bfloat16, device=DEV)
+        # the pools carry this step's K/V already: re-running the step rewrites the same slots
+        _lib.stack_step_rows(plan, args, tok, bt, sl, rows, part)
+        plan.poll()
+        compare(f64(part), f64(full)[sel], f"rows {sel[:5]}")
+    empty = torch.empty(0, dtype=torch.int32, device=DEV)
+    _lib.stack_step_rows(plan, args, tok, bt, sl, empty, torch.empty(1, 96, dtype=torch.bfloat16,
+                                                                      device=DEV))
+    plan.poll()
+    bad = torch.tensor([1, T + 5], dtype=torch.int32, device=DEV)
+    out = torch.empty(2, 96, dtype=torch.bfloat16, device=DEV)
+    _lib.stack_step_rows(plan, args, tok, bt, sl, bad, out)
+    with pytest.raises(_lib.NanoflowError):
+        plan.poll()
+    assert bool((out[1] == 0).all())
+    plan.close()
+
+
 def test_llama8b_shaped_two_layer_stack_sampled_rows():
     shape = wl.llama8b_shape()
     ctx = wl.lognormal_contexts(96, 600.0, 1.0, 1, 4096, seed=1)
