@@ -702,7 +702,14 @@ def main():
         nb.close()
         ablation["overlap"] = value / world
 
-    launches_per_step = 1 + 4 * po.n_attn + 3 * po.n_ffn
+    # metadata; per attention nano-batch RMSNorm-1, QKV, decode attention, O, and
+    # the prefill-chunk attention where the nano-batch holds prefill rows (the
+    # tensor-core attention); per FFN nano-batch RMSNorm-2, gate/up, down
+    bounds = list(po.attn_bounds[: po.n_attn + 1])
+    n_dec = wk.batch.n_decode
+    with_prefill = sum(1 for a, b in zip(bounds, bounds[1:]) if b > n_dec) \
+        if po.attn_impl == _lib.NF_ATTN_MMA else 0
+    launches_per_step = 1 + 4 * po.n_attn + with_prefill + 3 * po.n_ffn
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
