@@ -299,6 +299,17 @@ nf_status nf_plan_host_wait(nf_plan plan);
  * the status word), or NF_ERR_CUDA for an asynchronous CUDA error. */
 nf_status nf_plan_poll(nf_plan plan, int wait);
 
+/* Failure-detection self-test: enqueues one warp that waits, through the
+ * bounded wait that every kernel of this library uses, on a shared-memory
+ * barrier that nothing arrives at (arrive = 0), or, as the control, one that
+ * it has arrived at itself (arrive = 1), for at most timeout_ns.  An expired
+ * wait sets the plan's status word as a kernel's would, so nf_plan_poll then
+ * returns NF_ERR_TIMEOUT; nothing else is affected and the plan stays usable.
+ * waited_ns: NULL or a device uint64 that receives the nanoseconds waited.
+ * NF_ERR_INVALID_ARG for a NULL plan or timeout_ns outside [1, 1e10]. */
+nf_status nf_plan_selftest_wait(nf_plan plan, int64_t timeout_ns, int32_t arrive, void* waited_ns,
+                                void* stream);
+
 /* Text of the last error on the calling thread ("" if none). */
 const char* nf_last_error(void);
 

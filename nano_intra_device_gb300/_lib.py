@@ -93,6 +93,7 @@ _SIGS = {
                                          c_void_p, c_void_p, c_void_p]),
     "nf_plan_host_wait": (c_int, [c_void_p]),
     "nf_plan_poll": (c_int, [c_void_p, c_int]),
+    "nf_plan_selftest_wait": (c_int, [c_void_p, c_int64, c_int32, c_void_p, c_void_p]),
     "nf_stack_step": (c_int, [c_void_p, POINTER(nf_stack_weights), c_void_p, POINTER(c_void_p), POINTER(c_void_p), c_void_p, c_void_p, c_void_p, c_void_p]),
     "nf_stack_step_rows": (c_int, [c_void_p, POINTER(nf_stack_weights), c_void_p, POINTER(c_void_p), POINTER(c_void_p),
                                    c_void_p, c_void_p, c_void_p, c_int32, c_void_p, c_void_p]),
@@ -286,6 +287,13 @@ class Plan:
 
     def poll(self, wait=True):
         check(lib().nf_plan_poll(self.h, 1 if wait else 0))
+
+    def selftest_wait(self, timeout_ns, arrive, waited_ns=None, stream=None):
+        """Enqueue the failure-detection self-test (a bounded wait on a barrier
+        nothing arrives at unless `arrive`); waited_ns: optional int64 device
+        tensor that receives the time waited."""
+        check(lib().nf_plan_selftest_wait(self.h, int(timeout_ns), 1 if arrive else 0,
+                                          ptr(waited_ns), stream_handle(stream)))
 
 
 def layer_step(plan: Plan, w: dict, x, k_pool, v_pool, block_table, seq_lens, y, stream=None):

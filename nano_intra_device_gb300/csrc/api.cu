@@ -1659,6 +1659,17 @@ nf_status nf_plan_poll(nf_plan p, int wait) {
   return NF_OK;
 }
 
+nf_status nf_plan_selftest_wait(nf_plan p, int64_t timeout_ns, int32_t arrive, void* waited_ns,
+                                void* stream) {
+  if (!p) return fail(NF_ERR_INVALID_ARG, "plan is NULL");
+  if (timeout_ns < 1 || timeout_ns > 10000000000LL)
+    return fail(NF_ERR_INVALID_ARG, "timeout_ns must lie in [1, 1e10]");
+  NF_CUDA(nf::launch_selftest_wait(p->status, static_cast<unsigned long long>(timeout_ns),
+                                   arrive ? 1 : 0, static_cast<unsigned long long*>(waited_ns),
+                                   static_cast<cudaStream_t>(stream)));
+  return NF_OK;
+}
+
 nf_status nf_step_metadata(nf_plan p, const int32_t* bt, const int32_t* sl, void* stream) {
   if (!p || !bt || !sl) return fail(NF_ERR_INVALID_ARG, "NULL argument");
   return run_meta(p, bt, sl, static_cast<cudaStream_t>(stream));

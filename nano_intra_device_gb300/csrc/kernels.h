@@ -200,4 +200,11 @@ cudaError_t launch_attention_prefill(const AttnArgs& a, const CUtensorMap& tk,
                                      const CUtensorMap& tv, const int4* tiles, int n_tiles,
                                      cudaStream_t stream);
 
+// Failure-detection self-test (selftest.cu): one warp waits, with the bounded
+// wait of every kernel here, on a barrier nothing arrives at (arrive = 0) or
+// that it arrived at itself (1); an expired wait sets ST_TIMEOUT in *status.
+// waited_ns (device, optional) receives the time waited.
+cudaError_t launch_selftest_wait(uint32_t* status, unsigned long long timeout_ns, int arrive,
+                                 unsigned long long* waited_ns, cudaStream_t stream);
+
 }  // namespace nf

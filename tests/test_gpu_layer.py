@@ -277,3 +277,32 @@ def test_llama8b_small_decode_batches(n_tok, nano):
     plan, y, kp, vp = case.run(_lib.make_opts(n_tok, ab, ab, executor=ex, attn_sms=64))
     plan.close()
     _check_layer(case, ref, y, kp, vp, np.arange(n_tok))
+
+
+def test_expired_device_wait_is_reported_and_the_plan_stays_usable(tiny):
+    """Failure detection without a fault: a bounded wait on a barrier that
+    nothing arrives at gives up after its limit, nf_plan_poll reports
+    NF_ERR_TIMEOUT once (and clears it), and the same plan then runs a layer
+    step that matches the oracle; the control (a barrier already arrived at)
+    reports nothing."""
+    case, ref = tiny
+    T = case.batch.n_tokens
+    plan = _lib.Plan(case.shape, case.batch, _lib.make_opts(T))
+    waited = torch.zeros(1, dtype=torch.int64, device=DEV)
+    plan.selftest_wait(1_000_000, arrive=False, waited_ns=waited)      # 1 ms limit
+    with pytest.raises(_lib.NanoflowError) as err:
+        plan.poll()
+    assert err.value.code == _lib.NF_ERR_TIMEOUT
+    assert 1_000_000 <= int(waited.item()) < 1_000_000_000
+    plan.poll()                                    # reported once: the status was cleared
+    plan.selftest_wait(2_000_000_000, arrive=True, waited_ns=waited)
+    plan.poll()
+    assert int(waited.item()) < 1_000_000
+    kp, vp = case.kp.clone(), case.vp.clone()
+    y = torch.empty_like(case.xd)
+    _lib.layer_step(plan, case.wd, case.xd, kp, vp, case.bt, case.sl, y)
+    plan.poll()
+    compare(f64(y), ref["y"], "y after an expired wait")
+    with pytest.raises(_lib.NanoflowError):
+        plan.selftest_wait(0, arrive=True)
+    plan.close()
