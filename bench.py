@@ -291,7 +291,18 @@ def run_stack(args):
     bt = torch.from_numpy(batch.block_table).to(dev)
     sl = torch.from_numpy(batch.seq_lens).to(dev)
     logits = torch.empty(B, vocab, dtype=torch.bfloat16, device=dev)
-    plan = _lib.Plan(shape, batch, None)
+    opts = None  # the library's search
+    if args.plan.startswith("n="):
+        # a forced two-stream plan: with the same nano-batches in both groups the
+        # stack runs the cross-layer window
+        kv = dict(p.split("=") for p in args.plan.split(","))
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        n, a_sms = int(kv["n"]), int(kv.get("sms", sms * 5 // 8))
+        T = batch.n_tokens
+        g = 128 if T >= 128 * n else 1
+        ab = [0] + [max(1, int(round(T * i / n / g))) * g for i in range(1, n)] + [T]
+        opts = _lib.make_opts(T, ab, ab, executor=_lib.NF_EXEC_STREAMS, attn_sms=a_sms)
+    plan = _lib.Plan(shape, batch, opts)
     sa = _lib.StackArgs(embed, norm_f, lm_head, layers, pools)
     stream = torch.cuda.current_stream()
     step = lambda: _lib.stack_step(plan, sa, tokens, bt, sl, logits)  # noqa: E731
@@ -353,10 +364,14 @@ def run_70b(args):
     la = _lib.LayersArgs(layers, pools)
     stream = torch.cuda.current_stream()
     sms = _lib.device_sm_count()
+    # the two-stream candidates run the cross-layer window (no join between
+    # layers); measured on GB300 the optimum is 2 nano-batches with 29-31 % of
+    # the SMs on attention, and the step time moves steeply with that share
     cands = [("search", None), ("sequential", _lib.make_opts(T))]
-    for n in (2, 4):
+    for n, fracs in ((2, (0.27, 0.28, 0.29, 0.30, 0.31, 0.32)), (3, (0.26, 0.27))):
         ab = [0] + [int(round(T * i / n / 128)) * 128 for i in range(1, n)] + [T]
-        for a_sms in (sms * 4 // 16, sms * 6 // 16, sms * 8 // 16):
+        for f in fracs:
+            a_sms = int(round(sms * f))
             cands.append((f"n={n},attn_sms={a_sms}",
                           _lib.make_opts(T, ab, ab, executor=_lib.NF_EXEC_STREAMS, attn_sms=a_sms)))
     tried = {}

@@ -257,7 +257,11 @@ nf_status nf_stack_step_rows(nf_plan plan, const nf_stack_weights* w, const int3
  * layers, k_pools, v_pools: HOST arrays [n_layers] (device weights and pools
  * as for nf_layer_step).  x, y: device [T, H] bf16, distinct; x is not
  * modified.  The step metadata is computed once for all layers.  Allocation
- * and capture behave as for nf_stack_step. */
+ * and capture behave as for nf_stack_step.  With the two-stream executor and
+ * the same n >= 2 nano-batches in both groups (the same holds for
+ * nf_stack_step), the layers are not joined: nano-batch i of layer l + 1
+ * starts right after the FFN of nano-batch i of layer l (the pages'
+ * cross-layer window); results do not depend on it. */
 nf_status nf_layers_step(nf_plan plan, const nf_layer_weights* layers, int32_t n_layers,
                          const void* x, void* const* k_pools, void* const* v_pools,
                          const int32_t* block_table, const int32_t* seq_lens, void* y,

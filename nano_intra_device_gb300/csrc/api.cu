@@ -1276,11 +1276,93 @@ nf_status ensure_layers(nf_plan p, int n_layers) {
   return NF_OK;
 }
 
+// Whether run_layers pipelines nano-batches across layers: the two-stream
+// executor with at least two nano-batches, the same in both groups.
+bool cross_layer(nf_plan p, int n_layers) {
+  const nf_plan_opts& o = p->opts;
+  if (o.executor != NF_EXEC_STREAMS || o.n_attn < 2 || n_layers < 2 || o.n_ffn != o.n_attn)
+    return false;
+  for (int i = 0; i <= o.n_attn; ++i)
+    if (o.attn_bounds[i] != o.ffn_bounds[i]) return false;
+  return true;
+}
+
+// The two-stream executor over several layers with no join between layers
+// (the pages' cross-layer window, "Auto-Search Stage I": the pipeline search
+// spans neighbouring layers): nano-batch i of layer l + 1 starts its QKV
+// projection right after the FFN of nano-batch i of layer l on the GEMM
+// stream, so its attention runs beside the GEMMs of the other nano-batches of
+// layer l instead of waiting for the whole layer.  Order on the streams:
+//   GEMM:      QKV(0, 0..n-1) | O(l, i) FFN(l, i) QKV(l+1, i) for l, then i
+//   attention: A(0, 0..n-1)   | A(l+1, i) after QKV(l+1, i)
+// Every buffer the plan shares between layers (n1, q, o, h, n2, a, the split-K
+// and split-KV workspaces) is either written and read on one stream in that
+// order, or touched on both streams only in rows of different nano-batches;
+// the K/V that the attention of nano-batch i reads were appended by the QKV
+// projections of nano-batches <= i of its layer, which precede it on the GEMM
+// stream.
+nf_status run_layers_pipelined(nf_plan p, const nf_layer_weights* layers, int n_layers,
+                               const std::vector<const void*>& act, void* const* k_pools,
+                               void* const* v_pools, const int32_t* bt, const int32_t* sl,
+                               cudaStream_t st) {
+  const nf_plan_opts& o = p->opts;
+  const int n = o.n_attn, all = p->num_sms;
+  const int attn_grid = o.attn_sms > 0 ? o.attn_sms : (all * 5) / 8;
+  const int gsm = o.gemm_sms > 0 ? o.gemm_sms : (all - attn_grid > 0 ? all - attn_grid : all);
+  struct Reset {
+    nf_plan p;
+    ~Reset() { p->cur_set = 0; }
+  } reset_{p};
+  cudaEvent_t ev_start = p->ev[0], ev_done = p->ev[1];
+  cudaEvent_t* ev_q = &p->ev[2];
+  cudaEvent_t* ev_a = &p->ev[2 + NF_MAX_NANO];
+  NF_CUDA(cudaEventRecord(ev_start, st));
+  NF_CUDA(cudaStreamWaitEvent(p->s_gemm, ev_start, 0));
+  NF_CUDA(cudaStreamWaitEvent(p->s_attn, ev_start, 0));
+  NF_TRY(run_meta(p, bt, sl, p->s_gemm));
+  // QKV of nano-batch i of layer l on the GEMM stream, its attention on the other
+  auto front = [&](int l, int i, int grid) -> nf_status {
+    const nf_layer_weights* w = &layers[l];
+    NF_TRY(refresh_weight_maps(p, w));
+    NF_TRY(run_qkv(p, w, act[l], k_pools[l], v_pools[l], o.attn_bounds[i], o.attn_bounds[i + 1],
+                   grid, p->s_gemm, i));
+    NF_CUDA(cudaEventRecord(ev_q[i], p->s_gemm));
+    NF_CUDA(cudaStreamWaitEvent(p->s_attn, ev_q[i], 0));
+    p->cur_set = l;
+    NF_TRY(run_attention(p, i, p->q, k_pools[l], v_pools[l], bt, p->o, attn_grid, p->s_attn));
+    NF_CUDA(cudaEventRecord(ev_a[i], p->s_attn));
+    return NF_OK;
+  };
+  for (int i = 0; i < n; ++i) NF_TRY(front(0, i, i == 0 ? all : gsm));
+  for (int l = 0; l < n_layers; ++l) {
+    for (int i = 0; i < n; ++i) {
+      // nothing overlaps the last nano-batch of the last layer
+      const int grid = (l == n_layers - 1 && i == n - 1) ? all : gsm;
+      NF_CUDA(cudaStreamWaitEvent(p->s_gemm, ev_a[i], 0));
+      NF_TRY(refresh_weight_maps(p, &layers[l]));
+      NF_TRY(run_oproj(p, act[l], o.attn_bounds[i], o.attn_bounds[i + 1], grid, p->s_gemm, i));
+      NF_TRY(run_ffn(p, &layers[l], const_cast<void*>(act[l + 1]), o.ffn_bounds[i],
+                     o.ffn_bounds[i + 1], grid, p->s_gemm, i));
+      if (l + 1 < n_layers) NF_TRY(front(l + 1, i, gsm));
+    }
+  }
+  NF_CUDA(cudaEventRecord(ev_done, p->s_gemm));
+  NF_CUDA(cudaStreamWaitEvent(st, ev_done, 0));
+  return NF_OK;
+}
+
 // Metadata once, then layer l reads `in` (x for l = 0) and writes `out` (y for
 // the last layer), ping-ponging between the plan's activation buffers.
 nf_status run_layers(nf_plan p, const nf_layer_weights* layers, int n_layers, const void* x,
                      void* const* k_pools, void* const* v_pools, const int32_t* bt,
                      const int32_t* sl, void* y, cudaStream_t st) {
+  if (cross_layer(p, n_layers)) {
+    std::vector<const void*> act(n_layers + 1);
+    act[0] = x;
+    for (int l = 0; l < n_layers; ++l)
+      act[l + 1] = l == n_layers - 1 ? y : (act[l] == p->xa ? (const void*)p->xb : (const void*)p->xa);
+    return run_layers_pipelined(p, layers, n_layers, act, k_pools, v_pools, bt, sl, st);
+  }
   NF_TRY(run_meta(p, bt, sl, st));
   const void* cur = x;
   for (int l = 0; l < n_layers; ++l) {

@@ -51,8 +51,12 @@ def _run(shape, batch, opts, embed, norm_f, lm_head, tokens, layers, pools):
 
 
 @pytest.mark.parametrize("executor,bounds", [(_lib.NF_EXEC_SEQUENTIAL, None),
-                                             (_lib.NF_EXEC_STREAMS, [0, 20, 36])])
+                                             (_lib.NF_EXEC_STREAMS, [0, 20, 36]),
+                                             (_lib.NF_EXEC_STREAMS, [0, 6, 21, 36])])
 def test_tiny_stack_matches_oracle(executor, bounds):
+    """Two-stream plans with the same nano-batches in both groups run the
+    cross-layer window (no join between layers); the tiny batch's prefill
+    sequences cross the nano-batch bounds."""
     shape, batch = wl.tiny_shape(), wl.tiny_batch()
     embed, norm_f, lm_head, tokens, layers, pools = _stack(shape, batch, 3, 96)
     ref = orc.stack_step(shape, embed, norm_f, lm_head, [orc.weights_f64(w) for w in layers],
@@ -102,7 +106,11 @@ def test_stack_logits_for_selected_rows_only():
     plan.close()
 
 
-def test_llama8b_shaped_two_layer_stack_sampled_rows():
+@pytest.mark.parametrize("bounds,attn_sms", [(None, 0), ([0, 112, 128], 76)])
+def test_llama8b_shaped_two_layer_stack_sampled_rows(bounds, attn_sms):
+    """Sequential, and the cross-layer window with the nano-batch bound inside
+    the 32-token prefill chunk (its second part attends to K/V the first part's
+    QKV projection appended)."""
     shape = wl.llama8b_shape()
     ctx = wl.lognormal_contexts(96, 600.0, 1.0, 1, 4096, seed=1)
     batch = wl.make_batch(shape, ctx, [32], None, seed_bt=2, max_pages=4096 // 16)
@@ -111,19 +119,25 @@ def test_llama8b_shaped_two_layer_stack_sampled_rows():
     ref = orc.stack_step(shape, embed, norm_f, lm_head, [orc.weights_f64(w) for w in layers],
                          tokens.numpy(), pools, batch.block_table, batch.seq_lens, batch.q_lens,
                          rows=rows)
-    plan, args, logits, _, _ = _run(shape, batch, _lib.make_opts(batch.n_tokens), embed, norm_f,
-                                    lm_head, tokens, layers, pools)
+    ex = _lib.NF_EXEC_SEQUENTIAL if bounds is None else _lib.NF_EXEC_STREAMS
+    opts = _lib.make_opts(batch.n_tokens, bounds, executor=ex, attn_sms=attn_sms)
+    plan, args, logits, _, _ = _run(shape, batch, opts, embed, norm_f, lm_head, tokens, layers, pools)
     plan.close()
     compare_stack(f64(logits)[rows], ref["logits"], "8B-shaped stack logits", 2)
 
 
-def test_stack_cuda_graph_replay_equals_eager():
+@pytest.mark.parametrize("bounds", [None, [0, 32, 64]])
+def test_stack_cuda_graph_replay_equals_eager(bounds):
+    """A captured stack step replays bit for bit, also with the cross-layer
+    window (two streams forked from and joined to the capturing stream)."""
     shape = wl.llama8b_shape()
     ctx = wl.lognormal_contexts(64, 600.0, 1.0, 1, 2048, seed=3)
     batch = wl.make_batch(shape, ctx, [], None, seed_bt=4, max_pages=2048 // 16)
     embed, norm_f, lm_head, tokens, layers, pools = _stack(shape, batch, 4, 8192, gain_std=0.0)
-    plan, args, logits, (tok, bt, sl), dp = _run(shape, batch, _lib.make_opts(batch.n_tokens), embed,
-                                                 norm_f, lm_head, tokens, layers, pools)
+    ex = _lib.NF_EXEC_SEQUENTIAL if bounds is None else _lib.NF_EXEC_STREAMS
+    opts = _lib.make_opts(batch.n_tokens, bounds, executor=ex, attn_sms=64)
+    plan, args, logits, (tok, bt, sl), dp = _run(shape, batch, opts, embed, norm_f, lm_head, tokens,
+                                                 layers, pools)
     eager = logits.clone()
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
@@ -162,7 +176,8 @@ def _run_layers(shape, batch, opts, layers, pools, x):
 
 @pytest.mark.parametrize("n_layers", [1, 2, 3])
 @pytest.mark.parametrize("executor,bounds", [(_lib.NF_EXEC_SEQUENTIAL, None),
-                                             (_lib.NF_EXEC_STREAMS, [0, 20, 36])])
+                                             (_lib.NF_EXEC_STREAMS, [0, 20, 36]),
+                                             (_lib.NF_EXEC_STREAMS, [0, 5, 19, 30, 36])])
 def test_tiny_layers_step_matches_oracle(n_layers, executor, bounds):
     shape, batch = wl.tiny_shape(), wl.tiny_batch()
     layers = [wl.make_weights(shape, seed=70 + i, gain_std=0.1) for i in range(n_layers)]
