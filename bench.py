@@ -367,13 +367,18 @@ def run_70b(args):
     # the two-stream candidates run the cross-layer window (no join between
     # layers); measured on GB300 the optimum is 2 nano-batches with 29-31 % of
     # the SMs on attention, and the step time moves steeply with that share
+    # (also the pages' 70B structure: 4 attention nano-batches, 2 FFN ones)
     cands = [("search", None), ("sequential", _lib.make_opts(T))]
-    for n, fracs in ((2, (0.27, 0.28, 0.29, 0.30, 0.31, 0.32)), (3, (0.26, 0.27))):
-        ab = [0] + [int(round(T * i / n / 128)) * 128 for i in range(1, n)] + [T]
+
+    def bounds(n):
+        return [0] + [int(round(T * i / n / 128)) * 128 for i in range(1, n)] + [T]
+    for n, nf, fracs in ((2, 2, (0.27, 0.28, 0.29, 0.30, 0.31, 0.32)), (3, 3, (0.26, 0.27)),
+                         (4, 2, (0.26, 0.29))):
         for f in fracs:
             a_sms = int(round(sms * f))
-            cands.append((f"n={n},attn_sms={a_sms}",
-                          _lib.make_opts(T, ab, ab, executor=_lib.NF_EXEC_STREAMS, attn_sms=a_sms)))
+            name = f"n={n},attn_sms={a_sms}" + (f",n_ffn={nf}" if nf != n else "")
+            cands.append((name, _lib.make_opts(T, bounds(n), bounds(nf),
+                                               executor=_lib.NF_EXEC_STREAMS, attn_sms=a_sms)))
     tried = {}
     for name, o in cands:
         plan = _lib.Plan(shape, batch, o)

@@ -1277,24 +1277,22 @@ nf_status ensure_layers(nf_plan p, int n_layers) {
 }
 
 // Whether run_layers pipelines nano-batches across layers: the two-stream
-// executor with at least two nano-batches, the same in both groups.
+// executor with at least two attention nano-batches.
 bool cross_layer(nf_plan p, int n_layers) {
   const nf_plan_opts& o = p->opts;
-  if (o.executor != NF_EXEC_STREAMS || o.n_attn < 2 || n_layers < 2 || o.n_ffn != o.n_attn)
-    return false;
-  for (int i = 0; i <= o.n_attn; ++i)
-    if (o.attn_bounds[i] != o.ffn_bounds[i]) return false;
-  return true;
+  return o.executor == NF_EXEC_STREAMS && o.n_attn >= 2 && n_layers >= 2;
 }
 
 // The two-stream executor over several layers with no join between layers
 // (the pages' cross-layer window, "Auto-Search Stage I": the pipeline search
-// spans neighbouring layers): nano-batch i of layer l + 1 starts its QKV
-// projection right after the FFN of nano-batch i of layer l on the GEMM
-// stream, so its attention runs beside the GEMMs of the other nano-batches of
-// layer l instead of waiting for the whole layer.  Order on the streams:
-//   GEMM:      QKV(0, 0..n-1) | O(l, i) FFN(l, i) QKV(l+1, i) for l, then i
-//   attention: A(0, 0..n-1)   | A(l+1, i) after QKV(l+1, i)
+// spans neighbouring layers): attention nano-batch i of layer l + 1 starts
+// its QKV projection on the GEMM stream as soon as the FFN nano-batches of
+// layer l that cover its rows are done, so its attention runs beside the
+// GEMMs of the other nano-batches of layer l instead of waiting for the whole
+// layer.  Order on the streams (FFN nano-batch j runs after the O projection
+// that completes its rows, as in one layer):
+//   GEMM:      QKV(0, 0..n-1) | O(l, i), FFN(l, j) ..., QKV(l+1, k) ... for l, then i
+//   attention: A(0, 0..n-1)   | A(l+1, k) after QKV(l+1, k)
 // Every buffer the plan shares between layers (n1, q, o, h, n2, a, the split-K
 // and split-KV workspaces) is either written and read on one stream in that
 // order, or touched on both streams only in rows of different nano-batches;
@@ -1335,15 +1333,25 @@ nf_status run_layers_pipelined(nf_plan p, const nf_layer_weights* layers, int n_
   };
   for (int i = 0; i < n; ++i) NF_TRY(front(0, i, i == 0 ? all : gsm));
   for (int l = 0; l < n_layers; ++l) {
+    int next_ffn = 0, next_front = 0;
     for (int i = 0; i < n; ++i) {
-      // nothing overlaps the last nano-batch of the last layer
+      // nothing overlaps what follows the last attention of the last layer
       const int grid = (l == n_layers - 1 && i == n - 1) ? all : gsm;
       NF_CUDA(cudaStreamWaitEvent(p->s_gemm, ev_a[i], 0));
       NF_TRY(refresh_weight_maps(p, &layers[l]));
       NF_TRY(run_oproj(p, act[l], o.attn_bounds[i], o.attn_bounds[i + 1], grid, p->s_gemm, i));
-      NF_TRY(run_ffn(p, &layers[l], const_cast<void*>(act[l + 1]), o.ffn_bounds[i],
-                     o.ffn_bounds[i + 1], grid, p->s_gemm, i));
-      if (l + 1 < n_layers) NF_TRY(front(l + 1, i, gsm));
+      while (next_ffn < o.n_ffn && o.ffn_bounds[next_ffn + 1] <= o.attn_bounds[i + 1]) {
+        NF_TRY(refresh_weight_maps(p, &layers[l]));
+        NF_TRY(run_ffn(p, &layers[l], const_cast<void*>(act[l + 1]), o.ffn_bounds[next_ffn],
+                       o.ffn_bounds[next_ffn + 1], grid, p->s_gemm, next_ffn));
+        ++next_ffn;
+        // the next layer's attention nano-batches whose rows are now complete
+        while (l + 1 < n_layers && next_front < n &&
+               o.attn_bounds[next_front + 1] <= o.ffn_bounds[next_ffn]) {
+          NF_TRY(front(l + 1, next_front, gsm));
+          ++next_front;
+        }
+      }
     }
   }
   NF_CUDA(cudaEventRecord(ev_done, p->s_gemm));

@@ -191,6 +191,26 @@ def test_tiny_layers_step_matches_oracle(n_layers, executor, bounds):
     compare_stack(f64(y), ref["y"], f"{n_layers} tiny layers", n_layers - 1)
 
 
+@pytest.mark.parametrize("ab,fb", [([0, 5, 19, 30, 36], [0, 19, 36]),   # 4-way attention, 2-way FFN
+                                   ([0, 20, 36], [0, 10, 36]),          # FFN bound inside a nano-batch
+                                   ([0, 12, 24, 36], [0, 36])])
+def test_tiny_cross_layer_window_with_other_ffn_splits(ab, fb):
+    """The cross-layer window when the FFN group is split differently from
+    the attention group: a next-layer nano-batch starts once the FFN
+    nano-batches covering its rows are done."""
+    shape, batch = wl.tiny_shape(), wl.tiny_batch()
+    layers = [wl.make_weights(shape, seed=90 + i, gain_std=0.1) for i in range(3)]
+    pools = [wl.make_pools(shape, batch, DEV, seed=95 + i) for i in range(3)]
+    x = wl.make_x(shape, batch.n_tokens, seed=11)
+    ref = orc.layers_step(shape, [orc.weights_f64(w) for w in layers], x, pools,
+                          batch.block_table, batch.seq_lens, batch.q_lens)
+    opts = _lib.make_opts(batch.n_tokens, ab, fb, executor=_lib.NF_EXEC_STREAMS, attn_sms=24,
+                          kv_chunk=32)
+    plan, y = _run_layers(shape, batch, opts, layers, pools, x)
+    plan.close()
+    compare_stack(f64(y), ref["y"], f"3 tiny layers, attention {ab}, FFN {fb}", 2)
+
+
 def test_llama70b_shaped_layer_sampled_rows():
     """One LLaMA-2-70B-shaped layer (hidden 8192, 64 query heads over 8 KV heads,
     FFN 28672) on a mixed batch, sampled rows against the float64 oracle.
