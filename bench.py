@@ -367,8 +367,11 @@ def run_70b(args):
     # the two-stream candidates run the cross-layer window (no join between
     # layers); measured on GB300 the optimum is 2 nano-batches with 29-31 % of
     # the SMs on attention, and the step time moves steeply with that share
-    # (also the pages' 70B structure: 4 attention nano-batches, 2 FFN ones)
-    cands = [("search", None), ("sequential", _lib.make_opts(T))]
+    # (also the pages' 70B structure: 4 attention nano-batches, 2 FFN ones).
+    # "search" is the layer-aware search's pick (it scores the window over the
+    # 10 layers); every candidate's model prediction is reported beside its time.
+    searched, _ = _lib.plan_search(shape, batch, None, sms, n_layers=L)
+    cands = [("search", searched), ("sequential", _lib.make_opts(T))]
 
     def bounds(n):
         return [0] + [int(round(T * i / n / 128)) * 128 for i in range(1, n)] + [T]
@@ -379,11 +382,12 @@ def run_70b(args):
             name = f"n={n},attn_sms={a_sms}" + (f",n_ffn={nf}" if nf != n else "")
             cands.append((name, _lib.make_opts(T, bounds(n), bounds(nf),
                                                executor=_lib.NF_EXEC_STREAMS, attn_sms=a_sms)))
-    tried = {}
+    tried, model = {}, {}
     for name, o in cands:
         plan = _lib.Plan(shape, batch, o)
         tried[name] = (time_steps(lambda: _lib.layers_step(plan, la, x, bt, sl, y), 3, 1, 1, stream),
                        _lib.opts_dict(plan.info()[0]))
+        model[name] = round(_lib.plan_predict(shape, batch, plan.info()[0], None, sms, L) / 1e3, 3)
         plan.poll()
         plan.close()
     best = min(tried, key=lambda k: tried[k][0])
@@ -412,7 +416,8 @@ def run_70b(args):
             "roofline_10_layers": {"frac": rf["t_roof"] / (ms * 1e-3), "t_roof_ms": rf["t_roof"] * 1e3,
                                    "t_flop_ms": rf["t_flop"] * 1e3, "t_byte_ms": rf["t_byte"] * 1e3,
                                    "bound": rf["bound"]},
-            "candidates_ms": {k: round(v[0], 3) for k, v in tried.items()}}
+            "candidates_ms": {k: round(v[0], 3) for k, v in tried.items()},
+            "candidates_model_ms": model}
     print(json.dumps(line), flush=True)
     plan.close()
 

@@ -479,6 +479,26 @@ nf_status nf_plan_search(const nf_model_shape* shape, const nf_batch_desc* batch
                          const char* profile_json, int32_t num_sms, nf_plan_opts* out,
                          double* predicted_us);
 
+/* The same for a step of n_layers layers run by nf_layers_step or
+ * nf_stack_step, whose two-stream plans pipeline nano-batches across layers
+ * (the pages search a window of neighbouring layers): candidates are the
+ * sequential plan and cross-layer plans of 2-4 attention nano-batches (equal
+ * FFN splits, or 2 FFN nano-batches under 4) with the attention share on a
+ * 1/64 grid, each scored by simulating the two streams over all the layers.
+ * The predicted time is that of all n_layers layers.  n_layers = 1 is
+ * nf_plan_search; NF_ERR_INVALID_ARG for n_layers < 1. */
+nf_status nf_plan_search_layers(const nf_model_shape* shape, const nf_batch_desc* batch,
+                                const char* profile_json, int32_t num_sms, int32_t n_layers,
+                                nf_plan_opts* out, double* predicted_us);
+
+/* The time the search's model predicts for a given plan over n_layers layers
+ * (the cross-layer window for a two-stream plan of >= 2 attention nano-batches
+ * when n_layers > 1), in microseconds: for comparing the model with measured
+ * plans.  NF_ERR_INVALID_ARG when the plan's bounds do not describe the batch. */
+nf_status nf_plan_predict(const nf_model_shape* shape, const nf_batch_desc* batch,
+                          const char* profile_json, int32_t num_sms, int32_t n_layers,
+                          const nf_plan_opts* plan, double* predicted_us);
+
 /* ---------------------------------------------------------------------------
  * Runtime around the step ("NanoFlow: Towards Optimal LLM Serving Throughput",
  * "The NanoFlow Runtime System"): requests in, greedy tokens out.

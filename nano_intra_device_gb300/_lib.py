@@ -123,6 +123,8 @@ _SIGS = {
     "nf_plan_trace_read": (c_int, [c_void_p, POINTER(nf_trace_entry), c_int32, POINTER(c_int32)]),
     "nf_profile": (c_int, [POINTER(nf_model_shape), c_int32, c_int32, c_char_p]),
     "nf_plan_search": (c_int, [POINTER(nf_model_shape), POINTER(nf_batch_desc), c_char_p, c_int32, POINTER(nf_plan_opts), POINTER(c_double)]),
+    "nf_plan_search_layers": (c_int, [POINTER(nf_model_shape), POINTER(nf_batch_desc), c_char_p, c_int32, c_int32, POINTER(nf_plan_opts), POINTER(c_double)]),
+    "nf_plan_predict": (c_int, [POINTER(nf_model_shape), POINTER(nf_batch_desc), c_char_p, c_int32, c_int32, POINTER(nf_plan_opts), POINTER(c_double)]),
 }
 
 _lib = None
@@ -400,15 +402,32 @@ def gemm_wrows(A, B, C, R=None, epilogue=NF_EPI_STORE, splits=0, max_sms=0, stre
                               stream_handle(stream)))
 
 
-def plan_search(shape, batch, profile_json=None, num_sms=152):
+def plan_search(shape, batch, profile_json=None, num_sms=152, n_layers=1):
+    """Host-only plan search; n_layers > 1 scores the cross-layer window of
+    nf_layers_step / nf_stack_step (predicted time of all the layers)."""
     o = nf_plan_opts()
     t = c_double()
     s = make_shape(shape)
     b = make_batch_desc(batch, True)
-    check(lib().nf_plan_search(ctypes.byref(s), ctypes.byref(b),
-                               profile_json.encode() if profile_json else None, num_sms,
-                               ctypes.byref(o), ctypes.byref(t)))
+    prof = profile_json.encode() if profile_json else None
+    if n_layers == 1:
+        check(lib().nf_plan_search(ctypes.byref(s), ctypes.byref(b), prof, num_sms,
+                                   ctypes.byref(o), ctypes.byref(t)))
+    else:
+        check(lib().nf_plan_search_layers(ctypes.byref(s), ctypes.byref(b), prof, num_sms,
+                                          n_layers, ctypes.byref(o), ctypes.byref(t)))
     return o, t.value
+
+
+def plan_predict(shape, batch, opts, profile_json=None, num_sms=152, n_layers=1):
+    """Microseconds the search's model predicts for `opts` over n_layers layers."""
+    t = c_double()
+    s = make_shape(shape)
+    b = make_batch_desc(batch, True)
+    check(lib().nf_plan_predict(ctypes.byref(s), ctypes.byref(b),
+                                profile_json.encode() if profile_json else None, num_sms, n_layers,
+                                ctypes.byref(opts), ctypes.byref(t)))
+    return t.value
 
 
 def device_sm_count():

@@ -43,12 +43,23 @@ struct Rates {
                                        // kernel, 8 warps, measured on 57 SMs in the step)
   double gemm_launch_s = 4e-6;
   double attn_launch_s = 4e-6;
-  // Interference measured on the 8B-shaped step with 76 attention SMs: attention
-  // keeps 0.85 of its alone bandwidth beside GEMMs, gate/up + down keep 0.6 ... 0.8
-  // of their per-SM rate beside attention (the lower end for 512-token nano-batches).
+  // tiled prefill attention (tensor cores, K/V from L2): FLOPs/s one SM
+  // sustains (a 2048-token chunk at the 8B shape: 34.4 GFLOP in 131.6 us on 152 SMs)
+  double attn_prefill_flops_per_sm = 1.72e12;
+  // Interference: attention keeps 0.85 of its alone bandwidth beside GEMMs on
+  // other SMs.  A GEMM beside attention keeps 1 - c u^2 of its per-SM rate, u the
+  // share of HBM bandwidth the attention draws: measured 0.6 ... 0.8 (0.65 taken)
+  // at the 8B-shaped step with 76 attention SMs (u ~ 0.75), and at least 0.87
+  // implied by the 70B-shaped step with 46 (u ~ 0.45); c = 0.62 fits both.  A
+  // profile may fix the factor instead (overlap_gemm_factor).
   double overlap_bw_factor = 0.85;     // attention speed kept beside a GEMM on other SMs
-  double overlap_gemm_factor = 0.65;   // GEMM speed kept beside attention on other SMs
+  double gemm_interference = 0.62;     // c
+  double overlap_gemm_factor = 0;      // > 0: GEMM speed kept beside attention, fixed
 };
+
+bool json_has(const std::string& s, const char* key) {
+  return s.find(std::string("\"") + key + "\"") != std::string::npos;
+}
 
 double json_number(const std::string& s, const char* key, double dflt) {
   const std::string k = std::string("\"") + key + "\"";
@@ -74,8 +85,14 @@ bool load_rates(const char* path, Rates* r) {
   r->gemm_launch_s = json_number(s, "gemm_launch_s", r->gemm_launch_s);
   r->attn_launch_s = json_number(s, "attn_launch_s", r->attn_launch_s);
   r->overlap_bw_factor = json_number(s, "overlap_bw_factor", r->overlap_bw_factor);
-  r->overlap_gemm_factor = json_number(s, "overlap_gemm_factor", r->overlap_gemm_factor);
+  // a fitted interference coefficient takes precedence over a fixed factor
+  if (json_has(s, "gemm_interference"))
+    r->gemm_interference = json_number(s, "gemm_interference", r->gemm_interference);
+  else
+    r->overlap_gemm_factor = json_number(s, "overlap_gemm_factor", r->overlap_gemm_factor);
   r->qkv_row_sm_s = json_number(s, "qkv_row_sm_s", r->qkv_row_sm_s);
+  r->attn_prefill_flops_per_sm =
+      json_number(s, "attn_prefill_flops_per_sm", r->attn_prefill_flops_per_sm);
   r->stream_sync_s = json_number(s, "stream_sync_s", r->stream_sync_s);
   return true;
 }
@@ -84,8 +101,14 @@ struct Model {
   nf_model_shape s;
   Rates r;
   int sms;
-  std::vector<double> row_kv_bytes;  // KV bytes each token's attention reads
-  std::vector<double> prefix;        // prefix sums of row_kv_bytes
+  // per token row: the K/V bytes its attention reads from HBM (a decode row
+  // its whole visible K/V; a prefill row a share of it, since the tiled kernel
+  // reads each page once for a tile of rows) and its prefill attention FLOPs
+  std::vector<double> row_kv_bytes;
+  std::vector<double> row_pf_flops;
+  std::vector<double> prefix, prefix_flops;  // prefix sums of both
+  std::vector<double> row_ctx;                // visible positions of each row
+  std::vector<double> prefix_cost;            // prefix sums of the rows' attention seconds
 
   double gemm_time(int rows, int N, int K, int S, int bn) const {
     if (rows <= 0) return 0;
@@ -106,11 +129,21 @@ struct Model {
     if (s.n_experts > 0) rows *= s.top_k;  // every token runs top_k experts
     return gemm_time(rows, s.ffn, s.hidden, S, 128) + gemm_time(rows, s.hidden, s.ffn, S, 256);
   }
+  // 1 / the share of its speed a GEMM keeps beside attention on attn_sms SMs
+  double gemm_slow(int attn_sms) const {
+    double f = r.overlap_gemm_factor;
+    if (f <= 0) {
+      const double u = std::min(r.hbm_bps, attn_sms * r.attn_bps_per_sm) * r.overlap_bw_factor / r.hbm_bps;
+      f = 1.0 - r.gemm_interference * u * u;
+    }
+    return 1.0 / std::max(0.2, f);
+  }
   double attn_time(int r0, int r1, int S, bool overlapped) const {
     const double bytes = prefix[r1] - prefix[r0];
+    const double pf = (prefix_flops[r1] - prefix_flops[r0]) / (S * r.attn_prefill_flops_per_sm);
     double bw = std::min(r.hbm_bps, S * r.attn_bps_per_sm);
     if (overlapped) bw *= r.overlap_bw_factor;
-    return bytes / bw + r.attn_launch_s;
+    return bytes / bw + pf + r.attn_launch_s;
   }
 };
 
@@ -131,7 +164,7 @@ double simulate(const Model& m, const nf_plan_opts& o) {
   const int gsm = o.gemm_sms > 0 ? o.gemm_sms : std::max(1, all - attn_sms);
   double tg = 0, ta = 0;
   std::vector<double> q_done(n), a_done(n);
-  const double slow = 1.0 / m.r.overlap_gemm_factor;
+  const double slow = m.gemm_slow(attn_sms);
   for (int i = 0; i < n; ++i) {
     tg += m.qkv_time(o.attn_bounds[i + 1] - o.attn_bounds[i], i == 0 ? all : gsm) * (i == 0 ? 1.0 : slow);
     q_done[i] = tg;
@@ -156,44 +189,117 @@ double simulate(const Model& m, const nf_plan_opts& o) {
   return tg;
 }
 
-// Boundaries that split the attention bytes of the batch evenly, on a grid.
-void balanced_bounds(const Model& m, int T, int n, int grid, int32_t* b) {
-  b[0] = 0;
-  b[n] = T;
-  const double total = m.prefix[T];
-  for (int i = 1; i < n; ++i) {
-    const double target = total * i / n;
-    int t = int(std::lower_bound(m.prefix.begin(), m.prefix.end(), target) - m.prefix.begin());
-    t = std::max(1, std::min(T - 1, (t + grid / 2) / grid * grid));
-    b[i] = std::max(t, b[i - 1] + 1);
+// The cross-layer window over L layers (api.cu's run_layers_pipelined): the
+// same operations in the same stream order, no join between layers; returns
+// the time of all L layers.  Nothing overlaps the first QKV projection of the
+// first layer and what follows the last attention of the last layer.
+double simulate_window(const Model& m, const nf_plan_opts& o, int L) {
+  const int all = m.sms, n = o.n_attn;
+  const int attn_sms = o.attn_sms;
+  const int gsm = o.gemm_sms > 0 ? o.gemm_sms : std::max(1, all - attn_sms);
+  const double slow = m.gemm_slow(attn_sms), sync = m.r.stream_sync_s;
+  double tg = 0, ta = 0;
+  std::vector<double> a_done(n);
+  auto rows = [&](int i) { return o.attn_bounds[i + 1] - o.attn_bounds[i]; };
+  auto front = [&](int i, int S, double f) {  // QKV on the GEMM stream, then its attention
+    tg += m.qkv_time(rows(i), S) * f;
+    ta = std::max(ta, tg + sync);
+    ta += m.attn_time(o.attn_bounds[i], o.attn_bounds[i + 1], attn_sms, true);
+    a_done[i] = ta;
+  };
+  for (int i = 0; i < n; ++i) front(i, i == 0 ? all : gsm, i == 0 ? 1.0 : slow);
+  for (int l = 0; l < L; ++l) {
+    int next_ffn = 0, next_front = 0;
+    for (int i = 0; i < n; ++i) {
+      const bool tail = l == L - 1 && i == n - 1;
+      const int S = tail ? all : gsm;
+      const double f = tail ? 1.0 : slow;
+      tg = std::max(tg, a_done[i] + sync);  // O projection i waits for attention i
+      tg += m.o_time(rows(i), S) * f;
+      while (next_ffn < o.n_ffn && o.ffn_bounds[next_ffn + 1] <= o.attn_bounds[i + 1]) {
+        tg += m.ffn_time(o.ffn_bounds[next_ffn + 1] - o.ffn_bounds[next_ffn], S) * f;
+        ++next_ffn;
+        while (l + 1 < L && next_front < n && o.attn_bounds[next_front + 1] <= o.ffn_bounds[next_ffn]) {
+          front(next_front, gsm, slow);
+          ++next_front;
+        }
+      }
+    }
   }
-  for (int i = n - 1; i >= 1; --i) b[i] = std::min(b[i], b[i + 1] - 1);
+  return tg;
 }
 
-}  // namespace
-
-extern "C" nf_status nf_plan_search(const nf_model_shape* shape, const nf_batch_desc* batch,
-                                    const char* profile_json, int32_t num_sms, nf_plan_opts* out,
-                                    double* predicted_us) {
-  if (!shape || !batch || !out || num_sms <= 0) return NF_ERR_INVALID_ARG;
-  Model m;
-  m.s = *shape;
-  m.sms = num_sms;
-  if (!load_rates(profile_json, &m.r)) return NF_ERR_INVALID_ARG;
+// The time model of a batch: per-row attention bytes and prefill FLOPs, and
+// the rates (a profile's, else the built-in ones).
+nf_status build_model(const nf_model_shape* shape, const nf_batch_desc* batch,
+                      const char* profile_json, int32_t num_sms, Model* m) {
+  m->s = *shape;
+  m->sms = num_sms;
+  if (!load_rates(profile_json, &m->r)) return NF_ERR_INVALID_ARG;
   const int n_seq = batch->n_decode + batch->n_prefill;
   const double kv_tok = 2.0 * shape->n_kv_heads * shape->head_dim * 2;
+  // rows of a prefill tile (128 query vectors: 128 / GQA group rows)
+  const double tile_rows = 128.0 / std::max(1, shape->n_q_heads / std::max(1, shape->n_kv_heads));
   const int default_ctx = batch->max_pages_per_seq * shape->page_size / 2;
   for (int s = 0; s < n_seq; ++s) {
     const int q = s < batch->n_decode ? 1 : batch->prefill_q_lens[s - batch->n_decode];
     if (q < 1) return NF_ERR_INVALID_ARG;
     const int L = batch->seq_lens_hint ? batch->seq_lens_hint[s]
                                        : (s < batch->n_decode ? default_ctx : q);
-    for (int i = 0; i < q; ++i) m.row_kv_bytes.push_back(double(L - q + i + 1) * kv_tok);
+    const bool pre = s >= batch->n_decode;
+    for (int i = 0; i < q; ++i) {
+      const double vis = double(L - q + i + 1);
+      m->row_kv_bytes.push_back(vis * kv_tok / (pre ? tile_rows : 1.0));
+      m->row_pf_flops.push_back(pre ? 4.0 * shape->n_q_heads * shape->head_dim * vis : 0.0);
+      m->row_ctx.push_back(vis);
+    }
   }
-  const int T = int(m.row_kv_bytes.size());
+  const int T = int(m->row_kv_bytes.size());
   if (T < 1) return NF_ERR_INVALID_ARG;
-  m.prefix.assign(T + 1, 0.0);
-  for (int t = 0; t < T; ++t) m.prefix[t + 1] = m.prefix[t] + m.row_kv_bytes[t];
+  m->prefix.assign(T + 1, 0.0);
+  m->prefix_flops.assign(T + 1, 0.0);
+  for (int t = 0; t < T; ++t) {
+    m->prefix[t + 1] = m->prefix[t] + m->row_kv_bytes[t];
+    m->prefix_flops[t + 1] = m->prefix_flops[t] + m->row_pf_flops[t];
+  }
+
+  // attention cost per row in seconds on the whole GPU: what nano-batch
+  // boundaries balance
+  m->prefix_cost.assign(T + 1, 0.0);
+  for (int t = 0; t < T; ++t)
+    m->prefix_cost[t + 1] = m->prefix_cost[t] + m->row_kv_bytes[t] / m->r.hbm_bps +
+                            m->row_pf_flops[t] / (num_sms * m->r.attn_prefill_flops_per_sm);
+  return NF_OK;
+}
+
+#define NF_MODEL_TRY(x)              \
+  do {                               \
+    const nf_status st_ = (x);       \
+    if (st_ != NF_OK) return st_;    \
+  } while (0)
+
+// Boundaries that split the attention cost of the batch evenly, on a grid.
+void balanced_bounds(const Model& m, int T, int n, int grid, int32_t* b) {
+  b[0] = 0;
+  b[n] = T;
+  const double total = m.prefix_cost[T];
+  for (int i = 1; i < n; ++i) {
+    const double target = total * i / n;
+    int t = int(std::lower_bound(m.prefix_cost.begin(), m.prefix_cost.end(), target) -
+                m.prefix_cost.begin());
+    t = std::max(1, std::min(T - 1, (t + grid / 2) / grid * grid));
+    b[i] = std::max(t, b[i - 1] + 1);
+  }
+  for (int i = n - 1; i >= 1; --i) b[i] = std::min(b[i], b[i + 1] - 1);
+}
+
+nf_status search(const nf_model_shape* shape, const nf_batch_desc* batch, const char* profile_json,
+                 int32_t num_sms, int32_t n_layers, nf_plan_opts* out, double* predicted_us) {
+  if (!shape || !batch || !out || num_sms <= 0 || n_layers < 1) return NF_ERR_INVALID_ARG;
+  Model m;
+  NF_MODEL_TRY(build_model(shape, batch, profile_json, num_sms, &m));
+  const int T = int(m.row_ctx.size());
+  const int n_seq = batch->n_decode + batch->n_prefill;
 
   // Split-KV piece length: the longest that still gives the resident
   // attention warps about one and a half pieces each (load balance), so that a
@@ -209,7 +315,7 @@ extern "C" nf_status nf_plan_search(const nf_model_shape* shape, const nf_batch_
       for (int s = 0; s < n_seq; ++s) {
         const int q = s < batch->n_decode ? 1 : batch->prefill_q_lens[s - batch->n_decode];
         for (int i = 0; i < q; ++i, ++t) {
-          const double ctx = m.row_kv_bytes[t] / kv_tok;
+          const double ctx = m.row_ctx[t];
           pieces += std::ceil(ctx / cand);
         }
       }
@@ -230,9 +336,44 @@ extern "C" nf_status nf_plan_search(const nf_model_shape* shape, const nf_batch_
   best.attn_warps = 8;
   best.gemm_stages = 4;
   best.timeout_ns = 2000000000LL;
-  double best_t = simulate(m, best);
+  double best_t = simulate(m, best) * n_layers;
 
   const int grid = T >= 1024 ? 128 : 1;  // nano-batches are multiples of 128 tokens
+  if (n_layers > 1) {
+    // the cross-layer window: equal splits of both groups, or the pages' 70B
+    // structure of 4 attention and 2 FFN nano-batches; attention shares on a
+    // 1/64 grid (the step time moves steeply with it)
+    for (int n = 2; n <= 4; ++n) {
+      if (T / grid < n) break;
+      nf_plan_opts o = best;
+      o.executor = NF_EXEC_STREAMS;
+      o.n_attn = n;
+      balanced_bounds(m, T, n, grid, o.attn_bounds);
+      for (int nf_ : {n, 2}) {
+        if (nf_ == 2 && n != 4) continue;
+        o.n_ffn = nf_;
+        if (nf_ == n) {
+          for (int i = 0; i <= n; ++i) o.ffn_bounds[i] = o.attn_bounds[i];
+        } else {
+          o.ffn_bounds[0] = 0;
+          o.ffn_bounds[1] = o.attn_bounds[n / 2];
+          o.ffn_bounds[2] = T;
+        }
+        for (int k = 8; k <= 40; ++k) {
+          o.attn_sms = std::max(1, num_sms * k / 64);
+          o.gemm_sms = 0;
+          const double t = simulate_window(m, o, n_layers);
+          if (t < best_t) {
+            best_t = t;
+            best = o;
+          }
+        }
+      }
+    }
+    *out = best;
+    if (predicted_us) *predicted_us = best_t * 1e6;
+    return NF_OK;
+  }
   for (int n = 2; n <= 4; ++n) {
     if (T / grid < n) break;
     nf_plan_opts o = best;
@@ -263,4 +404,47 @@ extern "C" nf_status nf_plan_search(const nf_model_shape* shape, const nf_batch_
   *out = best;
   if (predicted_us) *predicted_us = best_t * 1e6;
   return NF_OK;
+}
+
+// Predicted time of a given plan over n_layers layers, as the search scores it.
+nf_status predict(const nf_model_shape* shape, const nf_batch_desc* batch, const char* profile_json,
+                  int32_t num_sms, int32_t n_layers, const nf_plan_opts* o, double* us) {
+  if (!shape || !batch || !o || !us || num_sms <= 0 || n_layers < 1) return NF_ERR_INVALID_ARG;
+  Model m;
+  NF_MODEL_TRY(build_model(shape, batch, profile_json, num_sms, &m));
+  const int T = int(m.row_ctx.size());
+  for (int g = 0; g < 2; ++g) {  // bounds must describe this batch
+    const int n = g ? o->n_ffn : o->n_attn;
+    const int32_t* b = g ? o->ffn_bounds : o->attn_bounds;
+    if (n < 1 || n > NF_MAX_NANO || b[0] != 0 || b[n] != T) return NF_ERR_INVALID_ARG;
+    for (int i = 0; i < n; ++i)
+      if (b[i + 1] <= b[i]) return NF_ERR_INVALID_ARG;
+  }
+  if (o->executor == NF_EXEC_STREAMS && (o->attn_sms < 0 || o->attn_sms > num_sms))
+    return NF_ERR_INVALID_ARG;
+  const bool window = o->executor == NF_EXEC_STREAMS && o->n_attn >= 2 && n_layers >= 2;
+  const double t = window ? simulate_window(m, *o, n_layers) : simulate(m, *o) * n_layers;
+  *us = t * 1e6;
+  return NF_OK;
+}
+
+}  // namespace
+
+extern "C" nf_status nf_plan_predict(const nf_model_shape* shape, const nf_batch_desc* batch,
+                                     const char* profile_json, int32_t num_sms, int32_t n_layers,
+                                     const nf_plan_opts* plan, double* predicted_us) {
+  return predict(shape, batch, profile_json, num_sms, n_layers, plan, predicted_us);
+}
+
+extern "C" nf_status nf_plan_search(const nf_model_shape* shape, const nf_batch_desc* batch,
+                                    const char* profile_json, int32_t num_sms, nf_plan_opts* out,
+                                    double* predicted_us) {
+  return search(shape, batch, profile_json, num_sms, 1, out, predicted_us);
+}
+
+extern "C" nf_status nf_plan_search_layers(const nf_model_shape* shape, const nf_batch_desc* batch,
+                                           const char* profile_json, int32_t num_sms,
+                                           int32_t n_layers, nf_plan_opts* out,
+                                           double* predicted_us) {
+  return search(shape, batch, profile_json, num_sms, n_layers, out, predicted_us);
 }

@@ -70,3 +70,60 @@ def test_invalid_shape_is_rejected_on_host(L):
     with pytest.raises(_lib.NanoflowError) as e:
         _lib.Plan(shape, batch, _lib.make_opts(batch.n_tokens))
     assert e.value.code in (_lib.NF_ERR_INVALID_ARG, _lib.NF_ERR_CUDA)
+
+
+def _bounds(T, k):
+    g = 128 if T >= 128 * k else 1
+    return [0] + [int(round(T * i / k / g)) * g for i in range(1, k)] + [T]
+
+
+def test_layer_search_follows_the_measured_regimes(L):
+    """The layer-aware search scores the cross-layer window: it keeps the
+    sequential plan where attention is bound by HBM or the prefill attention by
+    the tensor cores (the 8B-shaped decode stack and a serving-like mix, both
+    measured slower when overlapped) and splits the GPU for the GEMM-dominated
+    70B-shaped step (measured faster overlapped)."""
+    s8, s70 = wl.llama8b_shape(), wl.llama70b_shape()
+    dec = wl.make_batch(s8, wl.lognormal_contexts(1024, 600.0, 1.0, 1, 8192, seed=1), [], None,
+                        seed_bt=2, max_pages=8192 // 16)
+    mix = wl.make_batch(s8, wl.lognormal_contexts(512, 600.0, 1.0, 1, 4096, seed=1),
+                        [512, 512, 512], [0, 1024, 2048], seed_bt=2, max_pages=4096 // 16)
+    for b in (dec, mix):
+        o, t = _lib.plan_search(s8, b, None, 152, n_layers=32)
+        _check_plan(o, b.n_tokens, 128)
+        assert o.executor == _lib.NF_EXEC_SEQUENTIAL and o.n_attn == 1
+    b70 = wl.llama70b_batch()
+    o, t = _lib.plan_search(s70, b70, None, 152, n_layers=10)
+    _check_plan(o, b70.n_tokens, 128)
+    assert o.executor == _lib.NF_EXEC_STREAMS and o.n_attn >= 2
+    assert 0.2 * 152 <= o.attn_sms <= 0.45 * 152
+    seq = _lib.plan_predict(s70, b70, _lib.make_opts(b70.n_tokens), None, 152, 10)
+    assert t < seq
+    # the prediction entry scores a plan exactly as the search did
+    assert _lib.plan_predict(s70, b70, o, None, 152, 10) == pytest.approx(t, rel=1e-12)
+    o1, t1 = _lib.plan_search(s8, wl.llama8b_batch(), None, 152)
+    assert _lib.plan_predict(s8, wl.llama8b_batch(), o1, None, 152, 1) == pytest.approx(t1, rel=1e-12)
+
+
+def test_plan_predict_model_properties(L):
+    """Properties of the time model: sequential layers add up; the window of
+    two layers is no slower than two joined layers of the same plan; a prefill
+    chunk costs more after a longer cached prefix; bounds that do not describe
+    the batch are rejected."""
+    s70, b70 = wl.llama70b_shape(), wl.llama70b_batch()
+    T = b70.n_tokens
+    seq = _lib.make_opts(T)
+    one = _lib.plan_predict(s70, b70, seq, None, 152, 1)
+    assert _lib.plan_predict(s70, b70, seq, None, 152, 10) == pytest.approx(10 * one, rel=1e-12)
+    o = _lib.make_opts(T, _bounds(T, 2), _bounds(T, 2), executor=_lib.NF_EXEC_STREAMS, attn_sms=46)
+    assert _lib.plan_predict(s70, b70, o, None, 152, 2) <= 2 * _lib.plan_predict(s70, b70, o, None, 152, 1)
+    s8 = wl.llama8b_shape()
+    short = wl.make_batch(s8, [100] * 64, [512], [0], seed_bt=2, max_pages=256)
+    long_ = wl.make_batch(s8, [100] * 64, [512], [3000], seed_bt=2, max_pages=256)
+    ts = _lib.plan_predict(s8, short, _lib.make_opts(short.n_tokens), None, 152, 1)
+    tl = _lib.plan_predict(s8, long_, _lib.make_opts(long_.n_tokens), None, 152, 1)
+    assert tl > ts
+    with pytest.raises(_lib.NanoflowError):
+        _lib.plan_predict(s70, b70, _lib.make_opts(T - 1), None, 152, 1)
+    with pytest.raises(_lib.NanoflowError):
+        _lib.plan_search(s70, b70, None, 152, n_layers=0)
