@@ -212,11 +212,13 @@ extern "C" nf_status nf_profile(const nf_model_shape* shape, int32_t max_tokens,
   add("hbm_bps", hbm);
   add("attn_bps_per_sm", abw.front().second / abw.front().first);
 
-  // 4) attention beside a GEMM on the other SMs (the measured R -> P table)
+  // 4) attention beside a GEMM on the other SMs (the measured R -> P table),
+  //    and the GEMM's slowdown as a function of the share u of HBM bandwidth
+  //    the attention draws: 1 - p_gemm = c u^2, c fitted by least squares
   js += "  \"overlap\": [";
-  double fac_sum = 0, gfac_sum = 0;
+  double fac_sum = 0, gfac_sum = 0, fit_num = 0, fit_den = 0;
   int fac_n = 0;
-  for (int k = 3; k <= 6; ++k) {
+  for (int k = 2; k <= 6; ++k) {
     const int Sa = sms * k / 8, Sg = sms - Sa;
     const double alone_a = time_ms([&] { nf::attention_on(plan, q, kp, vp, bt, sl, o, Sa, sa); }, sa, 3);
     const double alone_g = time_ms([&] { nf_gemm(A, W, C, nullptr, T, F, H, NF_EPI_SWIGLU, Sg, sg); }, sg, 3);
@@ -243,18 +245,22 @@ extern "C" nf_status nf_profile(const nf_model_shape* shape, int32_t max_tokens,
     cudaEventDestroy(g1);
     const double p_attn = alone_a / ta;
     const double p_gemm = alone_g * reps / tg;
+    const double u = std::min(1.0, kv_bytes / (ta * 1e-3) / hbm);
     fac_sum += p_attn;
     gfac_sum += p_gemm;
+    fit_num += (1.0 - p_gemm) * u * u;
+    fit_den += u * u * u * u;
     ++fac_n;
     std::snprintf(buf, sizeof(buf),
                   "%s{\"attn_sms\": %d, \"gemm_sms\": %d, \"attn_alone_ms\": %.5g, "
-                  "\"attn_overlap_ms\": %.5g, \"p_attn\": %.4g, \"p_gemm\": %.4g}",
-                  k == 3 ? "" : ", ", Sa, Sg, alone_a, (double)ta, p_attn, p_gemm);
+                  "\"attn_overlap_ms\": %.5g, \"p_attn\": %.4g, \"p_gemm\": %.4g, \"u\": %.4g}",
+                  k == 2 ? "" : ", ", Sa, Sg, alone_a, (double)ta, p_attn, p_gemm, u);
     js += buf;
   }
   js += "],\n";
   add("overlap_bw_factor", fac_sum / fac_n);
   add("overlap_gemm_factor", gfac_sum / fac_n);
+  add("gemm_interference", fit_den > 0 ? std::max(0.0, fit_num / fit_den) : 0.62);
   // launch cost: a one-tile GEMM
   add("gemm_launch_s", time_ms([&] { nf_gemm(A, W, C, nullptr, 128, 256, 64, 0, 0, sa); }, sa, 9) * 1e-3);
   add("attn_launch_s", 4e-6);
