@@ -306,3 +306,24 @@ def test_expired_device_wait_is_reported_and_the_plan_stays_usable(tiny):
     with pytest.raises(_lib.NanoflowError):
         plan.selftest_wait(0, arrive=True)
     plan.close()
+
+
+def test_profile_writes_rates_that_the_search_reads(tmp_path):
+    """nf_profile on a small shape: every rate the search reads is present and
+    physically sane (bandwidths below the measured copy peak's order, shares in
+    (0, 1]), and the search accepts the file."""
+    import ctypes
+    import json
+    shape = wl.tiny_shape()
+    path = tmp_path / "rates.json"
+    s = _lib.make_shape(shape)
+    _lib.check(_lib.lib().nf_profile(ctypes.byref(s), 256, 64, str(path).encode()))
+    d = json.loads(path.read_text())
+    for k in ("gemm_flops_per_sm", "hbm_bps", "attn_bps_per_sm", "overlap_bw_factor",
+              "overlap_gemm_factor", "gemm_interference", "gemm_launch_s"):
+        assert k in d and d[k] >= 0, k
+    assert 0 < d["hbm_bps"] < 2e13 and 0 < d["attn_bps_per_sm"] < 1e12
+    assert 0 < d["overlap_bw_factor"] <= 1.5 and 0 < d["overlap_gemm_factor"] <= 1.5
+    assert len(d["overlap"]) == 5 and all(0 <= e["u"] <= 1 for e in d["overlap"])
+    o, t = _lib.plan_search(shape, wl.tiny_batch(), str(path), _lib.device_sm_count())
+    assert o.n_attn >= 1 and t > 0
