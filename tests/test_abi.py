@@ -127,3 +127,10 @@ def test_plan_predict_model_properties(L):
         _lib.plan_predict(s70, b70, _lib.make_opts(T - 1), None, 152, 1)
     with pytest.raises(_lib.NanoflowError):
         _lib.plan_search(s70, b70, None, 152, n_layers=0)
+
+
+def test_empty_batch_is_rejected_on_host(L):
+    shape, batch = wl.tiny_shape(), wl.make_batch(wl.tiny_shape(), [], [], None, max_pages=4)
+    with pytest.raises(_lib.NanoflowError) as e:
+        _lib.Plan(shape, batch, _lib.make_opts(1))
+    assert e.value.code == _lib.NF_ERR_INVALID_ARG

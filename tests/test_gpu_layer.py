@@ -327,3 +327,27 @@ def test_profile_writes_rates_that_the_search_reads(tmp_path):
     assert len(d["overlap"]) == 5 and all(0 <= e["u"] <= 1 for e in d["overlap"])
     o, t = _lib.plan_search(shape, wl.tiny_batch(), str(path), _lib.device_sm_count())
     assert o.n_attn >= 1 and t > 0
+
+
+@pytest.mark.parametrize("decode_ctx,pq,pp,max_pages", [
+    ([1], [], [], 4),                       # one token that attends only to itself
+    ([], [1], [0], 4),                      # a one-token prompt
+    ([64, 16, 17, 33], [], [], 4),          # a row that fills its block table; page edges
+    ([64], [3], [61], 4),                   # a chunk that ends on the last slot of the table
+])
+def test_degenerate_batches_match_the_oracle(decode_ctx, pq, pp, max_pages):
+    """Edge cases of the step: a single token, a one-token prompt, rows whose
+    KV length fills every page of their block table or sits on a page edge,
+    and a prefill chunk whose last token takes the table's last slot."""
+    shape = wl.tiny_shape()
+    batch = wl.make_batch(shape, decode_ctx, pq, pp, seed_bt=9, max_pages=max_pages)
+    case = Case(shape, batch, seed=4)
+    ref = case.oracle()
+    T = batch.n_tokens
+    execs = [(_lib.NF_EXEC_SEQUENTIAL, None)]
+    if T >= 2:
+        execs.append((_lib.NF_EXEC_STREAMS, [0, T // 2, T]))
+    for ex, bounds in execs:
+        plan, y, _, _ = case.run(_lib.make_opts(T, bounds, executor=ex, attn_sms=24, kv_chunk=32))
+        plan.close()
+        compare(f64(y), ref["y"], f"degenerate batch {decode_ctx} {pq}/{pp}, executor {ex}")
