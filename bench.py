@@ -16,7 +16,9 @@ host-buffer entry point: every step copies its inputs in from pinned host
 memory and its output back, overlapped with the neighbouring steps' compute), the roofline of the dominant kernel (paged decode
 attention, HBM-bound) measured inside the timed steps, clocks sampled during
 the timed region, the CPU oracle timed on a bounded sample (cpu_baseline),
-and the sequential / nanobatch-only / overlapped comparison.
+and the sequential / nanobatch-only / overlapped comparison, with the same
+batch also run through 8 layers, sequential against the two-stream plan that
+pipelines nano-batches across layers (ablation_tokens_per_s.cross_layer).
 
 `--impl reference` times the CPU oracle itself on the same workload (bounded
 sample per step) and prints the same line with "impl": "reference".
@@ -58,10 +60,12 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-ablation", action="store_true")
     ap.add_argument("--plan", default="auto", help="auto | search | n=<k>,sms=<s>")
-    ap.add_argument("--workload", default="layer", choices=["layer", "stack", "70b", "moe", "serve"],
+    ap.add_argument("--workload", default="layer",
+                    choices=["layer", "stack", "70b", "layers8b", "moe", "serve"],
                     help="layer: the single 8B-shaped layer step (default); stack: the 32-layer "
                          "8B-shaped stack with embedding and LM head, decode batches; 70b: ten "
-                         "70B-shaped layers over a 4096-token mixed step; moe: one Mixtral-shaped "
+                         "70B-shaped layers over a 4096-token mixed step; layers8b: the layer "
+                         "step's 8B-shaped mixed batch through 16 layers; moe: one Mixtral-shaped "
                          "layer (8 experts, top-2) over a 2048-token mixed step; serve: the "
                          "runtime serving synthetic requests on the 32-layer 8B-shaped stack")
     ap.add_argument("--batch", type=int, default=256, help="decode requests of the stack workload")
@@ -160,6 +164,34 @@ class Workload:
         kv_tok = 2 * s.n_kv * s.head_dim * 2
         qo = 2 * self.T * s.n_q * s.head_dim * 2
         return int(b.seq_lens.sum()) * kv_tok + qo
+
+
+def cross_layer_ablation(wk: Workload, stream, L: int = 8, attn_frac: float = 0.45):
+    """The step's batch through L layers (the step's weights in every layer,
+    each layer its own KV pools), sequential against the two-stream plan with
+    2 nano-batches, which pipelines them across layers: per-layer milliseconds
+    and tokens/s of each."""
+    from nano_intra_device_gb300 import _lib
+    T = wk.T
+    sms = _lib.device_sm_count()
+    pools = [wl.make_pools(wk.shape, wk.batch, wk.dev, seed=200 + l) for l in range(L)]
+    la = _lib.LayersArgs([wk.w] * L, pools)
+    y = torch.empty_like(wk.x)
+    half = int(round(T / 2 / 128)) * 128
+    a_sms = int(round(sms * attn_frac))
+    out = {"layers": L, "overlap_plan": f"n=2,attn_sms={a_sms}"}
+    for name, o in (("sequential", _lib.make_opts(T)),
+                    ("overlap", _lib.make_opts(T, [0, half, T], [0, half, T],
+                                               executor=_lib.NF_EXEC_STREAMS, attn_sms=a_sms))):
+        plan = _lib.Plan(wk.shape, wk.batch, o)
+        ms = time_steps(lambda: _lib.layers_step(plan, la, wk.x, wk.bt, wk.sl, y), 5, 3, 1, stream)
+        plan.poll()
+        plan.close()
+        out[f"{name}_ms_per_layer"] = ms / L
+        out[f"{name}_tokens_per_s"] = T / (ms / L * 1e-3)
+    del pools, la
+    torch.cuda.empty_cache()
+    return out
 
 
 def oracle_sample(wk: Workload, n_decode: int, n_prefill: int, seed: int = 0):
@@ -336,18 +368,16 @@ def run_stack(args):
     plan.close()
 
 
-def run_70b(args):
-    """Ten LLaMA-2-70B-shaped layers over one 4096-token mixed step (3584 decode
-    requests, lognormal KV median 1000 clipped to [1, 4096], plus a 512-token
-    prefill chunk), each layer with its own weights and KV pools, through
-    nf_layers_step.  Plans: the search's pick, sequential, and SM-split overlap
-    candidates, each timed; the fastest is reported."""
+def run_layers_workload(args, shape, batch, L, metric, workload, fracs_by_n):
+    """L layers of `shape`, each with its own weights and KV pools, over one
+    mixed step through nf_layers_step.  Plans: the layer-aware search's pick,
+    sequential, and two-stream candidates (n attention nano-batches, n_ffn FFN
+    ones, attention on a fraction of the SMs), each timed; the fastest is
+    reported, with every candidate's time and the search model's prediction."""
     from nano_intra_device_gb300 import _lib
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    shape = wl.llama70b_shape()
-    batch = wl.llama70b_batch()
-    L, T, H, F = 10, batch.n_tokens, shape.hidden, shape.ffn
+    T, H, F = batch.n_tokens, shape.hidden, shape.ffn
     g = torch.Generator(device=dev).manual_seed(0)
 
     def rn(*sz, std=0.02):
@@ -365,18 +395,15 @@ def run_70b(args):
     stream = torch.cuda.current_stream()
     sms = _lib.device_sm_count()
     # the two-stream candidates run the cross-layer window (no join between
-    # layers); measured on GB300 the optimum is 2 nano-batches with 29-31 % of
-    # the SMs on attention, and the step time moves steeply with that share
-    # (also the pages' 70B structure: 4 attention nano-batches, 2 FFN ones).
-    # "search" is the layer-aware search's pick (it scores the window over the
-    # 10 layers); every candidate's model prediction is reported beside its time.
+    # layers); "search" is the layer-aware search's pick (it scores the window
+    # over all the layers), and each candidate's model prediction is reported
+    # beside its measured time
     searched, _ = _lib.plan_search(shape, batch, None, sms, n_layers=L)
     cands = [("search", searched), ("sequential", _lib.make_opts(T))]
 
     def bounds(n):
         return [0] + [int(round(T * i / n / 128)) * 128 for i in range(1, n)] + [T]
-    for n, nf, fracs in ((2, 2, (0.27, 0.28, 0.29, 0.30, 0.31, 0.32)), (3, 3, (0.26, 0.27)),
-                         (4, 2, (0.26, 0.29))):
+    for (n, nf), fracs in fracs_by_n.items():
         for f in fracs:
             a_sms = int(round(sms * f))
             name = f"n={n},attn_sms={a_sms}" + (f",n_ffn={nf}" if nf != n else "")
@@ -404,22 +431,49 @@ def run_70b(args):
     lw = cm.step_work(shape, batch.seq_lens, batch.q_lens)
     rf = cm.roofline_time({"flops": L * lw["flops"], "bytes": L * lw["bytes"]},
                           pk["bf16_tflops_sustained"] * 1e12, pk["hbm_gbs"] * 1e9)
-    line = {"metric": "tokens/s per GB300 for a 10-layer 70B-shaped mixed step; % of its roofline",
+    line = {"metric": metric,
             "value": T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16",
-            "data": "synthetic", "clocks": clk,
-            "config": {"workload": "llama2-70b-shaped, 10 layers, 4096-token step: 3584 decode "
-                                   "(lognormal KV median 1000, sigma 1, clip [1,4096]) + one "
-                                   "512-token prefill chunk, 16-token pages",
+            "warmup": args.warmup, "ms_per_step": ms, "ms_per_layer": ms / L,
+            "higher_is_better": True, "dtype": "bf16", "data": "synthetic", "clocks": clk,
+            "config": {"workload": workload, "layers": L,
                        "kv_read_gb_per_step": L * lw["kv_read_bytes"] / 1e9,
                        "plan": dict(tried[best][1], chosen=best)},
-            "roofline_10_layers": {"frac": rf["t_roof"] / (ms * 1e-3), "t_roof_ms": rf["t_roof"] * 1e3,
-                                   "t_flop_ms": rf["t_flop"] * 1e3, "t_byte_ms": rf["t_byte"] * 1e3,
-                                   "bound": rf["bound"]},
+            f"roofline_{L}_layers": {"frac": rf["t_roof"] / (ms * 1e-3), "t_roof_ms": rf["t_roof"] * 1e3,
+                                     "t_flop_ms": rf["t_flop"] * 1e3, "t_byte_ms": rf["t_byte"] * 1e3,
+                                     "bound": rf["bound"]},
             "candidates_ms": {k: round(v[0], 3) for k, v in tried.items()},
             "candidates_model_ms": model}
     print(json.dumps(line), flush=True)
     plan.close()
+
+
+def run_70b(args):
+    """Ten LLaMA-2-70B-shaped layers over one 4096-token mixed step (3584 decode
+    requests, lognormal KV median 1000 clipped to [1, 4096], plus a 512-token
+    prefill chunk).  Measured on GB300 the optimum is 2 nano-batches with 29-31 %
+    of the SMs on attention, and the step time moves steeply with that share;
+    the pages' 70B structure (4 attention nano-batches, 2 FFN ones) is among the
+    candidates."""
+    run_layers_workload(
+        args, wl.llama70b_shape(), wl.llama70b_batch(), 10,
+        "tokens/s per GB300 for a 10-layer 70B-shaped mixed step; % of its roofline",
+        "llama2-70b-shaped, 10 layers, 4096-token step: 3584 decode (lognormal KV median 1000, "
+        "sigma 1, clip [1,4096]) + one 512-token prefill chunk, 16-token pages",
+        {(2, 2): (0.27, 0.28, 0.29, 0.30, 0.31, 0.32), (3, 3): (0.26, 0.27), (4, 2): (0.26, 0.29)})
+
+
+def run_layers8b(args):
+    """The 8B-shaped mixed batch of the layer step (1792 decode requests +
+    one 256-token prefill chunk) through 16 layers, each with its own weights
+    and KV pools: the layer step as a model runs it, where the two-stream
+    executor can pipeline nano-batches across layers.  Measured on GB300 the
+    optimum is 2 nano-batches with ~42 % of the SMs on attention."""
+    run_layers_workload(
+        args, wl.llama8b_shape(), wl.llama8b_batch(), 16,
+        "tokens/s per GB300 for the 8B-shaped mixed batch through 16 layers; % of its roofline",
+        "llama3-8b-shaped, 16 layers, 2048-token step: 1792 decode (lognormal KV) + one "
+        "256-token prefill chunk, 16-token pages",
+        {(2, 2): (0.37, 0.39, 0.42, 0.45, 0.47, 0.50), (3, 3): (0.42, 0.46)})
 
 
 def run_moe(args):
@@ -589,6 +643,8 @@ def main():
         return run_stack(args)
     if args.workload == "70b":
         return run_70b(args)
+    if args.workload == "layers8b":
+        return run_layers8b(args)
     if args.workload == "moe":
         return run_moe(args)
     if args.workload == "serve":
@@ -726,6 +782,11 @@ def main():
         ablation["nanobatch_only"] = T / (time_steps(stepper(nb), 10, 3, world, stream) * 1e-3)
         nb.close()
         ablation["overlap"] = value / world
+        if world == 1:
+            # the same batch through several layers, where the overlap can run
+            # across layer boundaries (the single step has a head and a tail
+            # that nothing overlaps)
+            ablation["cross_layer"] = cross_layer_ablation(wk, stream)
 
     # metadata; per attention nano-batch RMSNorm-1, QKV, decode attention, O, and
     # the prefill-chunk attention where the nano-batch holds prefill rows (the
