@@ -232,9 +232,20 @@ double simulate_window(const Model& m, const nf_plan_opts& o, int L) {
 // The time model of a batch: per-row attention bytes and prefill FLOPs, and
 // the rates (a profile's, else the built-in ones).
 nf_status build_model(const nf_model_shape* shape, const nf_batch_desc* batch,
-                      const char* profile_json, int32_t num_sms, Model* m) {
+                      const char* profile_json, int32_t num_sms, bool window, Model* m) {
   m->s = *shape;
   m->sms = num_sms;
+  if (window && !profile_json) {
+    // The cross-layer window's simulation, calibrated on measured window plans
+    // (GB300; the 8B-shaped mixed batch through 16 layers, the 70B-shaped step,
+    // an 8B decode stack, a serving-like mix and MoE layers): these effective
+    // rates give the measured choice between overlap and the sequential plan
+    // in each.  The single-layer simulation keeps the in-step measurements
+    // above, which give its measured choices (the two simulations simplify
+    // different schedules, and their parameters absorb that).
+    m->r.attn_bps_per_sm = 95e9;
+    m->r.qkv_row_sm_s = 7e-6;
+  }
   if (!load_rates(profile_json, &m->r)) return NF_ERR_INVALID_ARG;
   const int n_seq = batch->n_decode + batch->n_prefill;
   const double kv_tok = 2.0 * shape->n_kv_heads * shape->head_dim * 2;
@@ -297,7 +308,7 @@ nf_status search(const nf_model_shape* shape, const nf_batch_desc* batch, const 
                  int32_t num_sms, int32_t n_layers, nf_plan_opts* out, double* predicted_us) {
   if (!shape || !batch || !out || num_sms <= 0 || n_layers < 1) return NF_ERR_INVALID_ARG;
   Model m;
-  NF_MODEL_TRY(build_model(shape, batch, profile_json, num_sms, &m));
+  NF_MODEL_TRY(build_model(shape, batch, profile_json, num_sms, n_layers > 1, &m));
   const int T = int(m.row_ctx.size());
   const int n_seq = batch->n_decode + batch->n_prefill;
 
@@ -337,6 +348,10 @@ nf_status search(const nf_model_shape* shape, const nf_batch_desc* batch, const 
   best.gemm_stages = 4;
   best.timeout_ns = 2000000000LL;
   double best_t = simulate(m, best) * n_layers;
+  // An overlapped plan replaces the sequential one only when the model
+  // predicts it at least 2 % faster: the model's error on measured plans is a
+  // few per cent, the size of the gains it ranks.
+  const double overlap_cap = 0.98 * best_t;
 
   const int grid = T >= 1024 ? 128 : 1;  // nano-batches are multiples of 128 tokens
   if (n_layers > 1) {
@@ -363,7 +378,7 @@ nf_status search(const nf_model_shape* shape, const nf_batch_desc* batch, const 
           o.attn_sms = std::max(1, num_sms * k / 64);
           o.gemm_sms = 0;
           const double t = simulate_window(m, o, n_layers);
-          if (t < best_t) {
+          if (t < best_t && t < overlap_cap) {
             best_t = t;
             best = o;
           }
@@ -394,7 +409,7 @@ nf_status search(const nf_model_shape* shape, const nf_batch_desc* batch, const 
         o.attn_sms = std::max(1, num_sms * k / 16);
         o.gemm_sms = 0;
         const double t = simulate(m, o);
-        if (t < best_t) {
+        if (t < best_t && t < overlap_cap) {
           best_t = t;
           best = o;
         }
@@ -410,8 +425,9 @@ nf_status search(const nf_model_shape* shape, const nf_batch_desc* batch, const 
 nf_status predict(const nf_model_shape* shape, const nf_batch_desc* batch, const char* profile_json,
                   int32_t num_sms, int32_t n_layers, const nf_plan_opts* o, double* us) {
   if (!shape || !batch || !o || !us || num_sms <= 0 || n_layers < 1) return NF_ERR_INVALID_ARG;
+  const bool window = o->executor == NF_EXEC_STREAMS && o->n_attn >= 2 && n_layers >= 2;
   Model m;
-  NF_MODEL_TRY(build_model(shape, batch, profile_json, num_sms, &m));
+  NF_MODEL_TRY(build_model(shape, batch, profile_json, num_sms, n_layers > 1, &m));
   const int T = int(m.row_ctx.size());
   for (int g = 0; g < 2; ++g) {  // bounds must describe this batch
     const int n = g ? o->n_ffn : o->n_attn;
@@ -422,7 +438,6 @@ nf_status predict(const nf_model_shape* shape, const nf_batch_desc* batch, const
   }
   if (o->executor == NF_EXEC_STREAMS && (o->attn_sms < 0 || o->attn_sms > num_sms))
     return NF_ERR_INVALID_ARG;
-  const bool window = o->executor == NF_EXEC_STREAMS && o->n_attn >= 2 && n_layers >= 2;
   const double t = window ? simulate_window(m, *o, n_layers) : simulate(m, *o) * n_layers;
   *us = t * 1e6;
   return NF_OK;

@@ -98,7 +98,7 @@ def test_layer_search_follows_the_measured_regimes(L):
     assert o.executor == _lib.NF_EXEC_STREAMS and o.n_attn >= 2
     assert 0.2 * 152 <= o.attn_sms <= 0.45 * 152
     seq = _lib.plan_predict(s70, b70, _lib.make_opts(b70.n_tokens), None, 152, 10)
-    assert t < seq
+    assert t < 0.98 * seq          # an overlapped plan must be predicted >= 2 % faster
     # the prediction entry scores a plan exactly as the search did
     assert _lib.plan_predict(s70, b70, o, None, 152, 10) == pytest.approx(t, rel=1e-12)
     o1, t1 = _lib.plan_search(s8, wl.llama8b_batch(), None, 152)
@@ -106,17 +106,19 @@ def test_layer_search_follows_the_measured_regimes(L):
 
 
 def test_plan_predict_model_properties(L):
-    """Properties of the time model: sequential layers add up; the window of
-    two layers is no slower than two joined layers of the same plan; a prefill
-    chunk costs more after a longer cached prefix; bounds that do not describe
-    the batch are rejected."""
+    """Properties of the time model: sequential layers add up (multi-layer
+    predictions share one calibration, the window's); a longer window costs
+    more; a prefill chunk costs more after a longer cached prefix; bounds that
+    do not describe the batch are rejected."""
     s70, b70 = wl.llama70b_shape(), wl.llama70b_batch()
     T = b70.n_tokens
     seq = _lib.make_opts(T)
-    one = _lib.plan_predict(s70, b70, seq, None, 152, 1)
-    assert _lib.plan_predict(s70, b70, seq, None, 152, 10) == pytest.approx(10 * one, rel=1e-12)
+    two = _lib.plan_predict(s70, b70, seq, None, 152, 2)
+    assert _lib.plan_predict(s70, b70, seq, None, 152, 10) == pytest.approx(5 * two, rel=1e-12)
     o = _lib.make_opts(T, _bounds(T, 2), _bounds(T, 2), executor=_lib.NF_EXEC_STREAMS, attn_sms=46)
-    assert _lib.plan_predict(s70, b70, o, None, 152, 2) <= 2 * _lib.plan_predict(s70, b70, o, None, 152, 1)
+    w2 = _lib.plan_predict(s70, b70, o, None, 152, 2)
+    w4 = _lib.plan_predict(s70, b70, o, None, 152, 4)
+    assert w2 < w4 < 2 * w2
     s8 = wl.llama8b_shape()
     short = wl.make_batch(s8, [100] * 64, [512], [0], seed_bt=2, max_pages=256)
     long_ = wl.make_batch(s8, [100] * 64, [512], [3000], seed_bt=2, max_pages=256)
