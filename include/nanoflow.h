@@ -455,6 +455,12 @@ typedef struct {
   float ms;
 } nf_trace_entry;
 nf_status nf_plan_trace_enable(nf_plan plan, int32_t max_steps);
+/* Which operations the trace records: bit NF_OP_x of op_mask (default: all).
+ * Each recorded operation adds a CUDA event before and after it on its
+ * stream, and an event between two kernels keeps the second from starting as
+ * a programmatic dependent of the first; recording only what is measured
+ * (e.g. 1 << NF_OP_ATTN) leaves the rest of the step as it runs untraced. */
+nf_status nf_plan_trace_ops(nf_plan plan, uint32_t op_mask);
 nf_status nf_plan_trace_read(nf_plan plan, nf_trace_entry* out, int32_t cap, int32_t* n_out);
 
 /* ---------------------------------------------------------------------------

@@ -120,6 +120,7 @@ _SIGS = {
     "nf_plan_buffer_size": (c_int, [c_void_p, c_int32, POINTER(c_size_t)]),
     "nf_plan_copy_buffer": (c_int, [c_void_p, c_int32, c_void_p, c_size_t]),
     "nf_plan_trace_enable": (c_int, [c_void_p, c_int32]),
+    "nf_plan_trace_ops": (c_int, [c_void_p, ctypes.c_uint32]),
     "nf_plan_trace_read": (c_int, [c_void_p, POINTER(nf_trace_entry), c_int32, POINTER(c_int32)]),
     "nf_profile": (c_int, [POINTER(nf_model_shape), c_int32, c_int32, c_char_p]),
     "nf_plan_search": (c_int, [POINTER(nf_model_shape), POINTER(nf_batch_desc), c_char_p, c_int32, POINTER(nf_plan_opts), POINTER(c_double)]),
@@ -278,6 +279,13 @@ class Plan:
 
     def trace_enable(self, max_steps):
         check(lib().nf_plan_trace_enable(self.h, max_steps))
+
+    def trace_ops(self, ops=None):
+        """Record only the named operations ("meta", "qkv", "attn", "oproj",
+        "ffn"); None: all."""
+        mask = 0xFFFFFFFF if ops is None else sum(
+            1 << k for k, v in NF_OP_NAMES.items() if v in ops)
+        check(lib().nf_plan_trace_ops(self.h, mask))
 
     def trace_read(self):
         n = c_int32()

@@ -182,6 +182,7 @@ struct nf_plan_s {
     cudaEvent_t b, e, s0;
   };
   int trace_left = 0, trace_step = 0;
+  uint32_t trace_ops = ~0u;  // bit NF_OP_x: record that operation
   cudaEvent_t trace_s0 = nullptr;
   std::vector<TraceRec> trace;
   std::vector<cudaEvent_t> ev_pool;
@@ -763,7 +764,7 @@ struct TraceScope {
   int op, nano;
   cudaEvent_t b = nullptr;
   TraceScope(nf_plan p_, cudaStream_t st_, int op_, int nano_) : p(p_), st(st_), op(op_), nano(nano_) {
-    if (p->trace_left > 0 && p->trace_s0) {
+    if (p->trace_left > 0 && p->trace_s0 && ((p->trace_ops >> op) & 1u)) {
       b = pooled_event(p);
       if (b) cudaEventRecord(b, st);
     }
@@ -1886,6 +1887,12 @@ nf_status nf_gemm_wrows(const void* A, const void* B, void* C, const void* R, in
   g.timeout_ns = kDefaultTimeoutNs;
   NF_CUDA(nf::launch_gemm_wrows(epilogue, c.tok, tw, tw2, tx, g, c.clusters, false,
                                 static_cast<cudaStream_t>(stream)));
+  return NF_OK;
+}
+
+nf_status nf_plan_trace_ops(nf_plan p, uint32_t op_mask) {
+  if (!p) return fail(NF_ERR_INVALID_ARG, "plan is NULL");
+  p->trace_ops = op_mask;
   return NF_OK;
 }
 

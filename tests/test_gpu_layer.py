@@ -351,3 +351,26 @@ def test_degenerate_batches_match_the_oracle(decode_ctx, pq, pp, max_pages):
         plan, y, _, _ = case.run(_lib.make_opts(T, bounds, executor=ex, attn_sms=24, kv_chunk=32))
         plan.close()
         compare(f64(y), ref["y"], f"degenerate batch {decode_ctx} {pq}/{pp}, executor {ex}")
+
+
+def test_trace_records_only_the_selected_operations(tiny):
+    """nf_plan_trace_ops: with only attention selected, the trace holds one
+    entry per attention nano-batch per step and nothing else; with all
+    selected, every operation of the step."""
+    case, _ = tiny
+    T = case.batch.n_tokens
+    plan = _lib.Plan(case.shape, case.batch, _lib.make_opts(T, [0, 18, T]))
+    kp, vp = case.kp.clone(), case.vp.clone()
+    y = torch.empty_like(case.xd)
+    for ops, want in ((["attn"], {"attn"}), (None, {"meta", "qkv", "attn", "oproj", "ffn"})):
+        plan.trace_ops(ops)
+        plan.trace_enable(2)
+        for _ in range(2):
+            _lib.layer_step(plan, case.wd, case.xd, kp, vp, case.bt, case.sl, y)
+        plan.poll()
+        tr = plan.trace_read()
+        plan.trace_enable(0)
+        assert {e["op"] for e in tr} == want
+        assert sum(e["op"] == "attn" for e in tr) == 2 * 2          # 2 nano-batches x 2 steps
+        assert all(e["ms"] >= 0 for e in tr)
+    plan.close()
