@@ -525,10 +525,15 @@ def run_moe(args):
     for _ in range(args.warmup):
         _lib.layer_step(plan, w, x, kp, vp, bt, sl, y)
     torch.cuda.synchronize()
-    plan.trace_enable(args.steps)
     clocks.start()
     ms = time_steps(lambda: _lib.layer_step(plan, w, x, kp, vp, bt, sl, y), args.steps, 0, 1, stream)
     clk = clocks.stop()
+    plan.poll()
+    # the per-operation breakdown from three more steps, traced (events between
+    # kernels would perturb the timed ones)
+    plan.trace_enable(3)
+    for _ in range(3):
+        _lib.layer_step(plan, w, x, kp, vp, bt, sl, y)
     plan.poll()
     trace = plan.trace_read()
     plan.trace_enable(0)
