@@ -8,16 +8,27 @@
 // nano-operation from a measured R -> P table.  On one GPU with two resource
 // classes (tensor-core GEMMs, HBM-bound attention) and a fixed operation order
 // the space is small: n <= 4 nano-batches on a 128-token grid, an SM split on a
-// 1/16 grid.  This file enumerates it and scores each candidate with a list-
-// scheduling simulation of the two streams, which is exact under the same
-// time model the MILP would use, and needs no solver.
+// 1/16 grid (1/64 for several layers).  This file enumerates it and scores each
+// candidate with a list-scheduling simulation of the two streams, which is
+// exact under the same time model the MILP would use, and needs no solver.
+// For a step of several layers the simulation follows the cross-layer window
+// of the executor (no join between layers; the pages search a window of
+// neighbouring layers).
 //
 // Time model (per nano-operation, on S SMs):
 //   GEMM M x N x K: waves = ceil(tiles / S) with 128 x 256 tiles, each tile
-//     2*128*256*K / (per-SM tensor rate); plus a launch cost;
-//   attention: KV bytes / min(HBM bandwidth, S * per-SM attention bandwidth);
-//     an SM share is an SM count because every kernel runs one CTA per SM.
-// The rates come from a profile written by nf_profile, else from defaults.
+//     2*128*256*K / (per-SM tensor rate); plus a launch cost; beside attention
+//     a GEMM keeps 1 - c u^2 of its rate, u the share of HBM bandwidth the
+//     attention draws;
+//   attention: decode K/V bytes / min(HBM bandwidth, S * per-SM attention
+//     bandwidth), plus prefill rows' FLOPs at the tiled prefill kernel's per-SM
+//     rate (a prefill row is charged a tile's share of its K/V bytes);
+//     an SM share is an SM count because every kernel runs one CTA per SM;
+//   a fixed cost per cross-stream dependency.
+// The rates come from a profile written by nf_profile, else from built-in
+// GB300 values: in-step measurements for the one-layer simulation, effective
+// values fitted to measured window plans for the multi-layer one.  An
+// overlapped plan must be predicted >= 2 % faster than the sequential one.
 #include <algorithm>
 #include <cmath>
 #include <cstdio>
