@@ -464,7 +464,7 @@ nf_status alloc_plan(nf_plan p) {
   }
   NF_CUDA(cudaStreamCreateWithFlags(&p->s_gemm, cudaStreamNonBlocking));
   NF_CUDA(cudaStreamCreateWithFlags(&p->s_attn, cudaStreamNonBlocking));
-  p->ev.resize(2 + 2 * NF_MAX_NANO);
+  p->ev.resize(4 + 2 * NF_MAX_NANO);  // start, done, QKV and attention per nano-batch, joins
   for (auto& e : p->ev) NF_CUDA(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
   const int BMr = 128;
   if (!nf::make_tmap_bf16(&p->tm_n1, p->n1, T, H, BMr) ||
@@ -872,6 +872,22 @@ nf_status run_attention(nf_plan p, int seg, const void* q, const void* kp, const
   return NF_OK;
 }
 
+// On an early return from a two-stream schedule, orders the caller's stream
+// after whatever the side streams already hold, so that no later work on it
+// overtakes them (the normal end joins through the GEMM stream, which has
+// waited for the last attention).
+struct SideStreamJoin {
+  nf_plan p;
+  cudaStream_t st;
+  bool done = false;
+  ~SideStreamJoin() {
+    if (done) return;
+    cudaEvent_t eg = p->ev[2 + 2 * NF_MAX_NANO], ea = p->ev[3 + 2 * NF_MAX_NANO];
+    if (cudaEventRecord(eg, p->s_gemm) == cudaSuccess) cudaStreamWaitEvent(st, eg, 0);
+    if (cudaEventRecord(ea, p->s_attn) == cudaSuccess) cudaStreamWaitEvent(st, ea, 0);
+  }
+};
+
 // One nano-operation of the layer; which = 0 QKV, 1 O, 2 RMSNorm-2 + gate/up + down.
 nf_status run_qkv(nf_plan p, const nf_layer_weights* w, const void* x, void* kp, void* vp, int r0,
                   int r1, int grid, cudaStream_t st, int nano = 0) {
@@ -1120,6 +1136,7 @@ nf_status layer_step(nf_plan p, const nf_layer_weights* w, const void* x, void* 
   NF_CUDA(cudaEventRecord(ev_start, st));
   NF_CUDA(cudaStreamWaitEvent(p->s_gemm, ev_start, 0));
   NF_CUDA(cudaStreamWaitEvent(p->s_attn, ev_start, 0));
+  SideStreamJoin join_{p, st};
   if (with_meta) NF_TRY(run_meta(p, bt, sl, p->s_gemm));
   for (int i = 0; i < n; ++i) {
     NF_TRY(run_qkv(p, w, x, kp, vp, o.attn_bounds[i], o.attn_bounds[i + 1],
@@ -1144,6 +1161,7 @@ nf_status layer_step(nf_plan p, const nf_layer_weights* w, const void* x, void* 
   }
   NF_CUDA(cudaEventRecord(ev_done, p->s_gemm));
   NF_CUDA(cudaStreamWaitEvent(st, ev_done, 0));
+  join_.done = true;
   return NF_OK;
 }
 
@@ -1318,6 +1336,7 @@ nf_status run_layers_pipelined(nf_plan p, const nf_layer_weights* layers, int n_
   NF_CUDA(cudaEventRecord(ev_start, st));
   NF_CUDA(cudaStreamWaitEvent(p->s_gemm, ev_start, 0));
   NF_CUDA(cudaStreamWaitEvent(p->s_attn, ev_start, 0));
+  SideStreamJoin join_{p, st};
   NF_TRY(run_meta(p, bt, sl, p->s_gemm));
   // QKV of nano-batch i of layer l on the GEMM stream, its attention on the other
   auto front = [&](int l, int i, int grid) -> nf_status {
@@ -1357,6 +1376,7 @@ nf_status run_layers_pipelined(nf_plan p, const nf_layer_weights* layers, int n_
   }
   NF_CUDA(cudaEventRecord(ev_done, p->s_gemm));
   NF_CUDA(cudaStreamWaitEvent(st, ev_done, 0));
+  join_.done = true;
   return NF_OK;
 }
 
