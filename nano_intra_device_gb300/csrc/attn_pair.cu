@@ -456,13 +456,10 @@ static cudaError_t launch_pair_t(const AttnArgs& a, int grid, cudaStream_t strea
   constexpr int V = 4 * GRP;
   constexpr int R = V >= 8 ? V / 8 : V;
   const int smem = PAIRS * (STAGES * 2 * PBLK) + PAIRS * static_cast<int>(sizeof(PairSmem<STAGES, R>)) + 128;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(attn_pair_kernel<GRP, PAIRS, STAGES>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  // once per process (the attribute is per function; thread-safe initialisation)
+  static const cudaError_t attr = cudaFuncSetAttribute(
+      attn_pair_kernel<GRP, PAIRS, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (attr != cudaSuccess) return attr;
   attn_pair_kernel<GRP, PAIRS, STAGES><<<grid, PAIRS * 64, smem, stream>>>(a);
   return cudaGetLastError();
 }

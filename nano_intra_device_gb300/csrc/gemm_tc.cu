@@ -536,14 +536,11 @@ template <int EPI, int STAGES, int BN>
 static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB,
                               const CUtensorMap& tmB2, const GemmArgs& args, int grid,
                               cudaStream_t stream) {
-  static bool attr_set = false;  // per process; the attribute is per function
   constexpr int smem = gemm_smem_bytes(STAGES, BN);
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI, STAGES, BN>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  // once per process (the attribute is per function; thread-safe initialisation)
+  static const cudaError_t attr = cudaFuncSetAttribute(
+      gemm_tc_kernel<EPI, STAGES, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (attr != cudaSuccess) return attr;
   gemm_tc_kernel<EPI, STAGES, BN><<<grid, GEMM_THREADS, smem, stream>>>(tmA, tmB, tmB2, args);
   return cudaGetLastError();
 }
@@ -589,17 +586,17 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 static EncodeTiledFn get_encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
+  // looked up once; the initialisation of a function-local static is
+  // thread-safe, so no caller sees it half done
+  static const EncodeTiledFn fn = [] {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
+      return reinterpret_cast<EncodeTiledFn>(p);
+    return static_cast<EncodeTiledFn>(nullptr);
+  }();
   return fn;
 }
 

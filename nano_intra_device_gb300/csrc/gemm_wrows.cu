@@ -29,6 +29,8 @@
 //    exchange rounds, also after an error (with zeros in place of the
 //    accumulator), and meet at a cluster barrier before they exit, so no CTA
 //    leaves while a peer may still address its shared memory.
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -491,15 +493,11 @@ __global__ void __launch_bounds__(WR_THREADS, 1)
 
 template <int EPI, int TOK, bool ONE>
 cudaError_t wr_prepare() {
-  static bool done = false;  // per process; the attribute is per function
-  if (!done) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_wrows_kernel<EPI, TOK, ONE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         WrCfg<EPI, TOK, ONE>::SMEM);
-    if (e != cudaSuccess) return e;
-    done = true;
-  }
-  return cudaSuccess;
+  // once per process (the attribute is per function; thread-safe initialisation)
+  static const cudaError_t attr =
+      cudaFuncSetAttribute(gemm_wrows_kernel<EPI, TOK, ONE>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, WrCfg<EPI, TOK, ONE>::SMEM);
+  return attr;
 }
 
 template <int EPI, int TOK, bool ONE>
@@ -538,8 +536,8 @@ cudaError_t wr_launch(const CUtensorMap& tmW, const CUtensorMap& tmW2, const CUt
 // Both variants take one SM per CTA, so one query serves them.
 template <int EPI, int TOK>
 int wr_max_clusters(int S) {
-  static int cache[WR_MAX_CLUSTER + 1] = {};
-  if (cache[S] == 0) {
+  static std::atomic<int> cache[WR_MAX_CLUSTER + 1];  // 0: not asked yet
+  if (cache[S].load(std::memory_order_relaxed) == 0) {
     int n = 0;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute at[1];
@@ -550,9 +548,10 @@ int wr_max_clusters(int S) {
       cudaGetLastError();
       n = 0;
     }
-    cache[S] = n > 0 ? n : -1;
+    cache[S].store(n > 0 ? n : -1, std::memory_order_relaxed);
   }
-  return cache[S] > 0 ? cache[S] : 0;
+  const int c = cache[S].load(std::memory_order_relaxed);
+  return c > 0 ? c : 0;
 }
 
 template <int EPI, int TOK>
