@@ -505,6 +505,18 @@ nf_status nf_plan_predict(const nf_model_shape* shape, const nf_batch_desc* batc
                           const char* profile_json, int32_t num_sms, int32_t n_layers,
                           const nf_plan_opts* plan, double* predicted_us);
 
+/* The order in which the two-stream executor issues the nano-operations of
+ * n_layers layers under the cross-layer window (host only; the executor and
+ * the search's simulation both follow it).  Operations in the order of the
+ * GEMM stream, 4 int32 each in out[]: kind (0 QKV projection, followed on the
+ * attention stream by that nano-batch's attention; 1 O projection, which waits
+ * for it; 2 FFN nano-batch), layer, nano-batch index, and 1 where the
+ * operation overlaps nothing and gets every SM.  Writes at most cap
+ * operations and the total count to *n_ops.  NF_ERR_INVALID_ARG when the
+ * plan's bounds are not increasing from 0 to one common end. */
+nf_status nf_window_schedule(const nf_plan_opts* plan, int32_t n_layers, int32_t* out, int32_t cap,
+                             int32_t* n_ops);
+
 /* ---------------------------------------------------------------------------
  * Runtime around the step ("NanoFlow: Towards Optimal LLM Serving Throughput",
  * "The NanoFlow Runtime System"): requests in, greedy tokens out.

@@ -126,6 +126,7 @@ _SIGS = {
     "nf_plan_search": (c_int, [POINTER(nf_model_shape), POINTER(nf_batch_desc), c_char_p, c_int32, POINTER(nf_plan_opts), POINTER(c_double)]),
     "nf_plan_search_layers": (c_int, [POINTER(nf_model_shape), POINTER(nf_batch_desc), c_char_p, c_int32, c_int32, POINTER(nf_plan_opts), POINTER(c_double)]),
     "nf_plan_predict": (c_int, [POINTER(nf_model_shape), POINTER(nf_batch_desc), c_char_p, c_int32, c_int32, POINTER(nf_plan_opts), POINTER(c_double)]),
+    "nf_window_schedule": (c_int, [POINTER(nf_plan_opts), c_int32, POINTER(c_int32), c_int32, POINTER(c_int32)]),
 }
 
 _lib = None
@@ -436,6 +437,17 @@ def plan_predict(shape, batch, opts, profile_json=None, num_sms=152, n_layers=1)
                                 profile_json.encode() if profile_json else None, num_sms, n_layers,
                                 ctypes.byref(opts), ctypes.byref(t)))
     return t.value
+
+
+def window_schedule(opts, n_layers):
+    """The cross-layer window's issue order: [(kind, layer, nano, full)], kind
+    "qkv" (then that nano-batch's attention), "o" or "ffn"."""
+    n = c_int32()
+    check(lib().nf_window_schedule(ctypes.byref(opts), n_layers, None, 0, ctypes.byref(n)))
+    buf = (c_int32 * (4 * max(1, n.value)))()
+    check(lib().nf_window_schedule(ctypes.byref(opts), n_layers, buf, n.value, ctypes.byref(n)))
+    kinds = {0: "qkv", 1: "o", 2: "ffn"}
+    return [(kinds[buf[4 * k]], buf[4 * k + 1], buf[4 * k + 2], buf[4 * k + 3]) for k in range(n.value)]
 
 
 def device_sm_count():

@@ -14,6 +14,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "internal.h"
+#include "schedule.h"
 
 using nf::GemmArgs;
 
@@ -1351,27 +1352,20 @@ nf_status run_layers_pipelined(nf_plan p, const nf_layer_weights* layers, int n_
     NF_CUDA(cudaEventRecord(ev_a[i], p->s_attn));
     return NF_OK;
   };
-  for (int i = 0; i < n; ++i) NF_TRY(front(0, i, i == 0 ? all : gsm));
-  for (int l = 0; l < n_layers; ++l) {
-    int next_ffn = 0, next_front = 0;
-    for (int i = 0; i < n; ++i) {
-      // nothing overlaps what follows the last attention of the last layer
-      const int grid = (l == n_layers - 1 && i == n - 1) ? all : gsm;
-      NF_CUDA(cudaStreamWaitEvent(p->s_gemm, ev_a[i], 0));
+  // the GEMM stream's order (schedule.h, also what the plan search simulates)
+  for (const nf::WindowOp& op : nf::window_schedule(o, n_layers)) {
+    const int grid = op.full ? all : gsm;
+    const int l = op.layer, i = op.nano;
+    if (op.kind == nf::WOP_QKV) {
+      NF_TRY(front(l, i, grid));
+    } else if (op.kind == nf::WOP_O) {
+      NF_CUDA(cudaStreamWaitEvent(p->s_gemm, ev_a[i], 0));  // attention i of layer l
       NF_TRY(refresh_weight_maps(p, &layers[l]));
       NF_TRY(run_oproj(p, act[l], o.attn_bounds[i], o.attn_bounds[i + 1], grid, p->s_gemm, i));
-      while (next_ffn < o.n_ffn && o.ffn_bounds[next_ffn + 1] <= o.attn_bounds[i + 1]) {
-        NF_TRY(refresh_weight_maps(p, &layers[l]));
-        NF_TRY(run_ffn(p, &layers[l], const_cast<void*>(act[l + 1]), o.ffn_bounds[next_ffn],
-                       o.ffn_bounds[next_ffn + 1], grid, p->s_gemm, next_ffn));
-        ++next_ffn;
-        // the next layer's attention nano-batches whose rows are now complete
-        while (l + 1 < n_layers && next_front < n &&
-               o.attn_bounds[next_front + 1] <= o.ffn_bounds[next_ffn]) {
-          NF_TRY(front(l + 1, next_front, gsm));
-          ++next_front;
-        }
-      }
+    } else {
+      NF_TRY(refresh_weight_maps(p, &layers[l]));
+      NF_TRY(run_ffn(p, &layers[l], const_cast<void*>(act[l + 1]), o.ffn_bounds[i],
+                     o.ffn_bounds[i + 1], grid, p->s_gemm, i));
     }
   }
   NF_CUDA(cudaEventRecord(ev_done, p->s_gemm));

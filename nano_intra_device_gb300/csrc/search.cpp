@@ -38,6 +38,7 @@
 #include <vector>
 
 #include "../../include/nanoflow.h"
+#include "schedule.h"
 
 namespace {
 
@@ -211,30 +212,20 @@ double simulate_window(const Model& m, const nf_plan_opts& o, int L) {
   const double slow = m.gemm_slow(attn_sms), sync = m.r.stream_sync_s;
   double tg = 0, ta = 0;
   std::vector<double> a_done(n);
-  auto rows = [&](int i) { return o.attn_bounds[i + 1] - o.attn_bounds[i]; };
-  auto front = [&](int i, int S, double f) {  // QKV on the GEMM stream, then its attention
-    tg += m.qkv_time(rows(i), S) * f;
-    ta = std::max(ta, tg + sync);
-    ta += m.attn_time(o.attn_bounds[i], o.attn_bounds[i + 1], attn_sms, true);
-    a_done[i] = ta;
-  };
-  for (int i = 0; i < n; ++i) front(i, i == 0 ? all : gsm, i == 0 ? 1.0 : slow);
-  for (int l = 0; l < L; ++l) {
-    int next_ffn = 0, next_front = 0;
-    for (int i = 0; i < n; ++i) {
-      const bool tail = l == L - 1 && i == n - 1;
-      const int S = tail ? all : gsm;
-      const double f = tail ? 1.0 : slow;
+  for (const nf::WindowOp& op : nf::window_schedule(o, L)) {
+    const int S = op.full ? all : gsm;
+    const double f = op.full ? 1.0 : slow;
+    const int i = op.nano;
+    if (op.kind == nf::WOP_QKV) {  // QKV on the GEMM stream, then its attention
+      tg += m.qkv_time(o.attn_bounds[i + 1] - o.attn_bounds[i], S) * f;
+      ta = std::max(ta, tg + sync);
+      ta += m.attn_time(o.attn_bounds[i], o.attn_bounds[i + 1], attn_sms, true);
+      a_done[i] = ta;
+    } else if (op.kind == nf::WOP_O) {
       tg = std::max(tg, a_done[i] + sync);  // O projection i waits for attention i
-      tg += m.o_time(rows(i), S) * f;
-      while (next_ffn < o.n_ffn && o.ffn_bounds[next_ffn + 1] <= o.attn_bounds[i + 1]) {
-        tg += m.ffn_time(o.ffn_bounds[next_ffn + 1] - o.ffn_bounds[next_ffn], S) * f;
-        ++next_ffn;
-        while (l + 1 < L && next_front < n && o.attn_bounds[next_front + 1] <= o.ffn_bounds[next_ffn]) {
-          front(next_front, gsm, slow);
-          ++next_front;
-        }
-      }
+      tg += m.o_time(o.attn_bounds[i + 1] - o.attn_bounds[i], S) * f;
+    } else {
+      tg += m.ffn_time(o.ffn_bounds[i + 1] - o.ffn_bounds[i], S) * f;
     }
   }
   return tg;
@@ -473,4 +464,26 @@ extern "C" nf_status nf_plan_search_layers(const nf_model_shape* shape, const nf
                                            int32_t n_layers, nf_plan_opts* out,
                                            double* predicted_us) {
   return search(shape, batch, profile_json, num_sms, n_layers, out, predicted_us);
+}
+
+extern "C" nf_status nf_window_schedule(const nf_plan_opts* o, int32_t n_layers, int32_t* out,
+                                        int32_t cap, int32_t* n_ops) {
+  if (!o || !n_ops || n_layers < 1 || cap < 0 || (cap > 0 && !out)) return NF_ERR_INVALID_ARG;
+  for (int g = 0; g < 2; ++g) {
+    const int n = g ? o->n_ffn : o->n_attn;
+    const int32_t* b = g ? o->ffn_bounds : o->attn_bounds;
+    if (n < 1 || n > NF_MAX_NANO || b[0] != 0) return NF_ERR_INVALID_ARG;
+    for (int i = 0; i < n; ++i)
+      if (b[i + 1] <= b[i]) return NF_ERR_INVALID_ARG;
+  }
+  if (o->attn_bounds[o->n_attn] != o->ffn_bounds[o->n_ffn]) return NF_ERR_INVALID_ARG;
+  const std::vector<nf::WindowOp> ops = nf::window_schedule(*o, n_layers);
+  *n_ops = static_cast<int32_t>(ops.size());
+  for (int k = 0; k < static_cast<int>(ops.size()) && k < cap; ++k) {
+    out[4 * k] = ops[k].kind;
+    out[4 * k + 1] = ops[k].layer;
+    out[4 * k + 2] = ops[k].nano;
+    out[4 * k + 3] = ops[k].full;
+  }
+  return NF_OK;
 }

@@ -136,3 +136,63 @@ def test_empty_batch_is_rejected_on_host(L):
     with pytest.raises(_lib.NanoflowError) as e:
         _lib.Plan(shape, batch, _lib.make_opts(1))
     assert e.value.code == _lib.NF_ERR_INVALID_ARG
+
+
+def _overlaps(a0, a1, b0, b1):
+    return a0 < b1 and b0 < a1
+
+
+@pytest.mark.parametrize("ab,fb", [([0, 1024, 2048], [0, 1024, 2048]),
+                                   ([0, 512, 1024, 1536, 2048], [0, 1024, 2048]),
+                                   ([0, 20, 36], [0, 10, 36]),
+                                   ([0, 12, 24, 36], [0, 36]),
+                                   ([0, 5, 19, 30, 36], [0, 19, 36])])
+@pytest.mark.parametrize("layers", [1, 2, 3, 5])
+def test_window_schedule_respects_every_dependency(L, ab, fb, layers):
+    """The cross-layer window's issue order (the one list the executor runs and
+    the search simulates), checked against dependencies derived here from the
+    nano-batch bounds: every operation once; O(l, i) after QKV(l, i); FFN(l, j)
+    after every O(l, i) sharing rows with it; QKV(l+1, k) after every FFN(l, j)
+    sharing rows with it (its input) and after O(l, k) (its q and o rows are
+    free again); QKV projections of a layer in row order (a prefill chunk across
+    a bound reads the K/V its earlier rows appended); FFN(l+1, j), which
+    overwrites layer l's input rows, after their last reader; and every SM only
+    for the first QKV and what follows the last attention."""
+    T = ab[-1]
+    opts = _lib.make_opts(T, ab, fb, executor=_lib.NF_EXEC_STREAMS, attn_sms=64)
+    ops = _lib.window_schedule(opts, layers)
+    pos = {}
+    for k, (kind, l, i, full) in enumerate(ops):
+        assert (kind, l, i) not in pos
+        pos[(kind, l, i)] = k
+    na, nf = len(ab) - 1, len(fb) - 1
+    assert len(ops) == layers * (2 * na + nf)
+    for l in range(layers):
+        for i in range(na):
+            assert pos[("o", l, i)] > pos[("qkv", l, i)]
+            if i:
+                assert pos[("qkv", l, i)] > pos[("qkv", l, i - 1)]
+        for j in range(nf):
+            for i in range(na):
+                if _overlaps(fb[j], fb[j + 1], ab[i], ab[i + 1]):
+                    assert pos[("ffn", l, j)] > pos[("o", l, i)]
+            if l + 1 < layers:
+                for i in range(na):          # layer l's readers of its input rows
+                    if _overlaps(fb[j], fb[j + 1], ab[i], ab[i + 1]):
+                        assert pos[("ffn", l + 1, j)] > pos[("o", l, i)]
+                        assert pos[("ffn", l + 1, j)] > pos[("qkv", l, i)]
+        if l + 1 < layers:
+            for k in range(na):
+                assert pos[("qkv", l + 1, k)] > pos[("o", l, k)]
+                for j in range(nf):
+                    if _overlaps(fb[j], fb[j + 1], ab[k], ab[k + 1]):
+                        assert pos[("qkv", l + 1, k)] > pos[("ffn", l, j)]
+    last_o = pos[("o", layers - 1, na - 1)]
+    for k, (kind, l, i, full) in enumerate(ops):
+        assert full == (1 if (k == 0 or k >= last_o) else 0), (k, kind, l, i)
+
+
+def test_window_schedule_rejects_bad_bounds(L):
+    o = _lib.make_opts(36, [0, 20, 36], [0, 10, 30])
+    with pytest.raises(_lib.NanoflowError):
+        _lib.window_schedule(o, 2)
