@@ -3,6 +3,7 @@ its host-only plan search returns valid plans."""
 import ctypes
 import os
 
+import numpy as np
 import pytest
 
 from nano_intra_device_gb300 import _lib, workload as wl
@@ -196,3 +197,26 @@ def test_window_schedule_rejects_bad_bounds(L):
     o = _lib.make_opts(36, [0, 20, 36], [0, 10, 30])
     with pytest.raises(_lib.NanoflowError):
         _lib.window_schedule(o, 2)
+
+
+def test_search_returns_valid_plans_on_random_batches(L):
+    """Random shapes, decode/prefill mixes and layer counts: every plan the
+    search returns is valid for its batch (bounds increasing from 0 to T on the
+    128-token grid at T >= 1024, counts within NF_MAX_NANO, an SM share below
+    the SM count), and nf_plan_predict reproduces the score it was chosen by."""
+    rng = np.random.default_rng(7)
+    shapes = [wl.tiny_shape(), wl.llama8b_shape(), wl.llama70b_shape()]
+    for trial in range(40):
+        shape = shapes[trial % 3]
+        n_dec = int(rng.integers(0, 1500))
+        pq = [int(q) for q in rng.integers(1, 700, int(rng.integers(0 if n_dec else 1, 4)))]
+        pp = [int(p) for p in rng.integers(0, 2000, len(pq))]
+        ctx = wl.lognormal_contexts(max(n_dec, 1), 600.0, 1.0, 1, 4096, seed=trial)[:n_dec]
+        b = wl.make_batch(shape, list(ctx), pq, pp, seed_bt=trial, max_pages=256)
+        layers = int(rng.choice([1, 4, 16]))
+        sms = int(rng.choice([76, 132, 152]))
+        o, t = _lib.plan_search(shape, b, None, sms, n_layers=layers)
+        T = b.n_tokens
+        _check_plan(o, T, 128 if T >= 1024 else 1)
+        assert 0 <= o.attn_sms < sms and t > 0
+        assert _lib.plan_predict(shape, b, o, None, sms, layers) == pytest.approx(t, rel=1e-9)
