@@ -47,7 +47,7 @@ extern "C" {
 typedef enum {
   NF_OK = 0,
   NF_ERR_INVALID_ARG = 1, /* a size, pointer or layout the library does not accept */
-  NF_ERR_UNSUPPORTED = 2, /* valid request this build does not implement */
+  NF_ERR_UNSUPPORTED = 2, /* a valid request the library does not implement */
   NF_ERR_OOM = 3,         /* device or host allocation failed */
   NF_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed */
   NF_ERR_TIMEOUT = 5,     /* a bounded device wait gave up (from nf_plan_poll) */
