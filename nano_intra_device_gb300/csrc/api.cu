@@ -54,14 +54,19 @@ struct GlobalSplitWs {
 // Split-K workspace of nf_gemm (no plan): allocated on first use.
 GlobalSplitWs* global_split_ws();
 
-// Status word for entry points that run without a plan (nf_gemm, nf_rmsnorm).
+// Status word for entry points that run without a plan (nf_gemm, nf_rmsnorm),
+// one per device (device memory belongs to the device current when allocated).
+constexpr int kMaxDevices = 64;
+std::mutex g_global_mu;
+
 uint32_t* global_status() {
-  static uint32_t* p = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    if (cudaMalloc(&p, sizeof(uint32_t)) == cudaSuccess) cudaMemset(p, 0, sizeof(uint32_t));
-  });
-  return p;
+  static uint32_t* p[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_global_mu);
+  if (!p[dev] && cudaMalloc(&p[dev], sizeof(uint32_t)) == cudaSuccess)
+    cudaMemset(p[dev], 0, sizeof(uint32_t));
+  return p[dev];
 }
 
 constexpr int64_t kDefaultTimeoutNs = 2000000000LL;
@@ -74,19 +79,27 @@ constexpr int kSplitMaxTiles = 256;
 constexpr int kSplitMaxUnits = 256;
 constexpr size_t kSplitPartBytes = (size_t)kSplitMaxUnits * 128 * 256 * 4;
 
+// nf_gemm's split-K workspace on the current device, allocated on first use
+// there (fields stay NULL when the allocation failed).
 GlobalSplitWs* global_split_ws() {
-  static GlobalSplitWs ws;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    if (cudaMalloc(&ws.part, kSplitPartBytes) != cudaSuccess ||
-        cudaMalloc(&ws.cnt, kSplitMaxTiles * 4) != cudaSuccess ||
-        cudaMemset(ws.cnt, 0, kSplitMaxTiles * 4) != cudaSuccess) {
-      ws.part = nullptr;
-      ws.cnt = nullptr;
+  static GlobalSplitWs ws[kMaxDevices];
+  static GlobalSplitWs none;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return &none;
+  std::lock_guard<std::mutex> lk(g_global_mu);
+  GlobalSplitWs& w = ws[dev];
+  if (!w.part) {
+    if (cudaMalloc(&w.part, kSplitPartBytes) != cudaSuccess ||
+        cudaMalloc(&w.cnt, kSplitMaxTiles * 4) != cudaSuccess ||
+        cudaMemset(w.cnt, 0, kSplitMaxTiles * 4) != cudaSuccess) {
+      if (w.part) cudaFree(w.part);
+      if (w.cnt) cudaFree(w.cnt);
+      w.part = nullptr;
+      w.cnt = nullptr;
       cudaGetLastError();
     }
-  });
-  return &ws;
+  }
+  return &w;
 }
 
 int choose_splits(int tiles, int K, int sms) {
@@ -111,6 +124,10 @@ struct nf_plan_s {
   int* set_stage = nullptr;     // pinned host staging of nf_plan_set_batch (two halves)
   float2* rope_cs = nullptr;    // RoPE (cos, sin) table [max_pages * page_size][head_dim / 2]
   int set_flip = 0;
+  // set_ev[h]: recorded after the copies out of staging half h; a later call
+  // waits for it before writing that half again
+  cudaEvent_t set_ev[2] = {nullptr, nullptr};
+  bool set_ev_live[2] = {false, false};
   std::vector<int> q_lens, tok_begin;
   nf_plan_opts opts{};
   int num_sms = 0;
@@ -165,7 +182,6 @@ struct nf_plan_s {
   // nf_plan_set_batch (two halves)
   int4* pf_tiles = nullptr;
   int4* pf_stage = nullptr;
-  int pf_flip = 0;
   int pf_seg[NF_MAX_NANO + 1] = {};
   // split-K GEMM workspace: fp32 partial tiles and per-tile arrival counters
   float* gemm_part = nullptr;
@@ -327,6 +343,8 @@ void free_plan(nf_plan p) {
     if (b) cudaFree(b);
   if (p->set_stage) cudaFreeHost(p->set_stage);
   if (p->pf_stage) cudaFreeHost(p->pf_stage);
+  for (cudaEvent_t e : p->set_ev)
+    if (e) cudaEventDestroy(e);
   for (auto& h : p->hgraphs)
     if (h.exec) cudaGraphExecDestroy(h.exec);
   if (p->s_host) cudaStreamDestroy(p->s_host);
@@ -1709,8 +1727,14 @@ nf_status nf_plan_set_batch(nf_plan p, const nf_batch_desc* b, const nf_plan_opt
     NF_CUDA(cudaHostAlloc(&p->set_stage, 2 * (2 * (size_t)p->seq_cap + 2 + NF_MAX_NANO + 1) * 4,
                           cudaHostAllocDefault));
   // Two halves, used alternately: a copy enqueued by the previous call may still
-  // be pending when this one writes.
-  int* h = p->set_stage + p->set_flip * (2 * p->seq_cap + 2 + NF_MAX_NANO + 1);
+  // be pending when this one writes.  The host may run further ahead than one
+  // call (steps are asynchronous), so before a half is written again the copies
+  // that read it last must have run: wait for the event recorded after them.
+  const int half = p->set_flip;
+  if (p->set_ev_live[half]) NF_CUDA(cudaEventSynchronize(p->set_ev[half]));
+  p->set_ev_live[half] = false;
+  if (!p->set_ev[half]) NF_CUDA(cudaEventCreateWithFlags(&p->set_ev[half], cudaEventDisableTiming));
+  int* h = p->set_stage + half * (2 * p->seq_cap + 2 + NF_MAX_NANO + 1);
   p->set_flip ^= 1;
   std::copy(q_lens.begin(), q_lens.end(), h);
   std::copy(tok_begin.begin(), tok_begin.end(), h + p->seq_cap);
@@ -1727,14 +1751,15 @@ nf_status nf_plan_set_batch(nf_plan p, const nf_batch_desc* b, const nf_plan_opt
     build_prefill_tiles(p, b->n_decode, n_seq, tok_begin, o, tiles, seg);
     if (!p->pf_stage)
       NF_CUDA(cudaHostAlloc(&p->pf_stage, 2 * (size_t)p->T_cap * sizeof(int4), cudaHostAllocDefault));
-    int4* hp = p->pf_stage + (size_t)p->pf_flip * p->T_cap;
-    p->pf_flip ^= 1;
+    int4* hp = p->pf_stage + (size_t)half * p->T_cap;  // guarded by the same event
     std::copy(tiles.begin(), tiles.end(), hp);
     if (!tiles.empty())
       NF_CUDA(cudaMemcpyAsync(p->pf_tiles, hp, tiles.size() * sizeof(int4), cudaMemcpyHostToDevice,
                               st));
     std::copy(seg, seg + o.n_attn + 1, p->pf_seg);
   }
+  NF_CUDA(cudaEventRecord(p->set_ev[half], st));
+  p->set_ev_live[half] = true;
   p->n_decode = b->n_decode;
   p->n_prefill = b->n_prefill;
   p->n_seq = n_seq;

@@ -407,13 +407,9 @@ __global__ void __launch_bounds__(WARPS * 32, 1) attn_kernel(const AttnArgs a) {
 template <int GRP, int NCH, int WARPS, int STAGES>
 static cudaError_t launch_t(const AttnArgs& a, int grid, cudaStream_t stream) {
   const int smem = attn_smem_bytes_cfg(NCH * 64, ATT_P, WARPS, STAGES, WARPS < 8);
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(attn_kernel<GRP, NCH, WARPS, STAGES>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  const cudaError_t e =
+      set_smem_limit(reinterpret_cast<const void*>(attn_kernel<GRP, NCH, WARPS, STAGES>), smem);
+  if (e != cudaSuccess) return e;
   attn_kernel<GRP, NCH, WARPS, STAGES><<<grid, WARPS * 32, smem, stream>>>(a);
   return cudaGetLastError();
 }

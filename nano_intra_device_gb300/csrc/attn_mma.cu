@@ -422,13 +422,9 @@ template <int GRP, int NCH, int WARPS, int STAGES, int PPI>
 static cudaError_t launch_mma_t(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
                                 int grid, bool programmatic, cudaStream_t stream) {
   const int smem = amma_smem_bytes(NCH * 64, WARPS, STAGES);
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel<GRP, NCH, WARPS, STAGES, PPI>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  const cudaError_t e = set_smem_limit(
+      reinterpret_cast<const void*>(attn_mma_kernel<GRP, NCH, WARPS, STAGES, PPI>), smem);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   cfg.blockDim = dim3(WARPS * 32, 1, 1);

@@ -456,9 +456,8 @@ static cudaError_t launch_pair_t(const AttnArgs& a, int grid, cudaStream_t strea
   constexpr int V = 4 * GRP;
   constexpr int R = V >= 8 ? V / 8 : V;
   const int smem = PAIRS * (STAGES * 2 * PBLK) + PAIRS * static_cast<int>(sizeof(PairSmem<STAGES, R>)) + 128;
-  // once per process (the attribute is per function; thread-safe initialisation)
-  static const cudaError_t attr = cudaFuncSetAttribute(
-      attn_pair_kernel<GRP, PAIRS, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  const cudaError_t attr =
+      set_smem_limit(reinterpret_cast<const void*>(attn_pair_kernel<GRP, PAIRS, STAGES>), smem);
   if (attr != cudaSuccess) return attr;
   attn_pair_kernel<GRP, PAIRS, STAGES><<<grid, PAIRS * 64, smem, stream>>>(a);
   return cudaGetLastError();

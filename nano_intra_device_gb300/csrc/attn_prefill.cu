@@ -267,9 +267,8 @@ template <int GRP, int NCH>
 cudaError_t launch_pf_t(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
                         const int4* tiles, int n_tiles, cudaStream_t stream) {
   const int smem = pf_smem_bytes(NCH * 64);
-  // once per process (the attribute is per function; thread-safe initialisation)
-  static const cudaError_t attr = cudaFuncSetAttribute(
-      attn_prefill_kernel<GRP, NCH>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  const cudaError_t attr =
+      set_smem_limit(reinterpret_cast<const void*>(attn_prefill_kernel<GRP, NCH>), smem);
   if (attr != cudaSuccess) return attr;
   attn_prefill_kernel<GRP, NCH><<<n_tiles * a.n_kv, PF_THREADS, smem, stream>>>(tk, tv, a, tiles);
   return cudaGetLastError();

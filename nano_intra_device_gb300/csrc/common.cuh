@@ -6,7 +6,29 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+#include <set>
+#include <tuple>
+
 namespace nf {
+
+// A kernel's dynamic shared-memory limit (cudaFuncSetAttribute) belongs to the
+// context of the device that is current when it is set, so it is set once per
+// (device, kernel, size), not once per process: a process that launches on a
+// second GPU sets it again there.
+inline cudaError_t set_smem_limit(const void* kernel, int bytes) {
+  static std::mutex mu;
+  static std::set<std::tuple<int, const void*, int>> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(mu);
+  const auto key = std::make_tuple(dev, kernel, bytes);
+  if (done.count(key)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.insert(key);
+  return e;
+}
 
 // Bits of the device status word a plan owns.  Kernels OR them in; the host
 // reads the word in nf_plan_poll.  No kernel ever traps.

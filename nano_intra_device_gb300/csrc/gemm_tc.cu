@@ -537,9 +537,8 @@ static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB,
                               const CUtensorMap& tmB2, const GemmArgs& args, int grid,
                               cudaStream_t stream) {
   constexpr int smem = gemm_smem_bytes(STAGES, BN);
-  // once per process (the attribute is per function; thread-safe initialisation)
-  static const cudaError_t attr = cudaFuncSetAttribute(
-      gemm_tc_kernel<EPI, STAGES, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  const cudaError_t attr =
+      set_smem_limit(reinterpret_cast<const void*>(gemm_tc_kernel<EPI, STAGES, BN>), smem);
   if (attr != cudaSuccess) return attr;
   gemm_tc_kernel<EPI, STAGES, BN><<<grid, GEMM_THREADS, smem, stream>>>(tmA, tmB, tmB2, args);
   return cudaGetLastError();

@@ -493,11 +493,8 @@ __global__ void __launch_bounds__(WR_THREADS, 1)
 
 template <int EPI, int TOK, bool ONE>
 cudaError_t wr_prepare() {
-  // once per process (the attribute is per function; thread-safe initialisation)
-  static const cudaError_t attr =
-      cudaFuncSetAttribute(gemm_wrows_kernel<EPI, TOK, ONE>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, WrCfg<EPI, TOK, ONE>::SMEM);
-  return attr;
+  return set_smem_limit(reinterpret_cast<const void*>(gemm_wrows_kernel<EPI, TOK, ONE>),
+                        WrCfg<EPI, TOK, ONE>::SMEM);
 }
 
 template <int EPI, int TOK, bool ONE>
