@@ -344,8 +344,10 @@ nf_status nf_step_metadata(nf_plan plan, const int32_t* block_table, const int32
 nf_status nf_attention(nf_plan plan, const void* q, const void* k_pool, const void* v_pool,
                        const int32_t* block_table, const int32_t* seq_lens, void* o, void* stream);
 
-/* Size of the fixed device working memory of nf_attention_noalloc. */
+/* Size of the fixed device working memory of nf_attention_noalloc, and the
+ * largest number of prefill chunks one call takes. */
 #define NF_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+#define NF_NOALLOC_MAX_PREFILL 64
 
 /* nf_attention for callers that cannot allocate device memory.  No counterpart
  * on the pages: it exists for callers of this library that must not call
@@ -353,29 +355,46 @@ nf_status nf_attention(nf_plan plan, const void* q, const void* k_pool, const vo
  * pool and gives an operator only its input and output pointers, or a hot
  * loop that cannot take the device synchronisation an allocation may cause.
  * It needs no plan.  Inputs and outputs are those of nf_attention (shape and
- * batch structure as for nf_plan_create; q, o device [T, n_q, head_dim];
- * pools, block table and seq_lens device, the cache already holding this
- * step's K/V).  Its working memory (token map, work list, counters, split-KV
- * partials with 2048-position pieces) is one static device array of
- * NF_NOALLOC_SCRATCH_BYTES, present on every GPU that loads the library until
- * the process exits.  A batch that needs more returns NF_ERR_INVALID_ARG
- * with the required size in nf_last_error(); the need is about
- * T * ceil(max_pages_per_seq * 16 / 2048) * n_kv * (head_dim * n_q / n_kv + 8) * 4
- * bytes plus 40 bytes per token (e.g. 1024 tokens of the Llama-3-8B shape
- * with contexts up to 2048 fit).
+ * batch structure as for nf_plan_create, with at most NF_NOALLOC_MAX_PREFILL
+ * prefill chunks; q, o device [T, n_q, head_dim]; pools, block table and
+ * seq_lens device, the cache already holding this step's K/V).  The batch
+ * structure travels by value in a kernel's arguments: no host table is copied.
+ *
+ * Working memory: one static device array of NF_NOALLOC_SCRATCH_BYTES, present
+ * on every GPU that loads the library until the process exits.  With
+ * grp = n_q / n_kv, n_seq = n_decode + n_prefill and
+ * C = ceil(max_pages_per_seq * 16 / 2048) split-KV pieces per row, a call
+ * needs 256 bytes (the status word) plus these regions, each rounded up to a
+ * multiple of 256 bytes:
+ *   4 n_seq, 4 (n_seq + 1), 8, four of 4 T, 8 T C, 8, 4, 4 T n_kv, and
+ *   4 T C n_kv (grp head_dim + 4 ceil(2 grp / 4))   (the split-KV partials).
+ * E.g. 1024 tokens of the Llama-3-8B shape with contexts up to 2048 fit.  A
+ * batch that needs more returns NF_ERR_INVALID_ARG with the required size in
+ * nf_last_error().
+ *
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress); make that first call before any stream capture.
  * Every call uses the same array and overwrites what the previous call left;
  * the counters that must start at zero are cleared by each call.  Calls whose
  * work overlaps on the GPU (two streams, or two threads) race on the array and
- * give wrong results: serialise them.  Device-side page-id checks still keep
- * every read inside the pool, but their status is not reported here.  This
- * call allocates nothing: no cudaMalloc, no cudaFree, no allocating library
- * routine. */
+ * give wrong results: serialise them.
+ *
+ * Errors found on the device (a page id outside the pool, an inconsistent
+ * length, a bounded wait that gave up) never fault: reads stay inside the pool
+ * and the kernels set bits in a status word kept in the array.  The bits stay
+ * set across calls until nf_attention_noalloc_poll reports and clears them.
+ * This call allocates nothing: no cudaMalloc, no cudaFree, no allocating
+ * library routine. */
 nf_status nf_attention_noalloc(const nf_model_shape* shape, const nf_batch_desc* batch,
                                const void* q, const void* k_pool, const void* v_pool,
                                const int32_t* block_table, const int32_t* seq_lens, void* o,
                                void* stream);
+
+/* Waits for `stream`, then reads and clears the status word that
+ * nf_attention_noalloc calls on the current device have set since the last
+ * poll: NF_OK if none, NF_ERR_TIMEOUT if a wait gave up, else NF_ERR_DEVICE
+ * (the reason in nf_last_error()).  Allocates nothing. */
+nf_status nf_attention_noalloc_poll(void* stream);
 
 /* RMSNorm of rows [0, rows): out = x * g / sqrt(mean(x^2) + eps), fp32
  * arithmetic, bf16 out.  x, out: device [rows, hidden]; g: device [hidden]. */
@@ -585,6 +604,12 @@ nf_status nf_runtime_sync(nf_runtime rt);
 nf_status nf_runtime_result(nf_runtime rt, int32_t id, int32_t* finished, int32_t* n_tokens,
                             int32_t* tokens, int32_t cap);
 nf_status nf_runtime_counts(nf_runtime rt, int32_t* waiting, int32_t* active, int32_t* free_pages);
+/* The logits of the last iteration that nf_runtime_step launched, for its
+ * emitting rows in row order: dst [n_rows, vocab] bf16, host or device (e.g. to
+ * check a model against a reference, or to sample differently).  Waits for that
+ * iteration's stream; the buffer is overwritten by the next step.  With dst
+ * NULL only n_rows is set.  cap_rows: rows dst holds. */
+nf_status nf_runtime_logits(nf_runtime rt, void* dst, int32_t cap_rows, int32_t* n_rows);
 /* Host-only runtimes: form the next batch / give the sampled tokens of an
  * iteration ([n_tokens], read where row_emit is 1).  At most two iterations
  * may await results. */

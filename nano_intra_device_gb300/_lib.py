@@ -108,11 +108,13 @@ _SIGS = {
     "nf_runtime_counts": (c_int, [c_void_p, POINTER(c_int32), POINTER(c_int32), POINTER(c_int32)]),
     "nf_runtime_form": (c_int, [c_void_p, POINTER(nf_runtime_batch)]),
     "nf_runtime_apply": (c_int, [c_void_p, c_int32, POINTER(c_int32)]),
+    "nf_runtime_logits": (c_int, [c_void_p, c_void_p, c_int32, POINTER(c_int32)]),
     "nf_last_error": (c_char_p, []),
     "nf_device_sm_count": (c_int32, []),
     "nf_step_metadata": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p]),
     "nf_attention": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     "nf_attention_noalloc": (c_int, [POINTER(nf_model_shape), POINTER(nf_batch_desc), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "nf_attention_noalloc_poll": (c_int, [c_void_p]),
     "nf_rmsnorm": (c_int, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_float, c_void_p]),
     "nf_gemm": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32, c_int32, c_void_p]),
     "nf_gemm_wrows": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32,
@@ -392,6 +394,12 @@ def attention_noalloc(shape, batch, q, k_pool, v_pool, block_table, seq_lens, o,
                                      stream_handle(stream)))
 
 
+def attention_noalloc_poll(stream=None):
+    """nf_attention_noalloc_poll: wait for the stream, then report and clear the
+    device-side status of nf_attention_noalloc calls on the current device."""
+    check(lib().nf_attention_noalloc_poll(stream_handle(stream)))
+
+
 def rmsnorm(x, g, out, eps, stream=None):
     check(lib().nf_rmsnorm(ptr(x), ptr(g), ptr(out), x.shape[0], x.shape[1], eps, stream_handle(stream)))
 
@@ -505,6 +513,15 @@ class Runtime:
 
     def sync(self):
         check(lib().nf_runtime_sync(self.h))
+
+    def logits(self):
+        """The last launched iteration's logits ([emitting rows, vocab] bf16, CPU)."""
+        import torch
+        n = c_int32()
+        check(lib().nf_runtime_logits(self.h, None, 0, ctypes.byref(n)))
+        out = torch.empty(max(n.value, 1), self.opts.vocab, dtype=torch.bfloat16)
+        check(lib().nf_runtime_logits(self.h, ptr(out), n.value, ctypes.byref(n)))
+        return out[: n.value]
 
     def result(self, rid, cap=4096):
         fin, n = c_int32(), c_int32()
