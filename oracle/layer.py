@@ -10,8 +10,16 @@ that result, because nano-batches share no data dependencies ("NanoFlow:
 Towards Optimal LLM Serving Throughput", "The Intra-Device Parallelism
 Mechanism").  So the oracle never splits the batch: it walks tokens in order.
 
-Arithmetic: float64 throughout.  bf16 inputs are converted exactly; nothing is
-rounded back to bf16 (not even the K/V it appends).
+Arithmetic: float64 throughout.  bf16 inputs are converted exactly.  By
+default nothing is rounded back to bf16 (not even the K/V it appends).  With
+``store="bf16"`` the tensors that a layer keeps in memory between its
+operations — n1, q and the appended k, v (after RoPE), the attention output o,
+h, n2, the SwiGLU product a, and a layer's output when another layer or the
+final norm reads it — are rounded to the nearest bf16 value (ties to even)
+where they are produced; every arithmetic step between them stays float64, and
+the returned outputs (y, logits) are not rounded.  The pages fix no precision;
+this mode is the plain reading of "a layer whose stored tensors are bf16",
+used to separate the error that storage in bf16 causes from the rest.
 
 Readings taken where the pages leave a step open (each is listed with its
 reason in the design notes):
@@ -73,6 +81,29 @@ def weights_f64(w: dict) -> dict:
     """Convert a weight dict (bf16 tensors) to float64 arrays once (expert
     stacks lazily, expert by expert)."""
     return {k: (_LazyExperts(v) if k.startswith("w_experts") else f64(v)) for k, v in w.items()}
+
+
+def bf16(v) -> np.ndarray:
+    """Round float64 values to the nearest bfloat16 value, ties to even,
+    returned as float64.
+
+    bfloat16 keeps 8 significant bits (1 implicit + 7 stored) and float32's
+    exponent range.  With v = m * 2^e, 0.5 <= |m| < 1, the representable
+    neighbours are the multiples of 2^(e-8); numpy's round() breaks ties to the
+    even multiple.  Normal range only (|v| >= 2^-126; values here are far
+    from it), zeros keep their sign.
+    """
+    v = np.asarray(v, dtype=np.float64)
+    m, e = np.frexp(v)
+    return np.ldexp(np.round(np.ldexp(m, 8)), e - 8)
+
+
+def _storage(store):
+    if store is None:
+        return lambda v: v
+    if store == "bf16":
+        return bf16
+    raise ValueError(f"store must be None or 'bf16', not {store!r}")
 
 
 # --------------------------------------------------------------------------
@@ -215,18 +246,20 @@ def expert_groups(experts, n_experts: int):
     return np.asarray(pairs, np.int64).reshape(-1, 2), np.asarray(offsets, np.int64)
 
 
-def moe_ffn(n2, w64: dict, logits, top_k: int, F: int):
+def moe_ffn(n2, w64: dict, logits, top_k: int, F: int, store=None):
     """sum over the token's selected experts e of weight_e * FFN_e(n2), with
     FFN_e(z) = (silu(z W_g,e^T) * (z W_u,e^T)) W_d,e^T; w64["w_experts_gate_up"][e]
     holds the gate rows then the up rows of expert e, w64["w_experts_down"][e]
-    its down matrix.  n2 [R, H], logits [R, E] for the same rows."""
+    its down matrix.  n2 [R, H], logits [R, E] for the same rows.  With
+    store="bf16" each expert's SwiGLU product is rounded to bf16."""
+    rnd = _storage(store)
     experts, weights = route(logits, top_k)
     out = np.zeros_like(n2)
     for i in range(n2.shape[0]):
         for j in range(top_k):
             e = int(experts[i, j])
             gu = w64["w_experts_gate_up"][e]
-            a = silu(n2[i] @ gu[:F].T) * (n2[i] @ gu[F:].T)
+            a = rnd(silu(n2[i] @ gu[:F].T) * (n2[i] @ gu[F:].T))
             out[i] += weights[i, j] * (a @ w64["w_experts_down"][e].T)
     return out
 
@@ -248,7 +281,7 @@ def _needed_rows(seq, rows):
 
 
 def layer_step(shape, w64: dict, x, k_pool, v_pool, block_table, seq_lens, q_lens,
-               rows=None, keep=False, router_logits=None) -> dict:
+               rows=None, keep=False, router_logits=None, store=None) -> dict:
     """One decoder-layer step over a mixed prefill+decode batch.
 
     shape: a Shape (hidden, n_q, n_kv, head_dim, ffn, rms_eps, rope_theta,
@@ -273,7 +306,11 @@ def layer_step(shape, w64: dict, x, k_pool, v_pool, block_table, seq_lens, q_len
     A mixture-of-experts layer (shape.n_experts > 0, weights w_experts_gate_up
     and w_experts_down) replaces the last two lines by y = h + moe_ffn(n2)
     with router_logits [T, n_experts] given for the step.
+
+    store: None (float64 throughout) or "bf16" (n1, q, k, v, o, h, n2 and a
+    rounded to bf16 where they are produced; y is returned unrounded).
     """
+    rnd = _storage(store)
     H, nq, nkv, d, F = shape.hidden, shape.n_q, shape.n_kv, shape.head_dim, shape.ffn
     P = shape.page_size
     q_lens = np.asarray(q_lens, np.int64)
@@ -286,13 +323,13 @@ def layer_step(shape, w64: dict, x, k_pool, v_pool, block_table, seq_lens, q_len
 
     # projections for every needed row
     xn = f64(x[torch.as_tensor(need)]) if isinstance(x, torch.Tensor) else f64(x)[need]
-    n1 = rmsnorm(xn, w64["norm1"], shape.rms_eps)
+    n1 = rnd(rmsnorm(xn, w64["norm1"], shape.rms_eps))
     qkv = n1 @ w64["w_qkv"].T
     q = qkv[:, : nq * d].reshape(-1, nq, d)
     k = qkv[:, nq * d: (nq + nkv) * d].reshape(-1, nkv, d)
-    v = qkv[:, (nq + nkv) * d:].reshape(-1, nkv, d)
-    q = rope(q, pos[need], shape.rope_theta)
-    k = rope(k, pos[need], shape.rope_theta)
+    v = rnd(qkv[:, (nq + nkv) * d:].reshape(-1, nkv, d))
+    q = rnd(rope(q, pos[need], shape.rope_theta))
+    k = rnd(rope(k, pos[need], shape.rope_theta))
     new_k = {int(t): k[i] for i, t in enumerate(need)}
     new_v = {int(t): v[i] for i, t in enumerate(need)}
     qrow = {int(t): q[i] for i, t in enumerate(need)}
@@ -323,18 +360,19 @@ def layer_step(shape, w64: dict, x, k_pool, v_pool, block_table, seq_lens, q_len
             K[pp] = new_k[tt]
             V[pp] = new_v[tt]
         o[i] = attention_one(qrow[t], K, V, nq, nkv)
+    o = rnd(o)
 
     xr = np.stack([xrow[t] for t in rows.tolist()])
-    h = xr + o.reshape(len(rows), nq * d) @ w64["w_o"].T
-    n2 = rmsnorm(h, w64["norm2"], shape.rms_eps)
+    h = rnd(xr + o.reshape(len(rows), nq * d) @ w64["w_o"].T)
+    n2 = rnd(rmsnorm(h, w64["norm2"], shape.rms_eps))
     if getattr(shape, "n_experts", 0):
         lg = np.asarray(router_logits, np.float64)[rows]
         a = None
-        y = h + moe_ffn(n2, w64, lg, shape.top_k, F)
+        y = h + moe_ffn(n2, w64, lg, shape.top_k, F, store=store)
     else:
         gate = n2 @ w64["w_gate_up"][:F].T
         up = n2 @ w64["w_gate_up"][F:].T
-        a = silu(gate) * up
+        a = rnd(silu(gate) * up)
         y = h + a @ w64["w_down"].T
 
     out = {
@@ -357,7 +395,7 @@ def layer_step(shape, w64: dict, x, k_pool, v_pool, block_table, seq_lens, q_len
 # a stack of layers with embedding and LM head
 
 def layers_step(shape, layers64: list, x, pools: list, block_table, seq_lens, q_lens,
-                rows=None) -> dict:
+                rows=None, store=None) -> dict:
     """Several decoder layers over one mixed step: layer l takes the previous
     layer's output (x for the first) and reads its own K/V pools; the block
     table and lengths are shared ("NanoFlow: Towards Optimal LLM Serving
@@ -367,8 +405,12 @@ def layers_step(shape, layers64: list, x, pools: list, block_table, seq_lens, q_
     layers64: float64 weight dicts; pools: (k_pool, v_pool) per layer; x: [T, H].
     rows: the tokens whose output is wanted; every layer computes the rows
     those need (their earlier prefill rows).  Returns {"rows", "y" [len(rows),
-    H], "x_all" [T, H] (rows outside the needed set are left as given)}.
+    H], "x_all" [T, H] (rows outside the needed set are left as given),
+    "appended": per layer (slots, k_new, v_new) of the computed rows}.
+    store: as in layer_step; with "bf16" every layer's output but the last is
+    rounded to bf16 before the next layer reads it.
     """
+    rnd = _storage(store)
     q_lens = np.asarray(q_lens, np.int64)
     seq_lens = np.asarray(seq_lens, np.int64)
     seq, _ = token_map(q_lens, seq_lens)
@@ -376,15 +418,19 @@ def layers_step(shape, layers64: list, x, pools: list, block_table, seq_lens, q_
     rows = np.arange(T, dtype=np.int64) if rows is None else np.asarray(rows, np.int64)
     need = _needed_rows(seq, rows)
     x = np.array(f64(x), copy=True)
-    for w64, (kp, vp) in zip(layers64, pools):
-        out = layer_step(shape, w64, x, kp, vp, block_table, seq_lens, q_lens, rows=need)
+    n_layers = len(layers64)
+    appended = []
+    for li, (w64, (kp, vp)) in enumerate(zip(layers64, pools)):
+        out = layer_step(shape, w64, x, kp, vp, block_table, seq_lens, q_lens, rows=need,
+                         store=store)
+        appended.append((out["slots"], out["k_new"], out["v_new"]))
         x = x.copy()
-        x[need] = out["y"]
-    return {"rows": rows, "y": x[rows], "x_all": x}
+        x[need] = out["y"] if li == n_layers - 1 else rnd(out["y"])
+    return {"rows": rows, "y": x[rows], "x_all": x, "appended": appended}
 
 
 def stack_step(shape, embed, norm_f, lm_head, layers64: list, tokens, pools: list, block_table,
-               seq_lens, q_lens, rows=None) -> dict:
+               seq_lens, q_lens, rows=None, store=None) -> dict:
     """A decoder stack over one mixed step: x = embed[tokens]; each layer's step
     (its own K/V pools, the shared block table and lengths); logits =
     RMSNorm(x; norm_f) lm_head^T.
@@ -392,8 +438,12 @@ def stack_step(shape, embed, norm_f, lm_head, layers64: list, tokens, pools: lis
     layers64: float64 weight dicts, one per layer (see weights_f64); pools:
     (k_pool, v_pool) per layer.  rows: the tokens whose logits are wanted;
     every layer computes the rows those need (their earlier prefill rows).
-    Returns {"rows", "logits" [len(rows), vocab], "x_final"}.
+    Returns {"rows", "logits" [len(rows), vocab], "x_final", "appended" (as in
+    layers_step)}.
+    store: as in layers_step; with "bf16" the last layer's output and the
+    final norm's output are rounded too (the logits are not).
     """
+    rnd = _storage(store)
     q_lens = np.asarray(q_lens, np.int64)
     seq_lens = np.asarray(seq_lens, np.int64)
     seq, _ = token_map(q_lens, seq_lens)
@@ -403,6 +453,8 @@ def stack_step(shape, embed, norm_f, lm_head, layers64: list, tokens, pools: lis
     E = f64(embed)
     x = np.zeros((T, shape.hidden))
     x[need] = E[np.asarray(tokens)[need]]
-    out = layers_step(shape, layers64, x, pools, block_table, seq_lens, q_lens, rows=rows)
-    xf = rmsnorm(out["y"], f64(norm_f), shape.rms_eps)
-    return {"rows": rows, "logits": xf @ f64(lm_head).T, "x_final": out["y"]}
+    out = layers_step(shape, layers64, x, pools, block_table, seq_lens, q_lens, rows=rows,
+                      store=store)
+    xf = rnd(rmsnorm(rnd(out["y"]), f64(norm_f), shape.rms_eps))
+    return {"rows": rows, "logits": xf @ f64(lm_head).T, "x_final": out["y"],
+            "appended": out["appended"]}

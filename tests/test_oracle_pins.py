@@ -201,19 +201,24 @@ def _tiny_inputs(gain_std=0.1, seed=0):
     return shape, b, w, x, k, v
 
 
-def _brute_layer(shape, w, x, k_pool, v_pool, b):
+def _brute_layer(shape, w, x, k_pool, v_pool, b, store=False, inter=None):
     """Independent float64 restatement of the layer on tiny inputs: complex
     rotation for RoPE, each sequence's full contiguous K/V rebuilt position by
-    position, one dense masked softmax per sequence and head."""
+    position, one dense masked softmax per sequence and head.  With store=True
+    the stored tensors (n1, q and k after RoPE, v, o, h, n2, a) go through
+    torch's own bf16 conversion (via float32) where they are produced; inter,
+    if a dict, receives them."""
     H, nq, nkv, d, F, P = (shape.hidden, shape.n_q, shape.n_kv, shape.head_dim,
                            shape.ffn, shape.page_size)
+    rnd = (lambda u: u.float().to(torch.bfloat16).double()) if store else (lambda u: u)
+    inter = {} if inter is None else inter
     X = x.double()
     W = {kk: vv.double() for kk, vv in w.items()}
-    n1 = X * torch.rsqrt((X * X).mean(-1, keepdim=True) + shape.rms_eps) * W["norm1"]
+    n1 = rnd(X * torch.rsqrt((X * X).mean(-1, keepdim=True) + shape.rms_eps) * W["norm1"])
     proj = torch.einsum("th,rh->tr", n1, W["w_qkv"])
     q = proj[:, :nq * d].reshape(-1, nq, d)
     k = proj[:, nq * d:(nq + nkv) * d].reshape(-1, nkv, d)
-    v = proj[:, (nq + nkv) * d:].reshape(-1, nkv, d)
+    v = rnd(proj[:, (nq + nkv) * d:].reshape(-1, nkv, d))
     # positions
     pos, sid = [], []
     for s in range(b.n_seq):
@@ -228,7 +233,7 @@ def _brute_layer(shape, w, x, k_pool, v_pool, b):
     def cplx(u):
         z = torch.complex(u[..., :half], u[..., half:]) * rot[:, None, :]
         return torch.cat([z.real, z.imag], -1)
-    q, k = cplx(q), cplx(k)
+    q, k = rnd(cplx(q)), rnd(cplx(k))
     o = torch.zeros(len(pos), nq, d, dtype=torch.float64)
     for s in range(b.n_seq):
         L = int(b.seq_lens[s])
@@ -250,11 +255,14 @@ def _brute_layer(shape, w, x, k_pool, v_pool, b):
             mask = torch.tensor([[j <= pos[t] for j in range(L)] for t in toks])
             S = S.masked_fill(~mask, -math.inf)
             o[toks, h] = torch.softmax(S, -1) @ Vc[:, g, :]
-    hres = X + o.reshape(len(pos), nq * d) @ W["w_o"].T
-    n2 = hres * torch.rsqrt((hres * hres).mean(-1, keepdim=True) + shape.rms_eps) * W["norm2"]
+    o = rnd(o)
+    hres = rnd(X + o.reshape(len(pos), nq * d) @ W["w_o"].T)
+    n2 = rnd(hres * torch.rsqrt((hres * hres).mean(-1, keepdim=True) + shape.rms_eps) * W["norm2"])
     gu = n2 @ W["w_gate_up"].T
-    a = torch.nn.functional.silu(gu[:, :F]) * gu[:, F:]
+    a = rnd(torch.nn.functional.silu(gu[:, :F]) * gu[:, F:])
     y = hres + a @ W["w_down"].T
+    inter.update(n1=n1.numpy(), q=q.numpy(), o=o.numpy(), h=hres.numpy(), n2=n2.numpy(),
+                 a=a.numpy())
     return y.numpy(), k.numpy(), v.numpy()
 
 
@@ -266,6 +274,79 @@ def test_layer_matches_independent_brute_force():
     np.testing.assert_allclose(out["k_new"], k, rtol=1e-11, atol=1e-12)
     np.testing.assert_allclose(out["v_new"], v, rtol=1e-11, atol=1e-12)
     assert np.all(np.isfinite(out["y"]))
+
+
+def test_bf16_rounding_matches_torch_and_the_definition():
+    """oracle.bf16 against torch's float32 -> bfloat16 conversion (random
+    normal values, exact ties between two bf16 neighbours, values near powers
+    of two), and on float64 inputs against the definition: the nearer of the
+    two bf16 neighbours, enumerated from the float32 bit pattern, ties to the
+    even one."""
+    rng = np.random.default_rng(0)
+    vals = [rng.standard_normal(50000).astype(np.float32) * 8,
+            ((rng.integers(0x0080, 0x7F7F, 20000).astype(np.uint32) << 16) | 0x8000).view(np.float32),
+            ((rng.integers(0x0080, 0x7F7F, 20000).astype(np.uint32) << 16) | 0x7FFF).view(np.float32)]
+    for v in vals:
+        v = v * np.where(rng.random(v.shape) < 0.5, -1, 1).astype(np.float32)
+        ref = torch.from_numpy(v).to(torch.bfloat16).double().numpy()
+        assert np.array_equal(orc.bf16(v.astype(np.float64)), ref)
+    # float64 inputs: brute force over the two neighbours
+    x = rng.standard_normal(20000) * np.exp2(rng.integers(-20, 20, 20000))
+    lo_bits = (np.abs(x).astype(np.float32).view(np.uint32) & 0xFFFF0000)   # truncate to bf16
+    lo = lo_bits.view(np.float32).astype(np.float64)
+    lo = np.where(lo > np.abs(x), (lo_bits - 0x10000).view(np.float32).astype(np.float64), lo)
+    lo_bits = np.abs(lo).astype(np.float32).view(np.uint32)
+    hi = (lo_bits + 0x10000).view(np.float32).astype(np.float64)
+    a = np.abs(x)
+    pick_hi = (hi - a < a - lo) | ((hi - a == a - lo) & ((lo_bits >> 16) & 1 == 1))
+    want = np.sign(x) * np.where(pick_hi, hi, lo)
+    assert np.array_equal(orc.bf16(x), want)
+    assert orc.bf16(np.array([0.0]))[0] == 0.0
+
+
+def test_layer_bf16_storage_matches_the_brute_force_with_torch_rounding():
+    """store="bf16" rounds exactly the stored tensors, where they are produced:
+    every intermediate it returns is a bf16 value and equals the independent
+    restatement's, which rounds through torch's conversion (rare one-step
+    differences allowed: torch rounds float64 via float32, and a difference
+    propagates), and the output moves off the exact layer by the expected
+    bf16-sized amount."""
+    shape, b, w, x, kp, vp = _tiny_inputs()
+    w64 = orc.weights_f64(w)
+    ex = orc.layer_step(shape, w64, x, kp, vp, b.block_table, b.seq_lens, b.q_lens, keep=True)
+    st = orc.layer_step(shape, w64, x, kp, vp, b.block_table, b.seq_lens, b.q_lens, keep=True,
+                        store="bf16")
+    inter = {}
+    y, k, v = _brute_layer(shape, w, x, kp, vp, b, store=True, inter=inter)
+    inter.update(k_new=k, v_new=v)
+    for key in ("n1", "q", "k_new", "v_new", "o", "h", "n2", "a"):
+        got = st[key].reshape(inter[key].shape)
+        assert np.array_equal(orc.bf16(got), got), key            # stored values are bf16
+        same = np.mean(got == inter[key])
+        step = 2 * np.ldexp(1.0, np.frexp(np.abs(inter[key]))[1] - 9)
+        assert same > 0.99 and np.all(np.abs(got - inter[key]) <= step + 1e-300), (key, same)
+        assert not np.array_equal(got, ex[key].reshape(got.shape)), key   # rounding happened
+    np.testing.assert_allclose(st["y"], y, rtol=0, atol=1e-3)
+    d = st["y"] - ex["y"]
+    rl = np.linalg.norm(d) / np.linalg.norm(ex["y"])
+    assert 1e-5 < rl < 5e-3
+
+
+def test_stack_bf16_storage_rounds_between_layers_only():
+    """layers_step with store="bf16": the last layer's output is returned
+    unrounded, the layers before hand the next a bf16 value (equal to running
+    the layers one at a time, rounding in between)."""
+    shape, b, w, x, kp, vp = _tiny_inputs()
+    w2 = wl.make_weights(shape, seed=5, gain_std=0.1)
+    k2, v2 = wl.make_pools(shape, b, "cpu", seed=8)
+    L = [orc.weights_f64(w), orc.weights_f64(w2)]
+    both = orc.layers_step(shape, L, x, [(kp, vp), (k2, v2)], b.block_table, b.seq_lens,
+                           b.q_lens, store="bf16")
+    one = orc.layer_step(shape, L[0], x, kp, vp, b.block_table, b.seq_lens, b.q_lens, store="bf16")
+    two = orc.layer_step(shape, L[1], orc.bf16(one["y"]), k2, v2, b.block_table, b.seq_lens,
+                         b.q_lens, store="bf16")
+    assert np.array_equal(both["y"], two["y"])
+    assert not np.array_equal(orc.bf16(two["y"]), two["y"])
 
 
 def test_layer_zero_weights_is_identity_and_zero_gate_gives_h():
