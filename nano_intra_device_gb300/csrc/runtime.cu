@@ -283,6 +283,7 @@ struct nf_runtime_s {
   cudaEvent_t done[2] = {nullptr, nullptr};
   cudaStream_t last_stream = nullptr;
   int launched = 0;
+  int last_emit = 0;  // emitting rows of the last launched iteration (its logits rows)
 };
 
 namespace {
@@ -526,7 +527,23 @@ nf_status nf_runtime_step(nf_runtime rt, const nf_stack_weights* w, void* const*
       cudaEventRecord(rt->done[k], st) != cudaSuccess)
     return rfail(NF_ERR_CUDA, "runtime sampling failed");
   rt->last_stream = st;
+  rt->last_emit = n_emit;
   ++rt->launched;
+  return NF_OK;
+}
+
+nf_status nf_runtime_logits(nf_runtime rt, void* dst, int32_t cap_rows, int32_t* n_rows) {
+  if (!rt || !n_rows) return rfail(NF_ERR_INVALID_ARG, "NULL argument");
+  if (rt->opts.host_only) return rfail(NF_ERR_INVALID_ARG, "a host-only runtime has no logits");
+  *n_rows = rt->launched ? rt->last_emit : 0;
+  if (*n_rows == 0 || !dst) return NF_OK;
+  if (cap_rows < *n_rows)
+    return rfail(NF_ERR_INVALID_ARG, "the last iteration has %d logits rows, more than cap_rows %d",
+                 *n_rows, cap_rows);
+  if (cudaStreamSynchronize(rt->last_stream) != cudaSuccess ||
+      cudaMemcpy(dst, rt->d_logits, (size_t)*n_rows * rt->opts.vocab * 2, cudaMemcpyDefault) !=
+          cudaSuccess)
+    return rfail(NF_ERR_CUDA, "reading the logits failed");
   return NF_OK;
 }
 

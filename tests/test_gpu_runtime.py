@@ -14,7 +14,8 @@ import torch
 
 from nano_intra_device_gb300 import _lib, workload as wl
 from oracle import layer as orc
-from tests.helpers import compare, f64
+from tests.helpers import f64, parity
+from tests.serving import OracleServer, greedy, row_tokens, serving_model
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -40,15 +41,16 @@ def test_plan_follows_a_smaller_batch():
                         (big, None)):
         kp, vp = wl.make_pools(shape, batch, DEV, seed=6)
         x = wl.make_x(shape, batch.n_tokens, seed=7)
-        ref = orc.layer_step(shape, orc.weights_f64(w), x, kp, vp, batch.block_table,
-                             batch.seq_lens, batch.q_lens)
+        w64 = orc.weights_f64(w)
+        ex, em = (orc.layer_step(shape, w64, x, kp, vp, batch.block_table, batch.seq_lens,
+                                 batch.q_lens, store=st) for st in (None, "bf16"))
         plan.set_batch(batch, opts)
         y = torch.empty(batch.n_tokens, shape.hidden, dtype=torch.bfloat16, device=DEV)
         _lib.layer_step(plan, wd, x.to(DEV), kp, vp, torch.from_numpy(batch.block_table).to(DEV),
                         torch.from_numpy(batch.seq_lens).to(DEV), y)
         plan.poll()
         assert plan.info()[1] == batch.n_tokens
-        compare(f64(y), ref["y"], f"y after set_batch ({batch.n_tokens} tokens)")
+        parity(f64(y), ex["y"], em["y"], f"y after set_batch ({batch.n_tokens} tokens)")
     with pytest.raises(_lib.NanoflowError):       # more tokens than the plan holds
         plan.set_batch(wl.make_batch(shape, [4] * 60, [], None, max_pages=8))
     plan.close()
@@ -109,6 +111,70 @@ def test_runtime_serves_requests_end_to_end(replan):
     assert max(sizes) == b_dense
     if replan >= 0:
         assert replanned >= 2      # the mix moved from prompts to decoding
+    else:
+        assert replanned == 0
+    rt.close()
+
+
+@pytest.mark.parametrize("replan", [0.1, -1.0])
+def test_runtime_serves_a_real_model_like_the_oracle(replan):
+    """A random-weight two-layer stack (non-zero projections, norm gains other
+    than 1, an LM head with a clear top-1 margin) served by nf_runtime on the
+    GPU.  After every iteration the batch the scheduler formed is replayed
+    through the oracle's stack step with the oracle's own K/V pools (updated
+    from the K/V it appends), on the tokens the GPU's decode rows consumed:
+    the GPU's logits of the emitting rows match both oracles at the stated
+    bounds, its greedy tokens equal the oracle's, and the runtime's final
+    outputs are those tokens.  Prompt chunks continue over several iterations
+    and decode rows read K/V appended in earlier ones (dropping that K/V moves
+    these logits by 1.5 to 4)."""
+    shape = wl.tiny_shape()
+    vocab, n_layers, b_dense, max_pages, num_pages = 96, 2, 40, 8, 64
+    model = serving_model(shape, n_layers, vocab, seed=0)
+    embed, norm_f, lm_head, layers = model
+    pools = [(torch.zeros(num_pages, shape.n_kv, 16, shape.head_dim, dtype=torch.bfloat16, device=DEV),
+              torch.zeros(num_pages, shape.n_kv, 16, shape.head_dim, dtype=torch.bfloat16, device=DEV))
+             for _ in range(n_layers)]
+    sa = _lib.StackArgs(embed.to(DEV), norm_f.to(DEV), lm_head.to(DEV),
+                        [{k: v.to(DEV) for k, v in w.items()} for w in layers], pools)
+    rt = _lib.Runtime(shape, b_dense, 8, max_pages, num_pages, vocab, eos_token=-1,
+                      replan_threshold=replan)
+    rng = np.random.default_rng(2)
+    prompts, n_out = {}, {}
+    for _ in range(10):
+        pl = int(rng.integers(1, 60))
+        prompt = rng.integers(0, vocab, pl).tolist()
+        mn = int(rng.integers(1, 20))
+        rid = rt.submit(prompt, mn)
+        prompts[rid], n_out[rid] = prompt, mn
+    exact = OracleServer(shape, model, num_pages, max_pages)
+    emul = OracleServer(shape, model, num_pages, max_pages, store="bf16")
+    gen = {r: [] for r in prompts}
+    stream = torch.cuda.current_stream()
+    iters, replanned = 0, 0
+    for _ in range(500):
+        b = rt.step(sa, stream)
+        if b["n_tokens"] == 0:
+            break
+        iters += 1
+        replanned += b["replanned"]
+        lg = f64(rt.logits())                       # waits for this iteration
+        toks = row_tokens(b, prompts, gen)
+        ex, em = exact.step(b, toks), emul.step(b, toks)
+        if lg.size:
+            parity(lg, ex, em, f"served logits, iteration {b['iteration']}")
+            assert np.array_equal(greedy(lg), greedy(ex)), b["iteration"]
+        emit = [t for t, e in enumerate(b["row_emit"]) if e]
+        for j, t in enumerate(emit):
+            gen[b["row_request"][t]].append(int(greedy(lg[j:j + 1])[0]))
+    rt.sync()
+    assert iters >= 10
+    for rid in prompts:
+        fin, toks = rt.result(rid)
+        assert fin and toks == gen[rid][: n_out[rid]], rid
+    assert rt.counts() == (0, 0, num_pages)
+    if replan >= 0:
+        assert replanned >= 2
     else:
         assert replanned == 0
     rt.close()

@@ -231,3 +231,86 @@ def test_runtime_rejects_bad_requests_and_out_of_order_results():
     with pytest.raises(_lib.NanoflowError):
         rt.apply(b0["iteration"], [5])    # given twice
     rt.close()
+
+
+# ---------------------------------------------------------------- a real model
+def _alone(shape, model, prompt, n_out, max_pages):
+    """Greedy outputs of one request served alone: the whole prompt as one
+    prefill chunk into fresh pools, then one decode step per output."""
+    from tests.serving import OracleServer, greedy
+    srv = OracleServer(shape, model, max_pages, max_pages)
+    bt = list(range(max_pages))
+    out, logits = [], []
+    L = len(prompt)
+    b = dict(n_decode=0, n_prefill=1, block_table=bt, seq_lens=[L], prefill_q_lens=[L],
+             row_emit=[0] * (L - 1) + [1])
+    lg = srv.step(b, prompt)
+    out.append(int(greedy(lg)[0]))
+    logits.append(lg[0])
+    for i in range(1, n_out):
+        b = dict(n_decode=1, n_prefill=0, block_table=bt, seq_lens=[L + i], prefill_q_lens=[],
+                 row_emit=[1])
+        lg = srv.step(b, [out[-1]])
+        out.append(int(greedy(lg)[0]))
+        logits.append(lg[0])
+    return out, logits
+
+
+def test_served_model_equals_each_request_served_alone():
+    """A random-weight two-layer stack served through the scheduler (host-only
+    runtime; the oracle computes every batch it forms, with its own K/V pools)
+    gives every request exactly the greedy outputs, and to float64 rounding the
+    logits, of the same request served alone.  Batches mix decode rows with
+    prompt chunks that continue over several iterations, and decode rows read
+    K/V appended in earlier iterations, so batching, chunking, page allocation
+    and the one-iteration-late token arrival must all leave the arithmetic of
+    each request unchanged."""
+    from tests.serving import OracleServer, greedy, row_tokens, serving_model
+    shape = wl.tiny_shape()
+    vocab, n_layers, b_dense, max_pages, num_pages = 96, 2, 40, 8, 64
+    model = serving_model(shape, n_layers, vocab, seed=0)
+    rt = _lib.Runtime(shape, b_dense, 8, max_pages, num_pages, vocab, eos_token=-1, host_only=True)
+    rng = np.random.default_rng(2)
+    prompts, n_out = {}, {}
+    for _ in range(10):
+        pl = int(rng.integers(1, 60))
+        prompt = rng.integers(0, vocab, pl).tolist()
+        mn = int(rng.integers(1, 20))
+        rid = rt.submit(prompt, mn)
+        prompts[rid], n_out[rid] = prompt, mn
+    srv = OracleServer(shape, model, num_pages, max_pages)
+    gen = {r: [] for r in prompts}
+    glog = {r: [] for r in prompts}
+    pending, continued, cross_iter_decode = [], 0, 0
+    for _ in range(1000):
+        b = rt.form()
+        if b["n_tokens"]:
+            toks = row_tokens(b, prompts, gen)
+            lg = srv.step(b, toks)
+            emit = [t for t, e in enumerate(b["row_emit"]) if e]
+            sampled = [-1] * b["n_tokens"]
+            for j, t in enumerate(emit):
+                rid = b["row_request"][t]
+                gen[rid].append(int(greedy(lg[j:j + 1])[0]))
+                glog[rid].append(lg[j])
+                sampled[t] = gen[rid][-1]
+            nd = b["n_decode"]
+            continued += sum(1 for t in range(nd, b["n_tokens"])
+                             if b["row_token"][t] >= 0 and b["row_pos"][t] > 0
+                             and (t == nd or b["row_request"][t - 1] != b["row_request"][t]))
+            cross_iter_decode += nd
+            pending.append((b["iteration"], sampled))
+        if len(pending) == 2 or (b["n_tokens"] == 0 and pending):
+            itn, smp = pending.pop(0)
+            rt.apply(itn, smp)
+        if b["n_tokens"] == 0 and not pending:
+            break
+    assert continued >= 3 and cross_iter_decode >= 20     # the batches exercise both
+    for rid in prompts:
+        fin, toks = rt.result(rid)
+        assert fin and toks == gen[rid][: n_out[rid]]
+        want, wlog = _alone(shape, model, prompts[rid], n_out[rid], max_pages)
+        assert toks == want, rid
+        np.testing.assert_allclose(np.stack(glog[rid][: n_out[rid]]), np.stack(wlog),
+                                   rtol=1e-9, atol=1e-9)
+    rt.close()
