@@ -24,3 +24,17 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+def pytest_sessionfinish(session, exitstatus):
+    """Write every parity comparison of the session to $NF_PARITY_LOG (JSON)."""
+    path = os.environ.get("NF_PARITY_LOG")
+    if not path:
+        return
+    import json
+    try:
+        from tests.helpers import RECORD
+    except Exception:  # pragma: no cover
+        return
+    with open(path, "w") as f:
+        json.dump(RECORD, f, indent=0)

@@ -7,7 +7,7 @@ import torch
 
 from nano_intra_device_gb300 import _lib, workload as wl
 from oracle import layer as orc
-from tests.helpers import compare, f64
+from tests.helpers import f64, parity
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -21,6 +21,14 @@ def _case(shape, batch, seed=0, logits=None):
     kp, vp = wl.make_pools(shape, batch, DEV, seed=seed + 3)
     x = wl.make_x(shape, batch.n_tokens, seed=seed + 5)
     return w, kp, vp, x
+
+
+def _oracles(shape, w, x, kp, vp, batch, logits, rows=None):
+    """(exact, bf16-storage) oracle results of the MoE layer."""
+    w64 = orc.weights_f64(w)
+    return tuple(orc.layer_step(shape, w64, x, kp, vp, batch.block_table, batch.seq_lens,
+                                batch.q_lens, rows=rows, router_logits=logits, store=st)
+                 for st in (None, "bf16"))
 
 
 def _run(shape, batch, opts, w, kp, vp, x):
@@ -74,13 +82,12 @@ def test_moe_routing_ties_and_idle_experts():
     logits = torch.zeros(T, shape.n_experts)
     logits[: T // 2, 3] = 1.0          # first half: expert 3, then the tie 0
     w, kp, vp, x = _case(shape, batch, seed=2, logits=logits)
-    ref = orc.layer_step(shape, orc.weights_f64(w), x, kp, vp, batch.block_table, batch.seq_lens,
-                         batch.q_lens, router_logits=logits.numpy())
+    ex, em = _oracles(shape, w, x, kp, vp, batch, logits.numpy())
     plan, y = _run(shape, batch, _lib.make_opts(T), w, kp, vp, x)
     off, _, _, _ = _routing(plan, shape, T)
     plan.close()
     assert list(np.diff(off)) == [T, T - T // 2, 0, T // 2]   # expert 2 idle
-    compare(f64(y), ref["y"], "MoE y (ties)")
+    parity(f64(y), ex["y"], em["y"], "MoE y (ties)")
 
 
 @pytest.mark.parametrize("executor,ab,fb", [
@@ -91,12 +98,11 @@ def test_moe_routing_ties_and_idle_experts():
 def test_tiny_moe_layer_matches_oracle(executor, ab, fb):
     shape, batch = wl.tiny_moe_shape(), wl.tiny_batch()
     w, kp, vp, x = _case(shape, batch, seed=3)
-    ref = orc.layer_step(shape, orc.weights_f64(w), x, kp, vp, batch.block_table, batch.seq_lens,
-                         batch.q_lens, router_logits=w["router_logits"].numpy())
+    ex, em = _oracles(shape, w, x, kp, vp, batch, w["router_logits"].numpy())
     opts = _lib.make_opts(batch.n_tokens, ab, fb, executor=executor, attn_sms=24, kv_chunk=32)
     plan, y = _run(shape, batch, opts, w, kp, vp, x)
     plan.close()
-    compare(f64(y), ref["y"], "tiny MoE y")
+    parity(f64(y), ex["y"], em["y"], "tiny MoE y")
 
 
 def test_mixtral_shaped_layer_sampled_rows():
@@ -106,11 +112,10 @@ def test_mixtral_shaped_layer_sampled_rows():
     w, kp, vp, x = _case(shape, batch, seed=4)
     ctx = batch.seq_lens[: batch.n_decode]
     rows = [0, int(np.argmax(ctx)), int(np.argmin(ctx)), 239, 240, 260, T - 1]
-    ref = orc.layer_step(shape, orc.weights_f64(w), x, kp, vp, batch.block_table, batch.seq_lens,
-                         batch.q_lens, rows=rows, router_logits=w["router_logits"].numpy())
+    ex, em = _oracles(shape, w, x, kp, vp, batch, w["router_logits"].numpy(), rows=rows)
     for ab in ([0, T], [0, 128, T]):
         opts = _lib.make_opts(T, ab, ab, executor=_lib.NF_EXEC_STREAMS if len(ab) > 2 else 0,
                               attn_sms=76)
         plan, y = _run(shape, batch, opts, w, kp, vp, x)
         plan.close()
-        compare(f64(y)[rows], ref["y"], f"Mixtral-shaped y, bounds {ab}")
+        parity(f64(y)[rows], ex["y"], em["y"], f"Mixtral-shaped y, bounds {ab}")
