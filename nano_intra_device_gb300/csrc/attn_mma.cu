@@ -21,8 +21,12 @@
 // [num_pages * n_kv * 16, d] with 128-byte swizzle, so that the ldmatrix loads
 // of 8 positions at the same dims hit 8 different bank groups.  Positions past
 // the end of a piece read row 0 of its page instead (P is 0 there), so a stale
-// or poisoned slot never reaches the accumulators.  P enters the PV product in
-// bf16, and the denominators sum the same bf16 values.
+// or poisoned slot never reaches the accumulators.  P enters the PV product
+// as two bf16 operands, hi = bf16(p) and lo = bf16(p - hi), in two MMAs on the
+// same V fragment: p keeps 16 significant bits instead of 8 (one bf16 P alone
+// perturbs each weight by up to 2^-9, which shows in o at the 1e-3 level and
+// then moves bf16 roundings of every tensor downstream), and the denominators
+// sum the fp32 values.
 #include "attn_merge.cuh"
 #include "common.cuh"
 #include "kernels.h"
@@ -302,15 +306,20 @@ __global__ void __launch_bounds__(WARPS * 32, WARPS == AMMA_SHARE_WARPS ? 4 : 1)
 #pragma unroll
       for (int i = 0; i < PPI; ++i) {
         if (k + i >= npg) break;  // warp-uniform
-        const uint32_t p01 = pack_bf16(ex2_approx(fmaf(sc[i][0], scale, -m0)),
-                                       ex2_approx(fmaf(sc[i][1], scale, -m1)));
-        const uint32_t p23 = pack_bf16(ex2_approx(fmaf(sc[i][2], scale, -m0)),
-                                       ex2_approx(fmaf(sc[i][3], scale, -m1)));
-        l0 += bf16lo(p01) + bf16lo(p23);
-        l1 += bf16hi(p01) + bf16hi(p23);
-        // P^T operand: (positions 2 lc (+1), head lr) and positions + 8
+        const float e0 = ex2_approx(fmaf(sc[i][0], scale, -m0));
+        const float e1 = ex2_approx(fmaf(sc[i][1], scale, -m1));
+        const float e2 = ex2_approx(fmaf(sc[i][2], scale, -m0));
+        const float e3 = ex2_approx(fmaf(sc[i][3], scale, -m1));
+        const uint32_t p01 = pack_bf16(e0, e1), p23 = pack_bf16(e2, e3);
+        const uint32_t r01 = pack_bf16(e0 - bf16lo(p01), e1 - bf16hi(p01));
+        const uint32_t r23 = pack_bf16(e2 - bf16lo(p23), e3 - bf16hi(p23));
+        l0 += e0 + e2;
+        l1 += e1 + e3;
+        // P^T operands (hi and lo): (positions 2 lc (+1), head lr) and positions + 8
         const uint32_t pb0 = movmatrix_trans(p01);
         const uint32_t pb1 = movmatrix_trans(p23);
+        const uint32_t rb0 = movmatrix_trans(r01);
+        const uint32_t rb1 = movmatrix_trans(r23);
         uint32_t st, ph;
         slot_at(rs, rph, i, st, ph);
         const uint32_t slot = ring_u32 + st * SLOT;
@@ -320,6 +329,7 @@ __global__ void __launch_bounds__(WARPS * 32, WARPS == AMMA_SHARE_WARPS ? 4 : 1)
           for (int mi = 0; mi < KS; ++mi) {
             uint32_t vf[4];
             ldsm_x4_trans(slot + voff[mi], vf);
+            mma_16816(o[mi], vf, rb0, rb1);
             mma_16816(o[mi], vf, pb0, pb1);
           }
         } else {  // rows past the piece read row 0 instead (weighted 0)
@@ -328,6 +338,7 @@ __global__ void __launch_bounds__(WARPS * 32, WARPS == AMMA_SHARE_WARPS ? 4 : 1)
           for (int mi = 0; mi < KS; ++mi) {
             uint32_t vf[4];
             ldsm_x4_trans(slot + (past ? BLK + page_chunk_off(0, 2 * mi + v_ci) : voff[mi]), vf);
+            mma_16816(o[mi], vf, rb0, rb1);
             mma_16816(o[mi], vf, pb0, pb1);
           }
         }

@@ -17,8 +17,9 @@
 //  * per page and warp: S[16 x 16] = Q K^T (Q the A operand, from registers;
 //    K by ldmatrix), the causal mask by position, an online softmax per row in
 //    base 2, P moved to the A-operand layout straight from the accumulators,
-//    and O[16 x d] += P V (V by ldmatrix.trans).  P enters PV in bf16 and the
-//    denominators sum the same bf16 values, as in the decode kernel;
+//    and O[16 x d] += P V (V by ldmatrix.trans).  P enters PV as two bf16
+//    operands (hi = bf16(p), lo = bf16(p - hi)) and the denominators sum the
+//    fp32 values, as in the decode kernel;
 //  * every wait is bounded; on expiry the kernel flags ST_TIMEOUT and the
 //    producer waits (bounded) for the copies it issued before the CTA exits.
 #include "common.cuh"
@@ -221,22 +222,29 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       o[j][2] *= c[1];
       o[j][3] *= c[1];
     }
-    // P as the A operand of a k16 step: (row lr, keys 2 lc ..), (lr + 8, ..), then keys + 8
-    uint32_t pa[4];
+    // P as the A operand of a k16 step: (row lr, keys 2 lc ..), (lr + 8, ..), then
+    // keys + 8; as two bf16 operands, hi = bf16(p) and lo = bf16(p - hi), so that
+    // each weight keeps 16 significant bits; the denominators sum the fp32 values
+    uint32_t pa[4], pr[4];
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-      const uint32_t p0 = pack_bf16(ex2_approx(x[j][0] - m[0]), ex2_approx(x[j][1] - m[0]));
-      const uint32_t p1 = pack_bf16(ex2_approx(x[j][2] - m[1]), ex2_approx(x[j][3] - m[1]));
-      l[0] += bf16lo(p0) + bf16hi(p0);
-      l[1] += bf16lo(p1) + bf16hi(p1);
+      const float e0 = ex2_approx(x[j][0] - m[0]), e1 = ex2_approx(x[j][1] - m[0]);
+      const float e2 = ex2_approx(x[j][2] - m[1]), e3 = ex2_approx(x[j][3] - m[1]);
+      const uint32_t p0 = pack_bf16(e0, e1), p1 = pack_bf16(e2, e3);
+      l[0] += e0 + e1;
+      l[1] += e2 + e3;
       pa[2 * j] = p0;
       pa[2 * j + 1] = p1;
+      pr[2 * j] = pack_bf16(e0 - bf16lo(p0), e1 - bf16hi(p0));
+      pr[2 * j + 1] = pack_bf16(e2 - bf16lo(p1), e3 - bf16hi(p1));
     }
     const bool redirect = v_past && k == npages - 1;
 #pragma unroll
     for (int nn = 0; nn < KS; ++nn) {
       uint32_t vb[4];
       ldsm_x4_trans(slot + (redirect ? BLK + page_chunk_off(0, 2 * nn + (mj >> 1)) : voff[nn]), vb);
+      mma_16816(o[2 * nn], pr, vb[0], vb[1]);
+      mma_16816(o[2 * nn + 1], pr, vb[2], vb[3]);
       mma_16816(o[2 * nn], pa, vb[0], vb[1]);
       mma_16816(o[2 * nn + 1], pa, vb[2], vb[3]);
     }

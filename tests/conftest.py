@@ -27,7 +27,8 @@ def pytest_collection_modifyitems(config, items):
 
 
 def pytest_sessionfinish(session, exitstatus):
-    """Write every parity comparison of the session to $NF_PARITY_LOG (JSON)."""
+    """Write every parity comparison of the session to $NF_PARITY_LOG (JSON)
+    and a per-test summary table beside it ($NF_PARITY_LOG with .md)."""
     path = os.environ.get("NF_PARITY_LOG")
     if not path:
         return
@@ -38,3 +39,17 @@ def pytest_sessionfinish(session, exitstatus):
         return
     with open(path, "w") as f:
         json.dump(RECORD, f, indent=0)
+    worst = {}
+    for r in RECORD:
+        key = (r["test"].split("::")[-1], r["name"].split(",")[0], r["oracle"])
+        w = worst.setdefault(key, dict(r, count=0))
+        w["count"] += 1
+        for k in ("max_abs", "rel_l2"):
+            w[k] = max(w[k], r[k])
+    lines = ["| test | output | oracle | checks | elements | max-abs | rel-L2 | rms(ref) |",
+             "|---|---|---|---|---|---|---|---|"]
+    for (test, name, oracle), w in worst.items():
+        lines.append(f"| {test} | {name} | {oracle} | {w['count']} | {w['n']} | {w['max_abs']:.4g} | "
+                     f"{w['rel_l2']:.3g} | {w['rms_ref']:.3g} |")
+    with open(os.path.splitext(path)[0] + ".md", "w") as f:
+        f.write("\n".join(lines) + "\n")
