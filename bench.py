@@ -678,7 +678,7 @@ def main():
     so, _ = searched.info()
     cands = [("search", searched), ("sequential", make_plan(_lib.make_opts(T)))]
     if args.plan == "auto":
-        for n in (2, 3):
+        for n in (2, 3, 4):
             ab = [0] + [int(round(T * i / n / 128)) * 128 for i in range(1, n)] + [T]
             for a_sms in (sms * 7 // 16, sms * 8 // 16, sms * 9 // 16, sms * 10 // 16):
                 o = _lib.make_opts(T, ab, ab, executor=_lib.NF_EXEC_STREAMS, attn_sms=a_sms)
@@ -695,6 +695,10 @@ def main():
         p.poll()
     best_name = min(tried, key=tried.get)
     plan = dict(cands)[best_name]
+    # the fastest overlapped candidate (two streams, n >= 2), for the ablation
+    ovl = [nm for nm in tried if nm.startswith("n=")]
+    ovl_name = min(ovl, key=tried.get) if ovl else None
+    ovl_opts = dict(cands)[ovl_name].info()[0] if ovl_name else None
     for name, p in cands:
         if p is not plan:
             p.close()
@@ -733,8 +737,7 @@ def main():
     attn_bytes_per_launch = wk.attn_bytes / n_attn
     attn_ms = sum(attn) / max(1, len(attn))
     achieved = attn_bytes_per_launch / (attn_ms * 1e-3) / 1e9
-    mma = po.attn_impl == _lib.NF_ATTN_MMA
-    src_name = "attn_mma.cu" if mma else "attn.cu"
+    src_name = "attn_mma.cu"
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "attn_traffic.json")
     if os.path.exists(tpath):
@@ -742,8 +745,7 @@ def main():
         src = open(os.path.join(ROOT, "nano_intra_device_gb300", "csrc", src_name), "rb").read()
         if tj.get("source_sha256") == hashlib.sha256(src).hexdigest():
             traffic = tj.get("bytes_per_launch", {}).get(str(n_attn))
-    kname = ("attn_mma_kernel (paged GQA attention, tensor cores)" if mma else
-             "attn_kernel (paged GQA attention, CUDA-core FMA)")
+    kname = "attn_mma_kernel (paged GQA attention, tensor cores)"
     roof = {"bound": "hbm", "kernel": kname,
             "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
             "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
@@ -786,18 +788,27 @@ def main():
     d2h = yhs[0].numel() * 2
 
     # ablation: sequential, nanobatch-only, overlapped (same kernels)
+    # (the pages' Fig. 9 ablation: non-overlap, nanobatch-only, overlap): the
+    # sequential plan; the best overlapped candidate's split run on one stream;
+    # that candidate itself.  Each timed the same way, 10 steps after 3.
     ablation = None
     if not args.no_ablation:
         ablation = {}
         seq = make_plan(_lib.make_opts(T))
         ablation["sequential_n1"] = T / (time_steps(stepper(seq), 10, 3, world, stream) * 1e-3)
         seq.close()
-        ab = list(po.attn_bounds[: po.n_attn + 1])
-        fb = list(po.ffn_bounds[: po.n_ffn + 1])
-        nb = make_plan(_lib.make_opts(T, ab, fb, executor=_lib.NF_EXEC_SEQUENTIAL))
-        ablation["nanobatch_only"] = T / (time_steps(stepper(nb), 10, 3, world, stream) * 1e-3)
-        nb.close()
-        ablation["overlap"] = value / world
+        if ovl_opts is not None:
+            ab = list(ovl_opts.attn_bounds[: ovl_opts.n_attn + 1])
+            fb = list(ovl_opts.ffn_bounds[: ovl_opts.n_ffn + 1])
+            nb = make_plan(_lib.make_opts(T, ab, fb, executor=_lib.NF_EXEC_SEQUENTIAL))
+            ablation["nanobatch_only"] = T / (time_steps(stepper(nb), 10, 3, world, stream) * 1e-3)
+            nb.close()
+            ov = make_plan(_lib.make_opts(T, ab, fb, executor=_lib.NF_EXEC_STREAMS,
+                                          attn_sms=ovl_opts.attn_sms))
+            ablation["overlap"] = T / (time_steps(stepper(ov), 10, 3, world, stream) * 1e-3)
+            ov.close()
+            ablation["overlap_plan"] = ovl_name
+            ablation["nanobatch_only_plan"] = f"{ovl_name.split(',')[0]}, one stream"
         if world == 1:
             # the same batch through several layers, where the overlap can run
             # across layer boundaries (the single step has a head and a tail

@@ -62,9 +62,9 @@ typedef enum {
 } nf_executor;
 
 typedef enum {
-  NF_ATTN_AUTO = 0, /* tensor-core kernel where supported, else the FMA kernel */
-  NF_ATTN_FMA = 1,  /* dot products on the CUDA cores (packed fp32 FMA) */
-  NF_ATTN_MMA = 2   /* dot products on the tensor cores (mma.sync, bf16 x bf16 -> fp32) */
+  NF_ATTN_AUTO = 0, /* the tensor-core kernel (the only attention kernel) */
+  NF_ATTN_MMA = 2   /* dot products on the tensor cores (mma.sync, bf16 x bf16 -> fp32);
+                       value 1 (a CUDA-core kernel, removed) is refused */
 } nf_attn_impl;
 
 /* Shape of one Llama-style decoder layer.  head_dim in {64, 128};
@@ -119,24 +119,21 @@ typedef struct {
   int32_t attn_sms;   /* SMs for attention while it overlaps GEMMs (0 = automatic) */
   int32_t gemm_sms;   /* SMs for a GEMM while it overlaps attention (0 = the rest) */
   int32_t kv_chunk;   /* split-KV piece in tokens, multiple of page_size, <= 2048 (0 = 1024) */
-  int32_t attn_warps; /* warps per attention CTA (0 = 8).  Tensor-core kernel: 4 shares
-                         each SM with one GEMM CTA of gemm_stages = 2 (3-page rings, 117 KB,
-                         <= 128 registers a thread); 5 ... 8, 10, 12 or 14 fill an SM, ring
-                         stages per warp as deep as shared memory allows (5: 5, 6: 4, 7: 4,
-                         8: 3, more warps: 2 pages).  FMA kernel: 8; 12 / 16 as warp pairs
-                         that split head_dim 128; 4 or 5 share each SM with one GEMM CTA of
-                         gemm_stages = 2 */
+  int32_t attn_warps; /* warps per attention CTA (0 = 8): 4 shares each SM with one GEMM
+                         CTA of gemm_stages = 2 (3-page rings, 117 KB, <= 128 registers a
+                         thread); 5 ... 8, 10, 12 or 14 fill an SM, ring stages per warp as
+                         deep as shared memory allows (5: 5, 6: 4, 7: 4, 8: 3, more warps:
+                         2 pages) */
   int32_t gemm_stages; /* shared-memory ring stages of the GEMM kernel: 4 fills an SM;
-                          2 lets an attention CTA of 4 or 5 warps run on the same SM (0 = 4) */
+                          2 lets an attention CTA of 4 warps run on the same SM (0 = 4) */
   int32_t gemm_split_k; /* 0: a GEMM of at most 128 tokens runs the weight-row kernel (128
                            output features x 64 or 128 tokens a tile, K split over the CTAs
                            of a cluster, partial tiles summed in distributed shared memory);
                            a larger one splits K across CTAs when it has fewer output tiles
                            than half its SMs.  1: token-row tiles, never split.  2: token-row
                            tiles, split as in 0 (no weight-row kernel) */
-  int32_t attn_impl;  /* nf_attn_impl.  NF_ATTN_AUTO picks the FMA kernel for its own
-                         attn_warps 5 and 16, else the tensor-core kernel where the shape
-                         allows it; nf_plan_info reports the kernel chosen */
+  int32_t attn_impl;  /* nf_attn_impl (0 or 2: the tensor-core kernel); nf_plan_info
+                         reports NF_ATTN_MMA */
   int32_t validate;   /* 1 = check page ids and lengths on the device */
   int64_t timeout_ns; /* limit of every device-side wait (0 = 2e9) */
 } nf_plan_opts;

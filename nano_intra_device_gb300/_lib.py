@@ -19,7 +19,7 @@ NF_MAX_NANO = 8
 NF_OK, NF_ERR_INVALID_ARG, NF_ERR_UNSUPPORTED, NF_ERR_OOM, NF_ERR_CUDA, NF_ERR_TIMEOUT, \
     NF_ERR_DEVICE, NF_ERR_INTERNAL = range(8)
 NF_EXEC_SEQUENTIAL, NF_EXEC_STREAMS = 0, 1
-NF_ATTN_AUTO, NF_ATTN_FMA, NF_ATTN_MMA = 0, 1, 2
+NF_ATTN_AUTO, NF_ATTN_MMA = 0, 2
 NF_EPI_STORE, NF_EPI_RESID, NF_EPI_SWIGLU = 0, 1, 2
 (NF_BUF_TOK_SEQ, NF_BUF_TOK_POS, NF_BUF_TOK_SLOT, NF_BUF_ITEMS, NF_BUF_ITEM_SEG, NF_BUF_N1,
  NF_BUF_Q, NF_BUF_O, NF_BUF_H, NF_BUF_N2, NF_BUF_A, NF_BUF_MOE_OFF, NF_BUF_MOE_PERM,
@@ -221,7 +221,7 @@ def opts_dict(o: nf_plan_opts) -> dict:
             "attn_sms": o.attn_sms, "gemm_sms": o.gemm_sms, "kv_chunk": o.kv_chunk,
             "attn_warps": o.attn_warps, "gemm_stages": o.gemm_stages,
             "gemm_split_k": o.gemm_split_k,
-            "attn_impl": {NF_ATTN_FMA: "fma", NF_ATTN_MMA: "mma"}.get(o.attn_impl, "auto")}
+            "attn_impl": {NF_ATTN_MMA: "mma"}.get(o.attn_impl, "auto")}
 
 
 def make_weights_struct(w: dict) -> nf_layer_weights:

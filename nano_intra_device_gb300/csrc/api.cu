@@ -315,19 +315,15 @@ nf_status check_opts(const nf_plan_opts* o, int T, int num_sms) {
     return fail(NF_ERR_INVALID_ARG, "SM shares must lie in [0, %d]", num_sms);
   if (o->timeout_ns <= 0) return fail(NF_ERR_INVALID_ARG, "timeout_ns must be positive");
   const int aw = o->attn_warps;
-  if (aw < 4 || (aw > 8 && aw != 10 && aw != 12 && aw != 14 && aw != 16))
-    return fail(NF_ERR_INVALID_ARG, "attn_warps must be 4 ... 8, 10, 12, 14 or 16");
+  if (aw < 4 || (aw > 8 && aw != 10 && aw != 12 && aw != 14))
+    return fail(NF_ERR_INVALID_ARG, "attn_warps must be 4 ... 8, 10, 12 or 14");
   if (o->gemm_stages < 2 || o->gemm_stages > 4)
     return fail(NF_ERR_INVALID_ARG, "gemm_stages must be 2, 3 or 4");
   if (o->gemm_split_k < 0 || o->gemm_split_k > 2)
     return fail(NF_ERR_INVALID_ARG,
                 "gemm_split_k must be 0 (automatic), 1 (never) or 2 (token-row tiles only)");
-  if (o->attn_impl < NF_ATTN_AUTO || o->attn_impl > NF_ATTN_MMA)
-    return fail(NF_ERR_INVALID_ARG, "attn_impl must be 0 (automatic), 1 (FMA) or 2 (MMA)");
-  if (o->attn_impl == NF_ATTN_MMA && aw == 16)
-    return fail(NF_ERR_INVALID_ARG, "the tensor-core attention runs 4 ... 8, 10, 12 or 14 warps");
-  if (o->attn_impl == NF_ATTN_FMA && aw != 4 && aw != 5 && aw != 8 && aw != 12 && aw != 16)
-    return fail(NF_ERR_INVALID_ARG, "the FMA attention runs 4, 5, 8, 12 or 16 warps per CTA");
+  if (o->attn_impl != NF_ATTN_AUTO && o->attn_impl != NF_ATTN_MMA)
+    return fail(NF_ERR_INVALID_ARG, "attn_impl must be 0 (automatic) or 2 (tensor cores)");
   return NF_OK;
 }
 
@@ -569,22 +565,13 @@ nf_status build_plan(const nf_model_shape* shape, const nf_batch_desc* batch,
     const nf_model_shape& sh = p->shape;
     const bool mma_ok = nf::attention_mma_supported(sh.n_q_heads, sh.n_kv_heads, sh.head_dim,
                                                     sh.page_size, p->num_pages);
-    if (p->opts.attn_impl == NF_ATTN_MMA && !mma_ok) {
+    if (!mma_ok) {
       delete p;
-      return fail(NF_ERR_UNSUPPORTED, "tensor-core attention: unsupported shape or pool size");
+      return fail(NF_ERR_UNSUPPORTED, "attention: unsupported shape or pool size (page 16, "
+                  "head_dim 64 or 128, n_q / n_kv in 1, 2, 4, 8)");
     }
-    // automatic: the tensor cores, except for the FMA kernel's own 5-warp
-    // shared-SM and 16-warp warp-pair configurations
-    const int w = p->opts.attn_warps;
-    const bool fma_cfg = w == 5 || w == 16;
-    const bool fma_has = w == 4 || w == 5 || w == 8 || w == 12 || w == 16;
-    p->attn_mma = p->opts.attn_impl == NF_ATTN_MMA ||
-                  (p->opts.attn_impl == NF_ATTN_AUTO && mma_ok && !fma_cfg);
-    if (!p->attn_mma && !fma_has) {
-      delete p;
-      return fail(NF_ERR_UNSUPPORTED, "attn_warps %d needs the tensor-core attention", w);
-    }
-    p->opts.attn_impl = p->attn_mma ? NF_ATTN_MMA : NF_ATTN_FMA;  // nf_plan_info reports the choice
+    p->attn_mma = true;
+    p->opts.attn_impl = NF_ATTN_MMA;  // nf_plan_info reports the kernel
   }
   s = alloc_plan(p);
   if (s != NF_OK) {
@@ -885,9 +872,7 @@ nf_status run_attention(nf_plan p, int seg, const void* q, const void* kp, const
     if (n_pf > 0)
       NF_CUDA(nf::launch_attention_prefill(a, pm->tk, pm->tv, p->pf_tiles + p->pf_seg[seg], n_pf, st));
     NF_CUDA(nf::launch_attention_mma(a, pm->tk, pm->tv, grid, n_pf > 0, st));
-    return NF_OK;
   }
-  NF_CUDA(nf::launch_attention(a, grid, st));
   return NF_OK;
 }
 

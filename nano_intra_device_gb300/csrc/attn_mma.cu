@@ -1,15 +1,15 @@
 // Paged GQA attention with the dot products on the tensor cores.
 //
-// Same operation, work list and split-KV records as the CUDA-core kernel
-// (attn.cu): each token row attends to positions 0..pos of its sequence through
-// the block table, one warp per piece (row, chunk of kv_chunk positions, KV
-// head), pieces fetched from a per-nano-batch counter by a persistent grid.
-// Decode attention moves far more bytes than it computes on ("NanoFlow: Towards
-// Optimal LLM Serving Throughput", "The Intra-Device Parallelism Mechanism":
-// the memory-bound operation).  The CUDA-core kernel spends about 47 issue
-// slots per (position, KV head), so it needs nearly every SM to keep HBM busy;
-// here one page costs about 60 warp instructions, so a fraction of the SMs
-// saturates HBM and the rest stay free for the GEMMs of another nano-batch.
+// Each token row attends to positions 0..pos of its sequence through the block
+// table.  The work list cuts every row into split-KV pieces (row, chunk of
+// kv_chunk positions); one warp takes one piece for one KV head, fetched from a
+// per-nano-batch counter by a persistent grid, and pieces of a row that was cut
+// are merged by log-sum-exp (attn_merge.cuh).  Decode attention moves far more
+// bytes than it computes on ("NanoFlow: Towards Optimal LLM Serving
+// Throughput", "The Intra-Device Parallelism Mechanism": the memory-bound
+// operation); with the dot products on the tensor cores one page costs about 60
+// warp instructions, so that part of the SMs can keep HBM busy while the rest
+// run the GEMMs of another nano-batch.
 //
 // Per page (16 positions) and KV head, with the GQA group of GRP query heads
 // padded to the 8 columns of an m16n8k16 tile:
@@ -33,6 +33,10 @@
 #include "mma_frag.cuh"
 
 namespace nf {
+
+int attn_partial_floats(int n_q, int n_kv, int head_dim) {
+  return partial_rec_floats(n_q / n_kv, head_dim);
+}
 
 constexpr int AMMA_MAX_PIECE_PAGES = 2048 / AMMA_P;  // longest piece: 4 page ids per lane
 constexpr int AMMA_MIN_SMEM = 120 * 1024;            // > half an SM: one CTA per SM

@@ -160,8 +160,8 @@ struct AttnArgs {
   int seg;                   // which attention nano-batch
   int n_q, n_kv, head_dim, page_size, max_pages, num_pages, kv_chunk, max_chunks;
   float scale_log2;          // log2(e) / sqrt(d)
-  int warps;                 // warps per CTA: 8 (3 pages in flight each); 12 or 16: warp
-                             // pairs (head_dim 128); 4 or 5 leave room for a 2-stage GEMM CTA
+  int warps;                 // warps per CTA: 8 (3 pages in flight each); 4 leaves room for a
+                             // 2-stage GEMM CTA on the same SM
   // tensor-core decode kernel: with prefill_elsewhere set, rows of sequences
   // n_decode_seqs and up (the prefill chunks) are left to the prefill kernel
   int prefill_elsewhere;
@@ -176,9 +176,6 @@ int attn_partial_floats(int n_q, int n_kv, int head_dim);  // floats per (row, c
 __host__ __device__ constexpr int partial_rec_floats(int grp, int head_dim) {
   return grp * head_dim + ((2 * grp + 3) / 4) * 4;
 }
-// Warp-pair variant for head_dim 128 (warps 12: 6 pairs x 4 stages; 16: 8 pairs x 3).
-cudaError_t launch_attention_pair(const AttnArgs& a, int grid, cudaStream_t stream);
-cudaError_t launch_attention(const AttnArgs& a, int grid, cudaStream_t stream);
 // Tensor-core variant (mma.sync m16n8k16, bf16 operands, fp32 accumulators) of
 // the same operation with the same records; K and V pages arrive by 2-D TMA
 // copies through maps over the pools viewed as [num_pages * n_kv * 16, d]
