@@ -338,7 +338,7 @@ nf_status search(const nf_model_shape* shape, const nf_batch_desc* batch, const 
       }
     }
   }
-  nf_plan_opts best;
+  nf_plan_opts best{};
   std::memset(&best, 0, sizeof(best));
   best.n_attn = 1;
   best.attn_bounds[1] = T;
