@@ -69,12 +69,6 @@ def parse():
                          "layer (8 experts, top-2) over a 2048-token mixed step; serve: the "
                          "runtime serving synthetic requests on the 32-layer 8B-shaped stack")
     ap.add_argument("--batch", type=int, default=256, help="decode requests of the stack workload")
-    ap.add_argument("--attn-prefetch", type=int, default=0,
-                    help="pages each attention warp prefetches into L2 beyond its ring")
-    ap.add_argument("--attn-warps", type=int, default=0)
-    ap.add_argument("--attn", default="mma", choices=["mma", "ws"],
-                    help="decode attention kernel of the layer workload: per-warp rings (mma) or "
-                         "warp-specialised (ws)")
     return ap.parse_args()
 
 
@@ -672,13 +666,7 @@ def main():
     pk = peaks()
     sms = _lib.device_sm_count()
 
-    attn_impl = _lib.NF_ATTN_WS if args.attn == "ws" else _lib.NF_ATTN_MMA
-
     def make_plan(opts):
-        if opts is not None:
-            opts.attn_impl = attn_impl
-            opts.attn_prefetch = args.attn_prefetch
-            opts.attn_warps = args.attn_warps
         return _lib.Plan(wk.shape, wk.batch, opts)
 
     def stepper(plan):

@@ -63,11 +63,9 @@ typedef enum {
 
 typedef enum {
   NF_ATTN_AUTO = 0, /* NF_ATTN_MMA */
-  NF_ATTN_MMA = 2,  /* dot products on the tensor cores (mma.sync, bf16 x bf16 -> fp32), each
-                       warp streaming its own pages; value 1 (a CUDA-core kernel, removed) is
-                       refused */
-  NF_ATTN_WS = 3    /* the same arithmetic, warp-specialised: one producer warp streams the
-                       pages of 12 consumer warps (attn_warps ignored) */
+  NF_ATTN_MMA = 2   /* dot products on the tensor cores (mma.sync, bf16 x bf16 -> fp32), each
+                       warp streaming its own pages; values 1 (a CUDA-core kernel) and 3 (a
+                       warp-specialised variant), both removed, are refused */
 } nf_attn_impl;
 
 /* Shape of one Llama-style decoder layer.  head_dim in {64, 128};
@@ -137,8 +135,6 @@ typedef struct {
                            tiles, split as in 0 (no weight-row kernel) */
   int32_t attn_impl;  /* nf_attn_impl; nf_plan_info reports the kernel chosen */
   int32_t validate;   /* 1 = check page ids and lengths on the device */
-  int32_t attn_prefetch; /* decode attention (NF_ATTN_MMA): pages a warp asks L2 to fetch
-                            beyond its ring, 0 ... 32 (0 = none) */
   int64_t timeout_ns; /* limit of every device-side wait (0 = 2e9) */
 } nf_plan_opts;
 

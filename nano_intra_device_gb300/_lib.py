@@ -19,7 +19,7 @@ NF_MAX_NANO = 8
 NF_OK, NF_ERR_INVALID_ARG, NF_ERR_UNSUPPORTED, NF_ERR_OOM, NF_ERR_CUDA, NF_ERR_TIMEOUT, \
     NF_ERR_DEVICE, NF_ERR_INTERNAL = range(8)
 NF_EXEC_SEQUENTIAL, NF_EXEC_STREAMS = 0, 1
-NF_ATTN_AUTO, NF_ATTN_MMA, NF_ATTN_WS = 0, 2, 3
+NF_ATTN_AUTO, NF_ATTN_MMA = 0, 2
 NF_EPI_STORE, NF_EPI_RESID, NF_EPI_SWIGLU = 0, 1, 2
 (NF_BUF_TOK_SEQ, NF_BUF_TOK_POS, NF_BUF_TOK_SLOT, NF_BUF_ITEMS, NF_BUF_ITEM_SEG, NF_BUF_N1,
  NF_BUF_Q, NF_BUF_O, NF_BUF_H, NF_BUF_N2, NF_BUF_A, NF_BUF_MOE_OFF, NF_BUF_MOE_PERM,
@@ -45,7 +45,7 @@ class nf_plan_opts(Structure):
                 ("executor", c_int32), ("attn_sms", c_int32), ("gemm_sms", c_int32),
                 ("kv_chunk", c_int32), ("attn_warps", c_int32), ("gemm_stages", c_int32),
                 ("gemm_split_k", c_int32), ("attn_impl", c_int32), ("validate", c_int32),
-                ("attn_prefetch", c_int32), ("timeout_ns", c_int64)]
+                ("timeout_ns", c_int64)]
 
 
 class nf_runtime_opts(Structure):
@@ -195,8 +195,7 @@ def make_batch_desc(batch, hint=True):
 
 def make_opts(T, attn_bounds=None, ffn_bounds=None, executor=NF_EXEC_SEQUENTIAL, attn_sms=0,
               gemm_sms=0, kv_chunk=1024, validate=0, timeout_ns=2_000_000_000,
-              attn_warps=0, gemm_stages=0, gemm_split_k=0, attn_impl=0,
-              attn_prefetch=0) -> nf_plan_opts:
+              attn_warps=0, gemm_stages=0, gemm_split_k=0, attn_impl=0) -> nf_plan_opts:
     ab = list(attn_bounds) if attn_bounds is not None else [0, T]
     fb = list(ffn_bounds) if ffn_bounds is not None else list(ab)
     o = nf_plan_opts()
@@ -212,7 +211,6 @@ def make_opts(T, attn_bounds=None, ffn_bounds=None, executor=NF_EXEC_SEQUENTIAL,
     o.gemm_stages = gemm_stages
     o.gemm_split_k = gemm_split_k
     o.attn_impl = attn_impl
-    o.attn_prefetch = attn_prefetch
     return o
 
 
@@ -223,8 +221,7 @@ def opts_dict(o: nf_plan_opts) -> dict:
             "attn_sms": o.attn_sms, "gemm_sms": o.gemm_sms, "kv_chunk": o.kv_chunk,
             "attn_warps": o.attn_warps, "gemm_stages": o.gemm_stages,
             "gemm_split_k": o.gemm_split_k,
-            "attn_impl": {NF_ATTN_MMA: "mma", NF_ATTN_WS: "ws"}.get(o.attn_impl, "auto"),
-            "attn_prefetch": o.attn_prefetch}
+            "attn_impl": {NF_ATTN_MMA: "mma"}.get(o.attn_impl, "auto")}
 
 
 def make_weights_struct(w: dict) -> nf_layer_weights:

@@ -20,7 +20,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libnanoflow.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["api.cu", "gemm_tc.cu", "gemm_wrows.cu", "attn_mma.cu", "attn_ws.cu", "attn_prefill.cu", "meta.cu", "moe.cu", "rmsnorm.cu", "runtime.cu",
+SOURCES = ["api.cu", "gemm_tc.cu", "gemm_wrows.cu", "attn_mma.cu", "attn_prefill.cu", "meta.cu", "moe.cu", "rmsnorm.cu", "runtime.cu",
            "profile.cu", "search.cpp", "noalloc.cu", "selftest.cu"]
 
 

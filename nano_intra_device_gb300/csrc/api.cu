@@ -322,13 +322,8 @@ nf_status check_opts(const nf_plan_opts* o, int T, int num_sms) {
   if (o->gemm_split_k < 0 || o->gemm_split_k > 2)
     return fail(NF_ERR_INVALID_ARG,
                 "gemm_split_k must be 0 (automatic), 1 (never) or 2 (token-row tiles only)");
-  if (o->attn_impl != NF_ATTN_AUTO && o->attn_impl != NF_ATTN_MMA && o->attn_impl != NF_ATTN_WS)
-    return fail(NF_ERR_INVALID_ARG,
-                "attn_impl must be 0 (automatic), 2 (tensor cores) or 3 (warp-specialised)");
-  if (o->attn_prefetch < 0 || o->attn_prefetch > 32)
-    return fail(NF_ERR_INVALID_ARG, "attn_prefetch must lie in [0, 32] pages");
-  if (o->attn_impl == NF_ATTN_WS && o->kv_chunk > 2048)
-    return fail(NF_ERR_INVALID_ARG, "the warp-specialised attention takes kv_chunk <= 2048");
+  if (o->attn_impl != NF_ATTN_AUTO && o->attn_impl != NF_ATTN_MMA)
+    return fail(NF_ERR_INVALID_ARG, "attn_impl must be 0 (automatic) or 2 (tensor cores)");
   return NF_OK;
 }
 
@@ -851,7 +846,6 @@ nf_status run_attention(nf_plan p, int seg, const void* q, const void* kp, const
   a.max_chunks = p->max_chunks;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p->shape.head_dim));
   a.warps = p->opts.attn_warps;
-  a.l2_prefetch = p->opts.attn_prefetch;
   a.prefill_elsewhere = p->attn_mma && p->n_prefill > 0;
   a.n_decode_seqs = p->n_decode;
   a.status = p->status;
@@ -877,10 +871,7 @@ nf_status run_attention(nf_plan p, int seg, const void* q, const void* kp, const
     const int n_pf = a.prefill_elsewhere ? p->pf_seg[seg + 1] - p->pf_seg[seg] : 0;
     if (n_pf > 0)
       NF_CUDA(nf::launch_attention_prefill(a, pm->tk, pm->tv, p->pf_tiles + p->pf_seg[seg], n_pf, st));
-    if (p->opts.attn_impl == NF_ATTN_WS)
-      NF_CUDA(nf::launch_attention_ws(a, pm->tk, pm->tv, grid, n_pf > 0, st));
-    else
-      NF_CUDA(nf::launch_attention_mma(a, pm->tk, pm->tv, grid, n_pf > 0, st));
+    NF_CUDA(nf::launch_attention_mma(a, pm->tk, pm->tv, grid, n_pf > 0, st));
   }
   return NF_OK;
 }
@@ -1220,7 +1211,7 @@ nf_status nf_plan_save(nf_plan p, const char* path) {
   FILE* f = std::fopen(path, "w");
   if (!f) return fail(NF_ERR_INVALID_ARG, "cannot open %s", path);
   const nf_model_shape& s = p->shape;
-  std::fprintf(f, "nanoflow-plan 3\n");
+  std::fprintf(f, "nanoflow-plan 2\n");
   std::fprintf(f, "shape %d %d %d %d %d %d %.9g %.9g\n", s.hidden, s.n_q_heads, s.n_kv_heads,
                s.head_dim, s.ffn, s.page_size, s.rms_eps, s.rope_theta);
   std::fprintf(f, "batch %d %d %d %d\n", p->n_decode, p->n_prefill, p->max_pages, p->num_pages);
@@ -1232,9 +1223,9 @@ nf_status nf_plan_save(nf_plan p, const char* path) {
   for (int i = 0; i <= o.n_attn; ++i) std::fprintf(f, " %d", o.attn_bounds[i]);
   std::fprintf(f, "\nffn %d", o.n_ffn);
   for (int i = 0; i <= o.n_ffn; ++i) std::fprintf(f, " %d", o.ffn_bounds[i]);
-  std::fprintf(f, "\nexec %d %d %d %d %d %lld %d %d %d %d %d\n", o.executor, o.attn_sms,
+  std::fprintf(f, "\nexec %d %d %d %d %d %lld %d %d %d %d\n", o.executor, o.attn_sms,
                o.gemm_sms, o.kv_chunk, o.validate, (long long)o.timeout_ns, o.attn_warps,
-               o.gemm_stages, o.gemm_split_k, o.attn_impl, o.attn_prefetch);
+               o.gemm_stages, o.gemm_split_k, o.attn_impl);
   std::fclose(f);
   return NF_OK;
 }
@@ -1248,7 +1239,7 @@ nf_status nf_plan_load(const char* path, nf_plan* out) {
   int nd = 0, np = 0, mp = 0, npg = 0, ver = 0;
   long long tmo = 0;
   std::vector<int> pq;
-  bool ok = std::fscanf(f, " nanoflow-plan %d", &ver) == 1 && ver == 3;
+  bool ok = std::fscanf(f, " nanoflow-plan %d", &ver) == 1 && ver == 2;
   ok = ok && std::fscanf(f, " shape %d %d %d %d %d %d %f %f", &s.hidden, &s.n_q_heads,
                          &s.n_kv_heads, &s.head_dim, &s.ffn, &s.page_size, &s.rms_eps,
                          &s.rope_theta) == 8;
@@ -1263,9 +1254,9 @@ nf_status nf_plan_load(const char* path, nf_plan* out) {
   for (int i = 0; ok && i <= o.n_attn; ++i) ok = std::fscanf(f, " %d", &o.attn_bounds[i]) == 1;
   ok = ok && std::fscanf(f, " ffn %d", &o.n_ffn) == 1 && o.n_ffn >= 1 && o.n_ffn <= NF_MAX_NANO;
   for (int i = 0; ok && i <= o.n_ffn; ++i) ok = std::fscanf(f, " %d", &o.ffn_bounds[i]) == 1;
-  ok = ok && std::fscanf(f, " exec %d %d %d %d %d %lld %d %d %d %d %d", &o.executor, &o.attn_sms,
+  ok = ok && std::fscanf(f, " exec %d %d %d %d %d %lld %d %d %d %d", &o.executor, &o.attn_sms,
                          &o.gemm_sms, &o.kv_chunk, &o.validate, &tmo, &o.attn_warps,
-                         &o.gemm_stages, &o.gemm_split_k, &o.attn_impl, &o.attn_prefetch) == 11;
+                         &o.gemm_stages, &o.gemm_split_k, &o.attn_impl) == 10;
   std::fclose(f);
   if (!ok) return fail(NF_ERR_INVALID_ARG, "%s is not a plan file", path);
   o.timeout_ns = tmo;

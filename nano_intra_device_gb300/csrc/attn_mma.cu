@@ -154,18 +154,6 @@ __global__ void __launch_bounds__(WARPS * 32, WARPS == AMMA_SHARE_WARPS ? 4 : 1)
       for (int b = 0; b < NCH; ++b)
         tma_load_2d_hint(sl + BLK + b * BOX, &tmV, &bar[st], b * 64, y, policy);
     };
-    // pages past the ring go to L2 ahead of their copies (a.l2_prefetch of them)
-    const int pfd = a.l2_prefetch;
-    auto prefetch_l2 = [&](int k) {  // page k of the piece (warp-uniform k; every lane calls)
-      const int page = page_id(k);
-      if (lane == 0) {
-        const size_t off = (static_cast<size_t>(page) * n_kv + g) * (P * D);
-        bulk_prefetch_l2(a.k_pool + off, BLK);
-        bulk_prefetch_l2(a.v_pool + off, BLK);
-      }
-    };
-    if (pfd > 0)
-      for (int k = STAGES; k < npg && k < STAGES + pfd; ++k) prefetch_l2(k);
     int issued = 0;
     {
       const int pre = npg < STAGES ? npg : STAGES;
@@ -363,9 +351,6 @@ __global__ void __launch_bounds__(WARPS * 32, WARPS == AMMA_SHARE_WARPS ? 4 : 1)
       int pg[PPI];
 #pragma unroll
       for (int i = 0; i < PPI; ++i) pg[i] = k + i + STAGES < npg ? page_id(k + i + STAGES) : -1;
-      if (pfd > 0)
-        for (int i = 0; i < PPI; ++i)
-          if (k + i + STAGES + pfd < npg) prefetch_l2(k + i + STAGES + pfd);
       __syncwarp();
       if (lane == 0 && pg[0] >= 0) fence_proxy_async_smem();
 #pragma unroll

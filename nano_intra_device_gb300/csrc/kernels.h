@@ -162,7 +162,6 @@ struct AttnArgs {
   float scale_log2;          // log2(e) / sqrt(d)
   int warps;                 // warps per CTA: 8 (3 pages in flight each); 4 leaves room for a
                              // 2-stage GEMM CTA on the same SM
-  int l2_prefetch;           // pages beyond a warp's ring to prefetch into L2 (0 = none)
   // tensor-core decode kernel: with prefill_elsewhere set, rows of sequences
   // n_decode_seqs and up (the prefill chunks) are left to the prefill kernel
   int prefill_elsewhere;
@@ -188,11 +187,6 @@ bool make_pool_tmap(CUtensorMap* map, const void* pool, int num_pages, int n_kv,
 // prefill kernel of the same nano-batch); the grid waits for it before it ends.
 cudaError_t launch_attention_mma(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
                                  int grid, bool programmatic, cudaStream_t stream);
-// Warp-specialised variant (attn_ws.cu): one producer warp feeds 11 consumer
-// warps' page rings (TMA, with L2 prefetch ahead); same records and results.
-// kv_chunk <= 2048.
-cudaError_t launch_attention_ws(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
-                                int grid, bool programmatic, cudaStream_t stream);
 // Causal attention of prefill-chunk rows (attn_prefill.cu), flash style on the
 // tensor cores: tiles[i] = (first row, end row, sequence, 0), rows of one
 // prefill sequence, at most prefill_tile_rows(n_q, n_kv) of them; one CTA per

@@ -317,73 +317,3 @@ def test_attention_llama8b_sampled_rows(warps):
                       [b.n_decode, b.n_decode + 1, T - 1] +
                       (b.n_decode + rng.choice(256, 8, replace=False)).tolist()))
     _attention_case(wl.llama8b_shape(), b, rows, [0, 1024, T], 512, warps=warps)
-
-
-# ------------------------------------------------ warp-specialised attention
-WS = _lib.NF_ATTN_WS
-
-
-@pytest.mark.parametrize("grp,d", [(1, 64), (2, 128), (4, 128), (8, 128), (8, 64), (4, 64)])
-@pytest.mark.parametrize("kv_chunk", [16, 256, 2048])
-def test_attention_ws_gqa_head_dims_and_pieces(grp, d, kv_chunk):
-    """The warp-specialised kernel on every GQA group and head_dim, with pieces
-    of one page (every row merged from many records), of 16 pages and whole
-    rows; rows of 1 to 1100 positions, page edges, a prefill chunk after a
-    prefix; every row against the oracle."""
-    shape = wl.Shape(hidden=512, n_q=2 * grp, n_kv=2, head_dim=d, ffn=512)
-    b = wl.make_batch(shape, [1, 15, 16, 17, 700, 1100], [9], [40], seed_bt=7)
-    _attention_case(shape, b, list(range(b.n_tokens)), [0, 3, b.n_tokens], kv_chunk, seed=grp,
-                    impl=WS)
-
-
-def test_attention_ws_llama8b_sampled_rows():
-    b = wl.llama8b_batch()
-    T = b.n_tokens
-    ctx = b.seq_lens[: b.n_decode]
-    rng = np.random.default_rng(0)
-    rows = sorted(set([int(np.argmax(ctx)), int(np.argmin(ctx))] +
-                      rng.choice(b.n_decode, 40, replace=False).tolist() +
-                      [b.n_decode, b.n_decode + 1, T - 1] +
-                      (b.n_decode + rng.choice(256, 8, replace=False)).tolist()))
-    _attention_case(wl.llama8b_shape(), b, rows, [0, 1024, T], 512, impl=WS)
-
-
-def test_attention_ws_equals_mma_kernel_bit_for_bit():
-    """Both kernels run the same per-page arithmetic in the same order and the
-    same merge: identical outputs."""
-    shape = wl.llama8b_shape()
-    b = wl.make_batch(shape, wl.lognormal_contexts(200, 600.0, 1.0, 1, 4096, seed=5), [48], None,
-                      seed_bt=6, max_pages=4096 // 16)
-    T = b.n_tokens
-    kp, vp = wl.make_pools(shape, b, DEV, seed=8, appended=True)
-    q = _rand(T, shape.n_q, shape.head_dim, seed=9).to(DEV)
-    bt = torch.from_numpy(b.block_table).to(DEV)
-    sl = torch.from_numpy(b.seq_lens).to(DEV)
-    outs = {}
-    for impl in (MMA, WS):
-        plan = _lib.Plan(shape, b, _lib.make_opts(T, [0, 100, T], kv_chunk=256, attn_impl=impl))
-        assert plan.info()[0].attn_impl == impl
-        o = torch.empty(T, shape.n_q, shape.head_dim, dtype=torch.bfloat16, device=DEV)
-        _lib.attention(plan, q, kp, vp, bt, sl, o)
-        plan.poll()
-        plan.close()
-        outs[impl] = o
-    assert torch.equal(outs[MMA], outs[WS])
-
-
-def test_attention_ws_reports_a_bad_page_without_reading_it():
-    shape = wl.tiny_shape()
-    b = wl.tiny_batch()
-    bt = b.block_table.copy()
-    bt[1, 1] = b.num_pages + 3
-    T = b.n_tokens
-    kp, vp = wl.make_pools(shape, b, DEV, seed=3, appended=True)
-    q = _rand(T, shape.n_q, shape.head_dim, seed=4).to(DEV)
-    plan = _lib.Plan(shape, b, _lib.make_opts(T, kv_chunk=32, attn_impl=WS))
-    o = torch.empty(T, shape.n_q, shape.head_dim, dtype=torch.bfloat16, device=DEV)
-    _lib.attention(plan, q, kp, vp, torch.from_numpy(bt).to(DEV),
-                   torch.from_numpy(b.seq_lens).to(DEV), o)
-    with pytest.raises(_lib.NanoflowError) as e:
-        plan.poll()
-    assert e.value.code == _lib.NF_ERR_DEVICE
-    plan.close()
