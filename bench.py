@@ -282,6 +282,29 @@ def run_reference(args):
 
 
 # -------------------------------------------------------------------- main
+def step_profile(shape, batch, n_layers):
+    """nf_profile_step on this batch structure (the R -> P table measured in
+    traced steps; registered for the shape, so plan creation without options
+    and the searches use it): its wall time, and each profiled plan's measured
+    against predicted step time."""
+    import tempfile
+    from nano_intra_device_gb300 import _lib
+    path = os.path.join(tempfile.mkdtemp(prefix="nf_profile_"), "step_profile.json")
+    t0 = time.perf_counter()
+    _lib.profile_step(shape, batch, n_layers, path)
+    d = json.load(open(path))
+    runs = d.get("runs", [])
+    err = [abs(r["predicted_ms"] / r["measured_ms"] - 1) for r in runs if r["measured_ms"] > 0]
+    return {"seconds": round(time.perf_counter() - t0, 2), "layers_profiled": d.get("n_layers"),
+            "rp_sms": d.get("rp_sms"), "rp_attn_gbs_per_sm": [round(x / 1e9, 1) for x in d.get("rp_attn_bps_per_sm", [])],
+            "rp_gemm_factor": [round(x, 3) for x in d.get("rp_gemm_factor", [])],
+            "stream_sync_us": round(d.get("stream_sync_s", 0) * 1e6, 1),
+            "model_error_mean": round(sum(err) / max(1, len(err)), 4),
+            "model_error_max": round(max(err, default=0), 4),
+            "runs": [[r["n_attn"], r["attn_sms"], round(r["measured_ms"], 3), round(r["predicted_ms"], 3)]
+                     for r in runs]}
+
+
 def time_steps(fn, steps, warmup, world, stream):
     for _ in range(warmup):
         fn()
@@ -378,6 +401,8 @@ def run_layers_workload(args, shape, batch, L, metric, workload, fracs_by_n):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     T, H, F = batch.n_tokens, shape.hidden, shape.ffn
+    # the step profile first: it allocates (and frees) its own weights and pool
+    prof = step_profile(shape, batch, L)
     g = torch.Generator(device=dev).manual_seed(0)
 
     def rn(*sz, std=0.02):
@@ -398,8 +423,9 @@ def run_layers_workload(args, shape, batch, L, metric, workload, fracs_by_n):
     # layers); "search" is the layer-aware search's pick (it scores the window
     # over all the layers), and each candidate's model prediction is reported
     # beside its measured time
-    searched, _ = _lib.plan_search(shape, batch, None, sms, n_layers=L)
-    cands = [("search", searched), ("sequential", _lib.make_opts(T))]
+    searched, _ = _lib.plan_search(shape, batch, None, sms, n_layers=L)   # the profile's rates
+    builtin, _ = _lib.plan_search(shape, batch, "", sms, n_layers=L)      # the built-in rates
+    cands = [("search", searched), ("search_builtin", builtin), ("sequential", _lib.make_opts(T))]
 
     def bounds(n):
         return [0] + [int(round(T * i / n / 128)) * 128 for i in range(1, n)] + [T]
@@ -442,7 +468,10 @@ def run_layers_workload(args, shape, batch, L, metric, workload, fracs_by_n):
                                      "t_flop_ms": rf["t_flop"] * 1e3, "t_byte_ms": rf["t_byte"] * 1e3,
                                      "bound": rf["bound"]},
             "candidates_ms": {k: round(v[0], 3) for k, v in tried.items()},
-            "candidates_model_ms": model}
+            "candidates_model_ms": model,
+            "search": {"pick": tried["search"][1], "pick_over_best": round(tried["search"][0] / tried[best][0], 4),
+                       "builtin_pick_over_best": round(tried["search_builtin"][0] / tried[best][0], 4),
+                       "step_profile": prof}}
     print(json.dumps(line), flush=True)
     plan.close()
 
@@ -504,7 +533,9 @@ def run_moe(args):
     sl = torch.from_numpy(batch.seq_lens).to(dev)
     stream = torch.cuda.current_stream()
     sms = _lib.device_sm_count()
-    cands = [("search", None), ("sequential", _lib.make_opts(T))]
+    prof = step_profile(shape, batch, 1)
+    cands = [("search", None), ("search_builtin", _lib.plan_search(shape, batch, "", sms)[0]),
+             ("sequential", _lib.make_opts(T))]
     for n in (2, 3):
         ab = [0] + [int(round(T * i / n / 128)) * 128 for i in range(1, n)] + [T]
         for a_sms in (sms * 6 // 16, sms * 8 // 16, sms * 10 // 16):
@@ -557,7 +588,10 @@ def run_moe(args):
                                "t_flop_ms": rf["t_flop"] * 1e3, "t_byte_ms": rf["t_byte"] * 1e3,
                                "bound": rf["bound"], "flops": work["flops"], "bytes": work["bytes"]},
             "ops_ms": {k: round(float(np.mean(v)), 4) for k, v in ops.items()},
-            "candidates_ms": {k: round(v, 3) for k, v in tried.items()}}
+            "candidates_ms": {k: round(v, 3) for k, v in tried.items()},
+            "search": {"pick_over_best": round(tried["search"] / tried[best], 4),
+                       "builtin_pick_over_best": round(tried["search_builtin"] / tried[best], 4),
+                       "step_profile": prof}}
     print(json.dumps(line), flush=True)
     plan.close()
 
@@ -674,9 +708,12 @@ def main():
 
     # candidates: the library's search, then measured neighbours (real timing of
     # the best predicted plans, the last step of the plan search)
-    searched = make_plan(None)
+    prof = step_profile(wk.shape, wk.batch, 1) if args.plan == "auto" else None
+    searched = make_plan(None)   # plan creation without options: the profile's rates
     so, _ = searched.info()
     cands = [("search", searched), ("sequential", make_plan(_lib.make_opts(T)))]
+    if prof is not None:
+        cands.append(("search_builtin", make_plan(_lib.plan_search(wk.shape, wk.batch, "", sms)[0])))
     if args.plan == "auto":
         for n in (2, 3, 4):
             ab = [0] + [int(round(T * i / n / 128)) * 128 for i in range(1, n)] + [T]
@@ -845,7 +882,11 @@ def main():
             "roofline": roof,
             "overlap": {"attn_gemm_concurrent_ms": overlap, "timeline_last_step": timeline},
             "ablation_tokens_per_s": ablation,
-            "plan_candidates_ms": tried}
+            "plan_candidates_ms": tried,
+            "search": None if prof is None else {
+                "pick": _lib.opts_dict(so), "pick_over_best": round(tried["search"] / tried[best_name], 4),
+                "builtin_pick_over_best": round(tried["search_builtin"] / tried[best_name], 4),
+                "step_profile": prof}}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         sample = oracle_sample(wk, 128, 16, seed=1)
         t = time_oracle(sample)

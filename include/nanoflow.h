@@ -493,10 +493,35 @@ nf_status nf_plan_trace_read(nf_plan plan, nf_trace_entry* out, int32_t cap, int
 nf_status nf_profile(const nf_model_shape* shape, int32_t max_tokens, int32_t mean_ctx,
                      const char* out_json);
 
+/* Measure the R -> P table inside the step itself ("Kernel Profiling and
+ * Interference Modeling": the performance P a kernel keeps for a resource
+ * share R): run this batch structure (seq_lens_hint required, synthetic
+ * weights and K/V) through min(n_layers, 32) layers under the sequential plan
+ * and under two-stream plans of 2, 3 and 4 nano-batches with attention on
+ * 3/16 ... 10/16 of the SMs (the cross-layer window when n_layers > 1), tracing
+ * every nano-operation; fit the search's rates to what ran (the GEMM tensor
+ * rate and attention bandwidth alone; per nano-batch count and attention SM
+ * count the attention's bytes/s per SM and the share of its rate a GEMM kept
+ * while the two overlapped; the cost of a cross-stream dependency and one
+ * factor on the GEMM shares, from the untraced step times); write them with
+ * each plan's measured
+ * and predicted step time to out_json, and register the file for this shape
+ * (nf_profile_use), so that plan creation without options and the searches
+ * below use it.  Allocates its own buffers (weights of one layer, one K/V pool
+ * of batch->num_pages pages); takes seconds. */
+nf_status nf_profile_step(const nf_model_shape* shape, const nf_batch_desc* batch,
+                          int32_t n_layers, const char* out_json);
+
+/* Register a profile (JSON written by nf_profile_step or nf_profile) for this
+ * shape in this process; json_path NULL forgets it.  The path is read when a
+ * search runs. */
+nf_status nf_profile_use(const nf_model_shape* shape, const char* json_path);
+
 /* Plan search on the host only (no device work): given a profile table
- * (JSON written by nf_profile, or NULL for the built-in roofline model), pick
- * the split and SM shares that minimise the predicted step time.  Fills `out`
- * and the predicted time in microseconds. */
+ * (a JSON path; NULL for the profile registered for the shape, else the
+ * built-in rates; "" for the built-in rates), pick the split and SM shares that
+ * minimise the predicted step time.  Fills `out` and the predicted time in
+ * microseconds.  nf_plan_create with opts NULL runs it with NULL. */
 nf_status nf_plan_search(const nf_model_shape* shape, const nf_batch_desc* batch,
                          const char* profile_json, int32_t num_sms, nf_plan_opts* out,
                          double* predicted_us);

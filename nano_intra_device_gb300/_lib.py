@@ -125,6 +125,8 @@ _SIGS = {
     "nf_plan_trace_ops": (c_int, [c_void_p, ctypes.c_uint32]),
     "nf_plan_trace_read": (c_int, [c_void_p, POINTER(nf_trace_entry), c_int32, POINTER(c_int32)]),
     "nf_profile": (c_int, [POINTER(nf_model_shape), c_int32, c_int32, c_char_p]),
+    "nf_profile_step": (c_int, [POINTER(nf_model_shape), POINTER(nf_batch_desc), c_int32, c_char_p]),
+    "nf_profile_use": (c_int, [POINTER(nf_model_shape), c_char_p]),
     "nf_plan_search": (c_int, [POINTER(nf_model_shape), POINTER(nf_batch_desc), c_char_p, c_int32, POINTER(nf_plan_opts), POINTER(c_double)]),
     "nf_plan_search_layers": (c_int, [POINTER(nf_model_shape), POINTER(nf_batch_desc), c_char_p, c_int32, c_int32, POINTER(nf_plan_opts), POINTER(c_double)]),
     "nf_plan_predict": (c_int, [POINTER(nf_model_shape), POINTER(nf_batch_desc), c_char_p, c_int32, c_int32, POINTER(nf_plan_opts), POINTER(c_double)]),
@@ -426,7 +428,7 @@ def plan_search(shape, batch, profile_json=None, num_sms=152, n_layers=1):
     t = c_double()
     s = make_shape(shape)
     b = make_batch_desc(batch, True)
-    prof = profile_json.encode() if profile_json else None
+    prof = None if profile_json is None else profile_json.encode()
     if n_layers == 1:
         check(lib().nf_plan_search(ctypes.byref(s), ctypes.byref(b), prof, num_sms,
                                    ctypes.byref(o), ctypes.byref(t)))
@@ -442,9 +444,23 @@ def plan_predict(shape, batch, opts, profile_json=None, num_sms=152, n_layers=1)
     s = make_shape(shape)
     b = make_batch_desc(batch, True)
     check(lib().nf_plan_predict(ctypes.byref(s), ctypes.byref(b),
-                                profile_json.encode() if profile_json else None, num_sms, n_layers,
-                                ctypes.byref(opts), ctypes.byref(t)))
+                                None if profile_json is None else profile_json.encode(), num_sms,
+                                n_layers, ctypes.byref(opts), ctypes.byref(t)))
     return t.value
+
+
+def profile_step(shape, batch, n_layers, out_json):
+    """nf_profile_step: the R -> P table measured in traced steps of this batch
+    structure; writes out_json and registers it for the shape."""
+    s = make_shape(shape)
+    b = make_batch_desc(batch, True)
+    check(lib().nf_profile_step(ctypes.byref(s), ctypes.byref(b), n_layers, out_json.encode()))
+
+
+def profile_use(shape, json_path):
+    """nf_profile_use: register (or, with None, forget) a profile for the shape."""
+    s = make_shape(shape)
+    check(lib().nf_profile_use(ctypes.byref(s), None if json_path is None else json_path.encode()))
 
 
 def window_schedule(opts, n_layers):

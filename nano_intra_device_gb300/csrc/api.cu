@@ -1334,6 +1334,22 @@ nf_status run_layers_pipelined(nf_plan p, const nf_layer_weights* layers, int n_
     nf_plan p;
     ~Reset() { p->cur_set = 0; }
   } reset_{p};
+  // a traced window is one traced step: every layer's nano-operations, timed
+  // from the step's start on the caller's stream
+  if (p->trace_left > 0) {
+    p->trace_s0 = pooled_event(p);
+    if (p->trace_s0) cudaEventRecord(p->trace_s0, st);
+  }
+  struct StepEnd {
+    nf_plan p;
+    ~StepEnd() {
+      if (p->trace_left > 0 && p->trace_s0) {
+        --p->trace_left;
+        ++p->trace_step;
+      }
+      p->trace_s0 = nullptr;
+    }
+  } step_end_{p};
   cudaEvent_t ev_start = p->ev[0], ev_done = p->ev[1];
   cudaEvent_t* ev_q = &p->ev[2];
   cudaEvent_t* ev_a = &p->ev[2 + NF_MAX_NANO];

@@ -2,6 +2,9 @@
 #pragma once
 #include <cuda_runtime.h>
 
+#include <string>
+#include <vector>
+
 #include "../../include/nanoflow.h"
 
 namespace nf {
@@ -11,4 +14,34 @@ nf_status attention_on(nf_plan p, const void* q, const void* kp, const void* vp,
                        cudaStream_t st);
 // Set the calling thread's nf_last_error() text and return `code`.
 nf_status set_last_error(nf_status code, const char* msg);
+
+// One plan of a step profile: the plan, the operations of its traced steps
+// (durations averaged over `steps` steps) and its untraced step time.
+struct TracedRun {
+  nf_plan_opts opts;
+  std::vector<nf_trace_entry> ops;
+  int steps;
+  double step_ms;
+};
+// Fit the plan search's rates to traced runs of one batch over n_layers
+// layers (runs[0] the sequential plan, the rest two-stream plans): the
+// interference-free GEMM rate and attention bandwidth, the R -> P table by
+// attention SM count, the cost of a cross-stream dependency.  Returns the JSON
+// that nf_plan_search reads (empty on invalid input).
+std::string fit_step_profile(const nf_model_shape* shape, const nf_batch_desc* batch, int num_sms,
+                             int n_layers, const std::vector<TracedRun>& runs);
+// The token bounds of a step profile's n nano-batches of T tokens: equal
+// shares on the 128-token grid (any granularity below 1024 tokens).
+inline void profile_bounds(int T, int n, int32_t* b) {
+  const int grid = T >= 1024 ? 128 : 1;
+  b[0] = 0;
+  for (int i = 1; i < n; ++i) {
+    const int t = (T * i / n + grid / 2) / grid * grid;
+    b[i] = t > b[i - 1] ? t : b[i - 1] + 1;
+  }
+  b[n] = T;
+}
+// The path of the profile registered for this shape (nf_profile_use or
+// nf_profile_step), or "".
+std::string registered_profile(const nf_model_shape* shape);
 }  // namespace nf

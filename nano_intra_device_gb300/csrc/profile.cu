@@ -278,3 +278,189 @@ extern "C" nf_status nf_profile(const nf_model_shape* shape, int32_t max_tokens,
   std::fclose(f);
   return NF_OK;
 }
+
+extern "C" nf_status nf_profile_step(const nf_model_shape* shape, const nf_batch_desc* batch,
+                                     int32_t n_layers, const char* out_json) {
+  if (!shape || !batch || !out_json || n_layers < 1 || !batch->seq_lens_hint)
+    return nf::set_last_error(NF_ERR_INVALID_ARG,
+                              "nf_profile_step: shape, batch with seq_lens_hint, n_layers >= 1 "
+                              "and out_json are required");
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return NF_ERR_CUDA;
+  const nf_model_shape& s = *shape;
+  const int n_seq = batch->n_decode + batch->n_prefill;
+  if (n_seq < 1 || batch->max_pages_per_seq < 1 || batch->num_pages < 1 ||
+      (batch->n_prefill > 0 && !batch->prefill_q_lens))
+    return nf::set_last_error(NF_ERR_INVALID_ARG, "nf_profile_step: invalid batch");
+  int T = 0;
+  size_t pages_needed = 0;
+  for (int i = 0; i < n_seq; ++i) {
+    const int q = i < batch->n_decode ? 1 : batch->prefill_q_lens[i - batch->n_decode];
+    const int L = batch->seq_lens_hint[i];
+    if (q < 1 || L < q || (L + s.page_size - 1) / s.page_size > batch->max_pages_per_seq)
+      return nf::set_last_error(NF_ERR_INVALID_ARG, "nf_profile_step: inconsistent lengths");
+    T += q;
+    pages_needed += (L + s.page_size - 1) / s.page_size;
+  }
+  if (pages_needed > (size_t)batch->num_pages)
+    return nf::set_last_error(NF_ERR_INVALID_ARG, "nf_profile_step: num_pages is too small");
+  // the layers share one set of weights and one pool (the rates do not depend
+  // on which bytes are read); a window's head and tail weigh as in the step
+  // being planned, so the profile runs all its layers (at most 32)
+  const int L = std::min(n_layers, 32);
+  const int H = s.hidden, F = s.ffn, QD = s.n_q_heads * s.head_dim;
+  const int NQKV = (s.n_q_heads + 2 * s.n_kv_heads) * s.head_dim;
+  const int E = s.n_experts;
+  const size_t page_elems = (size_t)s.n_kv_heads * s.page_size * s.head_dim;
+
+  Bufs B;
+  auto* wqkv = B.get<__nv_bfloat16>((size_t)NQKV * H * 2);
+  auto* wo = B.get<__nv_bfloat16>((size_t)H * QD * 2);
+  auto* g1 = B.get<__nv_bfloat16>((size_t)H * 2);
+  auto* g2 = B.get<__nv_bfloat16>((size_t)H * 2);
+  const size_t ffn_rows = (size_t)(E > 0 ? E : 1);
+  auto* wgu = B.get<__nv_bfloat16>(ffn_rows * 2 * F * H * 2);
+  auto* wd = B.get<__nv_bfloat16>(ffn_rows * H * F * 2);
+  float* logits = E > 0 ? B.get<float>((size_t)T * E * 4) : nullptr;
+  auto* x = B.get<__nv_bfloat16>((size_t)T * H * 2);
+  auto* y = B.get<__nv_bfloat16>((size_t)T * H * 2);
+  auto* kp = B.get<__nv_bfloat16>((size_t)batch->num_pages * page_elems * 2);
+  auto* vp = B.get<__nv_bfloat16>((size_t)batch->num_pages * page_elems * 2);
+  auto* bt = B.get<int32_t>((size_t)n_seq * batch->max_pages_per_seq * 4);
+  auto* sl = B.get<int32_t>((size_t)n_seq * 4);
+  if (!wqkv || !wo || !g1 || !g2 || !wgu || !wd || (E > 0 && !logits) || !x || !y || !kp || !vp ||
+      !bt || !sl)
+    return nf::set_last_error(NF_ERR_OOM, "nf_profile_step: device memory");
+  fill_bf16<<<1024, 256>>>(wqkv, (size_t)NQKV * H, 11, 0.03f);
+  fill_bf16<<<1024, 256>>>(wo, (size_t)H * QD, 12, 0.03f);
+  fill_bf16<<<64, 256>>>(g1, H, 13, 0.1f);
+  fill_bf16<<<64, 256>>>(g2, H, 14, 0.1f);
+  fill_bf16<<<1024, 256>>>(wgu, ffn_rows * 2 * F * H, 15, 0.03f);
+  fill_bf16<<<1024, 256>>>(wd, ffn_rows * H * F, 16, 0.03f);
+  fill_bf16<<<1024, 256>>>(x, (size_t)T * H, 17, 1.0f);
+  fill_bf16<<<4096, 256>>>(kp, (size_t)batch->num_pages * page_elems, 18, 1.0f);
+  fill_bf16<<<4096, 256>>>(vp, (size_t)batch->num_pages * page_elems, 19, 1.0f);
+  if (E > 0) {
+    std::vector<float> hl((size_t)T * E);
+    uint32_t h = 12345u;
+    for (float& v : hl) {  // router logits: a fixed pseudo-random draw
+      h = h * 1664525u + 1013904223u;
+      v = ((h >> 8) * (1.0f / 16777216.0f)) * 4.0f - 2.0f;
+    }
+    cudaMemcpy(logits, hl.data(), hl.size() * 4, cudaMemcpyHostToDevice);
+  }
+  {
+    // pages of each sequence from an affine permutation of the pool
+    const size_t np = (size_t)batch->num_pages, mp = (size_t)batch->max_pages_per_seq;
+    size_t mul = 2654435761ull % np;
+    auto gcd = [](size_t a, size_t b) { while (b) { size_t t = a % b; a = b; b = t; } return a; };
+    while (np > 1 && (mul < 1 || gcd(mul, np) != 1)) mul = (mul + 1) % np;
+    std::vector<int32_t> hbt((size_t)n_seq * mp, -1), hsl(n_seq);
+    size_t next = 0;
+    for (int i = 0; i < n_seq; ++i) {
+      hsl[i] = batch->seq_lens_hint[i];
+      const int npg = (hsl[i] + s.page_size - 1) / s.page_size;
+      for (int j = 0; j < npg; ++j) hbt[(size_t)i * mp + j] = (int32_t)((next++ * mul + 3) % np);
+    }
+    cudaMemcpy(bt, hbt.data(), hbt.size() * 4, cudaMemcpyHostToDevice);
+    cudaMemcpy(sl, hsl.data(), hsl.size() * 4, cudaMemcpyHostToDevice);
+  }
+  if (cudaDeviceSynchronize() != cudaSuccess) return NF_ERR_CUDA;
+
+  nf_layer_weights w{};
+  w.norm1 = g1;
+  w.norm2 = g2;
+  w.w_qkv = wqkv;
+  w.w_o = wo;
+  if (E > 0) {
+    w.w_experts_gate_up = wgu;
+    w.w_experts_down = wd;
+    w.router_logits = logits;
+  } else {
+    w.w_gate_up = wgu;
+    w.w_down = wd;
+  }
+  std::vector<nf_layer_weights> lw(L, w);
+  std::vector<void*> kps(L, kp), vps(L, vp);
+  cudaStream_t st;
+  cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking);
+
+  // the plans: sequential, then two-stream plans of 2, 3 and 4 nano-batches with
+  // attention on 3/16 ... 10/16 of the SMs (token bounds on the 128 grid)
+  std::vector<nf_plan_opts> plans;
+  {
+    nf_plan_opts o{};
+    o.n_attn = o.n_ffn = 1;
+    o.attn_bounds[1] = o.ffn_bounds[1] = T;
+    o.kv_chunk = 1024;
+    o.timeout_ns = 2000000000LL;
+    plans.push_back(o);
+    const int grid = T >= 1024 ? 128 : 1;
+    for (int n = 2; n <= 4; ++n) {
+      if (T / grid < n) break;
+      for (int k = 3; k <= 10; ++k) {
+        nf_plan_opts p = o;
+        p.executor = NF_EXEC_STREAMS;
+        p.n_attn = p.n_ffn = n;
+        nf::profile_bounds(T, n, p.attn_bounds);
+        for (int i = 0; i <= n; ++i) p.ffn_bounds[i] = p.attn_bounds[i];
+        p.attn_sms = sms * k / 16;
+        plans.push_back(p);
+      }
+    }
+  }
+  std::vector<nf::TracedRun> runs;
+  nf_status result = NF_OK;
+  cudaEvent_t e0, e1;
+  cudaEventCreate(&e0);
+  cudaEventCreate(&e1);
+  for (const nf_plan_opts& o : plans) {
+    nf_plan plan = nullptr;
+    nf_status ps = nf_plan_create(shape, batch, &o, &plan);
+    if (ps != NF_OK) {
+      result = ps;
+      break;
+    }
+    auto step = [&]() {
+      return L == 1 ? nf_layer_step(plan, &w, x, kp, vp, bt, sl, y, st)
+                    : nf_layers_step(plan, lw.data(), L, x, kps.data(), vps.data(), bt, sl, y, st);
+    };
+    nf_status ss = step();  // warm-up
+    cudaEventRecord(e0, st);
+    for (int r = 0; r < 3 && ss == NF_OK; ++r) ss = step();
+    cudaEventRecord(e1, st);
+    float ms = 0;
+    if (ss == NF_OK && cudaEventSynchronize(e1) == cudaSuccess) cudaEventElapsedTime(&ms, e0, e1);
+    nf::TracedRun run{o, {}, 2, ms / 3.0};
+    if (ss == NF_OK) ss = nf_plan_trace_ops(plan, ~0u);
+    // two calls: a sequential plan traces each layer as a step, a window the call
+    if (ss == NF_OK) ss = nf_plan_trace_enable(plan, o.executor == NF_EXEC_SEQUENTIAL ? 2 * L : 2);
+    for (int r = 0; r < 2 && ss == NF_OK; ++r) ss = step();
+    if (ss == NF_OK) {
+      int32_t n = 0;
+      ss = nf_plan_trace_read(plan, nullptr, 0, &n);
+      run.ops.resize(n);
+      if (ss == NF_OK && n > 0) ss = nf_plan_trace_read(plan, run.ops.data(), n, &n);
+    }
+    if (ss == NF_OK) ss = nf_plan_poll(plan, 1);
+    nf_plan_destroy(plan);
+    if (ss != NF_OK) {
+      result = ss;
+      break;
+    }
+    runs.push_back(std::move(run));
+  }
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  cudaStreamDestroy(st);
+  if (result != NF_OK) return result;
+  const std::string js = nf::fit_step_profile(shape, batch, sms, L, runs);
+  if (js.empty()) return nf::set_last_error(NF_ERR_INTERNAL, "nf_profile_step: the fit failed");
+  FILE* f = std::fopen(out_json, "w");
+  if (!f) return nf::set_last_error(NF_ERR_INVALID_ARG, "nf_profile_step: cannot write out_json");
+  std::fputs(js.c_str(), f);
+  std::fclose(f);
+  return nf_profile_use(shape, out_json);
+}

@@ -220,3 +220,98 @@ def test_search_returns_valid_plans_on_random_batches(L):
         _check_plan(o, T, 128 if T >= 1024 else 1)
         assert 0 <= o.attn_sms < sms and t > 0
         assert _lib.plan_predict(shape, b, o, None, sms, layers) == pytest.approx(t, rel=1e-9)
+
+
+def _profile(tmp_path, name, rp_sms, attn_bps, gemm_factor, sync=25e-6):
+    import json
+    p = tmp_path / name
+    p.write_text(json.dumps({"gemm_flops_per_sm": 11.45e12, "hbm_bps": 6.75e12,
+                             "attn_bps_per_sm": 78e9, "stream_sync_s": sync,
+                             "rp_sms": rp_sms, "rp_attn_bps_per_sm": attn_bps,
+                             "rp_gemm_factor": gemm_factor}))
+    return str(p)
+
+
+def test_search_reads_a_measured_rp_table(L, tmp_path):
+    """A profile's R -> P table (attention bytes/s per SM and the GEMM rate kept,
+    by attention SM count) drives the overlapped predictions: with no
+    interference and fast attention per SM the 70B-shaped window plan is
+    predicted faster than with strong interference, the sequential plan does
+    not depend on the table, and between two table points the prediction lies
+    between those of the points' values."""
+    s70 = wl.llama70b_shape()
+    b70 = wl.llama70b_batch()
+    T = b70.n_tokens
+    good = _profile(tmp_path, "good.json", [40, 80], [150e9, 150e9], [1.0, 1.0])
+    bad = _profile(tmp_path, "bad.json", [40, 80], [60e9, 60e9], [0.5, 0.5])
+    win = _lib.make_opts(T, [0, T // 2, T], [0, T // 2, T], executor=_lib.NF_EXEC_STREAMS,
+                         attn_sms=57)
+    seq = _lib.make_opts(T)
+    assert _lib.plan_predict(s70, b70, win, good, 152, 10) < _lib.plan_predict(s70, b70, win, bad, 152, 10)
+    assert _lib.plan_predict(s70, b70, seq, good, 152, 10) == pytest.approx(
+        _lib.plan_predict(s70, b70, seq, bad, 152, 10), rel=1e-12)
+    mixed = _profile(tmp_path, "mixed.json", [40, 80], [60e9, 150e9], [0.5, 1.0])
+    at40 = _lib.make_opts(T, [0, T // 2, T], [0, T // 2, T], executor=_lib.NF_EXEC_STREAMS, attn_sms=40)
+    at60 = _lib.make_opts(T, [0, T // 2, T], [0, T // 2, T], executor=_lib.NF_EXEC_STREAMS, attn_sms=60)
+    t_bad = _lib.plan_predict(s70, b70, at60, bad, 152, 10)
+    t_good = _lib.plan_predict(s70, b70, at60, good, 152, 10)
+    t_mid = _lib.plan_predict(s70, b70, at60, mixed, 152, 10)
+    assert t_good < t_mid < t_bad
+    # clamped below the table's first point: the first point's values
+    assert _lib.plan_predict(s70, b70, at40, mixed, 152, 10) == pytest.approx(
+        _lib.plan_predict(s70, b70, at40, bad, 152, 10), rel=1e-12)
+
+
+def test_registered_profile_is_the_default(L, tmp_path):
+    """nf_profile_use registers a profile for a shape: a NULL profile then
+    means that file, "" the built-in rates; other shapes are unaffected;
+    forgetting it restores the built-in rates."""
+    s70 = wl.llama70b_shape()
+    b70 = wl.llama70b_batch()
+    T = b70.n_tokens
+    bad = _profile(tmp_path, "bad.json", [40, 80], [60e9, 60e9], [0.5, 0.5])
+    win = _lib.make_opts(T, [0, T // 2, T], [0, T // 2, T], executor=_lib.NF_EXEC_STREAMS,
+                         attn_sms=57)
+    builtin = _lib.plan_predict(s70, b70, win, "", 152, 10)
+    assert _lib.plan_predict(s70, b70, win, None, 152, 10) == pytest.approx(builtin, rel=1e-12)
+    _lib.profile_use(s70, bad)
+    try:
+        assert _lib.plan_predict(s70, b70, win, None, 152, 10) == pytest.approx(
+            _lib.plan_predict(s70, b70, win, bad, 152, 10), rel=1e-12)
+        assert _lib.plan_predict(s70, b70, win, "", 152, 10) == pytest.approx(builtin, rel=1e-12)
+        o_reg, _ = _lib.plan_search(s70, b70, None, 152, n_layers=10)
+        o_bad, _ = _lib.plan_search(s70, b70, bad, 152, n_layers=10)
+        assert _lib.opts_dict(o_reg) == _lib.opts_dict(o_bad)
+        s8, b8 = wl.llama8b_shape(), wl.llama8b_batch()
+        assert _lib.plan_search(s8, b8, None, 152)[1] == pytest.approx(
+            _lib.plan_search(s8, b8, "", 152)[1], rel=1e-12)
+    finally:
+        _lib.profile_use(s70, None)
+    assert _lib.plan_predict(s70, b70, win, None, 152, 10) == pytest.approx(builtin, rel=1e-12)
+
+
+def test_search_picks_the_fastest_profiled_plan_of_the_same_batch(L, tmp_path):
+    """A profile measured on this very batch structure and layer count: the
+    search returns its fastest measured plan (an overlapped one only when it
+    measured at least 1 % faster than the sequential one), with the profile's
+    bounds rule; for another batch it falls back to the model."""
+    import json
+    s8, b8 = wl.llama8b_shape(), wl.llama8b_batch()
+    T = b8.n_tokens
+    prof = {"gemm_flops_per_sm": 11.45e12, "hbm_bps": 6.75e12, "attn_bps_per_sm": 78e9,
+            "rp_n": [2, 2], "rp_sms": [47, 95], "rp_attn_bps_per_sm": [78e9, 60e9],
+            "rp_gemm_factor": [0.8, 0.7], "batch_tokens": T, "batch_decode": b8.n_decode,
+            "n_layers": 16, "run_n": [1, 2, 2, 3], "run_sms": [0, 57, 66, 66],
+            "run_ms": [26.3, 25.4, 24.9, 25.0]}
+    p = tmp_path / "p.json"
+    p.write_text(json.dumps(prof))
+    o, t = _lib.plan_search(s8, b8, str(p), 152, n_layers=16)
+    assert o.executor == _lib.NF_EXEC_STREAMS and o.n_attn == 2 and o.attn_sms == 66
+    assert list(o.attn_bounds[:3]) == [0, 1024, T] and list(o.ffn_bounds[:3]) == [0, 1024, T]
+    assert t == pytest.approx(24.9e3, rel=1e-9)
+    prof["run_ms"] = [26.3, 26.2, 26.1, 26.2]          # less than 1 % better: sequential
+    p.write_text(json.dumps(prof))
+    o, t = _lib.plan_search(s8, b8, str(p), 152, n_layers=16)
+    assert o.executor == _lib.NF_EXEC_SEQUENTIAL and o.n_attn == 1 and t == pytest.approx(26.3e3)
+    o8, _ = _lib.plan_search(s8, b8, str(p), 152, n_layers=8)  # another layer count: the model
+    assert _lib.plan_predict(s8, b8, o8, str(p), 152, 8) > 0
