@@ -260,8 +260,8 @@ def big():
     return case, rows, case.oracle(rows=rows)
 
 
-@pytest.mark.parametrize("n,warps,stages", [(1, 8, 4), (2, 8, 4), (3, 16, 4), (4, 12, 4),
-                                            (2, 4, 2), (1, 16, 4)])
+@pytest.mark.parametrize("n,warps,stages", [(1, 8, 4), (2, 8, 4), (3, 14, 4), (4, 12, 4),
+                                            (2, 4, 2), (1, 10, 4)])
 def test_llama8b_sampled_rows_by_nano_batch_count(big, n, warps, stages):
     case, rows, ref = big
     T = case.batch.n_tokens
@@ -385,3 +385,30 @@ def test_trace_records_only_the_selected_operations(tiny):
         assert sum(e["op"] == "attn" for e in tr) == 2 * 2          # 2 nano-batches x 2 steps
         assert all(e["ms"] >= 0 for e in tr)
     plan.close()
+
+
+def test_step_profile_measures_the_rp_table_and_drives_plan_creation(tmp_path):
+    """nf_profile_step on the small batch through 2 layers: the JSON holds the
+    R -> P table (attention bytes/s per SM and GEMM rate kept, per nano-batch
+    count and SM count, all positive), every profiled plan with its measured
+    step time; it is registered, so plan creation without options returns the
+    fastest profiled plan, and forgetting it restores the built-in model."""
+    import json
+    shape, batch = wl.tiny_shape(), wl.tiny_batch()
+    path = str(tmp_path / "step.json")
+    _lib.profile_step(shape, batch, 2, path)
+    try:
+        d = json.load(open(path))
+        n = len(d["rp_sms"])
+        assert n > 0 and len(d["rp_n"]) == n and len(d["rp_gemm_factor"]) == n
+        assert all(v > 0 for v in d["rp_attn_bps_per_sm"]) and all(v > 0 for v in d["rp_gemm_factor"])
+        assert d["n_layers"] == 2 and d["batch_tokens"] == batch.n_tokens
+        assert len(d["run_ms"]) == 1 + 3 * 8 and all(t > 0 for t in d["run_ms"])
+        o, t = _lib.plan_search(shape, batch, None, _lib.device_sm_count(), n_layers=2)
+        i = min(range(len(d["run_ms"])), key=lambda k: d["run_ms"][k])
+        if d["run_n"][i] > 1 and d["run_ms"][i] <= 0.99 * d["run_ms"][0]:
+            assert o.n_attn == d["run_n"][i] and o.attn_sms == d["run_sms"][i]
+        assert t == pytest.approx(min(d["run_ms"][k] for k in range(len(d["run_ms"]))
+                                      if k == 0 or d["run_ms"][k] <= 0.99 * d["run_ms"][0]) * 1e3)
+    finally:
+        _lib.profile_use(shape, None)
