@@ -30,17 +30,11 @@ struct TracedRun {
 // that nf_plan_search reads (empty on invalid input).
 std::string fit_step_profile(const nf_model_shape* shape, const nf_batch_desc* batch, int num_sms,
                              int n_layers, const std::vector<TracedRun>& runs);
-// The token bounds of a step profile's n nano-batches of T tokens: equal
-// shares on the 128-token grid (any granularity below 1024 tokens).
-inline void profile_bounds(int T, int n, int32_t* b) {
-  const int grid = T >= 1024 ? 128 : 1;
-  b[0] = 0;
-  for (int i = 1; i < n; ++i) {
-    const int t = (T * i / n + grid / 2) / grid * grid;
-    b[i] = t > b[i - 1] ? t : b[i - 1] + 1;
-  }
-  b[n] = T;
-}
+// The attention nano-batch bounds the plan search generates for n nano-batches
+// of this batch (its attention cost split evenly, on the 128-token grid from
+// 1024 tokens): the plans a step profile measures.
+nf_status search_bounds(const nf_model_shape* shape, const nf_batch_desc* batch, int32_t num_sms,
+                        int n, int32_t* b);
 // The path of the profile registered for this shape (nf_profile_use or
 // nf_profile_step), or "".
 std::string registered_profile(const nf_model_shape* shape);

@@ -388,7 +388,8 @@ extern "C" nf_status nf_profile_step(const nf_model_shape* shape, const nf_batch
   cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking);
 
   // the plans: sequential, then two-stream plans of 2, 3 and 4 nano-batches with
-  // attention on 3/16 ... 10/16 of the SMs (token bounds on the 128 grid)
+  // attention on 3/16 ... 10/16 of the SMs, with the token bounds the plan
+  // search generates (attention cost split evenly on the 128-token grid)
   std::vector<nf_plan_opts> plans;
   {
     nf_plan_opts o{};
@@ -404,7 +405,7 @@ extern "C" nf_status nf_profile_step(const nf_model_shape* shape, const nf_batch
         nf_plan_opts p = o;
         p.executor = NF_EXEC_STREAMS;
         p.n_attn = p.n_ffn = n;
-        nf::profile_bounds(T, n, p.attn_bounds);
+        if (nf::search_bounds(shape, batch, sms, n, p.attn_bounds) != NF_OK) continue;
         for (int i = 0; i <= n; ++i) p.ffn_bounds[i] = p.attn_bounds[i];
         p.attn_sms = sms * k / 16;
         plans.push_back(p);

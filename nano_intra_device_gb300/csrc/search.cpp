@@ -366,11 +366,14 @@ nf_status build_model(const nf_model_shape* shape, const nf_batch_desc* batch,
   }
 
   // attention cost per row in seconds on the whole GPU: what nano-batch
-  // boundaries balance
+  // boundaries balance.  The built-in rates weigh bytes against FLOPs here, not
+  // a profile's, so that the boundaries depend on the batch alone and a step
+  // profile measures the very plans the search generates.
+  const Rates ref;
   m->prefix_cost.assign(T + 1, 0.0);
   for (int t = 0; t < T; ++t)
-    m->prefix_cost[t + 1] = m->prefix_cost[t] + m->row_kv_bytes[t] / m->r.hbm_bps +
-                            m->row_pf_flops[t] / (num_sms * m->r.attn_prefill_flops_per_sm);
+    m->prefix_cost[t + 1] = m->prefix_cost[t] + m->row_kv_bytes[t] / ref.hbm_bps +
+                            m->row_pf_flops[t] / (num_sms * ref.attn_prefill_flops_per_sm);
   return NF_OK;
 }
 
@@ -490,7 +493,7 @@ nf_status search(const nf_model_shape* shape, const nf_batch_desc* batch, const 
       if (bn > 1) {
         best.executor = NF_EXEC_STREAMS;
         best.n_attn = best.n_ffn = bn;
-        nf::profile_bounds(T, bn, best.attn_bounds);
+        balanced_bounds(m, T, bn, T >= 1024 ? 128 : 1, best.attn_bounds);
         for (int i = 0; i <= bn; ++i) best.ffn_bounds[i] = best.attn_bounds[i];
         best.attn_sms = bs;
       }
@@ -511,8 +514,9 @@ nf_status search(const nf_model_shape* shape, const nf_batch_desc* batch, const 
       o.executor = NF_EXEC_STREAMS;
       o.n_attn = n;
       balanced_bounds(m, T, n, grid, o.attn_bounds);
-      for (int nf_ : {n, 2}) {
-        if (nf_ == 2 && n != 4) continue;
+      const int ffn_counts[2] = {n, n == 4 ? 2 : 0};
+      for (int nf_ : ffn_counts) {
+        if (nf_ == 0) continue;
         o.n_ffn = nf_;
         if (nf_ == n) {
           for (int i = 0; i <= n; ++i) o.ffn_bounds[i] = o.attn_bounds[i];
@@ -598,6 +602,17 @@ nf_status predict(const nf_model_shape* shape, const nf_batch_desc* batch, const
 namespace nf {
 
 std::string registered_profile(const nf_model_shape* shape) { return profile_of(shape, nullptr); }
+
+nf_status search_bounds(const nf_model_shape* shape, const nf_batch_desc* batch, int32_t num_sms,
+                        int n, int32_t* b) {
+  if (!shape || !batch || !b || num_sms <= 0 || n < 1 || n > NF_MAX_NANO) return NF_ERR_INVALID_ARG;
+  Model m;
+  NF_MODEL_TRY(build_model(shape, batch, nullptr, num_sms, false, &m));
+  const int T = int(m.row_ctx.size());
+  if (T < n) return NF_ERR_INVALID_ARG;
+  balanced_bounds(m, T, n, T >= 1024 && T / 128 >= n ? 128 : 1, b);
+  return NF_OK;
+}
 
 namespace {
 

@@ -307,8 +307,20 @@ def test_search_picks_the_fastest_profiled_plan_of_the_same_batch(L, tmp_path):
     p.write_text(json.dumps(prof))
     o, t = _lib.plan_search(s8, b8, str(p), 152, n_layers=16)
     assert o.executor == _lib.NF_EXEC_STREAMS and o.n_attn == 2 and o.attn_sms == 66
-    assert list(o.attn_bounds[:3]) == [0, 1024, T] and list(o.ffn_bounds[:3]) == [0, 1024, T]
     assert t == pytest.approx(24.9e3, rel=1e-9)
+    # the bounds are those the model path generates for 2 nano-batches (the
+    # profile measured the search's own plans): a table that makes 2 nano-batches
+    # the only good choice there gives the same bounds
+    b = list(o.attn_bounds[:3])
+    assert b[0] == 0 and b[2] == T and b[1] % 128 == 0 and 0 < b[1] < T
+    assert list(o.ffn_bounds[:3]) == b
+    model = dict(prof, batch_tokens=-1, stream_sync_s=0.0, rp_n=[2, 2, 3, 3, 4, 4],
+                 rp_sms=[47, 95] * 3, rp_attn_bps_per_sm=[200e9] * 6,
+                 rp_gemm_factor=[1.0, 1.0, 0.2, 0.2, 0.2, 0.2])
+    pm = tmp_path / "m.json"
+    pm.write_text(json.dumps(model))
+    om, _ = _lib.plan_search(s8, b8, str(pm), 152, n_layers=16)
+    assert om.n_attn == 2 and list(om.attn_bounds[:3]) == b
     prof["run_ms"] = [26.3, 26.2, 26.1, 26.2]          # less than 1 % better: sequential
     p.write_text(json.dumps(prof))
     o, t = _lib.plan_search(s8, b8, str(p), 152, n_layers=16)
