@@ -340,7 +340,8 @@ nf_status build_model(const nf_model_shape* shape, const nf_batch_desc* batch,
   if (!load_rates(profile_json, &m->r)) return NF_ERR_INVALID_ARG;
   const int n_seq = batch->n_decode + batch->n_prefill;
   const double kv_tok = 2.0 * shape->n_kv_heads * shape->head_dim * 2;
-  // rows of a prefill tile (128 query vectors: 128 / GQA group rows)
+  // rows of a prefill tile (128 query vectors: 128 / GQA group rows), which
+  // read each page once
   const double tile_rows = 128.0 / std::max(1, shape->n_q_heads / std::max(1, shape->n_kv_heads));
   const int default_ctx = batch->max_pages_per_seq * shape->page_size / 2;
   for (int s = 0; s < n_seq; ++s) {

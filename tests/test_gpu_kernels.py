@@ -268,8 +268,8 @@ def test_attention_gqa_and_head_dims(grp, d, warps):
 
 @pytest.mark.parametrize("grp,d", [(1, 64), (2, 128), (4, 128), (8, 64), (8, 128)])
 def test_attention_prefill_tiles_cross_chunks_and_nano_batches(grp, d):
-    """Prefill chunks through the tiled causal kernel: chunks longer than a tile
-    (128 / grp rows), prefixes 0 to 513, a one-row chunk, and nano-batch
+    """Prefill chunks through the tiled causal kernel: chunks longer than a
+    tile (128 / grp rows), prefixes 0 to 513, a one-row chunk, and nano-batch
     boundaries that cut chunks; every row against the oracle."""
     shape = wl.Shape(hidden=512, n_q=2 * grp, n_kv=2, head_dim=d, ffn=512)
     b = wl.make_batch(shape, [5, 300], [150, 37, 1, 200], [0, 90, 7, 513], seed_bt=8)
