@@ -117,6 +117,16 @@ __global__ void __launch_bounds__(WR_THREADS, 1)
   const int n_tiles = args.n_tiles * args.m_tiles;  // weight tiles x token tiles
   const int nk = (args.K + WR_BK - 1) / WR_BK;
   const int kb0 = rank * nk / S, kb1 = (rank + 1) * nk / S;
+  // A tile walks its K range from an offset that spreads the tiles evenly over
+  // it, so that the CTAs, which start together, do not all read the same
+  // 128-byte column of the weight rows (rows 2K bytes apart) at once; the sum
+  // order is a function of the tile alone.
+  const int klen = kb1 - kb0;
+  auto kb_at = [&](int wt, int i) {
+    const int rot = static_cast<int>((static_cast<long long>(wt) * klen) / args.n_tiles) % klen;
+    const int j = i + rot;
+    return kb0 + (j >= klen ? j - klen : j);
+  };
   const uint64_t tmo = args.timeout_ns;
   // QKV: a tile holds 256 / d heads; its first A operand is dimensions
   // [0, d/2) of each, its second [d/2, d)
@@ -174,9 +184,10 @@ __global__ void __launch_bounds__(WR_THREADS, 1)
         }
       };
       // the first ring of weights does not depend on the kernel ahead
-      const int pre = first < n_tiles ? min(STAGES, kb1 - kb0) : 0;
+      const int pre = first < n_tiles ? min(STAGES, klen) : 0;
       for (int i = 0; i < pre; ++i)
-        load_w(smem + i * Cfg::STAGE, &tail->full[i], kb0 + i, first / args.m_tiles);
+        load_w(smem + i * Cfg::STAGE, &tail->full[i], kb_at(first / args.m_tiles, i),
+               first / args.m_tiles);
       pdl_wait();
       uint32_t st = 0, ph = 0;
       uint32_t issued_mask = 0, last_ph[WR_MAX_STAGES] = {};
@@ -184,14 +195,15 @@ __global__ void __launch_bounds__(WR_THREADS, 1)
       for (int tile = first; tile < n_tiles && ok; tile += stride) {
         const int wt = tile / args.m_tiles, tt = tile % args.m_tiles;
         const int x_row = args.m_begin + tt * TOK;
-        for (int kb = kb0; kb < kb1; ++kb) {
+        for (int i = 0; i < klen; ++i) {
+          const int kb = kb_at(wt, i);
           if (!mbar_wait(&tail->empty[st], ph ^ 1, tmo, abort_flag)) {
             ok = false;
             break;
           }
           uint8_t* sa = smem + st * Cfg::STAGE;
           uint64_t* bar = &tail->full[st];
-          if (tile != first || kb - kb0 >= pre) load_w(sa, bar, kb, wt);
+          if (tile != first || i >= pre) load_w(sa, bar, kb, wt);
           tma_load_2d(sa + NA * Cfg::W_BYTES, &tmX, bar, kb * WR_BK, x_row);
           issued_mask |= 1u << st;
           last_ph[st] = ph;
@@ -222,7 +234,7 @@ __global__ void __launch_bounds__(WR_THREADS, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * Cfg::ACC;
-        for (int kb = kb0; kb < kb1; ++kb) {
+        for (int i = 0; i < klen; ++i) {
           if (!mbar_wait(&tail->full[st], ph, tmo, abort_flag)) {
             ok = false;
             break;
@@ -234,7 +246,7 @@ __global__ void __launch_bounds__(WR_THREADS, 1)
           const uint64_t xd = desc_sw128_kmajor(sa + NA * Cfg::W_BYTES);
 #pragma unroll
           for (int k = 0; k < WR_BK / 16; ++k) {
-            const uint32_t accum = (kb != kb0) || (k != 0);
+            const uint32_t accum = (i != 0) || (k != 0);
             tc_mma_bf16(d_tmem, a0 + 2 * k, xd + 2 * k, IDESC, accum);
             if (NA == 2) tc_mma_bf16(d_tmem + TOK, a1 + 2 * k, xd + 2 * k, IDESC, accum);
           }
