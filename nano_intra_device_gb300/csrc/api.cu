@@ -174,7 +174,8 @@ struct nf_plan_s {
   bool attn_mma = false;
   struct PoolMaps {
     const void *k, *v;
-    CUtensorMap tk, tv;
+    CUtensorMap tk, tv;    // half-row boxes (prefill kernel)
+    CUtensorMap dk, dv;    // whole-page boxes (decode kernel)
   };
   std::vector<PoolMaps> pcache;
   // prefill-chunk attention: tiles of rows (first, end, sequence, 0) of every
@@ -860,7 +861,11 @@ nf_status run_attention(nf_plan p, int seg, const void* q, const void* kp, const
       c.v = vp;
       const nf_model_shape& sh = p->shape;
       if (!nf::make_pool_tmap(&c.tk, kp, p->num_pages, sh.n_kv_heads, sh.page_size, sh.head_dim) ||
-          !nf::make_pool_tmap(&c.tv, vp, p->num_pages, sh.n_kv_heads, sh.page_size, sh.head_dim))
+          !nf::make_pool_tmap(&c.tv, vp, p->num_pages, sh.n_kv_heads, sh.page_size, sh.head_dim) ||
+          !nf::make_pool_tmap_pages(&c.dk, kp, p->num_pages, sh.n_kv_heads, sh.page_size,
+                                    sh.head_dim) ||
+          !nf::make_pool_tmap_pages(&c.dv, vp, p->num_pages, sh.n_kv_heads, sh.page_size,
+                                    sh.head_dim))
         return fail(NF_ERR_INVALID_ARG, "KV pool tensor maps: pools must be 16-byte aligned");
       if (p->pcache.size() >= 4096) p->pcache.clear();
       p->pcache.push_back(c);
@@ -871,7 +876,7 @@ nf_status run_attention(nf_plan p, int seg, const void* q, const void* kp, const
     const int n_pf = a.prefill_elsewhere ? p->pf_seg[seg + 1] - p->pf_seg[seg] : 0;
     if (n_pf > 0)
       NF_CUDA(nf::launch_attention_prefill(a, pm->tk, pm->tv, p->pf_tiles + p->pf_seg[seg], n_pf, st));
-    NF_CUDA(nf::launch_attention_mma(a, pm->tk, pm->tv, grid, n_pf > 0, st));
+    NF_CUDA(nf::launch_attention_mma(a, pm->dk, pm->dv, grid, n_pf > 0, st));
   }
   return NF_OK;
 }

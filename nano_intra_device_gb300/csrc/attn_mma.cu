@@ -148,11 +148,13 @@ __global__ void __launch_bounds__(WARPS * 32, WARPS == AMMA_SHARE_WARPS ? 4 : 1)
       uint8_t* sl = ring + st * SLOT;
       const int y = (page * n_kv + g) * P;  // first pool row of the (page, KV head)
       mbar_arrive_expect_tx(&bar[st], SLOT);
-#pragma unroll
-      for (int b = 0; b < NCH; ++b) tma_load_2d_hint(sl + b * BOX, &tmK, &bar[st], b * 64, y, policy);
-#pragma unroll
-      for (int b = 0; b < NCH; ++b)
-        tma_load_2d_hint(sl + BLK + b * BOX, &tmV, &bar[st], b * 64, y, policy);
+      if (NCH == 2) {  // one box per (page, KV head): both 64-column halves
+        tma_load_3d_hint(sl, &tmK, &bar[st], 0, y, 0, policy);
+        tma_load_3d_hint(sl + BLK, &tmV, &bar[st], 0, y, 0, policy);
+      } else {
+        tma_load_2d_hint(sl, &tmK, &bar[st], 0, y, policy);
+        tma_load_2d_hint(sl + BLK, &tmV, &bar[st], 0, y, policy);
+      }
     };
     int issued = 0;
     {
@@ -466,6 +468,14 @@ bool make_pool_tmap(CUtensorMap* map, const void* pool, int num_pages, int n_kv,
                     int head_dim) {
   return make_tmap_bf16(map, pool, static_cast<uint64_t>(num_pages) * n_kv * page_size,
                         static_cast<uint64_t>(head_dim), static_cast<uint32_t>(page_size));
+}
+
+bool make_pool_tmap_pages(CUtensorMap* map, const void* pool, int num_pages, int n_kv,
+                          int page_size, int head_dim) {
+  if (head_dim != 128)
+    return make_pool_tmap(map, pool, num_pages, n_kv, page_size, head_dim);
+  return make_tmap_bf16_rows128(map, pool, static_cast<uint64_t>(num_pages) * n_kv * page_size,
+                                static_cast<uint32_t>(page_size));
 }
 
 cudaError_t launch_attention_mma(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,

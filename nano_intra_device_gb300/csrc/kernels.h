@@ -177,12 +177,20 @@ __host__ __device__ constexpr int partial_rec_floats(int grp, int head_dim) {
   return grp * head_dim + ((2 * grp + 3) / 4) * 4;
 }
 // Tensor-core variant (mma.sync m16n8k16, bf16 operands, fp32 accumulators) of
-// the same operation with the same records; K and V pages arrive by 2-D TMA
+// the same operation with the same records; K and V pages arrive by TMA
 // copies through maps over the pools viewed as [num_pages * n_kv * 16, d]
-// (make_pool_tmap).  Supported: page 16, d 64 or 128, GQA group 1, 2, 4 or 8.
+// (make_pool_tmap_pages).  Supported: page 16, d 64 or 128, GQA group 1, 2, 4 or 8.
 bool attention_mma_supported(int n_q, int n_kv, int head_dim, int page_size, int num_pages);
 bool make_pool_tmap(CUtensorMap* map, const void* pool, int num_pages, int n_kv, int page_size,
                     int head_dim);
+// The decode kernel's map over a pool: for d = 128 one 3-D box fetches a whole
+// (page, KV head) block of K or V (both 64-column halves, the same shared
+// layout as two 2-D boxes); for d = 64 the 2-D map above.
+bool make_pool_tmap_pages(CUtensorMap* map, const void* pool, int num_pages, int n_kv,
+                          int page_size, int head_dim);
+// A 3-D map over rows of 128 bf16: box = box_rows rows, landing as two
+// 128-byte-swizzled 64-column halves one after the other.
+bool make_tmap_bf16_rows128(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows);
 // programmatic: launch as a programmatic dependent of the kernel ahead (the
 // prefill kernel of the same nano-batch); the grid waits for it before it ends.
 cudaError_t launch_attention_mma(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -239,8 +239,10 @@ extern "C" nf_status nf_attention_noalloc(const nf_model_shape* shape, const nf_
   a.timeout_ns = 2000000000ull;
   // tensor maps over the pools: host-side descriptors, passed by value
   CUtensorMap tk, tv;
-  if (!nf::make_pool_tmap(&tk, k_pool, batch->num_pages, s.n_kv_heads, s.page_size, s.head_dim) ||
-      !nf::make_pool_tmap(&tv, v_pool, batch->num_pages, s.n_kv_heads, s.page_size, s.head_dim))
+  if (!nf::make_pool_tmap_pages(&tk, k_pool, batch->num_pages, s.n_kv_heads, s.page_size,
+                                s.head_dim) ||
+      !nf::make_pool_tmap_pages(&tv, v_pool, batch->num_pages, s.n_kv_heads, s.page_size,
+                                s.head_dim))
     return nf::set_last_error(NF_ERR_INVALID_ARG, "nf_attention_noalloc: KV pool tensor maps failed");
   if (nf::launch_attention_mma(a, tk, tv, sms, false, cs) != cudaSuccess)
     return nf::set_last_error(NF_ERR_CUDA, "nf_attention_noalloc: attention launch failed");
