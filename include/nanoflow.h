@@ -503,8 +503,9 @@ nf_status nf_profile(const nf_model_shape* shape, int32_t max_tokens, int32_t me
  * rate and attention bandwidth alone; per nano-batch count and attention SM
  * count the attention's bytes/s per SM and the share of its rate a GEMM kept
  * while the two overlapped; the cost of a cross-stream dependency and one
- * factor on the GEMM shares, from the untraced step times); write them with
- * each plan's measured
+ * factor on the GEMM shares, from the untraced step times; the sequential plan
+ * and the three fastest overlapped plans are timed again, interleaved over
+ * three rounds, and keep the median); write them with each plan's measured
  * and predicted step time to out_json, and register the file for this shape
  * (nf_profile_use), so that plan creation without options and the searches
  * below use it.  Allocates its own buffers (weights of one layer, one K/V pool

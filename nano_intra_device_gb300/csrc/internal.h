@@ -31,8 +31,8 @@ struct TracedRun {
 std::string fit_step_profile(const nf_model_shape* shape, const nf_batch_desc* batch, int num_sms,
                              int n_layers, const std::vector<TracedRun>& runs);
 // The attention nano-batch bounds the plan search generates for n nano-batches
-// of this batch (its attention cost split evenly, on the 128-token grid from
-// 1024 tokens): the plans a step profile measures.
+// of this batch (equal token shares, on the 128-token grid from 1024 tokens):
+// the plans a step profile measures.
 nf_status search_bounds(const nf_model_shape* shape, const nf_batch_desc* batch, int32_t num_sms,
                         int n, int32_t* b);
 // The path of the profile registered for this shape (nf_profile_use or

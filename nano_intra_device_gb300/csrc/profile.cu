@@ -389,7 +389,7 @@ extern "C" nf_status nf_profile_step(const nf_model_shape* shape, const nf_batch
 
   // the plans: sequential, then two-stream plans of 2, 3 and 4 nano-batches with
   // attention on 3/16 ... 10/16 of the SMs, with the token bounds the plan
-  // search generates (attention cost split evenly on the 128-token grid)
+  // search generates (equal shares on the 128-token grid)
   std::vector<nf_plan_opts> plans;
   {
     nf_plan_opts o{};
@@ -452,6 +452,50 @@ extern "C" nf_status nf_profile_step(const nf_model_shape* shape, const nf_batch
       break;
     }
     runs.push_back(std::move(run));
+  }
+  // Re-time the sequential plan and the three fastest overlapped ones,
+  // interleaved over rounds: the pick between plans within a few per cent of
+  // one another should not rest on one measurement each (the clocks move under
+  // the power cap).  Each keeps the median of its measurements.
+  if (result == NF_OK && runs.size() > 1) {
+    std::vector<int> idx;
+    for (size_t i = 0; i < runs.size(); ++i)
+      if (runs[i].opts.executor == NF_EXEC_SEQUENTIAL) idx.push_back(static_cast<int>(i));
+    std::vector<int> order;
+    for (size_t i = 0; i < runs.size(); ++i)
+      if (runs[i].opts.executor != NF_EXEC_SEQUENTIAL) order.push_back(static_cast<int>(i));
+    std::sort(order.begin(), order.end(), [&](int a, int b) { return runs[a].step_ms < runs[b].step_ms; });
+    for (size_t i = 0; i < order.size() && i < 3; ++i) idx.push_back(order[i]);
+    std::vector<nf_plan> pl(idx.size(), nullptr);
+    std::vector<std::vector<double>> t(idx.size());
+    for (size_t k = 0; k < idx.size() && result == NF_OK; ++k) {
+      result = nf_plan_create(shape, batch, &runs[idx[k]].opts, &pl[k]);
+      t[k].push_back(runs[idx[k]].step_ms);
+    }
+    for (int round = 0; round < 3 && result == NF_OK; ++round) {
+      for (size_t k = 0; k < idx.size() && result == NF_OK; ++k) {
+        nf_plan plan = pl[k];
+        auto step = [&]() {
+          return L == 1 ? nf_layer_step(plan, &w, x, kp, vp, bt, sl, y, st)
+                        : nf_layers_step(plan, lw.data(), L, x, kps.data(), vps.data(), bt, sl, y, st);
+        };
+        nf_status ss = step();
+        cudaEventRecord(e0, st);
+        for (int r = 0; r < 2 && ss == NF_OK; ++r) ss = step();
+        cudaEventRecord(e1, st);
+        float ms = 0;
+        if (ss == NF_OK && cudaEventSynchronize(e1) == cudaSuccess) cudaEventElapsedTime(&ms, e0, e1);
+        if (ss == NF_OK) ss = nf_plan_poll(plan, 1);
+        if (ss != NF_OK) result = ss;
+        t[k].push_back(ms / 2.0);
+      }
+    }
+    for (size_t k = 0; k < idx.size(); ++k) {
+      if (pl[k]) nf_plan_destroy(pl[k]);
+      std::vector<double> v = t[k];
+      std::sort(v.begin(), v.end());
+      if (result == NF_OK && !v.empty()) runs[idx[k]].step_ms = v[v.size() / 2];
+    }
   }
   cudaEventDestroy(e0);
   cudaEventDestroy(e1);
