@@ -289,6 +289,22 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     for (int u = blockIdx.x; u < total_tiles; u += gridDim.x) {
       const GemmTile x = decode(u);
       const int t = x.t, sp = x.sp;
+      // Residual epilogue: the residual's 32 columns of a chunk, loaded one
+      // chunk ahead; the first chunk's before the wait for the accumulator, so
+      // that its latency hides under the tile's MMAs.
+      uint4 r_next[4];
+      auto load_r = [&](int c) {
+        const int m_ = x.m0 + (warp & 3) * 32 + lane;
+        const int n_ = x.tn * BN + c * 32;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          r_next[i] = make_uint4(0u, 0u, 0u, 0u);
+          if (m_ < x.m_lim && n_ + 8 * i + 8 <= args.N)
+            r_next[i] = __ldg(reinterpret_cast<const uint4*>(args.R + static_cast<size_t>(m_) * args.ldr +
+                                                            n_ + 8 * i));
+        }
+      };
+      if (EPI == EPI_RESID) load_r(0);
       // the wait result must be warp-uniform: tcgen05.ld below is .sync.aligned
       const bool got = __all_sync(0xffffffffu, mbar_wait(&tail->tfull[acc], aph, tmo, abort_flag));
       if (!got) {
@@ -390,15 +406,20 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         __nv_bfloat16* crow = args.C + static_cast<size_t>(m) * args.ldc;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
+          uint4 r_cur[4];
+          if (EPI == EPI_RESID) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) r_cur[i] = r_next[i];
+            if (c + 1 < BN / 32) load_r(c + 1);
+          }
           fetch32(c * 32, v);
           const int n = tn * BN + c * 32;
           if (row_ok && n < args.N) {
             if (EPI == EPI_RESID) {
-              const __nv_bfloat16* rrow = args.R + static_cast<size_t>(m) * args.ldr + n;
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
                 if (n + 8 * i + 8 <= args.N) {
-                  uint4 u = *reinterpret_cast<const uint4*>(rrow + 8 * i);
+                  const uint4 u = r_cur[i];
                   v[8 * i + 0] += bf16lo(u.x); v[8 * i + 1] += bf16hi(u.x);
                   v[8 * i + 2] += bf16lo(u.y); v[8 * i + 3] += bf16hi(u.y);
                   v[8 * i + 4] += bf16lo(u.z); v[8 * i + 5] += bf16hi(u.z);
