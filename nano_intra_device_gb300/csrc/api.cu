@@ -174,7 +174,7 @@ struct nf_plan_s {
   bool attn_mma = false;
   struct PoolMaps {
     const void *k, *v;
-    CUtensorMap tk, tv;    // half-row boxes (prefill kernel)
+    CUtensorMap tk, tv;    // 8-row-group boxes (prefill kernel)
     CUtensorMap dk, dv;    // whole-page boxes (decode kernel)
   };
   std::vector<PoolMaps> pcache;
@@ -860,8 +860,10 @@ nf_status run_attention(nf_plan p, int seg, const void* q, const void* kp, const
       c.k = kp;
       c.v = vp;
       const nf_model_shape& sh = p->shape;
-      if (!nf::make_pool_tmap(&c.tk, kp, p->num_pages, sh.n_kv_heads, sh.page_size, sh.head_dim) ||
-          !nf::make_pool_tmap(&c.tv, vp, p->num_pages, sh.n_kv_heads, sh.page_size, sh.head_dim) ||
+      if (!nf::make_pool_tmap_groups(&c.tk, kp, p->num_pages, sh.n_kv_heads, sh.page_size,
+                                     sh.head_dim) ||
+          !nf::make_pool_tmap_groups(&c.tv, vp, p->num_pages, sh.n_kv_heads, sh.page_size,
+                                     sh.head_dim) ||
           !nf::make_pool_tmap_pages(&c.dk, kp, p->num_pages, sh.n_kv_heads, sh.page_size,
                                     sh.head_dim) ||
           !nf::make_pool_tmap_pages(&c.dv, vp, p->num_pages, sh.n_kv_heads, sh.page_size,

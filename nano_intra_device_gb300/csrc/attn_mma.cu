@@ -478,6 +478,13 @@ bool make_pool_tmap_pages(CUtensorMap* map, const void* pool, int num_pages, int
                                 static_cast<uint32_t>(page_size));
 }
 
+bool make_pool_tmap_groups(CUtensorMap* map, const void* pool, int num_pages, int n_kv,
+                           int page_size, int head_dim) {
+  if (head_dim != 128)
+    return make_pool_tmap(map, pool, num_pages, n_kv, page_size, head_dim);
+  return make_tmap_bf16_groups128(map, pool, static_cast<uint64_t>(num_pages) * n_kv * page_size);
+}
+
 cudaError_t launch_attention_mma(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
                                  int grid, bool programmatic, cudaStream_t stream) {
   if (grid <= 0 || !attention_mma_supported(a.n_q, a.n_kv, a.head_dim, a.page_size, a.num_pages))

@@ -11,8 +11,9 @@
 //    heads (vector v is row v / GRP of the tile, query head v % GRP of the
 //    group), one per tensor-memory lane;
 //  * two producer warps stream key blocks of 128 positions (8 pages) of K and
-//    of V of the KV head by 2-D TMA, into a three-stage K ring and a two-stage
-//    V ring; warp 1 issues the MMAs from one thread; eight softmax warps own
+//    of V of the KV head by TMA (one box per page: at d = 128 a 4-D box that
+//    lands as [8-position group][64-column half][8 positions], 1024-byte atoms
+//    of the 128-byte swizzle), into a three-stage K ring and a two-stage V ring; warp 1 issues the MMAs from one thread; eight softmax warps own
 //    half a vector (lane) each: 64 positions of every block and d / 2 columns
 //    of O; they write Q into shared memory, run the online softmax and the
 //    epilogue;
@@ -68,7 +69,9 @@ template <int NCH>
 struct TpLayout {
   static constexpr int D = NCH * 64;
   static constexpr int Q_BYTES = NCH * TP_REGION;   // [d/64][128 vectors][128 B]
-  static constexpr int KV_BYTES = NCH * TP_REGION;  // [d/64][128 positions][128 B]
+  // per stage: 16 groups of 8 positions, each [d/64][8 positions][128 B]
+  static constexpr int KV_BYTES = NCH * TP_REGION;
+  static constexpr int KV_GROUP = NCH * 1024;      // bytes between 8-position groups
   static constexpr int P_BYTES = 2 * TP_REGION;     // [keys/64][128 vectors][128 B]
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = Q_OFF + Q_BYTES;
@@ -199,11 +202,14 @@ __global__ void __launch_bounds__(TP_THREADS, 1)
         if (good) {
           uint8_t* dst = ring + s * Lay::KV_BYTES;
           mbar_arrive_expect_tx(&full[s], Lay::KV_BYTES);
+          // one box per (page, KV head): [group][half][8 positions][64 columns]
 #pragma unroll
-          for (int b = 0; b < NCH; ++b)
-#pragma unroll
-            for (int p = 0; p < TP_PAGES; ++p)
-              tma_load_2d(dst + b * TP_REGION + p * AMMA_P * 128, map, &full[s], b * 64, rows[p]);
+          for (int p = 0; p < TP_PAGES; ++p) {
+            if (NCH == 2)
+              tma_load_4d(dst + p * 2 * Lay::KV_GROUP, map, &full[s], 0, 0, 0, rows[p] / 8);
+            else
+              tma_load_2d(dst + p * 2 * Lay::KV_GROUP, map, &full[s], 0, rows[p]);
+          }
           out[s] = j;
         }
       }
@@ -234,8 +240,10 @@ __global__ void __launch_bounds__(TP_THREADS, 1)
 #pragma unroll
         for (int kk = 0; kk < TP_N / 16; ++kk) {
           // A = P: K-major, keys 16 kk .. in region kk / 4; B = V: MN-major,
-          // positions 16 kk .. = two 8-position atoms from byte 2048 kk
-          const uint64_t bdesc = desc_sw128_mnmajor(v_addr + kk * 2048, TP_REGION, 1024);
+          // positions 16 kk .. = two 8-position groups; the 64-column halves of a
+          // group 1024 bytes apart
+          const uint64_t bdesc =
+              desc_sw128_mnmajor(v_addr + kk * 2 * Lay::KV_GROUP, 1024, Lay::KV_GROUP);
           const uint64_t adesc = desc_sw128_kmajor(p_addr + (kk >> 2) * TP_REGION) + 2 * (kk & 3);
           tc_mma_bf16(o_tmem, adesc, bdesc, IDESC_PV, (i > 0) || (kk > 0));
         }
@@ -254,7 +262,8 @@ __global__ void __launch_bounds__(TP_THREADS, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t adesc = desc_sw128_kmajor(q_addr + (kk >> 2) * TP_REGION) + 2 * (kk & 3);
-          const uint64_t bdesc = desc_sw128_kmajor(k_addr + (kk >> 2) * TP_REGION) + 2 * (kk & 3);
+          const uint64_t bdesc =
+              desc_sw128_kmajor_sbo(k_addr + (kk >> 2) * 1024, Lay::KV_GROUP) + 2 * (kk & 3);
           tc_mma_bf16(tmem + s * TP_N, adesc, bdesc, IDESC_S, kk > 0);
         }
         any = true;
@@ -416,7 +425,8 @@ __global__ void __launch_bounds__(TP_THREADS, 1)
           break;
         }
         if (half < NCH && j * TP_N + r > last_pos) {
-          const uint32_t vrow = sbase + Lay::V_OFF + vs * Lay::KV_BYTES + half * TP_REGION + r * 128;
+          const uint32_t vrow = sbase + Lay::V_OFF + vs * Lay::KV_BYTES + (r >> 3) * Lay::KV_GROUP +
+                                half * 1024 + (r & 7) * 128;
 #pragma unroll
           for (int c = 0; c < 8; ++c) st_shared_v4(vrow + c * 16, make_uint4(0, 0, 0, 0));
         }

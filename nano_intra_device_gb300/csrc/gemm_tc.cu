@@ -637,6 +637,24 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
   return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_bf16_groups128(CUtensorMap* map, const void* base, uint64_t rows) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return false;
+  if ((reinterpret_cast<uintptr_t>(base) & 15) || rows == 0 || rows % 16) return false;
+  // dims (column within a half, row within an 8-row group, half, group): a box
+  // of two groups lands as [group][half][8 rows][64 columns], each 8 x 64 block
+  // a 1024-byte atom of the 128-byte swizzle
+  cuuint64_t dims[4] = {64, 8, 2, rows / 8};
+  cuuint64_t strides[3] = {256, 128, 2048};
+  cuuint32_t box[4] = {64, 8, 2, 2};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool make_tmap_bf16_rows128(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows) {
   EncodeTiledFn fn = get_encode_fn();
   if (!fn) return false;

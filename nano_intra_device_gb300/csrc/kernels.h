@@ -188,6 +188,15 @@ bool make_pool_tmap(CUtensorMap* map, const void* pool, int num_pages, int n_kv,
 // layout as two 2-D boxes); for d = 64 the 2-D map above.
 bool make_pool_tmap_pages(CUtensorMap* map, const void* pool, int num_pages, int n_kv,
                           int page_size, int head_dim);
+// The prefill kernel's map over a pool: for d = 128 one 4-D box fetches a
+// (page, KV head) block of K or V as [8-row group][64-column half][8 rows]
+// (1024-byte atoms of the 128-byte swizzle, groups 2048 bytes apart); for
+// d = 64 the 2-D map above.
+bool make_pool_tmap_groups(CUtensorMap* map, const void* pool, int num_pages, int n_kv,
+                           int page_size, int head_dim);
+// A 4-D map over rows of 128 bf16 (rows a multiple of 16): box = 16 rows as
+// [8-row group][64-column half][8 rows][64 columns].
+bool make_tmap_bf16_groups128(CUtensorMap* map, const void* base, uint64_t rows);
 // A 3-D map over rows of 128 bf16: box = box_rows rows, landing as two
 // 128-byte-swizzled 64-column halves one after the other.
 bool make_tmap_bf16_rows128(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows);
