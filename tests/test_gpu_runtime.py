@@ -56,6 +56,56 @@ def test_plan_follows_a_smaller_batch():
     plan.close()
 
 
+def test_set_batch_calls_queued_behind_a_long_step():
+    """The host runs three nf_plan_set_batch calls ahead of the stream (a long
+    busy kernel holds it): each batch's staged tables are still the ones its
+    own step reads, so every step equals that batch run alone on a fresh plan,
+    bit for bit."""
+    shape = wl.tiny_shape()
+    batches = [wl.make_batch(shape, [17, 33, 48, 64, 20, 9], [32, 12], None, seed_bt=3, max_pages=8),
+               wl.make_batch(shape, [5, 40], [7], None, seed_bt=4, max_pages=8),
+               wl.make_batch(shape, [9, 9, 30], [20], None, seed_bt=5, max_pages=8)]
+    for b in batches[1:]:
+        b.num_pages = batches[0].num_pages  # one pool for all
+    T = batches[0].n_tokens
+    w = wl.make_weights(shape, seed=5, gain_std=0.1)
+    wd = {k: v.to(DEV) for k, v in w.items()}
+    inputs = []
+    for i, b in enumerate(batches):
+        kp, vp = wl.make_pools(shape, b, DEV, seed=20 + i)
+        x = wl.make_x(shape, b.n_tokens, seed=30 + i).to(DEV)
+        inputs.append((x, kp, vp, torch.from_numpy(b.block_table).to(DEV),
+                       torch.from_numpy(b.seq_lens).to(DEV)))
+
+    def opts_for(b):
+        return _lib.make_opts(b.n_tokens, [0, b.n_tokens // 2, b.n_tokens],
+                              executor=_lib.NF_EXEC_STREAMS, attn_sms=24, kv_chunk=32)
+
+    alone = []
+    for b, (x, kp, vp, bt, sl) in zip(batches, inputs):
+        plan = _lib.Plan(shape, b, opts_for(b))
+        kq, vq = kp.clone(), vp.clone()
+        y = torch.empty(b.n_tokens, shape.hidden, dtype=torch.bfloat16, device=DEV)
+        _lib.layer_step(plan, wd, x, kq, vq, bt, sl, y)
+        plan.poll(wait=True)
+        plan.close()
+        alone.append(y)
+    plan = _lib.Plan(shape, batches[0], opts_for(batches[0]))
+    ys, pools = [], [(kp.clone(), vp.clone()) for (_, kp, vp, _, _) in inputs]
+    torch.cuda.synchronize()
+    torch.cuda._sleep(200_000_000)  # ~0.1 s of spinning ahead of every step below
+    for b, (x, _, _, bt, sl), (kq, vq) in zip(batches, inputs, pools):
+        plan.set_batch(b, opts_for(b))
+        y = torch.empty(b.n_tokens, shape.hidden, dtype=torch.bfloat16, device=DEV)
+        _lib.layer_step(plan, wd, x, kq, vq, bt, sl, y)
+        ys.append(y)
+    plan.poll(wait=True)
+    plan.close()
+    assert T == max(b.n_tokens for b in batches)
+    for i, (y, ya) in enumerate(zip(ys, alone)):
+        assert torch.equal(y, ya), f"batch {i} read another batch's staged tables"
+
+
 def _successor_model(shape, n_layers, vocab):
     g = torch.Generator().manual_seed(1)
     H = shape.hidden
