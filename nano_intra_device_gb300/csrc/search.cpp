@@ -418,10 +418,11 @@ nf_status search(const nf_model_shape* shape, const nf_batch_desc* batch, const 
   const int n_seq = batch->n_decode + batch->n_prefill;
 
   // Split-KV piece length: the longest that still gives the resident
-  // attention warps about one and a half pieces each (load balance), so that a
+  // attention warps about one piece each (9 pieces for 10 warps), so that a
   // small decode batch is not left to a few long pieces while most warps idle;
-  // shorter pieces than that cost more in merges than they gain (measured on
-  // 32-layer stacks at 64 and 256 decode requests).
+  // shorter pieces cost more in piece setup and merges than they gain (the
+  // 32-layer stacks at 64, 256 and 1024 decode requests: 512, 1024 and 1024
+  // positions, each the fastest of 256 ... 1024).
   int kv_chunk = 128;
   {
     const double warps = 8.0 * num_sms;
@@ -435,7 +436,7 @@ nf_status search(const nf_model_shape* shape, const nf_batch_desc* batch, const 
           pieces += std::ceil(ctx / cand);
         }
       }
-      if (pieces * shape->n_kv_heads >= 1.5 * warps) {
+      if (pieces * shape->n_kv_heads >= 0.9 * warps) {
         kv_chunk = cand;
         break;
       }
