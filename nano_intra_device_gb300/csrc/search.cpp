@@ -418,29 +418,32 @@ nf_status search(const nf_model_shape* shape, const nf_batch_desc* batch, const 
   const int n_seq = batch->n_decode + batch->n_prefill;
 
   // Split-KV piece length: the longest that still gives the resident
-  // attention warps about one piece each (9 pieces for 10 warps), so that a
-  // small decode batch is not left to a few long pieces while most warps idle;
-  // shorter pieces cost more in piece setup and merges than they gain (the
-  // 32-layer stacks at 64, 256 and 1024 decode requests: 512, 1024 and 1024
-  // positions, each the fastest of 256 ... 1024).
+  // attention warps about one and a half pieces each, so that a small decode
+  // batch is not left to a few long pieces while most warps idle; but not
+  // below 512 positions while those still give the warps about one piece each
+  // (4 for 5 warps): shorter pieces cost more in piece setup and merges than
+  // they gain.  Measured on the 32-layer stacks at 64, 128, 256 and 1024
+  // decode requests: 512, 512, 1024 and 1024 positions, each the fastest of
+  // 256 ... 1024.
   int kv_chunk = 128;
   {
     const double warps = 8.0 * num_sms;
-    for (int cand : {1024, 512, 256, 128}) {
+    auto pieces_of = [&](int cand) {
       double pieces = 0;
       int t = 0;
       for (int s = 0; s < n_seq; ++s) {
         const int q = s < batch->n_decode ? 1 : batch->prefill_q_lens[s - batch->n_decode];
-        for (int i = 0; i < q; ++i, ++t) {
-          const double ctx = m.row_ctx[t];
-          pieces += std::ceil(ctx / cand);
-        }
+        for (int i = 0; i < q; ++i, ++t) pieces += std::ceil(m.row_ctx[t] / cand);
       }
-      if (pieces * shape->n_kv_heads >= 0.9 * warps) {
+      return pieces * shape->n_kv_heads;
+    };
+    for (int cand : {1024, 512, 256, 128}) {
+      if (pieces_of(cand) >= 1.5 * warps) {
         kv_chunk = cand;
         break;
       }
     }
+    if (kv_chunk < 512 && pieces_of(512) >= 0.8 * warps) kv_chunk = 512;
   }
   nf_plan_opts best{};
   std::memset(&best, 0, sizeof(best));
