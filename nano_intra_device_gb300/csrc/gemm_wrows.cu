@@ -81,14 +81,6 @@ struct WrTail {
 };
 static_assert(sizeof(WrTail) <= WR_TAIL, "barrier block exceeds its reservation");
 
-__device__ __forceinline__ void wr_tmem_load32(uint32_t taddr, float* v) {
-  uint32_t r[32];
-  tc_ld_32x32b_x32(taddr, r);
-  tc_wait_ld();
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
 __device__ __forceinline__ uint2 pack4_bf16(float a, float b, float c, float d) {
   return make_uint2(pack_bf16(a, b), pack_bf16(c, d));
 }
@@ -308,46 +300,97 @@ __global__ void __launch_bounds__(WR_THREADS, 1)
     // consecutive features of one token) eb, eb + 128, ..., eb + 128 (QB - 1)
     // of the share's nq quads, token c0 + e / 32 of the round and features
     // (e % 32) * 4 of the tile.  Global operands are fetched for the whole
-    // batch first and the partial tiles of all ranks next, so their latencies
-    // overlap instead of adding up quad by quad.
-    constexpr int QB = EPI == EPI_QKV ? 4 : 8;
-    auto reduce_batch = [&](int wt, int tr0, int c0, int eb, int nq) {
-      uint2 rr[QB];
+    // batch first and the partial tiles of RG ranks next, all loaded before
+    // any is added (a peer's shared memory is a round trip away, about a
+    // microsecond under load), so their latencies overlap instead of adding up
+    // rank by rank; this CTA's own copy is read from its shared memory.
+    constexpr int QB = 4, RG = EPI == EPI_QKV ? 3 : 4;
+    // QKV: the positions, cache slots and RoPE (cos, sin) of a batch's quads,
+    // which do not depend on the products (a tile's first batch is fetched
+    // before its products are ready)
+    struct QkvIn {
       int pos[QB], slot[QB];
+      float4 cs0[QB], cs1[QB];
+    };
+    auto qkv_fetch = [&](int wt, int tr0, int c0, int eb, int nq, QkvIn& q) {
+#pragma unroll
+      for (int i = 0; i < QB; ++i) {
+        const int e = eb + 128 * i;
+        q.pos[i] = 0;
+        q.slot[i] = -1;
+        q.cs0[i] = q.cs1[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (e < nq) {
+          const int t = tr0 + c0 + e / 32;
+          q.pos[i] = __ldg(args.tok_pos + t);
+          q.slot[i] = __ldg(args.tok_slot + t);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < QB; ++i) {  // RoPE (cos, sin) from the table
+        const int e = eb + 128 * i;
+        const int q4 = (e % 32) * 4, jh = q4 % half;
+        if (e < nq && wt * hp + q4 / half < args.n_q + args.n_kv && q.pos[i] < args.rope_positions) {
+          const float4* cs =
+              reinterpret_cast<const float4*>(args.rope_cs + static_cast<size_t>(q.pos[i]) * half + jh);
+          q.cs0[i] = __ldg(cs);
+          q.cs1[i] = __ldg(cs + 1);
+        }
+      }
+    };
+    auto reduce_batch = [&](int wt, int tr0, int c0, int eb, int nq, const QkvIn* pre) {
+      uint2 rr[QB];
+      QkvIn qi;
+      if (EPI == EPI_QKV) {
+        if (pre) qi = *pre;
+        else qkv_fetch(wt, tr0, c0, eb, nq, qi);
+      }
 #pragma unroll
       for (int i = 0; i < QB; ++i) {
         const int e = eb + 128 * i;
         rr[i] = make_uint2(0u, 0u);
-        pos[i] = 0;
-        slot[i] = -1;
         if (e < nq) {
           const int t = tr0 + c0 + e / 32, q4 = (e % 32) * 4;
           if (EPI == EPI_RESID && wt * WR_BM + q4 < args.N)
             rr[i] = __ldg(reinterpret_cast<const uint2*>(args.R + static_cast<size_t>(t) * args.ldr +
                                                          wt * WR_BM + q4));
-          if (EPI == EPI_QKV) {
-            pos[i] = __ldg(args.tok_pos + t);
-            slot[i] = __ldg(args.tok_slot + t);
-          }
         }
       }
       float4 s0[QB], s1[QB];
 #pragma unroll
       for (int i = 0; i < QB; ++i) s0[i] = s1[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int j = 0; j < WR_MAX_CLUSTER; ++j) {
-        if (j < S) {  // rank order: the sum does not depend on timing
-          const float* src = static_cast<const float*>(__cluster_map_shared_rank(xbuf, j));
+      for (int j0 = 0; j0 < WR_MAX_CLUSTER; j0 += RG) {
+        if (j0 < S) {
+          float4 p0[RG][QB], p1[RG][QB];
 #pragma unroll
-          for (int i = 0; i < QB; ++i) {
-            const int e = eb + 128 * i;
-            if (e < nq) {
+          for (int jj = 0; jj < RG; ++jj) {
+            const int j = j0 + jj, jv = j < S ? j : rank;  // jv: an address that exists
+            const float* src = jv == rank
+                                   ? xbuf
+                                   : static_cast<const float*>(__cluster_map_shared_rank(xbuf, jv));
+#pragma unroll
+            for (int i = 0; i < QB; ++i) {
+              const int e = eb + 128 * i;
               const int idx = (c0 + e / 32) * WR_BM + (e % 32) * 4;
-              const float4 p = *reinterpret_cast<const float4*>(src + idx);
-              s0[i].x += p.x; s0[i].y += p.y; s0[i].z += p.z; s0[i].w += p.w;
-              if (NA == 2) {
-                const float4 u = *reinterpret_cast<const float4*>(src + WR_XC * WR_BM + idx);
-                s1[i].x += u.x; s1[i].y += u.y; s1[i].z += u.z; s1[i].w += u.w;
+              const bool on = j < S && e < nq;
+              p0[jj][i] = on ? *reinterpret_cast<const float4*>(src + idx) : z4;
+              if (NA == 2)
+                p1[jj][i] = on ? *reinterpret_cast<const float4*>(src + WR_XC * WR_BM + idx) : z4;
+            }
+          }
+          // rank order: the sum does not depend on timing
+#pragma unroll
+          for (int jj = 0; jj < RG; ++jj) {
+            if (j0 + jj < S) {
+#pragma unroll
+              for (int i = 0; i < QB; ++i) {
+                s0[i].x += p0[jj][i].x; s0[i].y += p0[jj][i].y;
+                s0[i].z += p0[jj][i].z; s0[i].w += p0[jj][i].w;
+                if (NA == 2) {
+                  s1[i].x += p1[jj][i].x; s1[i].y += p1[jj][i].y;
+                  s1[i].z += p1[jj][i].z; s1[i].w += p1[jj][i].w;
+                }
               }
             }
           }
@@ -355,18 +398,6 @@ __global__ void __launch_bounds__(WR_THREADS, 1)
       }
       if (EPI == EPI_QKV) {
         const int nqh = args.n_q, nkv = args.n_kv;
-        float4 cs0[QB], cs1[QB];
-#pragma unroll
-        for (int i = 0; i < QB; ++i) {  // RoPE (cos, sin) of the batch, from the table
-          const int e = eb + 128 * i;
-          const int q4 = (e % 32) * 4, j = q4 % half;
-          if (e < nq && wt * hp + q4 / half < nqh + nkv && pos[i] < args.rope_positions) {
-            const float4* cs =
-                reinterpret_cast<const float4*>(args.rope_cs + static_cast<size_t>(pos[i]) * half + j);
-            cs0[i] = __ldg(cs);
-            cs1[i] = __ldg(cs + 1);
-          }
-        }
 #pragma unroll
         for (int i = 0; i < QB; ++i) {
           const int e = eb + 128 * i;
@@ -378,26 +409,26 @@ __global__ void __launch_bounds__(WR_THREADS, 1)
           if (head < nqh) {
             dst = args.q_out + static_cast<size_t>(t) * nqh * d + static_cast<size_t>(head) * d + j;
           } else {
-            if (slot[i] < 0) continue;
+            if (qi.slot[i] < 0) continue;
             const bool is_k = head < nqh + nkv;
             const int gh = is_k ? head - nqh : head - nqh - nkv;
             const int P = args.page_size;
             __nv_bfloat16* pool = is_k ? args.k_pool : args.v_pool;
-            dst = pool + static_cast<size_t>(slot[i] / P) * nkv * P * d +
-                  static_cast<size_t>(gh) * P * d + static_cast<size_t>(slot[i] % P) * d + j;
+            dst = pool + static_cast<size_t>(qi.slot[i] / P) * nkv * P * d +
+                  static_cast<size_t>(gh) * P * d + static_cast<size_t>(qi.slot[i] % P) * d + j;
           }
           float lo[4] = {s0[i].x, s0[i].y, s0[i].z, s0[i].w};
           float hi[4] = {s1[i].x, s1[i].y, s1[i].z, s1[i].w};
           if (head < nqh + nkv) {  // RoPE on q and k: rotate (i, i + d/2) by pos theta^(-2i/d)
             float c[4], sn[4];
-            if (pos[i] < args.rope_positions) {
-              c[0] = cs0[i].x; sn[0] = cs0[i].y; c[1] = cs0[i].z; sn[1] = cs0[i].w;
-              c[2] = cs1[i].x; sn[2] = cs1[i].y; c[3] = cs1[i].z; sn[3] = cs1[i].w;
+            if (qi.pos[i] < args.rope_positions) {
+              c[0] = qi.cs0[i].x; sn[0] = qi.cs0[i].y; c[1] = qi.cs0[i].z; sn[1] = qi.cs0[i].w;
+              c[2] = qi.cs1[i].x; sn[2] = qi.cs1[i].y; c[3] = qi.cs1[i].z; sn[3] = qi.cs1[i].w;
             } else {
 #pragma unroll
               for (int k = 0; k < 4; ++k) {
                 const float inv_freq = exp2f(-(2.0f * (j + k) / d) * args.log2_theta);
-                sincosf(static_cast<float>(pos[i]) * inv_freq, &sn[k], &c[k]);
+                sincosf(static_cast<float>(qi.pos[i]) * inv_freq, &sn[k], &c[k]);
               }
             }
 #pragma unroll
@@ -421,7 +452,7 @@ __global__ void __launch_bounds__(WR_THREADS, 1)
           if (EPI == EPI_SWIGLU) {
             const float u[4] = {s1[i].x, s1[i].y, s1[i].z, s1[i].w};
 #pragma unroll
-            for (int k = 0; k < 4; ++k) o[k] = o[k] / (1.0f + __expf(-o[k])) * u[k];
+            for (int k = 0; k < 4; ++k) o[k] = __fdividef(o[k], 1.0f + __expf(-o[k])) * u[k];
           } else if (EPI == EPI_RESID) {
             o[0] += bf16lo(rr[i].x);
             o[1] += bf16hi(rr[i].x);
@@ -438,12 +469,64 @@ __global__ void __launch_bounds__(WR_THREADS, 1)
       const int wt = tile / args.m_tiles, tt = tile % args.m_tiles;
       const int t0 = args.m_begin + tt * TOK;
       const int nv = min(TOK, args.m_end - t0);  // tokens of this tile
+      QkvIn qpre;  // QKV: the inputs of this thread's first batch of round 0
+      if (EPI == EPI_QKV) {
+        const int ntok = min(WR_XC, nv);
+        const int c0 = rank * ntok / S, c1 = (rank + 1) * ntok / S;
+        qkv_fetch(wt, t0, c0, et, (c1 - c0) * 32, qpre);
+      }
       // warp-uniform: tcgen05.ld below is .sync.aligned
       const bool have =
           ok && __all_sync(0xffffffffu, mbar_wait(&tail->tfull[acc], aph, tmo, abort_flag));
       if (!have) fail();
       tc_fence_after();
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * Cfg::ACC;
+      if (EPI != EPI_QKV && S == 1) {
+        // The whole K range is in this accumulator: each thread finishes its
+        // feature (accumulator row) for the tile's tokens straight from tensor
+        // memory, 32 tokens a load, without the exchange copy.  A warp's stores
+        // of one token cover 32 consecutive features (64 bytes).
+        const int f = wt * WR_BM + row;
+#pragma unroll 1
+        for (int c = 0; c * 32 < nv; ++c) {
+          uint32_t v0[32], v1[32];
+          if (have) {
+            tc_ld_32x32b_x32(tb + c * 32, v0);
+            if (NA == 2) tc_ld_32x32b_x32(tb + TOK + c * 32, v1);
+            tc_wait_ld();
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v0[i] = v1[i] = 0u;
+          }
+          const int nt = min(32, nv - c * 32);
+          if (f < args.N) {
+            const size_t r0 = static_cast<size_t>(t0 + c * 32);
+            float rv[32];
+            if (EPI == EPI_RESID) {  // all residual loads in flight before the stores
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                rv[i] = i < nt ? __bfloat162float(__ldg(args.R + (r0 + i) * args.ldr + f)) : 0.f;
+            }
+            __nv_bfloat16* dst = args.C + r0 * args.ldc + f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              if (i < nt) {
+                float o = __uint_as_float(v0[i]);
+                if (EPI == EPI_SWIGLU) o = __fdividef(o, 1.0f + __expf(-o)) * __uint_as_float(v1[i]);
+                if (EPI == EPI_RESID) o += rv[i];
+                dst[static_cast<size_t>(i) * args.ldc] = __float2bfloat16_rn(o);
+              }
+            }
+          }
+        }
+        tc_fence_before();  // the accumulator is free for the tile after next
+        mbar_arrive(&tail->tempty[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          aph ^= 1;
+        }
+        continue;
+      }
       const int rounds = (nv + WR_XC - 1) / WR_XC;
       for (int g = 0; g < rounds; ++g) {
         // every rank must have read this CTA's previous copy before it is overwritten
@@ -451,21 +534,24 @@ __global__ void __launch_bounds__(WR_THREADS, 1)
             !__all_sync(0xffffffffu, mbar_wait_cluster(&tail->xdone, (xr - 1) & 1, tmo, abort_flag)))
           fail();
         // accumulator columns [g XC, g XC + XC) of each A operand -> xbuf[a][token][row]
+        // (both 32-column loads of an operand in flight before the wait)
+        static_assert(WR_XC == 64, "two 32-column loads a round");
 #pragma unroll 1
         for (int a = 0; a < NA; ++a) {
-#pragma unroll 1
-          for (int c32 = 0; c32 < WR_XC / 32; ++c32) {
-            float v[32];
-            if (have) {
-              wr_tmem_load32(tb + a * TOK + g * WR_XC + c32 * 32, v);
-            } else {
+          uint32_t v0[32], v1[32];
+          if (have) {
+            tc_ld_32x32b_x32(tb + a * TOK + g * WR_XC, v0);
+            tc_ld_32x32b_x32(tb + a * TOK + g * WR_XC + 32, v1);
+            tc_wait_ld();
+          } else {
 #pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] = 0.f;
-            }
-            float* dst = xbuf + (a * WR_XC + c32 * 32) * WR_BM + row;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) dst[i * WR_BM] = v[i];
+            for (int i = 0; i < 32; ++i) v0[i] = v1[i] = 0u;
           }
+          float* dst = xbuf + a * WR_XC * WR_BM + row;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) dst[i * WR_BM] = __uint_as_float(v0[i]);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) dst[(32 + i) * WR_BM] = __uint_as_float(v1[i]);
         }
         if (g == rounds - 1) {  // the accumulator is free for the tile after next
           tc_fence_before();
@@ -481,11 +567,17 @@ __global__ void __launch_bounds__(WR_THREADS, 1)
           const int ntok = min(WR_XC, nv - g * WR_XC);
           const int c0 = rank * ntok / S, c1 = (rank + 1) * ntok / S;
           const int nq = (c1 - c0) * 32;
-          for (int eb = et; eb < nq; eb += 128 * QB) reduce_batch(wt, t0 + g * WR_XC, c0, eb, nq);
+          for (int eb = et; eb < nq; eb += 128 * QB)
+            reduce_batch(wt, t0 + g * WR_XC, c0, eb, nq,
+                         EPI == EPI_QKV && g == 0 && eb == et ? &qpre : nullptr);
         }
-        epi_sync();
-        arrive_all(xdone_addr);
-        ++xr;
+        // the last round of the last tile needs no release: the cluster barrier
+        // before exit keeps every copy alive until all ranks have read it
+        if (tile + stride < n_tiles || g + 1 < rounds) {
+          epi_sync();
+          arrive_all(xdone_addr);
+          ++xr;
+        }
       }
       if (++acc == 2) {
         acc = 0;
