@@ -819,6 +819,25 @@ nf_status run_meta(nf_plan p, const int32_t* bt, const int32_t* sl, cudaStream_t
   return NF_OK;
 }
 
+// Whether this step's trace records operation `op` (its events would sit
+// between the kernels).
+bool op_traced(nf_plan p, int op) {
+  return p->trace_left > 0 && p->trace_s0 && ((p->trace_ops >> op) & 1u);
+}
+
+// The step metadata handed to the first QKV nano-operation, which runs it
+// between its RMSNorm and its GEMM: the GEMM's operand loads and products then
+// proceed beside the one-CTA metadata kernel, and only its epilogue (RoPE
+// positions, cache slots) waits for the token map.
+struct MetaIn {
+  const int32_t* bt;
+  const int32_t* sl;
+};
+
+// The metadata goes inside the first QKV unless the trace records either
+// operation (each keeps its own interval then).
+bool fold_meta(nf_plan p) { return !op_traced(p, NF_OP_META) && !op_traced(p, NF_OP_QKV); }
+
 nf_status run_attention(nf_plan p, int seg, const void* q, const void* kp, const void* vp,
                         const int32_t* bt, void* o, int grid, cudaStream_t st) {
   TraceScope ts_(p, st, NF_OP_ATTN, seg);
@@ -901,13 +920,17 @@ struct SideStreamJoin {
 
 // One nano-operation of the layer; which = 0 QKV, 1 O, 2 RMSNorm-2 + gate/up + down.
 nf_status run_qkv(nf_plan p, const nf_layer_weights* w, const void* x, void* kp, void* vp, int r0,
-                  int r1, int grid, cudaStream_t st, int nano = 0) {
+                  int r1, int grid, cudaStream_t st, int nano = 0, const MetaIn* meta = nullptr) {
   TraceScope ts_(p, st, NF_OP_QKV, nano);
   const nf_model_shape& s = p->shape;
   NF_CUDA(nf::launch_rmsnorm(static_cast<const __nv_bfloat16*>(x),
                              static_cast<const __nv_bfloat16*>(w->norm1), p->n1, r0, r1, s.hidden,
                              s.rms_eps, st));
+  // The weight-row kernel waits for the metadata in all its warps (after its
+  // weight prefetch); the token-row kernel only in its epilogue.
+  if (meta) NF_TRY(run_meta(p, meta->bt, meta->sl, st));
   GemmArgs g = base_args(p);
+  g.wait_prior = meta ? 1 : 0;
   g.m_begin = r0;
   g.m_end = r1;
   g.N = (s.n_q_heads + 2 * s.n_kv_heads) * s.head_dim;
@@ -1124,11 +1147,13 @@ nf_status layer_step(nf_plan p, const nf_layer_weights* w, const void* x, void* 
   } step_end_{p};
   const nf_plan_opts& o = p->opts;
   const int all = p->num_sms;
+  const bool fold = with_meta && fold_meta(p);
+  const MetaIn mi{bt, sl};
   if (o.executor == NF_EXEC_SEQUENTIAL) {
-    if (with_meta) NF_TRY(run_meta(p, bt, sl, st));
+    if (with_meta && !fold) NF_TRY(run_meta(p, bt, sl, st));
     for (int i = 0; i < o.n_attn; ++i) {
       const int r0 = o.attn_bounds[i], r1 = o.attn_bounds[i + 1];
-      NF_TRY(run_qkv(p, w, x, kp, vp, r0, r1, all, st, i));
+      NF_TRY(run_qkv(p, w, x, kp, vp, r0, r1, all, st, i, i == 0 && fold ? &mi : nullptr));
       NF_TRY(run_attention(p, i, p->q, kp, vp, bt, p->o, all, st));
       NF_TRY(run_oproj(p, x, r0, r1, all, st, i));
     }
@@ -1148,10 +1173,10 @@ nf_status layer_step(nf_plan p, const nf_layer_weights* w, const void* x, void* 
   NF_CUDA(cudaStreamWaitEvent(p->s_gemm, ev_start, 0));
   NF_CUDA(cudaStreamWaitEvent(p->s_attn, ev_start, 0));
   SideStreamJoin join_{p, st};
-  if (with_meta) NF_TRY(run_meta(p, bt, sl, p->s_gemm));
+  if (with_meta && !fold) NF_TRY(run_meta(p, bt, sl, p->s_gemm));
   for (int i = 0; i < n; ++i) {
     NF_TRY(run_qkv(p, w, x, kp, vp, o.attn_bounds[i], o.attn_bounds[i + 1],
-                   i == 0 ? all : gemm_overlap, p->s_gemm, i));
+                   i == 0 ? all : gemm_overlap, p->s_gemm, i, i == 0 && fold ? &mi : nullptr));
     NF_CUDA(cudaEventRecord(ev_q[i], p->s_gemm));
   }
   for (int i = 0; i < n; ++i) {
@@ -1364,13 +1389,19 @@ nf_status run_layers_pipelined(nf_plan p, const nf_layer_weights* layers, int n_
   NF_CUDA(cudaStreamWaitEvent(p->s_gemm, ev_start, 0));
   NF_CUDA(cudaStreamWaitEvent(p->s_attn, ev_start, 0));
   SideStreamJoin join_{p, st};
-  NF_TRY(run_meta(p, bt, sl, p->s_gemm));
+  // the GEMM stream's order (schedule.h, also what the plan search simulates);
+  // it opens with the QKV of layer 0's first nano-batch, which takes the metadata
+  const std::vector<nf::WindowOp> sched = nf::window_schedule(o, n_layers);
+  const bool fold = fold_meta(p) && !sched.empty() && sched[0].kind == nf::WOP_QKV &&
+                    sched[0].layer == 0 && sched[0].nano == 0;
+  const MetaIn mi{bt, sl};
+  if (!fold) NF_TRY(run_meta(p, bt, sl, p->s_gemm));
   // QKV of nano-batch i of layer l on the GEMM stream, its attention on the other
   auto front = [&](int l, int i, int grid) -> nf_status {
     const nf_layer_weights* w = &layers[l];
     NF_TRY(refresh_weight_maps(p, w));
     NF_TRY(run_qkv(p, w, act[l], k_pools[l], v_pools[l], o.attn_bounds[i], o.attn_bounds[i + 1],
-                   grid, p->s_gemm, i));
+                   grid, p->s_gemm, i, fold && l == 0 && i == 0 ? &mi : nullptr));
     NF_CUDA(cudaEventRecord(ev_q[i], p->s_gemm));
     NF_CUDA(cudaStreamWaitEvent(p->s_attn, ev_q[i], 0));
     p->cur_set = l;
@@ -1378,8 +1409,7 @@ nf_status run_layers_pipelined(nf_plan p, const nf_layer_weights* layers, int n_
     NF_CUDA(cudaEventRecord(ev_a[i], p->s_attn));
     return NF_OK;
   };
-  // the GEMM stream's order (schedule.h, also what the plan search simulates)
-  for (const nf::WindowOp& op : nf::window_schedule(o, n_layers)) {
+  for (const nf::WindowOp& op : sched) {
     const int grid = op.full ? all : gsm;
     const int l = op.layer, i = op.nano;
     if (op.kind == nf::WOP_QKV) {
@@ -1400,8 +1430,9 @@ nf_status run_layers_pipelined(nf_plan p, const nf_layer_weights* layers, int n_
   return NF_OK;
 }
 
-// Metadata once, then layer l reads `in` (x for l = 0) and writes `out` (y for
-// the last layer), ping-ponging between the plan's activation buffers.
+// Metadata once (with layer 0), then layer l reads `in` (x for l = 0) and
+// writes `out` (y for the last layer), ping-ponging between the plan's
+// activation buffers.
 nf_status run_layers(nf_plan p, const nf_layer_weights* layers, int n_layers, const void* x,
                      void* const* k_pools, void* const* v_pools, const int32_t* bt,
                      const int32_t* sl, void* y, cudaStream_t st) {
@@ -1412,15 +1443,15 @@ nf_status run_layers(nf_plan p, const nf_layer_weights* layers, int n_layers, co
       act[l + 1] = l == n_layers - 1 ? y : (act[l] == p->xa ? (const void*)p->xb : (const void*)p->xa);
     return run_layers_pipelined(p, layers, n_layers, act, k_pools, v_pools, bt, sl, st);
   }
-  NF_TRY(run_meta(p, bt, sl, st));
   const void* cur = x;
   for (int l = 0; l < n_layers; ++l) {
     // intermediate outputs alternate between xa and xb; the caller makes sure
     // that y is not the last layer's input
     void* nxt = l == n_layers - 1 ? y : (cur == p->xa ? (void*)p->xb : (void*)p->xa);
     p->cur_set = l;
+    // the metadata runs once, inside layer 0 (it clears every layer's counters)
     const nf_status r = layer_step(p, &layers[l], cur, k_pools[l], v_pools[l], bt, sl, nxt, st,
-                                   /*with_meta=*/false);
+                                   /*with_meta=*/l == 0);
     p->cur_set = 0;
     if (r != NF_OK) return r;
     cur = nxt;

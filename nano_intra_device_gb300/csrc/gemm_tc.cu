@@ -275,6 +275,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
   } else {
     // ---------------------------------------------------------- epilogue
+    // Every CTA's epilogue waits here, so the grid ends after the kernel it
+    // depends on even where a CTA has no tile.
+    if (args.wait_prior) pdl_wait();
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const int row_in_tile = quarter * 32 + lane;
     uint32_t acc = 0, aph = 0, esync = 0;
@@ -561,8 +564,17 @@ static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB,
   const cudaError_t attr =
       set_smem_limit(reinterpret_cast<const void*>(gemm_tc_kernel<EPI, STAGES, BN>), smem);
   if (attr != cudaSuccess) return attr;
-  gemm_tc_kernel<EPI, STAGES, BN><<<grid, GEMM_THREADS, smem, stream>>>(tmA, tmB, tmB2, args);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = args.wait_prior ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<EPI, STAGES, BN>, tmA, tmB, tmB2, args);
 }
 
 template <int EPI, int BN>

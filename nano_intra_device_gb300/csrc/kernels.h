@@ -51,6 +51,11 @@ struct GemmArgs {
   int b_group_rows;
   int b2_row_off;
   float* Cf;            // EPI_STORE_F32 output, row stride ldc
+  // 1: launched as a programmatic dependent of the step-metadata kernel, whose
+  // outputs (token positions and cache slots) only the epilogue reads; A was
+  // complete before that kernel started.  The TMA and MMA warps start at once,
+  // the epilogue warps wait for the metadata before their first tile.
+  int wait_prior;
   uint32_t* status;
   unsigned long long timeout_ns;
 };

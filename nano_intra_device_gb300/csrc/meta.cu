@@ -35,6 +35,9 @@ __device__ __forceinline__ int upper_index(const int* bounds, int n, int t) {
 constexpr int META_SMEM_SEQ = 8192;  // sequences whose token starts fit in shared memory
 
 __global__ void __launch_bounds__(META_THREADS) meta_kernel(const MetaArgs a) {
+  // The first QKV GEMM of the step may start now on the other SMs: only its
+  // epilogue reads the token map, after waiting for this grid.
+  pdl_trigger();
   __shared__ int hist[META_MAX_SEG * META_MAX_BUCKETS];
   __shared__ int cursor[META_MAX_SEG * META_MAX_BUCKETS];
   __shared__ int sbegin[META_SMEM_SEQ + 1];
