@@ -667,6 +667,12 @@ GemmArgs base_args(nf_plan p) {
   return g;
 }
 
+// Token-row GEMMs of the sequential executor start as programmatic dependents
+// of the kernel ahead of them on the stream (the one that writes their A) and
+// request their first weights before they wait for it.  The two-stream
+// executor puts event waits between its GEMMs, so it launches them plainly.
+int weights_first(nf_plan p) { return p->opts.executor == NF_EXEC_SEQUENTIAL ? 1 : 0; }
+
 int cap_grid(int tiles, int cap) { return tiles < cap ? tiles : cap; }
 
 // Output columns per tile for a residual GEMM of m_tiles row tiles and N
@@ -931,6 +937,7 @@ nf_status run_qkv(nf_plan p, const nf_layer_weights* w, const void* x, void* kp,
   if (meta) NF_TRY(run_meta(p, meta->bt, meta->sl, st));
   GemmArgs g = base_args(p);
   g.wait_prior = meta ? 1 : 0;
+  g.weights_first = meta ? 0 : weights_first(p);
   g.m_begin = r0;
   g.m_end = r1;
   g.N = (s.n_q_heads + 2 * s.n_kv_heads) * s.head_dim;
@@ -991,6 +998,7 @@ nf_status run_oproj(nf_plan p, const void* x, int r0, int r1, int grid, cudaStre
   g.bn = pick_bn(g.m_tiles, g.N, grid);
   g.n_tiles = (g.N + g.bn - 1) / g.bn;
   g.splits = p->opts.gemm_split_k == 1 ? 1 : choose_splits(g.m_tiles * g.n_tiles, g.K, grid);
+  g.weights_first = weights_first(p);
   const CUtensorMap& wo = g.bn == 224 ? p->tm_wo224 : p->tm_wo;
   NF_CUDA(nf::launch_gemm(nf::EPI_RESID, p->tm_o, wo, wo, g,
                           cap_grid(g.m_tiles * g.n_tiles * g.splits, grid), st));
@@ -1064,6 +1072,7 @@ nf_status run_ffn(nf_plan p, const nf_layer_weights* w, void* y, int r0, int r1,
                                   xmap(p, XM_N2, c.tok), g, c.clusters, true, st));
   } else {
     g.splits = p->opts.gemm_split_k == 1 ? 1 : choose_splits(g.m_tiles * g.n_tiles, g.K, grid);
+    g.weights_first = weights_first(p);
     NF_CUDA(nf::launch_gemm(nf::EPI_SWIGLU, p->tm_n2, p->tm_wg, p->tm_wu, g,
                             cap_grid(g.m_tiles * g.n_tiles * g.splits, grid), st));
   }
@@ -1093,6 +1102,7 @@ nf_status run_ffn(nf_plan p, const nf_layer_weights* w, void* y, int r0, int r1,
   d.bn = pick_bn(d.m_tiles, d.N, grid);
   d.n_tiles = (d.N + d.bn - 1) / d.bn;
   d.splits = p->opts.gemm_split_k == 1 ? 1 : choose_splits(d.m_tiles * d.n_tiles, d.K, grid);
+  d.weights_first = weights_first(p);
   const CUtensorMap& wd = d.bn == 224 ? p->tm_wd224 : p->tm_wd;
   NF_CUDA(nf::launch_gemm(nf::EPI_RESID, p->tm_a, wd, wd, d,
                           cap_grid(d.m_tiles * d.n_tiles * d.splits, grid), st));

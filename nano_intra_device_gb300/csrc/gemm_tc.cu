@@ -186,6 +186,31 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       uint32_t st = 0, ph = 0;
       uint32_t issued_mask = 0, last_ph[MAX_STAGES] = {0, 0, 0, 0};
       bool ok = true;
+      // the B part of a stage: k block kb of output-column tile tn
+      auto load_b = [&](uint8_t* sb, uint64_t* bar, int kb, int tn, int brow) {
+        if (EPI == EPI_SWIGLU) {
+          tma_load_2d(sb, &tmB, bar, kb * BK, brow + tn * (BN / 2));
+          tma_load_2d(sb + B_BYTES / 2, &tmB2, bar, kb * BK, brow + args.b2_row_off + tn * (BN / 2));
+        } else {
+          tma_load_2d(sb, &tmB, bar, kb * BK, brow + tn * BN);
+        }
+      };
+      // Programmatic dependent: the weights of the first tile's first stages
+      // (no kernel writes them) are requested before the wait for the kernel
+      // that writes A; each such stage's barrier expects its A bytes too.
+      int pre = 0;
+      if (args.weights_first) {
+        if (static_cast<int>(blockIdx.x) < total_tiles) {
+          const GemmTile x = decode(blockIdx.x);
+          const int kb0 = x.sp * nk / splits, kb1 = (x.sp + 1) * nk / splits;
+          pre = kb1 - kb0 < STAGES ? kb1 - kb0 : STAGES;
+          for (int i = 0; i < pre; ++i) {
+            mbar_arrive_expect_tx(&tail->full[i], STAGE_BYTES);
+            load_b(smem + i * STAGE_BYTES + A_BYTES, &tail->full[i], kb0 + i, x.tn, x.brow);
+          }
+        }
+        pdl_wait();
+      }
       for (int u = blockIdx.x; u < total_tiles && ok; u += gridDim.x) {
         const GemmTile x = decode(u);
         const int sp = x.sp, tn = x.tn, m0 = x.m0;
@@ -197,15 +222,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           }
           uint8_t* sa = smem + st * STAGE_BYTES;
           uint8_t* sb = sa + A_BYTES;
-          mbar_arrive_expect_tx(&tail->full[st], STAGE_BYTES);
+          // the first tile's first `pre` stages (st = kb - kb0, phase 0) hold
+          // their weights already
+          const bool have_b = u == static_cast<int>(blockIdx.x) && kb - kb0 < pre;
+          if (!have_b) mbar_arrive_expect_tx(&tail->full[st], STAGE_BYTES);
           tma_load_2d(sa, &tmA, &tail->full[st], kb * BK, m0);
-          if (EPI == EPI_SWIGLU) {
-            tma_load_2d(sb, &tmB, &tail->full[st], kb * BK, x.brow + tn * (BN / 2));
-            tma_load_2d(sb + B_BYTES / 2, &tmB2, &tail->full[st], kb * BK,
-                        x.brow + args.b2_row_off + tn * (BN / 2));
-          } else {
-            tma_load_2d(sb, &tmB, &tail->full[st], kb * BK, x.brow + tn * BN);
-          }
+          if (!have_b) load_b(sb, &tail->full[st], kb, tn, x.brow);
           issued_mask |= 1u << st;
           last_ph[st] = ph;
           if (++st == STAGES) {
@@ -277,7 +299,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     // ---------------------------------------------------------- epilogue
     // Every CTA's epilogue waits here, so the grid ends after the kernel it
     // depends on even where a CTA has no tile.
-    if (args.wait_prior) pdl_wait();
+    if (args.wait_prior || args.weights_first) pdl_wait();
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const int row_in_tile = quarter * 32 + lane;
     uint32_t acc = 0, aph = 0, esync = 0;
@@ -573,7 +595,7 @@ static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB,
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
-  cfg.numAttrs = args.wait_prior ? 1 : 0;
+  cfg.numAttrs = args.wait_prior || args.weights_first ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<EPI, STAGES, BN>, tmA, tmB, tmB2, args);
 }
 
@@ -592,8 +614,11 @@ cudaError_t launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB,
                         const CUtensorMap& tmB2, const GemmArgs& args, int grid,
                         cudaStream_t stream) {
   if (grid <= 0) return cudaSuccess;
+  // the grouped GEMM reads the group offsets before any wait: never a
+  // programmatic dependent
   if (args.n_groups < 0 || args.n_groups > GEMM_MAX_GROUPS ||
-      (args.n_groups > 0 && (!args.group_off || args.splits > 1)))
+      (args.n_groups > 0 && (!args.group_off || args.splits > 1 || args.wait_prior ||
+                             args.weights_first)))
     return cudaErrorInvalidValue;
   const int bn = args.bn ? args.bn : BN_DEFAULT;
   if (bn == 224) {  // residual epilogue only (the O and down projections)

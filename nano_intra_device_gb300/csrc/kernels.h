@@ -56,6 +56,11 @@ struct GemmArgs {
   // complete before that kernel started.  The TMA and MMA warps start at once,
   // the epilogue warps wait for the metadata before their first tile.
   int wait_prior;
+  // 1: launched as a programmatic dependent of the kernel that writes A (not
+  // B): the producer issues the B (weight) loads of its first ring stages
+  // before it waits for that kernel; A, the residual and every output come
+  // after the wait.  Not with the grouped GEMM.
+  int weights_first;
   uint32_t* status;
   unsigned long long timeout_ns;
 };
