@@ -791,7 +791,11 @@ struct TraceScope {
   }
 };
 
-nf_status run_meta(nf_plan p, const int32_t* bt, const int32_t* sl, cudaStream_t st) {
+// after_qkv: the step's RMSNorm-1 kernels write the token map, and this
+// launch (the work list only) follows the first QKV GEMM as its programmatic
+// dependent, on the SMs the GEMM's last wave leaves free.
+nf_status run_meta(nf_plan p, const int32_t* bt, const int32_t* sl, cudaStream_t st,
+                   bool after_qkv = false) {
   TraceScope ts_(p, st, NF_OP_META, 0);
   nf::MetaArgs m{};
   m.seq_lens = sl;
@@ -821,8 +825,32 @@ nf_status run_meta(nf_plan p, const int32_t* bt, const int32_t* sl, cudaStream_t
   m.fetch_stride = NF_MAX_NANO;
   m.status = p->status;
   m.validate = p->opts.validate;
+  m.map_done = after_qkv ? 1 : 0;
   NF_CUDA(nf::launch_meta(m, st));
   return NF_OK;
+}
+
+// The token map that RMSNorm-1 writes for its rows (see run_meta).
+nf::TokMap token_map_args(nf_plan p, const int32_t* bt, const int32_t* sl) {
+  nf::TokMap m{};
+  m.seq_lens = sl;
+  m.q_lens = p->d_q_lens;
+  m.tok_begin = p->d_tok_begin;
+  m.block_table = bt;
+  m.n_seq = p->n_seq;
+  m.n_decode = p->n_decode;
+  m.max_pages = p->max_pages;
+  m.num_pages = p->num_pages;
+  m.page_size = p->shape.page_size;
+  m.kv_chunk = p->opts.kv_chunk;
+  m.max_chunks = p->max_chunks;
+  m.validate = p->opts.validate;
+  m.tok_seq = p->tok_seq;
+  m.tok_pos = p->tok_pos;
+  m.tok_slot = p->tok_slot;
+  m.tok_nchunks = p->tok_nchunks;
+  m.status = p->status;
+  return m;
 }
 
 // Whether this step's trace records operation `op` (its events would sit
@@ -838,6 +866,12 @@ bool op_traced(nf_plan p, int op) {
 struct MetaIn {
   const int32_t* bt;
   const int32_t* sl;
+  enum Mode {
+    AHEAD,      // the metadata kernel between RMSNorm-1 and the GEMM
+    MAP_LIST,   // RMSNorm-1 maps the nano-batch's tokens; the work list of
+                // the step follows the GEMM as its programmatic dependent
+    MAP         // RMSNorm-1 maps the nano-batch's tokens
+  } mode;
 };
 
 // The metadata goes inside the first QKV unless the trace records either
@@ -929,15 +963,29 @@ nf_status run_qkv(nf_plan p, const nf_layer_weights* w, const void* x, void* kp,
                   int r1, int grid, cudaStream_t st, int nano = 0, const MetaIn* meta = nullptr) {
   TraceScope ts_(p, st, NF_OP_QKV, nano);
   const nf_model_shape& s = p->shape;
+  const bool map_in_norm = meta && meta->mode != MetaIn::AHEAD;
+  const bool meta_ahead = meta && meta->mode == MetaIn::AHEAD;
+  const nf::TokMap tm = map_in_norm ? token_map_args(p, meta->bt, meta->sl) : nf::TokMap{};
   NF_CUDA(nf::launch_rmsnorm(static_cast<const __nv_bfloat16*>(x),
                              static_cast<const __nv_bfloat16*>(w->norm1), p->n1, r0, r1, s.hidden,
-                             s.rms_eps, st));
-  // The weight-row kernel waits for the metadata in all its warps (after its
-  // weight prefetch); the token-row kernel only in its epilogue.
-  if (meta) NF_TRY(run_meta(p, meta->bt, meta->sl, st));
+                             s.rms_eps, st, map_in_norm ? &tm : nullptr));
+  // Metadata between the norm and the GEMM: the weight-row kernel waits for it
+  // in all its warps (after its weight prefetch), the token-row kernel only in
+  // its epilogue.
+  if (meta_ahead) NF_TRY(run_meta(p, meta->bt, meta->sl, st));
+  // The step's work list right after the GEMM, on the SMs its last wave
+  // leaves free; the attention that follows waits for both.
+  struct ListAfter {
+    nf_plan p;
+    const MetaIn* m;
+    cudaStream_t st;
+    nf_status go() const {
+      return m && m->mode == MetaIn::MAP_LIST ? run_meta(p, m->bt, m->sl, st, true) : NF_OK;
+    }
+  } const list_after{p, meta, st};
   GemmArgs g = base_args(p);
-  g.wait_prior = meta ? 1 : 0;
-  g.weights_first = meta ? 0 : weights_first(p);
+  g.wait_prior = meta_ahead ? 1 : 0;
+  g.weights_first = meta_ahead ? 0 : weights_first(p);
   g.m_begin = r0;
   g.m_end = r1;
   g.N = (s.n_q_heads + 2 * s.n_kv_heads) * s.head_dim;
@@ -959,13 +1007,13 @@ nf_status run_qkv(nf_plan p, const nf_layer_weights* w, const void* x, void* kp,
       g.splits = c.splits;
       NF_CUDA(nf::launch_gemm_wrows(nf::EPI_QKV, c.tok, p->tm_wqkv_h, p->tm_wqkv_h,
                                     xmap(p, XM_N1, c.tok), g, c.clusters, true, st));
-      return NF_OK;
+      return list_after.go();
     }
   }
   g.splits = p->opts.gemm_split_k == 1 ? 1 : choose_splits(g.m_tiles * g.n_tiles, g.K, grid);
   NF_CUDA(nf::launch_gemm(nf::EPI_QKV, p->tm_n1, p->tm_wqkv, p->tm_wqkv, g,
                           cap_grid(g.m_tiles * g.n_tiles * g.splits, grid), st));
-  return NF_OK;
+  return list_after.go();
 }
 
 nf_status run_oproj(nf_plan p, const void* x, int r0, int r1, int grid, cudaStream_t st,
@@ -1158,12 +1206,15 @@ nf_status layer_step(nf_plan p, const nf_layer_weights* w, const void* x, void* 
   const nf_plan_opts& o = p->opts;
   const int all = p->num_sms;
   const bool fold = with_meta && fold_meta(p);
-  const MetaIn mi{bt, sl};
   if (o.executor == NF_EXEC_SEQUENTIAL) {
+    // One stream: RMSNorm-1 of each nano-batch maps its tokens, and the work
+    // list is built beside the first QKV GEMM.
     if (with_meta && !fold) NF_TRY(run_meta(p, bt, sl, st));
+    const MetaIn first{bt, sl, MetaIn::MAP_LIST}, rest{bt, sl, MetaIn::MAP};
     for (int i = 0; i < o.n_attn; ++i) {
       const int r0 = o.attn_bounds[i], r1 = o.attn_bounds[i + 1];
-      NF_TRY(run_qkv(p, w, x, kp, vp, r0, r1, all, st, i, i == 0 && fold ? &mi : nullptr));
+      NF_TRY(run_qkv(p, w, x, kp, vp, r0, r1, all, st, i,
+                     !fold ? nullptr : i == 0 ? &first : &rest));
       NF_TRY(run_attention(p, i, p->q, kp, vp, bt, p->o, all, st));
       NF_TRY(run_oproj(p, x, r0, r1, all, st, i));
     }
@@ -1184,6 +1235,7 @@ nf_status layer_step(nf_plan p, const nf_layer_weights* w, const void* x, void* 
   NF_CUDA(cudaStreamWaitEvent(p->s_attn, ev_start, 0));
   SideStreamJoin join_{p, st};
   if (with_meta && !fold) NF_TRY(run_meta(p, bt, sl, p->s_gemm));
+  const MetaIn mi{bt, sl, MetaIn::AHEAD};
   for (int i = 0; i < n; ++i) {
     NF_TRY(run_qkv(p, w, x, kp, vp, o.attn_bounds[i], o.attn_bounds[i + 1],
                    i == 0 ? all : gemm_overlap, p->s_gemm, i, i == 0 && fold ? &mi : nullptr));
@@ -1404,7 +1456,7 @@ nf_status run_layers_pipelined(nf_plan p, const nf_layer_weights* layers, int n_
   const std::vector<nf::WindowOp> sched = nf::window_schedule(o, n_layers);
   const bool fold = fold_meta(p) && !sched.empty() && sched[0].kind == nf::WOP_QKV &&
                     sched[0].layer == 0 && sched[0].nano == 0;
-  const MetaIn mi{bt, sl};
+  const MetaIn mi{bt, sl, MetaIn::AHEAD};
   if (!fold) NF_TRY(run_meta(p, bt, sl, p->s_gemm));
   // QKV of nano-batch i of layer l on the GEMM stream, its attention on the other
   auto front = [&](int l, int i, int grid) -> nf_status {

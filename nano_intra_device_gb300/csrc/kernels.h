@@ -118,9 +118,29 @@ cudaError_t launch_moe_combine(const __nv_bfloat16* h, const float* part, const 
                                const float* pair_w, __nv_bfloat16* y, int r0, int n, int top_k,
                                int hidden, cudaStream_t stream);
 
+// ----------------------------------------------------------- token map
+// Inputs and outputs of the per-token map (tokmap.cuh): sequence, position,
+// cache slot and split-KV piece count of each token of the step.
+struct TokMap {
+  const int* seq_lens;      // device [n_seq]
+  const int* q_lens;        // device [n_seq]
+  const int* tok_begin;     // device [n_seq + 1]
+  const int* block_table;   // device [n_seq, max_pages]
+  int n_seq, n_decode;      // sequences; the first n_decode own one token each
+  int max_pages, num_pages, page_size, kv_chunk, max_chunks, validate;
+  int* tok_seq;             // out [n_tok]
+  int* tok_pos;             // out [n_tok]
+  int* tok_slot;            // out [n_tok]
+  int* tok_nchunks;         // out [n_tok]
+  uint32_t* status;
+};
+
 // --------------------------------------------------------------- RMSNorm
+// map != nullptr: the CTA of row t also writes the token map of token t
+// (RMSNorm-1 of a step, whose rows are the step's tokens).
 cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* g, __nv_bfloat16* out,
-                           int row_begin, int row_end, int hidden, float eps, cudaStream_t stream);
+                           int row_begin, int row_end, int hidden, float eps, cudaStream_t stream,
+                           const TokMap* map = nullptr);
 
 // Embedding lookup: x[t] = embed[tokens[t]] (rows of H bf16); an id outside
 // [0, vocab) flags ST_BAD_LEN and writes a zero row.
@@ -149,6 +169,11 @@ struct MetaArgs {
   int fetch_stride;         // fetch counters per set
   uint32_t* status;
   int validate;
+  // 1: the step's RMSNorm-1 kernels write the token map; this kernel derives
+  // positions for the work list itself, writes no token map, and is launched
+  // as a programmatic dependent of the first QKV GEMM (which reads nothing it
+  // writes): it waits for that GEMM only before it ends
+  int map_done;
 };
 cudaError_t launch_meta(const MetaArgs& a, cudaStream_t stream);
 

@@ -12,9 +12,12 @@
 //   Throughput", "Auto-Search Stage I", constraints on dependencies) and,
 //   inside a nano-batch, ordered longest first so the last pieces any warp
 //   picks up are the short ones.
-// One CTA does it all: a few thousand tokens, microseconds.
+// One CTA does it all: a few thousand tokens, microseconds.  In the
+// sequential executor the token map comes from RMSNorm-1 (rmsnorm.cu) and this
+// kernel, which then only builds the work list, runs beside the first QKV GEMM.
 #include "common.cuh"
 #include "kernels.h"
+#include "tokmap.cuh"
 
 namespace nf {
 
@@ -22,21 +25,12 @@ constexpr int META_THREADS = 1024;
 constexpr int META_MAX_SEG = 8;
 constexpr int META_MAX_BUCKETS = 128;
 
-__device__ __forceinline__ int upper_index(const int* bounds, int n, int t) {
-  // largest i in [0, n) with bounds[i] <= t
-  int lo = 0, hi = n - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (bounds[mid] <= t) lo = mid; else hi = mid - 1;
-  }
-  return lo;
-}
-
 constexpr int META_SMEM_SEQ = 8192;  // sequences whose token starts fit in shared memory
 
 __global__ void __launch_bounds__(META_THREADS) meta_kernel(const MetaArgs a) {
-  // The first QKV GEMM of the step may start now on the other SMs: only its
-  // epilogue reads the token map, after waiting for this grid.
+  // A programmatic dependent (the first QKV GEMM of a two-stream step, which
+  // reads the token map only in its epilogue, after waiting for this grid) may
+  // start now on the other SMs.
   pdl_trigger();
   __shared__ int hist[META_MAX_SEG * META_MAX_BUCKETS];
   __shared__ int cursor[META_MAX_SEG * META_MAX_BUCKETS];
@@ -55,46 +49,29 @@ __global__ void __launch_bounds__(META_THREADS) meta_kernel(const MetaArgs a) {
   const int* tb = in_smem ? sbegin : a.tok_begin;
 
   // pass 1: token map, slots, piece histogram
+  TokMap tm{};
+  tm.seq_lens = a.seq_lens;
+  tm.q_lens = a.q_lens;
+  tm.block_table = a.block_table;
+  tm.max_pages = a.max_pages;
+  tm.num_pages = a.num_pages;
+  tm.page_size = P;
+  tm.kv_chunk = C;
+  tm.max_chunks = a.max_chunks;
+  tm.validate = a.validate;
+  tm.status = a.status;
   for (int t = threadIdx.x; t < a.n_tok; t += META_THREADS) {
-    const int s = upper_index(tb, a.n_seq, t);
-    const int L = a.seq_lens[s], q = a.q_lens[s];
-    int pos = L - q + (t - tb[s]);
-    bool ok = true;
-    if (q < 1 || L < q || pos >= a.max_pages * P) {
-      raise_status(a.status, ST_BAD_LEN);
-      ok = false;
-      pos = 0;
+    const int s = tok_seq_search(tb, 0, a.n_seq, t);
+    const TokEntry e = token_entry(tm, s, tb[s], t, !a.map_done);
+    if (!a.map_done) {
+      a.tok_seq[t] = s;
+      a.tok_pos[t] = e.pos;
+      a.tok_slot[t] = e.slot;
+      a.tok_nchunks[t] = e.nch;
     }
-    int slot = -1;
-    if (ok) {
-      const int page = a.block_table[static_cast<size_t>(s) * a.max_pages + pos / P];
-      if (page >= 0 && page < a.num_pages) {
-        slot = page * P + pos % P;
-      } else {
-        raise_status(a.status, ST_BAD_PAGE);
-      }
-      if (a.validate) {  // every page the token's attention will read
-        for (int j = 0; j <= pos / P; ++j) {
-          const int pg = a.block_table[static_cast<size_t>(s) * a.max_pages + j];
-          if (pg < 0 || pg >= a.num_pages) {
-            raise_status(a.status, ST_BAD_PAGE);
-            break;
-          }
-        }
-      }
-    }
-    const int ctx = ok ? pos + 1 : 0;
-    int nch = (ctx + C - 1) / C;
-    if (nch > a.max_chunks) {
-      raise_status(a.status, ST_OVERFLOW);
-      nch = a.max_chunks;
-    }
-    a.tok_seq[t] = s;
-    a.tok_pos[t] = pos;
-    a.tok_slot[t] = slot;
-    a.tok_nchunks[t] = nch;
-    const int seg = upper_index(sseg, a.n_seg, t);
-    for (int c = 0; c < nch; ++c) {
+    const int ctx = e.nch > 0 ? e.pos + 1 : 0;
+    const int seg = tok_seq_search(sseg, 0, a.n_seg, t);
+    for (int c = 0; c < e.nch; ++c) {
       const int len = min(C, ctx - c * C);
       const int npg = (len + P - 1) / P;
       atomicAdd(&hist[seg * META_MAX_BUCKETS + (nb - npg)], 1);
@@ -117,11 +94,20 @@ __global__ void __launch_bounds__(META_THREADS) meta_kernel(const MetaArgs a) {
   }
   __syncthreads();
 
-  // pass 2: scatter pieces
+  // pass 2: scatter pieces (the token map is this kernel's own output, or
+  // derived again where the RMSNorm kernels write it)
   for (int t = threadIdx.x; t < a.n_tok; t += META_THREADS) {
-    const int ctx = a.tok_pos[t] + 1;
-    const int nch = a.tok_nchunks[t];
-    const int seg = upper_index(sseg, a.n_seg, t);
+    int ctx, nch;
+    if (a.map_done) {
+      const int s = tok_seq_search(tb, 0, a.n_seq, t);
+      const TokEntry e = token_entry(tm, s, tb[s], t, false);
+      nch = e.nch;
+      ctx = nch > 0 ? e.pos + 1 : 0;
+    } else {
+      ctx = a.tok_pos[t] + 1;
+      nch = a.tok_nchunks[t];
+    }
+    const int seg = tok_seq_search(sseg, 0, a.n_seg, t);
     for (int c = 0; c < nch; ++c) {
       const int len = min(C, ctx - c * C);
       const int npg = (len + P - 1) / P;
@@ -138,13 +124,24 @@ __global__ void __launch_bounds__(META_THREADS) meta_kernel(const MetaArgs a) {
   const int n_done = a.n_tok * a.n_kv * sets;  // multiple of 4: row_done is 16-byte aligned
   for (int i = threadIdx.x; i < n_done / 4; i += META_THREADS) reinterpret_cast<int4*>(a.row_done)[i] = z;
   for (int i = (n_done / 4) * 4 + threadIdx.x; i < n_done; i += META_THREADS) a.row_done[i] = 0;
+  // Launched as a programmatic dependent of the first QKV GEMM: end only after
+  // it, so that whatever follows on the stream sees both.
+  pdl_wait();
 }
 
 cudaError_t launch_meta(const MetaArgs& a, cudaStream_t stream) {
   if (a.n_seg > META_MAX_SEG || a.kv_chunk / a.page_size > META_MAX_BUCKETS)
     return cudaErrorInvalidValue;
-  meta_kernel<<<1, META_THREADS, 0, stream>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(1, 1, 1);
+  cfg.blockDim = dim3(META_THREADS, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = a.map_done ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, meta_kernel, a);
 }
 
 }  // namespace nf

@@ -3,6 +3,7 @@
 // transformer layer).  HBM-bound: one CTA per row, 16-byte loads, fp32 sums.
 #include "common.cuh"
 #include "kernels.h"
+#include "tokmap.cuh"
 
 namespace nf {
 
@@ -10,9 +11,25 @@ constexpr int RMS_THREADS = 128;
 
 __global__ void __launch_bounds__(RMS_THREADS)
     rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ g,
-                   __nv_bfloat16* __restrict__ out, int row_begin, int hidden, float eps) {
+                   __nv_bfloat16* __restrict__ out, int row_begin, int hidden, float eps,
+                   const TokMap map, int with_map) {
   pdl_trigger();
   const int row = row_begin + blockIdx.x;
+  if (with_map && threadIdx.x == RMS_THREADS - 32) {
+    // RMSNorm-1: row `row` is token `row` of the step.  The first n_decode
+    // sequences own one token each, so a decode row is its own sequence;
+    // otherwise search the token starts.
+    const int t = row;
+    int s = -1;
+    if (t < map.n_decode && t < map.n_seq && map.tok_begin[t] == t && map.tok_begin[t + 1] == t + 1)
+      s = t;
+    if (s < 0) s = tok_seq_search(map.tok_begin, 0, map.n_seq, t);
+    const TokEntry e = token_entry(map, s, map.tok_begin[s], t, true);
+    map.tok_seq[t] = s;
+    map.tok_pos[t] = e.pos;
+    map.tok_slot[t] = e.slot;
+    map.tok_nchunks[t] = e.nch;
+  }
   const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(row) * hidden);
   const uint4* gr = reinterpret_cast<const uint4*>(g);
   uint4* orow = reinterpret_cast<uint4*>(out + static_cast<size_t>(row) * hidden);
@@ -47,10 +64,12 @@ __global__ void __launch_bounds__(RMS_THREADS)
 }
 
 cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* g, __nv_bfloat16* out,
-                           int row_begin, int row_end, int hidden, float eps, cudaStream_t stream) {
+                           int row_begin, int row_end, int hidden, float eps, cudaStream_t stream,
+                           const TokMap* map) {
   if (row_end <= row_begin) return cudaSuccess;
+  const TokMap m = map ? *map : TokMap{};
   rmsnorm_kernel<<<row_end - row_begin, RMS_THREADS, 0, stream>>>(x, g, out, row_begin, hidden,
-                                                                   eps);
+                                                                   eps, m, map ? 1 : 0);
   return cudaGetLastError();
 }
 
