@@ -878,8 +878,13 @@ struct MetaIn {
 // operation (each keeps its own interval then).
 bool fold_meta(nf_plan p) { return !op_traced(p, NF_OP_META) && !op_traced(p, NF_OP_QKV); }
 
+// early: the kernel ahead on `st` is this nano-batch's QKV GEMM and the work
+// list and token map are older; the decode kernel (when no prefill tiles go
+// first) then starts as the GEMM's programmatic dependent and requests the K/V
+// pages that the GEMM does not write before it waits for it.
 nf_status run_attention(nf_plan p, int seg, const void* q, const void* kp, const void* vp,
-                        const int32_t* bt, void* o, int grid, cudaStream_t st) {
+                        const int32_t* bt, void* o, int grid, cudaStream_t st,
+                        bool early = false) {
   TraceScope ts_(p, st, NF_OP_ATTN, seg);
   nf::AttnArgs a{};
   a.q = static_cast<const __nv_bfloat16*>(q);
@@ -937,7 +942,8 @@ nf_status run_attention(nf_plan p, int seg, const void* q, const void* kp, const
     const int n_pf = a.prefill_elsewhere ? p->pf_seg[seg + 1] - p->pf_seg[seg] : 0;
     if (n_pf > 0)
       NF_CUDA(nf::launch_attention_prefill(a, pm->tk, pm->tv, p->pf_tiles + p->pf_seg[seg], n_pf, st));
-    NF_CUDA(nf::launch_attention_mma(a, pm->dk, pm->dv, grid, n_pf > 0, st));
+    a.early = early && n_pf == 0 ? 1 : 0;
+    NF_CUDA(nf::launch_attention_mma(a, pm->dk, pm->dv, grid, n_pf > 0 || a.early, st));
   }
   return NF_OK;
 }
@@ -959,8 +965,11 @@ struct SideStreamJoin {
 };
 
 // One nano-operation of the layer; which = 0 QKV, 1 O, 2 RMSNorm-2 + gate/up + down.
+// token_rows (optional, out): whether the GEMM ran the token-row kernel.
 nf_status run_qkv(nf_plan p, const nf_layer_weights* w, const void* x, void* kp, void* vp, int r0,
-                  int r1, int grid, cudaStream_t st, int nano = 0, const MetaIn* meta = nullptr) {
+                  int r1, int grid, cudaStream_t st, int nano = 0, const MetaIn* meta = nullptr,
+                  bool* token_rows = nullptr) {
+  if (token_rows) *token_rows = false;
   TraceScope ts_(p, st, NF_OP_QKV, nano);
   const nf_model_shape& s = p->shape;
   const bool map_in_norm = meta && meta->mode != MetaIn::AHEAD;
@@ -1013,6 +1022,7 @@ nf_status run_qkv(nf_plan p, const nf_layer_weights* w, const void* x, void* kp,
   g.splits = p->opts.gemm_split_k == 1 ? 1 : choose_splits(g.m_tiles * g.n_tiles, g.K, grid);
   NF_CUDA(nf::launch_gemm(nf::EPI_QKV, p->tm_n1, p->tm_wqkv, p->tm_wqkv, g,
                           cap_grid(g.m_tiles * g.n_tiles * g.splits, grid), st));
+  if (token_rows) *token_rows = true;
   return list_after.go();
 }
 
@@ -1213,9 +1223,15 @@ nf_status layer_step(nf_plan p, const nf_layer_weights* w, const void* x, void* 
     const MetaIn first{bt, sl, MetaIn::MAP_LIST}, rest{bt, sl, MetaIn::MAP};
     for (int i = 0; i < o.n_attn; ++i) {
       const int r0 = o.attn_bounds[i], r1 = o.attn_bounds[i + 1];
+      bool token_rows = false;
       NF_TRY(run_qkv(p, w, x, kp, vp, r0, r1, all, st, i,
-                     !fold ? nullptr : i == 0 ? &first : &rest));
-      NF_TRY(run_attention(p, i, p->q, kp, vp, bt, p->o, all, st));
+                     !fold ? nullptr : i == 0 ? &first : &rest, &token_rows));
+      // The attention starts early behind a token-row QKV GEMM (not right
+      // after the work-list kernel).  Behind the weight-row kernel it measured
+      // slower (the 64-row decode stack 4.87 -> 5.31 ms; the cause is not
+      // known), so there it waits for the GEMM as before.
+      NF_TRY(run_attention(p, i, p->q, kp, vp, bt, p->o, all, st,
+                           token_rows && !(fold && i == 0)));
       NF_TRY(run_oproj(p, x, r0, r1, all, st, i));
     }
     for (int j = 0; j < o.n_ffn; ++j)

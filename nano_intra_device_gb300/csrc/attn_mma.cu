@@ -108,6 +108,7 @@ __global__ void __launch_bounds__(WARPS * 32, WARPS == AMMA_SHARE_WARPS ? 4 : 1)
     voff[i] = BLK + page_chunk_off(v_row, 2 * i + v_ci);
   }
 
+  bool waited = !a.early;  // warp-uniform: this warp has waited for the QKV GEMM
   int next_idx = 0;
   if (lane == 0) next_idx = atomicAdd(&a.fetch[seg], 1);
   for (;;) {
@@ -162,11 +163,28 @@ __global__ void __launch_bounds__(WARPS * 32, WARPS == AMMA_SHARE_WARPS ? 4 : 1)
       int first[STAGES];
 #pragma unroll
       for (int k = 0; k < STAGES; ++k) first[k] = page_id(k < pre ? k : 0);
+      // Before the wait for the QKV GEMM only pages that it does not write: a
+      // decode row appends position ctx - 1; other rows are left whole.
+      int ahead = pre;
+      if (!waited) {
+        const int fresh = s < a.n_decode_seqs ? ctx - 1 : 0;
+        const int clean = fresh > b0 ? (fresh - b0) / P : 0;
+        ahead = clean < pre ? clean : pre;
+      }
       if (lane == 0) {
         fence_proxy_async_smem();  // the previous piece's reads of these slots come first
 #pragma unroll
         for (int k = 0; k < STAGES; ++k)
-          if (k < pre) issue_into((gk + k) % STAGES, first[k]);
+          if (k < ahead) issue_into((gk + k) % STAGES, first[k]);
+      }
+      if (!waited) {
+        pdl_wait();  // q and this step's K/V are written
+        waited = true;
+        if (lane == 0) {
+#pragma unroll
+          for (int k = 0; k < STAGES; ++k)
+            if (k >= ahead && k < pre) issue_into((gk + k) % STAGES, first[k]);
+        }
       }
       issued = pre;
     }

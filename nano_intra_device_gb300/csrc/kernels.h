@@ -201,6 +201,11 @@ struct AttnArgs {
   // n_decode_seqs and up (the prefill chunks) are left to the prefill kernel
   int prefill_elsewhere;
   int n_decode_seqs;
+  // tensor-core decode kernel, 1: launched as a programmatic dependent of the
+  // QKV GEMM that writes q and this step's K/V, with the work list and token
+  // map from earlier kernels.  A warp's first piece requests its pages that lie
+  // wholly before the first position the step writes, then waits for the GEMM.
+  int early;
   uint32_t* status;
   unsigned long long timeout_ns;
 };
