@@ -31,6 +31,8 @@ CONFIGS = [
     ("small 3-layer stack", "logits", r"test_tiny_stack_matches_oracle", r"^3-layer tiny stack logits$"),
     ("8B-shaped 2-layer stack + LM head", "logits", r"test_llama8b_shaped_two_layer_stack",
      r"^8B-shaped 2-layer stack logits$"),
+    ("8B-shaped decode-only batch (256 rows), 2 layers on one stream, 1 and 2 nano-batches", "y",
+     r"test_llama8b_shaped_decode_layers_on_one_stream", r"^8B-shaped decode layers on one stream"),
     ("70B-shaped layer, sampled rows", "y", r"test_llama70b_shaped_layer_sampled_rows",
      r"^70B-shaped layer y$"),
     ("70B-shaped 2 layers, window n = 2 on 46 SMs", "y", r"test_llama70b_shaped_layers_overlapped",

@@ -205,6 +205,35 @@ def test_tiny_cross_layer_window_with_other_ffn_splits(ab, fb):
     parity(f64(y), ex["y"], em["y"], f"3 tiny layers, attention {ab}, FFN {fb}")
 
 
+@pytest.mark.parametrize("bounds", [None, [0, 128, 256]])
+def test_llama8b_shaped_decode_layers_on_one_stream(bounds):
+    """A decode-only batch past the weight-row kernel's token range (256 rows,
+    so every QKV projection runs the token-row kernel) through two layers on
+    one stream.  After the first layer's first attention (and for the second
+    nano-batch of each layer) the decode attention starts as the programmatic
+    dependent of its QKV GEMM and requests, before it waits for the GEMM, the
+    pages that lie wholly before its row's new position.  Split-KV pieces of
+    256 positions put piece starts inside long rows; the sampled rows include
+    contexts that end on a page boundary, one past it, the shortest and the
+    longest, against both oracles."""
+    shape = wl.llama8b_shape()
+    ctx = wl.lognormal_contexts(256, 600.0, 1.0, 1, 4096, seed=21)
+    ctx[7], ctx[130] = 48, 49            # the new position ends / starts a page
+    ctx[200] = 1
+    batch = wl.make_batch(shape, ctx, [], None, seed_bt=22, max_pages=4096 // 16)
+    T = batch.n_tokens
+    layers = [wl.make_weights(shape, seed=40 + i, gain_std=0.1) for i in range(2)]
+    pools = [wl.make_pools(shape, batch, DEV, seed=45 + i) for i in range(2)]
+    x = wl.make_x(shape, T, seed=23)
+    rows = sorted({0, 7, 127, 128, 130, 200, 255, int(np.argmax(ctx)), int(np.argmin(ctx))})
+    ex, em = both(orc.layers_step, shape, [orc.weights_f64(w) for w in layers], x, pools,
+                  batch.block_table, batch.seq_lens, batch.q_lens, rows=rows)
+    opts = _lib.make_opts(T, bounds, executor=_lib.NF_EXEC_SEQUENTIAL, kv_chunk=256)
+    plan, y = _run_layers(shape, batch, opts, layers, pools, x)
+    plan.close()
+    parity(f64(y)[rows], ex["y"], em["y"], f"8B-shaped decode layers on one stream, bounds {bounds}")
+
+
 def test_llama70b_shaped_layer_sampled_rows():
     """One LLaMA-2-70B-shaped layer (hidden 8192, 64 query heads over 8 KV heads,
     FFN 28672) on a mixed batch, sampled rows against both oracles at the
