@@ -859,10 +859,13 @@ bool op_traced(nf_plan p, int op) {
   return p->trace_left > 0 && p->trace_s0 && ((p->trace_ops >> op) & 1u);
 }
 
-// The step metadata handed to the first QKV nano-operation, which runs it
-// between its RMSNorm and its GEMM: the GEMM's operand loads and products then
-// proceed beside the one-CTA metadata kernel, and only its epilogue (RoPE
-// positions, cache slots) waits for the token map.
+// How a QKV nano-operation takes part in the step metadata.  AHEAD (two
+// streams): the one-CTA metadata kernel runs between RMSNorm-1 and the GEMM,
+// whose operand loads and products proceed beside it while its epilogue (RoPE
+// positions, cache slots) waits for the token map.  MAP_LIST / MAP (one
+// stream): RMSNorm-1 writes the token map of its rows, the GEMM follows it as
+// a programmatic dependent, and after the first one the work-list kernel runs
+// on the SMs the GEMM's last wave leaves free.
 struct MetaIn {
   const int32_t* bt;
   const int32_t* sl;
