@@ -204,7 +204,13 @@ void nf_plan_destroy(nf_plan plan);
  * seq_lens: device int32 [n_seq], KV length of each sequence AFTER this step:
  *   decode token i sits at position seq_lens[i] - 1; prefill chunk j continues
  *   its prompt at position seq_lens[s] - prefill_q_lens[j].
- * Returns after enqueueing on `stream`. */
+ * A slot this step writes must not be read by another sequence of the step
+ *   (a page that two sequences share may hold only positions before both
+ *   sequences' new tokens).
+ * Returns after enqueueing on `stream`.  The step's first kernel waits for all
+ * work enqueued on `stream` before it and work enqueued after it waits for the
+ * step's last kernel; inside the step, kernels may start as programmatic
+ * dependents of the one ahead and wait for it before they read its output. */
 nf_status nf_layer_step(nf_plan plan, const nf_layer_weights* w, const void* x, void* k_pool,
                         void* v_pool, const int32_t* block_table, const int32_t* seq_lens, void* y,
                         void* stream);
